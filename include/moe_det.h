@@ -1,0 +1,189 @@
+/*
+ * moe_det.h -- C ABI of libmoedet: a deterministic, batch-invariant
+ * Mixture-of-Experts layer forward with router replay, for GB300 (sm_103a).
+ *
+ * Sources the operations follow:
+ *   [TR] Composer 2 Technical Report, §6.2 "RL infrastructure", paragraph on
+ *        inference and weight sync (router replay: the inference engine
+ *        returns the chosen expert indices for every token at every MoE
+ *        layer; the trainer forward overrides the router's assignment with
+ *        them; the router still computes gate scores), and §6.1 "Training
+ *        infrastructure", Kernels paragraph and Fig. 10 (grouped expert
+ *        GEMMs, dispatch/combine with the combine in BF16, MXFP8 = E4M3
+ *        values with an E8M0 scale per 32-element block).
+ *   [TD] "1TB 权重 60 秒跨洋同步：Cursor 训练 Composer 2 的分布式 RL 工程",
+ *        section "浮点数不守规矩，MoE 火上浇油": a gate per layer picks 8 of
+ *        384 experts from the hidden state; batch-invariant kernels force
+ *        every accumulation into a fixed order; replay sends one integer per
+ *        chosen expert.
+ *   [CH] "「模型會作弊」：Cursor 訓練 Composer 2 的五大工程挑戰", section
+ *        "浮點數的陷阱：A+B+C ≠ C+B+A": the same facts.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers.  Every tensor argument is a DEVICE pointer unless stated
+ *     otherwise; all are row-major and rows are contiguous along the
+ *     reduction dimension K ("K-major").  bf16 means IEEE bfloat16 bit
+ *     patterns.  The caller allocates and owns every buffer, including the
+ *     workspace; the library allocates and frees nothing and keeps no state
+ *     between calls.
+ *   - Streams.  `stream` is a cudaStream_t (NULL = legacy default stream).
+ *     All work is enqueued on it in order; no call synchronises except
+ *     moe_get_status.  Calls on different streams need different workspaces.
+ *   - Host errors.  Null pointers, bad shapes, misalignment and a short
+ *     workspace are rejected before anything is launched, with the status
+ *     codes below; nothing is written in that case.
+ *   - Device errors.  Replayed ids outside [0, E) or repeated within a token
+ *     and bounded waits that run out are recorded in a status word inside
+ *     the workspace (read it with moe_get_status); kernels never trap.  A
+ *     token whose replayed ids are invalid gets an all-zero output row, zero
+ *     gate weights, and ids_out row {0, 1, ..., k-1}.
+ *   - Determinism.  For fixed inputs the outputs are bitwise identical run
+ *     to run, and the output row of a token depends only on that token's
+ *     hidden state, ids and the weights -- never on the other tokens of the
+ *     batch or on T.  Expert outputs of a token are added in ascending slot
+ *     order, then the shared expert, with fp32 accumulation ([TD], [CH]).
+ *   - Limits of this version.  k == 8; 8 <= E <= 512; d and F multiples of
+ *     64 (and of 128 for MXFP8 weights), 64 <= d, F <= 16384; n_shared in
+ *     {0, 1}; 1 <= T <= 2^20 (T == 0 is a no-op that returns MOE_OK).
+ *     Device pointers must be 16-byte aligned.
+ */
+#ifndef MOE_DET_H
+#define MOE_DET_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, declared here so that the header needs no CUDA
+ * include. */
+struct CUstream_st;
+typedef struct CUstream_st *moe_stream_t;
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_ARG = 1,          /* null pointer or invalid enum value          */
+    MOE_ERR_SHAPE = 2,        /* dimension outside the limits above          */
+    MOE_ERR_ALIGN = 3,        /* pointer not 16-byte aligned                 */
+    MOE_ERR_WORKSPACE = 4,    /* ws_bytes < moe_workspace_size(dims)         */
+    MOE_ERR_BAD_IDS = 5,      /* (device) replayed id out of range/repeated  */
+    MOE_ERR_TIMEOUT = 6,      /* (device) a bounded wait ran out             */
+    MOE_ERR_CUDA = 7,         /* a CUDA runtime/driver call failed           */
+    MOE_ERR_UNSUPPORTED = 8   /* valid request this build does not serve     */
+} moe_status;
+
+typedef enum {
+    MOE_W_BF16 = 0,   /* expert weights stored as bf16                        */
+    MOE_W_MXFP8 = 1   /* expert weights E4M3 + one E8M0 scale per 32 along K
+                         ([TR] §6.1: the MXFP8 format); router and shared
+                         expert stay bf16                                     */
+} moe_wfmt;
+
+/* Layer shape.  T tokens, hidden size d, E routed experts, k experts per
+ * token, expert FFN width F, n_shared always-on shared experts (weight 1). */
+typedef struct {
+    int64_t T;
+    int32_t d;
+    int32_t E;
+    int32_t k;
+    int32_t F;
+    int32_t n_shared;
+    int32_t wfmt;      /* moe_wfmt                                            */
+    int32_t out_fp32;  /* 1: `out` is fp32; 0: `out` is bf16 (round to nearest
+                          even of the same fp32 sum)                          */
+} moe_dims;
+
+/* Layer weights (all device pointers).
+ *   w_router  [E][d] bf16          router (gate) weights; logits = x . w_router^T
+ *   router_bias [E] fp32 or NULL   added to the logits before selection and
+ *                                  before the gate softmax
+ *   w_gate, w_up [E][F][d]         SwiGLU gate / up projections
+ *   w_down    [E][d][F]            down projection
+ *     bf16 for MOE_W_BF16; E4M3 bytes for MOE_W_MXFP8 with
+ *   s_gate, s_up [E][F][d/32], s_down [E][d][F/32]  E8M0 scale bytes
+ *     (NULL for MOE_W_BF16)
+ *   ws_gate, ws_up [F][d], ws_down [d][F]  bf16 shared expert (NULL when
+ *     n_shared == 0) */
+typedef struct {
+    const void *w_router;
+    const float *router_bias;
+    const void *w_gate;
+    const void *w_up;
+    const void *w_down;
+    const uint8_t *s_gate;
+    const uint8_t *s_up;
+    const uint8_t *s_down;
+    const void *ws_gate;
+    const void *ws_up;
+    const void *ws_down;
+} moe_weights;
+
+/* Byte offsets of the intermediate buffers inside the workspace, for
+ * inspection after a call (all int32 unless noted; pairs i = t*k + s):
+ *   status   int32[4]      device status word (moe_status bits), see below
+ *   logits   fp32 [T][E]   router logits (+ bias)
+ *   valid    int32[T]      1 = token's ids valid, 0 = replayed ids rejected
+ *   cnt      [E]           pairs routed to each expert (histogram)
+ *   off      [E+1]         exclusive prefix sum of cnt
+ *   perm     [T*k]         perm[dst] = i, expert-major and stable in i
+ *   inv      [T*k]         inv[i] = dst
+ *   xp       bf16 [T*k + T*n_shared][d]  gathered token rows (expert order),
+ *                                        then the shared-expert rows
+ *   h        bf16 [T*k + T*n_shared][F]  SwiGLU activations
+ *   y        bf16 [T*k][d]               routed expert outputs (dst order)
+ *   ysh      fp32 [T][d]                 shared expert output
+ * Offsets are 256-byte aligned; `total` equals moe_workspace_size(dims). */
+typedef struct {
+    size_t status, logits, valid, cnt, off, perm, inv, xp, h, y, ysh;
+    size_t total;
+} moe_ws_layout;
+
+/* Workspace bytes a call with these dims needs (0 if dims are invalid). */
+size_t moe_workspace_size(const moe_dims *dims);
+
+/* Fill *layout for dims.  MOE_ERR_ARG / MOE_ERR_SHAPE on bad input. */
+moe_status moe_workspace_layout(const moe_dims *dims, moe_ws_layout *layout);
+
+/* Routing only -- the side that records ids at inference ([TR] §6.2:
+ * "the engine returns the selected expert indices").  Computes the router
+ * logits of x [T][d] bf16, picks the k largest per token (descending logit,
+ * equal logits -> lower expert id; [TD]: 8 of 384), and their gate weights
+ * (softmax over all E renormalised over the chosen k).
+ * Out: ids_out [T][k] int32, gates_out [T][k] fp32. */
+moe_status moe_route(const moe_dims *dims, const void *x, const moe_weights *w,
+                     int32_t *ids_out, float *gates_out, void *ws,
+                     size_t ws_bytes, moe_stream_t stream);
+
+/* Full layer forward with the router's own selection:
+ *   out[t] = sum_{s<k} gates[t][s] * expert_{ids[t][s]}(x[t]) + shared(x[t]),
+ * expert(x) = W_down . (silu(W_gate . x) * (W_up . x)).  Out: out [T][d]
+ * (bf16 or fp32 per dims->out_fp32), ids_out, gates_out as in moe_route. */
+moe_status moe_forward(const moe_dims *dims, const void *x, const moe_weights *w,
+                       void *out, int32_t *ids_out, float *gates_out, void *ws,
+                       size_t ws_bytes, moe_stream_t stream);
+
+/* Full layer forward with router replay ([TR] §6.2; [TD]/[CH]: the trainer
+ * activates the recorded experts instead of its own gate's choice).
+ * ids_in [T][k] int32 (device) replaces the selection, slot order kept; the
+ * router still computes the gate weights over those ids.  Replaying the ids
+ * that moe_forward chose reproduces its output bitwise.  ids_out receives
+ * the ids actually used. */
+moe_status moe_forward_replay(const moe_dims *dims, const void *x,
+                              const moe_weights *w, const int32_t *ids_in,
+                              void *out, int32_t *ids_out, float *gates_out,
+                              void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Synchronise `stream` and return the device status of the last call that
+ * used this workspace: MOE_OK, MOE_ERR_BAD_IDS or MOE_ERR_TIMEOUT (the
+ * latter wins when both happened), or MOE_ERR_CUDA if reading it failed. */
+moe_status moe_get_status(const void *ws, moe_stream_t stream);
+
+/* Static, human-readable name of a status code. */
+const char *moe_status_str(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_DET_H */

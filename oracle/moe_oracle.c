@@ -1,0 +1,242 @@
+/*
+ * moe_oracle.c -- plain fp64 CPU oracle of the MoE layer forward with router
+ * replay.  TEST INFRASTRUCTURE ONLY: the CUDA product path never includes,
+ * links, loads or calls this file.  See moe_oracle.h for the definition it
+ * computes and the passages it follows.
+ *
+ * Style rule of this file: every function is the plain definition written
+ * out, loops in the order the definition reads, fp64 throughout.  OpenMP
+ * parallelism is only ever across independent outputs (tokens, rows); the
+ * summation order of every individual output is the one written here.
+ */
+#include "moe_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ---- exact decoders ------------------------------------------------------ */
+
+double oracle_bf16_to_f64(uint16_t h) {
+    /* bf16 is the top half of an IEEE binary32 pattern. */
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+double oracle_e4m3_to_f64(uint8_t b) {
+    /* OCP 8-bit E4M3 ("fn"): 1 sign, 4 exponent (bias 7), 3 mantissa bits,
+     * no infinities, S.1111.111 is NaN. [TR] §6.1 Kernels: MXFP8 values. */
+    int sign = (b >> 7) & 1;
+    int ex = (b >> 3) & 0xF;
+    int man = b & 7;
+    double v;
+    if (ex == 15 && man == 7) return NAN;
+    if (ex == 0)
+        v = ldexp((double)man, -9);          /* subnormal: man/8 * 2^(1-7) */
+    else
+        v = ldexp(8.0 + man, ex - 7 - 3);    /* (1 + man/8) * 2^(ex-7) */
+    return sign ? -v : v;
+}
+
+double oracle_e8m0_to_f64(uint8_t s) {
+    /* E8M0 block scale: 2^(s-127); 0xFF is NaN. [TR] §6.1: MXFP8 scale. */
+    if (s == 0xFF) return NAN;
+    return ldexp(1.0, (int)s - 127);
+}
+
+double oracle_matrix_elem(const oracle_matrix *m, int64_t K, int64_t r, int64_t c) {
+    if (m->fmt == ORACLE_W_BF16)
+        return oracle_bf16_to_f64(((const uint16_t *)m->values)[r * K + c]);
+    /* MXFP8: one E8M0 scale per 32 consecutive elements along K. */
+    double q = oracle_e4m3_to_f64(((const uint8_t *)m->values)[r * K + c]);
+    double sc = oracle_e8m0_to_f64(m->scales[r * (K / 32) + c / 32]);
+    return q * sc;
+}
+
+/* ---- routing --------------------------------------------------------------- */
+
+void oracle_router_logits(const uint16_t *x, const uint16_t *wr, const float *bias,
+                          int64_t T, int64_t d, int64_t E, double *logits) {
+    /* [TD] "每层有一个门控": the gate is a linear map of the hidden state. */
+    int64_t t;
+#pragma omp parallel for schedule(static)
+    for (t = 0; t < T; ++t) {
+        for (int64_t e = 0; e < E; ++e) {
+            double acc = 0.0;
+            for (int64_t j = 0; j < d; ++j)
+                acc += oracle_bf16_to_f64(x[t * d + j]) * oracle_bf16_to_f64(wr[e * d + j]);
+            if (bias) acc += (double)bias[e];
+            logits[t * E + e] = acc;
+        }
+    }
+}
+
+/* a ranks before b: larger logit first, equal logits -> lower expert id. */
+static int ranks_before(double la, int64_t a, double lb, int64_t b) {
+    if (la > lb) return 1;
+    if (la < lb) return 0;
+    return a < b;
+}
+
+void oracle_select_topk(const double *logits, int64_t T, int64_t E, int64_t k,
+                        int32_t *ids) {
+    /* [TD]: the gate picks 8 of 384 experts per token.  Selection: k rounds,
+     * each taking the best expert not yet chosen. */
+    int64_t t;
+#pragma omp parallel for schedule(static)
+    for (t = 0; t < T; ++t) {
+        const double *l = logits + t * E;
+        unsigned char *taken = (unsigned char *)calloc((size_t)E, 1);
+        for (int64_t s = 0; s < k; ++s) {
+            int64_t best = -1;
+            for (int64_t e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0 || ranks_before(l[e], e, l[best], best)) best = e;
+            }
+            taken[best] = 1;
+            ids[t * k + s] = (int32_t)best;
+        }
+        free(taken);
+    }
+}
+
+int64_t oracle_check_ids(const int32_t *ids, int64_t T, int64_t E, int64_t k,
+                         uint8_t *valid) {
+    int64_t bad = 0;
+    for (int64_t t = 0; t < T; ++t) {
+        int ok = 1;
+        for (int64_t s = 0; s < k; ++s) {
+            int32_t e = ids[t * k + s];
+            if (e < 0 || e >= E) ok = 0;
+            for (int64_t s2 = 0; s2 < s; ++s2)
+                if (ids[t * k + s2] == e) ok = 0;
+        }
+        valid[t] = (uint8_t)ok;
+        bad += !ok;
+    }
+    return bad;
+}
+
+void oracle_gate_weights(const double *logits, const int32_t *ids, int64_t T,
+                         int64_t E, int64_t k, double *gates) {
+    /* [TR] §6.2: under replay the router still computes the gate scores, over
+     * the replayed experts.  Softmax over all E followed by renormalisation
+     * over the chosen set equals the softmax of the chosen logits, since the
+     * common denominator cancels. */
+    for (int64_t t = 0; t < T; ++t) {
+        const double *l = logits + t * E;
+        double m = -INFINITY;
+        for (int64_t s = 0; s < k; ++s) {
+            double v = l[ids[t * k + s]];
+            if (v > m) m = v;
+        }
+        double den = 0.0;
+        for (int64_t s = 0; s < k; ++s) den += exp(l[ids[t * k + s]] - m);
+        for (int64_t s = 0; s < k; ++s)
+            gates[t * k + s] = exp(l[ids[t * k + s]] - m) / den;
+    }
+}
+
+/* ---- dispatch: stable counting sort -------------------------------------- */
+
+void oracle_counting_sort(const int32_t *ids, int64_t n_pairs, int64_t E,
+                          int32_t *cnt, int32_t *off, int32_t *perm, int32_t *inv) {
+    /* [TR] §6.1: tokens are dispatched to their experts and combined back.
+     * On one device, dispatch is a grouping of the (token, slot) pairs by
+     * expert that keeps the pair order inside each group. */
+    int32_t *next = (int32_t *)malloc((size_t)(E > 0 ? E : 1) * sizeof(int32_t));
+    for (int64_t e = 0; e < E; ++e) cnt[e] = 0;
+    for (int64_t i = 0; i < n_pairs; ++i) cnt[ids[i]] += 1;
+    off[0] = 0;
+    for (int64_t e = 0; e < E; ++e) off[e + 1] = off[e] + cnt[e];
+    for (int64_t e = 0; e < E; ++e) next[e] = off[e];
+    for (int64_t i = 0; i < n_pairs; ++i) {
+        int32_t dst = next[ids[i]]++;
+        perm[dst] = (int32_t)i;
+        inv[i] = dst;
+    }
+    free(next);
+}
+
+/* ---- expert FFN ------------------------------------------------------------ */
+
+static double silu(double a) { return a / (1.0 + exp(-a)); }
+
+void oracle_expert_ffn(const uint16_t *x, int64_t n, int64_t d, int64_t F,
+                       const oracle_matrix *wg, const oracle_matrix *wu,
+                       const oracle_matrix *wd, double *y) {
+    /* SwiGLU expert: h_f = silu(x . Wg[f]) * (x . Wu[f]);  y = sum_f h_f Wd[:, f].
+     * [TR] §6.1 and Fig. 10: the grouped expert GEMMs. */
+    double *xd = (double *)malloc((size_t)(n * d) * sizeof(double));
+    double *h = (double *)malloc((size_t)(n * F) * sizeof(double));
+    for (int64_t i = 0; i < n * d; ++i) xd[i] = oracle_bf16_to_f64(x[i]);
+
+    int64_t f;
+#pragma omp parallel for schedule(static)
+    for (f = 0; f < F; ++f) {
+        for (int64_t r = 0; r < n; ++r) {
+            double a = 0.0, b = 0.0;
+            for (int64_t j = 0; j < d; ++j) {
+                a += xd[r * d + j] * oracle_matrix_elem(wg, d, f, j);
+                b += xd[r * d + j] * oracle_matrix_elem(wu, d, f, j);
+            }
+            h[r * F + f] = silu(a) * b;
+        }
+    }
+    int64_t i;
+#pragma omp parallel for schedule(static)
+    for (i = 0; i < d; ++i) {
+        for (int64_t r = 0; r < n; ++r) {
+            double acc = 0.0;
+            for (int64_t ff = 0; ff < F; ++ff)
+                acc += h[r * F + ff] * oracle_matrix_elem(wd, F, i, ff);
+            y[r * d + i] = acc;
+        }
+    }
+    free(h);
+    free(xd);
+}
+
+/* ---- combine ----------------------------------------------------------------- */
+
+void oracle_combine(const double *y_slots, const double *gates,
+                    const double *y_shared, const uint8_t *valid, int64_t T,
+                    int64_t k, int64_t d, double *out) {
+    /* [TR] §6.1: combine; [TD]/[CH]: expert outputs are added in one fixed
+     * order -- slot 0 first, then 1, ..., then the always-on shared expert. */
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t i = 0; i < d; ++i) {
+            double acc = 0.0;
+            if (!valid || valid[t]) {
+                for (int64_t s = 0; s < k; ++s)
+                    acc += gates[t * k + s] * y_slots[(t * k + s) * d + i];
+                if (y_shared) acc += y_shared[t * d + i];
+            }
+            out[t * d + i] = acc;
+        }
+    }
+}
+
+int oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
+int oracle_get_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
