@@ -1,0 +1,340 @@
+// api.cu -- the C ABI of libmoedet (declared in include/moe_det.h): argument
+// validation, workspace carving, TMA descriptor set-up and the launch sequence
+//   router GEMM -> top-k/replay + gates -> counting sort -> gather
+//   -> grouped gate/up GEMM + SwiGLU -> grouped down GEMM -> fixed-order combine
+// of the MoE layer forward with router replay (Composer 2 Technical Report,
+// §6.2 "RL infrastructure" for replay, §6.1 "Training infrastructure" for the
+// grouped expert GEMMs and dispatch/combine).  Everything is enqueued on the
+// caller's stream; nothing is allocated and nothing synchronises except
+// moe_get_status.
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "moe_det.h"
+#include "moe_internal.h"
+
+using namespace moe;
+
+namespace {
+
+constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // bounded device waits: 1 s
+
+inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct Layout {
+    size_t status, logits, valid, cnt, off, perm, inv, scratch, xp, h, y, ysh, total;
+};
+
+bool dims_ok(const moe_dims* d) {
+    if (!d) return false;
+    if (d->T < 0 || d->T > (int64_t(1) << 20)) return false;
+    if (d->k != 8) return false;
+    if (d->E < 8 || d->E > 512) return false;
+    if (d->d < 64 || d->d > 16384 || d->d % 64) return false;
+    if (d->F < 64 || d->F > 16384 || d->F % 64) return false;
+    if (d->n_shared < 0 || d->n_shared > 1) return false;
+    if (d->wfmt != MOE_W_BF16 && d->wfmt != MOE_W_MXFP8) return false;
+    if (d->wfmt == MOE_W_MXFP8 && (d->d % 128 || d->F % 128)) return false;
+    if (d->out_fp32 != 0 && d->out_fp32 != 1) return false;
+    return true;
+}
+
+Layout make_layout(const moe_dims* d) {
+    Layout L{};
+    const size_t T = static_cast<size_t>(d->T), k = d->k, E = d->E, S = d->n_shared;
+    const size_t rows = T * k + T * S;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { const size_t at = o; o = align256(o + bytes); return at; };
+    L.status = take(16);
+    L.logits = take(T * E * 4);
+    L.valid = take(T * 4);
+    L.cnt = take(E * 4);
+    L.off = take((E + 1) * 4);
+    L.perm = take(T * k * 4);
+    L.inv = take(T * k * 4);
+    L.scratch = take(dispatch_scratch_bytes(static_cast<int64_t>(T * k), static_cast<int>(E)));
+    L.xp = take(rows * d->d * 2);
+    L.h = take(rows * d->F * 2);
+    L.y = take(T * k * d->d * 2);
+    L.ysh = take(S ? T * d->d * 4 : 0);
+    L.total = o;
+    return L;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 map over [rows][K] (K contiguous), box 64 x box_rows, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {K, rows};
+    const cuuint64_t strides[1] = {K * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+moe_status check_common(const moe_dims* d, const void* x, const moe_weights* w, void* ws,
+                        size_t ws_bytes) {
+    if (!d || !w) return MOE_ERR_ARG;
+    if (!dims_ok(d)) return MOE_ERR_SHAPE;
+    if (d->T == 0) return MOE_OK;
+    if (!x || !ws || !w->w_router) return MOE_ERR_ARG;
+    if (!al16(x) || !al16(ws) || !al16(w->w_router) || !al16(w->router_bias)) return MOE_ERR_ALIGN;
+    if (ws_bytes < make_layout(d).total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+moe_status check_experts(const moe_dims* d, const moe_weights* w) {
+    if (!w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_ARG;
+    if (!al16(w->w_gate) || !al16(w->w_up) || !al16(w->w_down)) return MOE_ERR_ALIGN;
+    if (d->wfmt == MOE_W_MXFP8) {
+        if (!w->s_gate || !w->s_up || !w->s_down) return MOE_ERR_ARG;
+        if (!al16(w->s_gate) || !al16(w->s_up) || !al16(w->s_down)) return MOE_ERR_ALIGN;
+    }
+    if (d->n_shared) {
+        if (!w->ws_gate || !w->ws_up || !w->ws_down) return MOE_ERR_ARG;
+        if (!al16(w->ws_gate) || !al16(w->ws_up) || !al16(w->ws_down)) return MOE_ERR_ALIGN;
+    }
+    return MOE_OK;
+}
+
+inline moe_status cu(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+#define MOE_TRY(expr)                         \
+    do {                                      \
+        const moe_status st_ = (expr);        \
+        if (st_ != MOE_OK) return st_;        \
+    } while (0)
+
+}  // namespace
+
+namespace {
+
+// Router logits (fp32, + bias) and the routing decision for every token.
+moe_status run_route(const moe_dims* d, const void* x, const moe_weights* w, const int32_t* ids_in,
+                     int32_t* ids_out, float* gates_out, uint8_t* ws, const Layout& L,
+                     cudaStream_t s) {
+    const int64_t T = d->T;
+    int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+    MOE_TRY(cu(cudaMemsetAsync(status, 0, 16, s)));
+    GemmParams p;
+    std::memset(&p, 0, sizeof p);
+    if (!make_map(&p.a0, w->w_router, d->d, d->E, BM)) return MOE_ERR_CUDA;
+    if (!make_map(&p.b, x, d->d, T, BN)) return MOE_ERR_CUDA;
+    p.G = 1;
+    p.n_single = static_cast<int32_t>(T);
+    p.M = d->E;
+    p.MT = (d->E + BM - 1) / BM;
+    p.KB = d->d / BK;
+    p.out = ws + L.logits;
+    p.ldo = d->E;
+    p.bias = w->router_bias;
+    p.status = status;
+    p.timeout_ns = kWaitTimeoutNs;
+    const int64_t tiles = int64_t(p.MT) * ((T + BN - 1) / BN);
+    const int sms = num_sms();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+    MOE_TRY(cu(launch_grouped_gemm(GEMM_ROUTER, p, grid, s)));
+    return cu(launch_topk_gates(reinterpret_cast<const float*>(ws + L.logits), T, d->E, d->k, ids_in,
+                                ids_out, gates_out, reinterpret_cast<int32_t*>(ws + L.valid), status,
+                                s));
+}
+
+// Dispatch, expert FFNs and combine, given ids/gates of every token.
+moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, void* out,
+                       const int32_t* ids, const float* gates, uint8_t* ws, const Layout& L,
+                       cudaStream_t s) {
+    const int64_t T = d->T;
+    const int k = d->k, E = d->E, S = d->n_shared;
+    const int64_t rows = T * k + T * S;
+    int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+    int32_t* cnt = reinterpret_cast<int32_t*>(ws + L.cnt);
+    int32_t* off = reinterpret_cast<int32_t*>(ws + L.off);
+    int32_t* perm = reinterpret_cast<int32_t*>(ws + L.perm);
+    int32_t* inv = reinterpret_cast<int32_t*>(ws + L.inv);
+    MOE_TRY(cu(launch_dispatch(ids, T, k, E, cnt, off, perm, inv,
+                               reinterpret_cast<int32_t*>(ws + L.scratch), s)));
+    MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), perm, T, k, d->d, S,
+                             reinterpret_cast<uint16_t*>(ws + L.xp), s)));
+    const int sms = num_sms();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    const int64_t ntile_bound = (T * k + BN - 1) / BN + E + (S ? (T + BN - 1) / BN : 0);
+
+    // gate/up projections with the SwiGLU epilogue -> H
+    GemmParams p1;
+    std::memset(&p1, 0, sizeof p1);
+    if (!make_map(&p1.a0, w->w_gate, d->d, uint64_t(E) * d->F, BM)) return MOE_ERR_CUDA;
+    if (!make_map(&p1.a1, w->w_up, d->d, uint64_t(E) * d->F, BM)) return MOE_ERR_CUDA;
+    if (S) {
+        if (!make_map(&p1.as0, w->ws_gate, d->d, d->F, BM)) return MOE_ERR_CUDA;
+        if (!make_map(&p1.as1, w->ws_up, d->d, d->F, BM)) return MOE_ERR_CUDA;
+    }
+    if (!make_map(&p1.b, ws + L.xp, d->d, rows, BN)) return MOE_ERR_CUDA;
+    p1.cnt = cnt;
+    p1.off = off;
+    p1.G = E;
+    p1.has_shared = S;
+    p1.shared_rows = static_cast<int32_t>(T);
+    p1.shared_b_off = static_cast<int32_t>(T * k);
+    p1.M = d->F;
+    p1.MT = (d->F + BM - 1) / BM;
+    p1.KB = d->d / BK;
+    p1.out = ws + L.h;
+    p1.ldo = d->F;
+    p1.status = status;
+    p1.timeout_ns = kWaitTimeoutNs;
+    int64_t tb = ntile_bound * p1.MT;
+    MOE_TRY(cu(launch_grouped_gemm(GEMM_SWIGLU, p1, static_cast<int>(tb < sms ? tb : sms), s)));
+
+    // down projection -> Y (routed, bf16) and Ysh (shared, fp32)
+    GemmParams p2;
+    std::memset(&p2, 0, sizeof p2);
+    if (!make_map(&p2.a0, w->w_down, d->F, uint64_t(E) * d->d, BM)) return MOE_ERR_CUDA;
+    if (S && !make_map(&p2.as0, w->ws_down, d->F, d->d, BM)) return MOE_ERR_CUDA;
+    if (!make_map(&p2.b, ws + L.h, d->F, rows, BN)) return MOE_ERR_CUDA;
+    p2.cnt = cnt;
+    p2.off = off;
+    p2.G = E;
+    p2.has_shared = S;
+    p2.shared_rows = static_cast<int32_t>(T);
+    p2.shared_b_off = static_cast<int32_t>(T * k);
+    p2.M = d->d;
+    p2.MT = (d->d + BM - 1) / BM;
+    p2.KB = d->F / BK;
+    p2.out = ws + L.y;
+    p2.out_shared = S ? ws + L.ysh : nullptr;
+    p2.ldo = d->d;
+    p2.status = status;
+    p2.timeout_ns = kWaitTimeoutNs;
+    tb = ntile_bound * p2.MT;
+    MOE_TRY(cu(launch_grouped_gemm(GEMM_DOWN, p2, static_cast<int>(tb < sms ? tb : sms), s)));
+
+    return cu(launch_combine(reinterpret_cast<const uint16_t*>(ws + L.y),
+                             S ? reinterpret_cast<const float*>(ws + L.ysh) : nullptr, inv, gates,
+                             reinterpret_cast<const int32_t*>(ws + L.valid), T, k, d->d,
+                             d->out_fp32, out, s));
+}
+
+moe_status forward_impl(const moe_dims* d, const void* x, const moe_weights* w,
+                        const int32_t* ids_in, bool replay, void* out, int32_t* ids_out,
+                        float* gates_out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_TRY(check_common(d, x, w, ws, ws_bytes));
+    if (d->T == 0) return MOE_OK;
+    MOE_TRY(check_experts(d, w));
+    if (!out || !ids_out || !gates_out || (replay && !ids_in)) return MOE_ERR_ARG;
+    if (!al16(out) || !al16(ids_out) || !al16(gates_out) || (replay && !al16(ids_in)))
+        return MOE_ERR_ALIGN;
+    if (d->wfmt != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
+    const Layout L = make_layout(d);
+    auto* s = reinterpret_cast<cudaStream_t>(stream);
+    auto* wsb = static_cast<uint8_t*>(ws);
+    MOE_TRY(run_route(d, x, w, replay ? ids_in : nullptr, ids_out, gates_out, wsb, L, s));
+    return run_experts(d, x, w, out, ids_out, gates_out, wsb, L, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_size(const moe_dims* dims) {
+    if (!dims_ok(dims)) return 0;
+    return make_layout(dims).total;
+}
+
+moe_status moe_workspace_layout(const moe_dims* dims, moe_ws_layout* out) {
+    if (!dims || !out) return MOE_ERR_ARG;
+    if (!dims_ok(dims)) return MOE_ERR_SHAPE;
+    const Layout L = make_layout(dims);
+    out->status = L.status;
+    out->logits = L.logits;
+    out->valid = L.valid;
+    out->cnt = L.cnt;
+    out->off = L.off;
+    out->perm = L.perm;
+    out->inv = L.inv;
+    out->xp = L.xp;
+    out->h = L.h;
+    out->y = L.y;
+    out->ysh = L.ysh;
+    out->total = L.total;
+    return MOE_OK;
+}
+
+moe_status moe_route(const moe_dims* dims, const void* x, const moe_weights* w, int32_t* ids_out,
+                     float* gates_out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_TRY(check_common(dims, x, w, ws, ws_bytes));
+    if (dims->T == 0) return MOE_OK;
+    if (!ids_out || !gates_out) return MOE_ERR_ARG;
+    if (!al16(ids_out) || !al16(gates_out)) return MOE_ERR_ALIGN;
+    const Layout L = make_layout(dims);
+    return run_route(dims, x, w, nullptr, ids_out, gates_out, static_cast<uint8_t*>(ws), L,
+                     reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward(const moe_dims* dims, const void* x, const moe_weights* w, void* out,
+                       int32_t* ids_out, float* gates_out, void* ws, size_t ws_bytes,
+                       moe_stream_t stream) {
+    return forward_impl(dims, x, w, nullptr, false, out, ids_out, gates_out, ws, ws_bytes, stream);
+}
+
+moe_status moe_forward_replay(const moe_dims* dims, const void* x, const moe_weights* w,
+                              const int32_t* ids_in, void* out, int32_t* ids_out, float* gates_out,
+                              void* ws, size_t ws_bytes, moe_stream_t stream) {
+    return forward_impl(dims, x, w, ids_in, true, out, ids_out, gates_out, ws, ws_bytes, stream);
+}
+
+moe_status moe_get_status(const void* ws, moe_stream_t stream) {
+    if (!ws) return MOE_ERR_ARG;
+    auto* s = reinterpret_cast<cudaStream_t>(stream);
+    int32_t h[4] = {0, 0, 0, 0};
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemcpy(h, ws, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (h[0] & STATUS_TIMEOUT) return MOE_ERR_TIMEOUT;
+    if (h[0] & STATUS_BAD_IDS) return MOE_ERR_BAD_IDS;
+    return MOE_OK;
+}
+
+const char* moe_status_str(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_ARG: return "MOE_ERR_ARG: null pointer or invalid enum value";
+        case MOE_ERR_SHAPE: return "MOE_ERR_SHAPE: dimension outside the supported limits";
+        case MOE_ERR_ALIGN: return "MOE_ERR_ALIGN: pointer not 16-byte aligned";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE: workspace smaller than moe_workspace_size";
+        case MOE_ERR_BAD_IDS: return "MOE_ERR_BAD_IDS: replayed expert id out of range or repeated";
+        case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT: a bounded device wait ran out";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA: a CUDA call failed";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: not supported by this build";
+    }
+    return "unknown moe_status";
+}
+
+}  // extern "C"

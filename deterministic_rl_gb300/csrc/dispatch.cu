@@ -1,0 +1,165 @@
+// dispatch.cu -- deterministic stable counting sort of the (token, slot) pairs
+// by expert id, and the gather of token rows into expert order.
+//
+// On one GPU the token dispatch of the Composer 2 Technical Report, §6.1
+// "Training infrastructure" (tokens dispatched to their experts, combined back
+// afterwards) is a grouping of the pairs i = t*k + s by expert.  Positions are
+// a pure function of the ids: dst(i) = off[e] + #{i' < i : id(i') = e}, built
+// from per-segment histograms, a segment-order scan and in-order ranks from
+// warp match masks -- no position ever depends on the order of atomics.
+#include <cstdint>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kSegPairs = 4096;  // pairs per segment (one CTA)
+constexpr int kSegWarps = 8;     // each warp ranks 512 consecutive pairs
+constexpr int kWarpPairs = kSegPairs / kSegWarps;
+constexpr int kMaxE = 512;
+
+// Pass 1: per-segment, per-warp histograms.  hist[seg][w][e].
+__global__ void __launch_bounds__(32 * kSegWarps) seg_hist_kernel(const int32_t* __restrict__ ids,
+                                                                  int64_t n, int E,
+                                                                  int32_t* __restrict__ hist) {
+    __shared__ int32_t h[kSegWarps][kMaxE];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < kSegWarps * kMaxE; i += blockDim.x) (&h[0][0])[i] = 0;
+    __syncthreads();
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kSegPairs + w * kWarpPairs;
+    for (int r = 0; r < kWarpPairs; r += 32) {
+        const int64_t i = base + r + lane;
+        const bool in = i < n;
+        const int key = in ? ids[i] : -1;
+        const uint32_t act = __ballot_sync(0xffffffffu, in);
+        if (in) {
+            const uint32_t peers = __match_any_sync(act, key);
+            if ((__ffs(peers) - 1) == lane) h[w][key] += __popc(peers);
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+    int32_t* out = hist + static_cast<int64_t>(blockIdx.x) * kSegWarps * E;
+    for (int i = threadIdx.x; i < kSegWarps * E; i += blockDim.x) out[i] = h[i / E][i % E];
+}
+
+// Pass 2 (one CTA): cnt[e], off[e] (exclusive over e), and each (segment, warp)
+// base position base[seg][w][e] = off[e] + pairs of e in earlier (seg, w).
+__global__ void __launch_bounds__(kMaxE) seg_scan_kernel(int32_t* __restrict__ hist, int nseg, int E,
+                                                         int32_t* __restrict__ cnt,
+                                                         int32_t* __restrict__ off) {
+    __shared__ int32_t tot[kMaxE];
+    __shared__ int32_t warp_sums[kMaxE / 32];
+    const int e = threadIdx.x;
+    int32_t run = 0;
+    if (e < E) {
+        for (int sw = 0; sw < nseg * kSegWarps; ++sw) {
+            int32_t* p = hist + static_cast<int64_t>(sw) * E + e;
+            const int32_t c = *p;
+            *p = run;
+            run += c;
+        }
+    }
+    tot[e] = e < E ? run : 0;
+    __syncthreads();
+    // exclusive scan of tot over e (E <= 512): warp scans, then warp totals
+    const int lane = e & 31, w = e >> 5;
+    int32_t incl = tot[e];
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, s);
+        if (lane >= s) incl += v;
+    }
+    if (lane == 31) warp_sums[w] = incl;
+    __syncthreads();
+    int32_t wbase = 0;
+    for (int i = 0; i < w; ++i) wbase += warp_sums[i];
+    const int32_t excl = wbase + incl - tot[e];
+    if (e < E) {
+        cnt[e] = tot[e];
+        off[e] = excl;
+        if (e == E - 1) off[E] = excl + tot[e];
+        for (int sw = 0; sw < nseg * kSegWarps; ++sw) hist[static_cast<int64_t>(sw) * E + e] += excl;
+    }
+}
+
+// Pass 3: in-order ranks inside each warp's 512 pairs; perm[dst] = i, inv[i] = dst.
+__global__ void __launch_bounds__(32 * kSegWarps) seg_scatter_kernel(
+    const int32_t* __restrict__ ids, int64_t n, int E, const int32_t* __restrict__ base_pos,
+    int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+    __shared__ int32_t pos[kSegWarps][kMaxE];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int32_t* b = base_pos + static_cast<int64_t>(blockIdx.x) * kSegWarps * E;
+    for (int i = threadIdx.x; i < kSegWarps * E; i += blockDim.x) pos[i / E][i % E] = b[i];
+    __syncthreads();
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * kSegPairs + w * kWarpPairs;
+    for (int r = 0; r < kWarpPairs; r += 32) {
+        const int64_t i = base + r + lane;
+        const bool in = i < n;
+        const int key = in ? ids[i] : -1;
+        const uint32_t act = __ballot_sync(0xffffffffu, in);
+        if (in) {
+            const uint32_t peers = __match_any_sync(act, key);
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            const int32_t dst = pos[w][key] + rank;
+            perm[dst] = static_cast<int32_t>(i);
+            inv[i] = dst;
+            __syncwarp(act);
+            if ((__ffs(peers) - 1) == lane) pos[w][key] += __popc(peers);
+        }
+        __syncwarp();
+    }
+}
+
+// Gather: xp[r] = x[perm[r] / k] for r < T*k, then xp[T*k + t] = x[t] for
+// the shared expert.  16-byte vectors; d % 8 == 0.
+__global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
+                                   int64_t n_pairs, int k, int vec_per_row, int64_t rows_total,
+                                   uint4* __restrict__ xp) {
+    for (int64_t r = blockIdx.x; r < rows_total; r += gridDim.x) {
+        const int64_t src = r < n_pairs ? perm[r] / k : r - n_pairs;
+        const uint4* s = x + src * vec_per_row;
+        uint4* dptr = xp + r * vec_per_row;
+        for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dptr[v] = s[v];
+    }
+}
+
+}  // namespace
+
+size_t dispatch_scratch_bytes(int64_t n_pairs, int E) {
+    const int64_t nseg = (n_pairs + kSegPairs - 1) / kSegPairs;
+    return static_cast<size_t>((nseg > 0 ? nseg : 1) * kSegWarps * E) * sizeof(int32_t);
+}
+
+cudaError_t launch_dispatch(const int32_t* ids, int64_t T, int k, int E, int32_t* cnt,
+                            int32_t* off, int32_t* perm, int32_t* inv, int32_t* scratch,
+                            cudaStream_t s) {
+    if (E > kMaxE) return cudaErrorInvalidValue;
+    const int64_t n = T * k;
+    const int nseg = static_cast<int>((n + kSegPairs - 1) / kSegPairs);
+    if (nseg > 0) {
+        seg_hist_kernel<<<nseg, 32 * kSegWarps, 0, s>>>(ids, n, E, scratch);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    seg_scan_kernel<<<1, kMaxE, 0, s>>>(scratch, nseg, E, cnt, off);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess || nseg == 0) return e;
+    seg_scatter_kernel<<<nseg, 32 * kSegWarps, 0, s>>>(ids, n, E, scratch, perm, inv);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int64_t T, int k, int d,
+                          int n_shared, uint16_t* xp, cudaStream_t s) {
+    const int64_t n_pairs = T * k;
+    const int64_t rows = n_pairs + (n_shared ? T : 0);
+    if (rows == 0) return cudaSuccess;
+    const int vpr = d / 8;
+    const int64_t grid = rows < 148 * 16 ? rows : 148 * 16;
+    gather_rows_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(
+        reinterpret_cast<const uint4*>(x), perm, n_pairs, k, vpr, rows, reinterpret_cast<uint4*>(xp));
+    return cudaGetLastError();
+}
+
+}  // namespace moe

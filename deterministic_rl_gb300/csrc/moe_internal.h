@@ -1,0 +1,73 @@
+// moe_internal.h -- parameters and launchers shared between the C-ABI layer
+// (api.cu) and the kernels.  Not part of the public interface.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace moe {
+
+// Tile shape of every tcgen05 GEMM: 128 weight rows (M) x 128 token rows (N)
+// x 64 along K per pipeline stage.  One schedule for every group size, so the
+// reduction order of each output element depends on K alone.
+constexpr int BM = 128;
+constexpr int BN = 128;
+constexpr int BK = 64;
+
+// Device status word bits (ws status[0]); status[1] = id of the kernel whose
+// wait ran out, status[2] = number of tokens with rejected replay ids.
+constexpr int STATUS_BAD_IDS = 1;
+constexpr int STATUS_TIMEOUT = 2;
+
+enum GemmMode : int { GEMM_ROUTER = 0, GEMM_SWIGLU = 1, GEMM_DOWN = 2 };
+
+// Grouped GEMM  D[g] = A[g] . B[g]^T  over groups g of token rows.
+// A: weight rows (K-major), B: token rows (K-major), both bf16 via TMA.
+// Routed group g < G has cnt[g] token rows starting at B row off[g] and uses
+// weight rows [g*M, g*M + M) of a0 (and a1); the optional shared group has
+// shared_rows token rows from B row shared_b_off and uses as0 (and as1).
+// For the router (cnt == nullptr) there is one group of n_single rows at 0.
+struct GemmParams {
+    CUtensorMap a0, a1, as0, as1, b;
+    const int32_t* cnt;
+    const int32_t* off;
+    int32_t G;
+    int32_t has_shared;
+    int32_t n_single;
+    int32_t shared_rows;
+    int32_t shared_b_off;
+    int32_t M;      // weight rows per group
+    int32_t MT;     // ceil(M / BM)
+    int32_t KB;     // K / BK
+    void* out;        // router: fp32 logits [T][ldo]; swiglu: bf16 H [rows][ldo]; down: bf16 Y
+    void* out_shared; // down: fp32 Ysh [T][ldo]
+    int32_t ldo;
+    const float* bias;  // router only
+    const uint8_t* sa0; // MXFP8 scales (unused by the bf16 kernels)
+    int32_t* status;
+    uint64_t timeout_ns;
+};
+
+size_t gemm_smem_bytes(int mode, int n_groups_total);
+cudaError_t launch_grouped_gemm(int mode, const GemmParams& p, int grid, cudaStream_t s);
+
+// Routing: top-k selection (own mode) or replay validation, then gate weights.
+cudaError_t launch_topk_gates(const float* logits, int64_t T, int E, int k,
+                              const int32_t* ids_in, int32_t* ids_out, float* gates_out,
+                              int32_t* valid, int32_t* status, cudaStream_t s);
+
+// Dispatch: stable counting sort of the T*k pairs by expert, then the gather
+// of token rows into expert order (plus the shared-expert copy of x).
+size_t dispatch_scratch_bytes(int64_t n_pairs, int E);
+cudaError_t launch_dispatch(const int32_t* ids, int64_t T, int k, int E, int32_t* cnt,
+                            int32_t* off, int32_t* perm, int32_t* inv, int32_t* scratch,
+                            cudaStream_t s);
+cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int64_t T, int k, int d,
+                          int n_shared, uint16_t* xp, cudaStream_t s);
+
+// Fixed-order combine of each token's k expert rows and the shared row.
+cudaError_t launch_combine(const uint16_t* y, const float* ysh, const int32_t* inv,
+                           const float* gates, const int32_t* valid, int64_t T, int k, int d,
+                           int out_fp32, void* out, cudaStream_t s);
+
+}  // namespace moe

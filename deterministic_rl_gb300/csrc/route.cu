@@ -1,0 +1,145 @@
+// route.cu -- top-k selection by warp-shuffle arg-max, replay-id validation,
+// and gate weights, one warp per token.
+//
+// Selection follows the gate of the Training Data No. 94 write-up (section
+// "浮点数不守规矩，MoE 火上浇油": a gate picks 8 of 384 experts from the
+// hidden state): the k largest logits in descending order, equal logits going
+// to the lower expert id.  Replay follows the Composer 2 Technical Report,
+// §6.2 "RL infrastructure": recorded ids replace the selection and the router
+// still computes the gate scores over them.  Gate weights are the softmax of
+// the k chosen logits (softmax over all E renormalised over the chosen set).
+// Own mode and replay share one gate routine, so replaying the ids own mode
+// chose gives bitwise the same weights.
+#include <cfloat>
+#include <climits>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr int kMaxK = 8;
+constexpr int kWarpsPerBlock = 8;
+
+// a ranks before b: larger value, or equal value and lower expert id.
+__device__ __forceinline__ bool before(float va, int ea, float vb, int eb) {
+    return va > vb || (va == vb && ea < eb);
+}
+
+template <int J>  // logits per lane: E <= 32 * J
+__global__ void __launch_bounds__(32 * kWarpsPerBlock) topk_gates_kernel(
+    const float* __restrict__ logits, int64_t T, int E, int k, const int32_t* __restrict__ ids_in,
+    int32_t* __restrict__ ids_out, float* __restrict__ gates_out, int32_t* __restrict__ valid,
+    int32_t* __restrict__ status) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const float* l = logits + t * E;
+
+    int sel[kMaxK];
+    float sl[kMaxK];
+    bool ok = true;
+    if (ids_in == nullptr) {
+        float v[J];
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int e = lane + 32 * j;
+            v[j] = e < E ? l[e] : -FLT_MAX;
+        }
+        uint32_t taken = 0;
+#pragma unroll
+        for (int s = 0; s < kMaxK; ++s) {
+            if (s >= k) break;
+            float bv = -FLT_MAX;
+            int be = INT_MAX;
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int e = lane + 32 * j;
+                if (e < E && !(taken >> j & 1u) && before(v[j], e, bv, be)) {
+                    bv = v[j];
+                    be = e;
+                }
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+                if (before(ov, oe, bv, be)) {
+                    bv = ov;
+                    be = oe;
+                }
+            }
+            if (be == INT_MAX) be = 0;  // only if every remaining logit is NaN
+            sel[s] = be;
+            sl[s] = bv;
+            if ((be & 31) == lane) taken |= 1u << (be >> 5);
+        }
+    } else {
+        int my = lane < k ? ids_in[t * k + lane] : 0;
+        bool good = lane >= k || (my >= 0 && my < E);
+#pragma unroll
+        for (int s = 0; s < kMaxK; ++s) {
+            if (s >= k) break;
+            const int other = __shfl_sync(0xffffffffu, my, s);
+            if (lane < k && s < lane && other == my) good = false;
+        }
+        ok = __all_sync(0xffffffffu, good);
+        const float lv = (ok && lane < k) ? l[my] : 0.0f;
+#pragma unroll
+        for (int s = 0; s < kMaxK; ++s) {
+            if (s >= k) break;
+            sel[s] = ok ? __shfl_sync(0xffffffffu, my, s) : s;
+            sl[s] = __shfl_sync(0xffffffffu, lv, s);
+        }
+        if (!ok && lane == 0) {
+            atomicOr(status, STATUS_BAD_IDS);
+            atomicAdd(status + 2, 1);
+        }
+    }
+
+    // Gate weights, identical arithmetic for own and replayed ids, fixed order.
+    float m = sl[0];
+#pragma unroll
+    for (int s = 1; s < kMaxK; ++s)
+        if (s < k) m = fmaxf(m, sl[s]);
+    float ex[kMaxK];
+    float den = 0.0f;
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s) {
+        ex[s] = s < k ? expf(sl[s] - m) : 0.0f;
+        den += ex[s];
+    }
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s) {
+        if (s < k && lane == s) {
+            ids_out[t * k + s] = sel[s];
+            gates_out[t * k + s] = ok ? ex[s] / den : 0.0f;
+        }
+    }
+    if (lane == 0) valid[t] = ok ? 1 : 0;
+}
+
+template <int J>
+cudaError_t launch_j(const float* logits, int64_t T, int E, int k, const int32_t* ids_in,
+                     int32_t* ids_out, float* gates_out, int32_t* valid, int32_t* status,
+                     cudaStream_t s) {
+    const int64_t blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+    topk_gates_kernel<J><<<static_cast<unsigned>(blocks), 32 * kWarpsPerBlock, 0, s>>>(
+        logits, T, E, k, ids_in, ids_out, gates_out, valid, status);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_topk_gates(const float* logits, int64_t T, int E, int k,
+                              const int32_t* ids_in, int32_t* ids_out, float* gates_out,
+                              int32_t* valid, int32_t* status, cudaStream_t s) {
+    if (k < 1 || k > kMaxK || E < k || E > 512) return cudaErrorInvalidValue;
+    if (E <= 64) return launch_j<2>(logits, T, E, k, ids_in, ids_out, gates_out, valid, status, s);
+    if (E <= 128) return launch_j<4>(logits, T, E, k, ids_in, ids_out, gates_out, valid, status, s);
+    if (E <= 256) return launch_j<8>(logits, T, E, k, ids_in, ids_out, gates_out, valid, status, s);
+    if (E <= 384) return launch_j<12>(logits, T, E, k, ids_in, ids_out, gates_out, valid, status, s);
+    return launch_j<16>(logits, T, E, k, ids_in, ids_out, gates_out, valid, status, s);
+}
+
+}  // namespace moe

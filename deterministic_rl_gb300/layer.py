@@ -1,0 +1,106 @@
+"""MoELayer: holds the layer's device weights and a workspace and calls the C
+ABI through the binding, allocating output tensors with torch.  Marshalling
+only -- every computation happens in libmoedet."""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import binding as B
+
+
+class MoELayer:
+    def __init__(self, w_router, w_gate, w_up, w_down, *, k: int = 8, router_bias=None,
+                 s_gate=None, s_up=None, s_down=None, ws_gate=None, ws_up=None, ws_down=None,
+                 out_fp32: bool = False):
+        self.E, self.d = w_router.shape
+        self.F = w_gate.shape[1]
+        self.k = k
+        self.n_shared = 1 if ws_gate is not None else 0
+        self.wfmt = B.MOE_W_MXFP8 if s_gate is not None else B.MOE_W_BF16
+        self.out_fp32 = bool(out_fp32)
+        self.device = w_router.device
+        # keep references so the pointers stay valid
+        self._tensors = (w_router, router_bias, w_gate, w_up, w_down, s_gate, s_up, s_down,
+                         ws_gate, ws_up, ws_down)
+        self.weights = B.make_weights(*self._tensors)
+        self._ws = None
+        self._ws_T = -1
+
+    @classmethod
+    def from_inputs(cls, inp, out_fp32: bool = False) -> "MoELayer":
+        return cls(inp.w_router, inp.w_gate, inp.w_up, inp.w_down, k=inp.cfg.k,
+                   router_bias=inp.router_bias, s_gate=inp.s_gate, s_up=inp.s_up,
+                   s_down=inp.s_down, ws_gate=inp.ws_gate, ws_up=inp.ws_up,
+                   ws_down=inp.ws_down, out_fp32=out_fp32)
+
+    def dims(self, T: int) -> B.Dims:
+        return B.Dims(T, self.d, self.E, self.k, self.F, self.n_shared, self.wfmt,
+                      int(self.out_fp32))
+
+    def workspace(self, T: int) -> torch.Tensor:
+        """A workspace for T tokens (reused while T does not grow)."""
+        if self._ws is None or T > self._ws_T:
+            n = B.moe_workspace_size(self.dims(T))
+            if n == 0:
+                raise B.MoEError(B.MOE_ERR_SHAPE, "moe_workspace_size")
+            self._ws = torch.empty(n, dtype=torch.uint8, device=self.device)
+            self._ws_T = T
+        return self._ws
+
+    def outputs(self, T: int):
+        odt = torch.float32 if self.out_fp32 else torch.bfloat16
+        out = torch.empty((T, self.d), dtype=odt, device=self.device)
+        ids = torch.empty((T, self.k), dtype=torch.int32, device=self.device)
+        gates = torch.empty((T, self.k), dtype=torch.float32, device=self.device)
+        return out, ids, gates
+
+    def route(self, x: torch.Tensor, stream=None):
+        T = x.shape[0]
+        ids = torch.empty((T, self.k), dtype=torch.int32, device=self.device)
+        gates = torch.empty((T, self.k), dtype=torch.float32, device=self.device)
+        B.moe_route(self.dims(T), x, self.weights, ids, gates, self.workspace(T), stream)
+        return ids, gates
+
+    def forward(self, x: torch.Tensor, replay_ids: Optional[torch.Tensor] = None, stream=None,
+                outputs=None):
+        T = x.shape[0]
+        out, ids, gates = outputs if outputs is not None else self.outputs(T)
+        ws = self.workspace(T)
+        if replay_ids is None:
+            B.moe_forward(self.dims(T), x, self.weights, out, ids, gates, ws, stream)
+        else:
+            B.moe_forward_replay(self.dims(T), x, self.weights, replay_ids, out, ids, gates, ws,
+                                 stream)
+        return out, ids, gates
+
+    def status(self, stream=None) -> int:
+        return B.moe_get_status(self._ws, stream)
+
+    def intermediates(self, T: int) -> dict:
+        """Views of the workspace's intermediate buffers after a call with T tokens."""
+        L = B.moe_workspace_layout(self.dims(T))
+        ws = self.workspace(T)
+        k, E, d, F = self.k, self.E, self.d, self.F
+        rows = T * k + T * self.n_shared
+
+        def view(off, n, dt):
+            nbytes = n * torch.tensor([], dtype=dt).element_size()
+            return ws[off:off + nbytes].view(dt)
+
+        r = {
+            "status": view(L.status, 4, torch.int32),
+            "logits": view(L.logits, T * E, torch.float32).view(T, E),
+            "valid": view(L.valid, T, torch.int32),
+            "cnt": view(L.cnt, E, torch.int32),
+            "off": view(L.off, E + 1, torch.int32),
+            "perm": view(L.perm, T * k, torch.int32),
+            "inv": view(L.inv, T * k, torch.int32),
+            "xp": view(L.xp, rows * d, torch.bfloat16).view(rows, d),
+            "h": view(L.h, rows * F, torch.bfloat16).view(rows, F),
+            "y": view(L.y, T * k * d, torch.bfloat16).view(T * k, d),
+        }
+        if self.n_shared:
+            r["ysh"] = view(L.ysh, T * d, torch.float32).view(T, d)
+        return r

@@ -23,6 +23,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 import threading
 from dataclasses import dataclass
@@ -32,7 +33,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "moe_oracle.c")
-_LIB_PATH = os.path.join(_HERE, "liboracle.so")
+_LIB_PATH = os.path.join(_HERE, f"liboracle.{platform.machine()}.so")
 _lib = None
 _lock = threading.Lock()
 

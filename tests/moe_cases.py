@@ -1,0 +1,135 @@
+"""Shared helpers of the GPU tests: feeding device-resident layer inputs to the
+fp64 oracle (one expert at a time), and the comparison rules.
+
+Comparison rules (fp32 arithmetic on the GPU against the exact oracle):
+  * ids: the set must equal the oracle's wherever the oracle's fp64 gap between
+    the 8th and 9th logit exceeds 1e-3; the slot order must match too where
+    every adjacent gap among the top 8 exceeds 1e-4.  Elsewhere the GPU's set
+    must be a valid top-8 within 1e-3 of the oracle's logits.
+  * logits: |l_gpu - l_oracle| <= 1e-5 * max(1, max|l|).
+  * gates: |w_gpu - w_oracle| <= 1e-6 + (2e-5 + 1e-6) * w_oracle (softmax of
+    logits that are each within 1e-5).
+  * output (the fp32 combine result): relative Frobenius error <= 5e-3 and
+    max-abs error <= 3e-2; the bf16 output equals the fp32 result rounded to
+    nearest even.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from oracle import Expert, Matrix
+from deterministic_rl_gb300.synthetic import bf16_bits, u8
+
+# fp32 logit error bound: d <= 16384 bf16 products of magnitude ~ |x||w| summed
+# in fp32 stay within 1e-5 of the exact value for logits of order 1.
+LOGIT_ERR = 1e-5
+ID_SET_MARGIN = 1e-3
+ID_ORDER_MARGIN = 1e-4
+REL_FRO = 5e-3
+MAX_ABS = 3e-2
+
+
+def _mat(w: torch.Tensor, s) -> Matrix:
+    if w.dtype == torch.bfloat16:
+        return Matrix(bf16_bits(w))
+    return Matrix(u8(w), u8(s))
+
+
+def expert_getter(inp):
+    def get(e: int) -> Expert:
+        sg = inp.s_gate[e] if inp.s_gate is not None else None
+        su = inp.s_up[e] if inp.s_up is not None else None
+        sd = inp.s_down[e] if inp.s_down is not None else None
+        return Expert(_mat(inp.w_gate[e], sg), _mat(inp.w_up[e], su), _mat(inp.w_down[e], sd))
+    return get
+
+
+def shared_experts(inp):
+    if inp.ws_gate is None:
+        return []
+    return [Expert(Matrix(bf16_bits(inp.ws_gate)), Matrix(bf16_bits(inp.ws_up)),
+                   Matrix(bf16_bits(inp.ws_down)))]
+
+
+def router_host(inp):
+    bias = None if inp.router_bias is None else inp.router_bias.detach().cpu().numpy()
+    return bf16_bits(inp.w_router), bias
+
+
+def oracle_layer(inp, tokens=None, replay_ids=None, x=None):
+    """Oracle layer output for the given token indices (default: all)."""
+    xt = inp.x if x is None else x
+    if tokens is not None:
+        xt = xt[torch.as_tensor(tokens, device=xt.device)]
+    wr, bias = router_host(inp)
+    return oracle.layer_forward(bf16_bits(xt), wr, bias, expert_getter(inp), shared_experts(inp),
+                                inp.cfg.k, replay_ids=replay_ids)
+
+
+def oracle_replay_ids(inp, tokens=None):
+    """Recorded ids: the oracle's own routing of the perturbed hidden states."""
+    xs = inp.x_replay_src
+    if tokens is not None:
+        xs = xs[torch.as_tensor(tokens, device=xs.device)]
+    wr, bias = router_host(inp)
+    lg = oracle.router_logits(bf16_bits(xs), wr, bias)
+    return oracle.select_topk(lg, inp.cfg.k)
+
+
+def check_ids(gpu_ids: np.ndarray, logits: np.ndarray, k: int):
+    """Apply the id rules; returns the mask of tokens whose GPU ids equal the
+    oracle's own selection exactly (set and order)."""
+    T, E = logits.shape
+    order = np.argsort(-logits, axis=1, kind="stable")
+    srt = np.take_along_axis(logits, order, axis=1)
+    gap8 = srt[:, k - 1] - srt[:, k]
+    gaps = srt[:, :k - 1] - srt[:, 1:k]
+    ref = oracle.select_topk(logits, k)
+    same = np.all(gpu_ids == ref, axis=1)
+    for t in range(T):
+        g = gpu_ids[t]
+        assert len(set(g.tolist())) == k and g.min() >= 0 and g.max() < E, (t, g)
+        if gap8[t] > ID_SET_MARGIN:
+            assert set(g.tolist()) == set(ref[t].tolist()), (t, g, ref[t], gap8[t])
+            if gaps[t].min() > ID_ORDER_MARGIN:
+                assert (g == ref[t]).all(), (t, g, ref[t])
+        else:
+            chosen = logits[t, g]
+            others = np.delete(logits[t], g)
+            assert chosen.min() >= others.max() - ID_SET_MARGIN, (t, g)
+            # within the chosen set, slots stay in descending order up to fp32 error
+            assert (np.diff(chosen) <= ID_ORDER_MARGIN).all(), (t, chosen)
+    return same
+
+
+def check_logits(gpu_logits: np.ndarray, ref_logits: np.ndarray):
+    """fp32 router logits (bf16 products, fp32 accumulation over d) against fp64."""
+    err = np.abs(gpu_logits.astype(np.float64) - ref_logits)
+    scale = max(1.0, float(np.abs(ref_logits).max()))
+    assert err.max() <= LOGIT_ERR * scale, float(err.max())
+    return float(err.max())
+
+
+def check_gates(gpu_gates: np.ndarray, ref_gates: np.ndarray):
+    """A gate weight is a softmax of k logits, so a logit error of at most
+    LOGIT_ERR moves it by at most 2 * LOGIT_ERR * w; fp32 exp and division add
+    a few ulp (< 1e-6 * w), and 1e-6 absolute covers the tiny weights."""
+    err = np.abs(gpu_gates.astype(np.float64) - ref_gates)
+    bound = 1e-6 + (2 * LOGIT_ERR + 1e-6) * np.abs(ref_gates)
+    assert (err <= bound).all(), float((err - bound).max())
+
+
+def check_out(gpu_out32: np.ndarray, ref: np.ndarray):
+    diff = gpu_out32.astype(np.float64) - ref
+    den = np.linalg.norm(ref)
+    rel = np.linalg.norm(diff) / den if den > 0 else np.linalg.norm(diff)
+    mx = np.abs(diff).max() if diff.size else 0.0
+    assert rel <= REL_FRO, f"relative Frobenius error {rel:.3e} > {REL_FRO}"
+    assert mx <= MAX_ABS, f"max-abs error {mx:.3e} > {MAX_ABS}"
+    return rel, mx
+
+
+def bf16_of(t32: torch.Tensor) -> torch.Tensor:
+    return t32.to(torch.bfloat16)

@@ -1,0 +1,144 @@
+"""The C-ABI library loads and exports every function include/*.h declares, and
+its host-side validation rejects bad arguments before launching anything.
+CPU only: no call here reaches the GPU (fake pointers are never dereferenced
+because each call fails validation first)."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+from deterministic_rl_gb300 import binding as B
+from deterministic_rl_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return B.load()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        names += re.findall(r"\b(moe_[a-z_]+)\s*\([^;{]*\)\s*;", src)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(names) == set(B.EXPORTED), names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def good_dims(**kw):
+    d = dict(T=64, d=7168, E=384, k=8, F=2048, n_shared=1)
+    d.update(kw)
+    return B.Dims(**d)
+
+
+def test_workspace_size_and_layout(lib):
+    d = good_dims()
+    n = B.moe_workspace_size(d)
+    L = B.moe_workspace_layout(d)
+    assert L.total == n > 0
+    offs = [L.status, L.logits, L.valid, L.cnt, L.off, L.perm, L.inv, L.xp, L.h, L.y, L.ysh]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    assert L.logits - L.status >= 16
+    assert L.valid - L.logits >= 64 * 384 * 4
+    assert L.h - L.xp >= (64 * 8 + 64) * 7168 * 2
+    assert n - L.ysh >= 64 * 7168 * 4
+    # the workspace grows linearly in T (no hidden per-call allocation)
+    assert B.moe_workspace_size(good_dims(T=128)) > n
+
+
+@pytest.mark.parametrize("bad", [dict(k=4), dict(E=4), dict(E=1024), dict(d=100), dict(F=96),
+                                 dict(n_shared=2), dict(T=-1), dict(T=(1 << 20) + 1),
+                                 dict(wfmt=7), dict(out_fp32=2), dict(wfmt=1, d=192)])
+def test_bad_dims_rejected(lib, bad):
+    d = good_dims(**bad)
+    assert B.moe_workspace_size(d) == 0
+    with pytest.raises(B.MoEError) as ei:
+        B.moe_workspace_layout(d)
+    assert ei.value.code == B.MOE_ERR_SHAPE
+
+
+class _Fake:
+    """Stands in for a tensor: an address that validation never dereferences."""
+    def __init__(self, addr, nbytes=16):
+        self.addr, self.nbytes = addr, nbytes
+
+    def data_ptr(self):
+        return self.addr
+
+    def numel(self):
+        return self.nbytes
+
+    def element_size(self):
+        return 1
+
+
+_DEFAULT_WS = _Fake(0x10000)
+
+
+def _call(lib, fn, dims, x, w, *ptrs, ws=_DEFAULT_WS, ws_bytes=None):
+    nbytes = ws_bytes if ws_bytes is not None else (B.moe_workspace_size(dims) or 1)
+    cargs = [ctypes.c_void_p(p.data_ptr() if p is not None else None) for p in ptrs]
+    f = getattr(lib, fn)
+    return f(ctypes.byref(dims.c()), ctypes.c_void_p(x.data_ptr() if x else None),
+             ctypes.byref(w), *cargs, ctypes.c_void_p(ws.data_ptr() if ws else None),
+             nbytes, ctypes.c_void_p(None))
+
+
+def _weights(**override):
+    base = dict(w_router=_Fake(0x20000), router_bias=None, w_gate=_Fake(0x30000),
+                w_up=_Fake(0x40000), w_down=_Fake(0x50000), ws_gate=_Fake(0x60000),
+                ws_up=_Fake(0x70000), ws_down=_Fake(0x80000))
+    base.update(override)
+    return B.make_weights(**base)
+
+
+def test_host_validation_codes(lib):
+    d = good_dims()
+    x, out, ids, g = _Fake(0x1000), _Fake(0x2000), _Fake(0x3000), _Fake(0x4000)
+    fwd = lambda w=_weights(), **kw: _call(lib, "moe_forward", kw.pop("dims", d), kw.pop("x", x), w,
+                                           kw.pop("out", out), kw.pop("ids", ids),
+                                           kw.pop("g", g), **kw)
+    # T == 0 is a no-op
+    assert fwd(dims=good_dims(T=0)) == B.MOE_OK
+    # null pointers
+    assert fwd(x=None) == B.MOE_ERR_ARG
+    assert fwd(out=None) == B.MOE_ERR_ARG
+    assert fwd(w=_weights(w_gate=None)) == B.MOE_ERR_ARG
+    assert fwd(w=_weights(ws_down=None)) == B.MOE_ERR_ARG
+    assert fwd(ws=None) == B.MOE_ERR_ARG
+    # misaligned pointers
+    assert fwd(x=_Fake(0x1004)) == B.MOE_ERR_ALIGN
+    assert fwd(w=_weights(w_up=_Fake(0x40008))) == B.MOE_ERR_ALIGN
+    assert fwd(g=_Fake(0x4002)) == B.MOE_ERR_ALIGN
+    # short workspace
+    assert fwd(ws_bytes=B.moe_workspace_size(d) - 1) == B.MOE_ERR_WORKSPACE
+    # bad shapes
+    assert fwd(dims=good_dims(E=3)) == B.MOE_ERR_SHAPE
+    # MXFP8 weights without their scales
+    assert fwd(dims=good_dims(wfmt=1)) == B.MOE_ERR_ARG
+    # replay needs its ids
+    rc = _call(lib, "moe_forward_replay", d, x, _weights(), None, out, ids, g)
+    assert rc == B.MOE_ERR_ARG
+    # routing only: outputs required
+    assert _call(lib, "moe_route", d, x, _weights(), None, g) == B.MOE_ERR_ARG
+    assert lib.moe_get_status(None, None) == B.MOE_ERR_ARG
+
+
+def test_status_strings(lib):
+    for code in range(9):
+        s = B.moe_status_str(code)
+        assert s.startswith("MOE_")
+    assert "unknown" in B.moe_status_str(99)
