@@ -1,0 +1,446 @@
+#!/usr/bin/env python3
+"""Benchmark of the deterministic MoE layer forward with router replay.
+
+One step = one full layer call (router GEMM, top-k or replay + gates, dispatch,
+gather, grouped gate/up GEMM with SwiGLU, grouped down GEMM, fixed-order
+combine) over one batch of synthetic tokens, through the C ABI.  The default
+workload is the decode-like replay layer: T=64 tokens, d=7168, E=384 experts,
+top-8, expert FFN 2048, one shared expert, bf16 weights, recorded ids from a
+perturbed copy of the hidden states.  Prints one JSON line (rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--config NAME] [--mode replay|own]
+
+Under torchrun each rank runs its own batch on its own GPU (weak scaling, no
+collective on the data path; a barrier and a max over ranks for timing).
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (384-expert top-8, d=7168, replay, bf16); % of roofline"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 2 ** 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNELS_PER_STEP = 9  # router GEMM, top-k, hist, scan, scatter, gather, gate/up, down, combine
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="c2_decode_replay")
+    ap.add_argument("--mode", choices=["replay", "own"], default="replay")
+    ap.add_argument("--cpu-sample", type=int, default=8,
+                    help="tokens of the workload the CPU-baseline oracle runs on")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_desc(cfg, mode):
+    return (f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} top-{cfg.k} F={cfg.F} "
+            f"shared={cfg.n_shared} weights={cfg.wfmt} mode={mode}")
+
+
+def layer_work(cfg, touched):
+    """Algorithmic FLOPs and bytes of one layer call (touched = routed experts
+    with at least one token)."""
+    T, d, E, k, F, S = cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.n_shared
+    flops = T * (2 * d * E + 6 * d * F * (k + S))
+    wbytes = 3 * d * F * (2 if cfg.wfmt == "bf16" else (1 + 1 / 32))
+    nbytes = (touched * wbytes + S * 3 * d * F * 2 + E * d * 2 + T * d * 2 + T * d * 2
+              + T * k * (4 + 4 + 4))
+    return flops, nbytes
+
+
+def gate_up_bytes(cfg, touched):
+    """Algorithmic bytes of one grouped gate/up GEMM launch: the gate and up
+    weights of every touched expert (and the shared one) read once, the
+    gathered token rows read, the SwiGLU activations written."""
+    T, d, k, F, S = cfg.T, cfg.d, cfg.k, cfg.F, cfg.n_shared
+    rows = T * k + T * S
+    wb = 2 if cfg.wfmt == "bf16" else (1 + 1 / 32)
+    return (touched + S) * 2 * F * d * wb + rows * d * 2 + rows * F * 2
+
+
+def down_bytes(cfg, touched):
+    T, d, k, F, S = cfg.T, cfg.d, cfg.k, cfg.F, cfg.n_shared
+    rows = T * k + T * S
+    wb = 2 if cfg.wfmt == "bf16" else (1 + 1 / 32)
+    return (touched + S) * d * F * wb + rows * F * 2 + T * k * d * 2 + S * T * d * 4
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.15)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[3:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, _, r in rows:
+            for n, v in zip(names, r[1:]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def stored_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if the
+    kernel source has not changed since it was captured; else None."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f).get(kernel)
+    if not d:
+        return None
+    src = os.path.join(ROOT, "deterministic_rl_gb300", "csrc", d.get("source", "gemm.cu"))
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    return d.get("bytes_per_launch") if h == d.get("source_sha256_16") else None
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, value):
+    if world == 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64,
+                     device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def host_experts(inp, ids_np):
+    """The oracle's view of the experts a token sample uses, fetched to host."""
+    import numpy as np
+    import oracle
+    from oracle import Expert, Matrix
+    from deterministic_rl_gb300.synthetic import bf16_bits, u8
+
+    def mat(w, s):
+        return Matrix(bf16_bits(w)) if s is None else Matrix(u8(w), u8(s))
+    cache = {}
+    for e in sorted(set(np.asarray(ids_np).reshape(-1).tolist())):
+        cache[e] = Expert(mat(inp.w_gate[e], None if inp.s_gate is None else inp.s_gate[e]),
+                          mat(inp.w_up[e], None if inp.s_up is None else inp.s_up[e]),
+                          mat(inp.w_down[e], None if inp.s_down is None else inp.s_down[e]))
+    shared = []
+    if inp.ws_gate is not None:
+        shared = [Expert(Matrix(bf16_bits(inp.ws_gate)), Matrix(bf16_bits(inp.ws_up)),
+                         Matrix(bf16_bits(inp.ws_down)))]
+    return cache, shared
+
+
+def oracle_sample(inp, tokens, mode):
+    """Inputs of an oracle run over the given token indices: hidden states,
+    router, recorded ids (the oracle's routing of the perturbed copy) and the
+    experts they touch, all on the host."""
+    import numpy as np
+    import torch
+    import oracle
+    from deterministic_rl_gb300.synthetic import bf16_bits
+    idx = torch.as_tensor(tokens, device=inp.x.device)
+    x = bf16_bits(inp.x[idx])
+    wr = bf16_bits(inp.w_router)
+    bias = None if inp.router_bias is None else inp.router_bias.cpu().numpy()
+    if mode == "replay":
+        lg = oracle.router_logits(bf16_bits(inp.x_replay_src[idx]), wr, bias)
+        rid = oracle.select_topk(lg, inp.cfg.k)
+        need = rid
+    else:
+        rid = None
+        need = oracle.select_topk(oracle.router_logits(x, wr, bias), inp.cfg.k)
+    cache, shared = host_experts(inp, need)
+    return x, wr, bias, rid, cache, shared
+
+
+def time_oracle(inp, tokens, mode, repeats=1):
+    import oracle
+    x, wr, bias, rid, cache, shared = oracle_sample(inp, tokens, mode)
+    cores = oracle.set_threads(os.cpu_count() or 1)
+    t0 = time.perf_counter()
+    for _ in range(repeats):
+        oracle.layer_forward(x, wr, bias, lambda e: cache[e], shared, inp.cfg.k, replay_ids=rid)
+    dt = time.perf_counter() - t0
+    return len(tokens) * repeats / dt, cores, dt
+
+
+def run_reference(args):
+    """The fp64 CPU oracle as it stands, on a bounded sample of the workload."""
+    import torch
+    import oracle
+    from deterministic_rl_gb300.synthetic import CONFIGS, make_layer
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    cfg = CONFIGS[args.config]
+    oracle.build()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = make_layer(cfg, dev)  # same seeded bytes as the GPU arm
+    per_step = 1
+    pool = list(range(min(cfg.T, 8)))
+    x, wr, bias, rid, cache, shared = oracle_sample(inp, pool, args.mode)
+    cores = oracle.set_threads(os.cpu_count() or 1)
+
+    def step(i):
+        j = i % len(pool)
+        oracle.layer_forward(x[j:j + per_step], wr, bias, lambda e: cache[e], shared, cfg.k,
+                             replay_ids=None if rid is None else rid[j:j + per_step])
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = args.steps * per_step / dt
+    sample = (f"{per_step} token per step, cycling over the first {len(pool)} tokens of "
+              f"{cfg.name} ({args.mode}); fp64 oracle on {cores} host threads")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_desc(cfg, args.mode)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+    from deterministic_rl_gb300 import MoELayer, binding as B, build as lib_build
+    from deterministic_rl_gb300.synthetic import CONFIGS, make_layer
+    world, rank, local = dist_setup(args)
+    lib_build.build()
+    cfg = CONFIGS[args.config]
+    # weak scaling: every rank runs its own batch (seed offset by rank)
+    inp = make_layer(cfg.with_(seed=cfg.seed + 1000 * rank) if rank else cfg, "cuda")
+    layer = MoELayer.from_inputs(inp)
+    T, K = cfg.T, args.steps
+    replay = None
+    if args.mode == "replay":
+        rid, _ = layer.route(inp.x_replay_src)  # recorded at "inference": untimed
+        replay = rid.clone()
+    outs = layer.outputs(T)
+
+    def step(x=inp.x, ids=replay):
+        layer.forward(x, replay_ids=ids, outputs=outs)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if layer.status() != 0:
+        raise RuntimeError(f"device status after warm-up: {B.status_str(layer.status())}")
+    cnt = layer.intermediates(T)["cnt"].cpu()
+    touched = int((cnt > 0).sum())
+    flops, nbytes = layer_work(cfg, touched)
+    need_flush = nbytes < 2 * L2_BYTES
+    flush = torch.empty(2 * L2_BYTES, dtype=torch.uint8, device="cuda") if need_flush else None
+
+    ns = len(B.STAGES)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * ns)] for _ in range(K)]
+    step_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(K)]
+    for row in evs:
+        for e in row:
+            e.record()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record()
+        for i in range(K):
+            if need_flush:
+                flush.zero_()
+            step_ev[i][0].record()
+            B.moe_set_stage_events(evs[i])
+            step()
+            step_ev[i][1].record()
+        end.record()
+        torch.cuda.synchronize()
+    B.moe_set_stage_events(None)
+    barrier(world)
+    if layer.status() != 0:
+        raise RuntimeError(f"device status after timing: {B.status_str(layer.status())}")
+    if need_flush:
+        elapsed = sum(a.elapsed_time(b) for a, b in step_ev)
+    else:
+        elapsed = start.elapsed_time(end)
+    t_ms = max_over_ranks(world, elapsed)
+    ms_per_step = t_ms / K
+    value = world * T * K / (t_ms / 1e3)
+    stage_ms = {name: statistics.fmean(evs[i][2 * j].elapsed_time(evs[i][2 * j + 1]) for i in range(K))
+                for j, name in enumerate(B.STAGES)}
+
+    pk, pk_kind = peaks()
+    hbm = float(pk["hbm_gbs"])
+    tensor = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    gu_bytes = gate_up_bytes(cfg, touched)
+    gu_ms = stage_ms["gate_up"]
+    achieved = gu_bytes / (gu_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm, "traffic": stored_traffic("gate_up"),
+                "kernel": "grouped_gemm_kernel<GEMM_SWIGLU> (grouped gate/up GEMM + SwiGLU)",
+                "algorithmic_bytes_per_launch": gu_bytes, "avg_launch_ms": gu_ms,
+                "peak_source": f"{pk_kind} (MEASURED_PEAKS.json hbm_gbs)" if pk_kind == "measured"
+                else "fallback 6.8 TB/s"}
+    t_roof = max(flops / (tensor * 1e12), nbytes / (hbm * 1e9))
+    layer_roof = {"flops": flops, "bytes": nbytes, "touched_experts": touched,
+                  "bound": "tensor" if flops / (tensor * 1e12) > nbytes / (hbm * 1e9) else "hbm",
+                  "roofline_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_per_step,
+                  "frac_nominal_8tbs": 1e3 * max(flops / 2.25e15, nbytes / 8e12) / ms_per_step,
+                  "peaks": f"{pk_kind}: {hbm} GB/s, {tensor} TFLOP/s bf16"}
+
+    e2e = None
+    if not args.no_e2e:
+        x_h = inp.x.cpu().pin_memory()
+        rid_h = replay.cpu().pin_memory() if replay is not None else None
+        out_h = torch.empty(outs[0].shape, dtype=outs[0].dtype, pin_memory=True)
+        ids_h = torch.empty(outs[1].shape, dtype=outs[1].dtype, pin_memory=True)
+        g_h = torch.empty(outs[2].shape, dtype=outs[2].dtype, pin_memory=True)
+        x_d = torch.empty_like(inp.x)
+        rid_d = torch.empty_like(replay) if replay is not None else None
+        Ke = max(1, min(K, 100))
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(Ke):
+            x_d.copy_(x_h, non_blocking=True)
+            if rid_d is not None:
+                rid_d.copy_(rid_h, non_blocking=True)
+            layer.forward(x_d, replay_ids=rid_d, outputs=outs)
+            out_h.copy_(outs[0], non_blocking=True)
+            ids_h.copy_(outs[1], non_blocking=True)
+            g_h.copy_(outs[2], non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        dt = max_over_ranks(world, time.perf_counter() - t0)
+        h2d = x_h.numel() * 2 + (rid_h.numel() * 4 if rid_h is not None else 0)
+        d2h = out_h.numel() * out_h.element_size() + ids_h.numel() * 4 + g_h.numel() * 4
+        e2e = {"value": world * T * Ke / dt, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": Ke,
+               "api": "MoELayer.forward -> moe_forward_replay (C ABI), pinned host buffers"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        tokens = list(range(min(T, args.cpu_sample)))
+        v, cores, dt = time_oracle(inp, tokens, args.mode)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"first {len(tokens)} tokens of {cfg.name} ({args.mode}), one fp64 "
+                         f"oracle layer pass, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": workload_desc(cfg, args.mode), "tokens_per_step": T,
+                           "parallelism": f"replicas x{world} (own batch per GPU, no collective)",
+                           "l2": ("L2 flushed between steps" if need_flush else
+                                  f"inputs larger than L2: {nbytes / 1e9:.1f} GB read per step")},
+                "roofline": roofline, "layer_roofline": layer_roof, "stages_ms": stage_ms,
+                "clocks": clk.summary(), "e2e": e2e, "gpu_launches": KERNELS_PER_STEP * K,
+                "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

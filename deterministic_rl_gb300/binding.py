@@ -32,7 +32,9 @@ MOE_W_MXFP8 = 1
 
 # Every function the header declares, in declaration order.
 EXPORTED = ("moe_workspace_size", "moe_workspace_layout", "moe_route", "moe_forward",
-            "moe_forward_replay", "moe_get_status", "moe_status_str")
+            "moe_forward_replay", "moe_get_status", "moe_status_str", "moe_set_stage_events")
+
+STAGES = ("router_gemm", "topk", "dispatch", "gather", "gate_up", "down", "combine")
 
 
 class moe_dims(ctypes.Structure):
@@ -88,6 +90,8 @@ def load(path: str = LIB_PATH):
     lib.moe_get_status.argtypes = [P, P]
     lib.moe_status_str.restype = ctypes.c_char_p
     lib.moe_status_str.argtypes = [ctypes.c_int]
+    lib.moe_set_stage_events.restype = ctypes.c_int
+    lib.moe_set_stage_events.argtypes = [ctypes.c_void_p]
     _lib = lib
     return lib
 
@@ -176,3 +180,14 @@ def moe_get_status(ws, stream=None) -> int:
 
 def moe_status_str(code: int) -> str:
     return status_str(code)
+
+
+def moe_set_stage_events(events) -> int:
+    """events: None, or a sequence of 2 * len(STAGES) torch.cuda.Event objects
+    (created with enable_timing=True and already recorded once so that their
+    handles exist).  See the header for the semantics."""
+    if events is None:
+        return int(load().moe_set_stage_events(None))
+    assert len(events) == 2 * len(STAGES)
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    return int(load().moe_set_stage_events(ctypes.cast(arr, ctypes.c_void_p)))

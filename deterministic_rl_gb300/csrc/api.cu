@@ -127,6 +127,15 @@ moe_status check_experts(const moe_dims* d, const moe_weights* w) {
 
 inline moe_status cu(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
+// Per-host-thread stage timing events (moe_set_stage_events); null = off.
+thread_local cudaEvent_t g_stage_events[2 * MOE_NUM_STAGES];
+thread_local bool g_stage_timing = false;
+
+inline moe_status mark(int stage, int edge, cudaStream_t s) {
+    if (!g_stage_timing) return MOE_OK;
+    return cu(cudaEventRecord(g_stage_events[2 * stage + edge], s));
+}
+
 #define MOE_TRY(expr)                         \
     do {                                      \
         const moe_status st_ = (expr);        \
@@ -162,10 +171,14 @@ moe_status run_route(const moe_dims* d, const void* x, const moe_weights* w, con
     const int sms = num_sms();
     if (sms <= 0) return MOE_ERR_CUDA;
     const int grid = static_cast<int>(tiles < sms ? tiles : sms);
+    MOE_TRY(mark(MOE_STAGE_ROUTER_GEMM, 0, s));
     MOE_TRY(cu(launch_grouped_gemm(GEMM_ROUTER, p, grid, s)));
-    return cu(launch_topk_gates(reinterpret_cast<const float*>(ws + L.logits), T, d->E, d->k, ids_in,
-                                ids_out, gates_out, reinterpret_cast<int32_t*>(ws + L.valid), status,
-                                s));
+    MOE_TRY(mark(MOE_STAGE_ROUTER_GEMM, 1, s));
+    MOE_TRY(mark(MOE_STAGE_TOPK, 0, s));
+    MOE_TRY(cu(launch_topk_gates(reinterpret_cast<const float*>(ws + L.logits), T, d->E, d->k,
+                                 ids_in, ids_out, gates_out,
+                                 reinterpret_cast<int32_t*>(ws + L.valid), status, s)));
+    return mark(MOE_STAGE_TOPK, 1, s);
 }
 
 // Dispatch, expert FFNs and combine, given ids/gates of every token.
@@ -180,10 +193,14 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     int32_t* off = reinterpret_cast<int32_t*>(ws + L.off);
     int32_t* perm = reinterpret_cast<int32_t*>(ws + L.perm);
     int32_t* inv = reinterpret_cast<int32_t*>(ws + L.inv);
+    MOE_TRY(mark(MOE_STAGE_DISPATCH, 0, s));
     MOE_TRY(cu(launch_dispatch(ids, T, k, E, cnt, off, perm, inv,
                                reinterpret_cast<int32_t*>(ws + L.scratch), s)));
+    MOE_TRY(mark(MOE_STAGE_DISPATCH, 1, s));
+    MOE_TRY(mark(MOE_STAGE_GATHER, 0, s));
     MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), perm, T, k, d->d, S,
                              reinterpret_cast<uint16_t*>(ws + L.xp), s)));
+    MOE_TRY(mark(MOE_STAGE_GATHER, 1, s));
     const int sms = num_sms();
     if (sms <= 0) return MOE_ERR_CUDA;
     const int64_t ntile_bound = (T * k + BN - 1) / BN + E + (S ? (T + BN - 1) / BN : 0);
@@ -212,7 +229,9 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     p1.status = status;
     p1.timeout_ns = kWaitTimeoutNs;
     int64_t tb = ntile_bound * p1.MT;
+    MOE_TRY(mark(MOE_STAGE_GATE_UP, 0, s));
     MOE_TRY(cu(launch_grouped_gemm(GEMM_SWIGLU, p1, static_cast<int>(tb < sms ? tb : sms), s)));
+    MOE_TRY(mark(MOE_STAGE_GATE_UP, 1, s));
 
     // down projection -> Y (routed, bf16) and Ysh (shared, fp32)
     GemmParams p2;
@@ -235,12 +254,16 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     p2.status = status;
     p2.timeout_ns = kWaitTimeoutNs;
     tb = ntile_bound * p2.MT;
+    MOE_TRY(mark(MOE_STAGE_DOWN, 0, s));
     MOE_TRY(cu(launch_grouped_gemm(GEMM_DOWN, p2, static_cast<int>(tb < sms ? tb : sms), s)));
+    MOE_TRY(mark(MOE_STAGE_DOWN, 1, s));
 
-    return cu(launch_combine(reinterpret_cast<const uint16_t*>(ws + L.y),
-                             S ? reinterpret_cast<const float*>(ws + L.ysh) : nullptr, inv, gates,
-                             reinterpret_cast<const int32_t*>(ws + L.valid), T, k, d->d,
-                             d->out_fp32, out, s));
+    MOE_TRY(mark(MOE_STAGE_COMBINE, 0, s));
+    MOE_TRY(cu(launch_combine(reinterpret_cast<const uint16_t*>(ws + L.y),
+                              S ? reinterpret_cast<const float*>(ws + L.ysh) : nullptr, inv, gates,
+                              reinterpret_cast<const int32_t*>(ws + L.valid), T, k, d->d,
+                              d->out_fp32, out, s)));
+    return mark(MOE_STAGE_COMBINE, 1, s);
 }
 
 moe_status forward_impl(const moe_dims* d, const void* x, const moe_weights* w,
@@ -319,6 +342,17 @@ moe_status moe_get_status(const void* ws, moe_stream_t stream) {
     if (cudaMemcpy(h, ws, sizeof h, cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
     if (h[0] & STATUS_TIMEOUT) return MOE_ERR_TIMEOUT;
     if (h[0] & STATUS_BAD_IDS) return MOE_ERR_BAD_IDS;
+    return MOE_OK;
+}
+
+moe_status moe_set_stage_events(void* const* events) {
+    if (!events) {
+        g_stage_timing = false;
+        return MOE_OK;
+    }
+    for (int i = 0; i < 2 * MOE_NUM_STAGES; ++i)
+        g_stage_events[i] = static_cast<cudaEvent_t>(events[i]);
+    g_stage_timing = true;
     return MOE_OK;
 }
 

@@ -183,6 +183,27 @@ moe_status moe_get_status(const void *ws, moe_stream_t stream);
 /* Static, human-readable name of a status code. */
 const char *moe_status_str(moe_status s);
 
+/* Stages of one layer call, in launch order. */
+typedef enum {
+    MOE_STAGE_ROUTER_GEMM = 0,  /* logits = x . w_router^T + bias             */
+    MOE_STAGE_TOPK = 1,         /* selection or replay check, gate weights    */
+    MOE_STAGE_DISPATCH = 2,     /* histogram, offsets, stable permutation     */
+    MOE_STAGE_GATHER = 3,       /* token rows into expert order               */
+    MOE_STAGE_GATE_UP = 4,      /* grouped gate/up GEMM with SwiGLU           */
+    MOE_STAGE_DOWN = 5,         /* grouped down GEMM                          */
+    MOE_STAGE_COMBINE = 6,      /* fixed-order weighted sum per token         */
+    MOE_NUM_STAGES = 7
+} moe_stage;
+
+/* Optional per-stage timing for profiling.  `events` points to
+ * 2 * MOE_NUM_STAGES cudaEvent_t handles created by the caller (or is NULL to
+ * switch timing off).  While set, every call from the calling host thread
+ * records events[2*j] on its stream just before stage j and events[2*j+1]
+ * just after it (moe_route records only its two stages).  The setting is per
+ * host thread; the library does not own or destroy the events.  Returns
+ * MOE_OK. */
+moe_status moe_set_stage_events(void *const *events);
+
 #ifdef __cplusplus
 }
 #endif
