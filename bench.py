@@ -46,7 +46,9 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="c2_decode_replay")
     ap.add_argument("--mode", choices=["replay", "own"], default="replay")
-    ap.add_argument("--cpu-sample", type=int, default=8,
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the expert count (small captures for the profiler)")
+    ap.add_argument("--cpu-sample", type=int, default=64,
                     help="tokens of the workload the CPU-baseline oracle runs on")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -262,6 +264,8 @@ def run_reference(args):
     if rank != 0:
         return 0
     cfg = CONFIGS[args.config]
+    if args.experts:
+        cfg = cfg.with_(name=f"{cfg.name}_E{args.experts}", E=args.experts)
     oracle.build()
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = make_layer(cfg, dev)  # same seeded bytes as the GPU arm
@@ -301,6 +305,8 @@ def run_ours(args):
     world, rank, local = dist_setup(args)
     lib_build.build()
     cfg = CONFIGS[args.config]
+    if args.experts:
+        cfg = cfg.with_(name=f"{cfg.name}_E{args.experts}", E=args.experts)
     # weak scaling: every rank runs its own batch (seed offset by rank)
     inp = make_layer(cfg.with_(seed=cfg.seed + 1000 * rank) if rank else cfg, "cuda")
     layer = MoELayer.from_inputs(inp)
