@@ -32,7 +32,8 @@ MOE_W_MXFP8 = 1
 
 # Every function the header declares, in declaration order.
 EXPORTED = ("moe_workspace_size", "moe_workspace_layout", "moe_route", "moe_forward",
-            "moe_forward_replay", "moe_get_status", "moe_status_str", "moe_set_stage_events")
+            "moe_forward_replay", "moe_get_status", "moe_status_str", "moe_set_stage_events",
+            "moe_route_static")
 
 STAGES = ("router_gemm", "topk", "dispatch", "gather", "gate_up", "down", "combine")
 
@@ -92,6 +93,8 @@ def load(path: str = LIB_PATH):
     lib.moe_status_str.argtypes = [ctypes.c_int]
     lib.moe_set_stage_events.restype = ctypes.c_int
     lib.moe_set_stage_events.argtypes = [ctypes.c_void_p]
+    lib.moe_route_static.restype = ctypes.c_int
+    lib.moe_route_static.argtypes = [D, P, W, P, P, P]
     _lib = lib
     return lib
 
@@ -191,3 +194,14 @@ def moe_set_stage_events(events) -> int:
     assert len(events) == 2 * len(STAGES)
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     return int(load().moe_set_stage_events(ctypes.cast(arr, ctypes.c_void_p)))
+
+
+def moe_route_static(dims: Dims, x, weights: moe_weights, ids_out, gates_out, stream=None,
+                     check: bool = True) -> int:
+    """Routing whose scratch is the library's static device array: for callers
+    that cannot allocate device memory (see the header)."""
+    rc = load().moe_route_static(ctypes.byref(dims.c()), _p(x), ctypes.byref(weights),
+                                 _p(ids_out), _p(gates_out), _stream(stream))
+    if check and rc != MOE_OK:
+        raise MoEError(rc, "moe_route_static")
+    return rc

@@ -204,6 +204,35 @@ typedef enum {
  * MOE_OK. */
 moe_status moe_set_stage_events(void *const *events);
 
+/* Routing that allocates nothing -- the pages have no counterpart of this
+ * call; it is a convenience of this library.
+ *
+ * Same computation and outputs as moe_route (ids_out [T][k] int32 and
+ * gates_out [T][k] fp32, device pointers the caller owns), but the scratch
+ * memory moe_route takes from the caller's workspace (status word, per-token
+ * flags, fp32 logits) lives in a static device array of 4 MiB inside this
+ * library, which every GPU that loads the library holds until the process
+ * exits.  It is meant for callers that cannot allocate device memory: an
+ * inference engine recording routing decisions inside its decode loop, where
+ * all device memory belongs to the engine's own pool and a cudaMalloc would
+ * synchronise the device or fail, or a plugin whose host framework hands it
+ * only input and output buffers.  The call itself makes no cudaMalloc,
+ * cudaFree or other allocating call.
+ *
+ * Limit: 256 + round_up(4*T, 256) + 4*T*E <= 4 MiB (T <= 2723 at E = 384);
+ * larger requests return MOE_ERR_WORKSPACE before any launch.  Shape, null
+ * and alignment errors are reported as for moe_route.
+ * Set-up: the first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call before
+ * any stream capture begins.
+ * Sharing: every call uses the same array, which keeps the last call's
+ * contents; the call clears its status word itself.  Calls that overlap on the
+ * GPU (other streams, other host threads) race on the array and must be
+ * serialised by the caller.  The device status word is not readable through
+ * this entry point. */
+moe_status moe_route_static(const moe_dims *dims, const void *x, const moe_weights *w,
+                            int32_t *ids_out, float *gates_out, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
