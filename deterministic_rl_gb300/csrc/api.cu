@@ -157,6 +157,8 @@ moe_status run_route(const moe_dims* d, const void* x, const moe_weights* w, con
     std::memset(&p, 0, sizeof p);
     if (!make_map(&p.a0, w->w_router, d->d, d->E, BM)) return MOE_ERR_CUDA;
     if (!make_map(&p.b, x, d->d, T, BN)) return MOE_ERR_CUDA;
+    if (!make_map(&p.b32, x, d->d, T, 32)) return MOE_ERR_CUDA;
+    p.partial_b = 1;
     p.G = 1;
     p.n_single = static_cast<int32_t>(T);
     p.M = d->E;
@@ -203,18 +205,23 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     MOE_TRY(mark(MOE_STAGE_GATHER, 1, s));
     const int sms = num_sms();
     if (sms <= 0) return MOE_ERR_CUDA;
-    const int64_t ntile_bound = (T * k + BN - 1) / BN + E + (S ? (T + BN - 1) / BN : 0);
+    auto ntile_bound = [&](int bn) {
+        return (T * k + bn - 1) / bn + E + (S ? (T + bn - 1) / bn : 0);
+    };
 
     // gate/up projections with the SwiGLU epilogue -> H
     GemmParams p1;
     std::memset(&p1, 0, sizeof p1);
-    if (!make_map(&p1.a0, w->w_gate, d->d, uint64_t(E) * d->F, BM)) return MOE_ERR_CUDA;
-    if (!make_map(&p1.a1, w->w_up, d->d, uint64_t(E) * d->F, BM)) return MOE_ERR_CUDA;
+    const uint32_t r1 = gemm_rows(GEMM_SWIGLU);  // gate rows (and up rows) per tile
+    if (!make_map(&p1.a0, w->w_gate, d->d, uint64_t(E) * d->F, r1)) return MOE_ERR_CUDA;
+    if (!make_map(&p1.a1, w->w_up, d->d, uint64_t(E) * d->F, r1)) return MOE_ERR_CUDA;
     if (S) {
-        if (!make_map(&p1.as0, w->ws_gate, d->d, d->F, BM)) return MOE_ERR_CUDA;
-        if (!make_map(&p1.as1, w->ws_up, d->d, d->F, BM)) return MOE_ERR_CUDA;
+        if (!make_map(&p1.as0, w->ws_gate, d->d, d->F, r1)) return MOE_ERR_CUDA;
+        if (!make_map(&p1.as1, w->ws_up, d->d, d->F, r1)) return MOE_ERR_CUDA;
     }
-    if (!make_map(&p1.b, ws + L.xp, d->d, rows, BN)) return MOE_ERR_CUDA;
+    if (!make_map(&p1.b, ws + L.xp, d->d, rows, gemm_bn(GEMM_SWIGLU) / 2)) return MOE_ERR_CUDA;
+    if (!make_map(&p1.b32, ws + L.xp, d->d, rows, 32)) return MOE_ERR_CUDA;
+    p1.partial_b = 1;
     p1.cnt = cnt;
     p1.off = off;
     p1.G = E;
@@ -222,15 +229,16 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     p1.shared_rows = static_cast<int32_t>(T);
     p1.shared_b_off = static_cast<int32_t>(T * k);
     p1.M = d->F;
-    p1.MT = (d->F + BM - 1) / BM;
+    p1.MT = (d->F + 2 * r1 - 1) / (2 * r1);  // tiles of 2 * r1 rows: one CTA pair
     p1.KB = d->d / BK;
     p1.out = ws + L.h;
     p1.ldo = d->F;
     p1.status = status;
     p1.timeout_ns = kWaitTimeoutNs;
-    int64_t tb = ntile_bound * p1.MT;
+    int64_t tb = ntile_bound(gemm_bn(GEMM_SWIGLU)) * p1.MT;
+    const int pairs = sms / 2;
     MOE_TRY(mark(MOE_STAGE_GATE_UP, 0, s));
-    MOE_TRY(cu(launch_grouped_gemm(GEMM_SWIGLU, p1, static_cast<int>(tb < sms ? tb : sms), s)));
+    MOE_TRY(cu(launch_pair_gemm(GEMM_SWIGLU, p1, static_cast<int>(tb < pairs ? tb : pairs), s)));
     MOE_TRY(mark(MOE_STAGE_GATE_UP, 1, s));
 
     // down projection -> Y (routed, bf16) and Ysh (shared, fp32)
@@ -238,7 +246,9 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     std::memset(&p2, 0, sizeof p2);
     if (!make_map(&p2.a0, w->w_down, d->F, uint64_t(E) * d->d, BM)) return MOE_ERR_CUDA;
     if (S && !make_map(&p2.as0, w->ws_down, d->F, d->d, BM)) return MOE_ERR_CUDA;
-    if (!make_map(&p2.b, ws + L.h, d->F, rows, BN)) return MOE_ERR_CUDA;
+    if (!make_map(&p2.b, ws + L.h, d->F, rows, gemm_bn(GEMM_DOWN) / 2)) return MOE_ERR_CUDA;
+    if (!make_map(&p2.b32, ws + L.h, d->F, rows, 32)) return MOE_ERR_CUDA;
+    p2.partial_b = 1;
     p2.cnt = cnt;
     p2.off = off;
     p2.G = E;
@@ -246,16 +256,16 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     p2.shared_rows = static_cast<int32_t>(T);
     p2.shared_b_off = static_cast<int32_t>(T * k);
     p2.M = d->d;
-    p2.MT = (d->d + BM - 1) / BM;
+    p2.MT = (d->d + 2 * BM - 1) / (2 * BM);  // tiles of 256 rows: one CTA pair
     p2.KB = d->F / BK;
     p2.out = ws + L.y;
     p2.out_shared = S ? ws + L.ysh : nullptr;
     p2.ldo = d->d;
     p2.status = status;
     p2.timeout_ns = kWaitTimeoutNs;
-    tb = ntile_bound * p2.MT;
+    tb = ntile_bound(gemm_bn(GEMM_DOWN)) * p2.MT;
     MOE_TRY(mark(MOE_STAGE_DOWN, 0, s));
-    MOE_TRY(cu(launch_grouped_gemm(GEMM_DOWN, p2, static_cast<int>(tb < sms ? tb : sms), s)));
+    MOE_TRY(cu(launch_pair_gemm(GEMM_DOWN, p2, static_cast<int>(tb < pairs ? tb : pairs), s)));
     MOE_TRY(mark(MOE_STAGE_DOWN, 1, s));
 
     MOE_TRY(mark(MOE_STAGE_COMBINE, 0, s));

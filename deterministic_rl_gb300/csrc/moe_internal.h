@@ -7,11 +7,12 @@
 
 namespace moe {
 
-// Tile shape of every tcgen05 GEMM: 128 weight rows (M) x 128 token rows (N)
+// Tile shape of the tcgen05 GEMMs: 128 weight rows (M) x BN token rows (N)
 // x 64 along K per pipeline stage.  One schedule for every group size, so the
 // reduction order of each output element depends on K alone.
 constexpr int BM = 128;
-constexpr int BN = 128;
+constexpr int BN = 128;         // token tile of the router GEMM
+constexpr int BN_EXPERT = 256;  // token tile of the expert (gate/up, down) GEMMs
 constexpr int BK = 64;
 
 // Device status word bits (ws status[0]); status[1] = id of the kernel whose
@@ -21,6 +22,12 @@ constexpr int STATUS_TIMEOUT = 2;
 
 enum GemmMode : int { GEMM_ROUTER = 0, GEMM_SWIGLU = 1, GEMM_DOWN = 2 };
 
+// Token (N) tile of each GEMM; fixed per GEMM, never chosen from the data.
+constexpr int gemm_bn(int mode) { return mode == GEMM_ROUTER ? BN : BN_EXPERT; }
+// Weight rows of one output tile: the gate/up GEMM's 128-row MMA tile holds 64
+// gate rows and the 64 matching up rows.
+constexpr int gemm_rows(int mode) { return mode == GEMM_SWIGLU ? 64 : BM; }
+
 // Grouped GEMM  D[g] = A[g] . B[g]^T  over groups g of token rows.
 // A: weight rows (K-major), B: token rows (K-major), both bf16 via TMA.
 // Routed group g < G has cnt[g] token rows starting at B row off[g] and uses
@@ -29,6 +36,8 @@ enum GemmMode : int { GEMM_ROUTER = 0, GEMM_SWIGLU = 1, GEMM_DOWN = 2 };
 // For the router (cnt == nullptr) there is one group of n_single rows at 0.
 struct GemmParams {
     CUtensorMap a0, a1, as0, as1, b;
+    CUtensorMap b32;    // same tensor as b with a 32-row box (partial token tiles)
+    int32_t partial_b;  // 1: load only the 32-row boxes a tile's tokens occupy
     const int32_t* cnt;
     const int32_t* off;
     int32_t G;
@@ -37,7 +46,7 @@ struct GemmParams {
     int32_t shared_rows;
     int32_t shared_b_off;
     int32_t M;      // weight rows per group
-    int32_t MT;     // ceil(M / BM)
+    int32_t MT;     // ceil(M / gemm_rows(mode))
     int32_t KB;     // K / BK
     void* out;        // router: fp32 logits [T][ldo]; swiglu: bf16 H [rows][ldo]; down: bf16 Y
     void* out_shared; // down: fp32 Ysh [T][ldo]
@@ -50,6 +59,9 @@ struct GemmParams {
 
 size_t gemm_smem_bytes(int mode, int n_groups_total);
 cudaError_t launch_grouped_gemm(int mode, const GemmParams& p, int grid, cudaStream_t s);
+// The expert GEMMs (GEMM_SWIGLU, GEMM_DOWN) on 2-CTA clusters (cta_group::2):
+// `clusters` pairs of SMs; M is split in tiles of 2 * gemm_rows(mode) rows.
+cudaError_t launch_pair_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s);
 
 // Routing: top-k selection (own mode) or replay validation, then gate weights.
 cudaError_t launch_topk_gates(const float* logits, int64_t T, int E, int k,
