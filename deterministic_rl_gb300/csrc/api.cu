@@ -10,6 +10,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -37,7 +38,7 @@ bool dims_ok(const moe_dims* d) {
     if (d->F < 64 || d->F > 16384 || d->F % 64) return false;
     if (d->n_shared < 0 || d->n_shared > 1) return false;
     if (d->wfmt != MOE_W_BF16 && d->wfmt != MOE_W_MXFP8) return false;
-    if (d->wfmt == MOE_W_MXFP8 && (d->d % 128 || d->F % 128)) return false;
+    if (d->wfmt == MOE_W_MXFP8 && (d->d % 512 || d->F % 512)) return false;
     if (d->out_fp32 != 0 && d->out_fp32 != 1) return false;
     return true;
 }
@@ -88,6 +89,21 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint3
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D byte map over [rows][K] (K bytes contiguous), box box_k x box_rows, no
+// swizzle: MXFP8 weight tiles (64-byte boxes) and their E8M0 scales (16-byte).
+bool make_map_u8(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t box_k,
+                 uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {K, rows};
+    const cuuint64_t strides[1] = {K};
+    const cuuint32_t box[2] = {box_k, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -183,6 +199,23 @@ moe_status run_route(const moe_dims* d, const void* x, const moe_weights* w, con
     return mark(MOE_STAGE_TOPK, 1, s);
 }
 
+// Kernel family of the expert GEMMs: the one-SM kernel for batches of at most
+// kOneSmMaxTokens tokens (bf16 weights), SM pairs otherwise.  Both compute each
+// output element with the same MMAs in the same K order.  MOE_EXPERT_KERNEL=
+// one_sm | pair in the environment forces one family (bf16 weights only).
+bool one_sm_experts(const moe_dims* d) {
+    if (d->wfmt != MOE_W_BF16) return false;
+    static const int forced = [] {
+        const char* e = std::getenv("MOE_EXPERT_KERNEL");
+        if (!e) return 0;
+        if (std::strcmp(e, "one_sm") == 0) return 1;
+        if (std::strcmp(e, "pair") == 0) return 2;
+        return 0;
+    }();
+    if (forced) return forced == 1;
+    return d->T <= kOneSmMaxTokens;
+}
+
 // Dispatch, expert FFNs and combine, given ids/gates of every token.
 moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, void* out,
                        const int32_t* ids, const float* gates, uint8_t* ws, const Layout& L,
@@ -205,67 +238,85 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     MOE_TRY(mark(MOE_STAGE_GATHER, 1, s));
     const int sms = num_sms();
     if (sms <= 0) return MOE_ERR_CUDA;
-    auto ntile_bound = [&](int bn) {
-        return (T * k + bn - 1) / bn + E + (S ? (T + bn - 1) / bn : 0);
+
+    const bool mx = d->wfmt == MOE_W_MXFP8;
+    const bool one = one_sm_experts(d);
+    const int bn = one ? BN : BN_EXPERT;                           // tokens per tile
+    const uint32_t box_b = one ? BN : BN_EXPERT / 2;              // token rows per CTA
+    const uint32_t rg = one ? BM : gemm_rows(GEMM_SWIGLU);        // gate (= up) rows per CTA
+    const int tile_g = one ? BM : 2 * gemm_rows(GEMM_SWIGLU);     // gate rows per tile
+    const int tile_d = one ? BM : 2 * BM;                         // down rows per tile
+    const int64_t ntiles = (T * k + bn - 1) / bn + E + (S ? (T + bn - 1) / bn : 0);
+    const int units = one ? sms : sms / 2;                        // CTAs or CTA pairs
+    const uint64_t EF = uint64_t(E) * d->F, ED = uint64_t(E) * d->d;
+
+    auto common = [&](GemmParams& p) {
+        p.cnt = cnt;
+        p.off = off;
+        p.G = E;
+        p.has_shared = S;
+        p.shared_rows = static_cast<int32_t>(T);
+        p.shared_b_off = static_cast<int32_t>(T * k);
+        p.partial_b = 1;
+        p.status = status;
+        p.timeout_ns = kWaitTimeoutNs;
     };
 
     // gate/up projections with the SwiGLU epilogue -> H
     GemmParams p1;
     std::memset(&p1, 0, sizeof p1);
-    const uint32_t r1 = gemm_rows(GEMM_SWIGLU);  // gate rows (and up rows) per tile
-    if (!make_map(&p1.a0, w->w_gate, d->d, uint64_t(E) * d->F, r1)) return MOE_ERR_CUDA;
-    if (!make_map(&p1.a1, w->w_up, d->d, uint64_t(E) * d->F, r1)) return MOE_ERR_CUDA;
-    if (S) {
-        if (!make_map(&p1.as0, w->ws_gate, d->d, d->F, r1)) return MOE_ERR_CUDA;
-        if (!make_map(&p1.as1, w->ws_up, d->d, d->F, r1)) return MOE_ERR_CUDA;
+    common(p1);
+    if (mx) {
+        if (!make_map_u8(&p1.a0, w->w_gate, d->d, EF, BK, rg)) return MOE_ERR_CUDA;
+        if (!make_map_u8(&p1.a1, w->w_up, d->d, EF, BK, rg)) return MOE_ERR_CUDA;
+        if (!make_map_u8(&p1.sa0, w->s_gate, d->d / 32, EF, 16, rg)) return MOE_ERR_CUDA;
+        if (!make_map_u8(&p1.sa1, w->s_up, d->d / 32, EF, 16, rg)) return MOE_ERR_CUDA;
+    } else {
+        if (!make_map(&p1.a0, w->w_gate, d->d, EF, rg)) return MOE_ERR_CUDA;
+        if (!make_map(&p1.a1, w->w_up, d->d, EF, rg)) return MOE_ERR_CUDA;
     }
-    if (!make_map(&p1.b, ws + L.xp, d->d, rows, gemm_bn(GEMM_SWIGLU) / 2)) return MOE_ERR_CUDA;
+    if (S) {
+        if (!make_map(&p1.as0, w->ws_gate, d->d, d->F, rg)) return MOE_ERR_CUDA;
+        if (!make_map(&p1.as1, w->ws_up, d->d, d->F, rg)) return MOE_ERR_CUDA;
+    }
+    if (!make_map(&p1.b, ws + L.xp, d->d, rows, box_b)) return MOE_ERR_CUDA;
     if (!make_map(&p1.b32, ws + L.xp, d->d, rows, 32)) return MOE_ERR_CUDA;
-    p1.partial_b = 1;
-    p1.cnt = cnt;
-    p1.off = off;
-    p1.G = E;
-    p1.has_shared = S;
-    p1.shared_rows = static_cast<int32_t>(T);
-    p1.shared_b_off = static_cast<int32_t>(T * k);
     p1.M = d->F;
-    p1.MT = (d->F + 2 * r1 - 1) / (2 * r1);  // tiles of 2 * r1 rows: one CTA pair
+    p1.MT = (d->F + tile_g - 1) / tile_g;
     p1.KB = d->d / BK;
     p1.out = ws + L.h;
     p1.ldo = d->F;
-    p1.status = status;
-    p1.timeout_ns = kWaitTimeoutNs;
-    int64_t tb = ntile_bound(gemm_bn(GEMM_SWIGLU)) * p1.MT;
-    const int pairs = sms / 2;
+    int64_t tb = ntiles * p1.MT;
+    const int g1 = static_cast<int>(tb < units ? tb : units);
     MOE_TRY(mark(MOE_STAGE_GATE_UP, 0, s));
-    MOE_TRY(cu(launch_pair_gemm(GEMM_SWIGLU, p1, static_cast<int>(tb < pairs ? tb : pairs), s)));
+    MOE_TRY(cu(one ? launch_grouped_gemm(GEMM_SWIGLU, p1, g1, s)
+                   : launch_pair_gemm(GEMM_SWIGLU, p1, g1, s, mx)));
     MOE_TRY(mark(MOE_STAGE_GATE_UP, 1, s));
 
     // down projection -> Y (routed, bf16) and Ysh (shared, fp32)
     GemmParams p2;
     std::memset(&p2, 0, sizeof p2);
-    if (!make_map(&p2.a0, w->w_down, d->F, uint64_t(E) * d->d, BM)) return MOE_ERR_CUDA;
+    common(p2);
+    if (mx) {
+        if (!make_map_u8(&p2.a0, w->w_down, d->F, ED, BK, BM)) return MOE_ERR_CUDA;
+        if (!make_map_u8(&p2.sa0, w->s_down, d->F / 32, ED, 16, BM)) return MOE_ERR_CUDA;
+    } else if (!make_map(&p2.a0, w->w_down, d->F, ED, BM)) {
+        return MOE_ERR_CUDA;
+    }
     if (S && !make_map(&p2.as0, w->ws_down, d->F, d->d, BM)) return MOE_ERR_CUDA;
-    if (!make_map(&p2.b, ws + L.h, d->F, rows, gemm_bn(GEMM_DOWN) / 2)) return MOE_ERR_CUDA;
+    if (!make_map(&p2.b, ws + L.h, d->F, rows, box_b)) return MOE_ERR_CUDA;
     if (!make_map(&p2.b32, ws + L.h, d->F, rows, 32)) return MOE_ERR_CUDA;
-    p2.partial_b = 1;
-    p2.cnt = cnt;
-    p2.off = off;
-    p2.G = E;
-    p2.has_shared = S;
-    p2.shared_rows = static_cast<int32_t>(T);
-    p2.shared_b_off = static_cast<int32_t>(T * k);
     p2.M = d->d;
-    p2.MT = (d->d + 2 * BM - 1) / (2 * BM);  // tiles of 256 rows: one CTA pair
+    p2.MT = (d->d + tile_d - 1) / tile_d;
     p2.KB = d->F / BK;
     p2.out = ws + L.y;
     p2.out_shared = S ? ws + L.ysh : nullptr;
     p2.ldo = d->d;
-    p2.status = status;
-    p2.timeout_ns = kWaitTimeoutNs;
-    tb = ntile_bound(gemm_bn(GEMM_DOWN)) * p2.MT;
+    tb = ntiles * p2.MT;
+    const int g2 = static_cast<int>(tb < units ? tb : units);
     MOE_TRY(mark(MOE_STAGE_DOWN, 0, s));
-    MOE_TRY(cu(launch_pair_gemm(GEMM_DOWN, p2, static_cast<int>(tb < pairs ? tb : pairs), s)));
+    MOE_TRY(cu(one ? launch_grouped_gemm(GEMM_DOWN, p2, g2, s)
+                   : launch_pair_gemm(GEMM_DOWN, p2, g2, s, mx)));
     MOE_TRY(mark(MOE_STAGE_DOWN, 1, s));
 
     MOE_TRY(mark(MOE_STAGE_COMBINE, 0, s));
@@ -285,7 +336,8 @@ moe_status forward_impl(const moe_dims* d, const void* x, const moe_weights* w,
     if (!out || !ids_out || !gates_out || (replay && !ids_in)) return MOE_ERR_ARG;
     if (!al16(out) || !al16(ids_out) || !al16(gates_out) || (replay && !al16(ids_in)))
         return MOE_ERR_ALIGN;
-    if (d->wfmt != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
+    // MXFP8 expert weights: the shared expert (bf16 by definition) is not served.
+    if (d->wfmt == MOE_W_MXFP8 && d->n_shared) return MOE_ERR_UNSUPPORTED;
     const Layout L = make_layout(d);
     auto* s = reinterpret_cast<cudaStream_t>(stream);
     auto* wsb = static_cast<uint8_t*>(ws);

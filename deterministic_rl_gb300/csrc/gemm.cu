@@ -16,11 +16,11 @@
 //   warp 0      TMA producer (one elected lane)
 //   warp 1      TMEM owner + MMA issuer (one elected lane)
 //   warps 2..5  epilogue: TMEM -> registers -> global (lane quarter = warp % 4)
-// Weights are the MMA's M side (128 rows per tile) and tokens the N side, so a
-// weight tile is read once per BN tokens of its expert.  For the gate/up GEMM
-// the 128 weight rows of a tile are 64 gate rows and the 64 matching up rows
-// (two TMA boxes), so one M=128 x N=256 MMA serves both projections; the
-// epilogue pairs each gate lane with its up lane through shared memory.
+// Weights are the MMA's M side (128 rows per tile) and tokens the N side, so
+// a weight tile is read once per 128 tokens of its expert.  This one-SM kernel
+// serves the router and, for small batches, the expert GEMMs (its stages carry
+// 32 KB of gate/up weights, which keeps HBM busy when weights are streamed);
+// gemm_pair.cu serves the expert GEMMs of large batches.
 #include <cuda_bf16.h>
 
 #include "moe_internal.h"
@@ -30,34 +30,29 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 192;
-constexpr uint32_t kABytes = BM * BK * 2;  // 128 weight rows x 64 along K
+constexpr uint32_t kABytes = BM * BK * 2;
+constexpr uint32_t kBBytes = BN * BK * 2;
 constexpr uint32_t kBox32Bytes = 32 * BK * 2;
 constexpr int kMaxGroups = 1024;
-constexpr int kXPad = 33;  // exchange buffer row pitch (floats), avoids bank conflicts
 
 template <int MODE>
 struct Cfg {
-    static constexpr bool kPair = MODE == GEMM_SWIGLU;
-    static constexpr int kRows = gemm_rows(MODE);
-    static constexpr int kBN = gemm_bn(MODE);
-    static constexpr uint32_t kBBytes = kBN * BK * 2;
-    static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-    static constexpr int kStages = kStageBytes > 32768 ? 4 : 6;
-    static constexpr int kAccCols = kBN;
-    static constexpr uint32_t kTmemCols = 2 * kAccCols <= 256 ? 256 : 512;
-    static constexpr uint32_t kIdesc = idesc_bf16_f32(BM, kBN);
-    static constexpr uint32_t kXBytes = kPair ? 2 * 32 * kXPad * 4 : 0;
+    static constexpr bool kDual = MODE == GEMM_SWIGLU;
+    static constexpr int kStages = kDual ? 4 : 6;
+    static constexpr uint32_t kStageBytes = kABytes * (kDual ? 2 : 1) + kBBytes;
+    static constexpr int kAccCols = BN * (kDual ? 2 : 1);
+    static constexpr uint32_t kTmemCols = kDual ? 512 : 256;
 };
+
+constexpr uint32_t kIdesc = idesc_bf16_f32(BM, BN);
 
 struct Tile {
     int m, g, n_valid, brow, arow;
     bool shared;
 };
 
-template <int MODE>
 __device__ __forceinline__ Tile decode_tile(int t, const GemmParams& p, const int* tile_start,
                                             const int* gcnt, const int* goff, int GG) {
-    using C = Cfg<MODE>;
     Tile tl;
     tl.m = t % p.MT;
     const int j = t / p.MT;
@@ -68,10 +63,10 @@ __device__ __forceinline__ Tile decode_tile(int t, const GemmParams& p, const in
     }
     tl.g = lo;
     const int nt = j - tile_start[lo];
-    tl.n_valid = min(C::kBN, gcnt[lo] - nt * C::kBN);
-    tl.brow = goff[lo] + nt * C::kBN;
+    tl.n_valid = min(BN, gcnt[lo] - nt * BN);
+    tl.brow = goff[lo] + nt * BN;
     tl.shared = lo >= p.G;
-    tl.arow = (tl.shared ? 0 : lo * p.M) + tl.m * C::kRows;
+    tl.arow = (tl.shared ? 0 : lo * p.M) + tl.m * BM;
     return tl;
 }
 
@@ -87,15 +82,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    float* xbuf = reinterpret_cast<float*>(smem + C::kStages * C::kStageBytes);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes + C::kXBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
     uint64_t* empty = full + C::kStages;
     uint64_t* tfull = empty + C::kStages;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint64_t* xfull = drain + 1;
-    uint64_t* xempty = xfull + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xempty + 2);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
     const int GG = p.G + p.has_shared;
@@ -121,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             }
             gcnt[g] = c;
             goff[g] = o;
-            local += (c + C::kBN - 1) / C::kBN;
+            local += (c + BN - 1) / BN;
         }
         int incl = local;
 #pragma unroll
@@ -132,7 +124,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         int run = incl - local;
         for (int g = g0; g < min(g0 + per, GG); ++g) {
             tile_start[g] = run;
-            run += (gcnt[g] + C::kBN - 1) / C::kBN;
+            run += (gcnt[g] + BN - 1) / BN;
         }
         if (lane == 31) tile_start[GG] = incl;
     } else if (warp == 1) {
@@ -146,8 +138,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], 4);
-            mbar_init(&xfull[a], 1);
-            mbar_init(&xempty[a], 1);
         }
         mbar_init(drain, 1);
         *abort = 0;
@@ -173,13 +163,13 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             uint32_t issued = 0, last_par = 0;  // per-stage bit masks
             bool ok = true;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile tl = decode_tile<MODE>(t, p, tile_start, gcnt, goff, GG);
+                const Tile tl = decode_tile(t, p, tile_start, gcnt, goff, GG);
                 const CUtensorMap* ma0 = tl.shared ? &p.as0 : &p.a0;
                 const CUtensorMap* ma1 = tl.shared ? &p.as1 : &p.a1;
                 // Token rows: the whole box, or only the 32-row boxes in use.
                 const int nbox = (tl.n_valid + 31) >> 5;
-                const bool part = p.partial_b && nbox < C::kBN / 32;
-                const uint32_t bbytes = part ? nbox * kBox32Bytes : C::kBBytes;
+                const bool part = p.partial_b && nbox < BN / 32;
+                const uint32_t stage_bytes = C::kStageBytes - kBBytes + (part ? nbox * kBox32Bytes : kBBytes);
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort, tmo)) {
                         if (!*abort) raise_timeout(p, abort, 1);
@@ -187,14 +177,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         break;
                     }
                     uint8_t* st = smem + stage * C::kStageBytes;
-                    mbar_arrive_expect_tx(&full[stage], kABytes + bbytes);
-                    if constexpr (C::kPair) {
-                        tma_load_2d(st, ma0, &full[stage], kb * BK, tl.arow, pol_w);
-                        tma_load_2d(st + kABytes / 2, ma1, &full[stage], kb * BK, tl.arow, pol_w);
-                    } else {
-                        tma_load_2d(st, ma0, &full[stage], kb * BK, tl.arow, pol_w);
-                    }
-                    uint8_t* sb = st + kABytes;
+                    mbar_arrive_expect_tx(&full[stage], stage_bytes);
+                    tma_load_2d(st, ma0, &full[stage], kb * BK, tl.arow, pol_w);
+                    if constexpr (C::kDual)
+                        tma_load_2d(st + kABytes, ma1, &full[stage], kb * BK, tl.arow, pol_w);
+                    uint8_t* sb = st + kABytes * (C::kDual ? 2 : 1);
                     if (part) {
                         for (int i = 0; i < nbox; ++i)
                             tma_load_2d(sb + i * kBox32Bytes, &p.b32, &full[stage], kb * BK,
@@ -240,11 +227,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     }
                     tc_fence_after();
                     const uint32_t sa = smem_addr(smem + stage * C::kStageBytes);
-                    const uint32_t sb = sa + kABytes;
+                    const uint32_t sb = sa + kABytes * (C::kDual ? 2 : 1);
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
+                    for (int k = 0; k < BK / 16; ++k) {
+                        const uint32_t accum = (kb | k) != 0;
                         umma_bf16(d0, sdesc_kmajor_sw128(sa + k * 32), sdesc_kmajor_sw128(sb + k * 32),
-                                  C::kIdesc, (kb | k) != 0);
+                                  kIdesc, accum);
+                        if constexpr (C::kDual)
+                            umma_bf16(d0 + BN, sdesc_kmajor_sw128(sa + kABytes + k * 32),
+                                      sdesc_kmajor_sw128(sb + k * 32), kIdesc, accum);
+                    }
                     umma_commit(&empty[stage]);
                     if (++stage == C::kStages) {
                         stage = 0;
@@ -264,15 +256,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         }
     } else {
         // ---------------- epilogue (warps 2..5) ----------------
-        const int q = warp & 3;        // TMEM lane quarter this warp may read
-        const int pr = q & 1;          // gate/up exchange pair (SwiGLU)
-        const bool up_warp = q >= 2;   // SwiGLU: lanes 64..127 hold the up rows
+        const int q = warp & 3;
         int acc = 0;
         uint32_t acc_phase = 0;
-        uint32_t xph = 0;
-        bool ok = true;
-        for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-            const Tile tl = decode_tile<MODE>(t, p, tile_start, gcnt, goff, GG);
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const Tile tl = decode_tile(t, p, tile_start, gcnt, goff, GG);
             // The lanes decide together: tcgen05.ld below needs the whole warp.
             const bool ready = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort, tmo));
             if (!ready) {
@@ -280,51 +268,27 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 break;
             }
             tc_fence_after();
-            // weight row of this lane: expert e (router), f (gate/up), or i (down)
-            const int row = tl.m * C::kRows + (C::kPair ? pr : q) * 32 + lane;
+            const int row = tl.m * BM + q * 32 + lane;  // weight row: e, f or i
             const bool row_ok = row < p.M;
-            const uint32_t taddr =
-                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::kAccCols;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::kAccCols;
             for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
                 float v[32];
                 tmem_ld32(taddr + c0, v);
-                tmem_ld_wait();
                 if constexpr (MODE == GEMM_SWIGLU) {
-                    float* xb = xbuf + pr * 32 * kXPad + lane * kXPad;
-                    if (up_warp) {
-                        if (!__all_sync(0xffffffffu, mbar_wait(&xempty[pr], xph ^ 1u, abort, tmo))) {
-                            if (lane == 0 && !*abort) raise_timeout(p, abort, 7);
-                            ok = false;
-                            break;
-                        }
+                    float u[32];
+                    tmem_ld32(taddr + BN + c0, u);
+                    tmem_ld_wait();
+                    __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) xb[j] = v[j];
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&xfull[pr]);
-                    } else {
-                        if (!__all_sync(0xffffffffu, mbar_wait(&xfull[pr], xph, abort, tmo))) {
-                            if (lane == 0 && !*abort) raise_timeout(p, abort, 8);
-                            ok = false;
-                            break;
-                        }
-                        float u[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) u[j] = xb[j];
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&xempty[pr]);
-                        __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out);
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            if (row_ok && c0 + j < tl.n_valid) {
-                                const float g = v[j];
-                                const float h = g / (1.0f + expf(-g)) * u[j];
-                                H[static_cast<int64_t>(tl.brow + c0 + j) * p.ldo + row] =
-                                    __float2bfloat16_rn(h);
-                            }
+                    for (int j = 0; j < 32; ++j) {
+                        if (row_ok && c0 + j < tl.n_valid) {
+                            const float g = v[j];
+                            const float h = g / (1.0f + expf(-g)) * u[j];
+                            H[static_cast<int64_t>(tl.brow + c0 + j) * p.ldo + row] = __float2bfloat16_rn(h);
                         }
                     }
-                    xph ^= 1u;
                 } else if constexpr (MODE == GEMM_ROUTER) {
+                    tmem_ld_wait();
                     float* L = static_cast<float*>(p.out);
                     const float b = (row_ok && p.bias) ? p.bias[row] : 0.0f;
 #pragma unroll
@@ -332,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                         if (row_ok && c0 + j < tl.n_valid)
                             L[static_cast<int64_t>(tl.brow + c0 + j) * p.ldo + row] = v[j] + b;
                 } else {
+                    tmem_ld_wait();
                     if (tl.shared) {
                         float* Ys = static_cast<float*>(p.out_shared);
                         const int tok0 = tl.brow - p.shared_b_off + c0;
@@ -349,7 +314,6 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     }
                 }
             }
-            if (!ok) break;
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -371,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 template <int MODE>
 size_t smem_bytes_for(int GG) {
     using C = Cfg<MODE>;
-    return 1024 + C::kStages * C::kStageBytes + C::kXBytes + (2 * C::kStages + 9) * 8 + 16 +
+    return 1024 + C::kStages * C::kStageBytes + (2 * C::kStages + 5) * 8 + 16 +
            static_cast<size_t>(3 * GG + 1) * 4;
 }
 

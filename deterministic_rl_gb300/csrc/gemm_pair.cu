@@ -18,6 +18,8 @@
 // completion is multicast to both CTAs' "empty" and "tmem full" barriers; both
 // CTAs' epilogues arrive on the leader's "tmem empty" barrier.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 
 #include "moe_internal.h"
 #include "ptx.cuh"
@@ -25,26 +27,32 @@
 namespace moe {
 namespace {
 
-constexpr int kThreads = 192;
 constexpr int kPairN = BN_EXPERT;                // tokens per pair tile (256)
 constexpr int kHalfN = kPairN / 2;               // token rows held by each CTA
 constexpr uint32_t kABytes = BM * BK * 2;        // 128 weight rows x 64 along K
 constexpr uint32_t kBBytes = kHalfN * BK * 2;    // 128 token rows x 64 along K
 constexpr uint32_t kBox32Bytes = 32 * BK * 2;
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
-constexpr int kStages = 6;
 constexpr int kAccCols = kPairN;
 constexpr uint32_t kTmemCols = 2 * kAccCols;
 constexpr uint32_t kIdesc = idesc_bf16_f32(2 * BM, kPairN);
 constexpr int kXPad = 33;
 constexpr int kMaxGroups = 1024;
 
-template <int MODE>
+// MX: expert weights stored as MXFP8 (E4M3 bytes + one E8M0 scale per 32
+// along K).  Each stage then also holds the CTA's fp8 weight tile and a 16-byte
+// scale box per row (8 k-blocks of scales); four converter warps write the
+// exactly dequantised bf16 tile into the stage's MMA operand buffer.
+template <int MODE, bool MX>
 struct PCfg {
     static constexpr bool kPair = MODE == GEMM_SWIGLU;      // 64 gate + 64 up rows per CTA
     static constexpr int kRowsCta = gemm_rows(MODE);        // output weight rows per CTA
     static constexpr int kRowsTile = 2 * kRowsCta;          // per CTA pair
     static constexpr uint32_t kXBytes = kPair ? 2 * 32 * kXPad * 4 : 0;
+    static constexpr uint32_t kF8Bytes = MX ? BM * BK : 0;  // fp8 weight tile
+    static constexpr uint32_t kScBytes = MX ? BM * 16 : 0;  // scale boxes
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes + kF8Bytes + kScBytes;
+    static constexpr int kStages = MX ? 4 : 6;
+    static constexpr int kThreads = MX ? 320 : 192;
 };
 
 struct Tile {
@@ -69,7 +77,7 @@ __device__ __forceinline__ Tile decode_tile(int t, uint32_t rank, const GemmPara
     tl.n_valid = min(kPairN, gcnt[lo] - nt * kPairN);
     tl.brow = goff[lo] + nt * kPairN;
     tl.shared = lo >= p.G;
-    tl.arow = (tl.shared ? 0 : lo * p.M) + tl.m * PCfg<MODE>::kRowsTile + rank * PCfg<MODE>::kRowsCta;
+    tl.arow = (tl.shared ? 0 : lo * p.M) + tl.m * 2 * gemm_rows(MODE) + rank * gemm_rows(MODE);
     return tl;
 }
 
@@ -87,9 +95,54 @@ __device__ __forceinline__ void raise_timeout(const GemmParams& p, volatile int*
     *abort = 1;
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_constant__ GemmParams p) {
-    using C = PCfg<MODE>;
+// E8M0 scale byte -> 2^(s-127) as fp32 (0xFF is NaN).
+__device__ __forceinline__ float e8m0_scale(uint32_t s) {
+    if (s == 0) return __int_as_float(0x00400000);   // 2^-127, an fp32 subnormal
+    if (s == 255) return __int_as_float(0x7fc00000);
+    return __int_as_float(static_cast<int>(s << 23));
+}
+
+// Two E4M3 values (low byte first) -> two bf16 of value * scale, packed.
+// Exact: E4M3 -> f16 -> f32 are exact, the scale is a power of two, and the
+// product has at most 4 significant bits.
+__device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two, float scale) {
+    const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(two), __NV_E4M3);
+    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&hr));
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// Four E4M3 bytes of one 32-element block (scale byte s) -> four bf16 in two
+// words (element 0 in the low half of `lo`).  Exact.  For normal E4M3 inputs
+// and 7 <= s <= 246 the bf16 pattern is the E4M3 pattern with its exponent
+// re-biased by s - 7 (E4M3 exponent bias 7, bf16 bias 127, scale 2^(s-127)),
+// done with integer operations; zero, subnormal or NaN bytes and extreme
+// scales take the float route above.
+__device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t s, uint32_t& lo,
+                                                 uint32_t& hi) {
+    const uint32_t x7 = w & 0x7F7F7F7Fu;
+    const uint32_t ex = (w >> 3) & 0x0F0F0F0Fu;                       // exponent field per byte
+    const uint32_t zero_exp = (ex - 0x01010101u) & ~ex & 0x80808080u;  // some byte has exponent 0
+    const uint32_t nan = (x7 + 0x01010101u) & 0x80808080u;           // some byte is 0x7F / 0xFF
+    if ((zero_exp | nan) == 0u && s >= 7u && s <= 246u) {
+        const uint32_t a = __byte_perm(w, 0u, 0x4140);  // bytes 0, 1 -> low halves of two shorts
+        const uint32_t b = __byte_perm(w, 0u, 0x4342);  // bytes 2, 3
+        const uint32_t k = ((s - 7u) << 7) * 0x00010001u;
+        lo = (((a << 4) & 0x07F007F0u) + k) | ((a << 8) & 0x80008000u);
+        hi = (((b << 4) & 0x07F007F0u) + k) | ((b << 8) & 0x80008000u);
+    } else {
+        const float scale = e8m0_scale(s);
+        lo = e4m3x2_to_bf16x2(w & 0xFFFFu, scale);
+        hi = e4m3x2_to_bf16x2(w >> 16, scale);
+    }
+}
+
+template <int MODE, bool MX>
+__global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
+    pair_gemm_kernel(const __grid_constant__ GemmParams p) {
+    using C = PCfg<MODE, MX>;
+    constexpr int kStages = C::kStages;
+    constexpr uint32_t kStageBytes = C::kStageBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -101,7 +154,8 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     uint64_t* drain = tempty + 2;
     uint64_t* xfull = drain + 1;
     uint64_t* xempty = xfull + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(xempty + 2);
+    uint64_t* afull = xempty + 2;  // MX: fp8 tile + scales of a stage landed (local)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(afull + kStages);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
     const int GG = p.G + p.has_shared;
@@ -147,8 +201,11 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
         tmem_relinquish_pair();
     } else if (threadIdx.x == 64) {
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
+            // MX: the leader's full barrier also waits for the 4 converter
+            // warps of each CTA.
+            mbar_init(&full[s], MX ? 9 : 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&afull[s], 1);
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -189,7 +246,7 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
                 const int nv = min(max(tl.n_valid - static_cast<int>(rank) * kHalfN, 0), kHalfN);
                 const int nbox = (nv + 31) >> 5;
                 const bool whole = !p.partial_b || nbox == kHalfN / 32;
-                const uint32_t expect = 2 * kABytes + b_bytes(tl.n_valid, 0, p.partial_b) +
+                const uint32_t expect = (MX ? 0 : 2 * kABytes) + b_bytes(tl.n_valid, 0, p.partial_b) +
                                         b_bytes(tl.n_valid, 1, p.partial_b);
                 const int brow = tl.brow + static_cast<int>(rank) * kHalfN;
                 for (int kb = 0; kb < p.KB; ++kb) {
@@ -201,7 +258,23 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
                     uint8_t* st = smem + stage * kStageBytes;
                     if (leader) mbar_arrive_expect_tx(&full[stage], expect);
                     const uint32_t bar = map_to_rank(&full[stage], 0);
-                    if constexpr (C::kPair) {
+                    if constexpr (MX) {
+                        // fp8 tile and its scales into this CTA's staging; the
+                        // converter warps turn them into the bf16 operand.
+                        uint8_t* f8 = st + kABytes + kBBytes;
+                        uint8_t* sc = f8 + C::kF8Bytes;
+                        const int sx = (kb & ~7) * 2;  // 8 k-blocks of scales per box
+                        mbar_arrive_expect_tx(&afull[stage], C::kF8Bytes + C::kScBytes);
+                        if constexpr (C::kPair) {
+                            tma_load_2d(f8, &p.a0, &afull[stage], kb * BK, tl.arow, pol_w);
+                            tma_load_2d(f8 + C::kF8Bytes / 2, &p.a1, &afull[stage], kb * BK, tl.arow, pol_w);
+                            tma_load_2d(sc, &p.sa0, &afull[stage], sx, tl.arow, pol_w);
+                            tma_load_2d(sc + C::kScBytes / 2, &p.sa1, &afull[stage], sx, tl.arow, pol_w);
+                        } else {
+                            tma_load_2d(f8, &p.a0, &afull[stage], kb * BK, tl.arow, pol_w);
+                            tma_load_2d(sc, &p.sa0, &afull[stage], sx, tl.arow, pol_w);
+                        }
+                    } else if constexpr (C::kPair) {
                         tma_load_2d_pair(st, ma0, bar, kb * BK, tl.arow, pol_w);
                         tma_load_2d_pair(st + kABytes / 2, ma1, bar, kb * BK, tl.arow, pol_w);
                     } else {
@@ -275,6 +348,46 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
             }
             umma_commit_pair(drain, 0x1);
             if (!mbar_wait(drain, 0, nullptr, tmo)) raise_timeout(p, abort, 15);
+        }
+    } else if (warp >= 6) {
+        if constexpr (MX) {
+            // ---------------- converters (warps 6..9, both CTAs) ----------------
+            const int ctid = threadIdx.x - 192;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int t = cid; t < total && ok; t += ncl) {
+                for (int kb = 0; kb < p.KB; ++kb) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(&afull[stage], phase, abort, tmo))) {
+                        if (lane == 0 && !*abort) raise_timeout(p, abort, 19);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + stage * kStageBytes;
+                    const uint8_t* f8 = st + kABytes + kBBytes;
+                    const uint8_t* sc = f8 + C::kF8Bytes;
+                    // 128 rows x 8 chunks of 8 values; each chunk becomes one
+                    // 16-byte chunk of the 128-byte-swizzled bf16 row.
+#pragma unroll 2
+                    for (int it = 0; it < 8; ++it) {
+                        const int task = it * 128 + ctid;
+                        const int r = task >> 3, c = task & 7;
+                        const uint2 q = *reinterpret_cast<const uint2*>(f8 + r * 64 + c * 8);
+                        const uint32_t sbyte = sc[r * 16 + (kb & 7) * 2 + (c >> 2)];
+                        uint4 o;
+                        e4m3x4_to_bf16x4(q.x, sbyte, o.x, o.y);
+                        e4m3x4_to_bf16x4(q.y, sbyte, o.z, o.w);
+                        *reinterpret_cast<uint4*>(st + r * 128 + ((c ^ (r & 7)) << 4)) = o;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(map_to_rank(&full[stage], 0));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
         }
     } else {
         // ---------------- epilogue (warps 2..5, both CTAs) ----------------
@@ -375,23 +488,24 @@ __global__ void __launch_bounds__(kThreads, 1) pair_gemm_kernel(const __grid_con
     }
 }
 
-template <int MODE>
+template <int MODE, bool MX>
 size_t pair_smem_bytes(int GG) {
-    return 1024 + kStages * kStageBytes + PCfg<MODE>::kXBytes + (2 * kStages + 9) * 8 + 16 +
+    using C = PCfg<MODE, MX>;
+    return 1024 + C::kStages * C::kStageBytes + C::kXBytes + (3 * C::kStages + 9) * 8 + 16 +
            static_cast<size_t>(3 * GG + 1) * 4;
 }
 
-template <int MODE>
+template <int MODE, bool MX>
 cudaError_t launch_pair_mode(const GemmParams& p, int clusters, cudaStream_t s) {
     const int GG = p.G + p.has_shared;
-    const size_t smem = pair_smem_bytes<MODE>(GG);
-    cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<MODE>,
+    const size_t smem = pair_smem_bytes<MODE, MX>(GG);
+    cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<MODE, MX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(PCfg<MODE, MX>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -404,26 +518,30 @@ cudaError_t launch_pair_mode(const GemmParams& p, int clusters, cudaStream_t s) 
     // Persistent clusters: never more than can be resident at once, so that no
     // cluster's share of the static tile order waits for a second wave.
     int resident = 0;
-    e = cudaOccupancyMaxActiveClusters(&resident, pair_gemm_kernel<MODE>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&resident, pair_gemm_kernel<MODE, MX>, &cfg);
     if (e != cudaSuccess) return e;
     if (resident <= 0) return cudaErrorInvalidConfiguration;
     if (clusters > resident) {
         clusters = resident;
         cfg.gridDim = dim3(2 * clusters, 1, 1);
     }
-    return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<MODE>, p);
+    return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<MODE, MX>, p);
 }
 
 }  // namespace
 
-cudaError_t launch_pair_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s) {
+cudaError_t launch_pair_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s,
+                             int mxfp8) {
     if (p.G + p.has_shared > kMaxGroups || clusters <= 0 || !p.cnt || !p.off)
         return cudaErrorInvalidValue;
-    switch (mode) {
-        case GEMM_SWIGLU: return launch_pair_mode<GEMM_SWIGLU>(p, clusters, s);
-        case GEMM_DOWN: return launch_pair_mode<GEMM_DOWN>(p, clusters, s);
-        default: return cudaErrorInvalidValue;
-    }
+    if (mxfp8 && p.has_shared) return cudaErrorInvalidValue;  // shared expert is bf16
+    if (mode == GEMM_SWIGLU)
+        return mxfp8 ? launch_pair_mode<GEMM_SWIGLU, true>(p, clusters, s)
+                     : launch_pair_mode<GEMM_SWIGLU, false>(p, clusters, s);
+    if (mode == GEMM_DOWN)
+        return mxfp8 ? launch_pair_mode<GEMM_DOWN, true>(p, clusters, s)
+                     : launch_pair_mode<GEMM_DOWN, false>(p, clusters, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace moe

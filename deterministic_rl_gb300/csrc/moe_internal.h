@@ -11,8 +11,12 @@ namespace moe {
 // x 64 along K per pipeline stage.  One schedule for every group size, so the
 // reduction order of each output element depends on K alone.
 constexpr int BM = 128;
-constexpr int BN = 128;         // token tile of the router GEMM
-constexpr int BN_EXPERT = 256;  // token tile of the expert (gate/up, down) GEMMs
+constexpr int BN = 128;         // token tile of the one-SM GEMM (gemm.cu)
+constexpr int BN_EXPERT = 256;  // token tile of the SM-pair expert GEMMs (gemm_pair.cu)
+// Batches of at most this many tokens run the expert GEMMs on the one-SM kernel
+// (weight streaming); larger ones on SM pairs.  Both kernels compute every
+// output element with the same bf16 MMAs in the same K order (tested bitwise).
+constexpr int64_t kOneSmMaxTokens = 128;
 constexpr int BK = 64;
 
 // Device status word bits (ws status[0]); status[1] = id of the kernel whose
@@ -22,11 +26,9 @@ constexpr int STATUS_TIMEOUT = 2;
 
 enum GemmMode : int { GEMM_ROUTER = 0, GEMM_SWIGLU = 1, GEMM_DOWN = 2 };
 
-// Token (N) tile of each GEMM; fixed per GEMM, never chosen from the data.
-constexpr int gemm_bn(int mode) { return mode == GEMM_ROUTER ? BN : BN_EXPERT; }
-// Weight rows of one output tile: the gate/up GEMM's 128-row MMA tile holds 64
-// gate rows and the 64 matching up rows.
-constexpr int gemm_rows(int mode) { return mode == GEMM_SWIGLU ? 64 : BM; }
+// Weight rows per CTA of an SM-pair tile: the gate/up GEMM's 128-row MMA half
+// holds 64 gate rows and the 64 matching up rows.
+__host__ __device__ constexpr int gemm_rows(int mode) { return mode == GEMM_SWIGLU ? 64 : BM; }
 
 // Grouped GEMM  D[g] = A[g] . B[g]^T  over groups g of token rows.
 // A: weight rows (K-major), B: token rows (K-major), both bf16 via TMA.
@@ -52,7 +54,7 @@ struct GemmParams {
     void* out_shared; // down: fp32 Ysh [T][ldo]
     int32_t ldo;
     const float* bias;  // router only
-    const uint8_t* sa0; // MXFP8 scales (unused by the bf16 kernels)
+    CUtensorMap sa0, sa1;  // MXFP8: E8M0 scale maps matching a0, a1 (16-byte boxes)
     int32_t* status;
     uint64_t timeout_ns;
 };
@@ -61,7 +63,10 @@ size_t gemm_smem_bytes(int mode, int n_groups_total);
 cudaError_t launch_grouped_gemm(int mode, const GemmParams& p, int grid, cudaStream_t s);
 // The expert GEMMs (GEMM_SWIGLU, GEMM_DOWN) on 2-CTA clusters (cta_group::2):
 // `clusters` pairs of SMs; M is split in tiles of 2 * gemm_rows(mode) rows.
-cudaError_t launch_pair_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s);
+// mxfp8 != 0: a0/a1 are E4M3 weight maps (64-byte boxes) with scale maps
+// sa0/sa1; the kernel dequantises them exactly to bf16 in shared memory.
+cudaError_t launch_pair_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s,
+                             int mxfp8 = 0);
 
 // Routing: top-k selection (own mode) or replay validation, then gate weights.
 cudaError_t launch_topk_gates(const float* logits, int64_t T, int E, int k,

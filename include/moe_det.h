@@ -43,8 +43,9 @@
  *     batch or on T.  Expert outputs of a token are added in ascending slot
  *     order, then the shared expert, with fp32 accumulation ([TD], [CH]).
  *   - Limits of this version.  k == 8; 8 <= E <= 512; d and F multiples of
- *     64 (and of 128 for MXFP8 weights), 64 <= d, F <= 16384; n_shared in
- *     {0, 1}; 1 <= T <= 2^20 (T == 0 is a no-op that returns MOE_OK).
+ *     64 (and of 512 for MXFP8 weights), 64 <= d, F <= 16384; n_shared in
+ *     {0, 1} (0 with MXFP8 weights: MOE_ERR_UNSUPPORTED otherwise);
+ *     1 <= T <= 2^20 (T == 0 is a no-op that returns MOE_OK).
  *     Device pointers must be 16-byte aligned.
  */
 #ifndef MOE_DET_H

@@ -133,3 +133,46 @@ def check_out(gpu_out32: np.ndarray, ref: np.ndarray):
 
 def bf16_of(t32: torch.Tensor) -> torch.Tensor:
     return t32.to(torch.bfloat16)
+
+
+def make_near_ties(inp, frac: float, seed: int, margin: float = 1e-4):
+    """Adversarial near-tie tokens (workload 5): for a seeded `frac` of the
+    tokens, nudge single bf16 coordinates of x until the 8th and 9th largest
+    router logits (exact arithmetic on the stored bf16 values) are within
+    `margin`.  Returns the modified x (device bf16), the chosen token indices,
+    and a fresh perturbed copy of x for recording replay ids.  Input
+    construction only; the layer's own arithmetic is not involved."""
+    k = inp.cfg.k
+    T = inp.x.shape[0]
+    rng = np.random.default_rng(seed)
+    idx = np.sort(rng.choice(T, int(round(frac * T)), replace=False))
+    wr = torch.from_numpy(bf16_bits(inp.w_router).view(np.int16)).view(torch.bfloat16).double().numpy()
+    bias = 0.0 if inp.router_bias is None else inp.router_bias.double().cpu().numpy()
+    xs = inp.x[torch.as_tensor(idx, device=inp.x.device)].double().cpu().numpy()
+    done = 0
+    for n in range(len(idx)):
+        x = xs[n]
+        for _ in range(12):
+            lg = wr @ x + bias
+            order = np.argsort(-lg, kind="stable")
+            a, b = order[k - 1], order[k]
+            gap = lg[a] - lg[b]
+            if gap < margin:
+                done += 1
+                break
+            c = wr[a] - wr[b]
+            cand = np.argsort(-np.abs(c))[:256]
+            target = x[cand] - gap / c[cand]
+            new = torch.from_numpy(target).to(torch.bfloat16).double().numpy()
+            resid = np.abs(gap + (new - x[cand]) * c[cand])
+            resid[np.abs(new) > 4.0] = np.inf
+            j = cand[int(np.argmin(resid))]
+            x[j] = torch.tensor(float(new[cand.tolist().index(j)])).to(torch.bfloat16).double().item()
+        xs[n] = x
+    x_new = inp.x.clone()
+    x_new[torch.as_tensor(idx, device=inp.x.device)] = torch.from_numpy(xs).to(
+        device=inp.x.device, dtype=torch.float32).to(torch.bfloat16)
+    g = torch.Generator(device=inp.x.device).manual_seed(seed + 7)
+    noise = torch.randn(x_new.shape, generator=g, device=inp.x.device) * inp.cfg.replay_noise
+    x_rep = (x_new.float() + noise).to(torch.bfloat16)
+    return x_new, idx, x_rep, done
