@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--mode", choices=["replay", "own"], default="replay")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (small captures for the profiler)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override the token count (small captures for the profiler)")
     ap.add_argument("--cpu-sample", type=int, default=64,
                     help="tokens of the workload the CPU-baseline oracle runs on")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -266,6 +268,8 @@ def run_reference(args):
     cfg = CONFIGS[args.config]
     if args.experts:
         cfg = cfg.with_(name=f"{cfg.name}_E{args.experts}", E=args.experts)
+    if args.tokens:
+        cfg = cfg.with_(name=f"{cfg.name}_T{args.tokens}", T=args.tokens)
     oracle.build()
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = make_layer(cfg, dev)  # same seeded bytes as the GPU arm
@@ -307,6 +311,8 @@ def run_ours(args):
     cfg = CONFIGS[args.config]
     if args.experts:
         cfg = cfg.with_(name=f"{cfg.name}_E{args.experts}", E=args.experts)
+    if args.tokens:
+        cfg = cfg.with_(name=f"{cfg.name}_T{args.tokens}", T=args.tokens)
     # weak scaling: every rank runs its own batch (seed offset by rank)
     inp = make_layer(cfg.with_(seed=cfg.seed + 1000 * rank) if rank else cfg, "cuda")
     layer = MoELayer.from_inputs(inp)

@@ -39,20 +39,32 @@ constexpr int kXPad = 33;
 constexpr int kMaxGroups = 1024;
 
 // MX: expert weights stored as MXFP8 (E4M3 bytes + one E8M0 scale per 32
-// along K).  Each stage then also holds the CTA's fp8 weight tile and a 16-byte
-// scale box per row (8 k-blocks of scales); four converter warps write the
-// exactly dequantised bf16 tile into the stage's MMA operand buffer.
+// along K).  A dedicated producer warp (warp 14) streams the CTA's fp8 weight
+// tiles into their own ring, far ahead, and a 16-byte scale box per row every
+// 8 k-blocks into a small scale ring; eight converter warps (6..13) each
+// convert whole k-blocks (warp w takes k-blocks w, w+8, ...) into the operand
+// ring's A buffer, so several k-blocks are converted at once and HBM latency
+// never sits between a conversion and its MMA.
 template <int MODE, bool MX>
 struct PCfg {
     static constexpr bool kPair = MODE == GEMM_SWIGLU;      // 64 gate + 64 up rows per CTA
     static constexpr int kRowsCta = gemm_rows(MODE);        // output weight rows per CTA
     static constexpr int kRowsTile = 2 * kRowsCta;          // per CTA pair
     static constexpr uint32_t kXBytes = kPair ? 2 * 32 * kXPad * 4 : 0;
-    static constexpr uint32_t kF8Bytes = MX ? BM * BK : 0;  // fp8 weight tile
-    static constexpr uint32_t kScBytes = MX ? BM * 16 : 0;  // scale boxes
-    static constexpr uint32_t kStageBytes = kABytes + kBBytes + kF8Bytes + kScBytes;
-    static constexpr int kStages = MX ? 4 : 6;
-    static constexpr int kThreads = MX ? 320 : 192;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;  // operand ring entry
+    static constexpr int kStages = MX ? 5 : 6;
+    static constexpr uint32_t kF8Bytes = BM * BK;               // fp8 weight tile
+    static constexpr int kF8Stages = MX ? 5 : 0;
+    static constexpr uint32_t kScBytes = BM * 16;               // 8 k-blocks of scales
+    static constexpr int kScStages = MX ? 2 : 0;
+    static constexpr uint32_t kRingBytes =
+        kStages * kStageBytes + kF8Stages * kF8Bytes + kScStages * kScBytes;
+    static constexpr int kBarriers = 2 * kStages + 2 * kF8Stages + 2 * kScStages + 9;
+    static constexpr int kConvWarps = 8;
+    static constexpr int kConvPerKb = 2;                        // warps per k-block
+    static constexpr int kConvGroups = kConvWarps / kConvPerKb;  // k-blocks in flight
+    static constexpr int kThreads = MX ? 192 + 32 * kConvWarps + 32 : 192;
+    static constexpr int kFp8Warp = 6 + kConvWarps;
 };
 
 struct Tile {
@@ -137,6 +149,20 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t s, uint32_
     }
 }
 
+// Branch-free parts of e4m3x4_to_bf16x4: the re-biased patterns (valid when
+// the flag below is 0) and the flag "some byte is zero, subnormal or NaN".
+__device__ __forceinline__ uint32_t e4m3x4_special(uint32_t w) {
+    const uint32_t ex = (w >> 3) & 0x0F0F0F0Fu;
+    return ((ex - 0x01010101u) & ~ex & 0x80808080u) | (((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u);
+}
+
+__device__ __forceinline__ void e4m3x4_rebias(uint32_t w, uint32_t k, uint32_t& lo, uint32_t& hi) {
+    const uint32_t a = __byte_perm(w, 0u, 0x4140);
+    const uint32_t b = __byte_perm(w, 0u, 0x4342);
+    lo = (((a << 4) & 0x07F007F0u) + k) | ((a << 8) & 0x80008000u);
+    hi = (((b << 4) & 0x07F007F0u) + k) | ((b << 8) & 0x80008000u);
+}
+
 template <int MODE, bool MX>
 __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
     pair_gemm_kernel(const __grid_constant__ GemmParams p) {
@@ -146,16 +172,21 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    float* xbuf = reinterpret_cast<float*>(smem + kStages * kStageBytes);
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes + C::kXBytes);
+    uint8_t* f8ring = smem + kStages * kStageBytes;
+    uint8_t* scring = f8ring + C::kF8Stages * C::kF8Bytes;
+    float* xbuf = reinterpret_cast<float*>(smem + C::kRingBytes);
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kRingBytes + C::kXBytes);
     uint64_t* empty = full + kStages;
     uint64_t* tfull = empty + kStages;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
     uint64_t* xfull = drain + 1;
     uint64_t* xempty = xfull + 2;
-    uint64_t* afull = xempty + 2;  // MX: fp8 tile + scales of a stage landed (local)
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(afull + kStages);
+    uint64_t* f8full = xempty + 2;             // MX, local: fp8 tile landed
+    uint64_t* f8empty = f8full + C::kF8Stages;  // MX, local: converters done with it
+    uint64_t* scfull = f8empty + C::kF8Stages;
+    uint64_t* scempty = scfull + C::kScStages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + C::kBarriers);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
     const int GG = p.G + p.has_shared;
@@ -203,9 +234,17 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
         for (int s = 0; s < kStages; ++s) {
             // MX: the leader's full barrier also waits for the 4 converter
             // warps of each CTA.
-            mbar_init(&full[s], MX ? 9 : 1);
+            // MX: + the converter warps of one k-block in each CTA
+            mbar_init(&full[s], MX ? 1 + 2 * C::kConvPerKb : 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&afull[s], 1);
+        }
+        for (int s = 0; s < C::kF8Stages; ++s) {
+            mbar_init(&f8full[s], 1);
+            mbar_init(&f8empty[s], C::kConvPerKb);
+        }
+        for (int s = 0; s < C::kScStages; ++s) {
+            mbar_init(&scfull[s], 1);
+            mbar_init(&scempty[s], 8 * C::kConvPerKb);  // 8 k-blocks per scale box
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
@@ -259,21 +298,7 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                     if (leader) mbar_arrive_expect_tx(&full[stage], expect);
                     const uint32_t bar = map_to_rank(&full[stage], 0);
                     if constexpr (MX) {
-                        // fp8 tile and its scales into this CTA's staging; the
-                        // converter warps turn them into the bf16 operand.
-                        uint8_t* f8 = st + kABytes + kBBytes;
-                        uint8_t* sc = f8 + C::kF8Bytes;
-                        const int sx = (kb & ~7) * 2;  // 8 k-blocks of scales per box
-                        mbar_arrive_expect_tx(&afull[stage], C::kF8Bytes + C::kScBytes);
-                        if constexpr (C::kPair) {
-                            tma_load_2d(f8, &p.a0, &afull[stage], kb * BK, tl.arow, pol_w);
-                            tma_load_2d(f8 + C::kF8Bytes / 2, &p.a1, &afull[stage], kb * BK, tl.arow, pol_w);
-                            tma_load_2d(sc, &p.sa0, &afull[stage], sx, tl.arow, pol_w);
-                            tma_load_2d(sc + C::kScBytes / 2, &p.sa1, &afull[stage], sx, tl.arow, pol_w);
-                        } else {
-                            tma_load_2d(f8, &p.a0, &afull[stage], kb * BK, tl.arow, pol_w);
-                            tma_load_2d(sc, &p.sa0, &afull[stage], sx, tl.arow, pol_w);
-                        }
+                        // the A operand comes from the converter warps
                     } else if constexpr (C::kPair) {
                         tma_load_2d_pair(st, ma0, bar, kb * BK, tl.arow, pol_w);
                         tma_load_2d_pair(st + kABytes / 2, ma1, bar, kb * BK, tl.arow, pol_w);
@@ -349,43 +374,143 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
             umma_commit_pair(drain, 0x1);
             if (!mbar_wait(drain, 0, nullptr, tmo)) raise_timeout(p, abort, 15);
         }
+    } else if (warp == C::kFp8Warp) {
+        if constexpr (MX) {
+            if (lane == 0) {
+                // ---------------- fp8 weight producer (both CTAs) ----------------
+                const uint64_t pol_w = l2_policy_evict_first();
+                int fs = 0, ss = 0;
+                uint32_t fph = 0, sph = 0;
+                uint32_t f_issued = 0, f_par = 0, s_issued = 0, s_par = 0;
+                bool ok = true;
+                for (int t = cid; t < total && ok; t += ncl) {
+                    const Tile tl = decode_tile<MODE>(t, rank, p, tile_start, gcnt, goff, GG);
+                    for (int kb = 0; kb < p.KB; ++kb) {
+                        if ((kb & 7) == 0) {  // scales of the next 8 k-blocks
+                            if (!mbar_wait(&scempty[ss], sph ^ 1u, abort, tmo)) {
+                                if (!*abort) raise_timeout(p, abort, 20);
+                                ok = false;
+                                break;
+                            }
+                            uint8_t* sc = scring + ss * C::kScBytes;
+                            mbar_arrive_expect_tx(&scfull[ss], C::kScBytes);
+                            if constexpr (C::kPair) {
+                                tma_load_2d(sc, &p.sa0, &scfull[ss], kb * 2, tl.arow, pol_w);
+                                tma_load_2d(sc + C::kScBytes / 2, &p.sa1, &scfull[ss], kb * 2, tl.arow, pol_w);
+                            } else {
+                                tma_load_2d(sc, &p.sa0, &scfull[ss], kb * 2, tl.arow, pol_w);
+                            }
+                            s_issued |= 1u << ss;
+                            s_par = (s_par & ~(1u << ss)) | (sph << ss);
+                            if (++ss == C::kScStages) {
+                                ss = 0;
+                                sph ^= 1u;
+                            }
+                        }
+                        if (!mbar_wait(&f8empty[fs], fph ^ 1u, abort, tmo)) {
+                            if (!*abort) raise_timeout(p, abort, 21);
+                            ok = false;
+                            break;
+                        }
+                        uint8_t* f8 = f8ring + fs * C::kF8Bytes;
+                        mbar_arrive_expect_tx(&f8full[fs], C::kF8Bytes);
+                        if constexpr (C::kPair) {
+                            tma_load_2d(f8, &p.a0, &f8full[fs], kb * BK, tl.arow, pol_w);
+                            tma_load_2d(f8 + C::kF8Bytes / 2, &p.a1, &f8full[fs], kb * BK, tl.arow, pol_w);
+                        } else {
+                            tma_load_2d(f8, &p.a0, &f8full[fs], kb * BK, tl.arow, pol_w);
+                        }
+                        f_issued |= 1u << fs;
+                        f_par = (f_par & ~(1u << fs)) | (fph << fs);
+                        if (++fs == C::kF8Stages) {
+                            fs = 0;
+                            fph ^= 1u;
+                        }
+                    }
+                }
+                for (int s2 = 0; s2 < C::kF8Stages; ++s2)
+                    if (f_issued & (1u << s2))
+                        if (!mbar_wait(&f8full[s2], (f_par >> s2) & 1u, nullptr, tmo))
+                            raise_timeout(p, abort, 22);
+                for (int s2 = 0; s2 < C::kScStages; ++s2)
+                    if (s_issued & (1u << s2))
+                        if (!mbar_wait(&scfull[s2], (s_par >> s2) & 1u, nullptr, tmo))
+                            raise_timeout(p, abort, 23);
+            }
+        }
     } else if (warp >= 6) {
         if constexpr (MX) {
-            // ---------------- converters (warps 6..9, both CTAs) ----------------
-            const int ctid = threadIdx.x - 192;
-            int stage = 0;
-            uint32_t phase = 0;
-            bool ok = true;
-            for (int t = cid; t < total && ok; t += ncl) {
-                for (int kb = 0; kb < p.KB; ++kb) {
-                    if (!__all_sync(0xffffffffu, mbar_wait(&afull[stage], phase, abort, tmo))) {
-                        if (lane == 0 && !*abort) raise_timeout(p, abort, 19);
-                        ok = false;
-                        break;
+            // ---------------- converters (warps 6..13, both CTAs) ----------------
+            // kConvGroups groups of kConvPerKb warps; group g converts this CTA's
+            // k-blocks i = g, g + kConvGroups, ... of the tile sequence, warp j
+            // of the group rows [j * 128 / kConvPerKb, ...).  A tile has KB
+            // k-blocks with KB % 8 == 0, so scale groups never straddle tiles.
+            // Phase safety of the parity waits below: a group's previous k-block
+            // i - G (G = kConvGroups) needed MMA(i - G - kStages) and the loads of
+            // k-block i - G and of its scale group; with G <= kStages,
+            // G <= kF8Stages and G <= 8 this proves that every slot a wait of
+            // k-block i looks at is at most one phase behind the awaited one.
+            static_assert(C::kConvGroups <= C::kStages && C::kConvGroups <= C::kF8Stages &&
+                              C::kConvGroups <= 8,
+                          "converter groups must not outrun the rings");
+            const int grp_w = (warp - 6) / C::kConvPerKb;
+            const int sub = (warp - 6) % C::kConvPerKb;
+            constexpr int kRowsPerWarp = BM / C::kConvPerKb;
+            const int my_tiles = cid < total ? (total - cid + ncl - 1) / ncl : 0;
+            const int64_t n_kb = static_cast<int64_t>(my_tiles) * p.KB;
+            auto wait_all = [&](uint64_t* bar, uint32_t par, int where) {
+                if (__all_sync(0xffffffffu, mbar_wait(bar, par, abort, tmo))) return true;
+                if (lane == 0 && !*abort) raise_timeout(p, abort, where);
+                return false;
+            };
+            for (int64_t i = grp_w; i < n_kb; i += C::kConvGroups) {
+                const int os = static_cast<int>(i % kStages);
+                const uint32_t oph = static_cast<uint32_t>((i / kStages) & 1);
+                const int fs = static_cast<int>(i % C::kF8Stages);
+                const uint32_t fph = static_cast<uint32_t>((i / C::kF8Stages) & 1);
+                const int64_t grp = i >> 3;
+                const int ss = static_cast<int>(grp % C::kScStages);
+                const uint32_t sph = static_cast<uint32_t>((grp / C::kScStages) & 1);
+                if (!wait_all(&scfull[ss], sph, 24) || !wait_all(&f8full[fs], fph, 25) ||
+                    !wait_all(&empty[os], oph ^ 1u, 26))
+                    break;
+                uint8_t* st = smem + os * kStageBytes;
+                const uint8_t* f8 = f8ring + fs * C::kF8Bytes;
+                const uint8_t* sc = scring + ss * C::kScBytes;
+                const int kb8 = static_cast<int>(i & 7);
+                // 128 rows x 4 tasks of 16 values (one scale each); a task
+                // becomes two 16-byte chunks of the 128-byte-swizzled row.
+#pragma unroll 4
+                for (int it = 0; it < (kRowsPerWarp * 4) / 32; ++it) {
+                    const int task = sub * kRowsPerWarp * 4 + it * 32 + lane;
+                    const int r = task >> 2, c2 = (task & 3) * 2;
+                    const uint4 q = *reinterpret_cast<const uint4*>(f8 + r * 64 + c2 * 8);
+                    const uint32_t sbyte = sc[r * 16 + kb8 * 2 + (c2 >> 2)];
+                    uint4 o0, o1;
+                    const uint32_t kk = ((sbyte - 7u) << 7) * 0x00010001u;
+                    e4m3x4_rebias(q.x, kk, o0.x, o0.y);
+                    e4m3x4_rebias(q.y, kk, o0.z, o0.w);
+                    e4m3x4_rebias(q.z, kk, o1.x, o1.y);
+                    e4m3x4_rebias(q.w, kk, o1.z, o1.w);
+                    const uint32_t special = e4m3x4_special(q.x) | e4m3x4_special(q.y) |
+                                             e4m3x4_special(q.z) | e4m3x4_special(q.w) |
+                                             (sbyte < 7u || sbyte > 246u);
+                    if (special) {  // rare: exact float route for all 16 values
+                        e4m3x4_to_bf16x4(q.x, sbyte, o0.x, o0.y);
+                        e4m3x4_to_bf16x4(q.y, sbyte, o0.z, o0.w);
+                        e4m3x4_to_bf16x4(q.z, sbyte, o1.x, o1.y);
+                        e4m3x4_to_bf16x4(q.w, sbyte, o1.z, o1.w);
                     }
-                    uint8_t* st = smem + stage * kStageBytes;
-                    const uint8_t* f8 = st + kABytes + kBBytes;
-                    const uint8_t* sc = f8 + C::kF8Bytes;
-                    // 128 rows x 8 chunks of 8 values; each chunk becomes one
-                    // 16-byte chunk of the 128-byte-swizzled bf16 row.
-#pragma unroll 2
-                    for (int it = 0; it < 8; ++it) {
-                        const int task = it * 128 + ctid;
-                        const int r = task >> 3, c = task & 7;
-                        const uint2 q = *reinterpret_cast<const uint2*>(f8 + r * 64 + c * 8);
-                        const uint32_t sbyte = sc[r * 16 + (kb & 7) * 2 + (c >> 2)];
-                        uint4 o;
-                        e4m3x4_to_bf16x4(q.x, sbyte, o.x, o.y);
-                        e4m3x4_to_bf16x4(q.y, sbyte, o.z, o.w);
-                        *reinterpret_cast<uint4*>(st + r * 128 + ((c ^ (r & 7)) << 4)) = o;
-                    }
-                    fence_proxy_async_smem();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive_cluster(map_to_rank(&full[stage], 0));
-                    if (++stage == kStages) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                    uint8_t* row = st + r * 128;
+                    *reinterpret_cast<uint4*>(row + ((c2 ^ (r & 7)) << 4)) = o0;
+                    *reinterpret_cast<uint4*>(row + (((c2 + 1) ^ (r & 7)) << 4)) = o1;
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive(&f8empty[fs]);
+                    mbar_arrive(&scempty[ss]);
+                    mbar_arrive_cluster(map_to_rank(&full[os], 0));
                 }
             }
         }
@@ -491,7 +616,7 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
 template <int MODE, bool MX>
 size_t pair_smem_bytes(int GG) {
     using C = PCfg<MODE, MX>;
-    return 1024 + C::kStages * C::kStageBytes + C::kXBytes + (3 * C::kStages + 9) * 8 + 16 +
+    return 1024 + C::kRingBytes + C::kXBytes + C::kBarriers * 8 + 16 +
            static_cast<size_t>(3 * GG + 1) * 4;
 }
 
