@@ -70,14 +70,16 @@ struct PCfg {
 struct Tile {
     int m, g, n_valid, brow, arow;
     bool shared;
+    bool reused;  // the expert has several token tiles: its weight tiles are read again
 };
 
 template <int MODE>
 __device__ __forceinline__ Tile decode_tile(int t, uint32_t rank, const GemmParams& p,
                                             const int* tile_start, const int* gcnt,
                                             const int* goff, int GG) {
+    // Within an expert the token tiles vary fastest, so all token tiles of a
+    // weight tile run back to back (on neighbouring clusters) and share it in L2.
     Tile tl;
-    tl.m = t % p.MT;
     const int j = t / p.MT;
     int lo = 0, hi = GG;
     while (hi - lo > 1) {
@@ -85,7 +87,11 @@ __device__ __forceinline__ Tile decode_tile(int t, uint32_t rank, const GemmPara
         if (tile_start[mid] <= j) lo = mid; else hi = mid;
     }
     tl.g = lo;
-    const int nt = j - tile_start[lo];
+    const int ntg = tile_start[lo + 1] - tile_start[lo];
+    const int l = t - tile_start[lo] * p.MT;
+    tl.m = l / ntg;
+    const int nt = l - tl.m * ntg;
+    tl.reused = ntg > 1;
     tl.n_valid = min(kPairN, gcnt[lo] - nt * kPairN);
     tl.brow = goff[lo] + nt * kPairN;
     tl.shared = lo >= p.G;
@@ -272,7 +278,8 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
             tma_prefetch_desc(&p.a0);
             tma_prefetch_desc(&p.b);
             if (p.has_shared) tma_prefetch_desc(&p.as0);
-            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_once = l2_policy_evict_first();
+            const uint64_t pol_again = l2_policy_evict_normal();
             const uint64_t pol_x = l2_policy_evict_last();
             int stage = 0;
             uint32_t phase = 0;
@@ -280,6 +287,7 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
             bool ok = true;
             for (int t = cid; t < total && ok; t += ncl) {
                 const Tile tl = decode_tile<MODE>(t, rank, p, tile_start, gcnt, goff, GG);
+                const uint64_t pol_w = tl.reused ? pol_again : pol_once;
                 const CUtensorMap* ma0 = tl.shared ? &p.as0 : &p.a0;
                 const CUtensorMap* ma1 = tl.shared ? &p.as1 : &p.a1;
                 const int nv = min(max(tl.n_valid - static_cast<int>(rank) * kHalfN, 0), kHalfN);
@@ -378,13 +386,15 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
         if constexpr (MX) {
             if (lane == 0) {
                 // ---------------- fp8 weight producer (both CTAs) ----------------
-                const uint64_t pol_w = l2_policy_evict_first();
+                const uint64_t pol_once = l2_policy_evict_first();
+                const uint64_t pol_again = l2_policy_evict_normal();
                 int fs = 0, ss = 0;
                 uint32_t fph = 0, sph = 0;
                 uint32_t f_issued = 0, f_par = 0, s_issued = 0, s_par = 0;
                 bool ok = true;
                 for (int t = cid; t < total && ok; t += ncl) {
                     const Tile tl = decode_tile<MODE>(t, rank, p, tile_start, gcnt, goff, GG);
+                    const uint64_t pol_w = tl.reused ? pol_again : pol_once;
                     for (int kb = 0; kb < p.KB; ++kb) {
                         if ((kb & 7) == 0) {  // scales of the next 8 k-blocks
                             if (!mbar_wait(&scempty[ss], sph ^ 1u, abort, tmo)) {
