@@ -9,6 +9,7 @@
 // moe_get_status.
 #include <cudaTypedefs.h>
 
+#include <atomic>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -216,6 +217,21 @@ bool one_sm_experts(const moe_dims* d) {
     return d->T <= kOneSmMaxTokens;
 }
 
+// Test hook for failure detection: MOE_TEST_STALL_CALLS=N makes the gate/up
+// GEMM of the next N forward calls (process-wide) issue no loads, so its MMA
+// wait runs out (bounded, 1 s) and the call reports MOE_ERR_TIMEOUT through
+// moe_get_status.  Unset in normal use.
+bool take_stall_test() {
+    static std::atomic<int> left{[] {
+        const char* e = std::getenv("MOE_TEST_STALL_CALLS");
+        return e ? std::atoi(e) : 0;
+    }()};
+    int v = left.load();
+    while (v > 0)
+        if (left.compare_exchange_weak(v, v - 1)) return true;
+    return false;
+}
+
 // Dispatch, expert FFNs and combine, given ids/gates of every token.
 moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, void* out,
                        const int32_t* ids, const float* gates, uint8_t* ws, const Layout& L,
@@ -286,6 +302,7 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     p1.KB = d->d / BK;
     p1.out = ws + L.h;
     p1.ldo = d->F;
+    p1.stall_test = take_stall_test() ? 1 : 0;
     int64_t tb = ntiles * p1.MT;
     const int g1 = static_cast<int>(tb < units ? tb : units);
     MOE_TRY(mark(MOE_STAGE_GATE_UP, 0, s));

@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, last_par = 0;  // per-stage bit masks
-            bool ok = true;
+            bool ok = p.stall_test == 0;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
                 const Tile tl = decode_tile(t, p, tile_start, gcnt, goff, GG);
                 const CUtensorMap* ma0 = tl.shared ? &p.as0 : &p.a0;

@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
             int stage = 0;
             uint32_t phase = 0;
             uint32_t issued = 0, last_par = 0;
-            bool ok = true;
+            bool ok = p.stall_test == 0;
             for (int t = cid; t < total && ok; t += ncl) {
                 const Tile tl = decode_tile<MODE>(t, rank, p, tile_start, gcnt, goff, GG);
                 const uint64_t pol_w = tl.reused ? pol_again : pol_once;
@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                 int fs = 0, ss = 0;
                 uint32_t fph = 0, sph = 0;
                 uint32_t f_issued = 0, f_par = 0, s_issued = 0, s_par = 0;
-                bool ok = true;
+                bool ok = p.stall_test == 0;
                 for (int t = cid; t < total && ok; t += ncl) {
                     const Tile tl = decode_tile<MODE>(t, rank, p, tile_start, gcnt, goff, GG);
                     const uint64_t pol_w = tl.reused ? pol_again : pol_once;

@@ -57,6 +57,7 @@ struct GemmParams {
     CUtensorMap sa0, sa1;  // MXFP8: E8M0 scale maps matching a0, a1 (16-byte boxes)
     int32_t* status;
     uint64_t timeout_ns;
+    int32_t stall_test;  // test hook: the producers issue nothing, so waits run out
 };
 
 size_t gemm_smem_bytes(int mode, int n_groups_total);
