@@ -23,12 +23,18 @@ using namespace moe;
 namespace {
 
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // bounded device waits: 1 s
+// The router GEMM splits K into this many fixed parts (when d/64 divides by it),
+// summed in a fixed order by the top-k kernel: more CTAs stream the router
+// weights at small T, and the split does not depend on T.
+constexpr int kRouterSplit = 4;
 
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-    size_t status, logits, valid, cnt, off, perm, inv, scratch, xp, h, y, ysh, total;
+    size_t status, logits, rpart, valid, cnt, off, perm, inv, scratch, xp, h, y, ysh, total;
 };
+
+inline int router_split(const moe_dims* d) { return (d->d / BK) % kRouterSplit == 0 ? kRouterSplit : 1; }
 
 bool dims_ok(const moe_dims* d) {
     if (!d) return false;
@@ -52,6 +58,7 @@ Layout make_layout(const moe_dims* d) {
     auto take = [&](size_t bytes) { const size_t at = o; o = align256(o + bytes); return at; };
     L.status = take(16);
     L.logits = take(T * E * 4);
+    L.rpart = take(router_split(d) > 1 ? T * E * 4 * router_split(d) : 0);
     L.valid = take(T * 4);
     L.cnt = take(E * 4);
     L.off = take((E + 1) * 4);
@@ -176,17 +183,20 @@ moe_status run_route(const moe_dims* d, const void* x, const moe_weights* w, con
     if (!make_map(&p.b, x, d->d, T, BN)) return MOE_ERR_CUDA;
     if (!make_map(&p.b32, x, d->d, T, 32)) return MOE_ERR_CUDA;
     p.partial_b = 1;
+    const int split = router_split(d);
+    p.ksplit = split;
+    p.split_stride = T * d->E;
     p.G = 1;
     p.n_single = static_cast<int32_t>(T);
     p.M = d->E;
     p.MT = (d->E + BM - 1) / BM;
     p.KB = d->d / BK;
-    p.out = ws + L.logits;
+    p.out = ws + (split > 1 ? L.rpart : L.logits);
     p.ldo = d->E;
-    p.bias = w->router_bias;
+    p.bias = split > 1 ? nullptr : w->router_bias;
     p.status = status;
     p.timeout_ns = kWaitTimeoutNs;
-    const int64_t tiles = int64_t(p.MT) * ((T + BN - 1) / BN);
+    const int64_t tiles = int64_t(p.MT) * ((T + BN - 1) / BN) * split;
     const int sms = num_sms();
     if (sms <= 0) return MOE_ERR_CUDA;
     const int grid = static_cast<int>(tiles < sms ? tiles : sms);
@@ -194,9 +204,16 @@ moe_status run_route(const moe_dims* d, const void* x, const moe_weights* w, con
     MOE_TRY(cu(launch_grouped_gemm(GEMM_ROUTER, p, grid, s)));
     MOE_TRY(mark(MOE_STAGE_ROUTER_GEMM, 1, s));
     MOE_TRY(mark(MOE_STAGE_TOPK, 0, s));
-    MOE_TRY(cu(launch_topk_gates(reinterpret_cast<const float*>(ws + L.logits), T, d->E, d->k,
-                                 ids_in, ids_out, gates_out,
-                                 reinterpret_cast<int32_t*>(ws + L.valid), status, s)));
+    if (split > 1)
+        MOE_TRY(cu(launch_topk_gates_split(reinterpret_cast<const float*>(ws + L.rpart), split,
+                                           T * d->E, w->router_bias,
+                                           reinterpret_cast<float*>(ws + L.logits), T, d->E, d->k,
+                                           ids_in, ids_out, gates_out,
+                                           reinterpret_cast<int32_t*>(ws + L.valid), status, s)));
+    else
+        MOE_TRY(cu(launch_topk_gates(reinterpret_cast<const float*>(ws + L.logits), T, d->E, d->k,
+                                     ids_in, ids_out, gates_out,
+                                     reinterpret_cast<int32_t*>(ws + L.valid), status, s)));
     return mark(MOE_STAGE_TOPK, 1, s);
 }
 

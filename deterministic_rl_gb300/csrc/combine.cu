@@ -33,6 +33,7 @@ template <bool OUT_F32, bool SHARED>
 __global__ void __launch_bounds__(kThreads) combine_kernel(
     const uint4* __restrict__ y, const float4* __restrict__ ysh, const int32_t* __restrict__ inv,
     const float* __restrict__ gates, const int32_t* __restrict__ valid, int k, int d, void* out) {
+    // block (t, c): token t, 8-element vectors [c * kThreads, (c + 1) * kThreads)
     const int64_t t = blockIdx.x;
     const int vec = d / 8;
     int32_t rows[kMaxK];
@@ -43,7 +44,9 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(
         g[s] = s < k ? gates[t * k + s] : 0.0f;
     }
     const bool ok = valid[t] != 0;
-    for (int v = threadIdx.x; v < vec; v += kThreads) {
+    {
+        const int v = blockIdx.y * kThreads + threadIdx.x;
+        if (v >= vec) return;
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
@@ -88,7 +91,7 @@ cudaError_t launch_combine(const uint16_t* y, const float* ysh, const int32_t* i
     if (k > kMaxK || d % 8) return cudaErrorInvalidValue;
     const auto* yv = reinterpret_cast<const uint4*>(y);
     const auto* sv = reinterpret_cast<const float4*>(ysh);
-    const unsigned grid = static_cast<unsigned>(T);
+    const dim3 grid(static_cast<unsigned>(T), static_cast<unsigned>((d / 8 + kThreads - 1) / kThreads));
     if (out_fp32) {
         if (ysh) combine_kernel<true, true><<<grid, kThreads, 0, s>>>(yv, sv, inv, gates, valid, k, d, out);
         else combine_kernel<true, false><<<grid, kThreads, 0, s>>>(yv, sv, inv, gates, valid, k, d, out);

@@ -112,6 +112,82 @@ __global__ void __launch_bounds__(32 * kSegWarps) seg_scatter_kernel(
     }
 }
 
+// All three passes in one CTA, for at most one segment of pairs (n <= 4096):
+// the decode-sized case, where three launches would cost more than the work.
+__global__ void __launch_bounds__(32 * kSegWarps) dispatch_small_kernel(
+    const int32_t* __restrict__ ids, int64_t n, int E, int32_t* __restrict__ cnt,
+    int32_t* __restrict__ off, int32_t* __restrict__ perm, int32_t* __restrict__ inv) {
+    __shared__ int32_t h[kSegWarps][kMaxE];
+    __shared__ int32_t warp_tot[kSegWarps];
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < kSegWarps * kMaxE; i += blockDim.x) (&h[0][0])[i] = 0;
+    __syncthreads();
+    const int64_t base = static_cast<int64_t>(w) * kWarpPairs;
+    for (int r = 0; r < kWarpPairs; r += 32) {  // per-warp histograms
+        const int64_t i = base + r + lane;
+        const bool in = i < n;
+        const int key = in ? ids[i] : -1;
+        const uint32_t act = __ballot_sync(0xffffffffu, in);
+        if (in) {
+            const uint32_t peers = __match_any_sync(act, key);
+            if ((__ffs(peers) - 1) == lane) h[w][key] += __popc(peers);
+        }
+        __syncwarp();
+    }
+    __syncthreads();
+    // exclusive scan over experts: thread handles experts 2*tid, 2*tid + 1
+    const int e0 = 2 * threadIdx.x;
+    int32_t c0 = 0, c1 = 0;
+    for (int ww = 0; ww < kSegWarps; ++ww) {
+        if (e0 < E) c0 += h[ww][e0];
+        if (e0 + 1 < E) c1 += h[ww][e0 + 1];
+    }
+    int32_t incl = c0 + c1;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+        const int32_t v = __shfl_up_sync(0xffffffffu, incl, s);
+        if (lane >= s) incl += v;
+    }
+    if (lane == 31) warp_tot[w] = incl;
+    __syncthreads();
+    int32_t wbase = 0;
+    for (int ww = 0; ww < w; ++ww) wbase += warp_tot[ww];
+    const int32_t ex0 = wbase + incl - c0 - c1;
+    const int32_t ex1 = ex0 + c0;
+    __syncthreads();
+    // per (warp, expert) start positions, in place of the histograms
+    for (int j = 0; j < 2; ++j) {
+        const int e = e0 + j;
+        if (e >= E) continue;
+        int32_t run = j ? ex1 : ex0;
+        cnt[e] = j ? c1 : c0;
+        off[e] = run;
+        if (e == E - 1) off[E] = run + (j ? c1 : c0);
+        for (int ww = 0; ww < kSegWarps; ++ww) {
+            const int32_t c = h[ww][e];
+            h[ww][e] = run;
+            run += c;
+        }
+    }
+    __syncthreads();
+    for (int r = 0; r < kWarpPairs; r += 32) {  // in-order ranks
+        const int64_t i = base + r + lane;
+        const bool in = i < n;
+        const int key = in ? ids[i] : -1;
+        const uint32_t act = __ballot_sync(0xffffffffu, in);
+        if (in) {
+            const uint32_t peers = __match_any_sync(act, key);
+            const int rank = __popc(peers & ((1u << lane) - 1u));
+            const int32_t dst = h[w][key] + rank;
+            perm[dst] = static_cast<int32_t>(i);
+            inv[i] = dst;
+            __syncwarp(act);
+            if ((__ffs(peers) - 1) == lane) h[w][key] += __popc(peers);
+        }
+        __syncwarp();
+    }
+}
+
 // Gather: xp[r] = x[perm[r] / k] for r < T*k, then xp[T*k + t] = x[t] for
 // the shared expert.  16-byte vectors; d % 8 == 0.
 __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
@@ -138,6 +214,10 @@ cudaError_t launch_dispatch(const int32_t* ids, int64_t T, int k, int E, int32_t
     if (E > kMaxE) return cudaErrorInvalidValue;
     const int64_t n = T * k;
     const int nseg = static_cast<int>((n + kSegPairs - 1) / kSegPairs);
+    if (nseg == 1) {
+        dispatch_small_kernel<<<1, 32 * kSegWarps, 0, s>>>(ids, n, E, cnt, off, perm, inv);
+        return cudaGetLastError();
+    }
     if (nseg > 0) {
         seg_hist_kernel<<<nseg, 32 * kSegWarps, 0, s>>>(ids, n, E, scratch);
         cudaError_t e = cudaGetLastError();

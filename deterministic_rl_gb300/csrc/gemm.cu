@@ -147,7 +147,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = tile_start[GG] * p.MT;
+    // Fixed K split (router): tile t covers K part t % S of output tile t / S.
+    const int S = p.ksplit > 1 ? p.ksplit : 1;
+    const int KBs = p.KB / S;
+    const int total = tile_start[GG] * p.MT * S;
     const uint64_t tmo = p.timeout_ns;
 
     if (warp == 0) {
@@ -163,14 +166,15 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             uint32_t issued = 0, last_par = 0;  // per-stage bit masks
             bool ok = p.stall_test == 0;
             for (int t = blockIdx.x; t < total && ok; t += gridDim.x) {
-                const Tile tl = decode_tile(t, p, tile_start, gcnt, goff, GG);
+                const Tile tl = decode_tile(t / S, p, tile_start, gcnt, goff, GG);
+                const int kb0 = (t % S) * KBs;
                 const CUtensorMap* ma0 = tl.shared ? &p.as0 : &p.a0;
                 const CUtensorMap* ma1 = tl.shared ? &p.as1 : &p.a1;
                 // Token rows: the whole box, or only the 32-row boxes in use.
                 const int nbox = (tl.n_valid + 31) >> 5;
                 const bool part = p.partial_b && nbox < BN / 32;
                 const uint32_t stage_bytes = C::kStageBytes - kBBytes + (part ? nbox * kBox32Bytes : kBBytes);
-                for (int kb = 0; kb < p.KB; ++kb) {
+                for (int kb = kb0; kb < kb0 + KBs; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort, tmo)) {
                         if (!*abort) raise_timeout(p, abort, 1);
                         ok = false;
@@ -219,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                 }
                 tc_fence_after();
                 const uint32_t d0 = tmem_base + acc * C::kAccCols;
-                for (int kb = 0; kb < p.KB; ++kb) {
+                for (int kb = 0; kb < KBs; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort, tmo)) {
                         if (!*abort) raise_timeout(p, abort, 4);
                         ok = false;
@@ -260,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const Tile tl = decode_tile(t, p, tile_start, gcnt, goff, GG);
+            const Tile tl = decode_tile(t / S, p, tile_start, gcnt, goff, GG);
             // The lanes decide together: tcgen05.ld below needs the whole warp.
             const bool ready = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort, tmo));
             if (!ready) {
@@ -289,7 +293,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     }
                 } else if constexpr (MODE == GEMM_ROUTER) {
                     tmem_ld_wait();
-                    float* L = static_cast<float*>(p.out);
+                    float* L = static_cast<float*>(p.out) + (t % S) * p.split_stride;
                     const float b = (row_ok && p.bias) ? p.bias[row] : 0.0f;
 #pragma unroll
                     for (int j = 0; j < 32; ++j)

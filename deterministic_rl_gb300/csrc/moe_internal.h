@@ -58,6 +58,9 @@ struct GemmParams {
     int32_t* status;
     uint64_t timeout_ns;
     int32_t stall_test;  // test hook: the producers issue nothing, so waits run out
+    int32_t ksplit;      // one-SM kernel: K split into this many fixed parts (0/1: none);
+                         // part s goes to out + s * split_stride (no bias)
+    int64_t split_stride;
 };
 
 size_t gemm_smem_bytes(int mode, int n_groups_total);
@@ -73,6 +76,13 @@ cudaError_t launch_pair_gemm(int mode, const GemmParams& p, int clusters, cudaSt
 cudaError_t launch_topk_gates(const float* logits, int64_t T, int E, int k,
                               const int32_t* ids_in, int32_t* ids_out, float* gates_out,
                               int32_t* valid, int32_t* status, cudaStream_t s);
+// Same, from nsplit partial logits (part s at parts + s * stride, summed in
+// order s = 0, 1, ..., then + bias); the final logits are stored to logits_out.
+cudaError_t launch_topk_gates_split(const float* parts, int nsplit, int64_t stride,
+                                    const float* bias, float* logits_out, int64_t T, int E,
+                                    int k, const int32_t* ids_in, int32_t* ids_out,
+                                    float* gates_out, int32_t* valid, int32_t* status,
+                                    cudaStream_t s);
 
 // Dispatch: stable counting sort of the T*k pairs by expert, then the gather
 // of token rows into expert order (plus the shared-expert copy of x).

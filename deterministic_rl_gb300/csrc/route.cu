@@ -26,14 +26,32 @@ __device__ __forceinline__ bool before(float va, int ea, float vb, int eb) {
     return va > vb || (va == vb && ea < eb);
 }
 
+// Logits of a token either come finished (logits) or as nsplit partial sums
+// over fixed K ranges (parts), added in order s = 0, 1, ... then + bias, and
+// stored to logits_out.
 template <int J>  // logits per lane: E <= 32 * J
 __global__ void __launch_bounds__(32 * kWarpsPerBlock) topk_gates_kernel(
-    const float* __restrict__ logits, int64_t T, int E, int k, const int32_t* __restrict__ ids_in,
-    int32_t* __restrict__ ids_out, float* __restrict__ gates_out, int32_t* __restrict__ valid,
-    int32_t* __restrict__ status) {
+    const float* logits, const float* __restrict__ parts, int nsplit, int64_t stride,
+    const float* __restrict__ bias, float* logits_out, int64_t T, int E, int k,
+    const int32_t* __restrict__ ids_in, int32_t* __restrict__ ids_out,
+    float* __restrict__ gates_out, int32_t* __restrict__ valid, int32_t* __restrict__ status) {
     const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
     if (t >= T) return;
+    if (parts) {
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int e = lane + 32 * j;
+            if (e < E) {
+                float acc = parts[t * E + e];
+                for (int s = 1; s < nsplit; ++s) acc += parts[s * stride + t * E + e];
+                if (bias) acc += bias[e];
+                logits_out[t * E + e] = acc;
+            }
+        }
+        __syncwarp();
+        logits = logits_out;
+    }
     const float* l = logits + t * E;
 
     int sel[kMaxK];
@@ -119,14 +137,39 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) topk_gates_kernel(
     if (lane == 0) valid[t] = ok ? 1 : 0;
 }
 
+struct TopkArgs {
+    const float* logits;
+    const float* parts;
+    int nsplit;
+    int64_t stride;
+    const float* bias;
+    float* logits_out;
+    int64_t T;
+    int E, k;
+    const int32_t* ids_in;
+    int32_t* ids_out;
+    float* gates_out;
+    int32_t* valid;
+    int32_t* status;
+};
+
 template <int J>
-cudaError_t launch_j(const float* logits, int64_t T, int E, int k, const int32_t* ids_in,
-                     int32_t* ids_out, float* gates_out, int32_t* valid, int32_t* status,
-                     cudaStream_t s) {
-    const int64_t blocks = (T + kWarpsPerBlock - 1) / kWarpsPerBlock;
+cudaError_t launch_j(const TopkArgs& a, cudaStream_t s) {
+    const int64_t blocks = (a.T + kWarpsPerBlock - 1) / kWarpsPerBlock;
     topk_gates_kernel<J><<<static_cast<unsigned>(blocks), 32 * kWarpsPerBlock, 0, s>>>(
-        logits, T, E, k, ids_in, ids_out, gates_out, valid, status);
+        a.logits, a.parts, a.nsplit, a.stride, a.bias, a.logits_out, a.T, a.E, a.k, a.ids_in,
+        a.ids_out, a.gates_out, a.valid, a.status);
     return cudaGetLastError();
+}
+
+cudaError_t launch_any(const TopkArgs& a, cudaStream_t s) {
+    if (a.k < 1 || a.k > kMaxK || a.E < a.k || a.E > 512) return cudaErrorInvalidValue;
+    if (a.T == 0) return cudaSuccess;
+    if (a.E <= 64) return launch_j<2>(a, s);
+    if (a.E <= 128) return launch_j<4>(a, s);
+    if (a.E <= 256) return launch_j<8>(a, s);
+    if (a.E <= 384) return launch_j<12>(a, s);
+    return launch_j<16>(a, s);
 }
 
 }  // namespace
@@ -134,12 +177,20 @@ cudaError_t launch_j(const float* logits, int64_t T, int E, int k, const int32_t
 cudaError_t launch_topk_gates(const float* logits, int64_t T, int E, int k,
                               const int32_t* ids_in, int32_t* ids_out, float* gates_out,
                               int32_t* valid, int32_t* status, cudaStream_t s) {
-    if (k < 1 || k > kMaxK || E < k || E > 512) return cudaErrorInvalidValue;
-    if (E <= 64) return launch_j<2>(logits, T, E, k, ids_in, ids_out, gates_out, valid, status, s);
-    if (E <= 128) return launch_j<4>(logits, T, E, k, ids_in, ids_out, gates_out, valid, status, s);
-    if (E <= 256) return launch_j<8>(logits, T, E, k, ids_in, ids_out, gates_out, valid, status, s);
-    if (E <= 384) return launch_j<12>(logits, T, E, k, ids_in, ids_out, gates_out, valid, status, s);
-    return launch_j<16>(logits, T, E, k, ids_in, ids_out, gates_out, valid, status, s);
+    const TopkArgs a{logits, nullptr, 1, 0, nullptr, nullptr, T, E, k, ids_in, ids_out,
+                     gates_out, valid, status};
+    return launch_any(a, s);
+}
+
+cudaError_t launch_topk_gates_split(const float* parts, int nsplit, int64_t stride,
+                                    const float* bias, float* logits_out, int64_t T, int E,
+                                    int k, const int32_t* ids_in, int32_t* ids_out,
+                                    float* gates_out, int32_t* valid, int32_t* status,
+                                    cudaStream_t s) {
+    if (!parts || !logits_out || nsplit < 1) return cudaErrorInvalidValue;
+    const TopkArgs a{logits_out, parts, nsplit, stride, bias, logits_out, T, E, k, ids_in,
+                     ids_out, gates_out, valid, status};
+    return launch_any(a, s);
 }
 
 }  // namespace moe

@@ -68,7 +68,8 @@ def test_replay_matches_oracle(cfg):
     mc.check_out(out32.cpu().numpy(), ref.out)
 
 
-@pytest.mark.parametrize("cfg", CASES[:3], ids=lambda c: c.name)
+@pytest.mark.parametrize("cfg", CASES[:3] + [small_cfg(1000, E=40), small_cfg(3000, E=384, d=256)],
+                         ids=lambda c: c.name)
 def test_dispatch_is_the_oracle_counting_sort(cfg):
     inp = make_layer(cfg, "cuda")
     layer = MoELayer.from_inputs(inp, out_fp32=True)
@@ -80,10 +81,12 @@ def test_dispatch_is_the_oracle_counting_sort(cfg):
     assert np.array_equal(im["off"].cpu().numpy(), off)
     assert np.array_equal(im["perm"].cpu().numpy(), perm)
     assert np.array_equal(im["inv"].cpu().numpy(), inv)
-    # gathered rows are the tokens' hidden states in expert order
-    xp = im["xp"]
-    src = torch.from_numpy(perm // cfg.k).long().cuda()
-    assert torch.equal(xp[: cfg.T * cfg.k], inp.x[src])
+    # gathered rows are the tokens' hidden states in expert order (rows are
+    # gathered into the workspace for batches of at most 128 tokens)
+    if cfg.T <= 128:
+        xp = im["xp"]
+        src = torch.from_numpy(perm // cfg.k).long().cuda()
+        assert torch.equal(xp[: cfg.T * cfg.k], inp.x[src])
 
 
 def test_replay_of_own_ids_is_bitwise_own():
