@@ -33,7 +33,7 @@ MOE_W_MXFP8 = 1
 # Every function the header declares, in declaration order.
 EXPORTED = ("moe_workspace_size", "moe_workspace_layout", "moe_route", "moe_forward",
             "moe_forward_replay", "moe_get_status", "moe_status_str", "moe_set_stage_events",
-            "moe_route_static")
+            "moe_route_static", "moe_forward_replay_filtered")
 
 STAGES = ("router_gemm", "topk", "dispatch", "gather", "gate_up", "down", "combine")
 
@@ -93,6 +93,9 @@ def load(path: str = LIB_PATH):
     lib.moe_status_str.argtypes = [ctypes.c_int]
     lib.moe_set_stage_events.restype = ctypes.c_int
     lib.moe_set_stage_events.argtypes = [ctypes.c_void_p]
+    lib.moe_forward_replay_filtered.restype = ctypes.c_int
+    lib.moe_forward_replay_filtered.argtypes = [D, P, W, P, ctypes.c_float, P, P, P, P,
+                                                ctypes.c_size_t, P]
     lib.moe_route_static.restype = ctypes.c_int
     lib.moe_route_static.argtypes = [D, P, W, P, P, P]
     _lib = lib
@@ -204,4 +207,15 @@ def moe_route_static(dims: Dims, x, weights: moe_weights, ids_out, gates_out, st
                                  _p(ids_out), _p(gates_out), _stream(stream))
     if check and rc != MOE_OK:
         raise MoEError(rc, "moe_route_static")
+    return rc
+
+
+def moe_forward_replay_filtered(dims: Dims, x, weights: moe_weights, ids_in, tau: float, out,
+                                ids_out, gates_out, ws, stream=None, check: bool = True) -> int:
+    rc = load().moe_forward_replay_filtered(ctypes.byref(dims.c()), _p(x), ctypes.byref(weights),
+                                            _p(ids_in), float(tau), _p(out), _p(ids_out),
+                                            _p(gates_out), _p(ws), ws.numel() * ws.element_size(),
+                                            _stream(stream))
+    if check and rc != MOE_OK:
+        raise MoEError(rc, "moe_forward_replay_filtered")
     return rc

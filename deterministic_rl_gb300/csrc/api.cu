@@ -10,6 +10,7 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -173,7 +174,7 @@ namespace {
 // Router logits (fp32, + bias) and the routing decision for every token.
 moe_status run_route(const moe_dims* d, const void* x, const moe_weights* w, const int32_t* ids_in,
                      int32_t* ids_out, float* gates_out, uint8_t* ws, const Layout& L,
-                     cudaStream_t s) {
+                     cudaStream_t s, bool filter = false, float tau = 0.0f) {
     const int64_t T = d->T;
     int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
     MOE_TRY(cu(cudaMemsetAsync(status, 0, 16, s)));
@@ -204,12 +205,14 @@ moe_status run_route(const moe_dims* d, const void* x, const moe_weights* w, con
     MOE_TRY(cu(launch_grouped_gemm(GEMM_ROUTER, p, grid, s)));
     MOE_TRY(mark(MOE_STAGE_ROUTER_GEMM, 1, s));
     MOE_TRY(mark(MOE_STAGE_TOPK, 0, s));
-    if (split > 1)
+    const float log_tau = tau > 0.0f ? std::log(tau) : -INFINITY;
+    if (split > 1 || filter)
         MOE_TRY(cu(launch_topk_gates_split(reinterpret_cast<const float*>(ws + L.rpart), split,
-                                           T * d->E, w->router_bias,
+                                           T * d->E, split > 1 ? w->router_bias : nullptr,
                                            reinterpret_cast<float*>(ws + L.logits), T, d->E, d->k,
                                            ids_in, ids_out, gates_out,
-                                           reinterpret_cast<int32_t*>(ws + L.valid), status, s)));
+                                           reinterpret_cast<int32_t*>(ws + L.valid), status, s,
+                                           filter ? 1 : 0, log_tau)));
     else
         MOE_TRY(cu(launch_topk_gates(reinterpret_cast<const float*>(ws + L.logits), T, d->E, d->k,
                                      ids_in, ids_out, gates_out,
@@ -363,7 +366,8 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
 
 moe_status forward_impl(const moe_dims* d, const void* x, const moe_weights* w,
                         const int32_t* ids_in, bool replay, void* out, int32_t* ids_out,
-                        float* gates_out, void* ws, size_t ws_bytes, moe_stream_t stream) {
+                        float* gates_out, void* ws, size_t ws_bytes, moe_stream_t stream,
+                        bool filter = false, float tau = 0.0f) {
     MOE_TRY(check_common(d, x, w, ws, ws_bytes));
     if (d->T == 0) return MOE_OK;
     MOE_TRY(check_experts(d, w));
@@ -375,7 +379,8 @@ moe_status forward_impl(const moe_dims* d, const void* x, const moe_weights* w,
     const Layout L = make_layout(d);
     auto* s = reinterpret_cast<cudaStream_t>(stream);
     auto* wsb = static_cast<uint8_t*>(ws);
-    MOE_TRY(run_route(d, x, w, replay ? ids_in : nullptr, ids_out, gates_out, wsb, L, s));
+    MOE_TRY(run_route(d, x, w, replay ? ids_in : nullptr, ids_out, gates_out, wsb, L, s, filter,
+                      tau));
     return run_experts(d, x, w, out, ids_out, gates_out, wsb, L, s);
 }
 
@@ -428,6 +433,15 @@ moe_status moe_forward_replay(const moe_dims* dims, const void* x, const moe_wei
                               const int32_t* ids_in, void* out, int32_t* ids_out, float* gates_out,
                               void* ws, size_t ws_bytes, moe_stream_t stream) {
     return forward_impl(dims, x, w, ids_in, true, out, ids_out, gates_out, ws, ws_bytes, stream);
+}
+
+moe_status moe_forward_replay_filtered(const moe_dims* dims, const void* x, const moe_weights* w,
+                                       const int32_t* ids_in, float tau, void* out,
+                                       int32_t* ids_out, float* gates_out, void* ws,
+                                       size_t ws_bytes, moe_stream_t stream) {
+    if (!(tau >= 0.0f && tau <= 1.0f)) return MOE_ERR_ARG;  // also rejects NaN
+    return forward_impl(dims, x, w, ids_in, true, out, ids_out, gates_out, ws, ws_bytes, stream,
+                        true, tau);
 }
 
 moe_status moe_get_status(const void* ws, moe_stream_t stream) {

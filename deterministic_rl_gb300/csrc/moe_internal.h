@@ -77,12 +77,15 @@ cudaError_t launch_topk_gates(const float* logits, int64_t T, int E, int k,
                               const int32_t* ids_in, int32_t* ids_out, float* gates_out,
                               int32_t* valid, int32_t* status, cudaStream_t s);
 // Same, from nsplit partial logits (part s at parts + s * stride, summed in
-// order s = 0, 1, ..., then + bias); the final logits are stored to logits_out.
+// order s = 0, 1, ..., then + bias; the final logits are stored to logits_out),
+// or, with nsplit == 1, from the finished logits in logits_out.  filter != 0
+// (replay only) applies the replay plausibility filter with threshold
+// ln(tau) = log_tau below the router's own k-th logit.
 cudaError_t launch_topk_gates_split(const float* parts, int nsplit, int64_t stride,
                                     const float* bias, float* logits_out, int64_t T, int E,
                                     int k, const int32_t* ids_in, int32_t* ids_out,
                                     float* gates_out, int32_t* valid, int32_t* status,
-                                    cudaStream_t s);
+                                    cudaStream_t s, int filter = 0, float log_tau = 0.0f);
 
 // Dispatch: stable counting sort of the T*k pairs by expert, then the gather
 // of token rows into expert order (plus the shared-expert copy of x).

@@ -26,6 +26,41 @@ __device__ __forceinline__ bool before(float va, int ea, float vb, int eb) {
     return va > vb || (va == vb && ea < eb);
 }
 
+// The k largest of the lane-distributed logits v (lane + 32 j), descending,
+// equal logits to the lower expert id: warp-shuffle arg-max, k rounds.
+template <int J>
+__device__ __forceinline__ void warp_topk(const float (&v)[J], int E, int k, int lane,
+                                          int (&sel)[kMaxK], float (&sl)[kMaxK]) {
+    uint32_t taken = 0;
+#pragma unroll
+    for (int s = 0; s < kMaxK; ++s) {
+        if (s >= k) break;
+        float bv = -FLT_MAX;
+        int be = INT_MAX;
+#pragma unroll
+        for (int j = 0; j < J; ++j) {
+            const int e = lane + 32 * j;
+            if (e < E && !(taken >> j & 1u) && before(v[j], e, bv, be)) {
+                bv = v[j];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+            if (before(ov, oe, bv, be)) {
+                bv = ov;
+                be = oe;
+            }
+        }
+        if (be == INT_MAX) be = 0;  // only if every remaining logit is NaN
+        sel[s] = be;
+        sl[s] = bv;
+        if ((be & 31) == lane) taken |= 1u << (be >> 5);
+    }
+}
+
 // Logits of a token either come finished (logits) or as nsplit partial sums
 // over fixed K ranges (parts), added in order s = 0, 1, ... then + bias, and
 // stored to logits_out.
@@ -34,7 +69,8 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) topk_gates_kernel(
     const float* logits, const float* __restrict__ parts, int nsplit, int64_t stride,
     const float* __restrict__ bias, float* logits_out, int64_t T, int E, int k,
     const int32_t* __restrict__ ids_in, int32_t* __restrict__ ids_out,
-    float* __restrict__ gates_out, int32_t* __restrict__ valid, int32_t* __restrict__ status) {
+    float* __restrict__ gates_out, int32_t* __restrict__ valid, int32_t* __restrict__ status,
+    int filter, float log_tau) {
     const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -57,41 +93,16 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) topk_gates_kernel(
     int sel[kMaxK];
     float sl[kMaxK];
     bool ok = true;
-    if (ids_in == nullptr) {
-        float v[J];
+    float v[J];
+    if (ids_in == nullptr || filter) {
 #pragma unroll
         for (int j = 0; j < J; ++j) {
             const int e = lane + 32 * j;
             v[j] = e < E ? l[e] : -FLT_MAX;
         }
-        uint32_t taken = 0;
-#pragma unroll
-        for (int s = 0; s < kMaxK; ++s) {
-            if (s >= k) break;
-            float bv = -FLT_MAX;
-            int be = INT_MAX;
-#pragma unroll
-            for (int j = 0; j < J; ++j) {
-                const int e = lane + 32 * j;
-                if (e < E && !(taken >> j & 1u) && before(v[j], e, bv, be)) {
-                    bv = v[j];
-                    be = e;
-                }
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-                if (before(ov, oe, bv, be)) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-            if (be == INT_MAX) be = 0;  // only if every remaining logit is NaN
-            sel[s] = be;
-            sl[s] = bv;
-            if ((be & 31) == lane) taken |= 1u << (be >> 5);
-        }
+    }
+    if (ids_in == nullptr) {
+        warp_topk<J>(v, E, k, lane, sel, sl);
     } else {
         int my = lane < k ? ids_in[t * k + lane] : 0;
         bool good = lane >= k || (my >= 0 && my < E);
@@ -112,6 +123,40 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) topk_gates_kernel(
         if (!ok && lane == 0) {
             atomicOr(status, STATUS_BAD_IDS);
             atomicAdd(status + 2, 1);
+        }
+        if (filter && ok) {
+            // Replay plausibility filter (Composer 2 Technical Report, §6.2):
+            // keep a replayed expert iff its logit is at least the router's own
+            // k-th logit + ln(tau); refill dropped slots, in slot order, with the
+            // router's own candidates not already present, in its own order.
+            int own[kMaxK];
+            float own_l[kMaxK];
+            warp_topk<J>(v, E, k, lane, own, own_l);
+            const float thr = own_l[k - 1] + log_tau;
+            bool kept[kMaxK];
+#pragma unroll
+            for (int s = 0; s < kMaxK; ++s) kept[s] = s < k && sl[s] >= thr;
+            int next = 0, replaced = 0;
+#pragma unroll
+            for (int s = 0; s < kMaxK; ++s) {
+                if (s >= k || kept[s]) continue;
+                for (;;) {
+                    const int c = own[next];
+                    const float cl = own_l[next];
+                    ++next;
+                    bool used = false;
+#pragma unroll
+                    for (int s2 = 0; s2 < kMaxK; ++s2)
+                        if (s2 < k && (kept[s2] || s2 < s) && sel[s2] == c) used = true;
+                    if (!used) {
+                        sel[s] = c;
+                        sl[s] = cl;
+                        break;
+                    }
+                }
+                ++replaced;
+            }
+            if (replaced && lane == 0) atomicAdd(status + 3, replaced);
         }
     }
 
@@ -151,6 +196,8 @@ struct TopkArgs {
     float* gates_out;
     int32_t* valid;
     int32_t* status;
+    int filter;
+    float log_tau;
 };
 
 template <int J>
@@ -158,7 +205,7 @@ cudaError_t launch_j(const TopkArgs& a, cudaStream_t s) {
     const int64_t blocks = (a.T + kWarpsPerBlock - 1) / kWarpsPerBlock;
     topk_gates_kernel<J><<<static_cast<unsigned>(blocks), 32 * kWarpsPerBlock, 0, s>>>(
         a.logits, a.parts, a.nsplit, a.stride, a.bias, a.logits_out, a.T, a.E, a.k, a.ids_in,
-        a.ids_out, a.gates_out, a.valid, a.status);
+        a.ids_out, a.gates_out, a.valid, a.status, a.filter, a.log_tau);
     return cudaGetLastError();
 }
 
@@ -178,7 +225,7 @@ cudaError_t launch_topk_gates(const float* logits, int64_t T, int E, int k,
                               const int32_t* ids_in, int32_t* ids_out, float* gates_out,
                               int32_t* valid, int32_t* status, cudaStream_t s) {
     const TopkArgs a{logits, nullptr, 1, 0, nullptr, nullptr, T, E, k, ids_in, ids_out,
-                     gates_out, valid, status};
+                     gates_out, valid, status, 0, 0.0f};
     return launch_any(a, s);
 }
 
@@ -186,10 +233,11 @@ cudaError_t launch_topk_gates_split(const float* parts, int nsplit, int64_t stri
                                     const float* bias, float* logits_out, int64_t T, int E,
                                     int k, const int32_t* ids_in, int32_t* ids_out,
                                     float* gates_out, int32_t* valid, int32_t* status,
-                                    cudaStream_t s) {
-    if (!parts || !logits_out || nsplit < 1) return cudaErrorInvalidValue;
-    const TopkArgs a{logits_out, parts, nsplit, stride, bias, logits_out, T, E, k, ids_in,
-                     ids_out, gates_out, valid, status};
+                                    cudaStream_t s, int filter, float log_tau) {
+    if (!logits_out || nsplit < 1 || (nsplit > 1 && !parts)) return cudaErrorInvalidValue;
+    if (filter && !ids_in) return cudaErrorInvalidValue;
+    const TopkArgs a{logits_out, nsplit > 1 ? parts : nullptr, nsplit, stride, bias, logits_out,
+                     T, E, k, ids_in, ids_out, gates_out, valid, status, filter, log_tau};
     return launch_any(a, s);
 }
 

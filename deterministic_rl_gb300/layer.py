@@ -64,11 +64,14 @@ class MoELayer:
         return ids, gates
 
     def forward(self, x: torch.Tensor, replay_ids: Optional[torch.Tensor] = None, stream=None,
-                outputs=None):
+                outputs=None, filter_tau: Optional[float] = None):
         T = x.shape[0]
         out, ids, gates = outputs if outputs is not None else self.outputs(T)
         ws = self.workspace(T)
-        if replay_ids is None:
+        if replay_ids is not None and filter_tau is not None:
+            B.moe_forward_replay_filtered(self.dims(T), x, self.weights, replay_ids, filter_tau,
+                                          out, ids, gates, ws, stream)
+        elif replay_ids is None:
             B.moe_forward(self.dims(T), x, self.weights, out, ids, gates, ws, stream)
         else:
             B.moe_forward_replay(self.dims(T), x, self.weights, replay_ids, out, ids, gates, ws,

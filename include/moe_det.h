@@ -123,7 +123,9 @@ typedef struct {
 
 /* Byte offsets of the intermediate buffers inside the workspace, for
  * inspection after a call (all int32 unless noted; pairs i = t*k + s):
- *   status   int32[4]      device status word (moe_status bits), see below
+ *   status   int32[4]      [0] device status bits, [1] where a wait ran out,
+ *                          [2] tokens with rejected replay ids, [3] slots replaced
+ *                          by the replay filter
  *   logits   fp32 [T][E]   router logits (+ bias)
  *   valid    int32[T]      1 = token's ids valid, 0 = replayed ids rejected
  *   cnt      [E]           pairs routed to each expert (histogram)
@@ -175,6 +177,25 @@ moe_status moe_forward_replay(const moe_dims *dims, const void *x,
                               const moe_weights *w, const int32_t *ids_in,
                               void *out, int32_t *ids_out, float *gates_out,
                               void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Router replay with the plausibility filter of [TR] §6.2 (replayed experts
+ * whose gate score falls below a threshold derived from the router's own
+ * top-k are dropped and replaced by the router's candidates).  The threshold is
+ * not given on the pages; this library reads it as a fraction tau of the own
+ * k-th expert's softmax score: replayed expert e is kept iff
+ *   logit_e >= logit_(own k-th) + ln(tau),   0 <= tau <= 1
+ * (tau = 0 keeps every replayed id and equals moe_forward_replay).  Dropped
+ * slots, in ascending slot order, take the router's own top-k experts, in its
+ * own order, that are not already among the token's ids; gate weights are the
+ * softmax over the final ids.  Arguments and outputs as moe_forward_replay;
+ * ids_out receives the ids actually used.  The total number of replaced slots
+ * of the call is added to status word 3 of the workspace (moe_ws_layout.status
+ * + 12 bytes, int32).  tau outside [0, 1] or NaN: MOE_ERR_ARG. */
+moe_status moe_forward_replay_filtered(const moe_dims *dims, const void *x,
+                                       const moe_weights *w, const int32_t *ids_in,
+                                       float tau, void *out, int32_t *ids_out,
+                                       float *gates_out, void *ws, size_t ws_bytes,
+                                       moe_stream_t stream);
 
 /* Synchronise `stream` and return the device status of the last call that
  * used this workspace: MOE_OK, MOE_ERR_BAD_IDS or MOE_ERR_TIMEOUT (the

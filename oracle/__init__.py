@@ -83,6 +83,8 @@ def _load():
         lib.oracle_select_topk.argtypes = [P, I, I, I, P]
         lib.oracle_check_ids.restype = ctypes.c_int64
         lib.oracle_check_ids.argtypes = [P, I, I, I, P]
+        lib.oracle_filter_replay.restype = None
+        lib.oracle_filter_replay.argtypes = [P, P, I, I, I, ctypes.c_double, P, P]
         lib.oracle_gate_weights.restype = None
         lib.oracle_gate_weights.argtypes = [P, P, I, I, I, P]
         lib.oracle_counting_sort.restype = None
@@ -191,6 +193,18 @@ def check_ids(ids: np.ndarray, E: int) -> np.ndarray:
     return valid
 
 
+def filter_replay(logits: np.ndarray, ids: np.ndarray, tau: float):
+    """Replay plausibility filter: returns (ids [T][k] int32, replaced [T] int32)."""
+    lg = _c(logits, np.float64)
+    ids = _c(ids, np.int32)
+    T, E = lg.shape
+    k = ids.shape[1]
+    out = np.empty((T, k), np.int32)
+    rep = np.empty(T, np.int32)
+    _load().oracle_filter_replay(_ptr(lg), _ptr(ids), T, E, k, float(tau), _ptr(out), _ptr(rep))
+    return out, rep
+
+
 def gate_weights(logits: np.ndarray, ids: np.ndarray) -> np.ndarray:
     lg = _c(logits, np.float64)
     ids = _c(ids, np.int32)
@@ -264,7 +278,8 @@ class LayerResult:
 
 def layer_forward(x: np.ndarray, w_router: np.ndarray, bias: Optional[np.ndarray],
                   get_expert: Callable[[int], Expert], shared: Sequence[Expert],
-                  k: int, replay_ids: Optional[np.ndarray] = None) -> LayerResult:
+                  k: int, replay_ids: Optional[np.ndarray] = None,
+                  filter_tau: Optional[float] = None) -> LayerResult:
     """The MoE layer for the tokens in x, in the order the definition reads:
     logits -> selection (own) or recorded ids (replay) -> gate weights ->
     each chosen expert's FFN on the token -> fixed-order combine.
@@ -272,6 +287,8 @@ def layer_forward(x: np.ndarray, w_router: np.ndarray, bias: Optional[np.ndarray
     get_expert(e) returns expert e's weights; it is called once per distinct
     expert the tokens use, in ascending e, so that large layers can be fed
     one expert at a time.  Replay tokens with invalid ids produce a zero row.
+    With filter_tau, the replayed ids of valid tokens first pass the replay
+    plausibility filter.
     """
     x = _c(x, np.uint16)
     T, d = x.shape
@@ -285,6 +302,9 @@ def layer_forward(x: np.ndarray, w_router: np.ndarray, bias: Optional[np.ndarray
         assert ids.shape == (T, k)
         valid = check_ids(ids, E)
         ids[valid == 0] = np.arange(k, dtype=np.int32)
+        if filter_tau is not None:
+            ids, _ = filter_replay(logits, ids, filter_tau)
+            ids[valid == 0] = np.arange(k, dtype=np.int32)
     gates = gate_weights(logits, ids)
     gates[valid == 0] = 0.0
     y_slots = np.zeros((T, k, d), np.float64)

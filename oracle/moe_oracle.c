@@ -143,6 +143,44 @@ void oracle_gate_weights(const double *logits, const int32_t *ids, int64_t T,
     }
 }
 
+void oracle_filter_replay(const double *logits, const int32_t *ids_in, int64_t T,
+                          int64_t E, int64_t k, double tau, int32_t *ids_out,
+                          int32_t *n_replaced) {
+    int32_t *own = (int32_t *)malloc((size_t)k * sizeof(int32_t));
+    unsigned char *kept = (unsigned char *)malloc((size_t)k);
+    for (int64_t t = 0; t < T; ++t) {
+        const double *l = logits + t * E;
+        const int32_t *in = ids_in + t * k;
+        int32_t *out = ids_out + t * k;
+        oracle_select_topk(l, 1, E, k, own);
+        /* threshold from the router's own k-th choice */
+        const double thr = tau > 0.0 ? l[own[k - 1]] + log(tau) : -INFINITY;
+        for (int64_t s = 0; s < k; ++s) {
+            kept[s] = l[in[s]] >= thr;
+            out[s] = in[s];
+        }
+        int32_t replaced = 0;
+        int64_t next = 0; /* next own candidate to try */
+        for (int64_t s = 0; s < k; ++s) {
+            if (kept[s]) continue;
+            for (;;) {
+                int32_t c = own[next++];
+                int taken = 0;
+                for (int64_t s2 = 0; s2 < k; ++s2)
+                    if ((kept[s2] || s2 < s) && out[s2] == c) taken = 1;
+                if (!taken) {
+                    out[s] = c;
+                    break;
+                }
+            }
+            ++replaced;
+        }
+        if (n_replaced) n_replaced[t] = replaced;
+    }
+    free(kept);
+    free(own);
+}
+
 /* ---- dispatch: stable counting sort -------------------------------------- */
 
 void oracle_counting_sort(const int32_t *ids, int64_t n_pairs, int64_t E,

@@ -83,6 +83,19 @@ void oracle_select_topk(const double *logits, int64_t T, int64_t E, int64_t k,
 int64_t oracle_check_ids(const int32_t *ids, int64_t T, int64_t E, int64_t k,
                          uint8_t *valid);
 
+/* Replay plausibility filter ([TR] §6.2: replayed experts whose gate score is
+ * below a plausibility threshold derived from the router's own top-k are
+ * dropped and replaced by the router's candidates).  Reading: with the router's
+ * own top-k o_0..o_{k-1} (descending), replayed id e is kept iff its softmax
+ * score is at least tau times that of o_{k-1}, i.e. l_e >= l_{o_{k-1}} + ln(tau)
+ * (tau = 0 keeps everything); each dropped slot, in ascending slot order, takes
+ * the next own candidate (in own order) that is not already among the token's
+ * ids.  ids_in must be valid (oracle_check_ids).  Writes ids_out [T][k] and,
+ * per token, the number of replaced slots (n_replaced [T], may be NULL). */
+void oracle_filter_replay(const double *logits, const int32_t *ids_in, int64_t T,
+                          int64_t E, int64_t k, double tau, int32_t *ids_out,
+                          int32_t *n_replaced);
+
 /* Gate weights over the given ids (own or replayed): softmax of the chosen
  * logits, i.e. softmax over all E renormalised over the chosen set. */
 void oracle_gate_weights(const double *logits, const int32_t *ids, int64_t T,

@@ -1,0 +1,129 @@
+"""Replay plausibility filter on the GPU (moe_forward_replay_filtered) against
+the oracle's filter: recorded ids where some slots name experts far below the
+router's own choice, so that the filter drops and refills them."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deterministic_rl_gb300 import build, MoELayer
+from deterministic_rl_gb300 import binding as B
+from deterministic_rl_gb300.synthetic import CONFIGS, make_layer
+import moe_cases as mc
+
+pytestmark = pytest.mark.gpu
+MARGIN = 1e-4  # decisions closer than this to a threshold may go either way in fp32
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    oracle.build()
+
+
+def doctored_ids(logits, k, seed):
+    """The router's own ids with 1-3 slots of a third of the tokens replaced by
+    experts ranked 9th to 40th (implausible under a tight threshold)."""
+    rng = np.random.default_rng(seed)
+    order = np.argsort(-logits, axis=1, kind="stable").astype(np.int32)
+    ids = order[:, :k].copy()
+    T, E = logits.shape
+    for t in rng.choice(T, T // 3, replace=False):
+        n = rng.integers(1, 4)
+        slots = rng.choice(k, n, replace=False)
+        far = rng.choice(np.arange(k, min(E, 40)), n, replace=False)
+        ids[t, slots] = order[t, far]
+    return ids
+
+
+def unambiguous(logits, rids, tau, k):
+    """Tokens whose filter decisions are not within MARGIN of a threshold."""
+    srt = -np.sort(-logits, axis=1)
+    ok = (srt[:, k - 1] - srt[:, k]) > 1e-3
+    ok &= (srt[:, :k - 1] - srt[:, 1:k]).min(axis=1) > MARGIN
+    if tau > 0:
+        thr = srt[:, k - 1] + math.log(tau)
+        rl = np.take_along_axis(logits, rids.astype(np.int64), axis=1)
+        near = np.abs(rl - thr[:, None]) <= MARGIN
+        if tau == 1.0:
+            # the router's own k-th expert sits exactly on the threshold in both
+            # precisions (ln 1 = 0) and is kept by both
+            kth = np.argsort(-logits, axis=1, kind="stable")[:, k - 1]
+            near &= rids != kth[:, None]
+        ok &= ~near.any(axis=1)
+    return ok
+
+
+@pytest.mark.parametrize("cfg", [CONFIGS["c1_tiny"],
+                                 CONFIGS["c1_tiny"].with_(name="filt_T300", T=300, n_shared=1, seed=9)],
+                         ids=lambda c: c.name)
+@pytest.mark.parametrize("tau", [0.0, 0.3, 1.0])
+def test_filtered_replay_matches_oracle(cfg, tau):
+    inp = make_layer(cfg, "cuda")
+    ref_plain = mc.oracle_layer(inp)
+    rids = doctored_ids(ref_plain.logits, cfg.k, seed=3)
+    layer = MoELayer.from_inputs(inp, out_fp32=True)
+    out, ids, gates = layer.forward(inp.x, replay_ids=torch.from_numpy(rids).cuda(), filter_tau=tau)
+    assert layer.status() == B.MOE_OK
+    exp_ids, exp_rep = oracle.filter_replay(ref_plain.logits, rids, tau)
+    g_ids = ids.cpu().numpy()
+    ok = unambiguous(ref_plain.logits, rids, tau, cfg.k)
+    assert ok.mean() > 0.9
+    assert np.array_equal(g_ids[ok], exp_ids[ok])
+    if tau == 0.0:
+        assert np.array_equal(g_ids, rids)
+    if ok.all():
+        assert int(layer.intermediates(cfg.T)["status"][3]) == int(exp_rep.sum())
+    # layer output where the ids agree
+    ref_f = oracle.layer_forward(*_oracle_args(inp), cfg.k, replay_ids=rids, filter_tau=tau)
+    assert np.array_equal(ref_f.ids[ok], exp_ids[ok])
+    mc.check_gates(gates.cpu().numpy()[ok], ref_f.gates[ok])
+    mc.check_out(out.cpu().numpy()[ok], ref_f.out[ok])
+
+
+def _oracle_args(inp):
+    from deterministic_rl_gb300.synthetic import bf16_bits
+    wr, bias = mc.router_host(inp)
+    return bf16_bits(inp.x), wr, bias, mc.expert_getter(inp), mc.shared_experts(inp)
+
+
+def test_filter_with_tau_zero_is_plain_replay_bitwise():
+    inp = make_layer(CONFIGS["c1_tiny"].with_(T=200, seed=4), "cuda")
+    rids = doctored_ids(mc.oracle_layer(inp).logits, 8, seed=5)
+    layer = MoELayer.from_inputs(inp, out_fp32=True)
+    r = torch.from_numpy(rids).cuda()
+    a = [t.clone() for t in layer.forward(inp.x, replay_ids=r)]
+    b = layer.forward(inp.x, replay_ids=r, filter_tau=0.0)
+    for u, v in zip(a, b):
+        assert torch.equal(u, v)
+
+
+def test_filter_rejects_bad_tau():
+    inp = make_layer(CONFIGS["c1_tiny"].with_(T=4), "cuda")
+    layer = MoELayer.from_inputs(inp)
+    out, ids, gates = layer.outputs(4)
+    r = torch.zeros((4, 8), dtype=torch.int32, device="cuda")
+    for tau in (-0.1, 1.5, float("nan")):
+        rc = B.moe_forward_replay_filtered(layer.dims(4), inp.x, layer.weights, r, tau, out, ids,
+                                           gates, layer.workspace(4), check=False)
+        assert rc == B.MOE_ERR_ARG
+
+
+@pytest.mark.slow
+def test_filtered_replay_decode_layer_full_size():
+    cfg = CONFIGS["c2_decode_replay"]
+    inp = make_layer(cfg, "cuda")
+    wr, bias = mc.router_host(inp)
+    from deterministic_rl_gb300.synthetic import bf16_bits
+    lg = oracle.router_logits(bf16_bits(inp.x), wr, bias)
+    rids = doctored_ids(lg, cfg.k, seed=11)
+    layer = MoELayer.from_inputs(inp, out_fp32=True)
+    out, ids, gates = layer.forward(inp.x, replay_ids=torch.from_numpy(rids).cuda(), filter_tau=0.5)
+    assert layer.status() == B.MOE_OK
+    exp_ids, _ = oracle.filter_replay(lg, rids, 0.5)
+    ok = unambiguous(lg, rids, 0.5, cfg.k)
+    assert np.array_equal(ids.cpu().numpy()[ok], exp_ids[ok])
+    ref = mc.oracle_layer(inp, replay_ids=exp_ids)
+    mc.check_out(out.cpu().numpy()[ok], ref.out[ok])

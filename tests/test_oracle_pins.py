@@ -327,3 +327,48 @@ def test_mxfp8_layer_equals_bf16_layer_on_dequantised_weights():
     a = oracle.layer_forward(x, wr, None, lambda e: exq[e], [], 8)
     b = oracle.layer_forward(x, wr, None, lambda e: exb[e], [], 8)
     assert np.array_equal(a.out, b.out)
+
+
+# ---- replay plausibility filter ------------------------------------------------
+
+def test_replay_filter_hand_worked_cases():
+    with open(os.path.join(GOLDEN, "replay_filter_cases.json")) as f:
+        g = json.load(f)
+    lg = np.array([g["logits"]], np.float64)
+    for c in g["cases"]:
+        out, rep = oracle.filter_replay(lg, np.array([c["replay"]], np.int32), c["tau"])
+        assert list(out[0]) == c["expect"], c
+        assert int(rep[0]) == c["replaced"], c
+
+
+def test_replay_filter_properties():
+    rng = np.random.default_rng(12)
+    T, E, k = 400, 24, 8
+    lg = rng.standard_normal((T, E))
+    own = oracle.select_topk(lg, k)
+    rids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    # tau = 0 keeps everything; replaying the router's own choice is never filtered
+    out0, rep0 = oracle.filter_replay(lg, rids, 0.0)
+    assert np.array_equal(out0, rids) and (rep0 == 0).all()
+    for tau in (0.1, 0.5, 1.0):
+        o, r = oracle.filter_replay(lg, own, tau)
+        assert np.array_equal(o, own) and (r == 0).all()
+    prev = np.zeros(T, np.int32)
+    for tau in (0.01, 0.1, 0.3, 0.7, 1.0):
+        out, rep = oracle.filter_replay(lg, rids, tau)
+        assert (rep >= prev).all()            # a higher threshold drops more
+        prev = rep
+        kth = np.take_along_axis(lg, own[:, -1:].astype(np.int64), 1)[:, 0]
+        for t in range(T):
+            assert len(set(out[t].tolist())) == k
+            for s in range(k):
+                if out[t, s] == rids[t, s]:
+                    assert lg[t, rids[t, s]] >= kth[t] + math.log(tau) - 1e-12
+                else:                          # replaced by an own candidate
+                    assert lg[t, rids[t, s]] < kth[t] + math.log(tau)
+                    assert out[t, s] in set(own[t].tolist())
+    # tau = 1 with replayed experts all outside the own top-k: the own top-k set
+    far = np.argsort(-lg, axis=1, kind="stable")[:, k:2 * k].astype(np.int32)
+    out, rep = oracle.filter_replay(lg, far, 1.0)
+    assert (rep == k).all()
+    assert np.array_equal(out, own)
