@@ -1,16 +1,23 @@
 // gemm_pair.cu -- the expert GEMMs (gate/up + SwiGLU, down) on pairs of SMs:
 // tcgen05.mma.cta_group::2 with M = 256 weight rows (128 in each CTA of a
-// 2-CTA cluster) and N = 256 tokens (each CTA loads and holds 128 of them).
-// Each SM thus loads 16 KB of weights and 16 KB of tokens per 64-wide K step
-// for 4.2 MFLOP of MMA work, a third less operand traffic than a one-SM
+// 2-CTA cluster) and up to N = 256 tokens (each CTA loads and holds half).
+// Each SM thus loads 16 KB of weights and up to 16 KB of tokens per 64-wide K
+// step for 4.2 MFLOP of MMA work, a third less operand traffic than a one-SM
 // 128 x 256 tile, and a 32 KB pipeline stage leaves room for six stages.
+// A tile with fewer tokens (the last tile of a group, or an expert that few
+// tokens chose) issues its MMAs with N = its token count rounded up to 64, so
+// the tensor pipe does not spend a full-width tile's time on padding while
+// the weights stream.
 //
 // These are the grouped expert GEMMs of the Composer 2 Technical Report,
 // §6.1 "Training infrastructure" (Fig. 10).  The fixed accumulation order of
 // the Training Data No. 94 write-up (section "浮点数不守规矩，MoE 火上浇油")
 // holds as in the one-SM kernel: one CTA pair produces each output element
-// from one MMA shape (M = 256, N = 256, K = 16 steps in K order, one TMEM
-// accumulator); no split-K, no atomics; the same schedule for every group size.
+// from M = 256 MMAs over K = 16 steps in K order into one TMEM accumulator; no
+// split-K, no atomics.  The MMA's N only selects how many independent output
+// columns (tokens) one instruction produces; each column's dot product takes
+// the same K steps whatever N is, so a token's result does not depend on how
+// many other tokens share its tile.
 //
 // Roles in each CTA (192 threads): warp 0 TMA producer; warp 1 TMEM owner and,
 // in the pair's leader (cluster rank 0), the MMA issuer; warps 2..5 epilogue.
@@ -34,7 +41,6 @@ constexpr uint32_t kBBytes = kHalfN * BK * 2;    // 128 token rows x 64 along K
 constexpr uint32_t kBox32Bytes = 32 * BK * 2;
 constexpr int kAccCols = kPairN;
 constexpr uint32_t kTmemCols = 2 * kAccCols;
-constexpr uint32_t kIdesc = idesc_bf16_f32(2 * BM, kPairN);
 constexpr int kXPad = 33;
 constexpr int kMaxGroups = 1024;
 
@@ -69,6 +75,7 @@ struct PCfg {
 
 struct Tile {
     int m, g, n_valid, brow, arow;
+    int half;     // MMA N / 2: token rows each CTA holds (a multiple of 32)
     bool shared;
     bool reused;  // the expert has several token tiles: its weight tiles are read again
 };
@@ -93,18 +100,26 @@ __device__ __forceinline__ Tile decode_tile(int t, uint32_t rank, const GemmPara
     const int nt = l - tl.m * ntg;
     tl.reused = ntg > 1;
     tl.n_valid = min(kPairN, gcnt[lo] - nt * kPairN);
+    tl.half = min(kPairN, max(64, (tl.n_valid + 63) & ~63)) >> 1;
     tl.brow = goff[lo] + nt * kPairN;
     tl.shared = lo >= p.G;
     tl.arow = (tl.shared ? 0 : lo * p.M) + tl.m * 2 * gemm_rows(MODE) + rank * gemm_rows(MODE);
     return tl;
 }
 
-// Token-row bytes CTA `rank` loads for a tile with n_valid tokens.
-__device__ __forceinline__ uint32_t b_bytes(int n_valid, uint32_t rank, int partial) {
-    const int nv = min(max(n_valid - static_cast<int>(rank) * kHalfN, 0), kHalfN);
-    const int nbox = (nv + 31) >> 5;
-    if (!partial || nbox == kHalfN / 32) return kBBytes;
-    return nbox * kBox32Bytes;
+// Token rows CTA `rank` holds of a tile: [rank * half, rank * half + half) of
+// the tile's tokens, of which this many exist; they are loaded in 32-row boxes
+// (a CTA with none leaves its rows stale: they only feed columns never stored).
+__device__ __forceinline__ int b_rows(const Tile& tl, uint32_t rank) {
+    return min(max(tl.n_valid - static_cast<int>(rank) * tl.half, 0), tl.half);
+}
+__device__ __forceinline__ uint32_t b_bytes(const Tile& tl, uint32_t rank) {
+    return ((b_rows(tl, rank) + 31) >> 5) * kBox32Bytes;
+}
+
+// Instruction descriptor for this tile's MMA: M = 256, N = 2 * half.
+__device__ __forceinline__ uint32_t tile_idesc(const Tile& tl) {
+    return idesc_bf16_f32(2 * BM, 2 * tl.half);
 }
 
 __device__ __forceinline__ void raise_timeout(const GemmParams& p, volatile int* abort, int where) {
@@ -278,8 +293,10 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
             tma_prefetch_desc(&p.a0);
             tma_prefetch_desc(&p.b);
             if (p.has_shared) tma_prefetch_desc(&p.as0);
+            // Weight tiles read by one cluster only stream through L2; those of
+            // an expert with several token tiles stay, like the token rows.
             const uint64_t pol_once = l2_policy_evict_first();
-            const uint64_t pol_again = l2_policy_evict_normal();
+            const uint64_t pol_again = l2_policy_evict_last();
             const uint64_t pol_x = l2_policy_evict_last();
             int stage = 0;
             uint32_t phase = 0;
@@ -290,12 +307,10 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                 const uint64_t pol_w = tl.reused ? pol_again : pol_once;
                 const CUtensorMap* ma0 = tl.shared ? &p.as0 : &p.a0;
                 const CUtensorMap* ma1 = tl.shared ? &p.as1 : &p.a1;
-                const int nv = min(max(tl.n_valid - static_cast<int>(rank) * kHalfN, 0), kHalfN);
-                const int nbox = (nv + 31) >> 5;
-                const bool whole = !p.partial_b || nbox == kHalfN / 32;
-                const uint32_t expect = (MX ? 0 : 2 * kABytes) + b_bytes(tl.n_valid, 0, p.partial_b) +
-                                        b_bytes(tl.n_valid, 1, p.partial_b);
-                const int brow = tl.brow + static_cast<int>(rank) * kHalfN;
+                const int nbox = (b_rows(tl, rank) + 31) >> 5;
+                const bool whole = nbox == kHalfN / 32;
+                const uint32_t expect = (MX ? 0 : 2 * kABytes) + b_bytes(tl, 0) + b_bytes(tl, 1);
+                const int brow = tl.brow + static_cast<int>(rank) * tl.half;
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort, tmo)) {
                         if (!*abort) raise_timeout(p, abort, 11);
@@ -353,6 +368,8 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d0 = tmem_base + acc * kAccCols;
+                const uint32_t idesc =
+                    tile_idesc(decode_tile<MODE>(t, rank, p, tile_start, gcnt, goff, GG));
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort, tmo)) {
                         if (!*abort) raise_timeout(p, abort, 14);
@@ -365,7 +382,7 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k)
                         umma_bf16_pair(d0, sdesc_kmajor_sw128(sa + k * 32),
-                                       sdesc_kmajor_sw128(sb + k * 32), kIdesc, (kb | k) != 0);
+                                       sdesc_kmajor_sw128(sb + k * 32), idesc, (kb | k) != 0);
                     umma_commit_pair(&empty[stage], 0x3);
                     if (++stage == kStages) {
                         stage = 0;
@@ -387,7 +404,7 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
             if (lane == 0) {
                 // ---------------- fp8 weight producer (both CTAs) ----------------
                 const uint64_t pol_once = l2_policy_evict_first();
-                const uint64_t pol_again = l2_policy_evict_normal();
+                const uint64_t pol_again = l2_policy_evict_last();
                 int fs = 0, ss = 0;
                 uint32_t fph = 0, sph = 0;
                 uint32_t f_issued = 0, f_par = 0, s_issued = 0, s_par = 0;

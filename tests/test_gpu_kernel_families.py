@@ -73,3 +73,28 @@ def test_forced_kernel_families_agree_bitwise(tmp_path, T, S, zipf):
         res[fam] = torch.load(path)
     for a, b in zip(res["one_sm"], res["pair"]):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("c", [1, 63, 64, 65, 128, 129, 192, 193, 255, 256, 257])
+def test_pair_tile_width_does_not_change_a_token(c):
+    """The SM-pair kernel issues a tile's MMAs with N = its token count rounded
+    up to 64.  Expert 0 gets the first c tokens (its tile N runs through 64,
+    128, 192, 256 and a second tile); every other expert's group is the same in
+    all runs.  Token 0's output and every other token's routed outputs must not
+    change with c."""
+    T = 300
+    inp = make_layer(_cfg(T, name="width", seed=13), "cuda")
+    layer = MoELayer.from_inputs(inp, out_fp32=True)
+    ids = torch.empty((T, 8), dtype=torch.int32)
+    ids[:, 1:] = torch.arange(1, 8, dtype=torch.int32)
+    ids[:, 0] = 8 + torch.arange(T, dtype=torch.int32) % 40
+    base = [t.clone() for t in layer.forward(inp.x, replay_ids=ids.cuda())]
+    ids[:c, 0] = 0
+    out, _, _ = layer.forward(inp.x, replay_ids=ids.cuda())
+    # tokens c.. route exactly as in the base run except that their slot-0
+    # groups lost tokens 0..c-1: still the same columns-independent results
+    assert torch.equal(out[c:], base[0][c:])
+    ids2 = ids.clone()
+    ids2[1:, 0] = 8 + torch.arange(1, T, dtype=torch.int32) % 40
+    single, _, _ = layer.forward(inp.x, replay_ids=ids2.cuda())   # expert 0: token 0 alone
+    assert torch.equal(out[0], single[0])
