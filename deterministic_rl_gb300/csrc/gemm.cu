@@ -80,8 +80,10 @@ template <int MODE>
 __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
     using C = Cfg<MODE>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // Offsetting the shared array itself (never through an integer) keeps every
+    // derived pointer in the shared address space, so that accesses through
+    // them compile to shared-memory loads and stores, not generic ones.
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kStages * C::kStageBytes);
     uint64_t* empty = full + C::kStages;
     uint64_t* tfull = empty + C::kStages;

@@ -56,7 +56,15 @@ struct PCfg {
     static constexpr bool kPair = MODE == GEMM_SWIGLU;      // 64 gate + 64 up rows per CTA
     static constexpr int kRowsCta = gemm_rows(MODE);        // output weight rows per CTA
     static constexpr int kRowsTile = 2 * kRowsCta;          // per CTA pair
-    static constexpr uint32_t kXBytes = kPair ? 2 * 32 * kXPad * 4 : 0;
+    // MX gate/up: the converters lay the CTA's 128 operand rows out as blocks
+    // of 16 gate rows followed by the same 16 up rows, so each epilogue warp's
+    // 32 accumulator lanes hold both halves of 16 rows and exchange them with
+    // a shuffle.  bf16 gate/up: TMA loads 64 gate rows and then 64 up rows
+    // (two large boxes; sixteen-row boxes cost more in TMA issue than the
+    // exchange they save) and the up warps pass their values to the gate
+    // warps through shared memory.
+    static constexpr bool kInterleave = kPair && MX;
+    static constexpr uint32_t kXBytes = kPair && !MX ? 2 * 32 * kXPad * 4 : 0;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;  // operand ring entry
     static constexpr int kStages = MX ? 5 : 6;
     static constexpr uint32_t kF8Bytes = BM * BK;               // fp8 weight tile
@@ -80,25 +88,64 @@ struct Tile {
     bool reused;  // the expert has several token tiles: its weight tiles are read again
 };
 
-template <int MODE>
-__device__ __forceinline__ Tile decode_tile(int t, uint32_t rank, const GemmParams& p,
-                                            const int* tile_start, const int* gcnt,
-                                            const int* goff, int GG) {
-    // Within an expert the token tiles vary fastest, so all token tiles of a
-    // weight tile run back to back (on neighbouring clusters) and share it in L2.
-    Tile tl;
-    const int j = t / p.MT;
+// The tile order.  Groups (experts, then the shared expert) with several token
+// tiles ("hot": their weight tiles are compute-bound, each read by several
+// clusters) and groups with one ("cold": each weight tile streams from HBM once
+// for a few tokens) form two lists, each in group order, and within a hot
+// group's weight tile its token tiles run back to back (on neighbouring
+// clusters) so that they share it in L2.  The two lists are merged in
+// proportion -- position t is hot iff floor((t + 1) H / N) > floor(t H / N),
+// H hot tiles of N -- so every wave of clusters mixes tensor-bound and
+// HBM-bound tiles instead of running the hot experts and the cold ones in
+// separate phases.  The order decides only which cluster computes a tile and
+// when, never how: each tile is still computed whole by one CTA pair.
+struct Sched {
+    const int* hs;    // [GG + 1] prefix of token tiles over hot groups
+    const int* cs;    // [GG + 1] prefix of cold groups
+    const int* gcnt;  // [GG] tokens per group
+    const int* goff;  // [GG] first token row of each group
+    int GG;
+    int64_t H, N;     // hot tiles, all tiles
+};
+
+__device__ __forceinline__ int find_group(const int* start, int GG, int j) {
+    // the last group whose start is <= j (groups of width 0 share a start
+    // with the next group and are never chosen)
     int lo = 0, hi = GG;
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
-        if (tile_start[mid] <= j) lo = mid; else hi = mid;
+        if (start[mid] <= j) lo = mid; else hi = mid;
     }
-    tl.g = lo;
-    const int ntg = tile_start[lo + 1] - tile_start[lo];
-    const int l = t - tile_start[lo] * p.MT;
-    tl.m = l / ntg;
-    const int nt = l - tl.m * ntg;
-    tl.reused = ntg > 1;
+    return lo;
+}
+
+template <int MODE>
+__device__ __forceinline__ Tile decode_tile(int t, uint32_t rank, const GemmParams& p,
+                                            const Sched& sc) {
+    Tile tl;
+    const int64_t h0 = static_cast<int64_t>(t) * sc.H / sc.N;
+    const int64_t h1 = static_cast<int64_t>(t + 1) * sc.H / sc.N;
+    int nt;
+    if (h1 > h0) {
+        const int j = static_cast<int>(h0);
+        const int g = find_group(sc.hs, sc.GG, j / p.MT);
+        const int ntg = sc.hs[g + 1] - sc.hs[g];
+        const int l = j - sc.hs[g] * p.MT;
+        tl.g = g;
+        tl.m = l / ntg;
+        nt = l - tl.m * ntg;
+        tl.reused = true;
+    } else {
+        const int j = t - static_cast<int>(h0);
+        const int g = find_group(sc.cs, sc.GG, j / p.MT);
+        tl.g = g;
+        tl.m = j - sc.cs[g] * p.MT;
+        nt = 0;
+        tl.reused = false;
+    }
+    const int lo = tl.g;
+    const int* gcnt = sc.gcnt;
+    const int* goff = sc.goff;
     tl.n_valid = min(kPairN, gcnt[lo] - nt * kPairN);
     tl.half = min(kPairN, max(64, (tl.n_valid + 63) & ~63)) >> 1;
     tl.brow = goff[lo] + nt * kPairN;
@@ -191,8 +238,10 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
     constexpr int kStages = C::kStages;
     constexpr uint32_t kStageBytes = C::kStageBytes;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // Offsetting the shared array itself (never through an integer) keeps every
+    // derived pointer in the shared address space, so that accesses through
+    // them compile to shared-memory loads and stores, not generic ones.
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
     uint8_t* f8ring = smem + kStages * kStageBytes;
     uint8_t* scring = f8ring + C::kF8Stages * C::kF8Bytes;
     float* xbuf = reinterpret_cast<float*>(smem + C::kRingBytes);
@@ -201,7 +250,7 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
     uint64_t* tfull = empty + kStages;
     uint64_t* tempty = tfull + 2;
     uint64_t* drain = tempty + 2;
-    uint64_t* xfull = drain + 1;
+    uint64_t* xfull = drain + 1;               // bf16 gate/up: up values in xbuf
     uint64_t* xempty = xfull + 2;
     uint64_t* f8full = xempty + 2;             // MX, local: fp8 tile landed
     uint64_t* f8empty = f8full + C::kF8Stages;  // MX, local: converters done with it
@@ -209,9 +258,10 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
     uint64_t* scempty = scfull + C::kScStages;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + C::kBarriers);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    int* tile_start = reinterpret_cast<int*>(tmem_slot + 4);
     const int GG = p.G + p.has_shared;
-    int* gcnt = tile_start + GG + 1;
+    int* hs = reinterpret_cast<int*>(tmem_slot + 4);
+    int* cs = hs + GG + 1;
+    int* gcnt = cs + GG + 1;
     int* goff = gcnt + GG;
 
     const int warp = threadIdx.x >> 5;
@@ -220,9 +270,10 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
     const bool leader = rank == 0;
 
     if (warp == 0) {
+        // per group: token tiles if hot (several), 1 in the cold count if cold
         const int per = (GG + 31) / 32;
         const int g0 = lane * per;
-        int local = 0;
+        int local_h = 0, local_c = 0;
         for (int g = g0; g < min(g0 + per, GG); ++g) {
             int c, o;
             if (g < p.G) {
@@ -234,20 +285,30 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
             }
             gcnt[g] = c;
             goff[g] = o;
-            local += (c + kPairN - 1) / kPairN;
+            const int ntg = (c + kPairN - 1) / kPairN;
+            if (ntg > 1) local_h += ntg; else local_c += ntg;
         }
-        int incl = local;
+        int incl_h = local_h, incl_c = local_c;
 #pragma unroll
         for (int s = 1; s < 32; s <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, s);
-            if (lane >= s) incl += v;
+            const int vh = __shfl_up_sync(0xffffffffu, incl_h, s);
+            const int vc = __shfl_up_sync(0xffffffffu, incl_c, s);
+            if (lane >= s) {
+                incl_h += vh;
+                incl_c += vc;
+            }
         }
-        int run = incl - local;
+        int run_h = incl_h - local_h, run_c = incl_c - local_c;
         for (int g = g0; g < min(g0 + per, GG); ++g) {
-            tile_start[g] = run;
-            run += (gcnt[g] + kPairN - 1) / kPairN;
+            hs[g] = run_h;
+            cs[g] = run_c;
+            const int ntg = (gcnt[g] + kPairN - 1) / kPairN;
+            if (ntg > 1) run_h += ntg; else run_c += ntg;
         }
-        if (lane == 31) tile_start[GG] = incl;
+        if (lane == 31) {
+            hs[GG] = incl_h;
+            cs[GG] = incl_c;
+        }
     } else if (warp == 1) {
         tmem_alloc_pair(tmem_slot, kTmemCols);
         tmem_relinquish_pair();
@@ -269,9 +330,9 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
-            mbar_init(&tempty[a], 8);  // 4 epilogue warps in each of the two CTAs
             mbar_init(&xfull[a], 1);
             mbar_init(&xempty[a], 1);
+            mbar_init(&tempty[a], 8);  // 4 epilogue warps in each of the two CTAs
         }
         mbar_init(drain, 1);
         *abort = 0;
@@ -282,7 +343,9 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
     cluster_sync();  // barriers of both CTAs initialised before any remote use
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const int total = tile_start[GG] * p.MT;
+    const Sched sched{hs, cs, gcnt, goff, GG, static_cast<int64_t>(hs[GG]) * p.MT,
+                   static_cast<int64_t>(hs[GG] + cs[GG]) * p.MT};
+    const int total = static_cast<int>(sched.N);
     const uint64_t tmo = p.timeout_ns;
     const int cid = static_cast<int>(cluster_id_x());
     const int ncl = static_cast<int>(nclusters_x());
@@ -303,7 +366,7 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
             uint32_t issued = 0, last_par = 0;
             bool ok = p.stall_test == 0;
             for (int t = cid; t < total && ok; t += ncl) {
-                const Tile tl = decode_tile<MODE>(t, rank, p, tile_start, gcnt, goff, GG);
+                const Tile tl = decode_tile<MODE>(t, rank, p, sched);
                 const uint64_t pol_w = tl.reused ? pol_again : pol_once;
                 const CUtensorMap* ma0 = tl.shared ? &p.as0 : &p.a0;
                 const CUtensorMap* ma1 = tl.shared ? &p.as1 : &p.a1;
@@ -369,7 +432,7 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                 tc_fence_after();
                 const uint32_t d0 = tmem_base + acc * kAccCols;
                 const uint32_t idesc =
-                    tile_idesc(decode_tile<MODE>(t, rank, p, tile_start, gcnt, goff, GG));
+                    tile_idesc(decode_tile<MODE>(t, rank, p, sched));
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort, tmo)) {
                         if (!*abort) raise_timeout(p, abort, 14);
@@ -410,7 +473,7 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                 uint32_t f_issued = 0, f_par = 0, s_issued = 0, s_par = 0;
                 bool ok = p.stall_test == 0;
                 for (int t = cid; t < total && ok; t += ncl) {
-                    const Tile tl = decode_tile<MODE>(t, rank, p, tile_start, gcnt, goff, GG);
+                    const Tile tl = decode_tile<MODE>(t, rank, p, sched);
                     const uint64_t pol_w = tl.reused ? pol_again : pol_once;
                     for (int kb = 0; kb < p.KB; ++kb) {
                         if ((kb & 7) == 0) {  // scales of the next 8 k-blocks
@@ -528,7 +591,12 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                         e4m3x4_to_bf16x4(q.z, sbyte, o1.x, o1.y);
                         e4m3x4_to_bf16x4(q.w, sbyte, o1.z, o1.w);
                     }
-                    uint8_t* row = st + r * 128;
+                    // operand row: gate/up rows alternate in 16-row blocks
+                    // (the low 3 bits, which pick the swizzle, are r's)
+                    const int ar = C::kInterleave ? ((r & 63) >> 4) * 2 * kSwigluBlock +
+                                                  (r >= 64 ? kSwigluBlock : 0) + (r & 15)
+                                            : r;
+                    uint8_t* row = st + ar * 128;
                     *reinterpret_cast<uint4*>(row + ((c2 ^ (r & 7)) << 4)) = o0;
                     *reinterpret_cast<uint4*>(row + (((c2 + 1) ^ (r & 7)) << 4)) = o1;
                 }
@@ -537,21 +605,31 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                 if (lane == 0) {
                     mbar_arrive(&f8empty[fs]);
                     mbar_arrive(&scempty[ss]);
-                    mbar_arrive_cluster(map_to_rank(&full[os], 0));
+                    if (leader)
+                        mbar_arrive(&full[os]);
+                    else
+                        mbar_arrive_operand_ready(map_to_rank(&full[os], 0));
                 }
             }
         }
     } else {
         // ---------------- epilogue (warps 2..5, both CTAs) ----------------
+        // Warp q reads accumulator lanes [32q, 32q + 32).  MX gate/up: lanes
+        // 0..15 of the warp hold gate rows f..f+15 and lanes 16..31 the same
+        // rows of the up projection; each lane swaps half of its 32 columns
+        // with the lane 16 away, then finishes 16 outputs of its row.  bf16
+        // gate/up: warps 0, 1 hold gate rows and warps 2, 3 the matching up
+        // rows, which they pass on through xbuf.
         const int q = warp & 3;
         const int pr = q & 1;
         const bool up_warp = q >= 2;
+        const bool up_lane = lane >= kSwigluBlock;
         int acc = 0;
         uint32_t acc_phase = 0;
         uint32_t xph = 0;
         bool ok = true;
         for (int t = cid; t < total && ok; t += ncl) {
-            const Tile tl = decode_tile<MODE>(t, rank, p, tile_start, gcnt, goff, GG);
+            const Tile tl = decode_tile<MODE>(t, rank, p, sched);
             const bool ready = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort, tmo));
             if (!ready) {
                 if (lane == 0 && !*abort) raise_timeout(p, abort, 16);
@@ -559,7 +637,8 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
             }
             tc_fence_after();
             const int row = tl.m * C::kRowsTile + static_cast<int>(rank) * C::kRowsCta +
-                            (C::kPair ? pr : q) * 32 + lane;
+                            (C::kInterleave ? q * kSwigluBlock + (lane & (kSwigluBlock - 1))
+                                            : (C::kPair ? pr : q) * 32 + lane);
             const bool row_ok = row < p.M;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
@@ -567,7 +646,22 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                 float v[32];
                 tmem_ld32(taddr + c0, v);
                 tmem_ld_wait();
-                if constexpr (MODE == GEMM_SWIGLU) {
+                if constexpr (C::kInterleave) {
+                    __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out);
+                    const int cb = c0 + (up_lane ? 16 : 0);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float lo = v[j], hi = v[16 + j];
+                        const float other = __shfl_xor_sync(0xffffffffu, up_lane ? lo : hi, 16);
+                        const float g = up_lane ? other : lo;
+                        const float u = up_lane ? hi : other;
+                        if (row_ok && cb + j < tl.n_valid) {
+                            const float h = g / (1.0f + expf(-g)) * u;
+                            H[static_cast<int64_t>(tl.brow + cb + j) * p.ldo + row] =
+                                __float2bfloat16_rn(h);
+                        }
+                    }
+                } else if constexpr (C::kPair) {
                     float* xb = xbuf + pr * 32 * kXPad + lane * kXPad;
                     if (up_warp) {
                         if (!__all_sync(0xffffffffu, mbar_wait(&xempty[pr], xph ^ 1u, abort, tmo))) {
@@ -644,7 +738,7 @@ template <int MODE, bool MX>
 size_t pair_smem_bytes(int GG) {
     using C = PCfg<MODE, MX>;
     return 1024 + C::kRingBytes + C::kXBytes + C::kBarriers * 8 + 16 +
-           static_cast<size_t>(3 * GG + 1) * 4;
+           static_cast<size_t>(4 * GG + 2) * 4;
 }
 
 template <int MODE, bool MX>

@@ -18,6 +18,11 @@ constexpr int BN_EXPERT = 256;  // token tile of the SM-pair expert GEMMs (gemm_
 // output element with the same bf16 MMAs in the same K order (tested bitwise).
 constexpr int64_t kOneSmMaxTokens = 128;
 constexpr int BK = 64;
+// In the SM-pair gate/up tile with MXFP8 weights each CTA's 128 converted
+// weight rows alternate in blocks: 16 gate rows, then the same 16 rows of the
+// up projection, four times, so that each epilogue warp's 32 accumulator lanes
+// hold both halves of 16 rows.
+constexpr int kSwigluBlock = 16;
 
 // Device status word bits (ws status[0]); status[1] = id of the kernel whose
 // wait ran out, status[2] = number of tokens with rejected replay ids.

@@ -244,6 +244,16 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                  : "memory");
 }
 
+// Arrive on the pair leader's mbarrier to say that this CTA's operand tile,
+// written by threads and published to the async proxy with
+// fence_proxy_async_smem(), is ready for the pair's MMA.  The tile is read only
+// by the tensor core, from this CTA's own shared memory, so the arrive needs no
+// cluster-scope release of this thread's writes (the costly part of
+// mbar_arrive_cluster); it carries the default CTA-scope release.
+__device__ __forceinline__ void mbar_arrive_operand_ready(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
 // 2-D tiled load into this CTA's shared memory whose completion is signalled on
 // the pair leader's mbarrier (shared::cluster address `bar_cluster`).
 __device__ __forceinline__ void tma_load_2d_pair(void* dst, const CUtensorMap* map,
