@@ -193,42 +193,43 @@ __device__ __forceinline__ uint32_t e4m3x2_to_bf16x2(uint32_t two, float scale) 
 }
 
 // Four E4M3 bytes of one 32-element block (scale byte s) -> four bf16 in two
-// words (element 0 in the low half of `lo`).  Exact.  For normal E4M3 inputs
-// and 7 <= s <= 246 the bf16 pattern is the E4M3 pattern with its exponent
-// re-biased by s - 7 (E4M3 exponent bias 7, bf16 bias 127, scale 2^(s-127)),
-// done with integer operations; zero, subnormal or NaN bytes and extreme
-// scales take the float route above.
+// words (element 0 in the low half of `lo`), exactly, by the float route above.
+// Used for blocks the integer route below does not cover.
 __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t s, uint32_t& lo,
                                                  uint32_t& hi) {
-    const uint32_t x7 = w & 0x7F7F7F7Fu;
-    const uint32_t ex = (w >> 3) & 0x0F0F0F0Fu;                       // exponent field per byte
-    const uint32_t zero_exp = (ex - 0x01010101u) & ~ex & 0x80808080u;  // some byte has exponent 0
-    const uint32_t nan = (x7 + 0x01010101u) & 0x80808080u;           // some byte is 0x7F / 0xFF
-    if ((zero_exp | nan) == 0u && s >= 7u && s <= 246u) {
-        const uint32_t a = __byte_perm(w, 0u, 0x4140);  // bytes 0, 1 -> low halves of two shorts
-        const uint32_t b = __byte_perm(w, 0u, 0x4342);  // bytes 2, 3
-        const uint32_t k = ((s - 7u) << 7) * 0x00010001u;
-        lo = (((a << 4) & 0x07F007F0u) + k) | ((a << 8) & 0x80008000u);
-        hi = (((b << 4) & 0x07F007F0u) + k) | ((b << 8) & 0x80008000u);
-    } else {
-        const float scale = e8m0_scale(s);
-        lo = e4m3x2_to_bf16x2(w & 0xFFFFu, scale);
-        hi = e4m3x2_to_bf16x2(w >> 16, scale);
-    }
+    const float scale = e8m0_scale(s);
+    lo = e4m3x2_to_bf16x2(w & 0xFFFFu, scale);
+    hi = e4m3x2_to_bf16x2(w >> 16, scale);
 }
 
-// Branch-free parts of e4m3x4_to_bf16x4: the re-biased patterns (valid when
-// the flag below is 0) and the flag "some byte is zero, subnormal or NaN".
+// Nonzero iff some byte of w is zero or subnormal (exponent field 0) or NaN
+// (low seven bits all ones): bit 7 of (b & 0x78) + 0x78 is set iff the
+// exponent is nonzero, bit 7 of (b & 0x7F) + 1 iff the low seven bits are ones;
+// neither sum carries out of its byte.
 __device__ __forceinline__ uint32_t e4m3x4_special(uint32_t w) {
-    const uint32_t ex = (w >> 3) & 0x0F0F0F0Fu;
-    return ((ex - 0x01010101u) & ~ex & 0x80808080u) | (((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u);
+    const uint32_t e = (w & 0x78787878u) + 0x78787878u;
+    const uint32_t n = (w & 0x7F7F7F7Fu) + 0x01010101u;
+    return (~e | n) & 0x80808080u;
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(a), "r"(sel));
+    return d;
+}
+
+// Four normal E4M3 bytes (none flagged by e4m3x4_special) with 7 <= s <= 246
+// -> four bf16, exactly.  The bf16 of e4m3 * 2^(s-127) is the E4M3 pattern
+// with its 7 exponent+mantissa bits moved to bf16 bits [10:4], the sign to bit
+// 15 and the exponent re-biased by s - 7 (E4M3 bias 7, bf16 bias 127); the
+// sum E + s - 7 stays within [1, 254], so it never carries into the sign.
+// The byte permute places each byte in the low half of a 16-bit lane with its
+// sign replicated through the high byte; a shift left by 4 then puts the
+// seven bits at [10:4] and a copy of the sign at bit 15, and the mask clears
+// the rest (including the four bits the low lane shifts into the high one).
 __device__ __forceinline__ void e4m3x4_rebias(uint32_t w, uint32_t k, uint32_t& lo, uint32_t& hi) {
-    const uint32_t a = __byte_perm(w, 0u, 0x4140);
-    const uint32_t b = __byte_perm(w, 0u, 0x4342);
-    lo = (((a << 4) & 0x07F007F0u) + k) | ((a << 8) & 0x80008000u);
-    hi = (((b << 4) & 0x07F007F0u) + k) | ((b << 8) & 0x80008000u);
+    lo = ((prmt(w, 0x9180u) << 4) & 0x87F087F0u) + k;  // bytes 0, 1
+    hi = ((prmt(w, 0xB3A2u) << 4) & 0x87F087F0u) + k;  // bytes 2, 3
 }
 
 template <int MODE, bool MX>
@@ -584,7 +585,7 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                     e4m3x4_rebias(q.w, kk, o1.z, o1.w);
                     const uint32_t special = e4m3x4_special(q.x) | e4m3x4_special(q.y) |
                                              e4m3x4_special(q.z) | e4m3x4_special(q.w) |
-                                             (sbyte < 7u || sbyte > 246u);
+                                             ((sbyte - 7u) > 239u);  // s outside [7, 246]
                     if (special) {  // rare: exact float route for all 16 values
                         e4m3x4_to_bf16x4(q.x, sbyte, o0.x, o0.y);
                         e4m3x4_to_bf16x4(q.y, sbyte, o0.z, o0.w);
@@ -642,10 +643,9 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
             const bool row_ok = row < p.M;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
-            for (int c0 = 0; c0 < tl.n_valid; c0 += 32) {
-                float v[32];
-                tmem_ld32(taddr + c0, v);
-                tmem_ld_wait();
+            // One chunk of 32 accumulator columns (tokens c0 .. c0 + 31);
+            // false when a wait of the bf16 gate/up handoff ran out.
+            auto chunk = [&](const float (&v)[32], int c0) -> bool {
                 if constexpr (C::kInterleave) {
                     __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out);
                     const int cb = c0 + (up_lane ? 16 : 0);
@@ -666,8 +666,7 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                     if (up_warp) {
                         if (!__all_sync(0xffffffffu, mbar_wait(&xempty[pr], xph ^ 1u, abort, tmo))) {
                             if (lane == 0 && !*abort) raise_timeout(p, abort, 17);
-                            ok = false;
-                            break;
+                            return false;
                         }
 #pragma unroll
                         for (int j = 0; j < 32; ++j) xb[j] = v[j];
@@ -676,8 +675,7 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                     } else {
                         if (!__all_sync(0xffffffffu, mbar_wait(&xfull[pr], xph, abort, tmo))) {
                             if (lane == 0 && !*abort) raise_timeout(p, abort, 18);
-                            ok = false;
-                            break;
+                            return false;
                         }
                         float u[32];
 #pragma unroll
@@ -713,6 +711,17 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                                     __float2bfloat16_rn(v[j]);
                     }
                 }
+                return true;
+            };
+            // two chunks per TMEM round trip
+            for (int c0 = 0; c0 < tl.n_valid && ok; c0 += 64) {
+                float va[32], vb[32];
+                tmem_ld32(taddr + c0, va);
+                tmem_ld32(taddr + c0 + 32, vb);
+                tmem_ld_wait();
+                tmem_regs_ready(va);
+                tmem_regs_ready(vb);
+                ok = chunk(va, c0) && (c0 + 32 >= tl.n_valid || chunk(vb, c0 + 32));
             }
             if (!ok) break;
             tc_fence_before();

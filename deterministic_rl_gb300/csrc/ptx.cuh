@@ -180,6 +180,15 @@ __device__ __forceinline__ void tmem_ld_wait() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Ties the registers of a tcgen05.ld to a point after tmem_ld_wait(): the
+// compiler sees them rewritten here, so no use of them moves above the wait.
+__device__ __forceinline__ void tmem_regs_ready(float (&v)[32]) {
+#pragma unroll
+    for (int i = 0; i < 32; i += 8)
+        asm volatile("" : "+f"(v[i]), "+f"(v[i + 1]), "+f"(v[i + 2]), "+f"(v[i + 3]), "+f"(v[i + 4]),
+                     "+f"(v[i + 5]), "+f"(v[i + 6]), "+f"(v[i + 7]));
+}
+
 // Shared-memory matrix descriptor for a K-major operand tile stored with the
 // 128-byte swizzle (rows of 128 bytes = 64 bf16 along K, 8-row atoms of
 // 1024 bytes, atoms stacked along M/N every 1024 bytes).

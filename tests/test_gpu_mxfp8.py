@@ -53,6 +53,33 @@ def test_mxfp8_equals_bf16_on_dequantised_weights_bitwise(T):
         assert torch.equal(x, y)
 
 
+def test_mxfp8_every_byte_pattern_and_float_route_scales_bitwise():
+    """Weight bytes drawn uniformly from every non-NaN E4M3 pattern (one in
+    sixteen is zero or subnormal, which the converters send down the exact
+    float route), scale bytes 3..6 (also the float route) or 112..121 (the
+    integer route): the layer must still equal the bf16 layer on the
+    dequantised weights bitwise."""
+    inp = make_layer(small_mx(T=300, seed=43), "cuda")
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(5)
+    pats = torch.tensor([b for b in range(256) if (b & 0x7F) != 0x7F], dtype=torch.uint8,
+                        device="cuda")
+    for w, sc in ((inp.w_gate, inp.s_gate), (inp.w_up, inp.s_up), (inp.w_down, inp.s_down)):
+        w.copy_(pats[torch.randint(0, len(pats), w.shape, generator=gen, device="cuda")])
+        slow = torch.rand(sc.shape, generator=gen, device="cuda") < 0.3
+        lo = torch.randint(3, 7, sc.shape, generator=gen, device="cuda")
+        mid = torch.randint(112, 122, sc.shape, generator=gen, device="cuda")
+        sc.copy_(torch.where(slow, lo, mid).to(torch.uint8))
+    mx = MoELayer.from_inputs(inp, out_fp32=True)
+    g, u, d = dequantised(inp)
+    bf = MoELayer(inp.w_router, g, u, d, router_bias=inp.router_bias, out_fp32=True)
+    a = mx.forward(inp.x)
+    b = bf.forward(inp.x)
+    assert torch.isfinite(a[0]).all()
+    for x, y in zip(a, b):
+        assert torch.equal(x, y)
+
+
 def test_mxfp8_small_layer_matches_oracle():
     inp = make_layer(small_mx(), "cuda")
     layer = MoELayer.from_inputs(inp, out_fp32=True)
