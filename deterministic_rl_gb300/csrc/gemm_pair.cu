@@ -47,10 +47,10 @@ constexpr int kMaxGroups = 1024;
 // MX: expert weights stored as MXFP8 (E4M3 bytes + one E8M0 scale per 32
 // along K).  A dedicated producer warp (warp 14) streams the CTA's fp8 weight
 // tiles into their own ring, far ahead, and a 16-byte scale box per row every
-// 8 k-blocks into a small scale ring; eight converter warps (6..13) each
-// convert whole k-blocks (warp w takes k-blocks w, w+8, ...) into the operand
-// ring's A buffer, so several k-blocks are converted at once and HBM latency
-// never sits between a conversion and its MMA.
+// 8 k-blocks into a small scale ring; eight converter warps, in four groups
+// of two, convert whole k-blocks (group g takes k-blocks g, g+4, ...) into the
+// operand ring's A buffer, so several k-blocks are converted at once and HBM
+// latency never sits between a conversion and its MMA.
 template <int MODE, bool MX>
 struct PCfg {
     static constexpr bool kPair = MODE == GEMM_SWIGLU;      // 64 gate + 64 up rows per CTA
@@ -224,12 +224,12 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
 // 15 and the exponent re-biased by s - 7 (E4M3 bias 7, bf16 bias 127); the
 // sum E + s - 7 stays within [1, 254], so it never carries into the sign.
 // The byte permute places each byte in the low half of a 16-bit lane with its
-// sign replicated through the high byte; a shift left by 4 then puts the
-// seven bits at [10:4] and a copy of the sign at bit 15, and the mask clears
-// the rest (including the four bits the low lane shifts into the high one).
+// sign replicated through the high byte; the mask keeps the seven bits [6:0]
+// and one copy of the sign (bit 11), and one multiply-add by 16 moves them to
+// [10:4] and bit 15 and adds the re-bias (no bit crosses into the other lane).
 __device__ __forceinline__ void e4m3x4_rebias(uint32_t w, uint32_t k, uint32_t& lo, uint32_t& hi) {
-    lo = ((prmt(w, 0x9180u) << 4) & 0x87F087F0u) + k;  // bytes 0, 1
-    hi = ((prmt(w, 0xB3A2u) << 4) & 0x87F087F0u) + k;  // bytes 2, 3
+    lo = (prmt(w, 0x9180u) & 0x087F087Fu) * 16u + k;  // bytes 0, 1
+    hi = (prmt(w, 0xB3A2u) & 0x087F087Fu) * 16u + k;  // bytes 2, 3
 }
 
 template <int MODE, bool MX>
@@ -544,8 +544,9 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
             static_assert(C::kConvGroups <= C::kStages && C::kConvGroups <= C::kF8Stages &&
                               C::kConvGroups <= 8,
                           "converter groups must not outrun the rings");
-            const int grp_w = (warp - 6) / C::kConvPerKb;
-            const int sub = (warp - 6) % C::kConvPerKb;
+            const int cw = warp - 6;  // 0 .. kConvWarps - 1
+            const int grp_w = cw / C::kConvPerKb;
+            const int sub = cw % C::kConvPerKb;
             constexpr int kRowsPerWarp = BM / C::kConvPerKb;
             const int my_tiles = cid < total ? (total - cid + ncl - 1) / ncl : 0;
             const int64_t n_kb = static_cast<int64_t>(my_tiles) * p.KB;
