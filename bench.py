@@ -35,7 +35,14 @@ METRIC = "MoE-layer tokens/s (384-expert top-8, d=7168, replay, bf16); % of roof
 UNIT = "tokens/s"
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNELS_PER_STEP = 9  # router GEMM, top-k, hist, scan, scatter, gather, gate/up, down, combine
+DISPATCH_SEGMENT_PAIRS = 4096  # (token, slot) pairs one dispatch CTA sorts
+
+
+def kernels_per_step(T, k):
+    """Launches of one layer call: router GEMM, top-k, dispatch (one kernel for
+    at most one segment of pairs, else histogram, scan and scatter), gather,
+    gate/up, down, combine."""
+    return 7 if T * k <= DISPATCH_SEGMENT_PAIRS else 9
 
 
 def parse():
@@ -443,7 +450,7 @@ def run_ours(args):
                            "l2": ("L2 flushed between steps" if need_flush else
                                   f"inputs larger than L2: {nbytes / 1e9:.1f} GB read per step")},
                 "roofline": roofline, "layer_roofline": layer_roof, "stages_ms": stage_ms,
-                "clocks": clk.summary(), "e2e": e2e, "gpu_launches": KERNELS_PER_STEP * K,
+                "clocks": clk.summary(), "e2e": e2e, "gpu_launches": kernels_per_step(T, cfg.k) * K,
                 "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if world > 1:
