@@ -3,7 +3,8 @@ distributions).  This module draws random numbers and encodes them into the
 storage formats the layer reads (bf16 rounding, MXFP8 block quantisation of
 the weights); it holds none of the layer's arithmetic -- no logits, no
 selection, no expert FFN, no combine.  Both the CUDA path's tests and the
-oracle consume the bytes it produces.
+oracle consume the bytes it produces.  NVFP4 is the forward format of the
+Composer 2 Technical Report, §6.1 (E2M1 values, E4M3 scale per 16, fp32 scale).
 
 Workloads (hidden size, expert count, top-k, expert width, shared expert, value
 distributions, seeds):
@@ -13,6 +14,8 @@ distributions, seeds):
   c4_train_32k     T=32768, same layer, uniform or Zipf (s=1.2) routing
   c5_mxfp8         T=16384, expert weights MXFP8 (E4M3 + E8M0 per 32 along K),
                    no shared expert, 10 % of tokens near-tied at ranks 8/9
+  c6_nvfp4         T=16384, expert weights NVFP4 (E2M1 + E4M3 per 16 along K +
+                   an fp32 scale per matrix), no shared expert
 Hidden states ~N(0,1); router ~N(0, variance 1/d); expert weights
 ~N(0, std 0.02); replay ids are recorded from a copy of the hidden states
 perturbed by N(0, std 1e-3).  The 384-choose-8 gate is from the Training Data
@@ -38,7 +41,7 @@ class MoEConfig:
     k: int
     F: int
     n_shared: int
-    wfmt: str = "bf16"            # "bf16" | "mxfp8"
+    wfmt: str = "bf16"            # "bf16" | "mxfp8" | "nvfp4"
     zipf: float = 0.0             # bias = -zipf * ln(rank_e); 0 = no bias
     near_tie_frac: float = 0.0    # fraction of tokens to near-tie (built in tests)
     replay_noise: float = 1e-3    # std of the perturbation replay ids come from
@@ -55,6 +58,7 @@ CONFIGS = {
     "c4_train_32k": MoEConfig("c4_train_32k", 3, 32768, 7168, 384, 8, 2048, 1),
     "c5_mxfp8": MoEConfig("c5_mxfp8", 4, 16384, 7168, 384, 8, 2048, 0, wfmt="mxfp8",
                           near_tie_frac=0.1),
+    "c6_nvfp4": MoEConfig("c6_nvfp4", 5, 16384, 7168, 384, 8, 2048, 0, wfmt="nvfp4"),
 }
 
 
@@ -65,15 +69,18 @@ class LayerInputs:
     x_replay_src: torch.Tensor           # [T][d] bf16, x + N(0, noise) rounded
     w_router: torch.Tensor               # [E][d] bf16
     router_bias: Optional[torch.Tensor]  # [E] fp32
-    w_gate: torch.Tensor                 # [E][F][d] bf16 | uint8 (E4M3)
+    w_gate: torch.Tensor                 # [E][F][d] bf16 | uint8 (E4M3) | [E][F][d/2] uint8 (E2M1 x2)
     w_up: torch.Tensor                   # [E][F][d]
     w_down: torch.Tensor                 # [E][d][F]
-    s_gate: Optional[torch.Tensor]       # [E][F][d/32] uint8 (E8M0) or None
+    s_gate: Optional[torch.Tensor]       # [E][F][d/32] uint8 (E8M0) | [E][F][d/16] (E4M3) | None
     s_up: Optional[torch.Tensor]
-    s_down: Optional[torch.Tensor]       # [E][d][F/32]
+    s_down: Optional[torch.Tensor]       # [E][d][F/32] | [E][d][F/16]
     ws_gate: Optional[torch.Tensor]      # [F][d] bf16 shared expert
     ws_up: Optional[torch.Tensor]
     ws_down: Optional[torch.Tensor]      # [d][F]
+    gs_gate: Optional[torch.Tensor] = None   # NVFP4: [E] fp32 scale per matrix
+    gs_up: Optional[torch.Tensor] = None
+    gs_down: Optional[torch.Tensor] = None
 
 
 def _randn(shape, std, gen, device) -> torch.Tensor:
@@ -99,6 +106,35 @@ def quantize_mxfp8(w: torch.Tensor):
     return q.reshape(rows, K).contiguous(), s.contiguous()
 
 
+def quantize_nvfp4(w: torch.Tensor):
+    """Encode fp32 [rows][K] as NVFP4 weights: one fp32 scale for the matrix,
+    ts = amax / (6 * 448); per 16-element block along K an E4M3 scale
+    S = E4M3(amax_b / 6 / ts) (nearest even, saturating); values
+    E2M1(w / (S * ts)) rounded to nearest with ties to the even code, packed two
+    per byte (element 2j in the low nibble).  Returns (packed uint8
+    [rows][K/2], scales uint8 [rows][K/16], ts as a 0-d float32 tensor)."""
+    rows, K = w.shape
+    assert K % 16 == 0
+    w = w.float()
+    ts = w.abs().max() / 2688.0
+    blocks = w.reshape(rows, K // 16, 16)
+    bmax = blocks.abs().amax(dim=-1)
+    if float(ts) > 0:
+        S = ((bmax / 6.0) / ts).to(torch.float8_e4m3fn)
+    else:
+        S = torch.zeros_like(bmax).to(torch.float8_e4m3fn)
+    denom = (S.float() * ts).unsqueeze(-1)
+    v = torch.where(denom > 0, blocks / torch.where(denom > 0, denom, torch.ones_like(denom)),
+                    torch.zeros_like(blocks))
+    a = v.abs()
+    m = ((a > 0.25).int() + (a >= 0.75).int() + (a > 1.25).int() + (a >= 1.75).int()
+         + (a > 2.5).int() + (a >= 3.5).int() + (a > 5.0).int())
+    code = m | (((v < 0) & (m > 0)).int() << 3)
+    code = code.reshape(rows, K).to(torch.uint8)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).contiguous()
+    return packed, S.view(torch.uint8).contiguous(), ts.to(torch.float32)
+
+
 def make_layer(cfg: MoEConfig, device="cpu") -> LayerInputs:
     """Draw every tensor of the layer from one generator seeded with cfg.seed,
     in a fixed order: x, router, per expert (gate, up, down), shared expert,
@@ -113,21 +149,38 @@ def make_layer(cfg: MoEConfig, device="cpu") -> LayerInputs:
     w_router = _randn((E, d), 1.0 / math.sqrt(d), gen, device).to(bf)
 
     mx = cfg.wfmt == "mxfp8"
-    wdt = torch.uint8 if mx else bf
-    w_gate = torch.empty((E, F, d), dtype=wdt, device=device)
-    w_up = torch.empty((E, F, d), dtype=wdt, device=device)
-    w_down = torch.empty((E, d, F), dtype=wdt, device=device)
-    s_gate = torch.empty((E, F, d // 32), dtype=torch.uint8, device=device) if mx else None
-    s_up = torch.empty((E, F, d // 32), dtype=torch.uint8, device=device) if mx else None
-    s_down = torch.empty((E, d, F // 32), dtype=torch.uint8, device=device) if mx else None
+    nv = cfg.wfmt == "nvfp4"
+    u8 = torch.uint8
+    if nv:
+        w_gate = torch.empty((E, F, d // 2), dtype=u8, device=device)
+        w_up = torch.empty((E, F, d // 2), dtype=u8, device=device)
+        w_down = torch.empty((E, d, F // 2), dtype=u8, device=device)
+        s_gate = torch.empty((E, F, d // 16), dtype=u8, device=device)
+        s_up = torch.empty((E, F, d // 16), dtype=u8, device=device)
+        s_down = torch.empty((E, d, F // 16), dtype=u8, device=device)
+        gs = [torch.empty(E, dtype=torch.float32, device=device) for _ in range(3)]
+    else:
+        wdt = u8 if mx else bf
+        w_gate = torch.empty((E, F, d), dtype=wdt, device=device)
+        w_up = torch.empty((E, F, d), dtype=wdt, device=device)
+        w_down = torch.empty((E, d, F), dtype=wdt, device=device)
+        s_gate = torch.empty((E, F, d // 32), dtype=u8, device=device) if mx else None
+        s_up = torch.empty((E, F, d // 32), dtype=u8, device=device) if mx else None
+        s_down = torch.empty((E, d, F // 32), dtype=u8, device=device) if mx else None
+        gs = [None, None, None]
     for e in range(E):
-        for dst, sdst, shape in ((w_gate, s_gate, (F, d)), (w_up, s_up, (F, d)),
-                                 (w_down, s_down, (d, F))):
+        for j, (dst, sdst, shape) in enumerate(((w_gate, s_gate, (F, d)), (w_up, s_up, (F, d)),
+                                                (w_down, s_down, (d, F)))):
             w = _randn(shape, cfg.w_std, gen, device)
             if mx:
                 q, s = quantize_mxfp8(w)
                 dst[e].copy_(q)
                 sdst[e].copy_(s)
+            elif nv:
+                q, s, ts = quantize_nvfp4(w)
+                dst[e].copy_(q)
+                sdst[e].copy_(s)
+                gs[j][e] = ts
             else:
                 dst[e].copy_(w.to(bf))
 
@@ -147,7 +200,7 @@ def make_layer(cfg: MoEConfig, device="cpu") -> LayerInputs:
     x_replay_src = (x.float() + noise).to(bf)
 
     return LayerInputs(cfg, x, x_replay_src, w_router, bias, w_gate, w_up, w_down,
-                       s_gate, s_up, s_down, ws_gate, ws_up, ws_down)
+                       s_gate, s_up, s_down, ws_gate, ws_up, ws_down, gs[0], gs[1], gs[2])
 
 
 def bf16_bits(t: torch.Tensor):

@@ -11,7 +11,8 @@ Sources (see ``moe_oracle.h`` for the full statement of the definition):
   * Composer 2 Technical Report, §6.2 "RL infrastructure" (router replay:
     recorded expert indices override the router's selection, the router still
     computes the gate scores) and §6.1 "Training infrastructure" (grouped
-    expert GEMMs, dispatch/combine, MXFP8 format).
+    expert GEMMs, dispatch/combine, MXFP8 format, and the NVFP4 forward with
+    per-token scales and IEEE division in the quantiser).
   * Training Data No. 94 write-up, section "浮点数不守规矩，MoE 火上浇油", and
     the "五大工程挑戰" write-up, section "浮點數的陷阱": 8 of 384 experts per
     token, fixed-order accumulation.
@@ -39,6 +40,7 @@ _lock = threading.Lock()
 
 W_BF16 = 0
 W_MXFP8 = 1
+W_NVFP4 = 2
 
 
 def build(force: bool = False) -> str:
@@ -48,7 +50,7 @@ def build(force: bool = False) -> str:
                                                    os.path.getmtime(os.path.join(_HERE, "moe_oracle.h")))):
         return _LIB_PATH
     tmp = _LIB_PATH + f".tmp{os.getpid()}"
-    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-fopenmp", "-Wall",
+    cmd = ["gcc", "-O2", "-std=c11", "-ffp-contract=off", "-fPIC", "-shared", "-fopenmp", "-Wall",
            "-o", tmp, _SRC, "-lm"]
     subprocess.check_call(cmd)
     os.replace(tmp, _LIB_PATH)
@@ -57,7 +59,7 @@ def build(force: bool = False) -> str:
 
 class _Matrix(ctypes.Structure):
     _fields_ = [("fmt", ctypes.c_int), ("values", ctypes.c_void_p),
-                ("scales", ctypes.c_void_p)]
+                ("scales", ctypes.c_void_p), ("tscale", ctypes.c_float)]
 
 
 def _load():
@@ -75,6 +77,16 @@ def _load():
         lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
         lib.oracle_e8m0_to_f64.restype = ctypes.c_double
         lib.oracle_e8m0_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e2m1_to_f64.restype = ctypes.c_double
+        lib.oracle_e2m1_to_f64.argtypes = [ctypes.c_uint8]
+        lib.oracle_e2m1_round.restype = ctypes.c_uint8
+        lib.oracle_e2m1_round.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_round.restype = ctypes.c_uint8
+        lib.oracle_e4m3_round.argtypes = [ctypes.c_float]
+        lib.oracle_round_bf16.restype = ctypes.c_double
+        lib.oracle_round_bf16.argtypes = [ctypes.c_double]
+        lib.oracle_nvfp4_quantize_rows.restype = None
+        lib.oracle_nvfp4_quantize_rows.argtypes = [P, I, I, P, P, P]
         lib.oracle_matrix_elem.restype = ctypes.c_double
         lib.oracle_matrix_elem.argtypes = [ctypes.POINTER(_Matrix), I, I, I]
         lib.oracle_router_logits.restype = None
@@ -127,28 +139,68 @@ def e8m0_to_f64(s: int) -> float:
     return _load().oracle_e8m0_to_f64(int(s) & 0xFF)
 
 
+def e2m1_to_f64(code: int) -> float:
+    return _load().oracle_e2m1_to_f64(int(code) & 0xF)
+
+
+def e2m1_round(v: float) -> int:
+    return int(_load().oracle_e2m1_round(float(v)))
+
+
+def e4m3_round(v: float) -> int:
+    return int(_load().oracle_e4m3_round(float(v)))
+
+
+def round_bf16(v: float) -> float:
+    return _load().oracle_round_bf16(float(v))
+
+
+def nvfp4_quantize_rows(x: np.ndarray):
+    """NVFP4 with per-row (per-token) scales, the quantiser of the NVFP4
+    forward: x [R][K] fp32 (bf16 values) -> (codes uint8 [R][K], block scales
+    uint8 E4M3 [R][K/16], row scales float32 [R])."""
+    x = _c(x, np.float32)
+    R, K = x.shape
+    assert K % 16 == 0
+    codes = np.empty((R, K), np.uint8)
+    bs = np.empty((R, K // 16), np.uint8)
+    rs = np.empty(R, np.float32)
+    _load().oracle_nvfp4_quantize_rows(_ptr(x), R, K, _ptr(codes), _ptr(bs), _ptr(rs))
+    return codes, bs, rs
+
+
 # ---- weights ----------------------------------------------------------------
 
 @dataclass
 class Matrix:
-    """One weight matrix [rows][K] as raw storage: bf16 bit patterns (uint16),
-    or E4M3 bytes (uint8) plus E8M0 scale bytes [rows][K//32]."""
+    """One weight matrix [rows][K] as raw storage: bf16 bit patterns (uint16);
+    or E4M3 bytes (uint8) plus E8M0 scale bytes [rows][K//32]; or (NVFP4, when
+    tscale is given) E2M1 codes packed two per byte [rows][K//2] plus E4M3
+    scale bytes [rows][K//16] and the matrix's fp32 scale."""
     values: np.ndarray
     scales: Optional[np.ndarray] = None
+    tscale: Optional[float] = None
 
     @property
     def fmt(self) -> int:
+        if self.tscale is not None:
+            return W_NVFP4
         return W_MXFP8 if self.scales is not None else W_BF16
+
+    @property
+    def K(self) -> int:
+        return self.values.shape[-1] * (2 if self.fmt == W_NVFP4 else 1)
 
     def _struct(self) -> _Matrix:
         if self.fmt == W_BF16:
             assert self.values.dtype == np.uint16
         else:
             assert self.values.dtype == np.uint8 and self.scales.dtype == np.uint8
-        return _Matrix(self.fmt, _ptr(self.values), _ptr(self.scales))
+        return _Matrix(self.fmt, _ptr(self.values), _ptr(self.scales),
+                       float(self.tscale) if self.tscale is not None else 0.0)
 
     def elem(self, r: int, c: int) -> float:
-        K = self.values.shape[-1]
+        K = self.K
         st = self._struct()
         return _load().oracle_matrix_elem(ctypes.byref(st), K, r, c)
 
@@ -234,8 +286,9 @@ def expert_ffn(x: np.ndarray, ex: Expert) -> np.ndarray:
     x = _c(x, np.uint16)
     n, d = x.shape
     F = ex.w_gate.values.shape[0]
-    assert ex.w_gate.values.shape == (F, d) and ex.w_up.values.shape == (F, d)
-    assert ex.w_down.values.shape == (d, F)
+    assert ex.w_gate.K == d and ex.w_up.K == d and ex.w_up.values.shape[0] == F
+    assert ex.w_down.values.shape[0] == d and ex.w_down.K == F
+    assert len({ex.w_gate.fmt, ex.w_up.fmt, ex.w_down.fmt}) == 1
     y = np.empty((n, d), np.float64)
     if n == 0:
         return y

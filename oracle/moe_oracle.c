@@ -50,9 +50,115 @@ double oracle_e8m0_to_f64(uint8_t s) {
     return ldexp(1.0, (int)s - 127);
 }
 
+/* ---- NVFP4 ([TR] §6.1 Kernels: FP4 E2M1 values, an E4M3 scale per 16 values,
+ * an FP32 scale per token; IEEE division in the quantiser) ------------------ */
+
+double oracle_e2m1_to_f64(uint8_t code) {
+    /* sign bit 3; exponent bits 2..1 with bias 1; mantissa bit 0. */
+    int sign = (code >> 3) & 1;
+    int ex = (code >> 1) & 3;
+    int man = code & 1;
+    double v = ex == 0 ? 0.5 * man : ldexp(1.0 + 0.5 * man, ex - 1);
+    return sign ? -v : v;
+}
+
+uint8_t oracle_e2m1_round(float vf) {
+    /* the nearest of the eight magnitudes; on a tie the even code; beyond the
+     * largest magnitude, the largest (saturation) */
+    const double a = fabs((double)vf);
+    int best = a >= 6.0 ? 7 : 0;
+    for (int m = 1; m < 8 && best != 7; ++m) {
+        const double dm = fabs(a - oracle_e2m1_to_f64((uint8_t)m));
+        const double db = fabs(a - oracle_e2m1_to_f64((uint8_t)best));
+        if (dm < db || (dm == db && m % 2 == 0)) best = m;
+    }
+    return (uint8_t)((vf < 0.0f && best != 0) ? (best | 8) : best);
+}
+
+uint8_t oracle_e4m3_round(float vf) {
+    /* E4M3 (fn): normals (1 + m/8) * 2^(e-7), e = 1..15 (448 the largest),
+     * subnormals m/8 * 2^-6.  Round to nearest, ties to even, saturate. */
+    const double v = (double)vf;
+    if (!(v > 0.0)) return 0;
+    if (v >= 448.0) return 0x7E;
+    int e;
+    frexp(v, &e);
+    int ex = e - 1; /* 2^ex <= v < 2^(ex+1) */
+    if (ex < -6) return (uint8_t)nearbyint(ldexp(v, 9)); /* multiples of 2^-9; 8 -> 2^-6 */
+    double m = nearbyint(ldexp(v, 3 - ex));                /* 8 .. 16 */
+    if (m == 16.0) {
+        m = 8.0;
+        ex += 1;
+    }
+    const int code = ((ex + 7) << 3) | ((int)m - 8);
+    return (uint8_t)(code > 0x7E ? 0x7E : code);
+}
+
+void oracle_nvfp4_quantize_rows(const float *x, int64_t R, int64_t K, uint8_t *codes,
+                                uint8_t *bscale, float *rscale) {
+    /* fp32 arithmetic throughout (built with -ffp-contract=off), divisions
+     * correctly rounded as the IEEE standard defines them. */
+    for (int64_t r = 0; r < R; ++r) {
+        const float *row = x + r * K;
+        float amax = 0.0f;
+        for (int64_t i = 0; i < K; ++i) amax = fmaxf(amax, fabsf(row[i]));
+        const float s = amax / 2688.0f; /* 6 * 448 */
+        rscale[r] = s;
+        for (int64_t b = 0; b < K / 16; ++b) {
+            float bmax = 0.0f;
+            for (int64_t i = 0; i < 16; ++i) bmax = fmaxf(bmax, fabsf(row[16 * b + i]));
+            uint8_t S = 0;
+            if (s > 0.0f) {
+                const float sixth = bmax / 6.0f;
+                S = oracle_e4m3_round(sixth / s);
+            }
+            bscale[r * (K / 16) + b] = S;
+            const float denom = (float)oracle_e4m3_to_f64(S) * s;
+            for (int64_t i = 0; i < 16; ++i) {
+                const int64_t c = 16 * b + i;
+                codes[r * K + c] = denom > 0.0f ? oracle_e2m1_round(row[c] / denom) : 0;
+            }
+        }
+    }
+}
+
+double oracle_round_bf16(double v) {
+    /* 8 significant bits, ties to even; bf16 shares fp32's exponent range
+     * (subnormal spacing 2^-133); beyond the largest finite value -> inf. */
+    if (v == 0.0 || !isfinite(v)) return v;
+    int e;
+    frexp(v, &e);
+    int ex = e - 1;
+    if (ex < -126) ex = -126;
+    const double r = ldexp(nearbyint(ldexp(v, 7 - ex)), ex - 7);
+    if (fabs(r) > 0x1.FEp127) return copysign(INFINITY, v);
+    return r;
+}
+
+/* Quantise rows and return the values the GEMM uses: e2m1 * e4m3 * row scale. */
+static void nvfp4_quantised_values(const float *x, int64_t R, int64_t K, double *out) {
+    uint8_t *codes = (uint8_t *)malloc((size_t)(R * K));
+    uint8_t *bs = (uint8_t *)malloc((size_t)(R * K / 16));
+    float *rs = (float *)malloc((size_t)R * sizeof(float));
+    oracle_nvfp4_quantize_rows(x, R, K, codes, bs, rs);
+    for (int64_t r = 0; r < R; ++r)
+        for (int64_t i = 0; i < K; ++i)
+            out[r * K + i] = oracle_e2m1_to_f64(codes[r * K + i]) *
+                             oracle_e4m3_to_f64(bs[r * (K / 16) + i / 16]) * (double)rs[r];
+    free(rs);
+    free(bs);
+    free(codes);
+}
+
 double oracle_matrix_elem(const oracle_matrix *m, int64_t K, int64_t r, int64_t c) {
     if (m->fmt == ORACLE_W_BF16)
         return oracle_bf16_to_f64(((const uint16_t *)m->values)[r * K + c]);
+    if (m->fmt == ORACLE_W_NVFP4) {
+        const uint8_t byte = ((const uint8_t *)m->values)[r * (K / 2) + c / 2];
+        const uint8_t code = (c & 1) ? (byte >> 4) : (byte & 15);
+        return oracle_e2m1_to_f64(code) * oracle_e4m3_to_f64(m->scales[r * (K / 16) + c / 16]) *
+               (double)m->tscale;
+    }
     /* MXFP8: one E8M0 scale per 32 consecutive elements along K. */
     double q = oracle_e4m3_to_f64(((const uint8_t *)m->values)[r * K + c]);
     double sc = oracle_e8m0_to_f64(m->scales[r * (K / 32) + c / 32]);
@@ -213,7 +319,16 @@ void oracle_expert_ffn(const uint16_t *x, int64_t n, int64_t d, int64_t F,
      * [TR] §6.1 and Fig. 10: the grouped expert GEMMs. */
     double *xd = (double *)malloc((size_t)(n * d) * sizeof(double));
     double *h = (double *)malloc((size_t)(n * F) * sizeof(double));
-    for (int64_t i = 0; i < n * d; ++i) xd[i] = oracle_bf16_to_f64(x[i]);
+    const int nv = wg->fmt == ORACLE_W_NVFP4;
+    if (nv) {
+        /* NVFP4 forward: the token rows enter the GEMM quantised */
+        float *xf = (float *)malloc((size_t)(n * d) * sizeof(float));
+        for (int64_t i = 0; i < n * d; ++i) xf[i] = (float)oracle_bf16_to_f64(x[i]);
+        nvfp4_quantised_values(xf, n, d, xd);
+        free(xf);
+    } else {
+        for (int64_t i = 0; i < n * d; ++i) xd[i] = oracle_bf16_to_f64(x[i]);
+    }
 
     int64_t f;
 #pragma omp parallel for schedule(static)
@@ -226,6 +341,13 @@ void oracle_expert_ffn(const uint16_t *x, int64_t n, int64_t d, int64_t F,
             }
             h[r * F + f] = silu(a) * b;
         }
+    }
+    if (nv) {
+        /* h is stored in bf16 and quantised again, row by row */
+        float *hf = (float *)malloc((size_t)(n * F) * sizeof(float));
+        for (int64_t i = 0; i < n * F; ++i) hf[i] = (float)oracle_round_bf16(h[i]);
+        nvfp4_quantised_values(hf, n, F, h);
+        free(hf);
     }
     int64_t i;
 #pragma omp parallel for schedule(static)

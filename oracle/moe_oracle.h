@@ -50,15 +50,19 @@ extern "C" {
 #endif
 
 /* Weight storage formats the oracle reads. */
-enum { ORACLE_W_BF16 = 0, ORACLE_W_MXFP8 = 1 };
+enum { ORACLE_W_BF16 = 0, ORACLE_W_MXFP8 = 1, ORACLE_W_NVFP4 = 2 };
 
 /* One weight matrix [rows][K], rows contiguous along K (K-major).
  * bf16: values = uint16 bf16 bit patterns, scales = NULL.
- * mxfp8: values = E4M3 (fn) bytes, scales = E8M0 bytes [rows][K/32]. */
+ * mxfp8: values = E4M3 (fn) bytes, scales = E8M0 bytes [rows][K/32].
+ * nvfp4: values = E2M1 codes packed two per byte [rows][K/2] (element 2j in the
+ *        low nibble), scales = E4M3 bytes [rows][K/16], tscale = the matrix's
+ *        FP32 scale; element = e2m1 * e4m3 * tscale. */
 typedef struct {
     int fmt;
     const void *values;
     const uint8_t *scales;
+    float tscale;
 } oracle_matrix;
 
 /* Exact decoders (bit pattern -> fp64). */
@@ -67,6 +71,32 @@ double oracle_e4m3_to_f64(uint8_t b);
 double oracle_e8m0_to_f64(uint8_t s);
 /* Element (r, c) of a weight matrix with K columns, dequantised exactly. */
 double oracle_matrix_elem(const oracle_matrix *m, int64_t K, int64_t r, int64_t c);
+
+/* ---- NVFP4 with per-token scales ([TR] §6.1, Kernels paragraph) ----------
+ * The MoE forward quantises BF16 values to FP4 E2M1 with one E4M3 scale per
+ * 16 consecutive values and one FP32 scale per token (per row), using IEEE
+ * division.  Readings (the pages name the format, not the arithmetic):
+ *   s    = amax(row) / (6 * 448)                       fp32, IEEE division
+ *   S_b  = E4M3_RNE(amax(block b) / 6 / s)             fp32 divisions, saturating
+ *   q_i  = E2M1_RNE(x_i / (S_b * s))                   fp32 product, IEEE division
+ * and the value the GEMM uses is e2m1(q_i) * e4m3(S_b) * s.  An all-zero row
+ * has s = 0 and all codes and block scales 0; a block whose S_b rounds to 0
+ * has all codes 0.  Zero is always encoded +0 (code 0).  Inputs are finite. */
+
+/* Value of a 4-bit E2M1 code: sign bit 3, exponent bits 2..1 (bias 1),
+ * mantissa bit 0; exponent 0 is subnormal (0 or 0.5). */
+double oracle_e2m1_to_f64(uint8_t code);
+/* E2M1 code of v, rounded to nearest (ties to the even code), magnitudes above
+ * 6 saturate to 6. */
+uint8_t oracle_e2m1_round(float v);
+/* E4M3 (fn) byte of v >= 0, rounded to nearest even, saturating at 448. */
+uint8_t oracle_e4m3_round(float v);
+/* Quantise R rows of K values (K % 16 == 0; bf16 values given as fp32):
+ * codes [R][K] (one code per byte), bscale [R][K/16], rscale [R]. */
+void oracle_nvfp4_quantize_rows(const float *x, int64_t R, int64_t K, uint8_t *codes,
+                                uint8_t *bscale, float *rscale);
+/* Round a double to the nearest bf16 value (ties to even), as a double. */
+double oracle_round_bf16(double v);
 
 /* Router logits for T tokens: logits[t][e] = sum_j x[t][j]*wr[e][j] + bias[e].
  * x [T][d] bf16, wr [E][d] bf16, bias [E] fp32 or NULL. */
@@ -110,7 +140,10 @@ void oracle_counting_sort(const int32_t *ids, int64_t n_pairs, int64_t E,
                           int32_t *cnt, int32_t *off, int32_t *perm, int32_t *inv);
 
 /* SwiGLU expert FFN applied to n token rows.
- * x [n][d] bf16 rows; wg, wu: [F][d]; wd: [d][F]; y [n][d] fp64. */
+ * x [n][d] bf16 rows; wg, wu: [F][d]; wd: [d][F]; y [n][d] fp64.
+ * With NVFP4 weights the FFN is the NVFP4 forward: each x row is quantised as
+ * above, h = silu(x.Wg) * (x.Wu) is rounded to bf16 and each h row quantised
+ * again before the down projection; everything else is exact fp64. */
 void oracle_expert_ffn(const uint16_t *x, int64_t n, int64_t d, int64_t F,
                        const oracle_matrix *wg, const oracle_matrix *wu,
                        const oracle_matrix *wd, double *y);

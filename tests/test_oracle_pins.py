@@ -372,3 +372,149 @@ def test_replay_filter_properties():
     out, rep = oracle.filter_replay(lg, far, 1.0)
     assert (rep == k).all()
     assert np.array_equal(out, own)
+
+
+# ---- NVFP4 with per-token scales ----------------------------------------------
+# The format of the Composer 2 Technical Report, section 6.1 (Kernels): FP4 E2M1
+# values, an FP8 E4M3 scale per 16 values, an FP32 scale per token, IEEE
+# division in the quantiser.
+
+E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # the published E2M1 value set
+
+
+def test_e2m1_decode_is_the_published_value_set():
+    got = [oracle.e2m1_to_f64(c) for c in range(16)]
+    assert got[:8] == E2M1_MAGNITUDES
+    assert got[8:] == [-m for m in E2M1_MAGNITUDES]
+
+
+@pytest.mark.parametrize("v,code", [
+    (0.0, 0), (0.25, 0), (0.2500001, 1), (0.5, 1), (0.75, 2), (1.25, 2), (1.5, 3),
+    (1.75, 4), (2.5, 4), (2.51, 5), (3.5, 6), (5.0, 6), (5.0001, 7), (6.0, 7), (1e30, 7),
+    (-0.2, 0), (-0.3, 9), (-0.75, 10), (-3.5, 14), (-100.0, 15)])
+def test_e2m1_rounding_ties_to_even_and_saturates(v, code):
+    assert oracle.e2m1_round(v) == code
+
+
+def test_e4m3_rounding_matches_torch_float8_conversion():
+    rng = np.random.default_rng(0)
+    # random values over the whole range, every representable value, and the
+    # exact midpoints between neighbours (ties)
+    grid = np.array([oracle.e4m3_to_f64(b) for b in range(0x7F)], np.float64)
+    mids = (grid[1:] + grid[:-1]) / 2
+    v = np.concatenate([rng.uniform(0, 463.9, 4000), np.exp(rng.uniform(-12, 6, 4000)), grid, mids])
+    v = v[v < 464].astype(np.float32)   # torch turns 464 and above into NaN
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    got = np.array([oracle.e4m3_round(x) for x in v], np.uint8)
+    assert np.array_equal(got, ref)
+    # the quantiser's scales saturate at the largest finite value, 448
+    for x in (464.0, 500.0, 1e30):
+        assert oracle.e4m3_round(x) == 0x7E
+
+
+def test_round_bf16_matches_torch_on_fp32_inputs():
+    rng = np.random.default_rng(1)
+    v = np.concatenate([rng.standard_normal(3000) * 10.0 ** rng.integers(-30, 30, 3000),
+                        np.ldexp(1.0 + rng.integers(0, 256, 500) / 256 + 1 / 512, 3)])
+    v = v.astype(np.float32)
+    ref = torch.from_numpy(v).to(torch.bfloat16).double().numpy()
+    got = np.array([oracle.round_bf16(float(x)) for x in v])
+    assert np.array_equal(got, ref)
+
+
+def test_nvfp4_golden_hand_worked_rows():
+    with open(os.path.join(GOLDEN, "nvfp4_rows.json")) as f:
+        g = json.load(f)
+    for case in g["cases"]:
+        row = np.array(case["row"], np.float32)[None]
+        codes, bs, rs = oracle.nvfp4_quantize_rows(row)
+        assert float(rs[0]) == case["row_scale"], case["name"]
+        assert bs[0].tolist() == case["block_scales"], case["name"]
+        assert codes[0].tolist() == case["codes"], case["name"]
+
+
+def _dequant(codes, bs, rs):
+    tab = np.array([oracle.e2m1_to_f64(c) for c in range(16)])
+    sc = np.array([oracle.e4m3_to_f64(b) for b in range(256)])
+    return tab[codes] * np.repeat(sc[bs], 16, axis=1) * rs.astype(np.float64)[:, None]
+
+
+def test_nvfp4_quantiser_properties():
+    rng = np.random.default_rng(2)
+    R, K = 64, 256
+    mag = 10.0 ** rng.uniform(-6, 3, (R, 1))
+    x = f64(rand_bf16(rng, (R, K))) * mag
+    x = f64(bf16(x)).astype(np.float32)
+    x[5, 16:32] = 0.0                        # an all-zero block
+    codes, bs, rs = oracle.nvfp4_quantize_rows(x)
+    xq = _dequant(codes, bs, rs)
+    denom = np.repeat(np.array([[oracle.e4m3_to_f64(b) for b in r] for r in bs]), 16, 1) * rs[:, None]
+    # where the block scale is a normal E4M3 value, every value is within half
+    # an E2M1 step (at most 1 unit of its block's scale, the step between 4 and
+    # 6 being 2) of its input, up to the fp32 rounding of the quotient the
+    # code is decided on; a block's largest value overshoots 6 units by at
+    # most the scale's rounding, 1/16
+    normal_el = np.repeat(bs >= 8, 16, axis=1)
+    assert np.all((np.abs(xq - x) <= (1.0 + 1e-6) * denom)[normal_el])
+    assert normal_el.mean() > 0.9
+    # a block's largest magnitude becomes +-6 (E4M3 rounding of the block scale
+    # moves it by at most 1/16 relative, which stays nearest to 6)
+    blocks = np.abs(x).reshape(R, K // 16, 16)
+    arg = blocks.argmax(-1)
+    top = np.take_along_axis(codes.reshape(R, K // 16, 16), arg[..., None], -1)[..., 0]
+    normal = (bs >= 8) & (bs < 0x7E)
+    assert np.all((top[normal] & 7) == 7)
+    # the zero block has scale 0 and codes 0
+    assert bs[5, 1] == 0 and not codes[5, 16:32].any()
+    # rows are independent: a row quantised alone gives the same bytes
+    c1, b1, r1 = oracle.nvfp4_quantize_rows(x[7:8])
+    assert np.array_equal(c1[0], codes[7]) and np.array_equal(b1[0], bs[7]) and r1[0] == rs[7]
+    # scaling a row by a power of two scales only the row scale (exactly)
+    c2, b2, r2 = oracle.nvfp4_quantize_rows(np.ldexp(x, -3))
+    assert np.array_equal(c2, codes) and np.array_equal(b2, bs)
+    assert np.array_equal(r2, np.ldexp(rs, -3))
+
+
+def _nvfp4_matrix(w):
+    from deterministic_rl_gb300.synthetic import quantize_nvfp4
+    q, s, ts = quantize_nvfp4(torch.from_numpy(w.astype(np.float32)))
+    return Matrix(q.numpy(), s.numpy(), float(ts))
+
+
+def test_nvfp4_weight_decode_is_code_times_scales():
+    rng = np.random.default_rng(3)
+    m = _nvfp4_matrix(rng.standard_normal((8, 64)) * 0.02)
+    K = 64
+    for r, c in [(0, 0), (1, 1), (3, 17), (7, 63)]:
+        byte = m.values[r, c // 2]
+        code = (byte >> 4) if c & 1 else (byte & 15)
+        want = E2M1_MAGNITUDES[code & 7] * (-1 if code & 8 else 1) * \
+            float(torch.tensor([m.scales[r, c // 16]], dtype=torch.uint8).view(torch.float8_e4m3fn).double()) * \
+            float(np.float32(m.tscale))
+        assert m.elem(r, c) == want
+    assert m.K == K
+
+
+def test_nvfp4_expert_ffn_matches_torch_fp64_pipeline():
+    """The NVFP4 expert FFN: quantise the token rows (pinned above), the GEMMs
+    and SwiGLU in torch float64 on the quantised values, round h to bf16
+    (pinned above), quantise h, the down GEMM in torch float64."""
+    rng = np.random.default_rng(4)
+    n, d, F = 5, 64, 48
+    wg, wu, wd = (_nvfp4_matrix(rng.standard_normal(s) * 0.05) for s in ((F, d), (F, d), (d, F)))
+    ex = Expert(wg, wu, wd)
+    xb = rand_bf16(rng, (n, d))
+    got = oracle.expert_ffn(xb, ex)
+
+    def dense(m, rows, K):
+        return torch.tensor([[m.elem(r, c) for c in range(K)] for r in range(rows)], dtype=torch.float64)
+
+    G, U, D = dense(wg, F, d), dense(wu, F, d), dense(wd, d, F)
+    xq = torch.from_numpy(_dequant(*oracle.nvfp4_quantize_rows(f64(xb).astype(np.float32))))
+    g = xq @ G.T
+    u = xq @ U.T
+    h = torch.nn.functional.silu(g) * u
+    hb = np.array([[oracle.round_bf16(float(v)) for v in row] for row in h.numpy()], np.float32)
+    hq = torch.from_numpy(_dequant(*oracle.nvfp4_quantize_rows(hb)))
+    want = (hq @ D.T).numpy()
+    np.testing.assert_allclose(got, want, rtol=1e-12, atol=1e-15)
