@@ -29,6 +29,7 @@ MOE_ERR_UNSUPPORTED = 8
 
 MOE_W_BF16 = 0
 MOE_W_MXFP8 = 1
+MOE_W_NVFP4 = 2
 
 # Every function the header declares, in declaration order.
 EXPORTED = ("moe_workspace_size", "moe_workspace_layout", "moe_route", "moe_forward",
@@ -47,13 +48,13 @@ class moe_dims(ctypes.Structure):
 class moe_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w_router", "router_bias", "w_gate", "w_up", "w_down", "s_gate", "s_up",
-                 "s_down", "ws_gate", "ws_up", "ws_down")]
+                 "s_down", "ws_gate", "ws_up", "ws_down", "gs_gate", "gs_up", "gs_down")]
 
 
 class moe_ws_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("status", "logits", "valid", "cnt", "off", "perm", "inv", "xp", "h", "y",
-                 "ysh", "total")]
+                 "ysh", "xq", "sx", "sxp", "sh", "total")]
 
 
 class MoEError(RuntimeError):
@@ -134,9 +135,11 @@ class Dims:
 
 
 def make_weights(w_router, router_bias, w_gate, w_up, w_down, s_gate=None, s_up=None,
-                 s_down=None, ws_gate=None, ws_up=None, ws_down=None) -> moe_weights:
+                 s_down=None, ws_gate=None, ws_up=None, ws_down=None, gs_gate=None, gs_up=None,
+                 gs_down=None) -> moe_weights:
     return moe_weights(*(_p(t) for t in (w_router, router_bias, w_gate, w_up, w_down, s_gate,
-                                         s_up, s_down, ws_gate, ws_up, ws_down)))
+                                         s_up, s_down, ws_gate, ws_up, ws_down, gs_gate, gs_up,
+                                         gs_down)))
 
 
 def moe_workspace_size(dims: Dims) -> int:

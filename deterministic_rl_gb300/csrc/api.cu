@@ -21,6 +21,10 @@
 
 using namespace moe;
 
+static_assert(moe::WFMT_BF16 == MOE_W_BF16 && moe::WFMT_MXFP8 == MOE_W_MXFP8 &&
+                  moe::WFMT_NVFP4 == MOE_W_NVFP4,
+              "weight format codes match the ABI");
+
 namespace {
 
 constexpr uint64_t kWaitTimeoutNs = 1000000000ull;  // bounded device waits: 1 s
@@ -32,7 +36,9 @@ constexpr int kRouterSplit = 4;
 inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 struct Layout {
-    size_t status, logits, rpart, valid, cnt, off, perm, inv, scratch, xp, h, y, ysh, total;
+    size_t status, logits, rpart, valid, cnt, off, perm, inv, scratch, xp, h, y, ysh;
+    size_t xq, sx, sxp, sh;  // NVFP4 only
+    size_t total;
 };
 
 inline int router_split(const moe_dims* d) { return (d->d / BK) % kRouterSplit == 0 ? kRouterSplit : 1; }
@@ -45,8 +51,9 @@ bool dims_ok(const moe_dims* d) {
     if (d->d < 64 || d->d > 16384 || d->d % 64) return false;
     if (d->F < 64 || d->F > 16384 || d->F % 64) return false;
     if (d->n_shared < 0 || d->n_shared > 1) return false;
-    if (d->wfmt != MOE_W_BF16 && d->wfmt != MOE_W_MXFP8) return false;
-    if (d->wfmt == MOE_W_MXFP8 && (d->d % 512 || d->F % 512)) return false;
+    if (d->wfmt != MOE_W_BF16 && d->wfmt != MOE_W_MXFP8 && d->wfmt != MOE_W_NVFP4) return false;
+    // block-scaled weights: scale rows are loaded 8 k-blocks (512 along K) at a time
+    if (d->wfmt != MOE_W_BF16 && (d->d % 512 || d->F % 512)) return false;
     if (d->out_fp32 != 0 && d->out_fp32 != 1) return false;
     return true;
 }
@@ -70,6 +77,11 @@ Layout make_layout(const moe_dims* d) {
     L.h = take(rows * d->F * 2);
     L.y = take(T * k * d->d * 2);
     L.ysh = take(S ? T * d->d * 4 : 0);
+    const bool nv = d->wfmt == MOE_W_NVFP4;
+    L.xq = take(nv ? T * d->d * 2 : 0);
+    L.sx = take(nv ? T * 4 : 0);
+    L.sxp = take(nv ? T * k * 4 : 0);
+    L.sh = take(nv ? T * k * 4 : 0);
     L.total = o;
     return L;
 }
@@ -139,10 +151,11 @@ moe_status check_common(const moe_dims* d, const void* x, const moe_weights* w, 
 moe_status check_experts(const moe_dims* d, const moe_weights* w) {
     if (!w->w_gate || !w->w_up || !w->w_down) return MOE_ERR_ARG;
     if (!al16(w->w_gate) || !al16(w->w_up) || !al16(w->w_down)) return MOE_ERR_ALIGN;
-    if (d->wfmt == MOE_W_MXFP8) {
+    if (d->wfmt != MOE_W_BF16) {
         if (!w->s_gate || !w->s_up || !w->s_down) return MOE_ERR_ARG;
         if (!al16(w->s_gate) || !al16(w->s_up) || !al16(w->s_down)) return MOE_ERR_ALIGN;
     }
+    if (d->wfmt == MOE_W_NVFP4 && (!w->gs_gate || !w->gs_up || !w->gs_down)) return MOE_ERR_ARG;
     if (d->n_shared) {
         if (!w->ws_gate || !w->ws_up || !w->ws_down) return MOE_ERR_ARG;
         if (!al16(w->ws_gate) || !al16(w->ws_up) || !al16(w->ws_down)) return MOE_ERR_ALIGN;
@@ -268,12 +281,25 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     MOE_TRY(cu(launch_dispatch(ids, T, k, E, cnt, off, perm, inv,
                                reinterpret_cast<int32_t*>(ws + L.scratch), s)));
     MOE_TRY(mark(MOE_STAGE_DISPATCH, 1, s));
-    MOE_TRY(mark(MOE_STAGE_GATHER, 0, s));
-    MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), perm, T, k, d->d, S,
-                             reinterpret_cast<uint16_t*>(ws + L.xp), s)));
-    MOE_TRY(mark(MOE_STAGE_GATHER, 1, s));
     const int sms = num_sms();
     if (sms <= 0) return MOE_ERR_CUDA;
+    const bool nv = d->wfmt == MOE_W_NVFP4;
+    float* sxp = reinterpret_cast<float*>(ws + L.sxp);
+    float* sh = reinterpret_cast<float*>(ws + L.sh);
+    MOE_TRY(mark(MOE_STAGE_GATHER, 0, s));
+    if (nv) {
+        // NVFP4: each token row quantised once (per-token scale), then gathered
+        MOE_TRY(cu(launch_nvfp4_qdq(static_cast<const uint16_t*>(x),
+                                    reinterpret_cast<uint16_t*>(ws + L.xq), nullptr,
+                                    reinterpret_cast<float*>(ws + L.sx), T, d->d, sms, s)));
+        MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(ws + L.xq), perm, T, k, d->d, S,
+                                 reinterpret_cast<uint16_t*>(ws + L.xp), s,
+                                 reinterpret_cast<const float*>(ws + L.sx), sxp)));
+    } else {
+        MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), perm, T, k, d->d, S,
+                                 reinterpret_cast<uint16_t*>(ws + L.xp), s)));
+    }
+    MOE_TRY(mark(MOE_STAGE_GATHER, 1, s));
 
     const bool mx = d->wfmt == MOE_W_MXFP8;
     const bool one = one_sm_experts(d);
@@ -307,6 +333,15 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
         if (!make_map_u8(&p1.a1, w->w_up, d->d, EF, BK, rg)) return MOE_ERR_CUDA;
         if (!make_map_u8(&p1.sa0, w->s_gate, d->d / 32, EF, 16, rg)) return MOE_ERR_CUDA;
         if (!make_map_u8(&p1.sa1, w->s_up, d->d / 32, EF, 16, rg)) return MOE_ERR_CUDA;
+    } else if (nv) {
+        // 32 code bytes (64 values) per row and k-block; 32 scale bytes per 8 k-blocks
+        if (!make_map_u8(&p1.a0, w->w_gate, d->d / 2, EF, BK / 2, rg)) return MOE_ERR_CUDA;
+        if (!make_map_u8(&p1.a1, w->w_up, d->d / 2, EF, BK / 2, rg)) return MOE_ERR_CUDA;
+        if (!make_map_u8(&p1.sa0, w->s_gate, d->d / 16, EF, 32, rg)) return MOE_ERR_CUDA;
+        if (!make_map_u8(&p1.sa1, w->s_up, d->d / 16, EF, 32, rg)) return MOE_ERR_CUDA;
+        p1.row_scale = sxp;
+        p1.wscale0 = w->gs_gate;
+        p1.wscale1 = w->gs_up;
     } else {
         if (!make_map(&p1.a0, w->w_gate, d->d, EF, rg)) return MOE_ERR_CUDA;
         if (!make_map(&p1.a1, w->w_up, d->d, EF, rg)) return MOE_ERR_CUDA;
@@ -327,7 +362,7 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     const int g1 = static_cast<int>(tb < units ? tb : units);
     MOE_TRY(mark(MOE_STAGE_GATE_UP, 0, s));
     MOE_TRY(cu(one ? launch_grouped_gemm(GEMM_SWIGLU, p1, g1, s)
-                   : launch_pair_gemm(GEMM_SWIGLU, p1, g1, s, mx)));
+                   : launch_pair_gemm(GEMM_SWIGLU, p1, g1, s, d->wfmt)));
     MOE_TRY(mark(MOE_STAGE_GATE_UP, 1, s));
 
     // down projection -> Y (routed, bf16) and Ysh (shared, fp32)
@@ -337,6 +372,11 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     if (mx) {
         if (!make_map_u8(&p2.a0, w->w_down, d->F, ED, BK, BM)) return MOE_ERR_CUDA;
         if (!make_map_u8(&p2.sa0, w->s_down, d->F / 32, ED, 16, BM)) return MOE_ERR_CUDA;
+    } else if (nv) {
+        if (!make_map_u8(&p2.a0, w->w_down, d->F / 2, ED, BK / 2, BM)) return MOE_ERR_CUDA;
+        if (!make_map_u8(&p2.sa0, w->s_down, d->F / 16, ED, 32, BM)) return MOE_ERR_CUDA;
+        p2.row_scale = sh;
+        p2.wscale0 = w->gs_down;
     } else if (!make_map(&p2.a0, w->w_down, d->F, ED, BM)) {
         return MOE_ERR_CUDA;
     }
@@ -352,8 +392,12 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     tb = ntiles * p2.MT;
     const int g2 = static_cast<int>(tb < units ? tb : units);
     MOE_TRY(mark(MOE_STAGE_DOWN, 0, s));
+    if (nv)  // NVFP4: each row of h quantised in place (per-token scale)
+        MOE_TRY(cu(launch_nvfp4_qdq(reinterpret_cast<const uint16_t*>(ws + L.h),
+                                    reinterpret_cast<uint16_t*>(ws + L.h), nullptr, sh, T * k,
+                                    d->F, sms, s)));
     MOE_TRY(cu(one ? launch_grouped_gemm(GEMM_DOWN, p2, g2, s)
-                   : launch_pair_gemm(GEMM_DOWN, p2, g2, s, mx)));
+                   : launch_pair_gemm(GEMM_DOWN, p2, g2, s, d->wfmt)));
     MOE_TRY(mark(MOE_STAGE_DOWN, 1, s));
 
     MOE_TRY(mark(MOE_STAGE_COMBINE, 0, s));
@@ -374,8 +418,8 @@ moe_status forward_impl(const moe_dims* d, const void* x, const moe_weights* w,
     if (!out || !ids_out || !gates_out || (replay && !ids_in)) return MOE_ERR_ARG;
     if (!al16(out) || !al16(ids_out) || !al16(gates_out) || (replay && !al16(ids_in)))
         return MOE_ERR_ALIGN;
-    // MXFP8 expert weights: the shared expert (bf16 by definition) is not served.
-    if (d->wfmt == MOE_W_MXFP8 && d->n_shared) return MOE_ERR_UNSUPPORTED;
+    // Block-scaled expert weights: the shared expert (bf16 by definition) is not served.
+    if (d->wfmt != MOE_W_BF16 && d->n_shared) return MOE_ERR_UNSUPPORTED;
     const Layout L = make_layout(d);
     auto* s = reinterpret_cast<cudaStream_t>(stream);
     auto* wsb = static_cast<uint8_t*>(ws);
@@ -408,6 +452,10 @@ moe_status moe_workspace_layout(const moe_dims* dims, moe_ws_layout* out) {
     out->h = L.h;
     out->y = L.y;
     out->ysh = L.ysh;
+    out->xq = L.xq;
+    out->sx = L.sx;
+    out->sxp = L.sxp;
+    out->sh = L.sh;
     out->total = L.total;
     return MOE_OK;
 }

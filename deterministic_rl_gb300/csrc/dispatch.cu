@@ -192,12 +192,14 @@ __global__ void __launch_bounds__(32 * kSegWarps) dispatch_small_kernel(
 // the shared expert.  16-byte vectors; d % 8 == 0.
 __global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
                                    int64_t n_pairs, int k, int vec_per_row, int64_t rows_total,
-                                   uint4* __restrict__ xp) {
+                                   uint4* __restrict__ xp, const float* __restrict__ scale_in,
+                                   float* __restrict__ scale_out) {
     for (int64_t r = blockIdx.x; r < rows_total; r += gridDim.x) {
         const int64_t src = r < n_pairs ? perm[r] / k : r - n_pairs;
         const uint4* s = x + src * vec_per_row;
         uint4* dptr = xp + r * vec_per_row;
         for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dptr[v] = s[v];
+        if (scale_out && threadIdx.x == 0) scale_out[r] = scale_in[src];
     }
 }
 
@@ -231,14 +233,16 @@ cudaError_t launch_dispatch(const int32_t* ids, int64_t T, int k, int E, int32_t
 }
 
 cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int64_t T, int k, int d,
-                          int n_shared, uint16_t* xp, cudaStream_t s) {
+                          int n_shared, uint16_t* xp, cudaStream_t s, const float* scale_in,
+                          float* scale_out) {
     const int64_t n_pairs = T * k;
     const int64_t rows = n_pairs + (n_shared ? T : 0);
     if (rows == 0) return cudaSuccess;
     const int vpr = d / 8;
     const int64_t grid = rows < 148 * 16 ? rows : 148 * 16;
     gather_rows_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(
-        reinterpret_cast<const uint4*>(x), perm, n_pairs, k, vpr, rows, reinterpret_cast<uint4*>(xp));
+        reinterpret_cast<const uint4*>(x), perm, n_pairs, k, vpr, rows, reinterpret_cast<uint4*>(xp),
+        scale_in, scale_out);
     return cudaGetLastError();
 }
 

@@ -51,8 +51,15 @@ constexpr int kMaxGroups = 1024;
 // of two, convert whole k-blocks (group g takes k-blocks g, g+4, ...) into the
 // operand ring's A buffer, so several k-blocks are converted at once and HBM
 // latency never sits between a conversion and its MMA.
-template <int MODE, bool MX>
+// NV: expert weights stored as NVFP4 (E2M1 codes two per byte + one E4M3 scale
+// per 16 along K + one fp32 scale per matrix), converted the same way (a
+// 32-byte code row and four scale bytes per row and k-block); the token
+// operand arrives as bf16 e2m1 * e4m3 values (quantised per token) and the
+// epilogue scales each output by its token's and its matrix's fp32 scales.
+template <int MODE, int FMT>
 struct PCfg {
+    static constexpr bool kConv = FMT != WFMT_BF16;   // weights converted in-kernel
+    static constexpr bool kNv = FMT == WFMT_NVFP4;
     static constexpr bool kPair = MODE == GEMM_SWIGLU;      // 64 gate + 64 up rows per CTA
     static constexpr int kRowsCta = gemm_rows(MODE);        // output weight rows per CTA
     static constexpr int kRowsTile = 2 * kRowsCta;          // per CTA pair
@@ -63,21 +70,23 @@ struct PCfg {
     // (two large boxes; sixteen-row boxes cost more in TMA issue than the
     // exchange they save) and the up warps pass their values to the gate
     // warps through shared memory.
-    static constexpr bool kInterleave = kPair && MX;
-    static constexpr uint32_t kXBytes = kPair && !MX ? 2 * 32 * kXPad * 4 : 0;
+    static constexpr bool kInterleave = kPair && kConv;
+    static constexpr uint32_t kXBytes = kPair && !kConv ? 2 * 32 * kXPad * 4 : 0;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;  // operand ring entry
-    static constexpr int kStages = MX ? 5 : 6;
-    static constexpr uint32_t kF8Bytes = BM * BK;               // fp8 weight tile
-    static constexpr int kF8Stages = MX ? 5 : 0;
-    static constexpr uint32_t kScBytes = BM * 16;               // 8 k-blocks of scales
-    static constexpr int kScStages = MX ? 2 : 0;
+    static constexpr int kStages = kConv ? 5 : 6;
+    static constexpr uint32_t kF8RowBytes = kNv ? BK / 2 : BK;  // weight bytes per row and k-block
+    static constexpr uint32_t kF8Bytes = BM * kF8RowBytes;      // fp8 / fp4 weight tile
+    static constexpr int kF8Stages = kConv ? 5 : 0;
+    static constexpr int kScPerKb = kNv ? BK / 16 : BK / 32;   // scale bytes per row and k-block
+    static constexpr uint32_t kScBytes = BM * 8 * kScPerKb;     // 8 k-blocks of scales
+    static constexpr int kScStages = kConv ? 2 : 0;
     static constexpr uint32_t kRingBytes =
         kStages * kStageBytes + kF8Stages * kF8Bytes + kScStages * kScBytes;
     static constexpr int kBarriers = 2 * kStages + 2 * kF8Stages + 2 * kScStages + 9;
     static constexpr int kConvWarps = 8;
     static constexpr int kConvPerKb = 2;                        // warps per k-block
     static constexpr int kConvGroups = kConvWarps / kConvPerKb;  // k-blocks in flight
-    static constexpr int kThreads = MX ? 192 + 32 * kConvWarps + 32 : 192;
+    static constexpr int kThreads = kConv ? 192 + 32 * kConvWarps + 32 : 192;
     static constexpr int kFp8Warp = 6 + kConvWarps;
 };
 
@@ -232,10 +241,47 @@ __device__ __forceinline__ void e4m3x4_rebias(uint32_t w, uint32_t k, uint32_t& 
     hi = (prmt(w, 0xB3A2u) & 0x087F087Fu) * 16u + k;  // bytes 2, 3
 }
 
-template <int MODE, bool MX>
-__global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
+// Sixteen E2M1 codes (two words, element 2j in the low nibble of byte j) of
+// one block with E4M3 scale byte s -> sixteen bf16 values e2m1 * e4m3, exactly
+// (a product of at most 2 and 4 significant bits).  The eight magnitudes
+// times the scale form a table whose low and high bytes the codes select
+// with byte permutes (a code's three magnitude bits are a permute selector);
+// each code's sign bit is moved to its bf16 sign bit.  A NaN scale gives NaN.
+__device__ __forceinline__ uint32_t prmt2(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+__device__ __forceinline__ void e2m1x16_to_bf16(uint2 q, uint32_t s, uint4& o0, uint4& o1) {
+    const float Sf = __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(s), __NV_E4M3)));
+    // magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6 times the scale, as bf16 pairs
+    const uint32_t w01 = prmt2(0u, __float_as_uint(0.5f * Sf), 0x7632);
+    const uint32_t w23 = prmt2(__float_as_uint(Sf), __float_as_uint(1.5f * Sf), 0x7632);
+    const uint32_t w45 = prmt2(__float_as_uint(2.0f * Sf), __float_as_uint(3.0f * Sf), 0x7632);
+    const uint32_t w67 = prmt2(__float_as_uint(4.0f * Sf), __float_as_uint(6.0f * Sf), 0x7632);
+    const uint32_t lo0 = prmt2(w01, w23, 0x6420), hi0 = prmt2(w01, w23, 0x7531);  // entries 0..3
+    const uint32_t lo1 = prmt2(w45, w67, 0x6420), hi1 = prmt2(w45, w67, 0x7531);  // entries 4..7
+    uint32_t out[8];
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {  // four codes per step: word h/2, half h%2
+        const uint32_t w = h < 2 ? q.x : q.y;
+        const uint32_t codes = (h & 1) ? (w >> 16) : w;
+        const uint32_t sel = codes & 0x7777u;
+        const uint32_t L = prmt2(lo0, lo1, sel), H = prmt2(hi0, hi1, sel);
+        // signs of codes 0..3 sit at bits 3, 7, 11, 15 of `codes`
+        out[2 * h] = prmt2(L, H, 0x5140) | ((codes << 12) & 0x8000u) | ((codes << 24) & 0x80000000u);
+        out[2 * h + 1] = prmt2(L, H, 0x7362) | ((codes << 4) & 0x8000u) | ((codes << 16) & 0x80000000u);
+    }
+    o0 = make_uint4(out[0], out[1], out[2], out[3]);
+    o1 = make_uint4(out[4], out[5], out[6], out[7]);
+}
+
+template <int MODE, int FMT>
+__global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
     pair_gemm_kernel(const __grid_constant__ GemmParams p) {
-    using C = PCfg<MODE, MX>;
+    using C = PCfg<MODE, FMT>;
+    constexpr bool MX = C::kConv;  // converter warps feed the A operand
     constexpr int kStages = C::kStages;
     constexpr uint32_t kStageBytes = C::kStageBytes;
     extern __shared__ uint8_t smem_raw[];
@@ -486,10 +532,11 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                             uint8_t* sc = scring + ss * C::kScBytes;
                             mbar_arrive_expect_tx(&scfull[ss], C::kScBytes);
                             if constexpr (C::kPair) {
-                                tma_load_2d(sc, &p.sa0, &scfull[ss], kb * 2, tl.arow, pol_w);
-                                tma_load_2d(sc + C::kScBytes / 2, &p.sa1, &scfull[ss], kb * 2, tl.arow, pol_w);
+                                tma_load_2d(sc, &p.sa0, &scfull[ss], kb * C::kScPerKb, tl.arow, pol_w);
+                                tma_load_2d(sc + C::kScBytes / 2, &p.sa1, &scfull[ss], kb * C::kScPerKb,
+                                            tl.arow, pol_w);
                             } else {
-                                tma_load_2d(sc, &p.sa0, &scfull[ss], kb * 2, tl.arow, pol_w);
+                                tma_load_2d(sc, &p.sa0, &scfull[ss], kb * C::kScPerKb, tl.arow, pol_w);
                             }
                             s_issued |= 1u << ss;
                             s_par = (s_par & ~(1u << ss)) | (sph << ss);
@@ -506,10 +553,11 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                         uint8_t* f8 = f8ring + fs * C::kF8Bytes;
                         mbar_arrive_expect_tx(&f8full[fs], C::kF8Bytes);
                         if constexpr (C::kPair) {
-                            tma_load_2d(f8, &p.a0, &f8full[fs], kb * BK, tl.arow, pol_w);
-                            tma_load_2d(f8 + C::kF8Bytes / 2, &p.a1, &f8full[fs], kb * BK, tl.arow, pol_w);
+                            tma_load_2d(f8, &p.a0, &f8full[fs], kb * C::kF8RowBytes, tl.arow, pol_w);
+                            tma_load_2d(f8 + C::kF8Bytes / 2, &p.a1, &f8full[fs], kb * C::kF8RowBytes,
+                                        tl.arow, pol_w);
                         } else {
-                            tma_load_2d(f8, &p.a0, &f8full[fs], kb * BK, tl.arow, pol_w);
+                            tma_load_2d(f8, &p.a0, &f8full[fs], kb * C::kF8RowBytes, tl.arow, pol_w);
                         }
                         f_issued |= 1u << fs;
                         f_par = (f_par & ~(1u << fs)) | (fph << fs);
@@ -576,22 +624,28 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                 for (int it = 0; it < (kRowsPerWarp * 4) / 32; ++it) {
                     const int task = sub * kRowsPerWarp * 4 + it * 32 + lane;
                     const int r = task >> 2, c2 = (task & 3) * 2;
-                    const uint4 q = *reinterpret_cast<const uint4*>(f8 + r * 64 + c2 * 8);
-                    const uint32_t sbyte = sc[r * 16 + kb8 * 2 + (c2 >> 2)];
                     uint4 o0, o1;
-                    const uint32_t kk = ((sbyte - 7u) << 7) * 0x00010001u;
-                    e4m3x4_rebias(q.x, kk, o0.x, o0.y);
-                    e4m3x4_rebias(q.y, kk, o0.z, o0.w);
-                    e4m3x4_rebias(q.z, kk, o1.x, o1.y);
-                    e4m3x4_rebias(q.w, kk, o1.z, o1.w);
-                    const uint32_t special = e4m3x4_special(q.x) | e4m3x4_special(q.y) |
-                                             e4m3x4_special(q.z) | e4m3x4_special(q.w) |
-                                             ((sbyte - 7u) > 239u);  // s outside [7, 246]
-                    if (special) {  // rare: exact float route for all 16 values
-                        e4m3x4_to_bf16x4(q.x, sbyte, o0.x, o0.y);
-                        e4m3x4_to_bf16x4(q.y, sbyte, o0.z, o0.w);
-                        e4m3x4_to_bf16x4(q.z, sbyte, o1.x, o1.y);
-                        e4m3x4_to_bf16x4(q.w, sbyte, o1.z, o1.w);
+                    if constexpr (C::kNv) {
+                        // block c2 / 2 of the row: 8 code bytes, one scale byte
+                        const uint2 q = *reinterpret_cast<const uint2*>(f8 + r * 32 + c2 * 4);
+                        e2m1x16_to_bf16(q, sc[r * 32 + kb8 * 4 + (c2 >> 1)], o0, o1);
+                    } else {
+                        const uint4 q = *reinterpret_cast<const uint4*>(f8 + r * 64 + c2 * 8);
+                        const uint32_t sbyte = sc[r * 16 + kb8 * 2 + (c2 >> 2)];
+                        const uint32_t kk = ((sbyte - 7u) << 7) * 0x00010001u;
+                        e4m3x4_rebias(q.x, kk, o0.x, o0.y);
+                        e4m3x4_rebias(q.y, kk, o0.z, o0.w);
+                        e4m3x4_rebias(q.z, kk, o1.x, o1.y);
+                        e4m3x4_rebias(q.w, kk, o1.z, o1.w);
+                        const uint32_t special = e4m3x4_special(q.x) | e4m3x4_special(q.y) |
+                                                 e4m3x4_special(q.z) | e4m3x4_special(q.w) |
+                                                 ((sbyte - 7u) > 239u);  // s outside [7, 246]
+                        if (special) {  // rare: exact float route for all 16 values
+                            e4m3x4_to_bf16x4(q.x, sbyte, o0.x, o0.y);
+                            e4m3x4_to_bf16x4(q.y, sbyte, o0.z, o0.w);
+                            e4m3x4_to_bf16x4(q.z, sbyte, o1.x, o1.y);
+                            e4m3x4_to_bf16x4(q.w, sbyte, o1.z, o1.w);
+                        }
                     }
                     // operand row: gate/up rows alternate in 16-row blocks
                     // (the low 3 bits, which pick the swizzle, are r's)
@@ -644,9 +698,15 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
             const bool row_ok = row < p.M;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
+            // NVFP4: the matrices' fp32 scales for this group
+            const float ws0 = C::kNv ? p.wscale0[tl.g] : 1.0f;
+            const float ws1 = C::kNv && C::kPair ? p.wscale1[tl.g] : 1.0f;
             // One chunk of 32 accumulator columns (tokens c0 .. c0 + 31);
             // false when a wait of the bf16 gate/up handoff ran out.
             auto chunk = [&](const float (&v)[32], int c0) -> bool {
+                // NVFP4: lane j holds the fp32 scale of the chunk's token j
+                const float tok_scale = C::kNv && c0 + lane < tl.n_valid
+                                            ? p.row_scale[tl.brow + c0 + lane] : 0.0f;
                 if constexpr (C::kInterleave) {
                     __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out);
                     const int cb = c0 + (up_lane ? 16 : 0);
@@ -654,8 +714,13 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                     for (int j = 0; j < 16; ++j) {
                         const float lo = v[j], hi = v[16 + j];
                         const float other = __shfl_xor_sync(0xffffffffu, up_lane ? lo : hi, 16);
-                        const float g = up_lane ? other : lo;
-                        const float u = up_lane ? hi : other;
+                        float g = up_lane ? other : lo;
+                        float u = up_lane ? hi : other;
+                        if constexpr (C::kNv) {
+                            const float st = __shfl_sync(0xffffffffu, tok_scale, cb - c0 + j);
+                            g *= st * ws0;
+                            u *= st * ws1;
+                        }
                         if (row_ok && cb + j < tl.n_valid) {
                             const float h = g / (1.0f + expf(-g)) * u;
                             H[static_cast<int64_t>(tl.brow + cb + j) * p.ldo + row] =
@@ -706,10 +771,13 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
                     } else {
                         __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j)
+                        for (int j = 0; j < 32; ++j) {
+                            float y = v[j];
+                            if constexpr (C::kNv) y *= __shfl_sync(0xffffffffu, tok_scale, j) * ws0;
                             if (row_ok && c0 + j < tl.n_valid)
                                 Y[static_cast<int64_t>(tl.brow + c0 + j) * p.ldo + row] =
-                                    __float2bfloat16_rn(v[j]);
+                                    __float2bfloat16_rn(y);
+                        }
                     }
                 }
                 return true;
@@ -744,24 +812,24 @@ __global__ void __launch_bounds__(PCfg<MODE, MX>::kThreads, 1)
     }
 }
 
-template <int MODE, bool MX>
+template <int MODE, int FMT>
 size_t pair_smem_bytes(int GG) {
-    using C = PCfg<MODE, MX>;
+    using C = PCfg<MODE, FMT>;
     return 1024 + C::kRingBytes + C::kXBytes + C::kBarriers * 8 + 16 +
            static_cast<size_t>(4 * GG + 2) * 4;
 }
 
-template <int MODE, bool MX>
+template <int MODE, int FMT>
 cudaError_t launch_pair_mode(const GemmParams& p, int clusters, cudaStream_t s) {
     const int GG = p.G + p.has_shared;
-    const size_t smem = pair_smem_bytes<MODE, MX>(GG);
-    cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<MODE, MX>,
+    const size_t smem = pair_smem_bytes<MODE, FMT>(GG);
+    cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<MODE, FMT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(PCfg<MODE, MX>::kThreads, 1, 1);
+    cfg.blockDim = dim3(PCfg<MODE, FMT>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -774,29 +842,35 @@ cudaError_t launch_pair_mode(const GemmParams& p, int clusters, cudaStream_t s) 
     // Persistent clusters: never more than can be resident at once, so that no
     // cluster's share of the static tile order waits for a second wave.
     int resident = 0;
-    e = cudaOccupancyMaxActiveClusters(&resident, pair_gemm_kernel<MODE, MX>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&resident, pair_gemm_kernel<MODE, FMT>, &cfg);
     if (e != cudaSuccess) return e;
     if (resident <= 0) return cudaErrorInvalidConfiguration;
     if (clusters > resident) {
         clusters = resident;
         cfg.gridDim = dim3(2 * clusters, 1, 1);
     }
-    return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<MODE, MX>, p);
+    return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<MODE, FMT>, p);
 }
 
 }  // namespace
 
 cudaError_t launch_pair_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s,
-                             int mxfp8) {
+                             int wfmt) {
     if (p.G + p.has_shared > kMaxGroups || clusters <= 0 || !p.cnt || !p.off)
         return cudaErrorInvalidValue;
-    if (mxfp8 && p.has_shared) return cudaErrorInvalidValue;  // shared expert is bf16
-    if (mode == GEMM_SWIGLU)
-        return mxfp8 ? launch_pair_mode<GEMM_SWIGLU, true>(p, clusters, s)
-                     : launch_pair_mode<GEMM_SWIGLU, false>(p, clusters, s);
-    if (mode == GEMM_DOWN)
-        return mxfp8 ? launch_pair_mode<GEMM_DOWN, true>(p, clusters, s)
-                     : launch_pair_mode<GEMM_DOWN, false>(p, clusters, s);
+    if (wfmt != WFMT_BF16 && p.has_shared) return cudaErrorInvalidValue;  // shared expert is bf16
+    if (wfmt == WFMT_NVFP4 && (!p.row_scale || !p.wscale0 || (mode == GEMM_SWIGLU && !p.wscale1)))
+        return cudaErrorInvalidValue;
+    if (mode == GEMM_SWIGLU) {
+        if (wfmt == WFMT_MXFP8) return launch_pair_mode<GEMM_SWIGLU, WFMT_MXFP8>(p, clusters, s);
+        if (wfmt == WFMT_NVFP4) return launch_pair_mode<GEMM_SWIGLU, WFMT_NVFP4>(p, clusters, s);
+        return launch_pair_mode<GEMM_SWIGLU, WFMT_BF16>(p, clusters, s);
+    }
+    if (mode == GEMM_DOWN) {
+        if (wfmt == WFMT_MXFP8) return launch_pair_mode<GEMM_DOWN, WFMT_MXFP8>(p, clusters, s);
+        if (wfmt == WFMT_NVFP4) return launch_pair_mode<GEMM_DOWN, WFMT_NVFP4>(p, clusters, s);
+        return launch_pair_mode<GEMM_DOWN, WFMT_BF16>(p, clusters, s);
+    }
     return cudaErrorInvalidValue;
 }
 

@@ -23,6 +23,10 @@ constexpr int BK = 64;
 // up projection, four times, so that each epilogue warp's 32 accumulator lanes
 // hold both halves of 16 rows.
 constexpr int kSwigluBlock = 16;
+// Expert weight storage formats (the values of the ABI's moe_wfmt).
+constexpr int WFMT_BF16 = 0;
+constexpr int WFMT_MXFP8 = 1;
+constexpr int WFMT_NVFP4 = 2;
 
 // Device status word bits (ws status[0]); status[1] = id of the kernel whose
 // wait ran out, status[2] = number of tokens with rejected replay ids.
@@ -66,16 +70,25 @@ struct GemmParams {
     int32_t ksplit;      // one-SM kernel: K split into this many fixed parts (0/1: none);
                          // part s goes to out + s * split_stride (no bias)
     int64_t split_stride;
+    // NVFP4: fp32 scale of each token row of B (applied to its output column),
+    // and the per-group fp32 scales of the weight matrices (a0 and a1).
+    const float* row_scale;
+    const float* wscale0;
+    const float* wscale1;
 };
 
 size_t gemm_smem_bytes(int mode, int n_groups_total);
 cudaError_t launch_grouped_gemm(int mode, const GemmParams& p, int grid, cudaStream_t s);
 // The expert GEMMs (GEMM_SWIGLU, GEMM_DOWN) on 2-CTA clusters (cta_group::2):
 // `clusters` pairs of SMs; M is split in tiles of 2 * gemm_rows(mode) rows.
-// mxfp8 != 0: a0/a1 are E4M3 weight maps (64-byte boxes) with scale maps
+// wfmt WFMT_MXFP8: a0/a1 are E4M3 weight maps (64-byte boxes) with scale maps
 // sa0/sa1; the kernel dequantises them exactly to bf16 in shared memory.
+// wfmt WFMT_NVFP4: a0/a1 are packed E2M1 maps (32-byte boxes) with E4M3
+// scale maps sa0/sa1 (32-byte boxes, one per 16 values); the kernel
+// dequantises them exactly to bf16 and scales each output by row_scale of its
+// token times the group's weight scale.
 cudaError_t launch_pair_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s,
-                             int mxfp8 = 0);
+                             int wfmt = 0);
 
 // Routing: top-k selection (own mode) or replay validation, then gate weights.
 cudaError_t launch_topk_gates(const float* logits, int64_t T, int E, int k,
@@ -98,8 +111,16 @@ size_t dispatch_scratch_bytes(int64_t n_pairs, int E);
 cudaError_t launch_dispatch(const int32_t* ids, int64_t T, int k, int E, int32_t* cnt,
                             int32_t* off, int32_t* perm, int32_t* inv, int32_t* scratch,
                             cudaStream_t s);
+// scale_in/scale_out (NVFP4): also copy each gathered row's fp32 scale.
 cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int64_t T, int k, int d,
-                          int n_shared, uint16_t* xp, cudaStream_t s);
+                          int n_shared, uint16_t* xp, cudaStream_t s,
+                          const float* scale_in = nullptr, float* scale_out = nullptr);
+
+// NVFP4 activations (per-token scales): quantise R rows of K bf16 values and
+// write the bf16 values e2m1 * e4m3 block scale (exact) to dst (may be src),
+// the fp32 row scales to rscale and, if not null, the E4M3 block scales.
+cudaError_t launch_nvfp4_qdq(const uint16_t* src, uint16_t* dst, uint8_t* bscale, float* rscale,
+                             int64_t R, int K, int sms, cudaStream_t s);
 
 // Fixed-order combine of each token's k expert rows and the shared row.
 cudaError_t launch_combine(const uint16_t* y, const float* ysh, const int32_t* inv,

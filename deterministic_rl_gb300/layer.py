@@ -13,17 +13,22 @@ from . import binding as B
 class MoELayer:
     def __init__(self, w_router, w_gate, w_up, w_down, *, k: int = 8, router_bias=None,
                  s_gate=None, s_up=None, s_down=None, ws_gate=None, ws_up=None, ws_down=None,
-                 out_fp32: bool = False):
+                 gs_gate=None, gs_up=None, gs_down=None, out_fp32: bool = False):
+        """Weight formats: bf16 (s_* None); MXFP8 (s_* E8M0 scales); NVFP4
+        (gs_* per-matrix fp32 scales given; w_* packed E2M1, s_* E4M3)."""
         self.E, self.d = w_router.shape
         self.F = w_gate.shape[1]
         self.k = k
         self.n_shared = 1 if ws_gate is not None else 0
-        self.wfmt = B.MOE_W_MXFP8 if s_gate is not None else B.MOE_W_BF16
+        if gs_gate is not None:
+            self.wfmt = B.MOE_W_NVFP4
+        else:
+            self.wfmt = B.MOE_W_MXFP8 if s_gate is not None else B.MOE_W_BF16
         self.out_fp32 = bool(out_fp32)
         self.device = w_router.device
         # keep references so the pointers stay valid
         self._tensors = (w_router, router_bias, w_gate, w_up, w_down, s_gate, s_up, s_down,
-                         ws_gate, ws_up, ws_down)
+                         ws_gate, ws_up, ws_down, gs_gate, gs_up, gs_down)
         self.weights = B.make_weights(*self._tensors)
         self._ws = None
         self._ws_T = -1
@@ -33,7 +38,8 @@ class MoELayer:
         return cls(inp.w_router, inp.w_gate, inp.w_up, inp.w_down, k=inp.cfg.k,
                    router_bias=inp.router_bias, s_gate=inp.s_gate, s_up=inp.s_up,
                    s_down=inp.s_down, ws_gate=inp.ws_gate, ws_up=inp.ws_up,
-                   ws_down=inp.ws_down, out_fp32=out_fp32)
+                   ws_down=inp.ws_down, gs_gate=inp.gs_gate, gs_up=inp.gs_up,
+                   gs_down=inp.gs_down, out_fp32=out_fp32)
 
     def dims(self, T: int) -> B.Dims:
         return B.Dims(T, self.d, self.E, self.k, self.F, self.n_shared, self.wfmt,
@@ -106,4 +112,9 @@ class MoELayer:
         }
         if self.n_shared:
             r["ysh"] = view(L.ysh, T * d, torch.float32).view(T, d)
+        if self.wfmt == B.MOE_W_NVFP4:
+            r["xq"] = view(L.xq, T * d, torch.bfloat16).view(T, d)
+            r["sx"] = view(L.sx, T, torch.float32)
+            r["sxp"] = view(L.sxp, T * k, torch.float32)
+            r["sh"] = view(L.sh, T * k, torch.float32)
         return r

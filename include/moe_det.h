@@ -77,9 +77,16 @@ typedef enum {
 
 typedef enum {
     MOE_W_BF16 = 0,   /* expert weights stored as bf16                        */
-    MOE_W_MXFP8 = 1   /* expert weights E4M3 + one E8M0 scale per 32 along K
+    MOE_W_MXFP8 = 1,  /* expert weights E4M3 + one E8M0 scale per 32 along K
                          ([TR] §6.1: the MXFP8 format); router and shared
                          expert stay bf16                                     */
+    MOE_W_NVFP4 = 2   /* the NVFP4 forward ([TR] §6.1, Kernels): expert
+                         weights E2M1 (two per byte) + one E4M3 scale per 16
+                         along K + one fp32 scale per matrix; the token rows
+                         entering each expert GEMM (x, and the SwiGLU
+                         activations h in bf16) are quantised to E2M1 with an
+                         E4M3 scale per 16 and an fp32 scale per token, with
+                         IEEE division.  Router stays bf16; no shared expert */
 } moe_wfmt;
 
 /* Layer shape.  T tokens, hidden size d, E routed experts, k experts per
@@ -104,7 +111,12 @@ typedef struct {
  *   w_down    [E][d][F]            down projection
  *     bf16 for MOE_W_BF16; E4M3 bytes for MOE_W_MXFP8 with
  *   s_gate, s_up [E][F][d/32], s_down [E][d][F/32]  E8M0 scale bytes
- *     (NULL for MOE_W_BF16)
+ *     (NULL for MOE_W_BF16);
+ *     for MOE_W_NVFP4 w_gate, w_up [E][F][d/2], w_down [E][d][F/2] bytes of
+ *     two E2M1 codes (element 2j in the low nibble of byte j) with
+ *   s_gate, s_up [E][F][d/16], s_down [E][d][F/16]  E4M3 scale bytes and
+ *   gs_gate, gs_up, gs_down [E] fp32  one scale per expert matrix
+ *     (NULL unless MOE_W_NVFP4); element = e2m1 * e4m3 * gs
  *   ws_gate, ws_up [F][d], ws_down [d][F]  bf16 shared expert (NULL when
  *     n_shared == 0) */
 typedef struct {
@@ -119,6 +131,9 @@ typedef struct {
     const void *ws_gate;
     const void *ws_up;
     const void *ws_down;
+    const float *gs_gate;
+    const float *gs_up;
+    const float *gs_down;
 } moe_weights;
 
 /* Byte offsets of the intermediate buffers inside the workspace, for
@@ -137,9 +152,16 @@ typedef struct {
  *   h        bf16 [T*k + T*n_shared][F]  SwiGLU activations
  *   y        bf16 [T*k][d]               routed expert outputs (dst order)
  *   ysh      fp32 [T][d]                 shared expert output
+ *   MOE_W_NVFP4 only (else empty):
+ *   xq       bf16 [T][d]   each token row quantised: e2m1 * e4m3 block scale
+ *   sx       fp32 [T]      each token row's fp32 scale
+ *   sxp      fp32 [T*k]    the scale of each gathered row of xp
+ *   sh       fp32 [T*k]    the scale of each row of h (h itself then holds
+ *                          e2m1 * e4m3 of the quantised activations)
  * Offsets are 256-byte aligned; `total` equals moe_workspace_size(dims). */
 typedef struct {
     size_t status, logits, valid, cnt, off, perm, inv, xp, h, y, ysh;
+    size_t xq, sx, sxp, sh;
     size_t total;
 } moe_ws_layout;
 

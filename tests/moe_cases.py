@@ -31,9 +31,11 @@ REL_FRO = 5e-3
 MAX_ABS = 3e-2
 
 
-def _mat(w: torch.Tensor, s) -> Matrix:
+def _mat(w: torch.Tensor, s, gs=None) -> Matrix:
     if w.dtype == torch.bfloat16:
         return Matrix(bf16_bits(w))
+    if gs is not None:  # NVFP4: packed E2M1, E4M3 scales per 16, fp32 matrix scale
+        return Matrix(u8(w), u8(s), float(gs))
     return Matrix(u8(w), u8(s))
 
 
@@ -42,7 +44,10 @@ def expert_getter(inp):
         sg = inp.s_gate[e] if inp.s_gate is not None else None
         su = inp.s_up[e] if inp.s_up is not None else None
         sd = inp.s_down[e] if inp.s_down is not None else None
-        return Expert(_mat(inp.w_gate[e], sg), _mat(inp.w_up[e], su), _mat(inp.w_down[e], sd))
+        nv = inp.gs_gate is not None
+        return Expert(_mat(inp.w_gate[e], sg, inp.gs_gate[e] if nv else None),
+                      _mat(inp.w_up[e], su, inp.gs_up[e] if nv else None),
+                      _mat(inp.w_down[e], sd, inp.gs_down[e] if nv else None))
     return get
 
 

@@ -1,0 +1,138 @@
+"""The NVFP4 forward with per-token scales (Composer 2 Technical Report, §6.1,
+Kernels: BF16 values quantised to FP4 E2M1 with an FP8 E4M3 scale per 16 and
+an FP32 scale per token, IEEE division in the quantiser) on the GPU:
+  * the token-row quantiser, bitwise against the oracle's (both take their
+    rounding decisions on the same fp32 quotients);
+  * the layer against the oracle (which quantises its own h, rounded to bf16,
+    the same way);
+  * batch invariance, bitwise: a token's scales depend on that token only."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deterministic_rl_gb300 import build, MoELayer
+from deterministic_rl_gb300 import binding as B
+from deterministic_rl_gb300.synthetic import CONFIGS, bf16_bits, make_layer
+import moe_cases as mc
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    oracle.build()
+
+
+def small_nv(T=300, E=32, seed=51):
+    return CONFIGS["c6_nvfp4"].with_(name=f"nv_T{T}", seed=seed, T=T, d=512, E=E, F=512)
+
+
+def _expect_quantised(x_bf16: torch.Tensor):
+    """The oracle's quantisation of bf16 rows: (values e2m1 * e4m3 as fp64,
+    row scales fp32, block scales)."""
+    xf = torch.from_numpy(bf16_bits(x_bf16).view(np.int16)).view(torch.bfloat16).float().numpy()
+    codes, bs, rs = oracle.nvfp4_quantize_rows(xf)
+    tab = np.array([oracle.e2m1_to_f64(c) for c in range(16)])
+    sc = np.array([oracle.e4m3_to_f64(b) for b in range(256)])
+    return tab[codes] * np.repeat(sc[bs], 16, axis=1), rs, bs
+
+
+@pytest.mark.parametrize("T", [1, 37, 300])
+def test_token_quantiser_bitwise_against_oracle(T):
+    inp = make_layer(small_nv(T), "cuda")
+    # rows of very different magnitudes, an all-zero row, a row with an all-zero block
+    x = inp.x.float() * torch.logspace(-4, 4, T, device="cuda").unsqueeze(1)
+    if T > 1:
+        x[0, :] = 0
+    if T > 2:
+        x[2, 32:48] = 0
+    x = x.to(torch.bfloat16).contiguous()
+    layer = MoELayer.from_inputs(inp, out_fp32=True)
+    layer.forward(x)
+    assert layer.status() == B.MOE_OK
+    im = layer.intermediates(T)
+    vals, rs, _ = _expect_quantised(x)
+    got = im["xq"].double().cpu().numpy()
+    assert np.array_equal(got, vals)
+    assert np.array_equal(im["sx"].cpu().numpy(), rs)
+
+
+def test_gathered_rows_carry_their_token_scale():
+    inp = make_layer(small_nv(200), "cuda")
+    layer = MoELayer.from_inputs(inp, out_fp32=True)
+    _, ids, _ = layer.forward(inp.x)
+    im = layer.intermediates(200)
+    perm = im["perm"].long()
+    tok = perm // 8
+    assert torch.equal(im["sxp"], im["sx"][tok])
+    assert torch.equal(im["xp"][: 200 * 8], im["xq"][tok])
+
+
+def test_activation_rows_are_quantised_values():
+    """h after the call holds e2m1 * e4m3 of each row's quantisation: every
+    16-value block is a set of E2M1 magnitudes times one E4M3 scale, and the
+    row scales are the rows' amax / 2688 up to that quantisation."""
+    inp = make_layer(small_nv(64), "cuda")
+    layer = MoELayer.from_inputs(inp, out_fp32=True)
+    layer.forward(inp.x)
+    im = layer.intermediates(64)
+    h = im["h"].float().cpu().numpy().reshape(-1, 16)
+    sh = im["sh"].cpu().numpy()
+    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    e4m3 = np.array([oracle.e4m3_to_f64(b) for b in range(0x7F)])
+    bmax = np.abs(h).max(axis=1)
+    nz = bmax > 0
+    # the largest value of a nonzero block is 6 x its E4M3 scale (see the
+    # oracle's pins: a block's largest magnitude becomes 6)
+    S = bmax[nz] / 6.0
+    exact = np.isin(S, e4m3)
+    assert exact.mean() > 0.99
+    ratio = np.abs(h[nz][exact]) / S[exact][:, None]
+    assert np.isin(ratio, mags).all()
+    assert (sh >= 0).all() and (sh > 0).mean() > 0.99
+
+
+@pytest.mark.parametrize("T,E", [(1, 16), (130, 32), (300, 32)])
+def test_nvfp4_layer_matches_oracle(T, E):
+    inp = make_layer(small_nv(T, E), "cuda")
+    layer = MoELayer.from_inputs(inp, out_fp32=True)
+    out, ids, gates = layer.forward(inp.x)
+    assert layer.status() == B.MOE_OK
+    ref = mc.oracle_layer(inp)
+    g_ids = ids.cpu().numpy()
+    ok = mc.check_ids(g_ids, ref.logits, 8)
+    ref_r = mc.oracle_layer(inp, replay_ids=g_ids) if not ok.all() else ref
+    mc.check_gates(gates.cpu().numpy(), ref_r.gates)
+    mc.check_out(out.cpu().numpy(), ref_r.out)
+
+
+def test_nvfp4_batch_invariance_and_determinism():
+    inp = make_layer(small_nv(1000, seed=53), "cuda")
+    layer = MoELayer.from_inputs(inp, out_fp32=True)
+    full = [t.clone() for t in layer.forward(inp.x)]
+    again = layer.forward(inp.x)
+    for a, b in zip(full, again):
+        assert torch.equal(a, b)
+    for lo, hi in ((0, 1), (0, 130), (500, 1000), (17, 40)):
+        part = layer.forward(inp.x[lo:hi].contiguous())
+        for a, b in zip(full, part):
+            assert torch.equal(a[lo:hi], b)
+
+
+def test_nvfp4_rejects_shared_expert_and_missing_scales():
+    inp = make_layer(small_nv(8), "cuda")
+    layer = MoELayer.from_inputs(inp)
+    out, ids, gates = layer.outputs(8)
+    dims = layer.dims(8)
+    dims.n_shared = 1
+    sh = torch.zeros((512, 512), dtype=torch.bfloat16, device="cuda")
+    w = B.make_weights(inp.w_router, None, inp.w_gate, inp.w_up, inp.w_down, inp.s_gate,
+                       inp.s_up, inp.s_down, sh, sh, sh, inp.gs_gate, inp.gs_up, inp.gs_down)
+    ws = torch.empty(B.moe_workspace_size(dims), dtype=torch.uint8, device="cuda")
+    assert B.moe_forward(dims, inp.x, w, out, ids, gates, ws, check=False) == B.MOE_ERR_UNSUPPORTED
+    w2 = B.make_weights(inp.w_router, None, inp.w_gate, inp.w_up, inp.w_down, inp.s_gate,
+                        inp.s_up, inp.s_down)
+    assert B.moe_forward(layer.dims(8), inp.x, w2, out, ids, gates, layer.workspace(8),
+                         check=False) == B.MOE_ERR_ARG
