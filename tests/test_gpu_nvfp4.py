@@ -136,3 +136,25 @@ def test_nvfp4_rejects_shared_expert_and_missing_scales():
                         inp.s_up, inp.s_down)
     assert B.moe_forward(layer.dims(8), inp.x, w2, out, ids, gates, layer.workspace(8),
                          check=False) == B.MOE_ERR_ARG
+
+
+def test_nvfp4_full_size_sampled_parity_and_invariance():
+    """The 16,384-token NVFP4 layer (d=7168, E=384, F=2048): a 512-token
+    sub-batch gives its rows bitwise, the token quantiser matches the oracle
+    on sampled rows bitwise, and sampled tokens match the oracle layer."""
+    cfg = CONFIGS["c6_nvfp4"]
+    inp = make_layer(cfg, "cuda")
+    layer = MoELayer.from_inputs(inp, out_fp32=True)
+    out, ids, gates = [t.clone() for t in layer.forward(inp.x)]
+    assert layer.status() == B.MOE_OK
+    im = layer.intermediates(cfg.T)
+    tk = np.array([0, 1, 777, 8191, 16383])
+    vals, rs, _ = _expect_quantised(inp.x[torch.as_tensor(tk, device="cuda")])
+    assert np.array_equal(im["xq"][torch.as_tensor(tk, device="cuda")].double().cpu().numpy(), vals)
+    assert np.array_equal(im["sx"].cpu().numpy()[tk], rs)
+    part = MoELayer.from_inputs(inp, out_fp32=True).forward(inp.x[:512].contiguous())
+    for a, b in zip((out, ids, gates), part):
+        assert torch.equal(a[:512], b)
+    ref = mc.oracle_layer(inp, tokens=tk)
+    same = mc.check_ids(ids.cpu().numpy()[tk], ref.logits, 8)
+    mc.check_out(out.cpu().numpy()[tk][same], ref.out[same])
