@@ -64,7 +64,7 @@ Layout make_layout(const moe_dims* d) {
     const size_t rows = T * k + T * S;
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align256(o + bytes); return at; };
-    L.status = take(16);
+    L.status = take(32);  // int32 [0..3] status words, [4..5] SM-pair GEMM tile counters
     L.logits = take(T * E * 4);
     L.rpart = take(router_split(d) > 1 ? T * E * 4 * router_split(d) : 0);
     L.valid = take(T * 4);
@@ -190,7 +190,7 @@ moe_status run_route(const moe_dims* d, const void* x, const moe_weights* w, con
                      cudaStream_t s, bool filter = false, float tau = 0.0f) {
     const int64_t T = d->T;
     int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
-    MOE_TRY(cu(cudaMemsetAsync(status, 0, 16, s)));
+    MOE_TRY(cu(cudaMemsetAsync(status, 0, 32, s)));
     GemmParams p;
     std::memset(&p, 0, sizeof p);
     if (!make_map(&p.a0, w->w_router, d->d, d->E, BM)) return MOE_ERR_CUDA;
@@ -358,6 +358,7 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     p1.out = ws + L.h;
     p1.ldo = d->F;
     p1.stall_test = take_stall_test() ? 1 : 0;
+    p1.tile_counter = status + 4;
     int64_t tb = ntiles * p1.MT;
     const int g1 = static_cast<int>(tb < units ? tb : units);
     MOE_TRY(mark(MOE_STAGE_GATE_UP, 0, s));
@@ -389,6 +390,7 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     p2.out = ws + L.y;
     p2.out_shared = S ? ws + L.ysh : nullptr;
     p2.ldo = d->d;
+    p2.tile_counter = status + 5;
     tb = ntiles * p2.MT;
     const int g2 = static_cast<int>(tb < units ? tb : units);
     MOE_TRY(mark(MOE_STAGE_DOWN, 0, s));

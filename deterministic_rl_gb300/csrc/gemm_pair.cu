@@ -82,7 +82,18 @@ struct PCfg {
     static constexpr int kScStages = kConv ? 2 : 0;
     static constexpr uint32_t kRingBytes =
         kStages * kStageBytes + kF8Stages * kF8Bytes + kScStages * kScBytes;
-    static constexpr int kBarriers = 2 * kStages + 2 * kF8Stages + 2 * kScStages + 9;
+    // tile queue: kQueue entries; arrivals releasing an entry on the leader:
+    // its MMA thread and 4 epilogue warps, the peer's producer and 4 epilogue
+    // warps, and with converters both CTAs' weight producers and converter warps
+    // bf16 weights: tiles come from a queue fed by a global counter (the
+    // token tiles of a weight tile start together and share it in L2).  The
+    // converting variants are limited by their converters, not by operand
+    // traffic, and run faster on the static round-robin order.
+    static constexpr bool kDynamic = !kConv;
+    static constexpr int kQueue = 8;
+    static constexpr int kQueueAhead = 2;  // < kQueue
+    static constexpr int kQueueReaders = 10 + (kConv ? 2 + 2 * 8 : 0);
+    static constexpr int kBarriers = 2 * kStages + 2 * kF8Stages + 2 * kScStages + 9 + 2 * kQueue;
     static constexpr int kConvWarps = 8;
     static constexpr int kConvPerKb = 2;                        // warps per k-block
     static constexpr int kConvGroups = kConvWarps / kConvPerKb;  // k-blocks in flight
@@ -303,10 +314,13 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
     uint64_t* f8empty = f8full + C::kF8Stages;  // MX, local: converters done with it
     uint64_t* scfull = f8empty + C::kF8Stages;
     uint64_t* scempty = scfull + C::kScStages;
+    uint64_t* qfull = scempty + C::kScStages;  // tile queue entry written (local)
+    uint64_t* qempty = qfull + C::kQueue;      // leader: entry read by every role
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + C::kBarriers);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* tq = reinterpret_cast<volatile int*>(tmem_slot + 4);  // [kQueue] tile indices
     const int GG = p.G + p.has_shared;
-    int* hs = reinterpret_cast<int*>(tmem_slot + 4);
+    int* hs = reinterpret_cast<int*>(tmem_slot + 4 + C::kQueue);
     int* cs = hs + GG + 1;
     int* gcnt = cs + GG + 1;
     int* goff = gcnt + GG;
@@ -381,6 +395,10 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
             mbar_init(&xempty[a], 1);
             mbar_init(&tempty[a], 8);  // 4 epilogue warps in each of the two CTAs
         }
+        for (int q = 0; q < C::kQueue; ++q) {
+            mbar_init(&qfull[q], 1);
+            mbar_init(&qempty[q], C::kQueueReaders);
+        }
         mbar_init(drain, 1);
         *abort = 0;
         fence_mbar_init();
@@ -394,8 +412,80 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
                    static_cast<int64_t>(hs[GG] + cs[GG]) * p.MT};
     const int total = static_cast<int>(sched.N);
     const uint64_t tmo = p.timeout_ns;
+
+    // ---- tile queue ----
+    // The pair takes tiles in order from the global counter: the leader's
+    // producer thread draws the next index, writes it into entry j % kQueue of
+    // both CTAs' queues (-1 once the tiles are exhausted) and arrives on both
+    // CTAs' "written" barriers (cluster-scope release for the peer); every
+    // other role reads entries j = 0, 1, ... in order (cluster-scope acquire)
+    // and releases each on the leader's "read" barrier.  Pairs that run ahead
+    // take more tiles, and the token tiles of a weight tile start together on
+    // whichever pairs are free, so they share it in L2.  An entry is rewritten
+    // only after all its readers released it, so a reader is never more than
+    // one phase behind.
+    auto q_release = [&](int slot) {
+        if (leader)
+            mbar_arrive(&qempty[slot]);
+        else
+            mbar_arrive_cluster(map_to_rank(&qempty[slot], 0));
+    };
+    // single-thread reader: false when the wait ran out (abort raised)
+    auto q_read = [&](int j, int& t, int where) -> bool {
+        const int slot = j % C::kQueue;
+        if (!mbar_wait_cluster(&qfull[slot], static_cast<uint32_t>(j / C::kQueue) & 1u, abort, tmo)) {
+            if (!*abort) raise_timeout(p, abort, where);
+            return false;
+        }
+        t = tq[slot];
+        q_release(slot);
+        return true;
+    };
+    // whole-warp reader
+    auto q_read_warp = [&](int j, int& t, int where) -> bool {
+        const int slot = j % C::kQueue;
+        if (!__all_sync(0xffffffffu, mbar_wait_cluster(&qfull[slot],
+                                                      static_cast<uint32_t>(j / C::kQueue) & 1u,
+                                                      abort, tmo))) {
+            if (lane == 0 && !*abort) raise_timeout(p, abort, where);
+            return false;
+        }
+        t = tq[slot];
+        __syncwarp();
+        if (lane == 0) q_release(slot);
+        return true;
+    };
+    // the leader's producer: draw and publish entry j
+    auto q_publish = [&](int j, int& t) -> bool {
+        const int slot = j % C::kQueue;
+        if (!mbar_wait(&qempty[slot], (static_cast<uint32_t>(j / C::kQueue) & 1u) ^ 1u, abort, tmo)) {
+            if (!*abort) raise_timeout(p, abort, 19);
+            return false;
+        }
+        t = atomicAdd(p.tile_counter, 1);
+        if (t >= total) t = -1;
+        tq[slot] = t;
+        st_shared_cluster_u32(map_to_rank(const_cast<int*>(&tq[slot]), 1), static_cast<uint32_t>(t));
+        mbar_arrive(&qfull[slot]);
+        mbar_arrive_cluster(map_to_rank(&qfull[slot], 1));
+        return true;
+    };
+    // static order: the pair's j-th tile is cid + j * ncl (-1 past the end)
     const int cid = static_cast<int>(cluster_id_x());
     const int ncl = static_cast<int>(nclusters_x());
+    auto tile_static = [&](int j) -> int {
+        const int64_t t = cid + static_cast<int64_t>(j) * ncl;
+        return t < total ? static_cast<int>(t) : -1;
+    };
+    // the j-th tile for a reader role (single thread or whole warp)
+    auto next_tile = [&](int j, int& t, int where, bool whole_warp) -> bool {
+        if constexpr (!C::kDynamic) {
+            t = tile_static(j);
+            return true;
+        } else {
+            return whole_warp ? q_read_warp(j, t, where) : q_read(j, t, where);
+        }
+    };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -412,7 +502,31 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
             uint32_t phase = 0;
             uint32_t issued = 0, last_par = 0;
             bool ok = p.stall_test == 0;
-            for (int t = cid; t < total && ok; t += ncl) {
+            // the leader publishes entries kQueueAhead beyond the one it loads,
+            // so that the weight producer of the converting variants learns
+            // the next tile early enough to prefetch it
+            int published = 0;
+            bool ended = false;
+            for (int j = 0; ok; ++j) {
+                int t;
+                if (!C::kDynamic) {
+                    t = tile_static(j);
+                } else if (leader) {
+                    while (!ended && published <= j + C::kQueueAhead) {
+                        int drawn;
+                        if (!q_publish(published, drawn)) {
+                            ok = false;
+                            break;
+                        }
+                        ++published;
+                        ended = drawn < 0;
+                    }
+                    if (!ok) break;
+                    t = tq[j % C::kQueue];  // written by this thread, not yet reusable
+                } else if (!next_tile(j, t, 19, false)) {
+                    break;
+                }
+                if (t < 0) break;
                 const Tile tl = decode_tile<MODE>(t, rank, p, sched);
                 const uint64_t pol_w = tl.reused ? pol_again : pol_once;
                 const CUtensorMap* ma0 = tl.shared ? &p.as0 : &p.a0;
@@ -471,7 +585,9 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true;
-            for (int t = cid; t < total && ok; t += ncl) {
+            for (int j = 0; ok; ++j) {
+                int t;
+                if (!next_tile(j, t, 27, false) || t < 0) break;
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort, tmo)) {
                     if (!*abort) raise_timeout(p, abort, 13);
                     break;
@@ -519,7 +635,9 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
                 uint32_t fph = 0, sph = 0;
                 uint32_t f_issued = 0, f_par = 0, s_issued = 0, s_par = 0;
                 bool ok = p.stall_test == 0;
-                for (int t = cid; t < total && ok; t += ncl) {
+                for (int j = 0; ok; ++j) {
+                    int t;
+                    if (!next_tile(j, t, 28, false) || t < 0) break;
                     const Tile tl = decode_tile<MODE>(t, rank, p, sched);
                     const uint64_t pol_w = tl.reused ? pol_again : pol_once;
                     for (int kb = 0; kb < p.KB; ++kb) {
@@ -596,14 +714,24 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
             const int grp_w = cw / C::kConvPerKb;
             const int sub = cw % C::kConvPerKb;
             constexpr int kRowsPerWarp = BM / C::kConvPerKb;
-            const int my_tiles = cid < total ? (total - cid + ncl - 1) / ncl : 0;
-            const int64_t n_kb = static_cast<int64_t>(my_tiles) * p.KB;
             auto wait_all = [&](uint64_t* bar, uint32_t par, int where) {
                 if (__all_sync(0xffffffffu, mbar_wait(bar, par, abort, tmo))) return true;
                 if (lane == 0 && !*abort) raise_timeout(p, abort, where);
                 return false;
             };
-            for (int64_t i = grp_w; i < n_kb; i += C::kConvGroups) {
+            // k-block i of the pair's sequence belongs to queue entry i / KB;
+            // KB is a multiple of the group count, so every group converts
+            // KB / kConvGroups k-blocks of every tile and reads every entry, in
+            // order, at its first k-block of that tile
+            const int per_tile = p.KB / C::kConvGroups;
+            int left = 0, j = 0;
+            for (int64_t i = grp_w;; i += C::kConvGroups) {
+                if (left == 0) {
+                    int t;
+                    if (!next_tile(j++, t, 29, true) || t < 0) break;
+                    left = per_tile;
+                }
+                --left;
                 const int os = static_cast<int>(i % kStages);
                 const uint32_t oph = static_cast<uint32_t>((i / kStages) & 1);
                 const int fs = static_cast<int>(i % C::kF8Stages);
@@ -684,7 +812,9 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
         uint32_t acc_phase = 0;
         uint32_t xph = 0;
         bool ok = true;
-        for (int t = cid; t < total && ok; t += ncl) {
+        for (int j = 0; ok; ++j) {
+            int t;
+            if (!next_tile(j, t, 30, true) || t < 0) break;
             const Tile tl = decode_tile<MODE>(t, rank, p, sched);
             const bool ready = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort, tmo));
             if (!ready) {
@@ -815,7 +945,7 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
 template <int MODE, int FMT>
 size_t pair_smem_bytes(int GG) {
     using C = PCfg<MODE, FMT>;
-    return 1024 + C::kRingBytes + C::kXBytes + C::kBarriers * 8 + 16 +
+    return 1024 + C::kRingBytes + C::kXBytes + C::kBarriers * 8 + 16 + C::kQueue * 4 +
            static_cast<size_t>(4 * GG + 2) * 4;
 }
 
@@ -856,7 +986,7 @@ cudaError_t launch_pair_mode(const GemmParams& p, int clusters, cudaStream_t s) 
 
 cudaError_t launch_pair_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s,
                              int wfmt) {
-    if (p.G + p.has_shared > kMaxGroups || clusters <= 0 || !p.cnt || !p.off)
+    if (p.G + p.has_shared > kMaxGroups || clusters <= 0 || !p.cnt || !p.off || !p.tile_counter)
         return cudaErrorInvalidValue;
     if (wfmt != WFMT_BF16 && p.has_shared) return cudaErrorInvalidValue;  // shared expert is bf16
     if (wfmt == WFMT_NVFP4 && (!p.row_scale || !p.wscale0 || (mode == GEMM_SWIGLU && !p.wscale1)))

@@ -75,6 +75,9 @@ struct GemmParams {
     const float* row_scale;
     const float* wscale0;
     const float* wscale1;
+    // SM-pair kernel: tiles are handed out in order by this counter (zeroed
+    // before the launch); which pair computes a tile never changes how.
+    int32_t* tile_counter;
 };
 
 size_t gemm_smem_bytes(int mode, int n_groups_total);
