@@ -265,6 +265,35 @@ bool take_stall_test() {
     return false;
 }
 
+// A second stream (and its fork/join events) per device and host thread, for
+// work that overlaps the caller's stream inside one call; created on first use
+// and kept for the life of the process.  Work on it is ordered against the
+// caller's stream by events only, so the call stays stream-ordered (and can be
+// captured in a CUDA graph).
+struct SideStream {
+    cudaStream_t stream = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
+};
+constexpr int kMaxDevices = 64;
+thread_local SideStream g_side[kMaxDevices];
+
+moe_status side_stream(SideStream** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+    SideStream& sd = g_side[dev];
+    if (!sd.stream) {
+        // highest priority: its persistent CTAs are placed first and the
+        // caller's memory-bound kernels fill the room they leave on each SM
+        int least = 0, greatest = 0;
+        MOE_TRY(cu(cudaDeviceGetStreamPriorityRange(&least, &greatest)));
+        MOE_TRY(cu(cudaStreamCreateWithPriority(&sd.stream, cudaStreamNonBlocking, greatest)));
+        MOE_TRY(cu(cudaEventCreateWithFlags(&sd.fork, cudaEventDisableTiming)));
+        MOE_TRY(cu(cudaEventCreateWithFlags(&sd.join, cudaEventDisableTiming)));
+    }
+    *out = &sd;
+    return MOE_OK;
+}
+
 // Dispatch, expert FFNs and combine, given ids/gates of every token.
 moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, void* out,
                        const int32_t* ids, const float* gates, uint8_t* ws, const Layout& L,
@@ -277,13 +306,62 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     int32_t* off = reinterpret_cast<int32_t*>(ws + L.off);
     int32_t* perm = reinterpret_cast<int32_t*>(ws + L.perm);
     int32_t* inv = reinterpret_cast<int32_t*>(ws + L.inv);
+    const int sms = num_sms();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    const bool mx = d->wfmt == MOE_W_MXFP8;
+    const bool nv = d->wfmt == MOE_W_NVFP4;
+    const bool one = one_sm_experts(d);
+    const int bn = one ? BN : BN_EXPERT;                           // tokens per tile
+    const uint32_t box_b = one ? BN : BN_EXPERT / 2;              // token rows per CTA
+    const uint32_t rg = one ? BM : gemm_rows(GEMM_SWIGLU);        // gate (= up) rows per CTA
+    const int tile_g = one ? BM : 2 * gemm_rows(GEMM_SWIGLU);     // gate rows per tile
+    const int tile_d = one ? BM : 2 * BM;                         // down rows per tile
+    const int units = one ? sms : sms / 2;                        // CTAs or CTA pairs
+    const uint64_t EF = uint64_t(E) * d->F, ED = uint64_t(E) * d->d;
+    // SM pairs, bf16, shared expert: the shared expert's gate/up needs no
+    // routing, so it runs on a second stream, reading x directly, while the
+    // dispatch and the gather run here; its tiles and the routed ones come
+    // from queues, so the two launches share the SMs however they overlap.
+    const bool overlap = S && !one && d->wfmt == MOE_W_BF16;
+    SideStream* side = nullptr;
+    if (overlap) {
+        MOE_TRY(side_stream(&side));
+        GemmParams ps;
+        std::memset(&ps, 0, sizeof ps);
+        ps.cnt = cnt;
+        ps.off = off;
+        ps.G = 0;
+        ps.has_shared = 1;
+        ps.shared_rows = static_cast<int32_t>(T);
+        ps.shared_b_off = 0;
+        ps.out_row_off = static_cast<int32_t>(T * k);
+        ps.partial_b = 1;
+        ps.status = status;
+        ps.timeout_ns = kWaitTimeoutNs;
+        if (!make_map(&ps.a0, w->ws_gate, d->d, d->F, rg)) return MOE_ERR_CUDA;
+        if (!make_map(&ps.a1, w->ws_up, d->d, d->F, rg)) return MOE_ERR_CUDA;
+        ps.as0 = ps.a0;
+        ps.as1 = ps.a1;
+        if (!make_map(&ps.b, x, d->d, T, box_b)) return MOE_ERR_CUDA;
+        if (!make_map(&ps.b32, x, d->d, T, 32)) return MOE_ERR_CUDA;
+        ps.M = d->F;
+        ps.MT = (d->F + tile_g - 1) / tile_g;
+        ps.KB = d->d / BK;
+        ps.out = ws + L.h;
+        ps.ldo = d->F;
+        ps.tile_counter = status + 6;
+        const int64_t tbs = (T + bn - 1) / bn * ps.MT;
+        MOE_TRY(cu(cudaEventRecord(side->fork, s)));
+        MOE_TRY(cu(cudaStreamWaitEvent(side->stream, side->fork, 0)));
+        MOE_TRY(cu(launch_pair_gemm(GEMM_SWIGLU, ps, static_cast<int>(tbs < units ? tbs : units),
+                                    side->stream, d->wfmt)));
+        MOE_TRY(cu(cudaEventRecord(side->join, side->stream)));
+    }
+    const int Sg = overlap ? 0 : S;  // shared expert inside the routed gate/up launch
     MOE_TRY(mark(MOE_STAGE_DISPATCH, 0, s));
     MOE_TRY(cu(launch_dispatch(ids, T, k, E, cnt, off, perm, inv,
                                reinterpret_cast<int32_t*>(ws + L.scratch), s)));
     MOE_TRY(mark(MOE_STAGE_DISPATCH, 1, s));
-    const int sms = num_sms();
-    if (sms <= 0) return MOE_ERR_CUDA;
-    const bool nv = d->wfmt == MOE_W_NVFP4;
     float* sxp = reinterpret_cast<float*>(ws + L.sxp);
     float* sh = reinterpret_cast<float*>(ws + L.sh);
     MOE_TRY(mark(MOE_STAGE_GATHER, 0, s));
@@ -296,21 +374,12 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
                                  reinterpret_cast<uint16_t*>(ws + L.xp), s,
                                  reinterpret_cast<const float*>(ws + L.sx), sxp)));
     } else {
-        MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), perm, T, k, d->d, S,
+        MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), perm, T, k, d->d, Sg,
                                  reinterpret_cast<uint16_t*>(ws + L.xp), s)));
     }
     MOE_TRY(mark(MOE_STAGE_GATHER, 1, s));
 
-    const bool mx = d->wfmt == MOE_W_MXFP8;
-    const bool one = one_sm_experts(d);
-    const int bn = one ? BN : BN_EXPERT;                           // tokens per tile
-    const uint32_t box_b = one ? BN : BN_EXPERT / 2;              // token rows per CTA
-    const uint32_t rg = one ? BM : gemm_rows(GEMM_SWIGLU);        // gate (= up) rows per CTA
-    const int tile_g = one ? BM : 2 * gemm_rows(GEMM_SWIGLU);     // gate rows per tile
-    const int tile_d = one ? BM : 2 * BM;                         // down rows per tile
     const int64_t ntiles = (T * k + bn - 1) / bn + E + (S ? (T + bn - 1) / bn : 0);
-    const int units = one ? sms : sms / 2;                        // CTAs or CTA pairs
-    const uint64_t EF = uint64_t(E) * d->F, ED = uint64_t(E) * d->d;
 
     auto common = [&](GemmParams& p) {
         p.cnt = cnt;
@@ -328,6 +397,7 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     GemmParams p1;
     std::memset(&p1, 0, sizeof p1);
     common(p1);
+    p1.has_shared = Sg;
     if (mx) {
         if (!make_map_u8(&p1.a0, w->w_gate, d->d, EF, BK, rg)) return MOE_ERR_CUDA;
         if (!make_map_u8(&p1.a1, w->w_up, d->d, EF, BK, rg)) return MOE_ERR_CUDA;
@@ -346,7 +416,7 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
         if (!make_map(&p1.a0, w->w_gate, d->d, EF, rg)) return MOE_ERR_CUDA;
         if (!make_map(&p1.a1, w->w_up, d->d, EF, rg)) return MOE_ERR_CUDA;
     }
-    if (S) {
+    if (Sg) {
         if (!make_map(&p1.as0, w->ws_gate, d->d, d->F, rg)) return MOE_ERR_CUDA;
         if (!make_map(&p1.as1, w->ws_up, d->d, d->F, rg)) return MOE_ERR_CUDA;
     }
@@ -393,6 +463,7 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     p2.tile_counter = status + 5;
     tb = ntiles * p2.MT;
     const int g2 = static_cast<int>(tb < units ? tb : units);
+    if (overlap) MOE_TRY(cu(cudaStreamWaitEvent(s, side->join, 0)));
     MOE_TRY(mark(MOE_STAGE_DOWN, 0, s));
     if (nv)  // NVFP4: each row of h quantised in place (per-token scale)
         MOE_TRY(cu(launch_nvfp4_qdq(reinterpret_cast<const uint16_t*>(ws + L.h),

@@ -853,7 +853,7 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
                         }
                         if (row_ok && cb + j < tl.n_valid) {
                             const float h = g / (1.0f + expf(-g)) * u;
-                            H[static_cast<int64_t>(tl.brow + cb + j) * p.ldo + row] =
+                            H[static_cast<int64_t>(tl.brow + p.out_row_off + cb + j) * p.ldo + row] =
                                 __float2bfloat16_rn(h);
                         }
                     }
@@ -884,7 +884,7 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
                             if (row_ok && c0 + j < tl.n_valid) {
                                 const float g = v[j];
                                 const float h = g / (1.0f + expf(-g)) * u[j];
-                                H[static_cast<int64_t>(tl.brow + c0 + j) * p.ldo + row] =
+                                H[static_cast<int64_t>(tl.brow + p.out_row_off + c0 + j) * p.ldo + row] =
                                     __float2bfloat16_rn(h);
                             }
                         }

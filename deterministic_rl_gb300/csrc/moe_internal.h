@@ -78,6 +78,9 @@ struct GemmParams {
     // SM-pair kernel: tiles are handed out in order by this counter (zeroed
     // before the launch); which pair computes a tile never changes how.
     int32_t* tile_counter;
+    // gate/up: SwiGLU output row = token row of B + out_row_off (the shared
+    // expert run on its own reads x directly and writes after the routed rows)
+    int32_t out_row_off;
 };
 
 size_t gemm_smem_bytes(int mode, int n_groups_total);
