@@ -311,7 +311,9 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     const bool mx = d->wfmt == MOE_W_MXFP8;
     const bool nv = d->wfmt == MOE_W_NVFP4;
     const bool one = one_sm_experts(d);
-    const int bn = one ? BN : BN_EXPERT;                           // tokens per tile
+    // MXFP8 / NVFP4 weights with few tokens: the SM-pair weight-streaming variant
+    const int small = !one && d->wfmt != MOE_W_BF16 && T <= kOneSmMaxTokens;
+    const int bn = one ? BN : (small ? 64 : BN_EXPERT);           // tokens per tile
     const uint32_t box_b = one ? BN : BN_EXPERT / 2;              // token rows per CTA
     const uint32_t rg = one ? BM : gemm_rows(GEMM_SWIGLU);        // gate (= up) rows per CTA
     const int tile_g = one ? BM : 2 * gemm_rows(GEMM_SWIGLU);     // gate rows per tile
@@ -433,7 +435,7 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     const int g1 = static_cast<int>(tb < units ? tb : units);
     MOE_TRY(mark(MOE_STAGE_GATE_UP, 0, s));
     MOE_TRY(cu(one ? launch_grouped_gemm(GEMM_SWIGLU, p1, g1, s)
-                   : launch_pair_gemm(GEMM_SWIGLU, p1, g1, s, d->wfmt)));
+                   : launch_pair_gemm(GEMM_SWIGLU, p1, g1, s, d->wfmt, small)));
     MOE_TRY(mark(MOE_STAGE_GATE_UP, 1, s));
 
     // down projection -> Y (routed, bf16) and Ysh (shared, fp32)
@@ -470,7 +472,7 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
                                     reinterpret_cast<uint16_t*>(ws + L.h), nullptr, sh, T * k,
                                     d->F, sms, s)));
     MOE_TRY(cu(one ? launch_grouped_gemm(GEMM_DOWN, p2, g2, s)
-                   : launch_pair_gemm(GEMM_DOWN, p2, g2, s, d->wfmt)));
+                   : launch_pair_gemm(GEMM_DOWN, p2, g2, s, d->wfmt, small)));
     MOE_TRY(mark(MOE_STAGE_DOWN, 1, s));
 
     MOE_TRY(mark(MOE_STAGE_COMBINE, 0, s));

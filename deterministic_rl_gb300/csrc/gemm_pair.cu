@@ -34,13 +34,9 @@
 namespace moe {
 namespace {
 
-constexpr int kPairN = BN_EXPERT;                // tokens per pair tile (256)
-constexpr int kHalfN = kPairN / 2;               // token rows held by each CTA
 constexpr uint32_t kABytes = BM * BK * 2;        // 128 weight rows x 64 along K
-constexpr uint32_t kBBytes = kHalfN * BK * 2;    // 128 token rows x 64 along K
 constexpr uint32_t kBox32Bytes = 32 * BK * 2;
-constexpr int kAccCols = kPairN;
-constexpr uint32_t kTmemCols = 2 * kAccCols;
+constexpr int kSmallTileN = 64;  // tokens per tile of the small-batch variant
 constexpr int kXPad = 33;
 constexpr int kMaxGroups = 1024;
 
@@ -56,10 +52,22 @@ constexpr int kMaxGroups = 1024;
 // 32-byte code row and four scale bytes per row and k-block); the token
 // operand arrives as bf16 e2m1 * e4m3 values (quantised per token) and the
 // epilogue scales each output by its token's and its matrix's fp32 scales.
-template <int MODE, int FMT>
+// SMALL (converting formats, batches of at most 128 tokens): weight streaming
+// with few tokens per expert.  Tiles of 64 tokens leave a 4 KB token slot per
+// stage, so four operand stages take 80 KB and the weight ring gets 96 KB (the
+// bytes in flight that streaming at an SM's share of HBM bandwidth needs), and
+// sixteen converter warps keep up with it.
+template <int MODE, int FMT, bool SMALL>
 struct PCfg {
     static constexpr bool kConv = FMT != WFMT_BF16;   // weights converted in-kernel
     static constexpr bool kNv = FMT == WFMT_NVFP4;
+    static constexpr bool kSmall = SMALL;
+    static constexpr int kTileN = SMALL ? kSmallTileN : BN_EXPERT;  // tokens per tile
+    static constexpr int kHalfN = kTileN / 2;                      // token rows per CTA
+    static constexpr uint32_t kBBytes = kHalfN * BK * 2;
+    static constexpr int kAccCols = kTileN;                        // TMEM columns per accumulator
+    static constexpr uint32_t kTmemCols = 2 * kAccCols;            // double-buffered
+    static constexpr int kChunks = SMALL ? 1 : 2;                  // 32-column TMEM loads per wait
     static constexpr bool kPair = MODE == GEMM_SWIGLU;      // 64 gate + 64 up rows per CTA
     static constexpr int kRowsCta = gemm_rows(MODE);        // output weight rows per CTA
     static constexpr int kRowsTile = 2 * kRowsCta;          // per CTA pair
@@ -73,10 +81,10 @@ struct PCfg {
     static constexpr bool kInterleave = kPair && kConv;
     static constexpr uint32_t kXBytes = kPair && !kConv ? 2 * 32 * kXPad * 4 : 0;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;  // operand ring entry
-    static constexpr int kStages = kConv ? 5 : 6;
+    static constexpr int kStages = SMALL ? 4 : (kConv ? 5 : 6);
     static constexpr uint32_t kF8RowBytes = kNv ? BK / 2 : BK;  // weight bytes per row and k-block
     static constexpr uint32_t kF8Bytes = BM * kF8RowBytes;      // fp8 / fp4 weight tile
-    static constexpr int kF8Stages = kConv ? 5 : 0;
+    static constexpr int kF8Stages = SMALL ? (kNv ? 24 : 12) : (kConv ? 5 : 0);
     static constexpr int kScPerKb = kNv ? BK / 16 : BK / 32;   // scale bytes per row and k-block
     static constexpr uint32_t kScBytes = BM * 8 * kScPerKb;     // 8 k-blocks of scales
     static constexpr int kScStages = kConv ? 2 : 0;
@@ -94,8 +102,8 @@ struct PCfg {
     static constexpr int kQueueAhead = 2;  // < kQueue
     static constexpr int kQueueReaders = 10 + (kConv ? 2 + 2 * 8 : 0);
     static constexpr int kBarriers = 2 * kStages + 2 * kF8Stages + 2 * kScStages + 9 + 2 * kQueue;
-    static constexpr int kConvWarps = 8;
-    static constexpr int kConvPerKb = 2;                        // warps per k-block
+    static constexpr int kConvWarps = SMALL ? 16 : 8;
+    static constexpr int kConvPerKb = SMALL ? 4 : 2;            // warps per k-block
     static constexpr int kConvGroups = kConvWarps / kConvPerKb;  // k-blocks in flight
     static constexpr int kThreads = kConv ? 192 + 32 * kConvWarps + 32 : 192;
     static constexpr int kFp8Warp = 6 + kConvWarps;
@@ -139,7 +147,7 @@ __device__ __forceinline__ int find_group(const int* start, int GG, int j) {
     return lo;
 }
 
-template <int MODE>
+template <int MODE, int TN>
 __device__ __forceinline__ Tile decode_tile(int t, uint32_t rank, const GemmParams& p,
                                             const Sched& sc) {
     Tile tl;
@@ -166,9 +174,9 @@ __device__ __forceinline__ Tile decode_tile(int t, uint32_t rank, const GemmPara
     const int lo = tl.g;
     const int* gcnt = sc.gcnt;
     const int* goff = sc.goff;
-    tl.n_valid = min(kPairN, gcnt[lo] - nt * kPairN);
-    tl.half = min(kPairN, max(64, (tl.n_valid + 63) & ~63)) >> 1;
-    tl.brow = goff[lo] + nt * kPairN;
+    tl.n_valid = min(TN, gcnt[lo] - nt * TN);
+    tl.half = min(TN, max(64, (tl.n_valid + 63) & ~63)) >> 1;
+    tl.brow = goff[lo] + nt * TN;
     tl.shared = lo >= p.G;
     tl.arow = (tl.shared ? 0 : lo * p.M) + tl.m * 2 * gemm_rows(MODE) + rank * gemm_rows(MODE);
     return tl;
@@ -288,10 +296,10 @@ __device__ __forceinline__ void e2m1x16_to_bf16(uint2 q, uint32_t s, uint4& o0, 
     o1 = make_uint4(out[4], out[5], out[6], out[7]);
 }
 
-template <int MODE, int FMT>
-__global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
+template <int MODE, int FMT, bool SMALL>
+__global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
     pair_gemm_kernel(const __grid_constant__ GemmParams p) {
-    using C = PCfg<MODE, FMT>;
+    using C = PCfg<MODE, FMT, SMALL>;
     constexpr bool MX = C::kConv;  // converter warps feed the A operand
     constexpr int kStages = C::kStages;
     constexpr uint32_t kStageBytes = C::kStageBytes;
@@ -346,7 +354,7 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
             }
             gcnt[g] = c;
             goff[g] = o;
-            const int ntg = (c + kPairN - 1) / kPairN;
+            const int ntg = (c + C::kTileN - 1) / C::kTileN;
             if (ntg > 1) local_h += ntg; else local_c += ntg;
         }
         int incl_h = local_h, incl_c = local_c;
@@ -363,7 +371,7 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
         for (int g = g0; g < min(g0 + per, GG); ++g) {
             hs[g] = run_h;
             cs[g] = run_c;
-            const int ntg = (gcnt[g] + kPairN - 1) / kPairN;
+            const int ntg = (gcnt[g] + C::kTileN - 1) / C::kTileN;
             if (ntg > 1) run_h += ntg; else run_c += ntg;
         }
         if (lane == 31) {
@@ -371,7 +379,7 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
             cs[GG] = incl_c;
         }
     } else if (warp == 1) {
-        tmem_alloc_pair(tmem_slot, kTmemCols);
+        tmem_alloc_pair(tmem_slot, C::kTmemCols);
         tmem_relinquish_pair();
     } else if (threadIdx.x == 64) {
         for (int s = 0; s < kStages; ++s) {
@@ -527,12 +535,12 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
                     break;
                 }
                 if (t < 0) break;
-                const Tile tl = decode_tile<MODE>(t, rank, p, sched);
+                const Tile tl = decode_tile<MODE, C::kTileN>(t, rank, p, sched);
                 const uint64_t pol_w = tl.reused ? pol_again : pol_once;
                 const CUtensorMap* ma0 = tl.shared ? &p.as0 : &p.a0;
                 const CUtensorMap* ma1 = tl.shared ? &p.as1 : &p.a1;
                 const int nbox = (b_rows(tl, rank) + 31) >> 5;
-                const bool whole = nbox == kHalfN / 32;
+                const bool whole = !C::kSmall && nbox == C::kHalfN / 32;
                 const uint32_t expect = (MX ? 0 : 2 * kABytes) + b_bytes(tl, 0) + b_bytes(tl, 1);
                 const int brow = tl.brow + static_cast<int>(rank) * tl.half;
                 for (int kb = 0; kb < p.KB; ++kb) {
@@ -593,9 +601,9 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d0 = tmem_base + acc * kAccCols;
+                const uint32_t d0 = tmem_base + acc * C::kAccCols;
                 const uint32_t idesc =
-                    tile_idesc(decode_tile<MODE>(t, rank, p, sched));
+                    tile_idesc(decode_tile<MODE, C::kTileN>(t, rank, p, sched));
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort, tmo)) {
                         if (!*abort) raise_timeout(p, abort, 14);
@@ -638,7 +646,7 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
                 for (int j = 0; ok; ++j) {
                     int t;
                     if (!next_tile(j, t, 28, false) || t < 0) break;
-                    const Tile tl = decode_tile<MODE>(t, rank, p, sched);
+                    const Tile tl = decode_tile<MODE, C::kTileN>(t, rank, p, sched);
                     const uint64_t pol_w = tl.reused ? pol_again : pol_once;
                     for (int kb = 0; kb < p.KB; ++kb) {
                         if ((kb & 7) == 0) {  // scales of the next 8 k-blocks
@@ -815,7 +823,7 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
         for (int j = 0; ok; ++j) {
             int t;
             if (!next_tile(j, t, 30, true) || t < 0) break;
-            const Tile tl = decode_tile<MODE>(t, rank, p, sched);
+            const Tile tl = decode_tile<MODE, C::kTileN>(t, rank, p, sched);
             const bool ready = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort, tmo));
             if (!ready) {
                 if (lane == 0 && !*abort) raise_timeout(p, abort, 16);
@@ -827,7 +835,7 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
                                             : (C::kPair ? pr : q) * 32 + lane);
             const bool row_ok = row < p.M;
             const uint32_t taddr =
-                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAccCols;
+                tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::kAccCols;
             // NVFP4: the matrices' fp32 scales for this group
             const float ws0 = C::kNv ? p.wscale0[tl.g] : 1.0f;
             const float ws1 = C::kNv && C::kPair ? p.wscale1[tl.g] : 1.0f;
@@ -912,15 +920,22 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
                 }
                 return true;
             };
-            // two chunks per TMEM round trip
-            for (int c0 = 0; c0 < tl.n_valid && ok; c0 += 64) {
-                float va[32], vb[32];
+            // kChunks chunks per TMEM round trip
+            for (int c0 = 0; c0 < tl.n_valid && ok; c0 += 32 * C::kChunks) {
+                float va[32];
                 tmem_ld32(taddr + c0, va);
-                tmem_ld32(taddr + c0 + 32, vb);
-                tmem_ld_wait();
-                tmem_regs_ready(va);
-                tmem_regs_ready(vb);
-                ok = chunk(va, c0) && (c0 + 32 >= tl.n_valid || chunk(vb, c0 + 32));
+                if constexpr (C::kChunks == 2) {
+                    float vb[32];
+                    tmem_ld32(taddr + c0 + 32, vb);
+                    tmem_ld_wait();
+                    tmem_regs_ready(va);
+                    tmem_regs_ready(vb);
+                    ok = chunk(va, c0) && (c0 + 32 >= tl.n_valid || chunk(vb, c0 + 32));
+                } else {
+                    tmem_ld_wait();
+                    tmem_regs_ready(va);
+                    ok = chunk(va, c0);
+                }
             }
             if (!ok) break;
             tc_fence_before();
@@ -938,28 +953,28 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT>::kThreads, 1)
     cluster_sync();  // neither CTA leaves while the pair may still touch its memory
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc_pair(tmem_base, kTmemCols);
+        tmem_dealloc_pair(tmem_base, C::kTmemCols);
     }
 }
 
-template <int MODE, int FMT>
+template <int MODE, int FMT, bool SMALL>
 size_t pair_smem_bytes(int GG) {
-    using C = PCfg<MODE, FMT>;
+    using C = PCfg<MODE, FMT, SMALL>;
     return 1024 + C::kRingBytes + C::kXBytes + C::kBarriers * 8 + 16 + C::kQueue * 4 +
            static_cast<size_t>(4 * GG + 2) * 4;
 }
 
-template <int MODE, int FMT>
+template <int MODE, int FMT, bool SMALL>
 cudaError_t launch_pair_mode(const GemmParams& p, int clusters, cudaStream_t s) {
     const int GG = p.G + p.has_shared;
-    const size_t smem = pair_smem_bytes<MODE, FMT>(GG);
-    cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<MODE, FMT>,
+    const size_t smem = pair_smem_bytes<MODE, FMT, SMALL>(GG);
+    cudaError_t e = cudaFuncSetAttribute(pair_gemm_kernel<MODE, FMT, SMALL>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2 * clusters, 1, 1);
-    cfg.blockDim = dim3(PCfg<MODE, FMT>::kThreads, 1, 1);
+    cfg.blockDim = dim3(PCfg<MODE, FMT, SMALL>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -972,34 +987,43 @@ cudaError_t launch_pair_mode(const GemmParams& p, int clusters, cudaStream_t s) 
     // Persistent clusters: never more than can be resident at once, so that no
     // cluster's share of the static tile order waits for a second wave.
     int resident = 0;
-    e = cudaOccupancyMaxActiveClusters(&resident, pair_gemm_kernel<MODE, FMT>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&resident, pair_gemm_kernel<MODE, FMT, SMALL>, &cfg);
     if (e != cudaSuccess) return e;
     if (resident <= 0) return cudaErrorInvalidConfiguration;
     if (clusters > resident) {
         clusters = resident;
         cfg.gridDim = dim3(2 * clusters, 1, 1);
     }
-    return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<MODE, FMT>, p);
+    return cudaLaunchKernelEx(&cfg, pair_gemm_kernel<MODE, FMT, SMALL>, p);
 }
 
 }  // namespace
 
 cudaError_t launch_pair_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s,
-                             int wfmt) {
+                             int wfmt, int small) {
     if (p.G + p.has_shared > kMaxGroups || clusters <= 0 || !p.cnt || !p.off || !p.tile_counter)
         return cudaErrorInvalidValue;
     if (wfmt != WFMT_BF16 && p.has_shared) return cudaErrorInvalidValue;  // shared expert is bf16
     if (wfmt == WFMT_NVFP4 && (!p.row_scale || !p.wscale0 || (mode == GEMM_SWIGLU && !p.wscale1)))
         return cudaErrorInvalidValue;
+    if (small && wfmt == WFMT_BF16) return cudaErrorInvalidValue;  // bf16 small batches: one-SM kernel
     if (mode == GEMM_SWIGLU) {
-        if (wfmt == WFMT_MXFP8) return launch_pair_mode<GEMM_SWIGLU, WFMT_MXFP8>(p, clusters, s);
-        if (wfmt == WFMT_NVFP4) return launch_pair_mode<GEMM_SWIGLU, WFMT_NVFP4>(p, clusters, s);
-        return launch_pair_mode<GEMM_SWIGLU, WFMT_BF16>(p, clusters, s);
+        if (wfmt == WFMT_MXFP8)
+            return small ? launch_pair_mode<GEMM_SWIGLU, WFMT_MXFP8, true>(p, clusters, s)
+                         : launch_pair_mode<GEMM_SWIGLU, WFMT_MXFP8, false>(p, clusters, s);
+        if (wfmt == WFMT_NVFP4)
+            return small ? launch_pair_mode<GEMM_SWIGLU, WFMT_NVFP4, true>(p, clusters, s)
+                         : launch_pair_mode<GEMM_SWIGLU, WFMT_NVFP4, false>(p, clusters, s);
+        return launch_pair_mode<GEMM_SWIGLU, WFMT_BF16, false>(p, clusters, s);
     }
     if (mode == GEMM_DOWN) {
-        if (wfmt == WFMT_MXFP8) return launch_pair_mode<GEMM_DOWN, WFMT_MXFP8>(p, clusters, s);
-        if (wfmt == WFMT_NVFP4) return launch_pair_mode<GEMM_DOWN, WFMT_NVFP4>(p, clusters, s);
-        return launch_pair_mode<GEMM_DOWN, WFMT_BF16>(p, clusters, s);
+        if (wfmt == WFMT_MXFP8)
+            return small ? launch_pair_mode<GEMM_DOWN, WFMT_MXFP8, true>(p, clusters, s)
+                         : launch_pair_mode<GEMM_DOWN, WFMT_MXFP8, false>(p, clusters, s);
+        if (wfmt == WFMT_NVFP4)
+            return small ? launch_pair_mode<GEMM_DOWN, WFMT_NVFP4, true>(p, clusters, s)
+                         : launch_pair_mode<GEMM_DOWN, WFMT_NVFP4, false>(p, clusters, s);
+        return launch_pair_mode<GEMM_DOWN, WFMT_BF16, false>(p, clusters, s);
     }
     return cudaErrorInvalidValue;
 }

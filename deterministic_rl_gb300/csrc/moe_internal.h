@@ -93,8 +93,10 @@ cudaError_t launch_grouped_gemm(int mode, const GemmParams& p, int grid, cudaStr
 // scale maps sa0/sa1 (32-byte boxes, one per 16 values); the kernel
 // dequantises them exactly to bf16 and scales each output by row_scale of its
 // token times the group's weight scale.
+// small != 0 (MXFP8 / NVFP4 weights, batches of at most kOneSmMaxTokens): the
+// weight-streaming variant with 64-token tiles and a deeper weight ring.
 cudaError_t launch_pair_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s,
-                             int wfmt = 0);
+                             int wfmt = 0, int small = 0);
 
 // Routing: top-k selection (own mode) or replay validation, then gate weights.
 cudaError_t launch_topk_gates(const float* logits, int64_t T, int E, int k,

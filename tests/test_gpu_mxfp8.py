@@ -137,3 +137,16 @@ def test_mxfp8_full_size_near_ties():
     ref_r = mc.oracle_layer(inp, tokens=tk, replay_ids=rid[tk])
     mc.check_gates(gates_r.cpu().numpy()[tk], ref_r.gates)
     mc.check_out(out_r.cpu().numpy()[tk], ref_r.out)
+
+
+def test_mxfp8_rows_equal_across_the_small_batch_variant():
+    """Batches of at most 128 tokens run the weight-streaming variant (64-token
+    tiles); larger ones the regular SM-pair kernel.  A token's bits do not
+    depend on which one ran."""
+    inp = make_layer(small_mx(T=600, seed=47), "cuda")
+    layer = MoELayer.from_inputs(inp, out_fp32=True)
+    full = [t.clone() for t in layer.forward(inp.x)]
+    for lo, hi in ((0, 1), (0, 64), (100, 228), (300, 429)):
+        part = layer.forward(inp.x[lo:hi].contiguous())
+        for a, b in zip(full, part):
+            assert torch.equal(a[lo:hi], b)
