@@ -34,7 +34,9 @@ MOE_W_NVFP4 = 2
 # Every function the header declares, in declaration order.
 EXPORTED = ("moe_workspace_size", "moe_workspace_layout", "moe_route", "moe_forward",
             "moe_forward_replay", "moe_get_status", "moe_status_str", "moe_set_stage_events",
-            "moe_route_static", "moe_forward_replay_filtered")
+            "moe_route_static", "moe_forward_replay_filtered", "moe_backward_weights_size",
+            "moe_backward_prepare_weights", "moe_backward_workspace_size",
+            "moe_backward_workspace_layout", "moe_backward")
 
 STAGES = ("router_gemm", "topk", "dispatch", "gather", "gate_up", "down", "combine")
 
@@ -55,6 +57,18 @@ class moe_ws_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("status", "logits", "valid", "cnt", "off", "perm", "inv", "xp", "h", "y",
                  "ysh", "xq", "sx", "sxp", "sh", "total")]
+
+
+class moe_grads(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in
+                ("d_router", "d_gate", "d_up", "d_down", "ds_gate", "ds_up", "ds_down")]
+
+
+class moe_bwd_ws_layout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in
+                ("status", "logits", "valid", "cnt", "off", "perm", "inv", "xp", "h", "y",
+                 "ids", "gates", "poff", "a", "b", "dg", "dl", "dyq", "dh", "dab", "dabq", "dxp",
+                 "xpt", "dyt", "ht", "dabt", "kpad", "total")]
 
 
 class MoEError(RuntimeError):
@@ -99,6 +113,17 @@ def load(path: str = LIB_PATH):
                                                 ctypes.c_size_t, P]
     lib.moe_route_static.restype = ctypes.c_int
     lib.moe_route_static.argtypes = [D, P, W, P, P, P]
+    lib.moe_backward_weights_size.restype = ctypes.c_size_t
+    lib.moe_backward_weights_size.argtypes = [D]
+    lib.moe_backward_prepare_weights.restype = ctypes.c_int
+    lib.moe_backward_prepare_weights.argtypes = [D, W, P, ctypes.c_size_t, P]
+    lib.moe_backward_workspace_size.restype = ctypes.c_size_t
+    lib.moe_backward_workspace_size.argtypes = [D]
+    lib.moe_backward_workspace_layout.restype = ctypes.c_int
+    lib.moe_backward_workspace_layout.argtypes = [D, ctypes.POINTER(moe_bwd_ws_layout)]
+    lib.moe_backward.restype = ctypes.c_int
+    lib.moe_backward.argtypes = [D, P, W, P, P, P, P, ctypes.POINTER(moe_grads), P,
+                                 ctypes.c_size_t, P]
     _lib = lib
     return lib
 
@@ -221,4 +246,47 @@ def moe_forward_replay_filtered(dims: Dims, x, weights: moe_weights, ids_in, tau
                                             _stream(stream))
     if check and rc != MOE_OK:
         raise MoEError(rc, "moe_forward_replay_filtered")
+    return rc
+
+
+# ---- backward ----
+
+def make_grads(d_router, d_gate, d_up, d_down, ds_gate=None, ds_up=None,
+               ds_down=None) -> moe_grads:
+    return moe_grads(*(_p(t) for t in (d_router, d_gate, d_up, d_down, ds_gate, ds_up, ds_down)))
+
+
+def moe_backward_weights_size(dims: Dims) -> int:
+    return int(load().moe_backward_weights_size(ctypes.byref(dims.c())))
+
+
+def moe_backward_prepare_weights(dims: Dims, weights: moe_weights, wt, stream=None,
+                                 check: bool = True) -> int:
+    rc = load().moe_backward_prepare_weights(ctypes.byref(dims.c()), ctypes.byref(weights),
+                                             _p(wt), wt.numel() * wt.element_size(),
+                                             _stream(stream))
+    if check and rc != MOE_OK:
+        raise MoEError(rc, "moe_backward_prepare_weights")
+    return rc
+
+
+def moe_backward_workspace_size(dims: Dims) -> int:
+    return int(load().moe_backward_workspace_size(ctypes.byref(dims.c())))
+
+
+def moe_backward_workspace_layout(dims: Dims) -> moe_bwd_ws_layout:
+    out = moe_bwd_ws_layout()
+    rc = load().moe_backward_workspace_layout(ctypes.byref(dims.c()), ctypes.byref(out))
+    if rc != MOE_OK:
+        raise MoEError(rc, "moe_backward_workspace_layout")
+    return out
+
+
+def moe_backward(dims: Dims, x, weights: moe_weights, wt, ids, dout, dx, grads: moe_grads, ws,
+                 stream=None, check: bool = True) -> int:
+    rc = load().moe_backward(ctypes.byref(dims.c()), _p(x), ctypes.byref(weights), _p(wt),
+                             _p(ids), _p(dout), _p(dx), ctypes.byref(grads), _p(ws),
+                             ws.numel() * ws.element_size(), _stream(stream))
+    if check and rc != MOE_OK:
+        raise MoEError(rc, "moe_backward")
     return rc

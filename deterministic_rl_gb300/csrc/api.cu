@@ -503,6 +503,305 @@ moe_status forward_impl(const moe_dims* d, const void* x, const moe_weights* w,
     return run_experts(d, x, w, out, ids_out, gates_out, wsb, L, s);
 }
 
+// ---- backward ------------------------------------------------------------------
+
+struct BwdLayout {
+    Layout f;  // the forward's regions first (status word at offset 0)
+    size_t ids, gates, poff, a, b, dg, dl, dyq, dh, dab, dabq, dxp, xpt, dyt, ht, dabt;
+    int64_t kpad;
+    size_t total;
+};
+
+struct BwdWeights {
+    size_t wdt, w2t, swdt, sw2t, total;
+};
+
+bool bwd_dims_ok(const moe_dims* d) {
+    return dims_ok(d) && d->wfmt == MOE_W_BF16 && d->d % 256 == 0 && d->F % 256 == 0;
+}
+
+moe_status bwd_dims_status(const moe_dims* d) {
+    if (!d) return MOE_ERR_ARG;
+    if (!dims_ok(d)) return MOE_ERR_SHAPE;
+    if (d->wfmt != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
+    if (d->d % 256 || d->F % 256) return MOE_ERR_SHAPE;
+    return MOE_OK;
+}
+
+BwdLayout make_bwd_layout(const moe_dims* d) {
+    BwdLayout L{};
+    L.f = make_layout(d);
+    const size_t T = static_cast<size_t>(d->T), k = d->k, E = d->E, S = d->n_shared;
+    const size_t D = d->d, F = d->F;
+    const size_t rows = T * k + T * S;
+    // every expert's token run is padded to a multiple of 64: at most
+    // rows + 63 per group, rounded up
+    L.kpad = static_cast<int64_t>((rows + 64 * (E + S) + 63) / 64 * 64);
+    const size_t kp = static_cast<size_t>(L.kpad);
+    size_t o = L.f.total;
+    auto take = [&](size_t bytes) { const size_t at = o; o = align256(o + bytes); return at; };
+    L.ids = take(T * k * 4);
+    L.gates = take(T * k * 4);
+    L.poff = take((E + S + 1) * 4);
+    L.a = take(rows * F * 4);
+    L.b = take(rows * F * 4);
+    L.dg = take(T * k * 4);
+    L.dl = take(T * k * 4);
+    L.dyq = take(rows * D * 2);
+    L.dh = take(rows * F * 4);
+    L.dab = take(rows * 2 * F * 4);
+    L.dabq = take(rows * 2 * F * 2);
+    L.dxp = take(rows * D * 4);
+    L.xpt = take(D * kp * 2);
+    L.dyt = take(D * kp * 2);
+    L.ht = take(F * kp * 2);
+    L.dabt = take(2 * F * kp * 2);
+    L.total = o;
+    return L;
+}
+
+BwdWeights make_bwd_weights(const moe_dims* d) {
+    BwdWeights W{};
+    const size_t E = d->E, S = d->n_shared, FD = size_t(d->F) * d->d;
+    size_t o = 0;
+    auto take = [&](size_t bytes) { const size_t at = o; o = align256(o + bytes); return at; };
+    W.wdt = take(E * FD * 2);
+    W.w2t = take(E * FD * 2 * 2);
+    W.swdt = take(S * FD * 2);
+    W.sw2t = take(S * FD * 2 * 2);
+    W.total = o;
+    return W;
+}
+
+moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w, const void* wt,
+                         const int32_t* ids, const void* dout, float* dx, const moe_grads* g,
+                         void* ws, size_t ws_bytes, cudaStream_t s) {
+    MOE_TRY(bwd_dims_status(d));
+    if (!w || !g) return MOE_ERR_ARG;
+    if (d->T == 0) return MOE_OK;
+    const int64_t T = d->T;
+    const int k = d->k, E = d->E, S = d->n_shared, D = d->d, F = d->F;
+    if (!x || !w->w_router || !wt || !ids || !dout || !dx || !ws) return MOE_ERR_ARG;
+    MOE_TRY(check_experts(d, w));
+    if (!g->d_router || !g->d_gate || !g->d_up || !g->d_down) return MOE_ERR_ARG;
+    if (S && (!g->ds_gate || !g->ds_up || !g->ds_down)) return MOE_ERR_ARG;
+    if (!al16(x) || !al16(w->w_router) || !al16(w->router_bias) || !al16(wt) || !al16(ids) ||
+        !al16(dout) || !al16(dx) || !al16(ws) || !al16(g->d_router) || !al16(g->d_gate) ||
+        !al16(g->d_up) || !al16(g->d_down) || !al16(g->ds_gate) || !al16(g->ds_up) ||
+        !al16(g->ds_down))
+        return MOE_ERR_ALIGN;
+    const BwdLayout L = make_bwd_layout(d);
+    if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+    const BwdWeights WW = make_bwd_weights(d);
+    const int sms = num_sms();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    auto* wsb = static_cast<uint8_t*>(ws);
+    auto* wtb = static_cast<const uint8_t*>(wt);
+    int32_t* status = reinterpret_cast<int32_t*>(wsb + L.f.status);
+    int32_t* cnt = reinterpret_cast<int32_t*>(wsb + L.f.cnt);
+    int32_t* off = reinterpret_cast<int32_t*>(wsb + L.f.off);
+    int32_t* perm = reinterpret_cast<int32_t*>(wsb + L.f.perm);
+    int32_t* inv = reinterpret_cast<int32_t*>(wsb + L.f.inv);
+    int32_t* valid = reinterpret_cast<int32_t*>(wsb + L.f.valid);
+    int32_t* ids_used = reinterpret_cast<int32_t*>(wsb + L.ids);
+    float* gates = reinterpret_cast<float*>(wsb + L.gates);
+    int32_t* poff = reinterpret_cast<int32_t*>(wsb + L.poff);
+    const int64_t Tk = T * k;
+    const int64_t rows = Tk + T * S;
+    const int G = E + S;
+
+    // 1. routing with the given ids (replay: checked, gate weights recomputed),
+    //    dispatch, padded token offsets, gather (with the shared rows)
+    MOE_TRY(run_route(d, x, w, ids, ids_used, gates, wsb, L.f, s));
+    MOE_TRY(cu(launch_dispatch(ids_used, T, k, E, cnt, off, perm, inv,
+                               reinterpret_cast<int32_t*>(wsb + L.f.scratch), s)));
+    MOE_TRY(cu(launch_seg_offsets(cnt, E, G, S ? static_cast<int>(T) : 0, poff, s)));
+    MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), perm, T, k, D, S,
+                             reinterpret_cast<uint16_t*>(wsb + L.f.xp), s)));
+
+    const int units = sms / 2;  // CTA pairs
+    const uint32_t box_b = BN_EXPERT / 2;
+    const uint32_t rg = gemm_rows(GEMM_SWIGLU);
+    const int64_t tok_tiles = (Tk + BN_EXPERT - 1) / BN_EXPERT + E;
+    const int64_t sh_tiles = S ? (T + BN_EXPERT - 1) / BN_EXPERT : 0;
+    auto common = [&](GemmParams& p, int has_shared, int32_t* counter) {
+        std::memset(&p, 0, sizeof p);
+        p.cnt = cnt;
+        p.off = off;
+        p.G = E;
+        p.has_shared = has_shared;
+        p.shared_rows = static_cast<int32_t>(T);
+        p.shared_b_off = static_cast<int32_t>(Tk);
+        p.partial_b = 1;
+        p.status = status;
+        p.timeout_ns = kWaitTimeoutNs;
+        p.tile_counter = counter;
+    };
+    auto launch = [&](int mode, const GemmParams& p, int64_t ntiles) {
+        const int64_t tb = ntiles * p.MT;
+        return cu(launch_pair_gemm(mode, p, static_cast<int>(tb < units ? tb : units), s));
+    };
+    const uint64_t EF = uint64_t(E) * F, ED = uint64_t(E) * D;
+
+    // 2. forward recompute: gate/up (H, and the fp32 pre-activations), down (Y)
+    {
+        GemmParams p;
+        common(p, S, status + 4);
+        if (!make_map(&p.a0, w->w_gate, D, EF, rg) || !make_map(&p.a1, w->w_up, D, EF, rg))
+            return MOE_ERR_CUDA;
+        if (S && (!make_map(&p.as0, w->ws_gate, D, F, rg) || !make_map(&p.as1, w->ws_up, D, F, rg)))
+            return MOE_ERR_CUDA;
+        if (!make_map(&p.b, wsb + L.f.xp, D, rows, box_b) ||
+            !make_map(&p.b32, wsb + L.f.xp, D, rows, 32))
+            return MOE_ERR_CUDA;
+        p.M = F;
+        p.MT = (F + 2 * rg - 1) / (2 * rg);
+        p.KB = D / BK;
+        p.out = wsb + L.f.h;
+        p.ldo = F;
+        p.save_a = reinterpret_cast<float*>(wsb + L.a);
+        p.save_b = reinterpret_cast<float*>(wsb + L.b);
+        MOE_TRY(launch(GEMM_SWIGLU, p, tok_tiles + sh_tiles));
+    }
+    {
+        GemmParams p;
+        common(p, 0, status + 5);
+        if (!make_map(&p.a0, w->w_down, F, ED, BM)) return MOE_ERR_CUDA;
+        if (!make_map(&p.b, wsb + L.f.h, F, rows, box_b) ||
+            !make_map(&p.b32, wsb + L.f.h, F, rows, 32))
+            return MOE_ERR_CUDA;
+        p.M = D;
+        p.MT = (D + 2 * BM - 1) / (2 * BM);
+        p.KB = F / BK;
+        p.out = wsb + L.f.y;
+        p.ldo = D;
+        MOE_TRY(launch(GEMM_DOWN, p, tok_tiles));
+    }
+
+    // 3. gate and router gradients; dx starts as the router's part
+    MOE_TRY(cu(launch_gate_bwd(static_cast<const uint16_t*>(dout),
+                               reinterpret_cast<const uint16_t*>(wsb + L.f.y), inv, ids_used, gates,
+                               valid, static_cast<const uint16_t*>(w->w_router),
+                               reinterpret_cast<float*>(wsb + L.dg),
+                               reinterpret_cast<float*>(wsb + L.dl), dx, T, k, D, sms, s)));
+    MOE_TRY(cu(launch_router_wgrad(reinterpret_cast<const uint16_t*>(wsb + L.f.xp), perm, cnt, off,
+                                   reinterpret_cast<const float*>(wsb + L.dl), g->d_router, E, D,
+                                   sms, s)));
+
+    // 4. dH = Q_d(dY) Q_d(Wd)  (SM-pair grouped GEMM, fp32 rows)
+    uint16_t* dyq = reinterpret_cast<uint16_t*>(wsb + L.dyq);
+    MOE_TRY(cu(launch_dy_rows(static_cast<const uint16_t*>(dout), gates, perm, valid, T, k, D, S,
+                              dyq, sms, s)));
+    {
+        GemmParams p;
+        common(p, S, status + 6);
+        if (!make_map(&p.a0, wtb + WW.wdt, D, EF, BM)) return MOE_ERR_CUDA;
+        if (S && !make_map(&p.as0, wtb + WW.swdt, D, F, BM)) return MOE_ERR_CUDA;
+        if (!make_map(&p.b, dyq, D, rows, box_b) || !make_map(&p.b32, dyq, D, rows, 32))
+            return MOE_ERR_CUDA;
+        p.M = F;
+        p.MT = (F + 2 * BM - 1) / (2 * BM);
+        p.KB = D / BK;
+        p.out = wsb + L.dh;
+        p.out_f32 = 1;
+        p.ldo = F;
+        MOE_TRY(launch(GEMM_DOWN, p, tok_tiles + sh_tiles));
+    }
+
+    // 5. SwiGLU backward -> [dA | dB] (fp32 and quantised along F)
+    float* dab = reinterpret_cast<float*>(wsb + L.dab);
+    uint16_t* dabq = reinterpret_cast<uint16_t*>(wsb + L.dabq);
+    MOE_TRY(cu(launch_swiglu_bwd(reinterpret_cast<const float*>(wsb + L.dh),
+                                 reinterpret_cast<const float*>(wsb + L.a),
+                                 reinterpret_cast<const float*>(wsb + L.b), dab, dabq, rows, F, sms,
+                                 s)));
+
+    // 6. dXp = Q_F(dA) Q_F(Wg) + Q_F(dB) Q_F(Wu)  (one K = 2F GEMM), then dx
+    {
+        GemmParams p;
+        common(p, S, status + 7);
+        if (!make_map(&p.a0, wtb + WW.w2t, 2 * F, ED, BM)) return MOE_ERR_CUDA;
+        if (S && !make_map(&p.as0, wtb + WW.sw2t, 2 * F, D, BM)) return MOE_ERR_CUDA;
+        if (!make_map(&p.b, dabq, 2 * F, rows, box_b) || !make_map(&p.b32, dabq, 2 * F, rows, 32))
+            return MOE_ERR_CUDA;
+        p.M = D;
+        p.MT = (D + 2 * BM - 1) / (2 * BM);
+        p.KB = 2 * F / BK;
+        p.out = wsb + L.dxp;
+        p.out_f32 = 1;
+        p.ldo = D;
+        MOE_TRY(launch(GEMM_DOWN, p, tok_tiles + sh_tiles));
+    }
+    MOE_TRY(cu(launch_dx_assemble(reinterpret_cast<const float*>(wsb + L.dxp), inv, dx, T, k, D, S,
+                                  sms, s)));
+
+    // 7. token-major operands, quantised along the tokens of each expert
+    uint16_t* xpt = reinterpret_cast<uint16_t*>(wsb + L.xpt);
+    uint16_t* dyt = reinterpret_cast<uint16_t*>(wsb + L.dyt);
+    uint16_t* ht = reinterpret_cast<uint16_t*>(wsb + L.ht);
+    uint16_t* dabt = reinterpret_cast<uint16_t*>(wsb + L.dabt);
+    const int srows = S ? static_cast<int>(T) : 0;
+    MOE_TRY(cu(launch_tq_segments(TQ_SRC_BF16, wsb + L.f.xp, D, nullptr, D, cnt, off, poff, E, G,
+                                  Tk, srows, L.kpad, xpt, sms, s)));
+    const SegDyArgs dya{static_cast<const uint16_t*>(dout), gates, perm, valid, k, Tk};
+    MOE_TRY(cu(launch_tq_segments(TQ_SRC_DY, nullptr, D, &dya, D, cnt, off, poff, E, G, Tk, srows,
+                                  L.kpad, dyt, sms, s)));
+    MOE_TRY(cu(launch_tq_segments(TQ_SRC_BF16, wsb + L.f.h, F, nullptr, F, cnt, off, poff, E, G,
+                                  Tk, srows, L.kpad, ht, sms, s)));
+    MOE_TRY(cu(launch_tq_segments(TQ_SRC_F32, dab, 2 * F, nullptr, 2 * F, cnt, off, poff, E, G, Tk,
+                                  srows, L.kpad, dabt, sms, s)));
+
+    // 8. weight gradients (ragged-K grouped GEMMs)
+    const int wm = wgrad_tile_m(), wn = wgrad_tile_n();
+    auto wlaunch = [&](WgradParams& p) {
+        const int64_t tiles = int64_t(p.G) * p.MT * p.NT;
+        return cu(launch_wgrad(p, static_cast<int>(tiles < sms ? tiles : sms), s));
+    };
+    {
+        WgradParams p;
+        std::memset(&p, 0, sizeof p);
+        if (!make_map(&p.a, ht, L.kpad, F, wm) || !make_map(&p.b, dyt, L.kpad, D, wn))
+            return MOE_ERR_CUDA;
+        p.poff = poff;
+        p.G = G;
+        p.G_routed = E;
+        p.M = F;
+        p.N = D;
+        p.MT = F / wm;
+        p.NT = D / wn;
+        p.n_split = D;
+        p.out0 = g->d_down;
+        p.sout0 = g->ds_down;
+        p.gstride = int64_t(D) * F;
+        p.status = status;
+        p.timeout_ns = kWaitTimeoutNs;
+        MOE_TRY(wlaunch(p));
+    }
+    {
+        WgradParams p;
+        std::memset(&p, 0, sizeof p);
+        if (!make_map(&p.a, xpt, L.kpad, D, wm) || !make_map(&p.b, dabt, L.kpad, 2 * F, wn))
+            return MOE_ERR_CUDA;
+        p.poff = poff;
+        p.G = G;
+        p.G_routed = E;
+        p.M = D;
+        p.N = 2 * F;
+        p.MT = D / wm;
+        p.NT = 2 * F / wn;
+        p.n_split = F;
+        p.out0 = g->d_gate;
+        p.out1 = g->d_up;
+        p.sout0 = g->ds_gate;
+        p.sout1 = g->ds_up;
+        p.gstride = int64_t(F) * D;
+        p.status = status;
+        p.timeout_ns = kWaitTimeoutNs;
+        MOE_TRY(wlaunch(p));
+    }
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -602,6 +901,93 @@ const char* moe_status_str(moe_status s) {
         case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED: not supported by this build";
     }
     return "unknown moe_status";
+}
+
+size_t moe_backward_weights_size(const moe_dims* dims) {
+    if (bwd_dims_status(dims) != MOE_OK) return 0;
+    return make_bwd_weights(dims).total;
+}
+
+moe_status moe_backward_prepare_weights(const moe_dims* d, const moe_weights* w, void* wt,
+                                        size_t wt_bytes, moe_stream_t stream) {
+    MOE_TRY(bwd_dims_status(d));
+    if (!w || !wt) return MOE_ERR_ARG;
+    MOE_TRY(check_experts(d, w));
+    if (!al16(wt)) return MOE_ERR_ALIGN;
+    const BwdWeights W = make_bwd_weights(d);
+    if (wt_bytes < W.total) return MOE_ERR_WORKSPACE;
+    const int sms = num_sms();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    auto* s = reinterpret_cast<cudaStream_t>(stream);
+    auto* o = static_cast<uint8_t*>(wt);
+    const int E = d->E, D = d->d, F = d->F;
+    const int64_t FD = int64_t(F) * D;
+    auto* wdt = reinterpret_cast<uint16_t*>(o + W.wdt);
+    auto* w2t = reinterpret_cast<uint16_t*>(o + W.w2t);
+    // Wd [d][F] -> [F][d] quantised along d; Wg, Wu [F][d] -> [d][2F] quantised along F
+    MOE_TRY(cu(launch_tq_batch(static_cast<const uint16_t*>(w->w_down), E, D, F, wdt, FD, D, 0, sms, s)));
+    MOE_TRY(cu(launch_tq_batch(static_cast<const uint16_t*>(w->w_gate), E, F, D, w2t, 2 * FD, 2 * F, 0,
+                               sms, s)));
+    MOE_TRY(cu(launch_tq_batch(static_cast<const uint16_t*>(w->w_up), E, F, D, w2t, 2 * FD, 2 * F, F,
+                               sms, s)));
+    if (d->n_shared) {
+        auto* swdt = reinterpret_cast<uint16_t*>(o + W.swdt);
+        auto* sw2t = reinterpret_cast<uint16_t*>(o + W.sw2t);
+        MOE_TRY(cu(launch_tq_batch(static_cast<const uint16_t*>(w->ws_down), 1, D, F, swdt, FD, D, 0,
+                                   sms, s)));
+        MOE_TRY(cu(launch_tq_batch(static_cast<const uint16_t*>(w->ws_gate), 1, F, D, sw2t, 2 * FD,
+                                   2 * F, 0, sms, s)));
+        MOE_TRY(cu(launch_tq_batch(static_cast<const uint16_t*>(w->ws_up), 1, F, D, sw2t, 2 * FD,
+                                   2 * F, F, sms, s)));
+    }
+    return MOE_OK;
+}
+
+size_t moe_backward_workspace_size(const moe_dims* dims) {
+    if (bwd_dims_status(dims) != MOE_OK) return 0;
+    return make_bwd_layout(dims).total;
+}
+
+moe_status moe_backward_workspace_layout(const moe_dims* dims, moe_bwd_ws_layout* out) {
+    if (!out) return MOE_ERR_ARG;
+    MOE_TRY(bwd_dims_status(dims));
+    const BwdLayout L = make_bwd_layout(dims);
+    out->status = L.f.status;
+    out->logits = L.f.logits;
+    out->valid = L.f.valid;
+    out->cnt = L.f.cnt;
+    out->off = L.f.off;
+    out->perm = L.f.perm;
+    out->inv = L.f.inv;
+    out->xp = L.f.xp;
+    out->h = L.f.h;
+    out->y = L.f.y;
+    out->ids = L.ids;
+    out->gates = L.gates;
+    out->poff = L.poff;
+    out->a = L.a;
+    out->b = L.b;
+    out->dg = L.dg;
+    out->dl = L.dl;
+    out->dyq = L.dyq;
+    out->dh = L.dh;
+    out->dab = L.dab;
+    out->dabq = L.dabq;
+    out->dxp = L.dxp;
+    out->xpt = L.xpt;
+    out->dyt = L.dyt;
+    out->ht = L.ht;
+    out->dabt = L.dabt;
+    out->kpad = static_cast<size_t>(L.kpad);
+    out->total = L.total;
+    return MOE_OK;
+}
+
+moe_status moe_backward(const moe_dims* dims, const void* x, const moe_weights* w, const void* wt,
+                        const int32_t* ids, const void* dout, float* dx, const moe_grads* grads,
+                        void* ws, size_t ws_bytes, moe_stream_t stream) {
+    return backward_impl(dims, x, w, wt, ids, dout, dx, grads, ws, ws_bytes,
+                         reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -1,0 +1,586 @@
+// backward.cu -- the element-wise, quantising and data-movement kernels of the
+// MoE layer backward (the grouped GEMMs are gemm_pair.cu and wgrad.cu).
+//
+// Composer 2 Technical Report, §6.1 "Training infrastructure" (Kernels): the
+// MoE backward runs its grouped GEMMs in standard MXFP8 -- E4M3 values with
+// one E8M0 scale per block of 32 elements.  MXFP8 is taken as the OCP
+// Microscaling Formats (MX) v1.0 specification defines it: per block,
+// X = floor(log2(max |v|)) - 8 (8 = the exponent of E4M3's largest normal),
+// element = E4M3(v * 2^-X), nearest even, clamped to +-448.  Every operand of
+// a grouped GEMM is quantised along that GEMM's contraction axis; the kernels
+// here write the dequantised values e4m3 * 2^X as bf16, which holds them
+// exactly (at most 4 significant bits, and the exponents the layer produces),
+// so the bf16 tcgen05 MMAs that follow multiply exactly the MXFP8 values.
+// The pages prefer a fast approximate division in the MXFP8 quantiser; the
+// scaling by 2^-X here is a multiplication by a power of two, which is exact.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+
+#include <cstdint>
+
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+// ---- MXFP8 helpers --------------------------------------------------------------
+
+// Shared exponent X of a block whose largest magnitude is amax (>= 0):
+// floor(log2 amax) - 8 within [-127, 127]; -127 for zero or subnormal amax.
+__device__ __forceinline__ int mx_block_exp(float amax) {
+    const int ef = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu);
+    if (ef == 0) return -127;
+    return max(ef - 127 - 8, -127);
+}
+
+// 2^n for n in [-127, 127] (2^-127 is an fp32 subnormal).
+__device__ __forceinline__ float exp2i(int n) {
+    return n >= -126 ? __uint_as_float(static_cast<uint32_t>(n + 127) << 23)
+                     : __uint_as_float(0x00400000u);
+}
+
+// e4m3(v * 2^-X) * 2^X, with inv = 2^-X and scale = 2^X.
+__device__ __forceinline__ float mx_qdq(float v, float inv, float scale) {
+    const __nv_fp8_storage_t q = __nv_cvt_float_to_fp8(v * inv, __NV_SATFINITE, __NV_E4M3);
+    return __half2float(__half(__nv_cvt_fp8_to_halfraw(q, __NV_E4M3))) * scale;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
+// Quantise 8 values with block exponent X and pack them as 8 bf16.
+__device__ __forceinline__ uint4 mx_qdq8(const float (&v)[8], int X) {
+    const float inv = exp2i(-X), sc = exp2i(X);
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = mx_qdq(v[i], inv, sc);
+    return make_uint4(pack_bf16x2(q[0], q[1]), pack_bf16x2(q[2], q[3]), pack_bf16x2(q[4], q[5]),
+                      pack_bf16x2(q[6], q[7]));
+}
+
+__device__ __forceinline__ float absmax8(const float (&v)[8]) {
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
+    return m;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// Largest magnitude over a block of 32 values held 8 per lane by 4
+// consecutive lanes (lanes 4i .. 4i + 3).
+__device__ __forceinline__ float block_amax4(float m) {
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    return fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+}
+
+// ---- row sources ----------------------------------------------------------------
+
+// 8 consecutive values of a row, as fp32.
+struct SrcBf16 {
+    const uint16_t* p;
+    int64_t ld;
+    __device__ __forceinline__ void load8(int64_t row, int c, float (&v)[8]) const {
+        unpack8(*reinterpret_cast<const uint4*>(p + row * ld + c), v);
+    }
+};
+
+struct SrcF32 {
+    const float* p;
+    int64_t ld;
+    __device__ __forceinline__ void load8(int64_t row, int c, float (&v)[8]) const {
+        const float4 a = *reinterpret_cast<const float4*>(p + row * ld + c);
+        const float4 b = *reinterpret_cast<const float4*>(p + row * ld + c + 4);
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+};
+
+// The gradient of an expert-input row: routed row r (dispatch order) is pair
+// perm[r] = t*k + s and holds gate(t, s) * dout[t]; shared-expert row Tk + t
+// holds dout[t]; both zero for a token whose replayed ids were rejected.
+struct SrcDy {
+    const uint16_t* dout;
+    const float* gates;
+    const int32_t* perm;
+    const int32_t* valid;
+    int k;
+    int64_t Tk;
+    int64_t ld;
+    __device__ __forceinline__ void load8(int64_t row, int c, float (&v)[8]) const {
+        int64_t t;
+        float w;
+        if (row < Tk) {
+            const int32_t pair = perm[row];
+            t = pair / k;
+            w = valid[t] ? gates[pair] : 0.0f;
+        } else {
+            t = row - Tk;
+            w = valid[t] ? 1.0f : 0.0f;
+        }
+        float x[8];
+        unpack8(*reinterpret_cast<const uint4*>(dout + t * ld + c), x);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = w * x[i];
+    }
+};
+
+// ---- row-wise quantisation: dY along d ----------------------------------------------
+
+// One warp per (row, 256-column chunk); lane l holds columns 8l .. 8l + 7.
+__global__ void __launch_bounds__(256) dy_rows_kernel(SrcDy src, uint16_t* __restrict__ out,
+                                                      int64_t rows, int d) {
+    const int lane = threadIdx.x & 31;
+    const int chunks = d / 256;
+    const int64_t items = rows * chunks;
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i < items;
+         i += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
+        const int64_t r = i / chunks;
+        const int c = static_cast<int>(i % chunks) * 256 + lane * 8;
+        float v[8];
+        src.load8(r, c, v);
+        const int X = mx_block_exp(block_amax4(absmax8(v)));
+        *reinterpret_cast<uint4*>(out + r * d + c) = mx_qdq8(v, X);
+    }
+}
+
+// ---- SwiGLU backward, then dA | dB quantised along F ---------------------------------
+
+// h = silu(a) * b with silu(a) = a * sigmoid(a):
+//   dA = dH * b * sigmoid(a) * (1 + a * (1 - sigmoid(a))),   dB = dH * silu(a).
+// Row r of dab holds [dA | dB] in fp32 (for the transposed quantiser) and row
+// r of dabq the same, quantised in blocks of 32 along F, as bf16.
+__global__ void __launch_bounds__(256) swiglu_bwd_kernel(
+    const float* __restrict__ dh, const float* __restrict__ A, const float* __restrict__ Bv,
+    float* __restrict__ dab, uint16_t* __restrict__ dabq, int64_t rows, int F) {
+    const int lane = threadIdx.x & 31;
+    const int chunks = F / 256;
+    const int64_t items = rows * chunks;
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i < items;
+         i += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
+        const int64_t r = i / chunks;
+        const int c = static_cast<int>(i % chunks) * 256 + lane * 8;
+        float g[8], a[8], b[8], da[8], db[8];
+        SrcF32{dh, F}.load8(r, c, g);
+        SrcF32{A, F}.load8(r, c, a);
+        SrcF32{Bv, F}.load8(r, c, b);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const float sg = 1.0f / (1.0f + expf(-a[j]));
+            da[j] = g[j] * b[j] * (sg * (1.0f + a[j] * (1.0f - sg)));
+            db[j] = g[j] * (a[j] * sg);
+        }
+        float* o = dab + r * 2 * F;
+        *reinterpret_cast<float4*>(o + c) = make_float4(da[0], da[1], da[2], da[3]);
+        *reinterpret_cast<float4*>(o + c + 4) = make_float4(da[4], da[5], da[6], da[7]);
+        *reinterpret_cast<float4*>(o + F + c) = make_float4(db[0], db[1], db[2], db[3]);
+        *reinterpret_cast<float4*>(o + F + c + 4) = make_float4(db[4], db[5], db[6], db[7]);
+        const int Xa = mx_block_exp(block_amax4(absmax8(da)));
+        const int Xb = mx_block_exp(block_amax4(absmax8(db)));
+        *reinterpret_cast<uint4*>(dabq + r * 2 * F + c) = mx_qdq8(da, Xa);
+        *reinterpret_cast<uint4*>(dabq + r * 2 * F + F + c) = mx_qdq8(db, Xb);
+    }
+}
+
+// ---- transposed quantisation (blocks of 32 along the rows) ----------------------------
+
+// Output column (the input's row axis) of a 32-row block, the input rows it
+// reads and how many of them exist.
+struct TqBlock {
+    int64_t in_row0;
+    int64_t out_col;  // element offset of the block's column 0 in the output
+    int nvalid;
+};
+
+struct TqArgs {
+    int C;        // input columns = output rows
+    int64_t ld;   // output row stride (elements)
+    uint16_t* out;
+    // segment mode: groups of rows, each padded to a multiple of 64 output
+    // columns starting at poff[g]; group g < E reads rows off[g] .. + cnt[g],
+    // group E (the shared expert) rows shared_row0 .. + shared_rows
+    const int32_t* cnt;
+    const int32_t* off;
+    const int32_t* poff;
+    int E, G;
+    int64_t shared_row0;
+    int shared_rows;
+    // batch mode: nb matrices of R rows; matrix b's block i -> output offset
+    // b * out_bstride + out_off + 32 i
+    int R;
+    int64_t out_bstride, out_off;
+    int64_t nblocks;  // 32-row blocks to visit
+};
+
+template <bool SEG>
+__device__ __forceinline__ bool tq_block(const TqArgs& a, int64_t rb, TqBlock& blk) {
+    if constexpr (SEG) {
+        const int64_t p = rb * 32;
+        if (p >= a.poff[a.G]) return false;
+        int lo = 0, hi = a.G;  // poff[lo] <= p < poff[lo + 1]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (a.poff[mid] <= p) lo = mid; else hi = mid;
+        }
+        const int local = static_cast<int>(p - a.poff[lo]);
+        const int n = lo < a.E ? a.cnt[lo] : a.shared_rows;
+        blk.in_row0 = (lo < a.E ? static_cast<int64_t>(a.off[lo]) : a.shared_row0) + local;
+        blk.nvalid = min(max(n - local, 0), 32);
+        blk.out_col = p;
+    } else {
+        const int per = a.R / 32;
+        const int64_t b = rb / per;
+        const int local = static_cast<int>(rb % per) * 32;
+        blk.in_row0 = b * a.R + local;
+        blk.nvalid = 32;
+        blk.out_col = b * a.out_bstride + a.out_off + local;
+    }
+    return true;
+}
+
+// CTA tile: one 32-row block x 64 columns.  Loading: thread t reads row t / 8,
+// columns 8 (t % 8) .. + 7.  Quantising: thread t takes column t / 4 and rows
+// 8 (t % 4) .. + 7 of it; the four threads of a column share the block
+// maximum and each writes 8 consecutive output elements (16 bytes).
+template <class Src, bool SEG>
+__global__ void __launch_bounds__(256) tq_kernel(Src src, TqArgs a) {
+    __shared__ float tile[32][65];
+    const int tid = threadIdx.x;
+    const int cchunks = a.C / 64;
+    const int64_t items = a.nblocks * cchunks;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int64_t rb = it / cchunks;
+        const int cb = static_cast<int>(it % cchunks) * 64;
+        TqBlock blk;
+        if (!tq_block<SEG>(a, rb, blk)) continue;  // uniform across the CTA
+        {
+            const int r = tid >> 3, c8 = (tid & 7) * 8;
+            float v[8];
+            if (r < blk.nvalid) {
+                src.load8(blk.in_row0 + r, cb + c8, v);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) tile[r][c8 + i] = v[i];
+        }
+        __syncthreads();
+        {
+            const int c = tid >> 2, part = tid & 3;
+            float v[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[i] = tile[part * 8 + i][c];
+            const int X = mx_block_exp(block_amax4(absmax8(v)));
+            *reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(cb + c) * a.ld + blk.out_col +
+                                      part * 8) = mx_qdq8(v, X);
+        }
+        __syncthreads();
+    }
+}
+
+// ---- padded segment offsets ----------------------------------------------------
+
+// poff[g + 1] = poff[g] + round_up(n_g, 64), n_g = cnt[g] for g < E and
+// shared_rows for the shared group; one warp.
+__global__ void seg_offsets_kernel(const int32_t* __restrict__ cnt, int E, int G, int shared_rows,
+                                   int32_t* __restrict__ poff) {
+    const int lane = threadIdx.x;
+    const int per = (G + 31) / 32;
+    const int g0 = lane * per;
+    int local = 0;
+    for (int g = g0; g < min(g0 + per, G); ++g) local += ((g < E ? cnt[g] : shared_rows) + 63) & ~63;
+    int incl = local;
+#pragma unroll
+    for (int s = 1; s < 32; s <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, s);
+        if (lane >= s) incl += v;
+    }
+    int run = incl - local;
+    for (int g = g0; g < min(g0 + per, G); ++g) {
+        poff[g] = run;
+        run += ((g < E ? cnt[g] : shared_rows) + 63) & ~63;
+    }
+    if (lane == 31) poff[G] = incl;
+}
+
+// ---- gate and router backward -------------------------------------------------------
+
+constexpr int kGateThreads = 256;
+constexpr int kMaxSlots = 8;
+
+// One CTA per token t:
+//   dg_s = dout[t] . Y[inv[t k + s]]                          (the gate gradient)
+//   dl_s = w_s (dg_s - sum_s' w_s' dg_s')                    (softmax over the chosen)
+//   dx[t] = sum_s dl_s Wr[ids[t, s]]   (the router's part of dx; s ascending)
+// All sums in a fixed order: per thread over its columns ascending, then a
+// fixed shuffle tree, then the warps in order.
+__global__ void __launch_bounds__(kGateThreads) gate_bwd_kernel(
+    const uint16_t* __restrict__ dout, const uint16_t* __restrict__ Y,
+    const int32_t* __restrict__ inv, const int32_t* __restrict__ ids,
+    const float* __restrict__ gates, const int32_t* __restrict__ valid,
+    const uint16_t* __restrict__ wr, float* __restrict__ dg_out, float* __restrict__ dl_out,
+    float* __restrict__ dx, int64_t T, int k, int d) {
+    __shared__ float part[kGateThreads / 32][kMaxSlots];
+    __shared__ float dl_s[kMaxSlots];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        float acc[kMaxSlots];
+        int64_t row[kMaxSlots];
+#pragma unroll
+        for (int s = 0; s < kMaxSlots; ++s) {
+            acc[s] = 0.0f;
+            row[s] = s < k ? inv[t * k + s] : 0;
+        }
+        for (int c = tid * 8; c < d; c += kGateThreads * 8) {
+            float g[8];
+            unpack8(*reinterpret_cast<const uint4*>(dout + t * d + c), g);
+#pragma unroll
+            for (int s = 0; s < kMaxSlots; ++s) {
+                if (s >= k) break;
+                float y[8];
+                unpack8(*reinterpret_cast<const uint4*>(Y + row[s] * d + c), y);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[s] = fmaf(g[i], y[i], acc[s]);
+            }
+        }
+#pragma unroll
+        for (int s = 0; s < kMaxSlots; ++s) {
+            float v = acc[s];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            if (lane == 0) part[warp][s] = v;
+        }
+        __syncthreads();
+        if (tid == 0) {
+            float dg[kMaxSlots], w[kMaxSlots];
+            float wdg = 0.0f;
+            for (int s = 0; s < k; ++s) {
+                float v = 0.0f;
+                for (int q = 0; q < kGateThreads / 32; ++q) v += part[q][s];
+                dg[s] = v;
+                w[s] = gates[t * k + s];
+                wdg = fmaf(w[s], v, wdg);
+            }
+            const bool ok = valid[t] != 0;
+            for (int s = 0; s < k; ++s) {
+                const float l = ok ? w[s] * (dg[s] - wdg) : 0.0f;
+                dl_s[s] = l;
+                dg_out[t * k + s] = ok ? dg[s] : 0.0f;
+                dl_out[t * k + s] = l;
+            }
+        }
+        __syncthreads();
+        for (int c = tid * 8; c < d; c += kGateThreads * 8) {
+            float o[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) o[i] = 0.0f;
+            for (int s = 0; s < k; ++s) {
+                const float l = dl_s[s];
+                float w8[8];
+                unpack8(*reinterpret_cast<const uint4*>(wr + static_cast<int64_t>(ids[t * k + s]) * d + c),
+                        w8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[i] = fmaf(l, w8[i], o[i]);
+            }
+            float* dst = dx + t * d + c;
+            *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<float4*>(dst + 4) = make_float4(o[4], o[5], o[6], o[7]);
+        }
+        __syncthreads();
+    }
+}
+
+// d_router[e] = sum over expert e's rows r (dispatch order) of dl[perm[r]] * Xp[r]:
+// thread = 8 columns of one expert, rows in ascending order.
+constexpr int kRouterWThreads = 128;
+__global__ void __launch_bounds__(kRouterWThreads) router_wgrad_kernel(
+    const uint16_t* __restrict__ xp, const int32_t* __restrict__ perm,
+    const int32_t* __restrict__ cnt, const int32_t* __restrict__ off,
+    const float* __restrict__ dl, float* __restrict__ d_router, int E, int d) {
+    const int cpb = kRouterWThreads * 8;
+    const int per_e = (d + cpb - 1) / cpb;
+    for (int it = blockIdx.x; it < E * per_e; it += gridDim.x) {
+        const int e = it / per_e;
+        const int c = (it % per_e) * cpb + threadIdx.x * 8;
+        if (c >= d) continue;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        const int64_t r0 = off[e], r1 = r0 + cnt[e];
+        for (int64_t r = r0; r < r1; ++r) {
+            const float l = dl[perm[r]];
+            float x[8];
+            unpack8(*reinterpret_cast<const uint4*>(xp + r * d + c), x);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc[i] = fmaf(l, x[i], acc[i]);
+        }
+        float* dst = d_router + static_cast<int64_t>(e) * d + c;
+        *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        *reinterpret_cast<float4*>(dst + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    }
+}
+
+// dx[t] = ((sum_s dXp[inv[t k + s]]) + dXp_shared[t]) + dx[t], the last term
+// being the router's part written by gate_bwd_kernel; s ascending.
+__global__ void __launch_bounds__(256) dx_assemble_kernel(
+    const float* __restrict__ dxp, const int32_t* __restrict__ inv, float* __restrict__ dx,
+    int64_t T, int k, int d, int has_shared) {
+    const int q = d / 4;
+    const int64_t Tk = T * k;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < T * q;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t t = i / q;
+        const int c = static_cast<int>(i % q) * 4;
+        float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        for (int s = 0; s < k; ++s) {
+            const float4 v = *reinterpret_cast<const float4*>(dxp + static_cast<int64_t>(inv[t * k + s]) * d + c);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        if (has_shared) {
+            const float4 v = *reinterpret_cast<const float4*>(dxp + (Tk + t) * d + c);
+            acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+        }
+        float4* o = reinterpret_cast<float4*>(dx + t * d + c);
+        const float4 r = *o;
+        acc.x += r.x; acc.y += r.y; acc.z += r.z; acc.w += r.w;
+        *o = acc;
+    }
+}
+
+inline int grid_for(int64_t items, int per_block, int sms, int per_sm = 8) {
+    int64_t b = (items + per_block - 1) / per_block;
+    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+    if (b > cap) b = cap;
+    return static_cast<int>(b < 1 ? 1 : b);
+}
+
+}  // namespace
+
+cudaError_t launch_seg_offsets(const int32_t* cnt, int E, int G, int shared_rows, int32_t* poff,
+                               cudaStream_t s) {
+    seg_offsets_kernel<<<1, 32, 0, s>>>(cnt, E, G, shared_rows, poff);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dy_rows(const uint16_t* dout, const float* gates, const int32_t* perm,
+                           const int32_t* valid, int64_t T, int k, int d, int n_shared,
+                           uint16_t* dyq, int sms, cudaStream_t s) {
+    if (d % 256) return cudaErrorInvalidValue;
+    const int64_t rows = T * k + T * n_shared;
+    if (rows == 0) return cudaSuccess;
+    SrcDy src{dout, gates, perm, valid, k, T * k, d};
+    dy_rows_kernel<<<grid_for(rows * (d / 256), 8, sms), 256, 0, s>>>(src, dyq, rows, d);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_bwd(const float* dh, const float* a, const float* b, float* dab,
+                              uint16_t* dabq, int64_t rows, int F, int sms, cudaStream_t s) {
+    if (F % 256) return cudaErrorInvalidValue;
+    if (rows == 0) return cudaSuccess;
+    swiglu_bwd_kernel<<<grid_for(rows * (F / 256), 8, sms), 256, 0, s>>>(dh, a, b, dab, dabq,
+                                                                        rows, F);
+    return cudaGetLastError();
+}
+
+namespace {
+template <class Src, bool SEG>
+cudaError_t tq_launch(const Src& src, const TqArgs& a, int sms, cudaStream_t s) {
+    if (a.C % 64 || a.ld % 8) return cudaErrorInvalidValue;
+    const int64_t items = a.nblocks * (a.C / 64);
+    if (items == 0) return cudaSuccess;
+    tq_kernel<Src, SEG><<<grid_for(items, 1, sms, 8), 256, 0, s>>>(src, a);
+    return cudaGetLastError();
+}
+}  // namespace
+
+cudaError_t launch_tq_segments(int src_kind, const void* src, int64_t src_ld, const SegDyArgs* dy,
+                               int C, const int32_t* cnt, const int32_t* off, const int32_t* poff,
+                               int E, int G, int64_t shared_row0, int shared_rows, int64_t kpad,
+                               uint16_t* out, int sms, cudaStream_t s) {
+    TqArgs a{};
+    a.C = C;
+    a.ld = kpad;
+    a.out = out;
+    a.cnt = cnt;
+    a.off = off;
+    a.poff = poff;
+    a.E = E;
+    a.G = G;
+    a.shared_row0 = shared_row0;
+    a.shared_rows = shared_rows;
+    a.nblocks = kpad / 32;
+    switch (src_kind) {
+        case TQ_SRC_BF16:
+            return tq_launch<SrcBf16, true>(SrcBf16{static_cast<const uint16_t*>(src), src_ld}, a, sms, s);
+        case TQ_SRC_F32:
+            return tq_launch<SrcF32, true>(SrcF32{static_cast<const float*>(src), src_ld}, a, sms, s);
+        case TQ_SRC_DY:
+            if (!dy) return cudaErrorInvalidValue;
+            return tq_launch<SrcDy, true>(
+                SrcDy{dy->dout, dy->gates, dy->perm, dy->valid, dy->k, dy->Tk, src_ld}, a, sms, s);
+        default:
+            return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_tq_batch(const uint16_t* src, int nb, int R, int C, uint16_t* out,
+                            int64_t out_bstride, int64_t out_ld, int64_t out_off, int sms,
+                            cudaStream_t s) {
+    if (R % 32) return cudaErrorInvalidValue;
+    TqArgs a{};
+    a.C = C;
+    a.ld = out_ld;
+    a.out = out;
+    a.R = R;
+    a.out_bstride = out_bstride;
+    a.out_off = out_off;
+    a.nblocks = static_cast<int64_t>(nb) * (R / 32);
+    if (out_off % 8 || out_bstride % 8) return cudaErrorInvalidValue;
+    return tq_launch<SrcBf16, false>(SrcBf16{src, C}, a, sms, s);
+}
+
+cudaError_t launch_gate_bwd(const uint16_t* dout, const uint16_t* y, const int32_t* inv,
+                            const int32_t* ids, const float* gates, const int32_t* valid,
+                            const uint16_t* wr, float* dg, float* dl, float* dx, int64_t T, int k,
+                            int d, int sms, cudaStream_t s) {
+    if (k > kMaxSlots || d % 8) return cudaErrorInvalidValue;
+    if (T == 0) return cudaSuccess;
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    const int grid = static_cast<int>(T < cap ? T : cap);
+    gate_bwd_kernel<<<grid, kGateThreads, 0, s>>>(dout, y, inv, ids, gates, valid, wr, dg, dl, dx,
+                                                  T, k, d);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_router_wgrad(const uint16_t* xp, const int32_t* perm, const int32_t* cnt,
+                                const int32_t* off, const float* dl, float* d_router, int E, int d,
+                                int sms, cudaStream_t s) {
+    if (d % 8) return cudaErrorInvalidValue;
+    const int cpb = kRouterWThreads * 8;
+    const int64_t items = static_cast<int64_t>(E) * ((d + cpb - 1) / cpb);
+    router_wgrad_kernel<<<grid_for(items, 1, sms, 16), kRouterWThreads, 0, s>>>(xp, perm, cnt, off,
+                                                                                dl, d_router, E, d);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dx_assemble(const float* dxp, const int32_t* inv, float* dx, int64_t T, int k,
+                               int d, int n_shared, int sms, cudaStream_t s) {
+    if (d % 4) return cudaErrorInvalidValue;
+    if (T == 0) return cudaSuccess;
+    dx_assemble_kernel<<<grid_for(T * (d / 4), 256, sms), 256, 0, s>>>(dxp, inv, dx, T, k, d,
+                                                                       n_shared);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

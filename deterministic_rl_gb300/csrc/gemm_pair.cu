@@ -892,20 +892,31 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                             if (row_ok && c0 + j < tl.n_valid) {
                                 const float g = v[j];
                                 const float h = g / (1.0f + expf(-g)) * u[j];
-                                H[static_cast<int64_t>(tl.brow + p.out_row_off + c0 + j) * p.ldo + row] =
-                                    __float2bfloat16_rn(h);
+                                const int64_t at =
+                                    static_cast<int64_t>(tl.brow + p.out_row_off + c0 + j) * p.ldo + row;
+                                H[at] = __float2bfloat16_rn(h);
+                                if (p.save_a) {  // the backward keeps the pre-activations
+                                    p.save_a[at] = g;
+                                    p.save_b[at] = u[j];
+                                }
                             }
                         }
                     }
                     xph ^= 1u;
                 } else {
-                    if (tl.shared) {
+                    if (tl.shared && p.out_shared) {
                         float* Ys = static_cast<float*>(p.out_shared);
                         const int tok0 = tl.brow - p.shared_b_off + c0;
 #pragma unroll
                         for (int j = 0; j < 32; ++j)
                             if (row_ok && c0 + j < tl.n_valid)
                                 Ys[static_cast<int64_t>(tok0 + j) * p.ldo + row] = v[j];
+                    } else if (!C::kConv && p.out_f32) {
+                        float* Yf = static_cast<float*>(p.out);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j)
+                            if (row_ok && c0 + j < tl.n_valid)
+                                Yf[static_cast<int64_t>(tl.brow + c0 + j) * p.ldo + row] = v[j];
                     } else {
                         __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll

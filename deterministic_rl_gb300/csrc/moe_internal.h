@@ -81,6 +81,13 @@ struct GemmParams {
     // gate/up: SwiGLU output row = token row of B + out_row_off (the shared
     // expert run on its own reads x directly and writes after the routed rows)
     int32_t out_row_off;
+    // SM-pair bf16 gate/up: if not null, also store the fp32 pre-activations
+    // (gate and up projections) of each H element, same indexing as H.
+    float* save_a;
+    float* save_b;
+    // SM-pair down (MODE 2): 1 = fp32 output rows; with out_shared null the
+    // shared group's rows are stored like routed rows (at its B rows).
+    int32_t out_f32;
 };
 
 size_t gemm_smem_bytes(int mode, int n_groups_total);
@@ -129,6 +136,79 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int64_t T, int
 // the fp32 row scales to rscale and, if not null, the E4M3 block scales.
 cudaError_t launch_nvfp4_qdq(const uint16_t* src, uint16_t* dst, uint8_t* bscale, float* rscale,
                              int64_t R, int K, int sms, cudaStream_t s);
+
+// ---- backward (backward.cu, wgrad.cu) ----
+
+// Grouped weight-gradient GEMM: for group g, out[g][n][m] = sum over the
+// group's K-blocks of A[m][k] * B[n][k] (a: [M][Kpad], b: [N][Kpad] bf16 maps
+// with 64 x 128 and 64 x 256 boxes), K range [poff[g], poff[g+1]) (multiples
+// of 64, zero-padded).  Rows n < n_split go to out0 (routed groups, group g at
+// + g * gstride) or sout0 (groups >= G_routed), rows n >= n_split (minus
+// n_split) to out1 / sout1.  Row stride M floats.
+struct WgradParams {
+    CUtensorMap a, b;
+    const int32_t* poff;
+    int32_t G, G_routed;
+    int32_t M, N, MT, NT, n_split;
+    float* out0;
+    float* out1;
+    float* sout0;
+    float* sout1;
+    int64_t gstride;
+    int32_t* status;
+    uint64_t timeout_ns;
+    int32_t stall_test;
+};
+constexpr int kMaxWgradGroups = 1024;
+cudaError_t launch_wgrad(const WgradParams& p, int grid, cudaStream_t s);
+int wgrad_tile_m();
+int wgrad_tile_n();
+
+// Padded segment offsets of the G = E (+1 shared) groups: poff[g + 1] =
+// poff[g] + round_up(n_g, 64).
+cudaError_t launch_seg_offsets(const int32_t* cnt, int E, int G, int shared_rows, int32_t* poff,
+                               cudaStream_t s);
+// dY rows (gate(t,s) * dout[t] for routed row perm^-1, dout[t] for shared row
+// Tk + t; zero for rejected tokens) quantised to MXFP8 along d -> bf16 rows.
+cudaError_t launch_dy_rows(const uint16_t* dout, const float* gates, const int32_t* perm,
+                           const int32_t* valid, int64_t T, int k, int d, int n_shared,
+                           uint16_t* dyq, int sms, cudaStream_t s);
+// SwiGLU backward: dab [rows][2F] fp32 = [dA | dB], dabq the same quantised
+// along F (bf16).
+cudaError_t launch_swiglu_bwd(const float* dh, const float* a, const float* b, float* dab,
+                              uint16_t* dabq, int64_t rows, int F, int sms, cudaStream_t s);
+// Transposed MXFP8 quantisation (blocks of 32 along the input's rows).
+enum TqSrc : int { TQ_SRC_BF16 = 0, TQ_SRC_F32 = 1, TQ_SRC_DY = 2 };
+struct SegDyArgs {
+    const uint16_t* dout;
+    const float* gates;
+    const int32_t* perm;
+    const int32_t* valid;
+    int k;
+    int64_t Tk;
+};
+// Segment mode: out[c][poff[g] + i] = Q(row i of group g)[c], groups padded
+// with zeros to their poff extent; out row stride kpad.
+cudaError_t launch_tq_segments(int src_kind, const void* src, int64_t src_ld, const SegDyArgs* dy,
+                               int C, const int32_t* cnt, const int32_t* off, const int32_t* poff,
+                               int E, int G, int64_t shared_row0, int shared_rows, int64_t kpad,
+                               uint16_t* out, int sms, cudaStream_t s);
+// Batch mode: nb matrices [R][C] bf16 -> out[b * out_bstride + c * out_ld +
+// out_off + r] quantised along r.
+cudaError_t launch_tq_batch(const uint16_t* src, int nb, int R, int C, uint16_t* out,
+                            int64_t out_bstride, int64_t out_ld, int64_t out_off, int sms,
+                            cudaStream_t s);
+// Gate gradients, softmax backward and the router's part of dx (written to dx).
+cudaError_t launch_gate_bwd(const uint16_t* dout, const uint16_t* y, const int32_t* inv,
+                            const int32_t* ids, const float* gates, const int32_t* valid,
+                            const uint16_t* wr, float* dg, float* dl, float* dx, int64_t T, int k,
+                            int d, int sms, cudaStream_t s);
+cudaError_t launch_router_wgrad(const uint16_t* xp, const int32_t* perm, const int32_t* cnt,
+                                const int32_t* off, const float* dl, float* d_router, int E, int d,
+                                int sms, cudaStream_t s);
+// dx[t] = (sum_s dxp[inv[t k + s]] + dxp[Tk + t]) + dx[t].
+cudaError_t launch_dx_assemble(const float* dxp, const int32_t* inv, float* dx, int64_t T, int k,
+                               int d, int n_shared, int sms, cudaStream_t s);
 
 // Fixed-order combine of each token's k expert rows and the shared row.
 cudaError_t launch_combine(const uint16_t* y, const float* ysh, const int32_t* inv,

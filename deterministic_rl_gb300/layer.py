@@ -32,6 +32,9 @@ class MoELayer:
         self.weights = B.make_weights(*self._tensors)
         self._ws = None
         self._ws_T = -1
+        self._wt = None      # the backward's weight copies (prepare_backward)
+        self._bws = None
+        self._bws_T = -1
 
     @classmethod
     def from_inputs(cls, inp, out_fp32: bool = False) -> "MoELayer":
@@ -118,3 +121,94 @@ class MoELayer:
             r["sxp"] = view(L.sxp, T * k, torch.float32)
             r["sh"] = view(L.sh, T * k, torch.float32)
         return r
+
+    # ---- backward -------------------------------------------------------------
+
+    def prepare_backward(self, stream=None) -> torch.Tensor:
+        """The weight copies the backward reads (quantised along its contraction
+        axes, transposed); call again after the weights change."""
+        n = B.moe_backward_weights_size(self.dims(1))
+        if n == 0:
+            raise B.MoEError(B.MOE_ERR_UNSUPPORTED, "moe_backward_weights_size")
+        if self._wt is None or self._wt.numel() < n:
+            self._wt = torch.empty(n, dtype=torch.uint8, device=self.device)
+        B.moe_backward_prepare_weights(self.dims(1), self.weights, self._wt, stream)
+        return self._wt
+
+    def backward_workspace(self, T: int) -> torch.Tensor:
+        if self._bws is None or T > self._bws_T:
+            n = B.moe_backward_workspace_size(self.dims(T))
+            if n == 0:
+                raise B.MoEError(B.MOE_ERR_SHAPE, "moe_backward_workspace_size")
+            self._bws = torch.empty(n, dtype=torch.uint8, device=self.device)
+            self._bws_T = T
+        return self._bws
+
+    def alloc_grads(self) -> dict:
+        E, d, F = self.E, self.d, self.F
+        f32 = dict(dtype=torch.float32, device=self.device)
+        g = {"d_router": torch.empty((E, d), **f32), "d_gate": torch.empty((E, F, d), **f32),
+             "d_up": torch.empty((E, F, d), **f32), "d_down": torch.empty((E, d, F), **f32)}
+        if self.n_shared:
+            g.update(ds_gate=torch.empty((F, d), **f32), ds_up=torch.empty((F, d), **f32),
+                     ds_down=torch.empty((d, F), **f32))
+        return g
+
+    def backward(self, x: torch.Tensor, ids: torch.Tensor, dout: torch.Tensor, stream=None,
+                 grads: Optional[dict] = None, dx: Optional[torch.Tensor] = None):
+        """Gradients for upstream gradient dout [T][d] bf16 with the forward's
+        ids [T][k]: returns (dx [T][d] fp32, dict of fp32 weight gradients).
+        Prepares the weight copies on first use."""
+        T = x.shape[0]
+        if self._wt is None:
+            self.prepare_backward(stream)
+        g = grads if grads is not None else self.alloc_grads()
+        if dx is None:
+            dx = torch.empty((T, self.d), dtype=torch.float32, device=self.device)
+        cg = B.make_grads(g["d_router"], g["d_gate"], g["d_up"], g["d_down"], g.get("ds_gate"),
+                          g.get("ds_up"), g.get("ds_down"))
+        B.moe_backward(self.dims(T), x, self.weights, self._wt, ids, dout, dx, cg,
+                       self.backward_workspace(T), stream)
+        return dx, g
+
+    def backward_status(self, stream=None) -> int:
+        return B.moe_get_status(self._bws, stream)
+
+    def backward_intermediates(self, T: int) -> dict:
+        """Views of the backward workspace's buffers after a backward of T tokens."""
+        L = B.moe_backward_workspace_layout(self.dims(T))
+        ws = self.backward_workspace(T)
+        k, E, d, F = self.k, self.E, self.d, self.F
+        rows = T * k + T * self.n_shared
+        kp = int(L.kpad)
+
+        def view(off, n, dt):
+            nbytes = n * torch.tensor([], dtype=dt).element_size()
+            return ws[off:off + nbytes].view(dt)
+
+        return {
+            "status": view(L.status, 4, torch.int32),
+            "valid": view(L.valid, T, torch.int32),
+            "cnt": view(L.cnt, E, torch.int32),
+            "off": view(L.off, E + 1, torch.int32),
+            "perm": view(L.perm, T * k, torch.int32),
+            "ids": view(L.ids, T * k, torch.int32).view(T, k),
+            "gates": view(L.gates, T * k, torch.float32).view(T, k),
+            "poff": view(L.poff, E + self.n_shared + 1, torch.int32),
+            "a": view(L.a, rows * F, torch.float32).view(rows, F),
+            "b": view(L.b, rows * F, torch.float32).view(rows, F),
+            "h": view(L.h, rows * F, torch.bfloat16).view(rows, F),
+            "y": view(L.y, T * k * d, torch.bfloat16).view(T * k, d),
+            "dg": view(L.dg, T * k, torch.float32).view(T, k),
+            "dl": view(L.dl, T * k, torch.float32).view(T, k),
+            "dyq": view(L.dyq, rows * d, torch.bfloat16).view(rows, d),
+            "dh": view(L.dh, rows * F, torch.float32).view(rows, F),
+            "dab": view(L.dab, rows * 2 * F, torch.float32).view(rows, 2 * F),
+            "dabq": view(L.dabq, rows * 2 * F, torch.bfloat16).view(rows, 2 * F),
+            "dxp": view(L.dxp, rows * d, torch.float32).view(rows, d),
+            "xpt": view(L.xpt, d * kp, torch.bfloat16).view(d, kp),
+            "dyt": view(L.dyt, d * kp, torch.bfloat16).view(d, kp),
+            "ht": view(L.ht, F * kp, torch.bfloat16).view(F, kp),
+            "dabt": view(L.dabt, 2 * F * kp, torch.bfloat16).view(2 * F, kp),
+        }
+

@@ -203,6 +203,29 @@ def make_layer(cfg: MoEConfig, device="cpu") -> LayerInputs:
                        s_gate, s_up, s_down, ws_gate, ws_up, ws_down, gs[0], gs[1], gs[2])
 
 
+def make_dout(cfg: MoEConfig, T: Optional[int] = None, device="cpu") -> torch.Tensor:
+    """The upstream gradient of the layer output for the backward: N(0, 1)
+    rounded to bf16, [T][d], from its own generator (seed cfg.seed + 7919)."""
+    device = torch.device(device)
+    gen = torch.Generator(device=device)
+    gen.manual_seed(cfg.seed + 7919)
+    T = cfg.T if T is None else T
+    return _randn((T, cfg.d), 1.0, gen, device).to(torch.bfloat16)
+
+
+def make_replay_ids(cfg: MoEConfig, T: Optional[int] = None, device="cpu") -> torch.Tensor:
+    """Recorded expert ids for replay: per token k distinct experts drawn
+    without replacement, with probability proportional to (e + 1)^-zipf
+    (uniform when cfg.zipf == 0), [T][k] int32, from their own generator
+    (seed cfg.seed + 104729)."""
+    gen = torch.Generator()
+    gen.manual_seed(cfg.seed + 104729)
+    T = cfg.T if T is None else T
+    p = (torch.arange(cfg.E, dtype=torch.float64) + 1.0) ** (-cfg.zipf)
+    ids = torch.multinomial(p.expand(T, cfg.E), cfg.k, replacement=False, generator=gen)
+    return ids.to(torch.int32).to(device)
+
+
 def bf16_bits(t: torch.Tensor):
     """bf16 tensor -> numpy uint16 bit patterns (host copy)."""
     import numpy as np

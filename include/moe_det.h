@@ -277,6 +277,87 @@ moe_status moe_set_stage_events(void *const *events);
 moe_status moe_route_static(const moe_dims *dims, const void *x, const moe_weights *w,
                             int32_t *ids_out, float *gates_out, moe_stream_t stream);
 
+/* ---- Backward ------------------------------------------------------------
+ *
+ * The gradient of the layer above for an upstream gradient dout, with the
+ * expert ids held fixed (the ids the forward used: its ids_out, own or
+ * replayed).  [TR] §6.1, Kernels paragraph: the MoE backward runs its grouped
+ * GEMMs in standard MXFP8 -- E4M3 values with one E8M0 scale per block of 32
+ * elements (OCP Microscaling Formats v1.0: shared exponent
+ * X = floor(log2 max|v|) - 8, elements E4M3(v / 2^X), nearest even, clamped
+ * to +-448).  Each grouped-GEMM operand is quantised along that GEMM's
+ * contraction axis:
+ *     dH  = Q_d(dY) . Q_d(Wd)                    dY = gate * dout (routed rows)
+ *     dXp = Q_F(dA) . Q_F(Wg) + Q_F(dB) . Q_F(Wu) dA, dB: SwiGLU backward of dH
+ *     dWd = Q_tok(dY)^T . Q_tok(H)
+ *     dWg = Q_tok(dA)^T . Q_tok(Xp),  dWu = Q_tok(dB)^T . Q_tok(Xp)
+ * where along tokens an expert's blocks start at its first row in dispatch
+ * order (pairs t*k + s ascending), the last block zero-padded.  The products
+ * are exact and accumulate in fp32 (tcgen05, TMEM).  The gate and router
+ * gradients are not grouped GEMMs and are taken in fp32 from the forward's
+ * values: dg_s = dout . Y_s (Y the forward's bf16 expert output),
+ * dl_s = w_s (dg_s - sum_s' w_s' dg_s'), d_router[e] = sum over e's rows of
+ * dl * x, and dx gets sum_s dl_s Wr[ids_s].  The router bias is an input, not
+ * a parameter: it has no gradient.  A token whose replayed ids are rejected
+ * has a zero forward row and contributes nothing.
+ *
+ * dx [T][d] fp32 = (sum_s dXp[slot s] + dXp_shared) + router part, slots
+ * ascending; its row for a token depends only on that token (batch
+ * invariant).  Weight gradients are fp32 and are written, not accumulated
+ * into; each element is one CTA's fixed-order K loop (bitwise repeatable).
+ *
+ * Limits: bf16 expert weights (MOE_ERR_UNSUPPORTED otherwise); d and F
+ * multiples of 256 (MOE_ERR_SHAPE otherwise); the other limits of the forward.
+ */
+typedef struct {
+    float *d_router;                  /* [E][d]                                  */
+    float *d_gate, *d_up;             /* [E][F][d]                               */
+    float *d_down;                    /* [E][d][F]                               */
+    float *ds_gate, *ds_up, *ds_down; /* shared expert: [F][d], [F][d], [d][F];  */
+                                      /* NULL when n_shared == 0                 */
+} moe_grads;
+
+/* Bytes of the backward's weight copies (see moe_backward_prepare_weights);
+ * 0 for dims the backward does not serve. */
+size_t moe_backward_weights_size(const moe_dims *dims);
+
+/* The expert weights quantised along the backward's contraction axes and
+ * transposed, into wt (device, caller-owned, moe_backward_weights_size bytes,
+ * 16-byte aligned): per expert Q_d(Wd)^T [F][d], then [Q_F(Wg)^T | Q_F(Wu)^T]
+ * [d][2F], then the same for the shared expert, as bf16 holding the exact
+ * MXFP8 values.  Depends on the weights only: call it once per weight update
+ * and pass wt to every moe_backward with those weights. */
+moe_status moe_backward_prepare_weights(const moe_dims *dims, const moe_weights *w, void *wt,
+                                        size_t wt_bytes, moe_stream_t stream);
+
+/* Workspace bytes of moe_backward (0 for dims it does not serve). */
+size_t moe_backward_workspace_size(const moe_dims *dims);
+
+/* Offsets (bytes into the backward workspace) of its regions; the first ones
+ * are those of the forward workspace (moe_ws_layout), so moe_get_status reads
+ * a backward workspace too.  Regions after a call: ids/gates the routing
+ * used, poff [E+S+1] int32 padded token offsets per expert, a/b [rows][F]
+ * fp32 gate/up pre-activations, dg/dl [T][k] fp32 gate and logit gradients,
+ * dyq [rows][d], dh [rows][F] fp32, dab [rows][2F] fp32 (dA | dB), dabq,
+ * dxp [rows][d] fp32, and the token-major operands xpt, dyt [d][kpad],
+ * ht [F][kpad], dabt [2F][kpad] (bf16), rows = T*k + T*n_shared. */
+typedef struct {
+    size_t status, logits, valid, cnt, off, perm, inv, xp, h, y;
+    size_t ids, gates, poff, a, b, dg, dl, dyq, dh, dab, dabq, dxp, xpt, dyt, ht, dabt;
+    size_t kpad; /* elements per row of the token-major operands */
+    size_t total;
+} moe_bwd_ws_layout;
+moe_status moe_backward_workspace_layout(const moe_dims *dims, moe_bwd_ws_layout *layout);
+
+/* The backward.  x [T][d] bf16, w (bf16 experts), wt (prepared from w), ids
+ * [T][k] int32 (the forward's ids), dout [T][d] bf16 -> dx [T][d] fp32 and the
+ * weight gradients in *grads (all device pointers).  Replayed ids are checked
+ * as in moe_forward_replay (moe_get_status reports MOE_ERR_BAD_IDS).
+ * Stream-ordered; no synchronisation. */
+moe_status moe_backward(const moe_dims *dims, const void *x, const moe_weights *w,
+                        const void *wt, const int32_t *ids, const void *dout, float *dx,
+                        const moe_grads *grads, void *ws, size_t ws_bytes, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -181,3 +181,59 @@ def make_near_ties(inp, frac: float, seed: int, margin: float = 1e-4):
     noise = torch.randn(x_new.shape, generator=g, device=inp.x.device) * inp.cfg.replay_noise
     x_rep = (x_new.float() + noise).to(torch.bfloat16)
     return x_new, idx, x_rep, done
+
+
+# ---- backward -------------------------------------------------------------------
+
+def _f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().to(torch.float64).cpu().numpy()
+
+
+def expert_values_getter(inp):
+    from oracle.backward import ExpertValues
+
+    def get(e: int):
+        return ExpertValues(_f64(inp.w_gate[e]), _f64(inp.w_up[e]), _f64(inp.w_down[e]))
+    return get
+
+
+def shared_values(inp):
+    from oracle.backward import ExpertValues
+    if inp.ws_gate is None:
+        return []
+    return [ExpertValues(_f64(inp.ws_gate), _f64(inp.ws_up), _f64(inp.ws_down))]
+
+
+def oracle_backward(inp, ids, dout, valid=None, **limits):
+    """The fp64 backward oracle on the layer's (bf16) inputs, ids [T][k] and
+    dout [T][d] (device or host tensors)."""
+    from oracle import backward
+    bias = None if inp.router_bias is None else _f64(inp.router_bias)
+    ids_np = ids.cpu().numpy() if isinstance(ids, torch.Tensor) else np.asarray(ids)
+    return backward.layer_backward(_f64(inp.x), _f64(inp.w_router), bias,
+                                   expert_values_getter(inp), shared_values(inp), ids_np,
+                                   _f64(dout), valid=valid, **limits)
+
+
+# Gradient comparison: relative Frobenius error <= 5e-3 (as for the forward
+# output) and every element within 3e-2 of the tensor's largest magnitude.
+# The GPU multiplies the same MXFP8 values as the oracle, so the difference is
+# fp32 accumulation order plus rare E4M3 code flips where an fp32 operand lies
+# within its rounding error of a rounding boundary (one E4M3 step, <= 2^-3 of
+# one operand element, in a few elements).
+GRAD_REL_FRO = 5e-3
+GRAD_MAX_ABS_REL = 3e-2
+
+
+def check_grad(name: str, gpu, ref: np.ndarray):
+    g = gpu.detach().to(torch.float64).cpu().numpy() if isinstance(gpu, torch.Tensor) else gpu
+    assert g.shape == ref.shape, (name, g.shape, ref.shape)
+    assert np.isfinite(g).all(), name
+    scale = float(np.abs(ref).max())
+    if scale == 0.0:
+        assert not g.any(), f"{name}: expected all zeros"
+        return
+    rel = float(np.linalg.norm(g - ref) / np.linalg.norm(ref))
+    mx = float(np.abs(g - ref).max())
+    assert rel <= GRAD_REL_FRO, f"{name}: relative Frobenius error {rel:.3e}"
+    assert mx <= GRAD_MAX_ABS_REL * scale, f"{name}: max-abs error {mx:.3e} (scale {scale:.3e})"

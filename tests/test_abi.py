@@ -142,3 +142,71 @@ def test_status_strings(lib):
         s = B.moe_status_str(code)
         assert s.startswith("MOE_")
     assert "unknown" in B.moe_status_str(99)
+
+
+# ---- backward ----------------------------------------------------------------
+
+def test_backward_sizes_and_layout(lib):
+    d = good_dims(T=4096)
+    n = B.moe_backward_workspace_size(d)
+    L = B.moe_backward_workspace_layout(d)
+    assert L.total == n > B.moe_workspace_size(d)
+    offs = [L.status, L.logits, L.valid, L.cnt, L.off, L.perm, L.inv, L.xp, L.h, L.y, L.ids,
+            L.gates, L.poff, L.a, L.b, L.dg, L.dl, L.dyq, L.dh, L.dab, L.dabq, L.dxp, L.xpt, L.dyt,
+            L.ht, L.dabt]
+    assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
+    rows = 4096 * 9
+    assert L.kpad % 64 == 0 and L.kpad >= rows + 63 * 385
+    assert L.xpt - L.dxp >= rows * 7168 * 4
+    assert n - L.dabt >= 2 * 2048 * L.kpad * 2
+    # the forward's status word sits at the same place
+    assert L.status == B.moe_workspace_layout(d).status
+    assert B.moe_backward_weights_size(d) >= (3 * 384 + 3) * 2048 * 7168 * 2
+    assert B.moe_backward_weights_size(good_dims(n_shared=0)) < B.moe_backward_weights_size(d)
+
+
+@pytest.mark.parametrize("bad", [dict(d=7168 - 64), dict(F=2048 + 64), dict(k=4), dict(wfmt=1),
+                                 dict(wfmt=2)])
+def test_backward_unserved_dims(lib, bad):
+    d = good_dims(**bad)
+    assert B.moe_backward_workspace_size(d) == 0
+    assert B.moe_backward_weights_size(d) == 0
+    with pytest.raises(B.MoEError):
+        B.moe_backward_workspace_layout(d)
+
+
+def _bwd(lib, dims=None, x=_Fake(0x1000), w=None, wt=_Fake(0x90000), ids=_Fake(0x3000),
+         dout=_Fake(0x5000), dx=_Fake(0x6000), grads=None, ws=_DEFAULT_WS, ws_bytes=None):
+    dims = dims or good_dims()
+    w = w or _weights()
+    grads = grads or B.moe_grads(0xA000, 0xB000, 0xC000, 0xD000, 0xE000, 0xF000, 0x11000)
+    nbytes = ws_bytes if ws_bytes is not None else (B.moe_backward_workspace_size(dims) or 1)
+    v = lambda p: ctypes.c_void_p(p.data_ptr() if p is not None else None)  # noqa: E731
+    return lib.moe_backward(ctypes.byref(dims.c()), v(x), ctypes.byref(w), v(wt), v(ids), v(dout),
+                            v(dx), ctypes.byref(grads), v(ws), nbytes, ctypes.c_void_p(None))
+
+
+def test_backward_host_validation_codes(lib):
+    assert _bwd(lib, dims=good_dims(T=0)) == B.MOE_OK
+    assert _bwd(lib, x=None) == B.MOE_ERR_ARG
+    assert _bwd(lib, wt=None) == B.MOE_ERR_ARG
+    assert _bwd(lib, ids=None) == B.MOE_ERR_ARG
+    assert _bwd(lib, dout=None) == B.MOE_ERR_ARG
+    assert _bwd(lib, dx=None) == B.MOE_ERR_ARG
+    assert _bwd(lib, ws=None) == B.MOE_ERR_ARG
+    assert _bwd(lib, w=_weights(w_down=None)) == B.MOE_ERR_ARG
+    assert _bwd(lib, grads=B.moe_grads(0xA000, 0xB000, 0xC000, 0xD000, None, None, None)) == B.MOE_ERR_ARG
+    assert _bwd(lib, dims=good_dims(n_shared=0),
+                grads=B.moe_grads(0xA000, 0xB000, 0xC000, 0xD000, None, None, None),
+                ws_bytes=1) == B.MOE_ERR_WORKSPACE
+    assert _bwd(lib, dout=_Fake(0x5008)) == B.MOE_ERR_ALIGN
+    assert _bwd(lib, grads=B.moe_grads(0xA004, 0xB000, 0xC000, 0xD000, 0xE000, 0xF000, 0x11000)) == B.MOE_ERR_ALIGN
+    assert _bwd(lib, ws_bytes=B.moe_backward_workspace_size(good_dims()) - 1) == B.MOE_ERR_WORKSPACE
+    assert _bwd(lib, dims=good_dims(wfmt=1)) == B.MOE_ERR_UNSUPPORTED
+    assert _bwd(lib, dims=good_dims(d=7168 - 64)) == B.MOE_ERR_SHAPE
+    # preparing the weight copies: short buffer, null weights
+    d = good_dims()
+    assert lib.moe_backward_prepare_weights(ctypes.byref(d.c()), ctypes.byref(_weights()),
+                                            ctypes.c_void_p(0x90000), 16, None) == B.MOE_ERR_WORKSPACE
+    assert lib.moe_backward_prepare_weights(ctypes.byref(d.c()), ctypes.byref(_weights(w_up=None)),
+                                            ctypes.c_void_p(0x90000), 1 << 40, None) == B.MOE_ERR_ARG
