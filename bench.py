@@ -9,7 +9,12 @@ top-8, expert FFN 2048, one shared expert, bf16 weights, recorded ids from a
 perturbed copy of the hidden states.  Prints one JSON line (rank 0).
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--config NAME] [--mode replay|own]
+                  [--config NAME] [--mode replay|own] [--pass forward|backward]
+
+--pass backward times the layer backward instead (MXFP8 expert GEMMs; one
+step = the weight copies quantised along the backward's contraction axes,
+then the whole backward of one batch with recorded ids), by default on the
+32k-token training layer.
 
 Under torchrun each rank runs its own batch on its own GPU (weak scaling, no
 collective on the data path; a barrier and a max over ranks for timing).
@@ -32,6 +37,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s (384-expert top-8, d=7168, replay, bf16); % of roofline"
+BWD_METRIC = ("MoE-layer backward tokens/s (384-expert top-8, d=7168, MXFP8 expert GEMMs, "
+              "recorded ids); % of roofline")
 UNIT = "tokens/s"
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -62,17 +69,25 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", default="c2_decode_replay")
+    ap.add_argument("--config", default=None,
+                    help="default: c2_decode_replay (forward), c4_train_32k (backward)")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward")
     ap.add_argument("--mode", choices=["replay", "own"], default="replay")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (small captures for the profiler)")
     ap.add_argument("--tokens", type=int, default=0,
                     help="override the token count (small captures for the profiler)")
-    ap.add_argument("--cpu-sample", type=int, default=64,
-                    help="tokens of the workload the CPU-baseline oracle runs on")
+    ap.add_argument("--cpu-sample", type=int, default=0,
+                    help="tokens of the workload the CPU-baseline oracle runs on "
+                         "(default 64 forward, 2 backward)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.config is None:
+        args.config = "c4_train_32k" if args.pass_ == "backward" else "c2_decode_replay"
+    if not args.cpu_sample:
+        args.cpu_sample = 2 if args.pass_ == "backward" else 64
+    return args
 
 
 def peaks():
@@ -498,8 +513,271 @@ def run_ours(args):
     return 0
 
 
+# ---- backward ----------------------------------------------------------------------
+
+def backward_kernel_flops(cfg):
+    """Algorithmic FLOPs of each grouped-GEMM launch of one backward."""
+    T, d, k, F, S = cfg.T, cfg.d, cfg.k, cfg.F, cfg.n_shared
+    rows = T * k + T * S
+    return {"gate_up": 4.0 * d * F * rows, "down": 2.0 * d * F * T * k, "dh": 2.0 * d * F * rows,
+            "dxp": 4.0 * d * F * rows, "wgrad_down": 2.0 * d * F * rows,
+            "wgrad_gate_up": 4.0 * d * F * rows}
+
+
+def backward_work(cfg):
+    """Algorithmic FLOPs and bytes of one backward step: the grouped GEMMs,
+    the router and gate gradients; every expert weight read once, every weight
+    gradient written once (fp32), x and dout read, dx written."""
+    T, d, E, k, F, S = cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.n_shared
+    flops = sum(backward_kernel_flops(cfg).values()) + 2.0 * T * E * d + 6.0 * T * k * d
+    nbytes = ((E + S) * 3 * d * F * (2 + 4) + E * d * (2 + 4) + T * d * (2 + 2 + 4)
+              + T * k * 4)
+    return flops, nbytes
+
+
+def backward_launches(cfg):
+    """Our kernels per backward step: weight copies (3, +3 for the shared
+    expert); router GEMM, top-k; dispatch (1 or 3); padded offsets; gather;
+    gate/up and down recompute; gate backward; router weight gradient; dY
+    quantiser; dH; SwiGLU backward; dXp; dx; four transposed quantisers; two
+    weight-gradient GEMMs."""
+    prep = 3 + 3 * cfg.n_shared
+    disp = 1 if cfg.T * cfg.k <= DISPATCH_SEGMENT_PAIRS else 3
+    return prep + 2 + disp + 1 + 1 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 4 + 2
+
+
+def _bwd_cfg(args):
+    from deterministic_rl_gb300.synthetic import CONFIGS
+    cfg = CONFIGS[args.config]
+    if args.experts:
+        cfg = cfg.with_(name=f"{cfg.name}_E{args.experts}", E=args.experts)
+    if args.tokens:
+        cfg = cfg.with_(name=f"{cfg.name}_T{args.tokens}", T=args.tokens)
+    return cfg
+
+
+def backward_workload_desc(cfg):
+    return (f"{cfg.name} backward: T={cfg.T} d={cfg.d} E={cfg.E} top-{cfg.k} F={cfg.F} "
+            f"shared={cfg.n_shared} bf16 weights, MXFP8 expert GEMMs, recorded ids")
+
+
+def oracle_backward_sample(inp, n):
+    """Host inputs of the backward oracle on the first n tokens: fp64 values of
+    x, the router, dout, the recorded ids and the experts they use."""
+    import numpy as np
+    import torch
+    from oracle.backward import ExpertValues
+    from deterministic_rl_gb300.synthetic import make_dout, make_replay_ids
+    f64 = lambda t: t.detach().to(torch.float64).cpu().numpy()  # noqa: E731
+    cfg = inp.cfg
+    ids = make_replay_ids(cfg)[:n].numpy()
+    dout = f64(make_dout(cfg, device=inp.x.device)[:n])
+    cache = {e: ExpertValues(f64(inp.w_gate[e]), f64(inp.w_up[e]), f64(inp.w_down[e]))
+             for e in sorted(set(ids.reshape(-1).tolist()))}
+    shared = ([ExpertValues(f64(inp.ws_gate), f64(inp.ws_up), f64(inp.ws_down))]
+              if inp.ws_gate is not None else [])
+    bias = None if inp.router_bias is None else f64(inp.router_bias)
+    return f64(inp.x[:n]), f64(inp.w_router), bias, ids, dout, cache, shared
+
+
+def time_oracle_backward(inp, n, min_seconds=10.0):
+    """The backward oracle (every gradient of an n-token batch) repeated until
+    about min_seconds of CPU work; tokens/s."""
+    from oracle import backward as OB
+    x, wr, bias, ids, dout, cache, shared = oracle_backward_sample(inp, n)
+    passes = 0
+    t0 = time.perf_counter()
+    while True:
+        OB.layer_backward(x, wr, bias, lambda e: cache[e], shared, ids, dout)
+        passes += 1
+        dt = time.perf_counter() - t0
+        if dt >= min_seconds or passes >= 100:
+            break
+    return n * passes / dt, os.cpu_count() or 1, dt, passes
+
+
+def run_backward_reference(args):
+    """The backward oracle as it stands on host cores: each step is the whole
+    backward of one token of the workload (cycling over the first 4)."""
+    import torch
+    from oracle import backward as OB
+    from deterministic_rl_gb300.synthetic import make_layer
+    world, rank, _ = dist_setup(args)
+    if rank != 0:
+        return 0
+    cfg = _bwd_cfg(args)
+    inp = make_layer(cfg, "cuda" if torch.cuda.is_available() else "cpu")
+    pool = 4
+    x, wr, bias, ids, dout, cache, shared = oracle_backward_sample(inp, pool)
+
+    def step(i):
+        j = i % pool
+        OB.layer_backward(x[j:j + 1], wr, bias, lambda e: cache[e], shared, ids[j:j + 1],
+                          dout[j:j + 1])
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    cores = os.cpu_count() or 1
+    sample = (f"1 token per step, cycling over the first {pool} tokens of {cfg.name}; fp64 numpy "
+              f"backward oracle (every gradient of the token), up to {cores} host threads")
+    line = {"impl": "reference", "metric": BWD_METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": backward_workload_desc(cfg)},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_backward_ours(args):
+    import torch
+    from deterministic_rl_gb300 import MoELayer, binding as B, build as lib_build
+    from deterministic_rl_gb300.synthetic import make_dout, make_layer, make_replay_ids
+    world, rank, local = dist_setup(args)
+    lib_build.build()
+    cfg = _bwd_cfg(args)
+    # weak scaling: every rank runs its own batch (seed offset by rank)
+    rcfg = cfg.with_(seed=cfg.seed + 1000 * rank) if rank else cfg
+    inp = make_layer(rcfg, "cuda")
+    layer = MoELayer.from_inputs(inp)
+    T, K = cfg.T, args.steps
+    ids = make_replay_ids(rcfg, device="cuda")
+    dout = make_dout(rcfg, device="cuda")
+    grads = layer.alloc_grads()
+    dx = torch.empty((T, cfg.d), dtype=torch.float32, device="cuda")
+
+    def step(x=inp.x, i=ids, g=dout):
+        layer.prepare_backward()
+        layer.backward(x, i, g, grads=grads, dx=dx)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if layer.backward_status() != 0:
+        raise RuntimeError(f"device status after warm-up: {B.status_str(layer.backward_status())}")
+    flops, nbytes = backward_work(cfg)
+    ns = len(B.BWD_STAGES)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * ns)] for _ in range(K)]
+    for row in evs:
+        for e in row:
+            e.record()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        start.record()
+        for i in range(K):
+            B.moe_set_backward_stage_events(evs[i])
+            step()
+        end.record()
+        torch.cuda.synchronize()
+    B.moe_set_backward_stage_events(None)
+    barrier(world)
+    if layer.backward_status() != 0:
+        raise RuntimeError(f"device status after timing: {B.status_str(layer.backward_status())}")
+    t_ms = max_over_ranks(world, start.elapsed_time(end))
+    ms_per_step = t_ms / K
+    value = world * T * K / (t_ms / 1e3)
+    stage_ms = {name: statistics.fmean(evs[i][2 * j].elapsed_time(evs[i][2 * j + 1])
+                                       for i in range(K))
+                for j, name in enumerate(B.BWD_STAGES)}
+
+    pk, pk_kind = peaks()
+    hbm = float(pk["hbm_gbs"])
+    tensor = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    tensor_s = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    kf = backward_kernel_flops(cfg)
+    kernels = {n: {"ms": stage_ms[n], "tflops": kf[n] / (stage_ms[n] / 1e3) / 1e12,
+                   "frac": kf[n] / (stage_ms[n] / 1e3) / 1e12 / tensor} for n in kf}
+    dom = max(kf, key=lambda n: stage_ms[n])
+    knames = {"gate_up": "pair_gemm_kernel<GEMM_SWIGLU, bf16> (gate/up recompute, keeps pre-activations)",
+              "down": "pair_gemm_kernel<GEMM_DOWN, bf16> (routed expert outputs)",
+              "dh": "pair_gemm_kernel<GEMM_DOWN, bf16> (dH = Q(dY) Q(Wd), fp32 rows)",
+              "dxp": "pair_gemm_kernel<GEMM_DOWN, bf16> (dXp, K = 2F, fp32 rows)",
+              "wgrad_down": "wgrad_kernel (dWd, ragged K)",
+              "wgrad_gate_up": "wgrad_kernel (dWg and dWu, ragged K)"}
+    achieved = kernels[dom]["tflops"]
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": tensor, "unit": "TFLOP/s",
+                "frac": achieved / tensor, "traffic": None, "kernel": knames[dom],
+                "algorithmic_flops_per_launch": kf[dom], "avg_launch_ms": stage_ms[dom],
+                "frac_of_sustained": achieved / tensor_s,
+                "peak_source": f"{pk_kind} (MEASURED_PEAKS.json bf16_tflops, burst)"
+                if pk_kind == "measured" else "fallback 1.9 PFLOP/s"}
+    t_roof = max(flops / (tensor * 1e12), nbytes / (hbm * 1e9))
+    layer_roof = {"flops": flops, "bytes": nbytes,
+                  "bound": "tensor" if flops / (tensor * 1e12) > nbytes / (hbm * 1e9) else "hbm",
+                  "roofline_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_per_step,
+                  "frac_of_sustained": 1e3 * max(flops / (tensor_s * 1e12), nbytes / (hbm * 1e9))
+                  / ms_per_step,
+                  "peaks": f"{pk_kind}: {hbm} GB/s, {tensor} TFLOP/s bf16 burst, "
+                           f"{tensor_s} sustained",
+                  "note": "bf16 tensor peak: the MMAs multiply the exact MXFP8 values in bf16"}
+
+    e2e = None
+    if not args.no_e2e:
+        x_h = inp.x.cpu().pin_memory()
+        ids_h = ids.cpu().pin_memory()
+        dout_h = dout.cpu().pin_memory()
+        dx_h = torch.empty(dx.shape, dtype=dx.dtype, pin_memory=True)
+        x_d, ids_d, dout_d = torch.empty_like(inp.x), torch.empty_like(ids), torch.empty_like(dout)
+        Ke = max(1, min(K, 20))
+        barrier(world)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(Ke):
+            x_d.copy_(x_h, non_blocking=True)
+            ids_d.copy_(ids_h, non_blocking=True)
+            dout_d.copy_(dout_h, non_blocking=True)
+            step(x_d, ids_d, dout_d)
+            dx_h.copy_(dx, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+        dt = max_over_ranks(world, time.perf_counter() - t0)
+        e2e = {"value": world * T * Ke / dt, "unit": UNIT,
+               "h2d_bytes_per_step": x_h.numel() * 2 + ids_h.numel() * 4 + dout_h.numel() * 2,
+               "d2h_bytes_per_step": dx_h.numel() * 4, "steps": Ke,
+               "api": "MoELayer.prepare_backward + MoELayer.backward -> "
+                      "moe_backward_prepare_weights + moe_backward (C ABI), pinned host buffers; "
+                      "weight gradients stay on the device"}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n = min(T, args.cpu_sample)
+        v, cores, dt, passes = time_oracle_backward(inp, n)
+        cpu = {"value": v, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"first {n} tokens of {cfg.name} (every gradient of that batch), "
+                         f"{passes} fp64 numpy backward-oracle passes, {dt:.1f} s"}
+
+    if rank == 0:
+        line = {"metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                "config": {"workload": backward_workload_desc(cfg), "tokens_per_step": T,
+                           "parallelism": f"replicas x{world} (own batch per GPU, no collective)",
+                           "l2": f"inputs larger than L2: {nbytes / 1e9:.1f} GB moved per step"},
+                "roofline": roofline, "layer_roofline": layer_roof, "kernels": kernels,
+                "stages_ms": stage_ms, "clocks": clk.summary(), "e2e": e2e,
+                "gpu_launches": backward_launches(cfg) * K, "cpu_baseline": cpu}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def main():
     args = parse()
+    if args.pass_ == "backward":
+        if args.impl == "reference":
+            return run_backward_reference(args)
+        return run_backward_ours(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

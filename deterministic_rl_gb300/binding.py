@@ -36,9 +36,11 @@ EXPORTED = ("moe_workspace_size", "moe_workspace_layout", "moe_route", "moe_forw
             "moe_forward_replay", "moe_get_status", "moe_status_str", "moe_set_stage_events",
             "moe_route_static", "moe_forward_replay_filtered", "moe_backward_weights_size",
             "moe_backward_prepare_weights", "moe_backward_workspace_size",
-            "moe_backward_workspace_layout", "moe_backward")
+            "moe_backward_workspace_layout", "moe_set_backward_stage_events", "moe_backward")
 
 STAGES = ("router_gemm", "topk", "dispatch", "gather", "gate_up", "down", "combine")
+BWD_STAGES = ("prepare", "route", "dispatch", "gate_up", "down", "gate", "dy", "dh", "swiglu",
+              "dxp", "dx", "transpose", "wgrad_down", "wgrad_gate_up")
 
 
 class moe_dims(ctypes.Structure):
@@ -121,6 +123,8 @@ def load(path: str = LIB_PATH):
     lib.moe_backward_workspace_size.argtypes = [D]
     lib.moe_backward_workspace_layout.restype = ctypes.c_int
     lib.moe_backward_workspace_layout.argtypes = [D, ctypes.POINTER(moe_bwd_ws_layout)]
+    lib.moe_set_backward_stage_events.restype = ctypes.c_int
+    lib.moe_set_backward_stage_events.argtypes = [ctypes.c_void_p]
     lib.moe_backward.restype = ctypes.c_int
     lib.moe_backward.argtypes = [D, P, W, P, P, P, P, ctypes.POINTER(moe_grads), P,
                                  ctypes.c_size_t, P]
@@ -290,3 +294,13 @@ def moe_backward(dims: Dims, x, weights: moe_weights, wt, ids, dout, dx, grads: 
     if check and rc != MOE_OK:
         raise MoEError(rc, "moe_backward")
     return rc
+
+
+def moe_set_backward_stage_events(events) -> int:
+    """events: None, or 2 * len(BWD_STAGES) recorded torch.cuda.Event objects."""
+    if events is None:
+        return int(load().moe_set_backward_stage_events(None))
+    assert len(events) == 2 * len(BWD_STAGES)
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    return int(load().moe_set_backward_stage_events(ctypes.cast(arr, ctypes.c_void_p)))
+

@@ -174,6 +174,14 @@ inline moe_status mark(int stage, int edge, cudaStream_t s) {
     return cu(cudaEventRecord(g_stage_events[2 * stage + edge], s));
 }
 
+thread_local cudaEvent_t g_bwd_events[2 * MOE_BWD_NUM_STAGES];
+thread_local bool g_bwd_timing = false;
+
+inline moe_status mark_b(int stage, int edge, cudaStream_t s) {
+    if (!g_bwd_timing) return MOE_OK;
+    return cu(cudaEventRecord(g_bwd_events[2 * stage + edge], s));
+}
+
 #define MOE_TRY(expr)                         \
     do {                                      \
         const moe_status st_ = (expr);        \
@@ -612,12 +620,16 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
 
     // 1. routing with the given ids (replay: checked, gate weights recomputed),
     //    dispatch, padded token offsets, gather (with the shared rows)
+    MOE_TRY(mark_b(MOE_BWD_STAGE_ROUTE, 0, s));
     MOE_TRY(run_route(d, x, w, ids, ids_used, gates, wsb, L.f, s));
+    MOE_TRY(mark_b(MOE_BWD_STAGE_ROUTE, 1, s));
+    MOE_TRY(mark_b(MOE_BWD_STAGE_DISPATCH, 0, s));
     MOE_TRY(cu(launch_dispatch(ids_used, T, k, E, cnt, off, perm, inv,
                                reinterpret_cast<int32_t*>(wsb + L.f.scratch), s)));
     MOE_TRY(cu(launch_seg_offsets(cnt, E, G, S ? static_cast<int>(T) : 0, poff, s)));
     MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), perm, T, k, D, S,
                              reinterpret_cast<uint16_t*>(wsb + L.f.xp), s)));
+    MOE_TRY(mark_b(MOE_BWD_STAGE_DISPATCH, 1, s));
 
     const int units = sms / 2;  // CTA pairs
     const uint32_t box_b = BN_EXPERT / 2;
@@ -661,7 +673,9 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
         p.ldo = F;
         p.save_a = reinterpret_cast<float*>(wsb + L.a);
         p.save_b = reinterpret_cast<float*>(wsb + L.b);
+        MOE_TRY(mark_b(MOE_BWD_STAGE_GATE_UP, 0, s));
         MOE_TRY(launch(GEMM_SWIGLU, p, tok_tiles + sh_tiles));
+        MOE_TRY(mark_b(MOE_BWD_STAGE_GATE_UP, 1, s));
     }
     {
         GemmParams p;
@@ -675,10 +689,13 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
         p.KB = F / BK;
         p.out = wsb + L.f.y;
         p.ldo = D;
+        MOE_TRY(mark_b(MOE_BWD_STAGE_DOWN, 0, s));
         MOE_TRY(launch(GEMM_DOWN, p, tok_tiles));
+        MOE_TRY(mark_b(MOE_BWD_STAGE_DOWN, 1, s));
     }
 
     // 3. gate and router gradients; dx starts as the router's part
+    MOE_TRY(mark_b(MOE_BWD_STAGE_GATE, 0, s));
     MOE_TRY(cu(launch_gate_bwd(static_cast<const uint16_t*>(dout),
                                reinterpret_cast<const uint16_t*>(wsb + L.f.y), inv, ids_used, gates,
                                valid, static_cast<const uint16_t*>(w->w_router),
@@ -687,11 +704,14 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
     MOE_TRY(cu(launch_router_wgrad(reinterpret_cast<const uint16_t*>(wsb + L.f.xp), perm, cnt, off,
                                    reinterpret_cast<const float*>(wsb + L.dl), g->d_router, E, D,
                                    sms, s)));
+    MOE_TRY(mark_b(MOE_BWD_STAGE_GATE, 1, s));
 
     // 4. dH = Q_d(dY) Q_d(Wd)  (SM-pair grouped GEMM, fp32 rows)
     uint16_t* dyq = reinterpret_cast<uint16_t*>(wsb + L.dyq);
+    MOE_TRY(mark_b(MOE_BWD_STAGE_DY, 0, s));
     MOE_TRY(cu(launch_dy_rows(static_cast<const uint16_t*>(dout), gates, perm, valid, T, k, D, S,
                               dyq, sms, s)));
+    MOE_TRY(mark_b(MOE_BWD_STAGE_DY, 1, s));
     {
         GemmParams p;
         common(p, S, status + 6);
@@ -705,16 +725,20 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
         p.out = wsb + L.dh;
         p.out_f32 = 1;
         p.ldo = F;
+        MOE_TRY(mark_b(MOE_BWD_STAGE_DH, 0, s));
         MOE_TRY(launch(GEMM_DOWN, p, tok_tiles + sh_tiles));
+        MOE_TRY(mark_b(MOE_BWD_STAGE_DH, 1, s));
     }
 
     // 5. SwiGLU backward -> [dA | dB] (fp32 and quantised along F)
     float* dab = reinterpret_cast<float*>(wsb + L.dab);
     uint16_t* dabq = reinterpret_cast<uint16_t*>(wsb + L.dabq);
+    MOE_TRY(mark_b(MOE_BWD_STAGE_SWIGLU, 0, s));
     MOE_TRY(cu(launch_swiglu_bwd(reinterpret_cast<const float*>(wsb + L.dh),
                                  reinterpret_cast<const float*>(wsb + L.a),
                                  reinterpret_cast<const float*>(wsb + L.b), dab, dabq, rows, F, sms,
                                  s)));
+    MOE_TRY(mark_b(MOE_BWD_STAGE_SWIGLU, 1, s));
 
     // 6. dXp = Q_F(dA) Q_F(Wg) + Q_F(dB) Q_F(Wu)  (one K = 2F GEMM), then dx
     {
@@ -730,10 +754,14 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
         p.out = wsb + L.dxp;
         p.out_f32 = 1;
         p.ldo = D;
+        MOE_TRY(mark_b(MOE_BWD_STAGE_DXP, 0, s));
         MOE_TRY(launch(GEMM_DOWN, p, tok_tiles + sh_tiles));
+        MOE_TRY(mark_b(MOE_BWD_STAGE_DXP, 1, s));
     }
+    MOE_TRY(mark_b(MOE_BWD_STAGE_DX, 0, s));
     MOE_TRY(cu(launch_dx_assemble(reinterpret_cast<const float*>(wsb + L.dxp), inv, dx, T, k, D, S,
                                   sms, s)));
+    MOE_TRY(mark_b(MOE_BWD_STAGE_DX, 1, s));
 
     // 7. token-major operands, quantised along the tokens of each expert
     uint16_t* xpt = reinterpret_cast<uint16_t*>(wsb + L.xpt);
@@ -741,6 +769,7 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
     uint16_t* ht = reinterpret_cast<uint16_t*>(wsb + L.ht);
     uint16_t* dabt = reinterpret_cast<uint16_t*>(wsb + L.dabt);
     const int srows = S ? static_cast<int>(T) : 0;
+    MOE_TRY(mark_b(MOE_BWD_STAGE_TRANSPOSE, 0, s));
     MOE_TRY(cu(launch_tq_segments(TQ_SRC_BF16, wsb + L.f.xp, D, nullptr, D, cnt, off, poff, E, G,
                                   Tk, srows, L.kpad, xpt, sms, s)));
     const SegDyArgs dya{static_cast<const uint16_t*>(dout), gates, perm, valid, k, Tk};
@@ -750,6 +779,7 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
                                   Tk, srows, L.kpad, ht, sms, s)));
     MOE_TRY(cu(launch_tq_segments(TQ_SRC_F32, dab, 2 * F, nullptr, 2 * F, cnt, off, poff, E, G, Tk,
                                   srows, L.kpad, dabt, sms, s)));
+    MOE_TRY(mark_b(MOE_BWD_STAGE_TRANSPOSE, 1, s));
 
     // 8. weight gradients (ragged-K grouped GEMMs)
     const int wm = wgrad_tile_m(), wn = wgrad_tile_n();
@@ -775,7 +805,9 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
         p.gstride = int64_t(D) * F;
         p.status = status;
         p.timeout_ns = kWaitTimeoutNs;
+        MOE_TRY(mark_b(MOE_BWD_STAGE_WGRAD_DOWN, 0, s));
         MOE_TRY(wlaunch(p));
+        MOE_TRY(mark_b(MOE_BWD_STAGE_WGRAD_DOWN, 1, s));
     }
     {
         WgradParams p;
@@ -797,7 +829,9 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
         p.gstride = int64_t(F) * D;
         p.status = status;
         p.timeout_ns = kWaitTimeoutNs;
+        MOE_TRY(mark_b(MOE_BWD_STAGE_WGRAD_GATE_UP, 0, s));
         MOE_TRY(wlaunch(p));
+        MOE_TRY(mark_b(MOE_BWD_STAGE_WGRAD_GATE_UP, 1, s));
     }
     return MOE_OK;
 }
@@ -925,6 +959,7 @@ moe_status moe_backward_prepare_weights(const moe_dims* d, const moe_weights* w,
     auto* wdt = reinterpret_cast<uint16_t*>(o + W.wdt);
     auto* w2t = reinterpret_cast<uint16_t*>(o + W.w2t);
     // Wd [d][F] -> [F][d] quantised along d; Wg, Wu [F][d] -> [d][2F] quantised along F
+    MOE_TRY(mark_b(MOE_BWD_STAGE_PREPARE, 0, s));
     MOE_TRY(cu(launch_tq_batch(static_cast<const uint16_t*>(w->w_down), E, D, F, wdt, FD, D, 0, sms, s)));
     MOE_TRY(cu(launch_tq_batch(static_cast<const uint16_t*>(w->w_gate), E, F, D, w2t, 2 * FD, 2 * F, 0,
                                sms, s)));
@@ -940,6 +975,17 @@ moe_status moe_backward_prepare_weights(const moe_dims* d, const moe_weights* w,
         MOE_TRY(cu(launch_tq_batch(static_cast<const uint16_t*>(w->ws_up), 1, F, D, sw2t, 2 * FD,
                                    2 * F, F, sms, s)));
     }
+    return mark_b(MOE_BWD_STAGE_PREPARE, 1, s);
+}
+
+moe_status moe_set_backward_stage_events(void* const* events) {
+    if (!events) {
+        g_bwd_timing = false;
+        return MOE_OK;
+    }
+    for (int i = 0; i < 2 * MOE_BWD_NUM_STAGES; ++i)
+        g_bwd_events[i] = static_cast<cudaEvent_t>(events[i]);
+    g_bwd_timing = true;
     return MOE_OK;
 }
 

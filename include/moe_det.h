@@ -349,6 +349,32 @@ typedef struct {
 } moe_bwd_ws_layout;
 moe_status moe_backward_workspace_layout(const moe_dims *dims, moe_bwd_ws_layout *layout);
 
+/* Stages of the backward, in launch order (moe_backward_prepare_weights
+ * records only MOE_BWD_STAGE_PREPARE). */
+typedef enum {
+    MOE_BWD_STAGE_PREPARE = 0,        /* weight copies quantised along the backward's K */
+    MOE_BWD_STAGE_ROUTE = 1,          /* router GEMM, replay check, gate weights        */
+    MOE_BWD_STAGE_DISPATCH = 2,       /* counting sort, padded offsets, gather          */
+    MOE_BWD_STAGE_GATE_UP = 3,        /* forward recompute: gate/up (H, pre-activations)*/
+    MOE_BWD_STAGE_DOWN = 4,           /* forward recompute: routed expert outputs Y     */
+    MOE_BWD_STAGE_GATE = 5,           /* gate/logit gradients, router part of dx, dWr   */
+    MOE_BWD_STAGE_DY = 6,             /* dY rows quantised along d                      */
+    MOE_BWD_STAGE_DH = 7,             /* dH = Q(dY) Q(Wd)                               */
+    MOE_BWD_STAGE_SWIGLU = 8,         /* SwiGLU backward, [dA | dB] quantised along F   */
+    MOE_BWD_STAGE_DXP = 9,            /* dXp = Q(dA) Q(Wg) + Q(dB) Q(Wu)                */
+    MOE_BWD_STAGE_DX = 10,            /* fixed-order sum into dx                        */
+    MOE_BWD_STAGE_TRANSPOSE = 11,     /* token-major operands quantised along tokens    */
+    MOE_BWD_STAGE_WGRAD_DOWN = 12,    /* dWd                                            */
+    MOE_BWD_STAGE_WGRAD_GATE_UP = 13, /* dWg, dWu                                       */
+    MOE_BWD_NUM_STAGES = 14
+} moe_bwd_stage;
+
+/* Per-stage timing of the backward, as moe_set_stage_events for the forward:
+ * `events` holds 2 * MOE_BWD_NUM_STAGES cudaEvent_t handles (or is NULL to
+ * switch it off); events[2*j] / events[2*j+1] are recorded on the call's
+ * stream just before / after stage j.  Per host thread.  Returns MOE_OK. */
+moe_status moe_set_backward_stage_events(void *const *events);
+
 /* The backward.  x [T][d] bf16, w (bf16 experts), wt (prepared from w), ids
  * [T][k] int32 (the forward's ids), dout [T][d] bf16 -> dx [T][d] fp32 and the
  * weight gradients in *grads (all device pointers).  Replayed ids are checked
