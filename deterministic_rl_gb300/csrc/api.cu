@@ -782,15 +782,15 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
     MOE_TRY(mark_b(MOE_BWD_STAGE_TRANSPOSE, 1, s));
 
     // 8. weight gradients (ragged-K grouped GEMMs)
-    const int wm = wgrad_tile_m(), wn = wgrad_tile_n();
+    const int wm = wgrad_tile_m(), wn = wgrad_tile_n(), wbox = wgrad_box_rows();
     auto wlaunch = [&](WgradParams& p) {
         const int64_t tiles = int64_t(p.G) * p.MT * p.NT;
-        return cu(launch_wgrad(p, static_cast<int>(tiles < sms ? tiles : sms), s));
+        return cu(launch_wgrad(p, static_cast<int>(tiles < units ? tiles : units), s));
     };
     {
         WgradParams p;
         std::memset(&p, 0, sizeof p);
-        if (!make_map(&p.a, ht, L.kpad, F, wm) || !make_map(&p.b, dyt, L.kpad, D, wn))
+        if (!make_map(&p.a, ht, L.kpad, F, wbox) || !make_map(&p.b, dyt, L.kpad, D, wbox))
             return MOE_ERR_CUDA;
         p.poff = poff;
         p.G = G;
@@ -812,7 +812,7 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
     {
         WgradParams p;
         std::memset(&p, 0, sizeof p);
-        if (!make_map(&p.a, xpt, L.kpad, D, wm) || !make_map(&p.b, dabt, L.kpad, 2 * F, wn))
+        if (!make_map(&p.a, xpt, L.kpad, D, wbox) || !make_map(&p.b, dabt, L.kpad, 2 * F, wbox))
             return MOE_ERR_CUDA;
         p.poff = poff;
         p.G = G;

@@ -93,6 +93,18 @@ struct SrcBf16 {
     __device__ __forceinline__ void load8(int64_t row, int c, float (&v)[8]) const {
         unpack8(*reinterpret_cast<const uint4*>(p + row * ld + c), v);
     }
+    __device__ __forceinline__ void load16(int64_t row, int c, float (&v)[16]) const {
+        const uint4* q = reinterpret_cast<const uint4*>(p + row * ld + c);
+        const uint4 a = q[0], b = q[1];
+        float lo[8], hi[8];
+        unpack8(a, lo);
+        unpack8(b, hi);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[i] = lo[i];
+            v[8 + i] = hi[i];
+        }
+    }
 };
 
 struct SrcF32 {
@@ -103,6 +115,14 @@ struct SrcF32 {
         const float4 b = *reinterpret_cast<const float4*>(p + row * ld + c + 4);
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    }
+    __device__ __forceinline__ void load16(int64_t row, int c, float (&v)[16]) const {
+        const float4* q = reinterpret_cast<const float4*>(p + row * ld + c);
+        const float4 a = q[0], b = q[1], e = q[2], f = q[3];
+        const float t[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w,
+                             e.x, e.y, e.z, e.w, f.x, f.y, f.z, f.w};
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = t[i];
     }
 };
 
@@ -132,6 +152,28 @@ struct SrcDy {
         unpack8(*reinterpret_cast<const uint4*>(dout + t * ld + c), x);
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = w * x[i];
+    }
+    __device__ __forceinline__ void load16(int64_t row, int c, float (&v)[16]) const {
+        int64_t t;
+        float w;
+        if (row < Tk) {
+            const int32_t pair = perm[row];
+            t = pair / k;
+            w = valid[t] ? gates[pair] : 0.0f;
+        } else {
+            t = row - Tk;
+            w = valid[t] ? 1.0f : 0.0f;
+        }
+        const uint4* q = reinterpret_cast<const uint4*>(dout + t * ld + c);
+        const uint4 a = q[0], b = q[1];
+        float lo[8], hi[8];
+        unpack8(a, lo);
+        unpack8(b, hi);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            v[i] = w * lo[i];
+            v[8 + i] = w * hi[i];
+        }
     }
 };
 
@@ -194,11 +236,11 @@ __global__ void __launch_bounds__(256) swiglu_bwd_kernel(
 
 // ---- transposed quantisation (blocks of 32 along the rows) ----------------------------
 
-// Output column (the input's row axis) of a 32-row block, the input rows it
-// reads and how many of them exist.
+// A tile covers 64 input rows (two MX blocks): its output columns, the input
+// rows it reads and how many of them exist.
 struct TqBlock {
     int64_t in_row0;
-    int64_t out_col;  // element offset of the block's column 0 in the output
+    int64_t out_col;  // element offset of the tile's column 0 in the output
     int nvalid;
 };
 
@@ -215,17 +257,19 @@ struct TqArgs {
     int E, G;
     int64_t shared_row0;
     int shared_rows;
-    // batch mode: nb matrices of R rows; matrix b's block i -> output offset
-    // b * out_bstride + out_off + 32 i
+    // batch mode: nb matrices of R rows; matrix b's tile i -> output offset
+    // b * out_bstride + out_off + 64 i
     int R;
     int64_t out_bstride, out_off;
-    int64_t nblocks;  // 32-row blocks to visit
+    int64_t ntiles;  // 64-row tiles to visit
 };
 
+constexpr int kTqRows = 64;
+
 template <bool SEG>
-__device__ __forceinline__ bool tq_block(const TqArgs& a, int64_t rb, TqBlock& blk) {
+__device__ __forceinline__ bool tq_tile(const TqArgs& a, int64_t rt, TqBlock& blk) {
     if constexpr (SEG) {
-        const int64_t p = rb * 32;
+        const int64_t p = rt * kTqRows;
         if (p >= a.poff[a.G]) return false;
         int lo = 0, hi = a.G;  // poff[lo] <= p < poff[lo + 1]
         while (hi - lo > 1) {
@@ -235,55 +279,64 @@ __device__ __forceinline__ bool tq_block(const TqArgs& a, int64_t rb, TqBlock& b
         const int local = static_cast<int>(p - a.poff[lo]);
         const int n = lo < a.E ? a.cnt[lo] : a.shared_rows;
         blk.in_row0 = (lo < a.E ? static_cast<int64_t>(a.off[lo]) : a.shared_row0) + local;
-        blk.nvalid = min(max(n - local, 0), 32);
+        blk.nvalid = min(max(n - local, 0), kTqRows);
         blk.out_col = p;
     } else {
-        const int per = a.R / 32;
-        const int64_t b = rb / per;
-        const int local = static_cast<int>(rb % per) * 32;
+        const int per = a.R / kTqRows;
+        const int64_t b = rt / per;
+        const int local = static_cast<int>(rt % per) * kTqRows;
         blk.in_row0 = b * a.R + local;
-        blk.nvalid = 32;
+        blk.nvalid = kTqRows;
         blk.out_col = b * a.out_bstride + a.out_off + local;
     }
     return true;
 }
 
-// CTA tile: one 32-row block x 64 columns.  Loading: thread t reads row t / 8,
-// columns 8 (t % 8) .. + 7.  Quantising: thread t takes column t / 4 and rows
-// 8 (t % 4) .. + 7 of it; the four threads of a column share the block
-// maximum and each writes 8 consecutive output elements (16 bytes).
+// CTA tile: 64 input rows (two MX blocks) x 64 columns.  Loading: thread t
+// reads row t / 4, columns 16 (t % 4) .. + 15 (32 or 64 bytes in flight per
+// thread).  Quantising: thread t takes column t / 4 and rows 16 (t % 4) .. + 15
+// of it; threads t and t ^ 1 hold the two halves of one 32-row block and
+// share its maximum; the four threads of a column write its 64 output
+// elements, one 128-byte line.
 template <class Src, bool SEG>
 __global__ void __launch_bounds__(256) tq_kernel(Src src, TqArgs a) {
-    __shared__ float tile[32][65];
+    __shared__ float tile[kTqRows][65];
     const int tid = threadIdx.x;
     const int cchunks = a.C / 64;
-    const int64_t items = a.nblocks * cchunks;
+    const int64_t items = a.ntiles * cchunks;
     for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
-        const int64_t rb = it / cchunks;
+        const int64_t rt = it / cchunks;
         const int cb = static_cast<int>(it % cchunks) * 64;
         TqBlock blk;
-        if (!tq_block<SEG>(a, rb, blk)) continue;  // uniform across the CTA
+        if (!tq_tile<SEG>(a, rt, blk)) continue;  // uniform across the CTA
         {
-            const int r = tid >> 3, c8 = (tid & 7) * 8;
-            float v[8];
+            const int r = tid >> 2, c16 = (tid & 3) * 16;
+            float v[16];
             if (r < blk.nvalid) {
-                src.load8(blk.in_row0 + r, cb + c8, v);
+                src.load16(blk.in_row0 + r, cb + c16, v);
             } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) v[i] = 0.0f;
+                for (int i = 0; i < 16; ++i) v[i] = 0.0f;
             }
 #pragma unroll
-            for (int i = 0; i < 8; ++i) tile[r][c8 + i] = v[i];
+            for (int i = 0; i < 16; ++i) tile[r][c16 + i] = v[i];
         }
         __syncthreads();
         {
             const int c = tid >> 2, part = tid & 3;
-            float v[8];
+            float v0[8], v1[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) v[i] = tile[part * 8 + i][c];
-            const int X = mx_block_exp(block_amax4(absmax8(v)));
-            *reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(cb + c) * a.ld + blk.out_col +
-                                      part * 8) = mx_qdq8(v, X);
+            for (int i = 0; i < 8; ++i) {
+                v0[i] = tile[part * 16 + i][c];
+                v1[i] = tile[part * 16 + 8 + i][c];
+            }
+            float m = fmaxf(absmax8(v0), absmax8(v1));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            const int X = mx_block_exp(m);
+            uint4* o = reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(cb + c) * a.ld +
+                                                blk.out_col + part * 16);
+            o[0] = mx_qdq8(v0, X);
+            o[1] = mx_qdq8(v1, X);
         }
         __syncthreads();
     }
@@ -418,12 +471,28 @@ __global__ void __launch_bounds__(kRouterWThreads) router_wgrad_kernel(
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
         const int64_t r0 = off[e], r1 = r0 + cnt[e];
-        for (int64_t r = r0; r < r1; ++r) {
-            const float l = dl[perm[r]];
-            float x[8];
-            unpack8(*reinterpret_cast<const uint4*>(xp + r * d + c), x);
+        // four rows' loads in flight; the products are added in row order
+        constexpr int kAhead = 4;
+        for (int64_t r = r0; r < r1; r += kAhead) {
+            const int nr = static_cast<int>(r1 - r < kAhead ? r1 - r : kAhead);
+            float l[kAhead];
+            uint4 xr[kAhead];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) acc[i] = fmaf(l, x[i], acc[i]);
+            for (int u = 0; u < kAhead; ++u) {
+                if (u < nr) {
+                    l[u] = dl[perm[r + u]];
+                    xr[u] = *reinterpret_cast<const uint4*>(xp + (r + u) * d + c);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kAhead; ++u) {
+                if (u < nr) {
+                    float x[8];
+                    unpack8(xr[u], x);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i] = fmaf(l[u], x[i], acc[i]);
+                }
+            }
         }
         float* dst = d_router + static_cast<int64_t>(e) * d + c;
         *reinterpret_cast<float4*>(dst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
@@ -497,7 +566,7 @@ namespace {
 template <class Src, bool SEG>
 cudaError_t tq_launch(const Src& src, const TqArgs& a, int sms, cudaStream_t s) {
     if (a.C % 64 || a.ld % 8) return cudaErrorInvalidValue;
-    const int64_t items = a.nblocks * (a.C / 64);
+    const int64_t items = a.ntiles * (a.C / 64);
     if (items == 0) return cudaSuccess;
     tq_kernel<Src, SEG><<<grid_for(items, 1, sms, 8), 256, 0, s>>>(src, a);
     return cudaGetLastError();
@@ -519,7 +588,8 @@ cudaError_t launch_tq_segments(int src_kind, const void* src, int64_t src_ld, co
     a.G = G;
     a.shared_row0 = shared_row0;
     a.shared_rows = shared_rows;
-    a.nblocks = kpad / 32;
+    if (kpad % kTqRows) return cudaErrorInvalidValue;
+    a.ntiles = kpad / kTqRows;
     switch (src_kind) {
         case TQ_SRC_BF16:
             return tq_launch<SrcBf16, true>(SrcBf16{static_cast<const uint16_t*>(src), src_ld}, a, sms, s);
@@ -537,7 +607,7 @@ cudaError_t launch_tq_segments(int src_kind, const void* src, int64_t src_ld, co
 cudaError_t launch_tq_batch(const uint16_t* src, int nb, int R, int C, uint16_t* out,
                             int64_t out_bstride, int64_t out_ld, int64_t out_off, int sms,
                             cudaStream_t s) {
-    if (R % 32) return cudaErrorInvalidValue;
+    if (R % kTqRows) return cudaErrorInvalidValue;
     TqArgs a{};
     a.C = C;
     a.ld = out_ld;
@@ -545,7 +615,7 @@ cudaError_t launch_tq_batch(const uint16_t* src, int nb, int R, int C, uint16_t*
     a.R = R;
     a.out_bstride = out_bstride;
     a.out_off = out_off;
-    a.nblocks = static_cast<int64_t>(nb) * (R / 32);
+    a.ntiles = static_cast<int64_t>(nb) * (R / kTqRows);
     if (out_off % 8 || out_bstride % 8) return cudaErrorInvalidValue;
     return tq_launch<SrcBf16, false>(SrcBf16{src, C}, a, sms, s);
 }

@@ -141,7 +141,7 @@ cudaError_t launch_nvfp4_qdq(const uint16_t* src, uint16_t* dst, uint8_t* bscale
 
 // Grouped weight-gradient GEMM: for group g, out[g][n][m] = sum over the
 // group's K-blocks of A[m][k] * B[n][k] (a: [M][Kpad], b: [N][Kpad] bf16 maps
-// with 64 x 128 and 64 x 256 boxes), K range [poff[g], poff[g+1]) (multiples
+// with 64 x wgrad_box_rows() boxes), K range [poff[g], poff[g+1]) (multiples
 // of 64, zero-padded).  Rows n < n_split go to out0 (routed groups, group g at
 // + g * gstride) or sout0 (groups >= G_routed), rows n >= n_split (minus
 // n_split) to out1 / sout1.  Row stride M floats.
@@ -160,9 +160,11 @@ struct WgradParams {
     int32_t stall_test;
 };
 constexpr int kMaxWgradGroups = 1024;
-cudaError_t launch_wgrad(const WgradParams& p, int grid, cudaStream_t s);
-int wgrad_tile_m();
-int wgrad_tile_n();
+// clusters: CTA pairs (the kernel runs on SM pairs, tcgen05 cta_group::2)
+cudaError_t launch_wgrad(const WgradParams& p, int clusters, cudaStream_t s);
+int wgrad_tile_m();    // A rows per tile (both CTAs)
+int wgrad_tile_n();    // B rows per tile (both CTAs)
+int wgrad_box_rows();  // rows of the a and b maps' boxes (one CTA's half)
 
 // Padded segment offsets of the G = E (+1 shared) groups: poff[g + 1] =
 // poff[g] + round_up(n_g, 64).
