@@ -90,20 +90,13 @@ __device__ __forceinline__ float block_amax4(float m) {
 struct SrcBf16 {
     const uint16_t* p;
     int64_t ld;
+    // transposed quantiser: 8 bf16 of a row as stored, and the row's factor
+    __device__ __forceinline__ uint4 raw8(int64_t row, int c, float& scale) const {
+        scale = 1.0f;
+        return *reinterpret_cast<const uint4*>(p + row * ld + c);
+    }
     __device__ __forceinline__ void load8(int64_t row, int c, float (&v)[8]) const {
         unpack8(*reinterpret_cast<const uint4*>(p + row * ld + c), v);
-    }
-    __device__ __forceinline__ void load16(int64_t row, int c, float (&v)[16]) const {
-        const uint4* q = reinterpret_cast<const uint4*>(p + row * ld + c);
-        const uint4 a = q[0], b = q[1];
-        float lo[8], hi[8];
-        unpack8(a, lo);
-        unpack8(b, hi);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            v[i] = lo[i];
-            v[8 + i] = hi[i];
-        }
     }
 };
 
@@ -115,14 +108,6 @@ struct SrcF32 {
         const float4 b = *reinterpret_cast<const float4*>(p + row * ld + c + 4);
         v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
         v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    }
-    __device__ __forceinline__ void load16(int64_t row, int c, float (&v)[16]) const {
-        const float4* q = reinterpret_cast<const float4*>(p + row * ld + c);
-        const float4 a = q[0], b = q[1], e = q[2], f = q[3];
-        const float t[16] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w,
-                             e.x, e.y, e.z, e.w, f.x, f.y, f.z, f.w};
-#pragma unroll
-        for (int i = 0; i < 16; ++i) v[i] = t[i];
     }
 };
 
@@ -137,6 +122,19 @@ struct SrcDy {
     int k;
     int64_t Tk;
     int64_t ld;
+    // transposed quantiser: 8 bf16 of dout[t] as stored, and the row's factor
+    __device__ __forceinline__ uint4 raw8(int64_t row, int c, float& scale) const {
+        int64_t t;
+        if (row < Tk) {
+            const int32_t pair = perm[row];
+            t = pair / k;
+            scale = valid[t] ? gates[pair] : 0.0f;
+        } else {
+            t = row - Tk;
+            scale = valid[t] ? 1.0f : 0.0f;
+        }
+        return *reinterpret_cast<const uint4*>(dout + t * ld + c);
+    }
     __device__ __forceinline__ void load8(int64_t row, int c, float (&v)[8]) const {
         int64_t t;
         float w;
@@ -152,28 +150,6 @@ struct SrcDy {
         unpack8(*reinterpret_cast<const uint4*>(dout + t * ld + c), x);
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = w * x[i];
-    }
-    __device__ __forceinline__ void load16(int64_t row, int c, float (&v)[16]) const {
-        int64_t t;
-        float w;
-        if (row < Tk) {
-            const int32_t pair = perm[row];
-            t = pair / k;
-            w = valid[t] ? gates[pair] : 0.0f;
-        } else {
-            t = row - Tk;
-            w = valid[t] ? 1.0f : 0.0f;
-        }
-        const uint4* q = reinterpret_cast<const uint4*>(dout + t * ld + c);
-        const uint4 a = q[0], b = q[1];
-        float lo[8], hi[8];
-        unpack8(a, lo);
-        unpack8(b, hi);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            v[i] = w * lo[i];
-            v[8 + i] = w * hi[i];
-        }
     }
 };
 
@@ -292,15 +268,90 @@ __device__ __forceinline__ bool tq_tile(const TqArgs& a, int64_t rt, TqBlock& bl
     return true;
 }
 
-// CTA tile: 64 input rows (two MX blocks) x 64 columns.  Loading: thread t
-// reads row t / 4, columns 16 (t % 4) .. + 15 (32 or 64 bytes in flight per
-// thread).  Quantising: thread t takes column t / 4 and rows 16 (t % 4) .. + 15
-// of it; threads t and t ^ 1 hold the two halves of one 32-row block and
-// share its maximum; the four threads of a column write its 64 output
-// elements, one 128-byte line.
+// Two layouts of the CTA tile (64 input rows = two MX blocks, x 64 columns),
+// both read down a column by the quantising threads without bank conflicts
+// (the column index is XOR-swizzled by the row group) and written with 16-byte
+// stores.  Quantising: thread t takes column t / 4 and rows 16 (t % 4) .. + 15;
+// threads t and t ^ 1 hold the two halves of one 32-row block and share its
+// maximum; the four threads of a column write its 64 output elements, one
+// 128-byte line.
+
+__device__ __forceinline__ void tq_store16(uint16_t* out, int64_t at, const float (&v)[16], int X) {
+    float v0[8], v1[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        v0[i] = v[i];
+        v1[i] = v[8 + i];
+    }
+    uint4* o = reinterpret_cast<uint4*>(out + at);
+    o[0] = mx_qdq8(v0, X);
+    o[1] = mx_qdq8(v1, X);
+}
+
+// bf16-valued rows (times a per-row factor): the tile holds the stored bf16 of
+// rows 2R and 2R + 1 of a column in one 32-bit word, tp[R][column ^ sw(R)],
+// sw(R) = 8 * ((R / 8) % 4).  Loading: thread t reads rows 2 (t / 8) and
+// 2 (t / 8) + 1, columns 8 (t % 8) .. + 7 (two 16-byte loads).
 template <class Src, bool SEG>
-__global__ void __launch_bounds__(256) tq_kernel(Src src, TqArgs a) {
-    __shared__ float tile[kTqRows][65];
+__global__ void __launch_bounds__(256, 8) tq16_kernel(Src src, TqArgs a) {
+    __shared__ __align__(16) uint32_t tp[kTqRows / 2][64];
+    __shared__ float rs[kTqRows];
+    const int tid = threadIdx.x;
+    const int cchunks = a.C / 64;
+    const int64_t items = a.ntiles * cchunks;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int64_t rt = it / cchunks;
+        const int cb = static_cast<int>(it % cchunks) * 64;
+        TqBlock blk;
+        if (!tq_tile<SEG>(a, rt, blk)) continue;  // uniform across the CTA
+        {
+            const int R = tid >> 3, c8 = (tid & 7) * 8;
+            uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+            float s0 = 0.0f, s1 = 0.0f;
+            if (2 * R < blk.nvalid) lo = src.raw8(blk.in_row0 + 2 * R, cb + c8, s0);
+            if (2 * R + 1 < blk.nvalid) hi = src.raw8(blk.in_row0 + 2 * R + 1, cb + c8, s1);
+            if ((tid & 7) == 0) {
+                rs[2 * R] = s0;
+                rs[2 * R + 1] = s1;
+            }
+            const uint32_t l[4] = {lo.x, lo.y, lo.z, lo.w}, h[4] = {hi.x, hi.y, hi.z, hi.w};
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                w[2 * i] = __byte_perm(l[i], h[i], 0x5410);      // column 2i of both rows
+                w[2 * i + 1] = __byte_perm(l[i], h[i], 0x7632);  // column 2i + 1
+            }
+            uint4* dst = reinterpret_cast<uint4*>(&tp[R][c8 ^ (((R >> 3) & 3) << 3)]);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+        __syncthreads();
+        {
+            const int c = tid >> 2, part = tid & 3;
+            float v[16];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t w = tp[part * 8 + j][c ^ (part << 3)];
+                v[2 * j] = __uint_as_float(w << 16) * rs[part * 16 + 2 * j];
+                v[2 * j + 1] = __uint_as_float(w & 0xFFFF0000u) * rs[part * 16 + 2 * j + 1];
+            }
+            float m = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            tq_store16(a.out, static_cast<int64_t>(cb + c) * a.ld + blk.out_col + part * 16, v,
+                       mx_block_exp(m));
+        }
+        __syncthreads();
+    }
+}
+
+// fp32 rows: the tile holds tf[r][column ^ sw(r)], sw(r) = 8 * ((r / 16) % 4).
+// Loading: thread t reads row t / 4, columns 16 (t % 4) .. + 15 (four 16-byte
+// loads), stored as four 16-byte stores.
+template <bool SEG>
+__global__ void __launch_bounds__(256, 8) tq32_kernel(SrcF32 src, TqArgs a) {
+    __shared__ __align__(16) float tf[kTqRows][64];
     const int tid = threadIdx.x;
     const int cchunks = a.C / 64;
     const int64_t items = a.ntiles * cchunks;
@@ -311,32 +362,31 @@ __global__ void __launch_bounds__(256) tq_kernel(Src src, TqArgs a) {
         if (!tq_tile<SEG>(a, rt, blk)) continue;  // uniform across the CTA
         {
             const int r = tid >> 2, c16 = (tid & 3) * 16;
-            float v[16];
+            float4 q[4] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f),
+                           make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
             if (r < blk.nvalid) {
-                src.load16(blk.in_row0 + r, cb + c16, v);
-            } else {
+                const float4* p4 =
+                    reinterpret_cast<const float4*>(src.p + (blk.in_row0 + r) * src.ld + cb + c16);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = 0.0f;
+                for (int i = 0; i < 4; ++i) q[i] = p4[i];
             }
+            const int sw = ((r >> 4) & 3) << 3;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) tile[r][c16 + i] = v[i];
+            for (int i = 0; i < 4; ++i)
+                *reinterpret_cast<float4*>(&tf[r][(c16 + 4 * i) ^ sw]) = q[i];
         }
         __syncthreads();
         {
             const int c = tid >> 2, part = tid & 3;
-            float v0[8], v1[8];
+            float v[16];
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                v0[i] = tile[part * 16 + i][c];
-                v1[i] = tile[part * 16 + 8 + i][c];
-            }
-            float m = fmaxf(absmax8(v0), absmax8(v1));
+            for (int i = 0; i < 16; ++i) v[i] = tf[part * 16 + i][c ^ (part << 3)];
+            float m = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
             m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            const int X = mx_block_exp(m);
-            uint4* o = reinterpret_cast<uint4*>(a.out + static_cast<int64_t>(cb + c) * a.ld +
-                                                blk.out_col + part * 16);
-            o[0] = mx_qdq8(v0, X);
-            o[1] = mx_qdq8(v1, X);
+            tq_store16(a.out, static_cast<int64_t>(cb + c) * a.ld + blk.out_col + part * 16, v,
+                       mx_block_exp(m));
         }
         __syncthreads();
     }
@@ -568,7 +618,16 @@ cudaError_t tq_launch(const Src& src, const TqArgs& a, int sms, cudaStream_t s) 
     if (a.C % 64 || a.ld % 8) return cudaErrorInvalidValue;
     const int64_t items = a.ntiles * (a.C / 64);
     if (items == 0) return cudaSuccess;
-    tq_kernel<Src, SEG><<<grid_for(items, 1, sms, 8), 256, 0, s>>>(src, a);
+    tq16_kernel<Src, SEG><<<grid_for(items, 1, sms, 8), 256, 0, s>>>(src, a);
+    return cudaGetLastError();
+}
+
+template <bool SEG>
+cudaError_t tq_launch32(const SrcF32& src, const TqArgs& a, int sms, cudaStream_t s) {
+    if (a.C % 64 || a.ld % 8) return cudaErrorInvalidValue;
+    const int64_t items = a.ntiles * (a.C / 64);
+    if (items == 0) return cudaSuccess;
+    tq32_kernel<SEG><<<grid_for(items, 1, sms, 8), 256, 0, s>>>(src, a);
     return cudaGetLastError();
 }
 }  // namespace
@@ -594,7 +653,7 @@ cudaError_t launch_tq_segments(int src_kind, const void* src, int64_t src_ld, co
         case TQ_SRC_BF16:
             return tq_launch<SrcBf16, true>(SrcBf16{static_cast<const uint16_t*>(src), src_ld}, a, sms, s);
         case TQ_SRC_F32:
-            return tq_launch<SrcF32, true>(SrcF32{static_cast<const float*>(src), src_ld}, a, sms, s);
+            return tq_launch32<true>(SrcF32{static_cast<const float*>(src), src_ld}, a, sms, s);
         case TQ_SRC_DY:
             if (!dy) return cudaErrorInvalidValue;
             return tq_launch<SrcDy, true>(
