@@ -13,8 +13,10 @@ perturbed copy of the hidden states.  Prints one JSON line (rank 0).
 
 --pass backward times the layer backward instead (MXFP8 expert GEMMs; one
 step = the weight copies quantised along the backward's contraction axes,
-then the whole backward of one batch with recorded ids), by default on the
-32k-token training layer.
+then the whole backward of one batch with recorded ids, forward recomputed),
+by default on the 32k-token training layer.  --pass train times a training
+step of the layer: weight copies, the forward keeping its activations, and
+the backward from them.
 
 Under torchrun each rank runs its own batch on its own GPU (weak scaling, no
 collective on the data path; a barrier and a max over ranks for timing).
@@ -39,6 +41,8 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE-layer tokens/s (384-expert top-8, d=7168, replay, bf16); % of roofline"
 BWD_METRIC = ("MoE-layer backward tokens/s (384-expert top-8, d=7168, MXFP8 expert GEMMs, "
               "recorded ids); % of roofline")
+TRAIN_METRIC = ("MoE-layer training-step tokens/s (forward + MXFP8 backward, 384-expert top-8, "
+                "d=7168, recorded ids); % of roofline")
 UNIT = "tokens/s"
 L2_BYTES = 129 * 2 ** 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -71,7 +75,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default=None,
                     help="default: c2_decode_replay (forward), c4_train_32k (backward)")
-    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward"], default="forward")
+    ap.add_argument("--pass", dest="pass_", choices=["forward", "backward", "train"],
+                    default="forward")
     ap.add_argument("--mode", choices=["replay", "own"], default="replay")
     ap.add_argument("--experts", type=int, default=0,
                     help="override the expert count (small captures for the profiler)")
@@ -84,9 +89,9 @@ def parse():
     ap.add_argument("--no-e2e", action="store_true")
     args = ap.parse_args()
     if args.config is None:
-        args.config = "c4_train_32k" if args.pass_ == "backward" else "c2_decode_replay"
+        args.config = "c4_train_32k" if args.pass_ != "forward" else "c2_decode_replay"
     if not args.cpu_sample:
-        args.cpu_sample = 2 if args.pass_ == "backward" else 64
+        args.cpu_sample = 2 if args.pass_ != "forward" else 64
     return args
 
 
@@ -515,27 +520,30 @@ def run_ours(args):
 
 # ---- backward ----------------------------------------------------------------------
 
-def backward_kernel_flops(cfg):
-    """Algorithmic FLOPs of each grouped-GEMM launch of one backward."""
+def backward_kernel_flops(cfg, train=False):
+    """Algorithmic FLOPs of each grouped-GEMM launch of one backward (train:
+    of one training step, whose down GEMM also forms the shared rows)."""
     T, d, k, F, S = cfg.T, cfg.d, cfg.k, cfg.F, cfg.n_shared
     rows = T * k + T * S
-    return {"gate_up": 4.0 * d * F * rows, "down": 2.0 * d * F * T * k, "dh": 2.0 * d * F * rows,
+    return {"gate_up": 4.0 * d * F * rows, "down": 2.0 * d * F * (rows if train else T * k),
+            "dh": 2.0 * d * F * rows,
             "dxp": 4.0 * d * F * rows, "wgrad_down": 2.0 * d * F * rows,
             "wgrad_gate_up": 4.0 * d * F * rows}
 
 
-def backward_work(cfg):
-    """Algorithmic FLOPs and bytes of one backward step: the grouped GEMMs,
-    the router and gate gradients; every expert weight read once, every weight
-    gradient written once (fp32), x and dout read, dx written."""
+def backward_work(cfg, train=False):
+    """Algorithmic FLOPs and bytes of one backward step (train: of one training
+    step): the grouped GEMMs, the router and gate gradients; every expert weight
+    read once, every weight gradient written once (fp32), x and dout read, dx
+    (and the layer output) written."""
     T, d, E, k, F, S = cfg.T, cfg.d, cfg.E, cfg.k, cfg.F, cfg.n_shared
-    flops = sum(backward_kernel_flops(cfg).values()) + 2.0 * T * E * d + 6.0 * T * k * d
+    flops = sum(backward_kernel_flops(cfg, train).values()) + 2.0 * T * E * d + 6.0 * T * k * d
     nbytes = ((E + S) * 3 * d * F * (2 + 4) + E * d * (2 + 4) + T * d * (2 + 2 + 4)
-              + T * k * 4)
+              + T * k * 4 + (T * d * 2 if train else 0))
     return flops, nbytes
 
 
-def backward_launches(cfg):
+def backward_launches(cfg, train=False):
     """Our kernels per backward step: weight copies (3, +3 for the shared
     expert); router GEMM, top-k; dispatch (1 or 3); padded offsets; gather;
     gate/up and down recompute; gate backward; router weight gradient; dY
@@ -543,7 +551,8 @@ def backward_launches(cfg):
     weight-gradient GEMMs."""
     prep = 3 + 3 * cfg.n_shared
     disp = 1 if cfg.T * cfg.k <= DISPATCH_SEGMENT_PAIRS else 3
-    return prep + 2 + disp + 1 + 1 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 4 + 2
+    # train: + the combine of the forward's output
+    return prep + 2 + disp + 1 + 1 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 4 + 2 + (1 if train else 0)
 
 
 def _bwd_cfg(args):
@@ -556,8 +565,9 @@ def _bwd_cfg(args):
     return cfg
 
 
-def backward_workload_desc(cfg):
-    return (f"{cfg.name} backward: T={cfg.T} d={cfg.d} E={cfg.E} top-{cfg.k} F={cfg.F} "
+def backward_workload_desc(cfg, train=False):
+    what = "training step (forward + backward)" if train else "backward"
+    return (f"{cfg.name} {what}: T={cfg.T} d={cfg.d} E={cfg.E} top-{cfg.k} F={cfg.F} "
             f"shared={cfg.n_shared} bf16 weights, MXFP8 expert GEMMs, recorded ids")
 
 
@@ -623,12 +633,14 @@ def run_backward_reference(args):
     value = args.steps / dt
     cores = os.cpu_count() or 1
     sample = (f"1 token per step, cycling over the first {pool} tokens of {cfg.name}; fp64 numpy "
-              f"backward oracle (every gradient of the token), up to {cores} host threads")
-    line = {"impl": "reference", "metric": BWD_METRIC, "value": value, "unit": UNIT,
-            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+              f"backward oracle (the token's forward activations and every gradient), up to "
+              f"{cores} host threads")
+    train = args.pass_ == "train"
+    line = {"impl": "reference", "metric": TRAIN_METRIC if train else BWD_METRIC, "value": value,
+            "unit": UNIT, "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": backward_workload_desc(cfg)},
+            "config": {"workload": backward_workload_desc(cfg, train)},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -653,16 +665,23 @@ def run_backward_ours(args):
     grads = layer.alloc_grads()
     dx = torch.empty((T, cfg.d), dtype=torch.float32, device="cuda")
 
+    train = args.pass_ == "train"
+    outs = layer.outputs(T)
+
     def step(x=inp.x, i=ids, g=dout):
         layer.prepare_backward()
-        layer.backward(x, i, g, grads=grads, dx=dx)
+        if train:
+            layer.forward_train(x, replay_ids=i, outputs=outs)
+            layer.backward_saved(g, grads=grads, dx=dx)
+        else:
+            layer.backward(x, i, g, grads=grads, dx=dx)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     if layer.backward_status() != 0:
         raise RuntimeError(f"device status after warm-up: {B.status_str(layer.backward_status())}")
-    flops, nbytes = backward_work(cfg)
+    flops, nbytes = backward_work(cfg, train)
     ns = len(B.BWD_STAGES)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * ns)] for _ in range(K)]
     for row in evs:
@@ -694,12 +713,12 @@ def run_backward_ours(args):
     hbm = float(pk["hbm_gbs"])
     tensor = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     tensor_s = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    kf = backward_kernel_flops(cfg)
+    kf = backward_kernel_flops(cfg, train)
     kernels = {n: {"ms": stage_ms[n], "tflops": kf[n] / (stage_ms[n] / 1e3) / 1e12,
                    "frac": kf[n] / (stage_ms[n] / 1e3) / 1e12 / tensor} for n in kf}
     dom = max(kf, key=lambda n: stage_ms[n])
-    knames = {"gate_up": "pair_gemm_kernel<GEMM_SWIGLU, bf16> (gate/up recompute, keeps pre-activations)",
-              "down": "pair_gemm_kernel<GEMM_DOWN, bf16> (routed expert outputs)",
+    knames = {"gate_up": "pair_gemm_kernel<GEMM_SWIGLU, bf16> (gate/up, keeps pre-activations)",
+              "down": "pair_gemm_kernel<GEMM_DOWN, bf16> (expert outputs)",
               "dh": "pair_gemm_kernel<GEMM_DOWN, bf16> (dH = Q(dY) Q(Wd), fp32 rows)",
               "dxp": "pair_gemm_kernel<GEMM_DOWN, bf16> (dXp, K = 2F, fp32 rows)",
               "wgrad_down": "wgrad_kernel (dWd, ragged K)",
@@ -727,6 +746,7 @@ def run_backward_ours(args):
         ids_h = ids.cpu().pin_memory()
         dout_h = dout.cpu().pin_memory()
         dx_h = torch.empty(dx.shape, dtype=dx.dtype, pin_memory=True)
+        out_h = torch.empty(outs[0].shape, dtype=outs[0].dtype, pin_memory=True)
         x_d, ids_d, dout_d = torch.empty_like(inp.x), torch.empty_like(ids), torch.empty_like(dout)
         Ke = max(1, min(K, 20))
         barrier(world)
@@ -738,14 +758,20 @@ def run_backward_ours(args):
             dout_d.copy_(dout_h, non_blocking=True)
             step(x_d, ids_d, dout_d)
             dx_h.copy_(dx, non_blocking=True)
+            if train:
+                out_h.copy_(outs[0], non_blocking=True)
             torch.cuda.current_stream().synchronize()
         dt = max_over_ranks(world, time.perf_counter() - t0)
         e2e = {"value": world * T * Ke / dt, "unit": UNIT,
                "h2d_bytes_per_step": x_h.numel() * 2 + ids_h.numel() * 4 + dout_h.numel() * 2,
-               "d2h_bytes_per_step": dx_h.numel() * 4, "steps": Ke,
-               "api": "MoELayer.prepare_backward + MoELayer.backward -> "
-                      "moe_backward_prepare_weights + moe_backward (C ABI), pinned host buffers; "
-                      "weight gradients stay on the device"}
+               "d2h_bytes_per_step": dx_h.numel() * 4 + (out_h.numel() * 2 if train else 0),
+               "steps": Ke,
+               "api": ("MoELayer.prepare_backward + forward_train + backward_saved -> "
+                       "moe_backward_prepare_weights + moe_forward_train + moe_backward_saved"
+                       if train else
+                       "MoELayer.prepare_backward + MoELayer.backward -> "
+                       "moe_backward_prepare_weights + moe_backward")
+                      + " (C ABI), pinned host buffers; weight gradients stay on the device"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -756,15 +782,16 @@ def run_backward_ours(args):
                          f"{passes} fp64 numpy backward-oracle passes, {dt:.1f} s"}
 
     if rank == 0:
-        line = {"metric": BWD_METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
+        line = {"metric": TRAIN_METRIC if train else BWD_METRIC, "value": value, "unit": UNIT,
+                "n_gpus": world, "steps": K,
                 "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-                "config": {"workload": backward_workload_desc(cfg), "tokens_per_step": T,
+                "config": {"workload": backward_workload_desc(cfg, train), "tokens_per_step": T,
                            "parallelism": f"replicas x{world} (own batch per GPU, no collective)",
                            "l2": f"inputs larger than L2: {nbytes / 1e9:.1f} GB moved per step"},
                 "roofline": roofline, "layer_roofline": layer_roof, "kernels": kernels,
                 "stages_ms": stage_ms, "clocks": clk.summary(), "e2e": e2e,
-                "gpu_launches": backward_launches(cfg) * K, "cpu_baseline": cpu}
+                "gpu_launches": backward_launches(cfg, train) * K, "cpu_baseline": cpu}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -774,7 +801,7 @@ def run_backward_ours(args):
 
 def main():
     args = parse()
-    if args.pass_ == "backward":
+    if args.pass_ != "forward":
         if args.impl == "reference":
             return run_backward_reference(args)
         return run_backward_ours(args)

@@ -36,7 +36,8 @@ EXPORTED = ("moe_workspace_size", "moe_workspace_layout", "moe_route", "moe_forw
             "moe_forward_replay", "moe_get_status", "moe_status_str", "moe_set_stage_events",
             "moe_route_static", "moe_forward_replay_filtered", "moe_backward_weights_size",
             "moe_backward_prepare_weights", "moe_backward_workspace_size",
-            "moe_backward_workspace_layout", "moe_set_backward_stage_events", "moe_backward")
+            "moe_backward_workspace_layout", "moe_set_backward_stage_events", "moe_backward",
+            "moe_forward_train", "moe_backward_saved")
 
 STAGES = ("router_gemm", "topk", "dispatch", "gather", "gate_up", "down", "combine")
 BWD_STAGES = ("prepare", "route", "dispatch", "gate_up", "down", "gate", "dy", "dh", "swiglu",
@@ -123,6 +124,11 @@ def load(path: str = LIB_PATH):
     lib.moe_backward_workspace_size.argtypes = [D]
     lib.moe_backward_workspace_layout.restype = ctypes.c_int
     lib.moe_backward_workspace_layout.argtypes = [D, ctypes.POINTER(moe_bwd_ws_layout)]
+    lib.moe_forward_train.restype = ctypes.c_int
+    lib.moe_forward_train.argtypes = [D, P, W, P, P, P, P, P, ctypes.c_size_t, P]
+    lib.moe_backward_saved.restype = ctypes.c_int
+    lib.moe_backward_saved.argtypes = [D, W, P, P, P, ctypes.POINTER(moe_grads), P,
+                                       ctypes.c_size_t, P]
     lib.moe_set_backward_stage_events.restype = ctypes.c_int
     lib.moe_set_backward_stage_events.argtypes = [ctypes.c_void_p]
     lib.moe_backward.restype = ctypes.c_int
@@ -303,4 +309,24 @@ def moe_set_backward_stage_events(events) -> int:
     assert len(events) == 2 * len(BWD_STAGES)
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     return int(load().moe_set_backward_stage_events(ctypes.cast(arr, ctypes.c_void_p)))
+
+
+def moe_forward_train(dims: Dims, x, weights: moe_weights, ids_in, out, ids_out, gates_out, ws,
+                      stream=None, check: bool = True) -> int:
+    rc = load().moe_forward_train(ctypes.byref(dims.c()), _p(x), ctypes.byref(weights),
+                                  _p(ids_in), _p(out), _p(ids_out), _p(gates_out), _p(ws),
+                                  ws.numel() * ws.element_size(), _stream(stream))
+    if check and rc != MOE_OK:
+        raise MoEError(rc, "moe_forward_train")
+    return rc
+
+
+def moe_backward_saved(dims: Dims, weights: moe_weights, wt, dout, dx, grads: moe_grads, ws,
+                       stream=None, check: bool = True) -> int:
+    rc = load().moe_backward_saved(ctypes.byref(dims.c()), ctypes.byref(weights), _p(wt),
+                                   _p(dout), _p(dx), ctypes.byref(grads), _p(ws),
+                                   ws.numel() * ws.element_size(), _stream(stream))
+    if check and rc != MOE_OK:
+        raise MoEError(rc, "moe_backward_saved")
+    return rc
 

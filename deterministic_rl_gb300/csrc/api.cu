@@ -581,23 +581,40 @@ BwdWeights make_bwd_weights(const moe_dims* d) {
     return W;
 }
 
-moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w, const void* wt,
-                         const int32_t* ids, const void* dout, float* dx, const moe_grads* g,
-                         void* ws, size_t ws_bytes, cudaStream_t s) {
+// What one call of the training path does.
+enum TrainMode {
+    TRAIN_BACKWARD = 0,  // moe_backward: routing with the given ids, forward recompute, backward
+    TRAIN_FORWARD = 1,   // moe_forward_train: the forward, keeping what the backward reads
+    TRAIN_SAVED = 2      // moe_backward_saved: the backward from a moe_forward_train workspace
+};
+
+moe_status train_impl(TrainMode mode, const moe_dims* d, const void* x, const moe_weights* w,
+                      const void* wt, const int32_t* ids, const void* dout, float* dx,
+                      const moe_grads* g, void* out, int32_t* ids_out, float* gates_out, void* ws,
+                      size_t ws_bytes, cudaStream_t s) {
     MOE_TRY(bwd_dims_status(d));
-    if (!w || !g) return MOE_ERR_ARG;
+    if (!w) return MOE_ERR_ARG;
+    const bool fwd = mode != TRAIN_SAVED;   // routing .. down GEMM
+    const bool bwd = mode != TRAIN_FORWARD;  // gradients
+    if (bwd && !g) return MOE_ERR_ARG;
     if (d->T == 0) return MOE_OK;
     const int64_t T = d->T;
     const int k = d->k, E = d->E, S = d->n_shared, D = d->d, F = d->F;
-    if (!x || !w->w_router || !wt || !ids || !dout || !dx || !ws) return MOE_ERR_ARG;
+    if ((fwd && !x) || !w->w_router || !ws) return MOE_ERR_ARG;
     MOE_TRY(check_experts(d, w));
-    if (!g->d_router || !g->d_gate || !g->d_up || !g->d_down) return MOE_ERR_ARG;
-    if (S && (!g->ds_gate || !g->ds_up || !g->ds_down)) return MOE_ERR_ARG;
-    if (!al16(x) || !al16(w->w_router) || !al16(w->router_bias) || !al16(wt) || !al16(ids) ||
-        !al16(dout) || !al16(dx) || !al16(ws) || !al16(g->d_router) || !al16(g->d_gate) ||
-        !al16(g->d_up) || !al16(g->d_down) || !al16(g->ds_gate) || !al16(g->ds_up) ||
-        !al16(g->ds_down))
-        return MOE_ERR_ALIGN;
+    if (!al16(x) || !al16(w->w_router) || !al16(w->router_bias) || !al16(ws)) return MOE_ERR_ALIGN;
+    if (mode == TRAIN_BACKWARD && !ids) return MOE_ERR_ARG;
+    if (mode == TRAIN_FORWARD && (!out || !ids_out || !gates_out)) return MOE_ERR_ARG;
+    if (!al16(ids) || !al16(out) || !al16(ids_out) || !al16(gates_out)) return MOE_ERR_ALIGN;
+    if (bwd) {
+        if (!wt || !dout || !dx) return MOE_ERR_ARG;
+        if (!g->d_router || !g->d_gate || !g->d_up || !g->d_down) return MOE_ERR_ARG;
+        if (S && (!g->ds_gate || !g->ds_up || !g->ds_down)) return MOE_ERR_ARG;
+        if (!al16(wt) || !al16(dout) || !al16(dx) || !al16(g->d_router) || !al16(g->d_gate) ||
+            !al16(g->d_up) || !al16(g->d_down) || !al16(g->ds_gate) || !al16(g->ds_up) ||
+            !al16(g->ds_down))
+            return MOE_ERR_ALIGN;
+    }
     const BwdLayout L = make_bwd_layout(d);
     if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
     const BwdWeights WW = make_bwd_weights(d);
@@ -618,8 +635,9 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
     const int64_t rows = Tk + T * S;
     const int G = E + S;
 
-    // 1. routing with the given ids (replay: checked, gate weights recomputed),
+    // 1. routing (own, or with the given ids: checked, gate weights computed),
     //    dispatch, padded token offsets, gather (with the shared rows)
+    if (fwd) {
     MOE_TRY(mark_b(MOE_BWD_STAGE_ROUTE, 0, s));
     MOE_TRY(run_route(d, x, w, ids, ids_used, gates, wsb, L.f, s));
     MOE_TRY(mark_b(MOE_BWD_STAGE_ROUTE, 1, s));
@@ -630,6 +648,7 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
     MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), perm, T, k, D, S,
                              reinterpret_cast<uint16_t*>(wsb + L.f.xp), s)));
     MOE_TRY(mark_b(MOE_BWD_STAGE_DISPATCH, 1, s));
+    }
 
     const int units = sms / 2;  // CTA pairs
     const uint32_t box_b = BN_EXPERT / 2;
@@ -655,7 +674,9 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
     };
     const uint64_t EF = uint64_t(E) * F, ED = uint64_t(E) * D;
 
-    // 2. forward recompute: gate/up (H, and the fp32 pre-activations), down (Y)
+    // 2. the forward's expert GEMMs: gate/up (H, and the fp32 pre-activations),
+    //    down (routed Y; the shared rows too when the forward's output is formed)
+    if (fwd) {
     {
         GemmParams p;
         common(p, S, status + 4);
@@ -678,9 +699,11 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
         MOE_TRY(mark_b(MOE_BWD_STAGE_GATE_UP, 1, s));
     }
     {
+        const int sh = mode == TRAIN_FORWARD ? S : 0;
         GemmParams p;
-        common(p, 0, status + 5);
+        common(p, sh, status + 5);
         if (!make_map(&p.a0, w->w_down, F, ED, BM)) return MOE_ERR_CUDA;
+        if (sh && !make_map(&p.as0, w->ws_down, F, D, BM)) return MOE_ERR_CUDA;
         if (!make_map(&p.b, wsb + L.f.h, F, rows, box_b) ||
             !make_map(&p.b32, wsb + L.f.h, F, rows, 32))
             return MOE_ERR_CUDA;
@@ -688,13 +711,30 @@ moe_status backward_impl(const moe_dims* d, const void* x, const moe_weights* w,
         p.MT = (D + 2 * BM - 1) / (2 * BM);
         p.KB = F / BK;
         p.out = wsb + L.f.y;
+        p.out_shared = sh ? wsb + L.f.ysh : nullptr;
         p.ldo = D;
         MOE_TRY(mark_b(MOE_BWD_STAGE_DOWN, 0, s));
-        MOE_TRY(launch(GEMM_DOWN, p, tok_tiles));
+        MOE_TRY(launch(GEMM_DOWN, p, tok_tiles + (sh ? sh_tiles : 0)));
         MOE_TRY(mark_b(MOE_BWD_STAGE_DOWN, 1, s));
     }
+    }
+    if (mode == TRAIN_FORWARD) {
+        // the layer output (fixed-order combine) and the routing the forward used
+        MOE_TRY(mark(MOE_STAGE_COMBINE, 0, s));
+        MOE_TRY(cu(launch_combine(reinterpret_cast<const uint16_t*>(wsb + L.f.y),
+                                  S ? reinterpret_cast<const float*>(wsb + L.f.ysh) : nullptr, inv,
+                                  gates, valid, T, k, D, d->out_fp32, out, s)));
+        MOE_TRY(mark(MOE_STAGE_COMBINE, 1, s));
+        MOE_TRY(cu(cudaMemcpyAsync(ids_out, ids_used, Tk * sizeof(int32_t),
+                                   cudaMemcpyDeviceToDevice, s)));
+        return cu(cudaMemcpyAsync(gates_out, gates, Tk * sizeof(float), cudaMemcpyDeviceToDevice,
+                                  s));
+    }
 
-    // 3. gate and router gradients; dx starts as the router's part
+    // 3. gate and router gradients; dx starts as the router's part.  The tile
+    //    counters of the two gradient GEMMs are cleared here (the backward may
+    //    run more than once on one training forward's workspace).
+    MOE_TRY(cu(cudaMemsetAsync(status + 6, 0, 2 * sizeof(int32_t), s)));
     MOE_TRY(mark_b(MOE_BWD_STAGE_GATE, 0, s));
     MOE_TRY(cu(launch_gate_bwd(static_cast<const uint16_t*>(dout),
                                reinterpret_cast<const uint16_t*>(wsb + L.f.y), inv, ids_used, gates,
@@ -1032,8 +1072,22 @@ moe_status moe_backward_workspace_layout(const moe_dims* dims, moe_bwd_ws_layout
 moe_status moe_backward(const moe_dims* dims, const void* x, const moe_weights* w, const void* wt,
                         const int32_t* ids, const void* dout, float* dx, const moe_grads* grads,
                         void* ws, size_t ws_bytes, moe_stream_t stream) {
-    return backward_impl(dims, x, w, wt, ids, dout, dx, grads, ws, ws_bytes,
-                         reinterpret_cast<cudaStream_t>(stream));
+    return train_impl(TRAIN_BACKWARD, dims, x, w, wt, ids, dout, dx, grads, nullptr, nullptr,
+                      nullptr, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_forward_train(const moe_dims* dims, const void* x, const moe_weights* w,
+                             const int32_t* ids_in, void* out, int32_t* ids_out, float* gates_out,
+                             void* ws, size_t ws_bytes, moe_stream_t stream) {
+    return train_impl(TRAIN_FORWARD, dims, x, w, nullptr, ids_in, nullptr, nullptr, nullptr, out,
+                      ids_out, gates_out, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+moe_status moe_backward_saved(const moe_dims* dims, const moe_weights* w, const void* wt,
+                              const void* dout, float* dx, const moe_grads* grads, void* ws,
+                              size_t ws_bytes, moe_stream_t stream) {
+    return train_impl(TRAIN_SAVED, dims, nullptr, w, wt, nullptr, dout, dx, grads, nullptr,
+                      nullptr, nullptr, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

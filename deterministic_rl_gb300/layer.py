@@ -171,6 +171,35 @@ class MoELayer:
                        self.backward_workspace(T), stream)
         return dx, g
 
+    def forward_train(self, x: torch.Tensor, replay_ids: Optional[torch.Tensor] = None,
+                      stream=None, outputs=None):
+        """The forward (own routing, or replay of replay_ids), keeping in the
+        backward workspace what backward_saved reads; same outputs as forward()."""
+        T = x.shape[0]
+        out, ids, gates = outputs if outputs is not None else self.outputs(T)
+        B.moe_forward_train(self.dims(T), x, self.weights, replay_ids, out, ids, gates,
+                            self.backward_workspace(T), stream)
+        self._saved_T = T
+        return out, ids, gates
+
+    def backward_saved(self, dout: torch.Tensor, stream=None, grads: Optional[dict] = None,
+                       dx: Optional[torch.Tensor] = None):
+        """The backward of the last forward_train (same results as backward()
+        on its x and ids, without recomputing the forward)."""
+        T = dout.shape[0]
+        if getattr(self, "_saved_T", None) != T:
+            raise ValueError("backward_saved needs a forward_train of the same batch first")
+        if self._wt is None:
+            self.prepare_backward(stream)
+        g = grads if grads is not None else self.alloc_grads()
+        if dx is None:
+            dx = torch.empty((T, self.d), dtype=torch.float32, device=self.device)
+        cg = B.make_grads(g["d_router"], g["d_gate"], g["d_up"], g["d_down"], g.get("ds_gate"),
+                          g.get("ds_up"), g.get("ds_down"))
+        B.moe_backward_saved(self.dims(T), self.weights, self._wt, dout, dx, cg,
+                             self.backward_workspace(T), stream)
+        return dx, g
+
     def backward_status(self, stream=None) -> int:
         return B.moe_get_status(self._bws, stream)
 

@@ -384,6 +384,23 @@ moe_status moe_backward(const moe_dims *dims, const void *x, const moe_weights *
                         const void *wt, const int32_t *ids, const void *dout, float *dx,
                         const moe_grads *grads, void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Training without the forward recompute: moe_forward_train is the layer
+ * forward (own routing when ids_in is NULL, replay otherwise -- same outputs,
+ * bitwise, as moe_forward / moe_forward_replay) run in a BACKWARD workspace
+ * (moe_backward_workspace_size), where it leaves what the backward reads: the
+ * routing, the gathered rows, H, the fp32 gate/up pre-activations and the
+ * routed expert outputs.  moe_backward_saved then computes exactly what
+ * moe_backward computes for the same x, weights, ids and dout (bitwise), from
+ * that workspace, without routing, dispatch or the forward's expert GEMMs.
+ * The caller keeps the workspace untouched in between and passes the same
+ * dims and weights to both calls; nothing checks that it did. */
+moe_status moe_forward_train(const moe_dims *dims, const void *x, const moe_weights *w,
+                             const int32_t *ids_in, void *out, int32_t *ids_out,
+                             float *gates_out, void *ws, size_t ws_bytes, moe_stream_t stream);
+moe_status moe_backward_saved(const moe_dims *dims, const moe_weights *w, const void *wt,
+                              const void *dout, float *dx, const moe_grads *grads, void *ws,
+                              size_t ws_bytes, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -210,3 +210,29 @@ def test_backward_host_validation_codes(lib):
                                             ctypes.c_void_p(0x90000), 16, None) == B.MOE_ERR_WORKSPACE
     assert lib.moe_backward_prepare_weights(ctypes.byref(d.c()), ctypes.byref(_weights(w_up=None)),
                                             ctypes.c_void_p(0x90000), 1 << 40, None) == B.MOE_ERR_ARG
+
+
+def test_training_entry_points_validate(lib):
+    d = good_dims()
+    ws = _DEFAULT_WS
+    nb = B.moe_backward_workspace_size(d)
+    v = lambda a: ctypes.c_void_p(a)  # noqa: E731
+    W = _weights()
+    f = lambda **kw: lib.moe_forward_train(  # noqa: E731
+        ctypes.byref(kw.get("dims", d).c()), v(kw.get("x", 0x1000)), ctypes.byref(kw.get("w", W)),
+        v(kw.get("ids", None)), v(kw.get("out", 0x2000)), v(kw.get("ids_out", 0x3000)),
+        v(kw.get("g", 0x4000)), v(0x10000), kw.get("nb", nb), v(None))
+    assert f(dims=good_dims(T=0)) == B.MOE_OK
+    assert f(x=None) == B.MOE_ERR_ARG
+    assert f(out=None) == B.MOE_ERR_ARG
+    assert f(g=0x4004) == B.MOE_ERR_ALIGN
+    assert f(nb=nb - 1) == B.MOE_ERR_WORKSPACE
+    assert f(dims=good_dims(wfmt=1)) == B.MOE_ERR_UNSUPPORTED
+    grads = B.moe_grads(0xA000, 0xB000, 0xC000, 0xD000, 0xE000, 0xF000, 0x11000)
+    sb = lambda **kw: lib.moe_backward_saved(  # noqa: E731
+        ctypes.byref(d.c()), ctypes.byref(W), v(kw.get("wt", 0x90000)), v(kw.get("dout", 0x5000)),
+        v(kw.get("dx", 0x6000)), ctypes.byref(grads), v(0x10000), kw.get("nb", nb), v(None))
+    assert sb(wt=None) == B.MOE_ERR_ARG
+    assert sb(dout=None) == B.MOE_ERR_ARG
+    assert sb(dx=0x6008) == B.MOE_ERR_ALIGN
+    assert sb(nb=16) == B.MOE_ERR_WORKSPACE

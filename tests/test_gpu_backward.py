@@ -203,3 +203,29 @@ def test_full_size_layer_sampled():
         mc.check_grad(f"d_up[{e}]", g["d_up"][e], r.d_up)
         mc.check_grad(f"d_down[{e}]", g["d_down"][e], r.d_down)
     assert torch.isfinite(g["ds_gate"]).all() and torch.isfinite(g["d_router"]).all()
+
+
+@pytest.mark.parametrize("cfg", [CONFIGS["c1_tiny"].with_(n_shared=1, name="c1_tiny_shared"),
+                                 small_cfg(300, zipf=1.0), small_cfg(37, shared=0)],
+                         ids=lambda c: c.name)
+def test_training_forward_and_saved_backward_match_the_separate_calls(cfg):
+    inp = make_layer(cfg, "cuda")
+    ref_layer = MoELayer.from_inputs(inp, out_fp32=True)
+    layer = MoELayer.from_inputs(inp, out_fp32=True)
+    dout = make_dout(cfg, device="cuda")
+    rid = make_replay_ids(cfg, device="cuda")
+    for replay in (None, rid):
+        out0, ids0, g0 = ref_layer.forward(inp.x, replay_ids=replay)
+        out1, ids1, g1 = layer.forward_train(inp.x, replay_ids=replay)
+        torch.cuda.synchronize()
+        assert torch.equal(out0, out1) and torch.equal(ids0, ids1) and torch.equal(g0, g1)
+        dx0, gr0 = ref_layer.backward(inp.x, ids0, dout)
+        dx0 = dx0.clone()
+        gr0 = {k: v.clone() for k, v in gr0.items()}
+        for _ in range(2):  # twice on one training forward
+            dx1, gr1 = layer.backward_saved(dout)
+            torch.cuda.synchronize()
+            assert torch.equal(dx0, dx1)
+            for k in gr0:
+                assert torch.equal(gr0[k], gr1[k]), k
+    assert layer.backward_status() == 0
