@@ -70,7 +70,7 @@ class moe_grads(ctypes.Structure):
 class moe_bwd_ws_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("status", "logits", "valid", "cnt", "off", "perm", "inv", "xp", "h", "y",
-                 "ids", "gates", "poff", "a", "b", "dg", "dl", "dyq", "dh", "dab", "dabq", "dxp",
+                 "ids", "gates", "poff", "a", "b", "dg", "dl", "dyq", "dh", "dabq", "dxp",
                  "xpt", "dyt", "ht", "dabt", "kpad", "total")]
 
 

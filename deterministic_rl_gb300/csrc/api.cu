@@ -515,7 +515,7 @@ moe_status forward_impl(const moe_dims* d, const void* x, const moe_weights* w,
 
 struct BwdLayout {
     Layout f;  // the forward's regions first (status word at offset 0)
-    size_t ids, gates, poff, a, b, dg, dl, dyq, dh, dab, dabq, dxp, xpt, dyt, ht, dabt;
+    size_t ids, gates, poff, a, b, dg, dl, dyq, dh, dabq, dxp, xpt, dyt, ht, dabt;
     int64_t kpad;
     size_t total;
 };
@@ -557,7 +557,6 @@ BwdLayout make_bwd_layout(const moe_dims* d) {
     L.dl = take(T * k * 4);
     L.dyq = take(rows * D * 2);
     L.dh = take(rows * F * 4);
-    L.dab = take(rows * 2 * F * 4);
     L.dabq = take(rows * 2 * F * 2);
     L.dxp = take(rows * D * 4);
     L.xpt = take(D * kp * 2);
@@ -748,9 +747,14 @@ moe_status train_impl(TrainMode mode, const moe_dims* d, const void* x, const mo
 
     // 4. dH = Q_d(dY) Q_d(Wd)  (SM-pair grouped GEMM, fp32 rows)
     uint16_t* dyq = reinterpret_cast<uint16_t*>(wsb + L.dyq);
+    uint16_t* xpt = reinterpret_cast<uint16_t*>(wsb + L.xpt);
+    uint16_t* dyt = reinterpret_cast<uint16_t*>(wsb + L.dyt);
+    uint16_t* ht = reinterpret_cast<uint16_t*>(wsb + L.ht);
+    uint16_t* dabt = reinterpret_cast<uint16_t*>(wsb + L.dabt);
+    const int srows = S ? static_cast<int>(T) : 0;
     MOE_TRY(mark_b(MOE_BWD_STAGE_DY, 0, s));
-    MOE_TRY(cu(launch_dy_rows(static_cast<const uint16_t*>(dout), gates, perm, valid, T, k, D, S,
-                              dyq, sms, s)));
+    const SegDyArgs dya{static_cast<const uint16_t*>(dout), gates, perm, valid, k, Tk};
+    MOE_TRY(cu(launch_dy_dual(dya, D, cnt, off, poff, E, G, srows, L.kpad, dyq, dyt, sms, s)));
     MOE_TRY(mark_b(MOE_BWD_STAGE_DY, 1, s));
     {
         GemmParams p;
@@ -770,14 +774,13 @@ moe_status train_impl(TrainMode mode, const moe_dims* d, const void* x, const mo
         MOE_TRY(mark_b(MOE_BWD_STAGE_DH, 1, s));
     }
 
-    // 5. SwiGLU backward -> [dA | dB] (fp32 and quantised along F)
-    float* dab = reinterpret_cast<float*>(wsb + L.dab);
+    // 5. SwiGLU backward -> [dA | dB], quantised along F and along tokens
     uint16_t* dabq = reinterpret_cast<uint16_t*>(wsb + L.dabq);
     MOE_TRY(mark_b(MOE_BWD_STAGE_SWIGLU, 0, s));
-    MOE_TRY(cu(launch_swiglu_bwd(reinterpret_cast<const float*>(wsb + L.dh),
-                                 reinterpret_cast<const float*>(wsb + L.a),
-                                 reinterpret_cast<const float*>(wsb + L.b), dab, dabq, rows, F, sms,
-                                 s)));
+    MOE_TRY(cu(launch_swiglu_dual(reinterpret_cast<const float*>(wsb + L.dh),
+                                  reinterpret_cast<const float*>(wsb + L.a),
+                                  reinterpret_cast<const float*>(wsb + L.b), F, cnt, off, poff, E, G,
+                                  Tk, srows, L.kpad, dabq, dabt, sms, s)));
     MOE_TRY(mark_b(MOE_BWD_STAGE_SWIGLU, 1, s));
 
     // 6. dXp = Q_F(dA) Q_F(Wg) + Q_F(dB) Q_F(Wu)  (one K = 2F GEMM), then dx
@@ -803,22 +806,12 @@ moe_status train_impl(TrainMode mode, const moe_dims* d, const void* x, const mo
                                   sms, s)));
     MOE_TRY(mark_b(MOE_BWD_STAGE_DX, 1, s));
 
-    // 7. token-major operands, quantised along the tokens of each expert
-    uint16_t* xpt = reinterpret_cast<uint16_t*>(wsb + L.xpt);
-    uint16_t* dyt = reinterpret_cast<uint16_t*>(wsb + L.dyt);
-    uint16_t* ht = reinterpret_cast<uint16_t*>(wsb + L.ht);
-    uint16_t* dabt = reinterpret_cast<uint16_t*>(wsb + L.dabt);
-    const int srows = S ? static_cast<int>(T) : 0;
+    // 7. token-major Xp and H, quantised along the tokens of each expert
     MOE_TRY(mark_b(MOE_BWD_STAGE_TRANSPOSE, 0, s));
-    MOE_TRY(cu(launch_tq_segments(TQ_SRC_BF16, wsb + L.f.xp, D, nullptr, D, cnt, off, poff, E, G,
-                                  Tk, srows, L.kpad, xpt, sms, s)));
-    const SegDyArgs dya{static_cast<const uint16_t*>(dout), gates, perm, valid, k, Tk};
-    MOE_TRY(cu(launch_tq_segments(TQ_SRC_DY, nullptr, D, &dya, D, cnt, off, poff, E, G, Tk, srows,
-                                  L.kpad, dyt, sms, s)));
-    MOE_TRY(cu(launch_tq_segments(TQ_SRC_BF16, wsb + L.f.h, F, nullptr, F, cnt, off, poff, E, G,
-                                  Tk, srows, L.kpad, ht, sms, s)));
-    MOE_TRY(cu(launch_tq_segments(TQ_SRC_F32, dab, 2 * F, nullptr, 2 * F, cnt, off, poff, E, G, Tk,
-                                  srows, L.kpad, dabt, sms, s)));
+    MOE_TRY(cu(launch_tq_segments(reinterpret_cast<const uint16_t*>(wsb + L.f.xp), D, D, cnt, off,
+                                  poff, E, G, Tk, srows, L.kpad, xpt, sms, s)));
+    MOE_TRY(cu(launch_tq_segments(reinterpret_cast<const uint16_t*>(wsb + L.f.h), F, F, cnt, off,
+                                  poff, E, G, Tk, srows, L.kpad, ht, sms, s)));
     MOE_TRY(mark_b(MOE_BWD_STAGE_TRANSPOSE, 1, s));
 
     // 8. weight gradients (ragged-K grouped GEMMs)
@@ -1057,7 +1050,6 @@ moe_status moe_backward_workspace_layout(const moe_dims* dims, moe_bwd_ws_layout
     out->dl = L.dl;
     out->dyq = L.dyq;
     out->dh = L.dh;
-    out->dab = L.dab;
     out->dabq = L.dabq;
     out->dxp = L.dxp;
     out->xpt = L.xpt;

@@ -61,12 +61,6 @@ __device__ __forceinline__ uint4 mx_qdq8(const float (&v)[8], int X) {
                       pack_bf16x2(q[6], q[7]));
 }
 
-__device__ __forceinline__ float absmax8(const float (&v)[8]) {
-    float m = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[i]));
-    return m;
-}
 
 __device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -75,13 +69,6 @@ __device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8]) {
         v[2 * i] = __uint_as_float(w[i] << 16);
         v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
-}
-
-// Largest magnitude over a block of 32 values held 8 per lane by 4
-// consecutive lanes (lanes 4i .. 4i + 3).
-__device__ __forceinline__ float block_amax4(float m) {
-    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    return fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
 }
 
 // ---- row sources ----------------------------------------------------------------
@@ -95,21 +82,8 @@ struct SrcBf16 {
         scale = 1.0f;
         return *reinterpret_cast<const uint4*>(p + row * ld + c);
     }
-    __device__ __forceinline__ void load8(int64_t row, int c, float (&v)[8]) const {
-        unpack8(*reinterpret_cast<const uint4*>(p + row * ld + c), v);
-    }
 };
 
-struct SrcF32 {
-    const float* p;
-    int64_t ld;
-    __device__ __forceinline__ void load8(int64_t row, int c, float (&v)[8]) const {
-        const float4 a = *reinterpret_cast<const float4*>(p + row * ld + c);
-        const float4 b = *reinterpret_cast<const float4*>(p + row * ld + c + 4);
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    }
-};
 
 // The gradient of an expert-input row: routed row r (dispatch order) is pair
 // perm[r] = t*k + s and holds gate(t, s) * dout[t]; shared-expert row Tk + t
@@ -135,80 +109,7 @@ struct SrcDy {
         }
         return *reinterpret_cast<const uint4*>(dout + t * ld + c);
     }
-    __device__ __forceinline__ void load8(int64_t row, int c, float (&v)[8]) const {
-        int64_t t;
-        float w;
-        if (row < Tk) {
-            const int32_t pair = perm[row];
-            t = pair / k;
-            w = valid[t] ? gates[pair] : 0.0f;
-        } else {
-            t = row - Tk;
-            w = valid[t] ? 1.0f : 0.0f;
-        }
-        float x[8];
-        unpack8(*reinterpret_cast<const uint4*>(dout + t * ld + c), x);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = w * x[i];
-    }
 };
-
-// ---- row-wise quantisation: dY along d ----------------------------------------------
-
-// One warp per (row, 256-column chunk); lane l holds columns 8l .. 8l + 7.
-__global__ void __launch_bounds__(256) dy_rows_kernel(SrcDy src, uint16_t* __restrict__ out,
-                                                      int64_t rows, int d) {
-    const int lane = threadIdx.x & 31;
-    const int chunks = d / 256;
-    const int64_t items = rows * chunks;
-    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i < items;
-         i += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
-        const int64_t r = i / chunks;
-        const int c = static_cast<int>(i % chunks) * 256 + lane * 8;
-        float v[8];
-        src.load8(r, c, v);
-        const int X = mx_block_exp(block_amax4(absmax8(v)));
-        *reinterpret_cast<uint4*>(out + r * d + c) = mx_qdq8(v, X);
-    }
-}
-
-// ---- SwiGLU backward, then dA | dB quantised along F ---------------------------------
-
-// h = silu(a) * b with silu(a) = a * sigmoid(a):
-//   dA = dH * b * sigmoid(a) * (1 + a * (1 - sigmoid(a))),   dB = dH * silu(a).
-// Row r of dab holds [dA | dB] in fp32 (for the transposed quantiser) and row
-// r of dabq the same, quantised in blocks of 32 along F, as bf16.
-__global__ void __launch_bounds__(256) swiglu_bwd_kernel(
-    const float* __restrict__ dh, const float* __restrict__ A, const float* __restrict__ Bv,
-    float* __restrict__ dab, uint16_t* __restrict__ dabq, int64_t rows, int F) {
-    const int lane = threadIdx.x & 31;
-    const int chunks = F / 256;
-    const int64_t items = rows * chunks;
-    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i < items;
-         i += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
-        const int64_t r = i / chunks;
-        const int c = static_cast<int>(i % chunks) * 256 + lane * 8;
-        float g[8], a[8], b[8], da[8], db[8];
-        SrcF32{dh, F}.load8(r, c, g);
-        SrcF32{A, F}.load8(r, c, a);
-        SrcF32{Bv, F}.load8(r, c, b);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const float sg = 1.0f / (1.0f + expf(-a[j]));
-            da[j] = g[j] * b[j] * (sg * (1.0f + a[j] * (1.0f - sg)));
-            db[j] = g[j] * (a[j] * sg);
-        }
-        float* o = dab + r * 2 * F;
-        *reinterpret_cast<float4*>(o + c) = make_float4(da[0], da[1], da[2], da[3]);
-        *reinterpret_cast<float4*>(o + c + 4) = make_float4(da[4], da[5], da[6], da[7]);
-        *reinterpret_cast<float4*>(o + F + c) = make_float4(db[0], db[1], db[2], db[3]);
-        *reinterpret_cast<float4*>(o + F + c + 4) = make_float4(db[4], db[5], db[6], db[7]);
-        const int Xa = mx_block_exp(block_amax4(absmax8(da)));
-        const int Xb = mx_block_exp(block_amax4(absmax8(db)));
-        *reinterpret_cast<uint4*>(dabq + r * 2 * F + c) = mx_qdq8(da, Xa);
-        *reinterpret_cast<uint4*>(dabq + r * 2 * F + F + c) = mx_qdq8(db, Xb);
-    }
-}
 
 // ---- transposed quantisation (blocks of 32 along the rows) ----------------------------
 
@@ -346,11 +247,51 @@ __global__ void __launch_bounds__(256, 8) tq16_kernel(Src src, TqArgs a) {
     }
 }
 
-// fp32 rows: the tile holds tf[r][column ^ sw(r)], sw(r) = 8 * ((r / 16) % 4).
-// Loading: thread t reads row t / 4, columns 16 (t % 4) .. + 15 (four 16-byte
-// loads), stored as four 16-byte stores.
-template <bool SEG>
-__global__ void __launch_bounds__(256, 8) tq32_kernel(SrcF32 src, TqArgs a) {
+// ---- fused row-wise and token-major quantisation ---------------------------------------
+
+// A tile of 64 padded token rows x 64 columns whose values are computed once
+// and quantised both ways: along the columns (blocks of 32 in a row; threads
+// t and t ^ 1 hold one block) into the row-major operand of the dH or dXp GEMM,
+// and along the rows (blocks of 32 tokens) into the token-major operand of the
+// weight-gradient GEMM.  The tile is kept in shared memory as fp32,
+// tf[r][column ^ sw(r)] with sw(r) = 8 * ((r / 16) % 4), so that the column
+// pass reads without bank conflicts.
+__device__ __forceinline__ int tf_sw(int r) { return ((r >> 4) & 3) << 3; }
+
+__device__ __forceinline__ void tf_put16(float (*tf)[64], int r, int c16, const float (&v)[16]) {
+    const int sw = tf_sw(r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        *reinterpret_cast<float4*>(&tf[r][(c16 + 4 * i) ^ sw]) =
+            make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+}
+
+// Row pass: the block maximum of threads t and t ^ 1 (every lane takes part in
+// the shuffle); the quantised values are written only for rows that exist.
+__device__ __forceinline__ void row_q16(const float (&v)[16], bool store, uint16_t* dst) {
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    if (store) tq_store16(dst, 0, v, mx_block_exp(m));
+}
+
+// Column pass: thread (column c, part) takes rows 16 part .. + 15 of column c.
+__device__ __forceinline__ void col_q16(const float (*tf)[64], int c, int part, uint16_t* dst) {
+    float v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = tf[part * 16 + i][c ^ (part << 3)];
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    tq_store16(dst, 0, v, mx_block_exp(m));
+}
+
+// dY = gate * dout in expert order: Q_d(dY) rows [rows][d] for the dH GEMM and
+// the token-major Q_tok(dY) [d][kpad] for the dWd GEMM, from one read of dout.
+__global__ void __launch_bounds__(256) dy_dual_kernel(SrcDy src, TqArgs a,
+                                                      uint16_t* __restrict__ dyq, int d) {
     __shared__ __align__(16) float tf[kTqRows][64];
     const int tid = threadIdx.x;
     const int cchunks = a.C / 64;
@@ -359,34 +300,88 @@ __global__ void __launch_bounds__(256, 8) tq32_kernel(SrcF32 src, TqArgs a) {
         const int64_t rt = it / cchunks;
         const int cb = static_cast<int>(it % cchunks) * 64;
         TqBlock blk;
-        if (!tq_tile<SEG>(a, rt, blk)) continue;  // uniform across the CTA
+        if (!tq_tile<true>(a, rt, blk)) continue;  // uniform across the CTA
         {
             const int r = tid >> 2, c16 = (tid & 3) * 16;
-            float4 q[4] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f),
-                           make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
-            if (r < blk.nvalid) {
-                const float4* p4 =
-                    reinterpret_cast<const float4*>(src.p + (blk.in_row0 + r) * src.ld + cb + c16);
+            const bool ok = r < blk.nvalid;
+            float v[16];
+            if (ok) {
+                float w;
+                float lo[8], hi[8];
+                unpack8(src.raw8(blk.in_row0 + r, cb + c16, w), lo);
+                unpack8(src.raw8(blk.in_row0 + r, cb + c16 + 8, w), hi);
 #pragma unroll
-                for (int i = 0; i < 4; ++i) q[i] = p4[i];
+                for (int i = 0; i < 8; ++i) {
+                    v[i] = w * lo[i];
+                    v[8 + i] = w * hi[i];
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = 0.0f;
             }
-            const int sw = ((r >> 4) & 3) << 3;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                *reinterpret_cast<float4*>(&tf[r][(c16 + 4 * i) ^ sw]) = q[i];
+            row_q16(v, ok, dyq + (blk.in_row0 + r) * d + cb + c16);
+            tf_put16(tf, r, c16, v);
         }
         __syncthreads();
         {
             const int c = tid >> 2, part = tid & 3;
-            float v[16];
+            col_q16(tf, c, part, a.out + static_cast<int64_t>(cb + c) * a.ld + blk.out_col + part * 16);
+        }
+        __syncthreads();
+    }
+}
+
+// SwiGLU backward (h = silu(a) * b, silu(a) = a * sigmoid(a)):
+//   dA = dH * b * sigmoid(a) * (1 + a * (1 - sigmoid(a))),   dB = dH * silu(a),
+// quantised into [Q_F(dA) | Q_F(dB)] rows [rows][2F] for the dXp GEMM and the
+// token-major [Q_tok(dA) ; Q_tok(dB)] [2F][kpad] for the dWg / dWu GEMM.
+__global__ void __launch_bounds__(256) swiglu_dual_kernel(
+    const float* __restrict__ dh, const float* __restrict__ A, const float* __restrict__ Bv,
+    TqArgs a, uint16_t* __restrict__ dabq, int F) {
+    __shared__ __align__(16) float ta[kTqRows][64];
+    __shared__ __align__(16) float tb[kTqRows][64];
+    const int tid = threadIdx.x;
+    const int cchunks = a.C / 64;
+    const int64_t items = a.ntiles * cchunks;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int64_t rt = it / cchunks;
+        const int cb = static_cast<int>(it % cchunks) * 64;
+        TqBlock blk;
+        if (!tq_tile<true>(a, rt, blk)) continue;  // uniform across the CTA
+        {
+            const int r = tid >> 2, c16 = (tid & 3) * 16;
+            const bool ok = r < blk.nvalid;
+            const int64_t row = blk.in_row0 + r;
+            float da[16], db[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) v[i] = tf[part * 16 + i][c ^ (part << 3)];
-            float m = 0.0f;
+            for (int q = 0; q < 4; ++q) {
+                float4 g = make_float4(0.f, 0.f, 0.f, 0.f), x = g, y = g;
+                if (ok) {
+                    g = *reinterpret_cast<const float4*>(dh + row * F + cb + c16 + 4 * q);
+                    x = *reinterpret_cast<const float4*>(A + row * F + cb + c16 + 4 * q);
+                    y = *reinterpret_cast<const float4*>(Bv + row * F + cb + c16 + 4 * q);
+                }
+                const float gg[4] = {g.x, g.y, g.z, g.w}, xa[4] = {x.x, x.y, x.z, x.w},
+                            yb[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-            for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-            tq_store16(a.out, static_cast<int64_t>(cb + c) * a.ld + blk.out_col + part * 16, v,
-                       mx_block_exp(m));
+                for (int j = 0; j < 4; ++j) {
+                    const float sg = 1.0f / (1.0f + expf(-xa[j]));
+                    da[4 * q + j] = gg[j] * yb[j] * (sg * (1.0f + xa[j] * (1.0f - sg)));
+                    db[4 * q + j] = gg[j] * (xa[j] * sg);
+                }
+            }
+            uint16_t* qrow = dabq + row * 2 * F + cb + c16;
+            row_q16(da, ok, qrow);
+            row_q16(db, ok, qrow + F);
+            tf_put16(ta, r, c16, da);
+            tf_put16(tb, r, c16, db);
+        }
+        __syncthreads();
+        {
+            const int c = tid >> 2, part = tid & 3;
+            const int64_t at = static_cast<int64_t>(cb + c) * a.ld + blk.out_col + part * 16;
+            col_q16(ta, c, part, a.out + at);
+            col_q16(tb, c, part, a.out + at + static_cast<int64_t>(F) * a.ld);
         }
         __syncthreads();
     }
@@ -592,26 +587,6 @@ cudaError_t launch_seg_offsets(const int32_t* cnt, int E, int G, int shared_rows
     return cudaGetLastError();
 }
 
-cudaError_t launch_dy_rows(const uint16_t* dout, const float* gates, const int32_t* perm,
-                           const int32_t* valid, int64_t T, int k, int d, int n_shared,
-                           uint16_t* dyq, int sms, cudaStream_t s) {
-    if (d % 256) return cudaErrorInvalidValue;
-    const int64_t rows = T * k + T * n_shared;
-    if (rows == 0) return cudaSuccess;
-    SrcDy src{dout, gates, perm, valid, k, T * k, d};
-    dy_rows_kernel<<<grid_for(rows * (d / 256), 8, sms), 256, 0, s>>>(src, dyq, rows, d);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_swiglu_bwd(const float* dh, const float* a, const float* b, float* dab,
-                              uint16_t* dabq, int64_t rows, int F, int sms, cudaStream_t s) {
-    if (F % 256) return cudaErrorInvalidValue;
-    if (rows == 0) return cudaSuccess;
-    swiglu_bwd_kernel<<<grid_for(rows * (F / 256), 8, sms), 256, 0, s>>>(dh, a, b, dab, dabq,
-                                                                        rows, F);
-    return cudaGetLastError();
-}
-
 namespace {
 template <class Src, bool SEG>
 cudaError_t tq_launch(const Src& src, const TqArgs& a, int sms, cudaStream_t s) {
@@ -622,20 +597,11 @@ cudaError_t tq_launch(const Src& src, const TqArgs& a, int sms, cudaStream_t s) 
     return cudaGetLastError();
 }
 
-template <bool SEG>
-cudaError_t tq_launch32(const SrcF32& src, const TqArgs& a, int sms, cudaStream_t s) {
-    if (a.C % 64 || a.ld % 8) return cudaErrorInvalidValue;
-    const int64_t items = a.ntiles * (a.C / 64);
-    if (items == 0) return cudaSuccess;
-    tq32_kernel<SEG><<<grid_for(items, 1, sms, 8), 256, 0, s>>>(src, a);
-    return cudaGetLastError();
-}
 }  // namespace
 
-cudaError_t launch_tq_segments(int src_kind, const void* src, int64_t src_ld, const SegDyArgs* dy,
-                               int C, const int32_t* cnt, const int32_t* off, const int32_t* poff,
-                               int E, int G, int64_t shared_row0, int shared_rows, int64_t kpad,
-                               uint16_t* out, int sms, cudaStream_t s) {
+namespace {
+TqArgs seg_args(int C, const int32_t* cnt, const int32_t* off, const int32_t* poff, int E, int G,
+                int64_t shared_row0, int shared_rows, int64_t kpad, uint16_t* out) {
     TqArgs a{};
     a.C = C;
     a.ld = kpad;
@@ -647,20 +613,44 @@ cudaError_t launch_tq_segments(int src_kind, const void* src, int64_t src_ld, co
     a.G = G;
     a.shared_row0 = shared_row0;
     a.shared_rows = shared_rows;
-    if (kpad % kTqRows) return cudaErrorInvalidValue;
     a.ntiles = kpad / kTqRows;
-    switch (src_kind) {
-        case TQ_SRC_BF16:
-            return tq_launch<SrcBf16, true>(SrcBf16{static_cast<const uint16_t*>(src), src_ld}, a, sms, s);
-        case TQ_SRC_F32:
-            return tq_launch32<true>(SrcF32{static_cast<const float*>(src), src_ld}, a, sms, s);
-        case TQ_SRC_DY:
-            if (!dy) return cudaErrorInvalidValue;
-            return tq_launch<SrcDy, true>(
-                SrcDy{dy->dout, dy->gates, dy->perm, dy->valid, dy->k, dy->Tk, src_ld}, a, sms, s);
-        default:
-            return cudaErrorInvalidValue;
-    }
+    return a;
+}
+}  // namespace
+
+cudaError_t launch_tq_segments(const uint16_t* src, int64_t src_ld, int C, const int32_t* cnt,
+                               const int32_t* off, const int32_t* poff, int E, int G,
+                               int64_t shared_row0, int shared_rows, int64_t kpad, uint16_t* out,
+                               int sms, cudaStream_t s) {
+    if (kpad % kTqRows) return cudaErrorInvalidValue;
+    return tq_launch<SrcBf16, true>(SrcBf16{src, src_ld},
+                                    seg_args(C, cnt, off, poff, E, G, shared_row0, shared_rows,
+                                             kpad, out),
+                                    sms, s);
+}
+
+cudaError_t launch_dy_dual(const SegDyArgs& dy, int d, const int32_t* cnt, const int32_t* off,
+                           const int32_t* poff, int E, int G, int shared_rows, int64_t kpad,
+                           uint16_t* dyq, uint16_t* dyt, int sms, cudaStream_t s) {
+    if (kpad % kTqRows || d % 64) return cudaErrorInvalidValue;
+    const TqArgs a = seg_args(d, cnt, off, poff, E, G, dy.Tk, shared_rows, kpad, dyt);
+    const int64_t items = a.ntiles * (d / 64);
+    if (items == 0) return cudaSuccess;
+    const SrcDy src{dy.dout, dy.gates, dy.perm, dy.valid, dy.k, dy.Tk, d};
+    dy_dual_kernel<<<grid_for(items, 1, sms, 8), 256, 0, s>>>(src, a, dyq, d);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_swiglu_dual(const float* dh, const float* a_pre, const float* b_pre, int F,
+                               const int32_t* cnt, const int32_t* off, const int32_t* poff, int E,
+                               int G, int64_t shared_row0, int shared_rows, int64_t kpad,
+                               uint16_t* dabq, uint16_t* dabt, int sms, cudaStream_t s) {
+    if (kpad % kTqRows || F % 64) return cudaErrorInvalidValue;
+    const TqArgs a = seg_args(F, cnt, off, poff, E, G, shared_row0, shared_rows, kpad, dabt);
+    const int64_t items = a.ntiles * (F / 64);
+    if (items == 0) return cudaSuccess;
+    swiglu_dual_kernel<<<grid_for(items, 1, sms, 4), 256, 0, s>>>(dh, a_pre, b_pre, a, dabq, F);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_tq_batch(const uint16_t* src, int nb, int R, int C, uint16_t* out,

@@ -170,17 +170,7 @@ int wgrad_box_rows();  // rows of the a and b maps' boxes (one CTA's half)
 // poff[g] + round_up(n_g, 64).
 cudaError_t launch_seg_offsets(const int32_t* cnt, int E, int G, int shared_rows, int32_t* poff,
                                cudaStream_t s);
-// dY rows (gate(t,s) * dout[t] for routed row perm^-1, dout[t] for shared row
-// Tk + t; zero for rejected tokens) quantised to MXFP8 along d -> bf16 rows.
-cudaError_t launch_dy_rows(const uint16_t* dout, const float* gates, const int32_t* perm,
-                           const int32_t* valid, int64_t T, int k, int d, int n_shared,
-                           uint16_t* dyq, int sms, cudaStream_t s);
-// SwiGLU backward: dab [rows][2F] fp32 = [dA | dB], dabq the same quantised
-// along F (bf16).
-cudaError_t launch_swiglu_bwd(const float* dh, const float* a, const float* b, float* dab,
-                              uint16_t* dabq, int64_t rows, int F, int sms, cudaStream_t s);
 // Transposed MXFP8 quantisation (blocks of 32 along the input's rows).
-enum TqSrc : int { TQ_SRC_BF16 = 0, TQ_SRC_F32 = 1, TQ_SRC_DY = 2 };
 struct SegDyArgs {
     const uint16_t* dout;
     const float* gates;
@@ -189,12 +179,26 @@ struct SegDyArgs {
     int k;
     int64_t Tk;
 };
-// Segment mode: out[c][poff[g] + i] = Q(row i of group g)[c], groups padded
-// with zeros to their poff extent; out row stride kpad.
-cudaError_t launch_tq_segments(int src_kind, const void* src, int64_t src_ld, const SegDyArgs* dy,
-                               int C, const int32_t* cnt, const int32_t* off, const int32_t* poff,
-                               int E, int G, int64_t shared_row0, int shared_rows, int64_t kpad,
-                               uint16_t* out, int sms, cudaStream_t s);
+// Segment mode: out[c][poff[g] + i] = Q(row i of group g)[c] for bf16 rows
+// (src, row stride src_ld), groups padded with zeros to their poff extent;
+// out row stride kpad.
+cudaError_t launch_tq_segments(const uint16_t* src, int64_t src_ld, int C, const int32_t* cnt,
+                               const int32_t* off, const int32_t* poff, int E, int G,
+                               int64_t shared_row0, int shared_rows, int64_t kpad, uint16_t* out,
+                               int sms, cudaStream_t s);
+// dY (gate(t,s) * dout[t] for the routed row of pair t*k + s, dout[t] for shared
+// row Tk + t; zero for rejected tokens), quantised along d into dyq [rows][d]
+// and along each expert's tokens into dyt [d][kpad].
+cudaError_t launch_dy_dual(const SegDyArgs& dy, int d, const int32_t* cnt, const int32_t* off,
+                           const int32_t* poff, int E, int G, int shared_rows, int64_t kpad,
+                           uint16_t* dyq, uint16_t* dyt, int sms, cudaStream_t s);
+// SwiGLU backward from dH and the fp32 pre-activations, quantised along F into
+// dabq [rows][2F] = [dA | dB] and along each expert's tokens into dabt
+// [2F][kpad] = [dA ; dB].
+cudaError_t launch_swiglu_dual(const float* dh, const float* a_pre, const float* b_pre, int F,
+                               const int32_t* cnt, const int32_t* off, const int32_t* poff, int E,
+                               int G, int64_t shared_row0, int shared_rows, int64_t kpad,
+                               uint16_t* dabq, uint16_t* dabt, int sms, cudaStream_t s);
 // Batch mode: nb matrices [R][C] bf16 -> out[b * out_bstride + c * out_ld +
 // out_off + r] quantised along r.
 cudaError_t launch_tq_batch(const uint16_t* src, int nb, int R, int C, uint16_t* out,

@@ -232,7 +232,6 @@ class MoELayer:
             "dl": view(L.dl, T * k, torch.float32).view(T, k),
             "dyq": view(L.dyq, rows * d, torch.bfloat16).view(rows, d),
             "dh": view(L.dh, rows * F, torch.float32).view(rows, F),
-            "dab": view(L.dab, rows * 2 * F, torch.float32).view(rows, 2 * F),
             "dabq": view(L.dabq, rows * 2 * F, torch.bfloat16).view(rows, 2 * F),
             "dxp": view(L.dxp, rows * d, torch.float32).view(rows, d),
             "xpt": view(L.xpt, d * kp, torch.bfloat16).view(d, kp),

@@ -338,12 +338,12 @@ size_t moe_backward_workspace_size(const moe_dims *dims);
  * a backward workspace too.  Regions after a call: ids/gates the routing
  * used, poff [E+S+1] int32 padded token offsets per expert, a/b [rows][F]
  * fp32 gate/up pre-activations, dg/dl [T][k] fp32 gate and logit gradients,
- * dyq [rows][d], dh [rows][F] fp32, dab [rows][2F] fp32 (dA | dB), dabq,
+ * dyq [rows][d], dh [rows][F] fp32, dabq [rows][2F] (quantised dA | dB),
  * dxp [rows][d] fp32, and the token-major operands xpt, dyt [d][kpad],
  * ht [F][kpad], dabt [2F][kpad] (bf16), rows = T*k + T*n_shared. */
 typedef struct {
     size_t status, logits, valid, cnt, off, perm, inv, xp, h, y;
-    size_t ids, gates, poff, a, b, dg, dl, dyq, dh, dab, dabq, dxp, xpt, dyt, ht, dabt;
+    size_t ids, gates, poff, a, b, dg, dl, dyq, dh, dabq, dxp, xpt, dyt, ht, dabt;
     size_t kpad; /* elements per row of the token-major operands */
     size_t total;
 } moe_bwd_ws_layout;

@@ -152,7 +152,7 @@ def test_backward_sizes_and_layout(lib):
     L = B.moe_backward_workspace_layout(d)
     assert L.total == n > B.moe_workspace_size(d)
     offs = [L.status, L.logits, L.valid, L.cnt, L.off, L.perm, L.inv, L.xp, L.h, L.y, L.ids,
-            L.gates, L.poff, L.a, L.b, L.dg, L.dl, L.dyq, L.dh, L.dab, L.dabq, L.dxp, L.xpt, L.dyt,
+            L.gates, L.poff, L.a, L.b, L.dg, L.dl, L.dyq, L.dh, L.dabq, L.dxp, L.xpt, L.dyt,
             L.ht, L.dabt]
     assert offs == sorted(offs) and all(o % 256 == 0 for o in offs)
     rows = 4096 * 9
