@@ -68,3 +68,55 @@ def test_concurrent_calls_on_two_streams_match_eager():
         assert torch.equal(x, y)
     for x, y in zip(rb, ob):
         assert torch.equal(x, y)
+
+
+def test_training_step_graph_capture_replays_bitwise():
+    """Weight copies + training forward + saved backward captured once and
+    replayed: the same bits as the eager calls, also for new inputs."""
+    from deterministic_rl_gb300.synthetic import make_dout, make_replay_ids
+    cfg = _cfg(300, 65).with_(d=512, F=256)
+    inp = make_layer(cfg, "cuda")
+    layer = MoELayer.from_inputs(inp, out_fp32=True)
+    ids = make_replay_ids(cfg, device="cuda")
+    dout = make_dout(cfg, device="cuda")
+    T = cfg.T
+    out_e, _, _ = layer.forward_train(inp.x, replay_ids=ids)
+    out_e = out_e.clone()
+    dx_e, g_e = layer.backward_saved(dout)
+    dx_e = dx_e.clone()
+    g_e = {k: v.clone() for k, v in g_e.items()}
+    x_s, ids_s, dout_s = inp.x.clone(), ids.clone(), dout.clone()
+    outs = layer.outputs(T)
+    grads = layer.alloc_grads()
+    dx = torch.empty((T, cfg.d), dtype=torch.float32, device="cuda")
+    s = torch.cuda.Stream()
+
+    def step():
+        layer.prepare_backward(stream=s)
+        layer.forward_train(x_s, replay_ids=ids_s, outputs=outs, stream=s)
+        layer.backward_saved(dout_s, grads=grads, dx=dx, stream=s)
+
+    with torch.cuda.stream(s):
+        step()  # warm-up on the capture stream
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    dx.zero_()
+    outs[0].zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], out_e) and torch.equal(dx, dx_e)
+    for k in g_e:
+        assert torch.equal(grads[k], g_e[k]), k
+    # new dout through the same graph
+    dout2 = make_dout(cfg.with_(seed=cfg.seed + 1), device="cuda")
+    dout_s.copy_(dout2)
+    g.replay()
+    torch.cuda.synchronize()
+    layer.forward_train(inp.x, replay_ids=ids)
+    dx2, g2 = layer.backward_saved(dout2)
+    torch.cuda.synchronize()
+    assert torch.equal(dx, dx2)
+    for k in g2:
+        assert torch.equal(grads[k], g2[k]), k
