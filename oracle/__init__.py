@@ -41,6 +41,7 @@ _lock = threading.Lock()
 W_BF16 = 0
 W_MXFP8 = 1
 W_NVFP4 = 2
+W_MXFP8_ACT = 3
 
 
 def build(force: bool = False) -> str:
@@ -87,6 +88,8 @@ def _load():
         lib.oracle_round_bf16.argtypes = [ctypes.c_double]
         lib.oracle_nvfp4_quantize_rows.restype = None
         lib.oracle_nvfp4_quantize_rows.argtypes = [P, I, I, P, P, P]
+        lib.oracle_mx_qdq_rows.restype = None
+        lib.oracle_mx_qdq_rows.argtypes = [P, I, I, P]
         lib.oracle_matrix_elem.restype = ctypes.c_double
         lib.oracle_matrix_elem.argtypes = [ctypes.POINTER(_Matrix), I, I, I]
         lib.oracle_router_logits.restype = None
@@ -169,6 +172,17 @@ def nvfp4_quantize_rows(x: np.ndarray):
     return codes, bs, rs
 
 
+def mx_qdq_rows(x: np.ndarray) -> np.ndarray:
+    """MXFP8 quantise-dequantise of each row of x [R][K] (K % 32 == 0) in blocks
+    of 32 along the row (OCP MX v1.0, E4M3 elements); fp64 in and out."""
+    x = _c(x, np.float64)
+    R, K = x.shape
+    assert K % 32 == 0
+    out = np.empty((R, K), np.float64)
+    _load().oracle_mx_qdq_rows(_ptr(x), R, K, _ptr(out))
+    return out
+
+
 # ---- weights ----------------------------------------------------------------
 
 @dataclass
@@ -180,12 +194,15 @@ class Matrix:
     values: np.ndarray
     scales: Optional[np.ndarray] = None
     tscale: Optional[float] = None
+    act_mx: bool = False  # MXFP8 weights whose expert FFN quantises its activations too
 
     @property
     def fmt(self) -> int:
         if self.tscale is not None:
             return W_NVFP4
-        return W_MXFP8 if self.scales is not None else W_BF16
+        if self.scales is None:
+            return W_BF16
+        return W_MXFP8_ACT if self.act_mx else W_MXFP8
 
     @property
     def K(self) -> int:

@@ -150,6 +150,30 @@ static void nvfp4_quantised_values(const float *x, int64_t R, int64_t K, double 
     free(codes);
 }
 
+void oracle_mx_qdq_rows(const double *in, int64_t R, int64_t K, double *out) {
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t b = 0; b < K / 32; ++b) {
+            const double *v = in + r * K + 32 * b;
+            double *o = out + r * K + 32 * b;
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) amax = fmax(amax, fabs(v[i]));
+            int X = -127;
+            if (amax > 0.0) {
+                int e;
+                frexp(amax, &e); /* amax = m * 2^e, m in [0.5, 1): floor(log2) = e - 1 */
+                X = e - 1 - 8;
+                if (X < -127) X = -127;
+                if (X > 127) X = 127;
+            }
+            for (int i = 0; i < 32; ++i) {
+                const double s = ldexp(fabs(v[i]), -X); /* exact: a power of two */
+                const double q = oracle_e4m3_to_f64(oracle_e4m3_round((float)s));
+                o[i] = ldexp(v[i] < 0.0 ? -q : q, X);
+            }
+        }
+    }
+}
+
 double oracle_matrix_elem(const oracle_matrix *m, int64_t K, int64_t r, int64_t c) {
     if (m->fmt == ORACLE_W_BF16)
         return oracle_bf16_to_f64(((const uint16_t *)m->values)[r * K + c]);
@@ -320,7 +344,12 @@ void oracle_expert_ffn(const uint16_t *x, int64_t n, int64_t d, int64_t F,
     double *xd = (double *)malloc((size_t)(n * d) * sizeof(double));
     double *h = (double *)malloc((size_t)(n * F) * sizeof(double));
     const int nv = wg->fmt == ORACLE_W_NVFP4;
-    if (nv) {
+    const int mxa = wg->fmt == ORACLE_W_MXFP8_ACT;
+    if (mxa) {
+        /* MXFP8 expert compute: the token rows enter the GEMM quantised along d */
+        for (int64_t i = 0; i < n * d; ++i) xd[i] = oracle_bf16_to_f64(x[i]);
+        oracle_mx_qdq_rows(xd, n, d, xd);
+    } else if (nv) {
         /* NVFP4 forward: the token rows enter the GEMM quantised */
         float *xf = (float *)malloc((size_t)(n * d) * sizeof(float));
         for (int64_t i = 0; i < n * d; ++i) xf[i] = (float)oracle_bf16_to_f64(x[i]);
@@ -341,6 +370,11 @@ void oracle_expert_ffn(const uint16_t *x, int64_t n, int64_t d, int64_t F,
             }
             h[r * F + f] = silu(a) * b;
         }
+    }
+    if (mxa) {
+        /* h is stored in bf16 and quantised along F, row by row */
+        for (int64_t i = 0; i < n * F; ++i) h[i] = oracle_round_bf16(h[i]);
+        oracle_mx_qdq_rows(h, n, F, h);
     }
     if (nv) {
         /* h is stored in bf16 and quantised again, row by row */

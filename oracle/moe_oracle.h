@@ -50,11 +50,14 @@ extern "C" {
 #endif
 
 /* Weight storage formats the oracle reads. */
-enum { ORACLE_W_BF16 = 0, ORACLE_W_MXFP8 = 1, ORACLE_W_NVFP4 = 2 };
+enum { ORACLE_W_BF16 = 0, ORACLE_W_MXFP8 = 1, ORACLE_W_NVFP4 = 2, ORACLE_W_MXFP8_ACT = 3 };
 
 /* One weight matrix [rows][K], rows contiguous along K (K-major).
  * bf16: values = uint16 bf16 bit patterns, scales = NULL.
  * mxfp8: values = E4M3 (fn) bytes, scales = E8M0 bytes [rows][K/32].
+ * mxfp8_act: stored as mxfp8; the expert FFN also quantises its activations
+ *        (oracle_mx_qdq_rows: each x row along d, each bf16-rounded h row
+ *        along F), the MXFP8 expert compute of [TR] §6.1.
  * nvfp4: values = E2M1 codes packed two per byte [rows][K/2] (element 2j in the
  *        low nibble), scales = E4M3 bytes [rows][K/16], tscale = the matrix's
  *        FP32 scale; element = e2m1 * e4m3 * tscale. */
@@ -97,6 +100,15 @@ void oracle_nvfp4_quantize_rows(const float *x, int64_t R, int64_t K, uint8_t *c
                                 uint8_t *bscale, float *rscale);
 /* Round a double to the nearest bf16 value (ties to even), as a double. */
 double oracle_round_bf16(double v);
+
+/* ---- MXFP8 (OCP Microscaling Formats v1.0, E4M3 elements) -----------------
+ * [TR] §6.1 (Kernels): MXFP8 = E4M3 values with one E8M0 scale per block of
+ * 32 elements.  Per block: X = floor(log2(max |v|)) - 8 (8 = the exponent of
+ * E4M3's largest normal), within [-127, 127], -127 for an all-zero block;
+ * each value becomes E4M3(v / 2^X) * 2^X, nearest even, clamped to +-448.
+ * Quantise-dequantise R rows of K values (K % 32 == 0) along the rows, in ->
+ * out (may alias); inputs are values that fp32 holds exactly (bf16 values). */
+void oracle_mx_qdq_rows(const double *in, int64_t R, int64_t K, double *out);
 
 /* Router logits for T tokens: logits[t][e] = sum_j x[t][j]*wr[e][j] + bias[e].
  * x [T][d] bf16, wr [E][d] bf16, bias [E] fp32 or NULL. */

@@ -271,3 +271,44 @@ def test_invalid_tokens_contribute_nothing():
     assert not a.dx[[2, 9]].any()
     for e in a.experts:
         np.testing.assert_array_equal(a.experts[e].d_down, b.experts[e].d_down)
+
+
+# ---- the C oracle's MXFP8 row quantiser (MXFP8 activations in the forward) -------
+
+def test_c_mx_quantiser_equals_the_numpy_one_and_the_golden_blocks():
+    rng = np.random.default_rng(19)
+    x = rng.standard_normal((64, 256)) * np.ldexp(1.0, rng.integers(-30, 30, (64, 1)))
+    x = _bf16_vals(_bf16_bits(x))                      # bf16 values, as the layer has
+    np.testing.assert_array_equal(oracle.mx_qdq_rows(x), B.mx_quantize(x, 1))
+    for b in _golden_blocks():
+        v = _expand(b["values"])
+        np.testing.assert_array_equal(oracle.mx_qdq_rows(v[None, :])[0], _expand(b["dequant"]))
+
+
+def test_mxfp8_activation_expert_ffn_is_the_quantised_pipeline():
+    """The expert FFN with MXFP8 activations equals, on the decoded MXFP8
+    weights, x quantised along d -> SwiGLU in fp64 -> h rounded to bf16 and
+    quantised along F -> down projection (each step a pinned function)."""
+    import torch as _t
+    from deterministic_rl_gb300.synthetic import quantize_mxfp8
+    rng = np.random.default_rng(20)
+    n, d, F = 5, 64, 96
+    x = _bf16_bits(rng.standard_normal((n, d)))
+    mats = []
+    for shape in ((F, d), (F, d), (d, F)):
+        q, sc = quantize_mxfp8(_t.from_numpy(rng.standard_normal(shape).astype(np.float32) * 0.3))
+        mats.append((q.numpy(), sc.numpy()))
+    ex = Expert(*[Matrix(q, sc, act_mx=True) for q, sc in mats])
+    y = oracle.expert_ffn(x, ex)
+
+    def dec(q, sc):
+        vals = np.array([oracle.e4m3_to_f64(b) for b in range(256)])[q.astype(np.int64)]
+        return vals * np.repeat(np.ldexp(1.0, sc.astype(np.int64) - 127), 32, axis=1)
+    wg, wu, wd = (dec(q, sc) for q, sc in mats)
+    xq = B.mx_quantize(_bf16_vals(x), 1)
+    h = B.silu(xq @ wg.T) * (xq @ wu.T)
+    hq = B.mx_quantize(B.bf16_round(h), 1)
+    np.testing.assert_allclose(y, hq @ wd.T, rtol=1e-12, atol=1e-12)
+    # and it differs from the bf16-activation FFN on the same weights
+    y_plain = oracle.expert_ffn(x, Expert(*[Matrix(q, sc) for q, sc in mats]))
+    assert not np.allclose(y, y_plain, rtol=1e-6, atol=0)
