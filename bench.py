@@ -50,18 +50,19 @@ DISPATCH_SEGMENT_PAIRS = 4096  # (token, slot) pairs one dispatch CTA sorts
 ONE_SM_MAX_TOKENS = 128        # bf16 batches up to this size run the one-SM expert GEMMs
 
 
-def kernels_per_step(T, k, wfmt="bf16"):
+def kernels_per_step(T, k, wfmt="bf16", act_mx=False):
     """Launches of one layer call: router GEMM, top-k, dispatch (one kernel for
     at most one segment of pairs, else histogram, scan and scatter), gather,
-    gate/up, down, combine; NVFP4 adds the two activation quantisers."""
+    gate/up, down, combine; NVFP4 and MXFP8 activations add the two activation
+    quantisers."""
     n = 7 if T * k <= DISPATCH_SEGMENT_PAIRS else 9
-    return n + (2 if wfmt == "nvfp4" else 0)
+    return n + (2 if wfmt == "nvfp4" or act_mx else 0)
 
 
 def launches_per_step(cfg):
     """kernels_per_step plus the shared expert's own gate/up launch when it
     runs on the second stream beside the routing."""
-    n = kernels_per_step(cfg.T, cfg.k, cfg.wfmt)
+    n = kernels_per_step(cfg.T, cfg.k, cfg.wfmt, cfg.act_mx)
     if cfg.n_shared and cfg.wfmt == "bf16" and cfg.T > ONE_SM_MAX_TOKENS:
         n += 1
     return n
@@ -105,8 +106,9 @@ def peaks():
 
 
 def workload_desc(cfg, mode):
+    act = " activations=mxfp8" if cfg.act_mx else ""
     return (f"{cfg.name}: T={cfg.T} d={cfg.d} E={cfg.E} top-{cfg.k} F={cfg.F} "
-            f"shared={cfg.n_shared} weights={cfg.wfmt} mode={mode}")
+            f"shared={cfg.n_shared} weights={cfg.wfmt}{act} mode={mode}")
 
 
 def weight_bytes_per_value(cfg):

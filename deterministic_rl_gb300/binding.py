@@ -30,6 +30,7 @@ MOE_ERR_UNSUPPORTED = 8
 MOE_W_BF16 = 0
 MOE_W_MXFP8 = 1
 MOE_W_NVFP4 = 2
+MOE_W_MXFP8_ACT = 3
 
 # Every function the header declares, in declaration order.
 EXPORTED = ("moe_workspace_size", "moe_workspace_layout", "moe_route", "moe_forward",

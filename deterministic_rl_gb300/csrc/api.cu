@@ -23,7 +23,7 @@ using namespace moe;
 
 static_assert(moe::WFMT_BF16 == MOE_W_BF16 && moe::WFMT_MXFP8 == MOE_W_MXFP8 &&
                   moe::WFMT_NVFP4 == MOE_W_NVFP4,
-              "weight format codes match the ABI");
+              "weight format codes match the ABI");  // MOE_W_MXFP8_ACT runs the MXFP8 kernels
 
 namespace {
 
@@ -51,7 +51,9 @@ bool dims_ok(const moe_dims* d) {
     if (d->d < 64 || d->d > 16384 || d->d % 64) return false;
     if (d->F < 64 || d->F > 16384 || d->F % 64) return false;
     if (d->n_shared < 0 || d->n_shared > 1) return false;
-    if (d->wfmt != MOE_W_BF16 && d->wfmt != MOE_W_MXFP8 && d->wfmt != MOE_W_NVFP4) return false;
+    if (d->wfmt != MOE_W_BF16 && d->wfmt != MOE_W_MXFP8 && d->wfmt != MOE_W_NVFP4 &&
+        d->wfmt != MOE_W_MXFP8_ACT)
+        return false;
     // block-scaled weights: scale rows are loaded 8 k-blocks (512 along K) at a time
     if (d->wfmt != MOE_W_BF16 && (d->d % 512 || d->F % 512)) return false;
     if (d->out_fp32 != 0 && d->out_fp32 != 1) return false;
@@ -78,7 +80,8 @@ Layout make_layout(const moe_dims* d) {
     L.y = take(T * k * d->d * 2);
     L.ysh = take(S ? T * d->d * 4 : 0);
     const bool nv = d->wfmt == MOE_W_NVFP4;
-    L.xq = take(nv ? T * d->d * 2 : 0);
+    const bool mxa = d->wfmt == MOE_W_MXFP8_ACT;
+    L.xq = take(nv || mxa ? T * d->d * 2 : 0);
     L.sx = take(nv ? T * 4 : 0);
     L.sxp = take(nv ? T * k * 4 : 0);
     L.sh = take(nv ? T * k * 4 : 0);
@@ -316,8 +319,12 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     int32_t* inv = reinterpret_cast<int32_t*>(ws + L.inv);
     const int sms = num_sms();
     if (sms <= 0) return MOE_ERR_CUDA;
-    const bool mx = d->wfmt == MOE_W_MXFP8;
+    // MXFP8 activations: MXFP8 weights (the same kernels) and activations
+    // quantised along K before each expert GEMM
+    const bool mxa = d->wfmt == MOE_W_MXFP8_ACT;
+    const bool mx = d->wfmt == MOE_W_MXFP8 || mxa;
     const bool nv = d->wfmt == MOE_W_NVFP4;
+    const int kfmt = mx ? WFMT_MXFP8 : d->wfmt;  // the GEMM kernels' weight format
     const bool one = one_sm_experts(d);
     // MXFP8 / NVFP4 weights with few tokens: the SM-pair weight-streaming variant
     const int small = !one && d->wfmt != MOE_W_BF16 && T <= kOneSmMaxTokens;
@@ -383,6 +390,12 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
         MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(ws + L.xq), perm, T, k, d->d, S,
                                  reinterpret_cast<uint16_t*>(ws + L.xp), s,
                                  reinterpret_cast<const float*>(ws + L.sx), sxp)));
+    } else if (mxa) {
+        // MXFP8 activations: each token row quantised once along d, then gathered
+        MOE_TRY(cu(launch_mx_rows(static_cast<const uint16_t*>(x),
+                                  reinterpret_cast<uint16_t*>(ws + L.xq), T, d->d, sms, s)));
+        MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(ws + L.xq), perm, T, k, d->d,
+                                 Sg, reinterpret_cast<uint16_t*>(ws + L.xp), s)));
     } else {
         MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), perm, T, k, d->d, Sg,
                                  reinterpret_cast<uint16_t*>(ws + L.xp), s)));
@@ -443,7 +456,7 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     const int g1 = static_cast<int>(tb < units ? tb : units);
     MOE_TRY(mark(MOE_STAGE_GATE_UP, 0, s));
     MOE_TRY(cu(one ? launch_grouped_gemm(GEMM_SWIGLU, p1, g1, s)
-                   : launch_pair_gemm(GEMM_SWIGLU, p1, g1, s, d->wfmt, small)));
+                   : launch_pair_gemm(GEMM_SWIGLU, p1, g1, s, kfmt, small)));
     MOE_TRY(mark(MOE_STAGE_GATE_UP, 1, s));
 
     // down projection -> Y (routed, bf16) and Ysh (shared, fp32)
@@ -475,12 +488,15 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     const int g2 = static_cast<int>(tb < units ? tb : units);
     if (overlap) MOE_TRY(cu(cudaStreamWaitEvent(s, side->join, 0)));
     MOE_TRY(mark(MOE_STAGE_DOWN, 0, s));
+    if (mxa)  // MXFP8 activations: each row of h quantised in place along F
+        MOE_TRY(cu(launch_mx_rows(reinterpret_cast<const uint16_t*>(ws + L.h),
+                                  reinterpret_cast<uint16_t*>(ws + L.h), T * k, d->F, sms, s)));
     if (nv)  // NVFP4: each row of h quantised in place (per-token scale)
         MOE_TRY(cu(launch_nvfp4_qdq(reinterpret_cast<const uint16_t*>(ws + L.h),
                                     reinterpret_cast<uint16_t*>(ws + L.h), nullptr, sh, T * k,
                                     d->F, sms, s)));
     MOE_TRY(cu(one ? launch_grouped_gemm(GEMM_DOWN, p2, g2, s)
-                   : launch_pair_gemm(GEMM_DOWN, p2, g2, s, d->wfmt, small)));
+                   : launch_pair_gemm(GEMM_DOWN, p2, g2, s, kfmt, small)));
     MOE_TRY(mark(MOE_STAGE_DOWN, 1, s));
 
     MOE_TRY(mark(MOE_STAGE_COMBINE, 0, s));

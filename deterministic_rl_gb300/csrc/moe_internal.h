@@ -216,6 +216,11 @@ cudaError_t launch_router_wgrad(const uint16_t* xp, const int32_t* perm, const i
 cudaError_t launch_dx_assemble(const float* dxp, const int32_t* inv, float* dx, int64_t T, int k,
                                int d, int n_shared, int sms, cudaStream_t s);
 
+// MXFP8 activations: R rows of K bf16 values (K % 256 == 0) quantised along
+// the row in blocks of 32, written as the exact bf16 values to dst (may be src).
+cudaError_t launch_mx_rows(const uint16_t* src, uint16_t* dst, int64_t R, int K, int sms,
+                           cudaStream_t s);
+
 // Fixed-order combine of each token's k expert rows and the shared row.
 cudaError_t launch_combine(const uint16_t* y, const float* ysh, const int32_t* inv,
                            const float* gates, const int32_t* valid, int64_t T, int k, int d,

@@ -1,0 +1,65 @@
+// mxfp8.cu -- MXFP8 activations of the forward with MXFP8 expert compute.
+//
+// Composer 2 Technical Report, §6.1 "Training infrastructure" (Kernels): the
+// tokens are quantised to MXFP8 before dispatch, and the expert compute runs
+// in MXFP8.  With MXFP8 weights, each token row of x is quantised along d and
+// each row of the SwiGLU output h (stored in bf16) along F, in blocks of 32
+// (mx.cuh); the expert GEMMs then multiply the exact MXFP8 values of both
+// operands.
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "moe_internal.h"
+#include "mx.cuh"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ void unpack8_bf16(const uint4& u, float (&v)[8]) {
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[2 * i] = __uint_as_float(w[i] << 16);
+        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+
+// One warp per (row, 256-column chunk): lane l holds columns 8l .. 8l + 7, so
+// a block of 32 is held by lanes 4i .. 4i + 3.  src and dst may be the same
+// rows (each lane reads its 8 values before it writes them).
+__global__ void __launch_bounds__(256) mx_rows_kernel(const uint4* src, uint4* dst, int64_t R,
+                                                      int K) {
+    const int lane = threadIdx.x & 31;
+    const int chunks = K / 256;
+    const int64_t items = R * chunks;
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i < items;
+         i += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
+        const int64_t r = i / chunks;
+        const int64_t at = (r * K + static_cast<int64_t>(i % chunks) * 256 + lane * 8) / 8;
+        float v[8];
+        unpack8_bf16(src[at], v);
+        float m = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+        m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+        dst[at] = mx_qdq8(v, mx_block_exp(m));
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_mx_rows(const uint16_t* src, uint16_t* dst, int64_t R, int K, int sms,
+                           cudaStream_t s) {
+    if (K % 256) return cudaErrorInvalidValue;
+    if (R == 0) return cudaSuccess;
+    int64_t blocks = (R * (K / 256) + 7) / 8;  // 8 warps per block
+    const int64_t cap = static_cast<int64_t>(sms) * 8;
+    if (blocks > cap) blocks = cap;
+    mx_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), R, K);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

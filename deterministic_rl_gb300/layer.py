@@ -13,17 +13,23 @@ from . import binding as B
 class MoELayer:
     def __init__(self, w_router, w_gate, w_up, w_down, *, k: int = 8, router_bias=None,
                  s_gate=None, s_up=None, s_down=None, ws_gate=None, ws_up=None, ws_down=None,
-                 gs_gate=None, gs_up=None, gs_down=None, out_fp32: bool = False):
-        """Weight formats: bf16 (s_* None); MXFP8 (s_* E8M0 scales); NVFP4
-        (gs_* per-matrix fp32 scales given; w_* packed E2M1, s_* E4M3)."""
+                 gs_gate=None, gs_up=None, gs_down=None, out_fp32: bool = False,
+                 act_mx: bool = False):
+        """Weight formats: bf16 (s_* None); MXFP8 (s_* E8M0 scales; with act_mx
+        the activations are quantised to MXFP8 too); NVFP4 (gs_* per-matrix
+        fp32 scales given; w_* packed E2M1, s_* E4M3)."""
         self.E, self.d = w_router.shape
         self.F = w_gate.shape[1]
         self.k = k
         self.n_shared = 1 if ws_gate is not None else 0
         if gs_gate is not None:
             self.wfmt = B.MOE_W_NVFP4
+        elif s_gate is not None:
+            self.wfmt = B.MOE_W_MXFP8_ACT if act_mx else B.MOE_W_MXFP8
         else:
-            self.wfmt = B.MOE_W_MXFP8 if s_gate is not None else B.MOE_W_BF16
+            if act_mx:
+                raise ValueError("MXFP8 activations need MXFP8 weights")
+            self.wfmt = B.MOE_W_BF16
         self.out_fp32 = bool(out_fp32)
         self.device = w_router.device
         # keep references so the pointers stay valid
@@ -42,7 +48,7 @@ class MoELayer:
                    router_bias=inp.router_bias, s_gate=inp.s_gate, s_up=inp.s_up,
                    s_down=inp.s_down, ws_gate=inp.ws_gate, ws_up=inp.ws_up,
                    ws_down=inp.ws_down, gs_gate=inp.gs_gate, gs_up=inp.gs_up,
-                   gs_down=inp.gs_down, out_fp32=out_fp32)
+                   gs_down=inp.gs_down, out_fp32=out_fp32, act_mx=inp.cfg.act_mx)
 
     def dims(self, T: int) -> B.Dims:
         return B.Dims(T, self.d, self.E, self.k, self.F, self.n_shared, self.wfmt,
@@ -115,6 +121,8 @@ class MoELayer:
         }
         if self.n_shared:
             r["ysh"] = view(L.ysh, T * d, torch.float32).view(T, d)
+        if self.wfmt == B.MOE_W_MXFP8_ACT:
+            r["xq"] = view(L.xq, T * d, torch.bfloat16).view(T, d)
         if self.wfmt == B.MOE_W_NVFP4:
             r["xq"] = view(L.xq, T * d, torch.bfloat16).view(T, d)
             r["sx"] = view(L.sx, T, torch.float32)

@@ -46,6 +46,7 @@ class MoEConfig:
     near_tie_frac: float = 0.0    # fraction of tokens to near-tie (built in tests)
     replay_noise: float = 1e-3    # std of the perturbation replay ids come from
     w_std: float = 0.02
+    act_mx: bool = False          # MXFP8 weights: activations quantised to MXFP8 too
 
     def with_(self, **kw) -> "MoEConfig":
         return replace(self, **kw)
@@ -59,6 +60,9 @@ CONFIGS = {
     "c5_mxfp8": MoEConfig("c5_mxfp8", 4, 16384, 7168, 384, 8, 2048, 0, wfmt="mxfp8",
                           near_tie_frac=0.1),
     "c6_nvfp4": MoEConfig("c6_nvfp4", 5, 16384, 7168, 384, 8, 2048, 0, wfmt="nvfp4"),
+    # the MXFP8 layer with MXFP8 activations as well (same seed, same weights)
+    "c5_mxfp8_act": MoEConfig("c5_mxfp8_act", 4, 16384, 7168, 384, 8, 2048, 0, wfmt="mxfp8",
+                              near_tie_frac=0.1, act_mx=True),
 }
 
 

@@ -43,8 +43,8 @@
  *     batch or on T.  Expert outputs of a token are added in ascending slot
  *     order, then the shared expert, with fp32 accumulation ([TD], [CH]).
  *   - Limits of this version.  k == 8; 8 <= E <= 512; d and F multiples of
- *     64 (and of 512 for MXFP8 weights), 64 <= d, F <= 16384; n_shared in
- *     {0, 1} (0 with MXFP8 weights: MOE_ERR_UNSUPPORTED otherwise);
+ *     64 (and of 512 for MXFP8 / NVFP4 weights), 64 <= d, F <= 16384; n_shared
+ *     in {0, 1} (0 with MXFP8 / NVFP4 weights: MOE_ERR_UNSUPPORTED otherwise);
  *     1 <= T <= 2^20 (T == 0 is a no-op that returns MOE_OK).
  *     Device pointers must be 16-byte aligned.
  */
@@ -80,13 +80,20 @@ typedef enum {
     MOE_W_MXFP8 = 1,  /* expert weights E4M3 + one E8M0 scale per 32 along K
                          ([TR] §6.1: the MXFP8 format); router and shared
                          expert stay bf16                                     */
-    MOE_W_NVFP4 = 2   /* the NVFP4 forward ([TR] §6.1, Kernels): expert
+    MOE_W_NVFP4 = 2,  /* the NVFP4 forward ([TR] §6.1, Kernels): expert
                          weights E2M1 (two per byte) + one E4M3 scale per 16
                          along K + one fp32 scale per matrix; the token rows
                          entering each expert GEMM (x, and the SwiGLU
                          activations h in bf16) are quantised to E2M1 with an
                          E4M3 scale per 16 and an fp32 scale per token, with
                          IEEE division.  Router stays bf16; no shared expert */
+    MOE_W_MXFP8_ACT = 3 /* MXFP8 expert compute ([TR] §6.1: tokens go out in
+                         MXFP8, the experts compute in MXFP8): weights as
+                         MOE_W_MXFP8, and the token rows entering each expert
+                         GEMM (x along d; the SwiGLU activations h, stored in
+                         bf16, along F) quantised to MXFP8 (OCP MX v1.0: per
+                         32 values X = floor(log2 max|v|) - 8, E4M3(v / 2^X)
+                         nearest even, clamped to +-448).  No shared expert */
 } moe_wfmt;
 
 /* Layer shape.  T tokens, hidden size d, E routed experts, k experts per

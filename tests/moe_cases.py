@@ -31,12 +31,12 @@ REL_FRO = 5e-3
 MAX_ABS = 3e-2
 
 
-def _mat(w: torch.Tensor, s, gs=None) -> Matrix:
+def _mat(w: torch.Tensor, s, gs=None, act_mx=False) -> Matrix:
     if w.dtype == torch.bfloat16:
         return Matrix(bf16_bits(w))
     if gs is not None:  # NVFP4: packed E2M1, E4M3 scales per 16, fp32 matrix scale
         return Matrix(u8(w), u8(s), float(gs))
-    return Matrix(u8(w), u8(s))
+    return Matrix(u8(w), u8(s), act_mx=act_mx)
 
 
 def expert_getter(inp):
@@ -45,9 +45,10 @@ def expert_getter(inp):
         su = inp.s_up[e] if inp.s_up is not None else None
         sd = inp.s_down[e] if inp.s_down is not None else None
         nv = inp.gs_gate is not None
-        return Expert(_mat(inp.w_gate[e], sg, inp.gs_gate[e] if nv else None),
-                      _mat(inp.w_up[e], su, inp.gs_up[e] if nv else None),
-                      _mat(inp.w_down[e], sd, inp.gs_down[e] if nv else None))
+        am = inp.cfg.act_mx
+        return Expert(_mat(inp.w_gate[e], sg, inp.gs_gate[e] if nv else None, am),
+                      _mat(inp.w_up[e], su, inp.gs_up[e] if nv else None, am),
+                      _mat(inp.w_down[e], sd, inp.gs_down[e] if nv else None, am))
     return get
 
 
