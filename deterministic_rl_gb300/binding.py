@@ -38,7 +38,8 @@ EXPORTED = ("moe_workspace_size", "moe_workspace_layout", "moe_route", "moe_forw
             "moe_route_static", "moe_forward_replay_filtered", "moe_backward_weights_size",
             "moe_backward_prepare_weights", "moe_backward_workspace_size",
             "moe_backward_workspace_layout", "moe_set_backward_stage_events", "moe_backward",
-            "moe_forward_train", "moe_backward_saved")
+            "moe_forward_train", "moe_backward_saved", "moe_packed_weights_size",
+            "moe_pack_weights")
 
 STAGES = ("router_gemm", "topk", "dispatch", "gather", "gate_up", "down", "combine")
 BWD_STAGES = ("prepare", "route", "dispatch", "gate_up", "down", "gate", "dy", "dh", "swiglu",
@@ -54,7 +55,8 @@ class moe_dims(ctypes.Structure):
 class moe_weights(ctypes.Structure):
     _fields_ = [(n, ctypes.c_void_p) for n in
                 ("w_router", "router_bias", "w_gate", "w_up", "w_down", "s_gate", "s_up",
-                 "s_down", "ws_gate", "ws_up", "ws_down", "gs_gate", "gs_up", "gs_down")]
+                 "s_down", "ws_gate", "ws_up", "ws_down", "gs_gate", "gs_up", "gs_down",
+                 "w_gate_up")]
 
 
 class moe_ws_layout(ctypes.Structure):
@@ -125,6 +127,10 @@ def load(path: str = LIB_PATH):
     lib.moe_backward_workspace_size.argtypes = [D]
     lib.moe_backward_workspace_layout.restype = ctypes.c_int
     lib.moe_backward_workspace_layout.argtypes = [D, ctypes.POINTER(moe_bwd_ws_layout)]
+    lib.moe_packed_weights_size.restype = ctypes.c_size_t
+    lib.moe_packed_weights_size.argtypes = [D]
+    lib.moe_pack_weights.restype = ctypes.c_int
+    lib.moe_pack_weights.argtypes = [D, W, P, ctypes.c_size_t, P]
     lib.moe_forward_train.restype = ctypes.c_int
     lib.moe_forward_train.argtypes = [D, P, W, P, P, P, P, P, ctypes.c_size_t, P]
     lib.moe_backward_saved.restype = ctypes.c_int
@@ -172,10 +178,10 @@ class Dims:
 
 def make_weights(w_router, router_bias, w_gate, w_up, w_down, s_gate=None, s_up=None,
                  s_down=None, ws_gate=None, ws_up=None, ws_down=None, gs_gate=None, gs_up=None,
-                 gs_down=None) -> moe_weights:
+                 gs_down=None, w_gate_up=None) -> moe_weights:
     return moe_weights(*(_p(t) for t in (w_router, router_bias, w_gate, w_up, w_down, s_gate,
                                          s_up, s_down, ws_gate, ws_up, ws_down, gs_gate, gs_up,
-                                         gs_down)))
+                                         gs_down, w_gate_up)))
 
 
 def moe_workspace_size(dims: Dims) -> int:
@@ -329,5 +335,18 @@ def moe_backward_saved(dims: Dims, weights: moe_weights, wt, dout, dx, grads: mo
                                    ws.numel() * ws.element_size(), _stream(stream))
     if check and rc != MOE_OK:
         raise MoEError(rc, "moe_backward_saved")
+    return rc
+
+
+def moe_packed_weights_size(dims: Dims) -> int:
+    return int(load().moe_packed_weights_size(ctypes.byref(dims.c())))
+
+
+def moe_pack_weights(dims: Dims, weights: moe_weights, packed, stream=None,
+                     check: bool = True) -> int:
+    rc = load().moe_pack_weights(ctypes.byref(dims.c()), ctypes.byref(weights), _p(packed),
+                                 packed.numel() * packed.element_size(), _stream(stream))
+    if check and rc != MOE_OK:
+        raise MoEError(rc, "moe_pack_weights")
     return rc
 

@@ -159,6 +159,8 @@ moe_status check_experts(const moe_dims* d, const moe_weights* w) {
         if (!al16(w->s_gate) || !al16(w->s_up) || !al16(w->s_down)) return MOE_ERR_ALIGN;
     }
     if (d->wfmt == MOE_W_NVFP4 && (!w->gs_gate || !w->gs_up || !w->gs_down)) return MOE_ERR_ARG;
+    if (!al16(w->w_gate_up)) return MOE_ERR_ALIGN;
+    if (w->w_gate_up && d->wfmt != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
     if (d->n_shared) {
         if (!w->ws_gate || !w->ws_up || !w->ws_down) return MOE_ERR_ARG;
         if (!al16(w->ws_gate) || !al16(w->ws_up) || !al16(w->ws_down)) return MOE_ERR_ALIGN;
@@ -340,6 +342,10 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     // dispatch and the gather run here; its tiles and the routed ones come
     // from queues, so the two launches share the SMs however they overlap.
     const bool overlap = S && !one && d->wfmt == MOE_W_BF16;
+    // packed gate/up weights (moe_pack_weights): routed experts, then the shared one
+    const bool packed = w->w_gate_up && !one && d->wfmt == MOE_W_BF16;
+    const uint8_t* pk = static_cast<const uint8_t*>(w->w_gate_up);
+    const uint8_t* pk_shared = pk ? pk + uint64_t(E) * 2 * d->F * d->d * 2 : nullptr;
     SideStream* side = nullptr;
     if (overlap) {
         MOE_TRY(side_stream(&side));
@@ -355,8 +361,14 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
         ps.partial_b = 1;
         ps.status = status;
         ps.timeout_ns = kWaitTimeoutNs;
-        if (!make_map(&ps.a0, w->ws_gate, d->d, d->F, rg)) return MOE_ERR_CUDA;
-        if (!make_map(&ps.a1, w->ws_up, d->d, d->F, rg)) return MOE_ERR_CUDA;
+        if (packed) {
+            if (!make_map(&ps.a0, pk_shared, d->d, 2 * d->F, 2 * rg)) return MOE_ERR_CUDA;
+            ps.a1 = ps.a0;
+            ps.a_packed = 1;
+        } else {
+            if (!make_map(&ps.a0, w->ws_gate, d->d, d->F, rg)) return MOE_ERR_CUDA;
+            if (!make_map(&ps.a1, w->ws_up, d->d, d->F, rg)) return MOE_ERR_CUDA;
+        }
         ps.as0 = ps.a0;
         ps.as1 = ps.a1;
         if (!make_map(&ps.b, x, d->d, T, box_b)) return MOE_ERR_CUDA;
@@ -435,13 +447,22 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
         p1.row_scale = sxp;
         p1.wscale0 = w->gs_gate;
         p1.wscale1 = w->gs_up;
+    } else if (packed) {
+        if (!make_map(&p1.a0, pk, d->d, 2 * EF, 2 * rg)) return MOE_ERR_CUDA;
+        p1.a1 = p1.a0;
+        p1.a_packed = 1;
     } else {
         if (!make_map(&p1.a0, w->w_gate, d->d, EF, rg)) return MOE_ERR_CUDA;
         if (!make_map(&p1.a1, w->w_up, d->d, EF, rg)) return MOE_ERR_CUDA;
     }
     if (Sg) {
-        if (!make_map(&p1.as0, w->ws_gate, d->d, d->F, rg)) return MOE_ERR_CUDA;
-        if (!make_map(&p1.as1, w->ws_up, d->d, d->F, rg)) return MOE_ERR_CUDA;
+        if (packed) {
+            if (!make_map(&p1.as0, pk_shared, d->d, 2 * d->F, 2 * rg)) return MOE_ERR_CUDA;
+            p1.as1 = p1.as0;
+        } else {
+            if (!make_map(&p1.as0, w->ws_gate, d->d, d->F, rg)) return MOE_ERR_CUDA;
+            if (!make_map(&p1.as1, w->ws_up, d->d, d->F, rg)) return MOE_ERR_CUDA;
+        }
     }
     if (!make_map(&p1.b, ws + L.xp, d->d, rows, box_b)) return MOE_ERR_CUDA;
     if (!make_map(&p1.b32, ws + L.xp, d->d, rows, 32)) return MOE_ERR_CUDA;
@@ -914,6 +935,33 @@ moe_status moe_workspace_layout(const moe_dims* dims, moe_ws_layout* out) {
     out->sxp = L.sxp;
     out->sh = L.sh;
     out->total = L.total;
+    return MOE_OK;
+}
+
+size_t moe_packed_weights_size(const moe_dims* dims) {
+    if (!dims_ok(dims) || dims->wfmt != MOE_W_BF16) return 0;
+    return size_t(dims->E + dims->n_shared) * 2 * dims->F * dims->d * 2;
+}
+
+moe_status moe_pack_weights(const moe_dims* d, const moe_weights* w, void* packed,
+                            size_t packed_bytes, moe_stream_t stream) {
+    if (!d || !w) return MOE_ERR_ARG;
+    if (!dims_ok(d)) return MOE_ERR_SHAPE;
+    if (d->wfmt != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
+    if (!packed || !w->w_gate || !w->w_up || (d->n_shared && (!w->ws_gate || !w->ws_up)))
+        return MOE_ERR_ARG;
+    if (!al16(packed) || !al16(w->w_gate) || !al16(w->w_up) || !al16(w->ws_gate) ||
+        !al16(w->ws_up))
+        return MOE_ERR_ALIGN;
+    if (packed_bytes < moe_packed_weights_size(d)) return MOE_ERR_WORKSPACE;
+    auto* s = reinterpret_cast<cudaStream_t>(stream);
+    auto* out = static_cast<uint16_t*>(packed);
+    MOE_TRY(cu(launch_pack_gate_up(static_cast<const uint16_t*>(w->w_gate),
+                                   static_cast<const uint16_t*>(w->w_up), d->E, d->F, d->d, out, s)));
+    if (d->n_shared)
+        MOE_TRY(cu(launch_pack_gate_up(static_cast<const uint16_t*>(w->ws_gate),
+                                       static_cast<const uint16_t*>(w->ws_up), 1, d->F, d->d,
+                                       out + int64_t(d->E) * 2 * d->F * d->d, s)));
     return MOE_OK;
 }
 

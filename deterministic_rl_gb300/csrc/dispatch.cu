@@ -246,4 +246,42 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int64_t T, int
     return cudaGetLastError();
 }
 
+namespace {
+
+// One thread per 16 bytes of the packed output: packed row ((g * F/64 + b) * 128
+// + i) is row 64 b + (i % 64) of gate[g] (i < 64) or of up[g] (i >= 64).
+__global__ void __launch_bounds__(256) pack_gate_up_kernel(const uint4* __restrict__ gate,
+                                                           const uint4* __restrict__ up,
+                                                           uint4* __restrict__ out, int64_t nmat,
+                                                           int F, int d) {
+    const int q = d / 8;  // uint4 per row
+    const int64_t rows = nmat * 2 * F;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < rows * q;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t prow = i / q;
+        const int c = static_cast<int>(i % q);
+        const int64_t blk = prow / 128;   // g * F/64 + b
+        const int r = static_cast<int>(prow % 128);
+        const int64_t g = blk / (F / 64);
+        const int b = static_cast<int>(blk % (F / 64));
+        const int64_t srow = g * F + 64 * b + (r & 63);
+        out[i] = (r < 64 ? gate : up)[srow * q + c];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_pack_gate_up(const uint16_t* gate, const uint16_t* up, int64_t nmat, int F,
+                                int d, uint16_t* packed, cudaStream_t s) {
+    if (F % 64 || d % 8) return cudaErrorInvalidValue;
+    const int64_t n = nmat * 2 * F * (d / 8);
+    if (n == 0) return cudaSuccess;
+    int64_t blocks = (n + 255) / 256;
+    if (blocks > 65536) blocks = 65536;
+    pack_gate_up_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        reinterpret_cast<const uint4*>(gate), reinterpret_cast<const uint4*>(up),
+        reinterpret_cast<uint4*>(packed), nmat, F, d);
+    return cudaGetLastError();
+}
+
 }  // namespace moe

@@ -555,8 +555,12 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                     if constexpr (MX) {
                         // the A operand comes from the converter warps
                     } else if constexpr (C::kPair) {
-                        tma_load_2d_pair(st, ma0, bar, kb * BK, tl.arow, pol_w);
-                        tma_load_2d_pair(st + kABytes / 2, ma1, bar, kb * BK, tl.arow, pol_w);
+                        if (p.a_packed) {  // gate and up rows adjacent: one copy
+                            tma_load_2d_pair(st, ma0, bar, kb * BK, 2 * tl.arow, pol_w);
+                        } else {
+                            tma_load_2d_pair(st, ma0, bar, kb * BK, tl.arow, pol_w);
+                            tma_load_2d_pair(st + kABytes / 2, ma1, bar, kb * BK, tl.arow, pol_w);
+                        }
                     } else {
                         tma_load_2d_pair(st, ma0, bar, kb * BK, tl.arow, pol_w);
                     }

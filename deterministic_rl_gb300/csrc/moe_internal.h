@@ -88,6 +88,10 @@ struct GemmParams {
     // SM-pair down (MODE 2): 1 = fp32 output rows; with out_shared null the
     // shared group's rows are stored like routed rows (at its B rows).
     int32_t out_f32;
+    // SM-pair bf16 gate/up: a0 (and as0) map the packed gate/up weights
+    // (64 gate rows then the same 64 up rows per block; 128-row boxes); the
+    // CTA's 128 operand rows are one box at packed row 2 * arow.
+    int32_t a_packed;
 };
 
 size_t gemm_smem_bytes(int mode, int n_groups_total);
@@ -220,6 +224,12 @@ cudaError_t launch_dx_assemble(const float* dxp, const int32_t* inv, float* dx, 
 // the row in blocks of 32, written as the exact bf16 values to dst (may be src).
 cudaError_t launch_mx_rows(const uint16_t* src, uint16_t* dst, int64_t R, int K, int sms,
                            cudaStream_t s);
+
+// Packed gate/up weights: G matrices pairs [F][d] (gate, up) -> [G][F/64][128][d]
+// (64 gate rows, then the same 64 up rows).  gate[g], up[g] are the g-th
+// matrices of the two lists given (routed experts, then the shared expert).
+cudaError_t launch_pack_gate_up(const uint16_t* gate, const uint16_t* up, int64_t nmat, int F,
+                                int d, uint16_t* packed, cudaStream_t s);
 
 // Fixed-order combine of each token's k expert rows and the shared row.
 cudaError_t launch_combine(const uint16_t* y, const float* ysh, const int32_t* inv,

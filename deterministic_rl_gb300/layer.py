@@ -50,6 +50,23 @@ class MoELayer:
                    ws_down=inp.ws_down, gs_gate=inp.gs_gate, gs_up=inp.gs_up,
                    gs_down=inp.gs_down, out_fp32=out_fp32, act_mx=inp.cfg.act_mx)
 
+    def pack_weights(self, stream=None) -> torch.Tensor:
+        """Pack the gate/up weights (bf16) for the SM-pair forward GEMM (one copy
+        per weight tile instead of two; same results).  Call again after the
+        weights change."""
+        n = B.moe_packed_weights_size(self.dims(1))
+        if n == 0:
+            raise B.MoEError(B.MOE_ERR_UNSUPPORTED, "moe_packed_weights_size")
+        self._packed = torch.empty(n, dtype=torch.uint8, device=self.device)
+        self.weights.w_gate_up = None
+        B.moe_pack_weights(self.dims(1), self.weights, self._packed, stream)
+        self.weights.w_gate_up = self._packed.data_ptr()
+        return self._packed
+
+    def unpack_weights(self) -> None:
+        self.weights.w_gate_up = None
+        self._packed = None
+
     def dims(self, T: int) -> B.Dims:
         return B.Dims(T, self.d, self.E, self.k, self.F, self.n_shared, self.wfmt,
                       int(self.out_fp32))

@@ -125,7 +125,14 @@ typedef struct {
  *   gs_gate, gs_up, gs_down [E] fp32  one scale per expert matrix
  *     (NULL unless MOE_W_NVFP4); element = e2m1 * e4m3 * gs
  *   ws_gate, ws_up [F][d], ws_down [d][F]  bf16 shared expert (NULL when
- *     n_shared == 0) */
+ *     n_shared == 0)
+ *   w_gate_up  optional (NULL = not used): the gate and up projections of the
+ *     routed experts and then of the shared expert, packed by
+ *     moe_pack_weights from the w_gate/w_up/ws_gate/ws_up given here
+ *     (bf16 only).  When set, the SM-pair gate/up GEMM of moe_forward /
+ *     moe_forward_replay(_filtered) reads each weight tile from it with one
+ *     copy instead of two; results are bitwise the same.  The caller repacks
+ *     after changing the weights; nothing checks that the copy is current. */
 typedef struct {
     const void *w_router;
     const float *router_bias;
@@ -141,6 +148,7 @@ typedef struct {
     const float *gs_gate;
     const float *gs_up;
     const float *gs_down;
+    const void *w_gate_up;
 } moe_weights;
 
 /* Byte offsets of the intermediate buffers inside the workspace, for
@@ -177,6 +185,19 @@ size_t moe_workspace_size(const moe_dims *dims);
 
 /* Fill *layout for dims.  MOE_ERR_ARG / MOE_ERR_SHAPE on bad input. */
 moe_status moe_workspace_layout(const moe_dims *dims, moe_ws_layout *layout);
+
+/* Bytes of the packed gate/up weights for dims (bf16 weights; 0 otherwise):
+ * (E + n_shared) * 2 * F * d * 2. */
+size_t moe_packed_weights_size(const moe_dims *dims);
+
+/* Pack w->w_gate, w->w_up (and ws_gate, ws_up) into `packed` (device,
+ * caller-owned, 16-byte aligned, moe_packed_weights_size bytes): per expert
+ * (routed ones, then the shared one), per block of 64 rows of F, the 64 gate
+ * rows and then the same 64 up rows, each row d bf16 values.  Set
+ * w->w_gate_up = packed afterwards to use it.  A pure copy; stream-ordered.
+ * MOE_ERR_UNSUPPORTED for non-bf16 weights. */
+moe_status moe_pack_weights(const moe_dims *dims, const moe_weights *w, void *packed,
+                            size_t packed_bytes, moe_stream_t stream);
 
 /* Routing only -- the side that records ids at inference ([TR] §6.2:
  * "the engine returns the selected expert indices").  Computes the router

@@ -236,3 +236,24 @@ def test_training_entry_points_validate(lib):
     assert sb(dout=None) == B.MOE_ERR_ARG
     assert sb(dx=0x6008) == B.MOE_ERR_ALIGN
     assert sb(nb=16) == B.MOE_ERR_WORKSPACE
+
+
+def test_pack_weights_validation(lib):
+    d = good_dims()
+    assert B.moe_packed_weights_size(d) == (384 + 1) * 2 * 2048 * 7168 * 2
+    assert B.moe_packed_weights_size(good_dims(wfmt=1)) == 0
+    v = ctypes.c_void_p
+    pk = lambda dims, w, ptr, n: lib.moe_pack_weights(  # noqa: E731
+        ctypes.byref(dims.c()), ctypes.byref(w), v(ptr), n, v(None))
+    n = B.moe_packed_weights_size(d)
+    assert pk(good_dims(wfmt=1), _weights(), 0x90000, n) == B.MOE_ERR_UNSUPPORTED
+    assert pk(d, _weights(), None, n) == B.MOE_ERR_ARG
+    assert pk(d, _weights(w_up=None), 0x90000, n) == B.MOE_ERR_ARG
+    assert pk(d, _weights(), 0x90008, n) == B.MOE_ERR_ALIGN
+    assert pk(d, _weights(), 0x90000, n - 1) == B.MOE_ERR_WORKSPACE
+    # a packed pointer with non-bf16 weights is refused by the forward
+    x, out, ids, g = _Fake(0x1000), _Fake(0x2000), _Fake(0x3000), _Fake(0x4000)
+    w = _weights(w_gate_up=_Fake(0x90000))
+    rc = _call(lib, "moe_forward", good_dims(wfmt=1, n_shared=0), x, w, out, ids, g)
+    assert rc in (B.MOE_ERR_ARG, B.MOE_ERR_UNSUPPORTED)
+    assert _call(lib, "moe_forward", d, x, _weights(w_gate_up=_Fake(0x90004)), out, ids, g) == B.MOE_ERR_ALIGN
