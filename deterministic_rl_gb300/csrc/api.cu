@@ -278,6 +278,21 @@ bool take_stall_test() {
     return false;
 }
 
+// Test hook for failure detection in the backward: MOE_TEST_STALL_BWD_CALLS=N
+// makes the dWg/dWu weight-gradient GEMM of the next N backward calls
+// (process-wide) issue no loads, so its MMA wait runs out (bounded, 1 s) and
+// moe_get_status reports MOE_ERR_TIMEOUT.  Unset in normal use.
+bool take_stall_test_bwd() {
+    static std::atomic<int> left{[] {
+        const char* e = std::getenv("MOE_TEST_STALL_BWD_CALLS");
+        return e ? std::atoi(e) : 0;
+    }()};
+    int v = left.load();
+    while (v > 0)
+        if (left.compare_exchange_weak(v, v - 1)) return true;
+    return false;
+}
+
 // A second stream (and its fork/join events) per device and host thread, for
 // work that overlaps the caller's stream inside one call; created on first use
 // and kept for the life of the process.  Work on it is ordered against the
@@ -899,6 +914,7 @@ moe_status train_impl(TrainMode mode, const moe_dims* d, const void* x, const mo
         p.gstride = int64_t(F) * D;
         p.status = status;
         p.timeout_ns = kWaitTimeoutNs;
+        p.stall_test = take_stall_test_bwd() ? 1 : 0;
         MOE_TRY(mark_b(MOE_BWD_STAGE_WGRAD_GATE_UP, 0, s));
         MOE_TRY(wlaunch(p));
         MOE_TRY(mark_b(MOE_BWD_STAGE_WGRAD_GATE_UP, 1, s));

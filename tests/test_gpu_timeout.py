@@ -59,3 +59,46 @@ def test_wait_that_runs_out_reports_timeout_and_context_survives(tmp_path, T):
     ref = MoELayer.from_inputs(inp, out_fp32=True).forward(inp.x)
     for a, b in zip(out, ref):
         assert torch.equal(a, b.cpu())
+
+
+_BWD_SCRIPT = r"""
+import sys, time, torch
+sys.path.insert(0, {root!r})
+from deterministic_rl_gb300 import MoELayer
+from deterministic_rl_gb300.synthetic import CONFIGS, make_layer, make_dout, make_replay_ids
+cfg = CONFIGS["c1_tiny"].with_(name="stall_bwd", seed=6, T=300, n_shared=1)
+inp = make_layer(cfg, "cuda")
+layer = MoELayer.from_inputs(inp)
+ids = make_replay_ids(cfg, device="cuda")
+dout = make_dout(cfg, device="cuda")
+t0 = time.time()
+layer.backward(inp.x, ids, dout)
+first = layer.backward_status()
+dt = time.time() - t0
+dx, g = layer.backward(inp.x, ids, dout)
+second = layer.backward_status()
+torch.save([first, second, dt, dx.cpu()] + [g[k].cpu() for k in sorted(g)], {path!r})
+"""
+
+
+def test_backward_wait_that_runs_out_reports_timeout_and_context_survives(tmp_path):
+    """MOE_TEST_STALL_BWD_CALLS=1: the weight-gradient GEMM of the first backward
+    issues no loads; its waits run out, the call reports MOE_ERR_TIMEOUT, and the
+    next backward in the same process succeeds and matches a clean run bitwise."""
+    from deterministic_rl_gb300.synthetic import make_dout, make_replay_ids
+    path = str(tmp_path / "b.pt")
+    env = dict(os.environ, MOE_TEST_STALL_BWD_CALLS="1")
+    subprocess.run([sys.executable, "-c", _BWD_SCRIPT.format(root=ROOT, path=path)], env=env,
+                   check=True, timeout=300)
+    first, second, dt, dx, *grads = torch.load(path)
+    assert first == B.MOE_ERR_TIMEOUT
+    assert second == B.MOE_OK
+    assert dt < 30
+    cfg = CONFIGS["c1_tiny"].with_(name="stall_bwd", seed=6, T=300, n_shared=1)
+    inp = make_layer(cfg, "cuda")
+    layer = MoELayer.from_inputs(inp)
+    rdx, rg = layer.backward(inp.x, make_replay_ids(cfg, device="cuda"), make_dout(cfg, device="cuda"))
+    torch.cuda.synchronize()
+    assert torch.equal(dx, rdx.cpu())
+    for a, k in zip(grads, sorted(rg)):
+        assert torch.equal(a, rg[k].cpu()), k
