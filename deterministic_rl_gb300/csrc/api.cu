@@ -414,17 +414,17 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
         MOE_TRY(cu(launch_nvfp4_qdq(static_cast<const uint16_t*>(x),
                                     reinterpret_cast<uint16_t*>(ws + L.xq), nullptr,
                                     reinterpret_cast<float*>(ws + L.sx), T, d->d, sms, s)));
-        MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(ws + L.xq), perm, T, k, d->d, S,
+        MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(ws + L.xq), inv, T, k, d->d, S,
                                  reinterpret_cast<uint16_t*>(ws + L.xp), s,
                                  reinterpret_cast<const float*>(ws + L.sx), sxp)));
     } else if (mxa) {
         // MXFP8 activations: each token row quantised once along d, then gathered
         MOE_TRY(cu(launch_mx_rows(static_cast<const uint16_t*>(x),
                                   reinterpret_cast<uint16_t*>(ws + L.xq), T, d->d, sms, s)));
-        MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(ws + L.xq), perm, T, k, d->d,
+        MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(ws + L.xq), inv, T, k, d->d,
                                  Sg, reinterpret_cast<uint16_t*>(ws + L.xp), s)));
     } else {
-        MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), perm, T, k, d->d, Sg,
+        MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), inv, T, k, d->d, Sg,
                                  reinterpret_cast<uint16_t*>(ws + L.xp), s)));
     }
     MOE_TRY(mark(MOE_STAGE_GATHER, 1, s));
@@ -696,7 +696,7 @@ moe_status train_impl(TrainMode mode, const moe_dims* d, const void* x, const mo
     MOE_TRY(cu(launch_dispatch(ids_used, T, k, E, cnt, off, perm, inv,
                                reinterpret_cast<int32_t*>(wsb + L.f.scratch), s)));
     MOE_TRY(cu(launch_seg_offsets(cnt, E, G, S ? static_cast<int>(T) : 0, poff, s)));
-    MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), perm, T, k, D, S,
+    MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), inv, T, k, D, S,
                              reinterpret_cast<uint16_t*>(wsb + L.f.xp), s)));
     MOE_TRY(mark_b(MOE_BWD_STAGE_DISPATCH, 1, s));
     }

@@ -188,18 +188,31 @@ __global__ void __launch_bounds__(32 * kSegWarps) dispatch_small_kernel(
     }
 }
 
-// Gather: xp[r] = x[perm[r] / k] for r < T*k, then xp[T*k + t] = x[t] for
-// the shared expert.  16-byte vectors; d % 8 == 0.
-__global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
-                                   int64_t n_pairs, int k, int vec_per_row, int64_t rows_total,
-                                   uint4* __restrict__ xp, const float* __restrict__ scale_in,
-                                   float* __restrict__ scale_out) {
-    for (int64_t r = blockIdx.x; r < rows_total; r += gridDim.x) {
-        const int64_t src = r < n_pairs ? perm[r] / k : r - n_pairs;
-        const uint4* s = x + src * vec_per_row;
-        uint4* dptr = xp + r * vec_per_row;
-        for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dptr[v] = s[v];
-        if (scale_out && threadIdx.x == 0) scale_out[r] = scale_in[src];
+// Gather, in token order: token t's row of x is read once and stored to
+// xp[inv[t*k + s]] for s = 0 .. k-1 (its rows in expert order) and, for the
+// shared expert, to xp[T*k + t].  16-byte vectors; d % 8 == 0.  scale_out
+// (NVFP4) receives the token's scale at the same rows.
+constexpr int kGatherMaxK = 16;
+
+__global__ void __launch_bounds__(256) gather_rows_kernel(
+    const uint4* __restrict__ x, const int32_t* __restrict__ inv, int64_t T, int k,
+    int vec_per_row, int n_shared, uint4* __restrict__ xp, const float* __restrict__ scale_in,
+    float* __restrict__ scale_out) {
+    __shared__ int64_t dst[kGatherMaxK + 1];
+    const int64_t Tk = T * k;
+    const int nd = k + (n_shared ? 1 : 0);
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        if (threadIdx.x < nd)
+            dst[threadIdx.x] = threadIdx.x < k ? static_cast<int64_t>(inv[t * k + threadIdx.x])
+                                               : Tk + t;
+        __syncthreads();
+        const uint4* src = x + t * vec_per_row;
+        for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) {
+            const uint4 val = src[v];
+            for (int j = 0; j < nd; ++j) xp[dst[j] * vec_per_row + v] = val;
+        }
+        if (scale_out && threadIdx.x < nd) scale_out[dst[threadIdx.x]] = scale_in[t];
+        __syncthreads();
     }
 }
 
@@ -232,16 +245,15 @@ cudaError_t launch_dispatch(const int32_t* ids, int64_t T, int k, int E, int32_t
     return cudaGetLastError();
 }
 
-cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int64_t T, int k, int d,
+cudaError_t launch_gather(const uint16_t* x, const int32_t* inv, int64_t T, int k, int d,
                           int n_shared, uint16_t* xp, cudaStream_t s, const float* scale_in,
                           float* scale_out) {
-    const int64_t n_pairs = T * k;
-    const int64_t rows = n_pairs + (n_shared ? T : 0);
-    if (rows == 0) return cudaSuccess;
+    if (k > kGatherMaxK || d % 8) return cudaErrorInvalidValue;
+    if (T == 0) return cudaSuccess;
     const int vpr = d / 8;
-    const int64_t grid = rows < 148 * 16 ? rows : 148 * 16;
+    const int64_t grid = T < 148 * 16 ? T : 148 * 16;
     gather_rows_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(
-        reinterpret_cast<const uint4*>(x), perm, n_pairs, k, vpr, rows, reinterpret_cast<uint4*>(xp),
+        reinterpret_cast<const uint4*>(x), inv, T, k, vpr, n_shared, reinterpret_cast<uint4*>(xp),
         scale_in, scale_out);
     return cudaGetLastError();
 }

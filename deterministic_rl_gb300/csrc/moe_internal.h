@@ -130,8 +130,10 @@ size_t dispatch_scratch_bytes(int64_t n_pairs, int E);
 cudaError_t launch_dispatch(const int32_t* ids, int64_t T, int k, int E, int32_t* cnt,
                             int32_t* off, int32_t* perm, int32_t* inv, int32_t* scratch,
                             cudaStream_t s);
-// scale_in/scale_out (NVFP4): also copy each gathered row's fp32 scale.
-cudaError_t launch_gather(const uint16_t* x, const int32_t* perm, int64_t T, int k, int d,
+// Rows in expert order: xp[inv[t*k + s]] = x[t], and xp[T*k + t] = x[t] for
+// the shared expert (n_shared).  scale_in/scale_out (NVFP4): also copy each
+// token's fp32 scale to its rows.
+cudaError_t launch_gather(const uint16_t* x, const int32_t* inv, int64_t T, int k, int d,
                           int n_shared, uint16_t* xp, cudaStream_t s,
                           const float* scale_in = nullptr, float* scale_out = nullptr);
 
