@@ -53,12 +53,18 @@ __global__ void __launch_bounds__(kMaxE) seg_scan_kernel(int32_t* __restrict__ h
     __shared__ int32_t warp_sums[kMaxE / 32];
     const int e = threadIdx.x;
     int32_t run = 0;
+    // nseg * kSegWarps entries per expert, a multiple of kSegWarps: eight loads
+    // are issued before their eight stores, the running sum kept in order
     if (e < E) {
-        for (int sw = 0; sw < nseg * kSegWarps; ++sw) {
-            int32_t* p = hist + static_cast<int64_t>(sw) * E + e;
-            const int32_t c = *p;
-            *p = run;
-            run += c;
+        for (int sw0 = 0; sw0 < nseg * kSegWarps; sw0 += kSegWarps) {
+            int32_t c[kSegWarps];
+#pragma unroll
+            for (int u = 0; u < kSegWarps; ++u) c[u] = hist[static_cast<int64_t>(sw0 + u) * E + e];
+#pragma unroll
+            for (int u = 0; u < kSegWarps; ++u) {
+                hist[static_cast<int64_t>(sw0 + u) * E + e] = run;
+                run += c[u];
+            }
         }
     }
     tot[e] = e < E ? run : 0;
@@ -80,7 +86,13 @@ __global__ void __launch_bounds__(kMaxE) seg_scan_kernel(int32_t* __restrict__ h
         cnt[e] = tot[e];
         off[e] = excl;
         if (e == E - 1) off[E] = excl + tot[e];
-        for (int sw = 0; sw < nseg * kSegWarps; ++sw) hist[static_cast<int64_t>(sw) * E + e] += excl;
+        for (int sw0 = 0; sw0 < nseg * kSegWarps; sw0 += kSegWarps) {
+            int32_t c[kSegWarps];
+#pragma unroll
+            for (int u = 0; u < kSegWarps; ++u) c[u] = hist[static_cast<int64_t>(sw0 + u) * E + e];
+#pragma unroll
+            for (int u = 0; u < kSegWarps; ++u) hist[static_cast<int64_t>(sw0 + u) * E + e] = c[u] + excl;
+        }
     }
 }
 
