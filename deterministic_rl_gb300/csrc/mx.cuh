@@ -33,27 +33,24 @@ __device__ __forceinline__ float exp2i(int n) {
                      : __uint_as_float(0x00400000u);
 }
 
-// e4m3(v * 2^-X) * 2^X, with inv = 2^-X and scale = 2^X.
-__device__ __forceinline__ float mx_qdq(float v, float inv, float scale) {
-    const __nv_fp8_storage_t q = __nv_cvt_float_to_fp8(v * inv, __NV_SATFINITE, __NV_E4M3);
-    return __half2float(__half(__nv_cvt_fp8_to_halfraw(q, __NV_E4M3))) * scale;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+// e4m3(v * 2^-X) * 2^X for two values, with inv = 2^-X and scale = 2^X,
+// packed as bf16x2 (a in the low half): one paired conversion to E4M3 and one
+// back to f16 (both exact per element), then the power-of-two rescale.
+__device__ __forceinline__ uint32_t mx_qdq2(float a, float b, float inv, float scale) {
+    const __nv_fp8x2_storage_t q =
+        __nv_cvt_float2_to_fp8x2(make_float2(a * inv, b * inv), __NV_SATFINITE, __NV_E4M3);
+    const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(q, __NV_E4M3)));
+    const __nv_bfloat162 r = __floats2bfloat162_rn(f.x * scale, f.y * scale);
+    return static_cast<uint32_t>(__bfloat16_as_ushort(r.x)) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(r.y)) << 16);
 }
 
 // Quantise 8 values with block exponent X and pack them as 8 bf16.
 __device__ __forceinline__ uint4 mx_qdq8(const float (&v)[8], int X) {
     const float inv = exp2i(-X), sc = exp2i(X);
-    float q[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = mx_qdq(v[i], inv, sc);
-    return make_uint4(pack_bf16x2(q[0], q[1]), pack_bf16x2(q[2], q[3]), pack_bf16x2(q[4], q[5]),
-                      pack_bf16x2(q[6], q[7]));
+    return make_uint4(mx_qdq2(v[0], v[1], inv, sc), mx_qdq2(v[2], v[3], inv, sc),
+                      mx_qdq2(v[4], v[5], inv, sc), mx_qdq2(v[6], v[7], inv, sc));
 }
-
 
 __device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8]) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};
