@@ -29,6 +29,7 @@ namespace {
 
 // 8 consecutive values of a row, as fp32.
 struct SrcBf16 {
+    static constexpr bool kUnitScale = true;  // every row's factor is 1
     const uint16_t* p;
     int64_t ld;
     // transposed quantiser: 8 bf16 of a row as stored, and the row's factor
@@ -50,9 +51,8 @@ struct SrcDy {
     int k;
     int64_t Tk;
     int64_t ld;
-    // transposed quantiser: 8 bf16 of dout[t] as stored, and the row's factor
-    __device__ __forceinline__ uint4 raw8(int64_t row, int c, float& scale) const {
-        int64_t t;
+    // the token t whose dout feeds row `row`, and the row's factor
+    __device__ __forceinline__ void row_of(int64_t row, int64_t& t, float& scale) const {
         if (row < Tk) {
             const int32_t pair = perm[row];
             t = pair / k;
@@ -61,6 +61,9 @@ struct SrcDy {
             t = row - Tk;
             scale = valid[t] ? 1.0f : 0.0f;
         }
+    }
+    // 8 bf16 of dout[t] as stored, from column c
+    __device__ __forceinline__ uint4 load8(int64_t t, int c) const {
         return *reinterpret_cast<const uint4*>(dout + t * ld + c);
     }
 };
@@ -143,14 +146,14 @@ __device__ __forceinline__ void tq_store16(uint16_t* out, int64_t at, const floa
     o[1] = mx_qdq8(v1, X);
 }
 
-// bf16-valued rows (times a per-row factor): the tile holds the stored bf16 of
+// bf16 rows as stored (sources whose row factor is 1): the tile holds the bf16 of
 // rows 2R and 2R + 1 of a column in one 32-bit word, tp[R][column ^ sw(R)],
 // sw(R) = 8 * ((R / 8) % 4).  Loading: thread t reads rows 2 (t / 8) and
 // 2 (t / 8) + 1, columns 8 (t % 8) .. + 7 (two 16-byte loads).
 template <class Src, bool SEG>
 __global__ void __launch_bounds__(256, 8) tq16_kernel(Src src, TqArgs a) {
+    static_assert(Src::kUnitScale, "the row factor is not applied");
     __shared__ __align__(16) uint32_t tp[kTqRows / 2][64];
-    __shared__ float rs[kTqRows];
     const int tid = threadIdx.x;
     const int cchunks = a.C / 64;
     const int64_t items = a.ntiles * cchunks;
@@ -165,10 +168,6 @@ __global__ void __launch_bounds__(256, 8) tq16_kernel(Src src, TqArgs a) {
             float s0 = 0.0f, s1 = 0.0f;
             if (2 * R < blk.nvalid) lo = src.raw8(blk.in_row0 + 2 * R, cb + c8, s0);
             if (2 * R + 1 < blk.nvalid) hi = src.raw8(blk.in_row0 + 2 * R + 1, cb + c8, s1);
-            if ((tid & 7) == 0) {
-                rs[2 * R] = s0;
-                rs[2 * R + 1] = s1;
-            }
             const uint32_t l[4] = {lo.x, lo.y, lo.z, lo.w}, h[4] = {hi.x, hi.y, hi.z, hi.w};
             uint32_t w[8];
 #pragma unroll
@@ -187,8 +186,8 @@ __global__ void __launch_bounds__(256, 8) tq16_kernel(Src src, TqArgs a) {
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const uint32_t w = tp[part * 8 + j][c ^ (part << 3)];
-                v[2 * j] = __uint_as_float(w << 16) * rs[part * 16 + 2 * j];
-                v[2 * j + 1] = __uint_as_float(w & 0xFFFF0000u) * rs[part * 16 + 2 * j + 1];
+                v[2 * j] = __uint_as_float(w << 16);
+                v[2 * j + 1] = __uint_as_float(w & 0xFFFF0000u);
             }
             float m = 0.0f;
 #pragma unroll
@@ -244,43 +243,61 @@ __device__ __forceinline__ void col_q16(const float (*tf)[64], int c, int part, 
 
 // dY = gate * dout in expert order: Q_d(dY) rows [rows][d] for the dH GEMM and
 // the token-major Q_tok(dY) [d][kpad] for the dWd GEMM, from one read of dout.
+// Each thread keeps one row of the tile (r = t / 4, 16 columns); which token
+// feeds its row in the CTA's next tile, and the row's factor, are looked up
+// while the current tile is quantised, so that only the dout load remains on
+// the path of each tile.
 __global__ void __launch_bounds__(256) dy_dual_kernel(SrcDy src, TqArgs a,
                                                       uint16_t* __restrict__ dyq, int d) {
     __shared__ __align__(16) float tf[kTqRows][64];
     const int tid = threadIdx.x;
+    const int r = tid >> 2, c16 = (tid & 3) * 16;
     const int cchunks = a.C / 64;
     const int64_t items = a.ntiles * cchunks;
-    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
-        const int64_t rt = it / cchunks;
+    // the tiles past the last group come last: the first invalid tile ends
+    // the CTA's work (uniform across the CTA)
+    int64_t it = blockIdx.x;
+    TqBlock blk;
+    if (it >= items || !tq_tile<true>(a, it / cchunks, blk)) return;
+    bool ok = r < blk.nvalid;
+    int64_t t = 0;
+    float w = 0.0f;
+    if (ok) src.row_of(blk.in_row0 + r, t, w);
+    for (;;) {
         const int cb = static_cast<int>(it % cchunks) * 64;
-        TqBlock blk;
-        if (!tq_tile<true>(a, rt, blk)) continue;  // uniform across the CTA
-        {
-            const int r = tid >> 2, c16 = (tid & 3) * 16;
-            const bool ok = r < blk.nvalid;
-            float v[16];
-            if (ok) {
-                float w;
-                float lo[8], hi[8];
-                unpack8(src.raw8(blk.in_row0 + r, cb + c16, w), lo);
-                unpack8(src.raw8(blk.in_row0 + r, cb + c16 + 8, w), hi);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    v[i] = w * lo[i];
-                    v[8 + i] = w * hi[i];
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = 0.0f;
-            }
-            row_q16(v, ok, dyq + (blk.in_row0 + r) * d + cb + c16);
-            tf_put16(tf, r, c16, v);
+        uint4 u0 = make_uint4(0, 0, 0, 0), u1 = u0;
+        if (ok) {
+            u0 = src.load8(t, cb + c16);
+            u1 = src.load8(t, cb + c16 + 8);
         }
+        const TqBlock cur = blk;
+        const bool cur_ok = ok;
+        const float cw = w;
+        it += gridDim.x;
+        const bool more = it < items && tq_tile<true>(a, it / cchunks, blk);
+        if (more) {
+            ok = r < blk.nvalid;
+            if (ok) src.row_of(blk.in_row0 + r, t, w);
+        }
+        float v[16];
+        {
+            float lo[8], hi[8];
+            unpack8(u0, lo);
+            unpack8(u1, hi);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                v[i] = cw * lo[i];
+                v[8 + i] = cw * hi[i];
+            }
+        }
+        row_q16(v, cur_ok, dyq + (cur.in_row0 + r) * d + cb + c16);
+        tf_put16(tf, r, c16, v);
         __syncthreads();
         {
             const int c = tid >> 2, part = tid & 3;
-            col_q16(tf, c, part, a.out + static_cast<int64_t>(cb + c) * a.ld + blk.out_col + part * 16);
+            col_q16(tf, c, part, a.out + static_cast<int64_t>(cb + c) * a.ld + cur.out_col + part * 16);
         }
+        if (!more) break;
         __syncthreads();
     }
 }
