@@ -385,88 +385,84 @@ __global__ void seg_offsets_kernel(const int32_t* __restrict__ cnt, int E, int G
 
 // ---- gate and router backward -------------------------------------------------------
 
-constexpr int kGateThreads = 256;
+constexpr int kGateWarps = 8;  // tokens in flight per CTA, one warp each
 constexpr int kMaxSlots = 8;
 
-// One CTA per token t:
+// One warp per token t:
 //   dg_s = dout[t] . Y[inv[t k + s]]                          (the gate gradient)
 //   dl_s = w_s (dg_s - sum_s' w_s' dg_s')                    (softmax over the chosen)
 //   dx[t] = sum_s dl_s Wr[ids[t, s]]   (the router's part of dx; s ascending)
-// All sums in a fixed order: per thread over its columns ascending, then a
-// fixed shuffle tree, then the warps in order.
-__global__ void __launch_bounds__(kGateThreads) gate_bwd_kernel(
+// All sums in a fixed order: per lane over its columns ascending (lane l takes
+// columns 8l .. 8l + 7 of every 256), then a butterfly over the lanes, which
+// leaves every lane the same total (each step adds the same two values).
+__global__ void __launch_bounds__(32 * kGateWarps) gate_bwd_kernel(
     const uint16_t* __restrict__ dout, const uint16_t* __restrict__ Y,
     const int32_t* __restrict__ inv, const int32_t* __restrict__ ids,
     const float* __restrict__ gates, const int32_t* __restrict__ valid,
     const uint16_t* __restrict__ wr, float* __restrict__ dg_out, float* __restrict__ dl_out,
     float* __restrict__ dx, int64_t T, int k, int d) {
-    __shared__ float part[kGateThreads / 32][kMaxSlots];
-    __shared__ float dl_s[kMaxSlots];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = static_cast<int64_t>(gridDim.x) * kGateWarps;
+    for (int64_t t = static_cast<int64_t>(blockIdx.x) * kGateWarps + (threadIdx.x >> 5); t < T;
+         t += nwarps) {
         float acc[kMaxSlots];
-        int64_t row[kMaxSlots];
+        int32_t row[kMaxSlots];
 #pragma unroll
         for (int s = 0; s < kMaxSlots; ++s) {
             acc[s] = 0.0f;
             row[s] = s < k ? inv[t * k + s] : 0;
         }
-        for (int c = tid * 8; c < d; c += kGateThreads * 8) {
+        for (int c = lane * 8; c < d; c += 256) {
             float g[8];
             unpack8(*reinterpret_cast<const uint4*>(dout + t * d + c), g);
 #pragma unroll
             for (int s = 0; s < kMaxSlots; ++s) {
                 if (s >= k) break;
                 float y[8];
-                unpack8(*reinterpret_cast<const uint4*>(Y + row[s] * d + c), y);
+                unpack8(*reinterpret_cast<const uint4*>(Y + static_cast<int64_t>(row[s]) * d + c), y);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) acc[s] = fmaf(g[i], y[i], acc[s]);
             }
         }
 #pragma unroll
-        for (int s = 0; s < kMaxSlots; ++s) {
-            float v = acc[s];
+        for (int s = 0; s < kMaxSlots; ++s)
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            if (lane == 0) part[warp][s] = v;
+            for (int o = 16; o > 0; o >>= 1) acc[s] += __shfl_xor_sync(0xffffffffu, acc[s], o);
+        const bool ok = valid[t] != 0;
+        float w[kMaxSlots], dl[kMaxSlots];
+        float wdg = 0.0f;
+#pragma unroll
+        for (int s = 0; s < kMaxSlots; ++s) {
+            w[s] = s < k ? gates[t * k + s] : 0.0f;
+            if (s < k) wdg = fmaf(w[s], acc[s], wdg);
         }
-        __syncthreads();
-        if (tid == 0) {
-            float dg[kMaxSlots], w[kMaxSlots];
-            float wdg = 0.0f;
-            for (int s = 0; s < k; ++s) {
-                float v = 0.0f;
-                for (int q = 0; q < kGateThreads / 32; ++q) v += part[q][s];
-                dg[s] = v;
-                w[s] = gates[t * k + s];
-                wdg = fmaf(w[s], v, wdg);
-            }
-            const bool ok = valid[t] != 0;
-            for (int s = 0; s < k; ++s) {
-                const float l = ok ? w[s] * (dg[s] - wdg) : 0.0f;
-                dl_s[s] = l;
-                dg_out[t * k + s] = ok ? dg[s] : 0.0f;
-                dl_out[t * k + s] = l;
+#pragma unroll
+        for (int s = 0; s < kMaxSlots; ++s) {
+            dl[s] = s < k && ok ? w[s] * (acc[s] - wdg) : 0.0f;
+            if (s < k && lane == s) {
+                dg_out[t * k + s] = ok ? acc[s] : 0.0f;
+                dl_out[t * k + s] = dl[s];
             }
         }
-        __syncthreads();
-        for (int c = tid * 8; c < d; c += kGateThreads * 8) {
+        int32_t id[kMaxSlots];
+#pragma unroll
+        for (int s = 0; s < kMaxSlots; ++s) id[s] = s < k ? ids[t * k + s] : 0;
+        for (int c = lane * 8; c < d; c += 256) {
             float o[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) o[i] = 0.0f;
-            for (int s = 0; s < k; ++s) {
-                const float l = dl_s[s];
-                float w8[8];
-                unpack8(*reinterpret_cast<const uint4*>(wr + static_cast<int64_t>(ids[t * k + s]) * d + c),
-                        w8);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) o[i] = fmaf(l, w8[i], o[i]);
+            for (int s = 0; s < kMaxSlots; ++s) {
+                if (s >= k) break;
+                float w8[8];
+                unpack8(*reinterpret_cast<const uint4*>(wr + static_cast<int64_t>(id[s]) * d + c), w8);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) o[i] = fmaf(dl[s], w8[i], o[i]);
             }
             float* dst = dx + t * d + c;
             *reinterpret_cast<float4*>(dst) = make_float4(o[0], o[1], o[2], o[3]);
             *reinterpret_cast<float4*>(dst + 4) = make_float4(o[4], o[5], o[6], o[7]);
         }
-        __syncthreads();
     }
 }
 
@@ -646,9 +642,10 @@ cudaError_t launch_gate_bwd(const uint16_t* dout, const uint16_t* y, const int32
                             int d, int sms, cudaStream_t s) {
     if (k > kMaxSlots || d % 8) return cudaErrorInvalidValue;
     if (T == 0) return cudaSuccess;
-    const int64_t cap = static_cast<int64_t>(sms) * 8;
-    const int grid = static_cast<int>(T < cap ? T : cap);
-    gate_bwd_kernel<<<grid, kGateThreads, 0, s>>>(dout, y, inv, ids, gates, valid, wr, dg, dl, dx,
+    const int64_t cap = static_cast<int64_t>(sms) * 4;  // resident CTAs at 64 registers
+    const int64_t blocks = (T + kGateWarps - 1) / kGateWarps;
+    const int grid = static_cast<int>(blocks < cap ? blocks : cap);
+    gate_bwd_kernel<<<grid, 32 * kGateWarps, 0, s>>>(dout, y, inv, ids, gates, valid, wr, dg, dl, dx,
                                                   T, k, d);
     return cudaGetLastError();
 }
