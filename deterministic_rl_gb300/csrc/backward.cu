@@ -306,7 +306,7 @@ __global__ void __launch_bounds__(256) dy_dual_kernel(SrcDy src, TqArgs a,
 //   dA = dH * b * sigmoid(a) * (1 + a * (1 - sigmoid(a))),   dB = dH * silu(a),
 // quantised into [Q_F(dA) | Q_F(dB)] rows [rows][2F] for the dXp GEMM and the
 // token-major [Q_tok(dA) ; Q_tok(dB)] [2F][kpad] for the dWg / dWu GEMM.
-__global__ void __launch_bounds__(256) swiglu_dual_kernel(
+__global__ void __launch_bounds__(256, 4) swiglu_dual_kernel(
     const float* __restrict__ dh, const float* __restrict__ A, const float* __restrict__ Bv,
     TqArgs a, uint16_t* __restrict__ dabq, int F) {
     __shared__ __align__(16) float ta[kTqRows][64];
