@@ -602,7 +602,7 @@ BwdLayout make_bwd_layout(const moe_dims* d) {
     auto take = [&](size_t bytes) { const size_t at = o; o = align256(o + bytes); return at; };
     L.ids = take(T * k * 4);
     L.gates = take(T * k * 4);
-    L.poff = take((E + S + 1) * 4);
+    L.poff = take((E + S + 1) * 4 + kp / 64 * 4);  // + the tile -> group table
     L.a = take(rows * F * 4);
     L.b = take(rows * F * 4);
     L.dg = take(T * k * 4);
@@ -695,7 +695,7 @@ moe_status train_impl(TrainMode mode, const moe_dims* d, const void* x, const mo
     MOE_TRY(mark_b(MOE_BWD_STAGE_DISPATCH, 0, s));
     MOE_TRY(cu(launch_dispatch(ids_used, T, k, E, cnt, off, perm, inv,
                                reinterpret_cast<int32_t*>(wsb + L.f.scratch), s)));
-    MOE_TRY(cu(launch_seg_offsets(cnt, E, G, S ? static_cast<int>(T) : 0, poff, s)));
+    MOE_TRY(cu(launch_seg_offsets(cnt, E, G, S ? static_cast<int>(T) : 0, poff, L.kpad / 64, s)));
     MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), inv, T, k, D, S,
                              reinterpret_cast<uint16_t*>(wsb + L.f.xp), s)));
     MOE_TRY(mark_b(MOE_BWD_STAGE_DISPATCH, 1, s));

@@ -88,6 +88,7 @@ struct TqArgs {
     const int32_t* cnt;
     const int32_t* off;
     const int32_t* poff;
+    const int32_t* tile_g;  // group of each 64-row tile, -1 past the last
     int E, G;
     int64_t shared_row0;
     int shared_rows;
@@ -104,12 +105,8 @@ template <bool SEG>
 __device__ __forceinline__ bool tq_tile(const TqArgs& a, int64_t rt, TqBlock& blk) {
     if constexpr (SEG) {
         const int64_t p = rt * kTqRows;
-        if (p >= a.poff[a.G]) return false;
-        int lo = 0, hi = a.G;  // poff[lo] <= p < poff[lo + 1]
-        while (hi - lo > 1) {
-            const int mid = (lo + hi) >> 1;
-            if (a.poff[mid] <= p) lo = mid; else hi = mid;
-        }
+        const int lo = a.tile_g[rt];  // poff[lo] <= p < poff[lo + 1]
+        if (lo < 0) return false;
         const int local = static_cast<int>(p - a.poff[lo]);
         const int n = lo < a.E ? a.cnt[lo] : a.shared_rows;
         blk.in_row0 = (lo < a.E ? static_cast<int64_t>(a.off[lo]) : a.shared_row0) + local;
@@ -383,6 +380,25 @@ __global__ void seg_offsets_kernel(const int32_t* __restrict__ cnt, int E, int G
     if (lane == 31) poff[G] = incl;
 }
 
+// tile_g[rt] = the group g with poff[g] <= 64 rt < poff[g + 1], or -1.
+__global__ void seg_tiles_kernel(const int32_t* __restrict__ poff, int G, int64_t ntiles,
+                                 int32_t* __restrict__ tile_g) {
+    for (int64_t rt = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; rt < ntiles;
+         rt += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t p = rt * kTqRows;
+        int g = -1;
+        if (p < poff[G]) {
+            int lo = 0, hi = G;
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (poff[mid] <= p) lo = mid; else hi = mid;
+            }
+            g = lo;
+        }
+        tile_g[rt] = g;
+    }
+}
+
 // ---- gate and router backward -------------------------------------------------------
 
 constexpr int kGateWarps = 8;  // tokens in flight per CTA, one warp each
@@ -549,8 +565,11 @@ inline int grid_for(int64_t items, int per_block, int sms, int per_sm = 8) {
 }  // namespace
 
 cudaError_t launch_seg_offsets(const int32_t* cnt, int E, int G, int shared_rows, int32_t* poff,
-                               cudaStream_t s) {
+                               int64_t ntiles, cudaStream_t s) {
     seg_offsets_kernel<<<1, 32, 0, s>>>(cnt, E, G, shared_rows, poff);
+    if (ntiles > 0)
+        seg_tiles_kernel<<<static_cast<unsigned>((ntiles + 255) / 256), 256, 0, s>>>(poff, G, ntiles,
+                                                                                   poff + G + 1);
     return cudaGetLastError();
 }
 
@@ -576,6 +595,7 @@ TqArgs seg_args(int C, const int32_t* cnt, const int32_t* off, const int32_t* po
     a.cnt = cnt;
     a.off = off;
     a.poff = poff;
+    a.tile_g = poff + G + 1;
     a.E = E;
     a.G = G;
     a.shared_row0 = shared_row0;

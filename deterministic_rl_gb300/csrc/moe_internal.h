@@ -173,9 +173,10 @@ int wgrad_tile_n();    // B rows per tile (both CTAs)
 int wgrad_box_rows();  // rows of the a and b maps' boxes (one CTA's half)
 
 // Padded segment offsets of the G = E (+1 shared) groups: poff[g + 1] =
-// poff[g] + round_up(n_g, 64).
+// poff[g] + round_up(n_g, 64); then, at poff + G + 1, the group of each of the
+// ntiles 64-row tiles (-1 past poff[G]).
 cudaError_t launch_seg_offsets(const int32_t* cnt, int E, int G, int shared_rows, int32_t* poff,
-                               cudaStream_t s);
+                               int64_t ntiles, cudaStream_t s);
 // Transposed MXFP8 quantisation (blocks of 32 along the input's rows).
 struct SegDyArgs {
     const uint16_t* dout;

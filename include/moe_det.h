@@ -364,7 +364,8 @@ size_t moe_backward_workspace_size(const moe_dims *dims);
 /* Offsets (bytes into the backward workspace) of its regions; the first ones
  * are those of the forward workspace (moe_ws_layout), so moe_get_status reads
  * a backward workspace too.  Regions after a call: ids/gates the routing
- * used, poff [E+S+1] int32 padded token offsets per expert, a/b [rows][F]
+ * used, poff [E+S+1] int32 padded token offsets per expert (followed by
+ * [kpad/64] int32: the group of each 64-row tile, -1 past the last), a/b [rows][F]
  * fp32 gate/up pre-activations, dg/dl [T][k] fp32 gate and logit gradients,
  * dyq [rows][d], dh [rows][F] fp32, dabq [rows][2F] (quantised dA | dB),
  * dxp [rows][d] fp32, and the token-major operands xpt, dyt [d][kpad],
