@@ -556,12 +556,13 @@ def backward_launches(cfg, train=False):
     """Our kernels per backward step: weight copies (3, +3 for the shared
     expert); router GEMM, top-k; dispatch (1 or 3); padded offsets and the
     tile -> group table; gather; gate/up and down (recomputed, or the training
-    forward's); gate backward; router weight gradient; dY quantiser; dH;
-    SwiGLU backward; dXp; dx; token-major Xp and H; two weight-gradient GEMMs."""
+    forward's); gate backward; router weight gradient; dY quantised along d (token
+    order) and along tokens; dH; SwiGLU backward; dXp; dx; token-major Xp and H;
+    two weight-gradient GEMMs."""
     prep = 3 + 3 * cfg.n_shared
     disp = 1 if cfg.T * cfg.k <= DISPATCH_SEGMENT_PAIRS else 3
     # train: + the combine of the forward's output
-    return prep + 2 + disp + 2 + 1 + 2 + 2 + 1 + 1 + 1 + 1 + 1 + 2 + 2 + (1 if train else 0)
+    return prep + 2 + disp + 2 + 1 + 2 + 2 + 2 + 1 + 1 + 1 + 1 + 2 + 2 + (1 if train else 0)
 
 
 def _bwd_cfg(args):

@@ -805,7 +805,7 @@ moe_status train_impl(TrainMode mode, const moe_dims* d, const void* x, const mo
     uint16_t* dabt = reinterpret_cast<uint16_t*>(wsb + L.dabt);
     const int srows = S ? static_cast<int>(T) : 0;
     MOE_TRY(mark_b(MOE_BWD_STAGE_DY, 0, s));
-    const SegDyArgs dya{static_cast<const uint16_t*>(dout), gates, perm, valid, k, Tk};
+    const SegDyArgs dya{static_cast<const uint16_t*>(dout), gates, perm, valid, k, Tk, inv, T, S};
     MOE_TRY(cu(launch_dy_dual(dya, D, cnt, off, poff, E, G, srows, L.kpad, dyq, dyt, sms, s)));
     MOE_TRY(mark_b(MOE_BWD_STAGE_DY, 1, s));
     {

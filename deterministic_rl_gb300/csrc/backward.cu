@@ -44,6 +44,7 @@ struct SrcBf16 {
 // perm[r] = t*k + s and holds gate(t, s) * dout[t]; shared-expert row Tk + t
 // holds dout[t]; both zero for a token whose replayed ids were rejected.
 struct SrcDy {
+    static constexpr bool kUnitScale = false;
     const uint16_t* dout;
     const float* gates;
     const int32_t* perm;
@@ -65,6 +66,12 @@ struct SrcDy {
     // 8 bf16 of dout[t] as stored, from column c
     __device__ __forceinline__ uint4 load8(int64_t t, int c) const {
         return *reinterpret_cast<const uint4*>(dout + t * ld + c);
+    }
+    // transposed quantiser: 8 bf16 of the row's dout as stored, and its factor
+    __device__ __forceinline__ uint4 raw8(int64_t row, int c, float& scale) const {
+        int64_t t;
+        row_of(row, t, scale);
+        return load8(t, c);
     }
 };
 
@@ -143,14 +150,15 @@ __device__ __forceinline__ void tq_store16(uint16_t* out, int64_t at, const floa
     o[1] = mx_qdq8(v1, X);
 }
 
-// bf16 rows as stored (sources whose row factor is 1): the tile holds the bf16 of
+// bf16 rows as stored, times the row's factor where the source has one (the
+// product is taken in fp32 before quantising): the tile holds the bf16 of
 // rows 2R and 2R + 1 of a column in one 32-bit word, tp[R][column ^ sw(R)],
 // sw(R) = 8 * ((R / 8) % 4).  Loading: thread t reads rows 2 (t / 8) and
 // 2 (t / 8) + 1, columns 8 (t % 8) .. + 7 (two 16-byte loads).
 template <class Src, bool SEG>
 __global__ void __launch_bounds__(256, 8) tq16_kernel(Src src, TqArgs a) {
-    static_assert(Src::kUnitScale, "the row factor is not applied");
     __shared__ __align__(16) uint32_t tp[kTqRows / 2][64];
+    __shared__ float rs[Src::kUnitScale ? 1 : kTqRows];
     const int tid = threadIdx.x;
     const int cchunks = a.C / 64;
     const int64_t items = a.ntiles * cchunks;
@@ -165,6 +173,12 @@ __global__ void __launch_bounds__(256, 8) tq16_kernel(Src src, TqArgs a) {
             float s0 = 0.0f, s1 = 0.0f;
             if (2 * R < blk.nvalid) lo = src.raw8(blk.in_row0 + 2 * R, cb + c8, s0);
             if (2 * R + 1 < blk.nvalid) hi = src.raw8(blk.in_row0 + 2 * R + 1, cb + c8, s1);
+            if constexpr (!Src::kUnitScale) {
+                if ((tid & 7) == 0) {
+                    rs[2 * R] = s0;
+                    rs[2 * R + 1] = s1;
+                }
+            }
             const uint32_t l[4] = {lo.x, lo.y, lo.z, lo.w}, h[4] = {hi.x, hi.y, hi.z, hi.w};
             uint32_t w[8];
 #pragma unroll
@@ -185,6 +199,10 @@ __global__ void __launch_bounds__(256, 8) tq16_kernel(Src src, TqArgs a) {
                 const uint32_t w = tp[part * 8 + j][c ^ (part << 3)];
                 v[2 * j] = __uint_as_float(w << 16);
                 v[2 * j + 1] = __uint_as_float(w & 0xFFFF0000u);
+                if constexpr (!Src::kUnitScale) {
+                    v[2 * j] *= rs[part * 16 + 2 * j];
+                    v[2 * j + 1] *= rs[part * 16 + 2 * j + 1];
+                }
             }
             float m = 0.0f;
 #pragma unroll
@@ -238,63 +256,47 @@ __device__ __forceinline__ void col_q16(const float (*tf)[64], int c, int part, 
     tq_store16(dst, 0, v, mx_block_exp(m));
 }
 
-// dY = gate * dout in expert order: Q_d(dY) rows [rows][d] for the dH GEMM and
-// the token-major Q_tok(dY) [d][kpad] for the dWd GEMM, from one read of dout.
-// Each thread keeps one row of the tile (r = t / 4, 16 columns); which token
-// feeds its row in the CTA's next tile, and the row's factor, are looked up
-// while the current tile is quantised, so that only the dout load remains on
-// the path of each tile.
-__global__ void __launch_bounds__(256) dy_dual_kernel(SrcDy src, TqArgs a,
-                                                      uint16_t* __restrict__ dyq, int d) {
-    __shared__ __align__(16) float tf[kTqRows][64];
-    const int tid = threadIdx.x;
-    const int r = tid >> 2, c16 = (tid & 3) * 16;
-    const int cchunks = a.C / 64;
-    const int64_t items = a.ntiles * cchunks;
-    // the tiles past the last group come last: the first invalid tile ends
-    // the CTA's work (uniform across the CTA)
-    int64_t it = blockIdx.x;
-    TqBlock blk;
-    if (it >= items || !tq_tile<true>(a, it / cchunks, blk)) return;
-    bool ok = r < blk.nvalid;
-    int64_t t = 0;
-    float w = 0.0f;
-    if (ok) src.row_of(blk.in_row0 + r, t, w);
-    for (;;) {
-        const int cb = static_cast<int>(it % cchunks) * 64;
-        uint4 u0 = make_uint4(0, 0, 0, 0), u1 = u0;
-        if (ok) {
-            u0 = src.load8(t, cb + c16);
-            u1 = src.load8(t, cb + c16 + 8);
+// Q_d(dY), dY = gate * dout, in token order: each token's dout row is read
+// once and its k routed rows (gate(t, s) * dout[t], at dispatch position
+// inv[t k + s]) and its shared-expert row (dout[t], at Tk + t) are quantised
+// along d and stored; zero rows for a token whose replayed ids were rejected.
+// Thread i takes 8 columns; four neighbouring threads hold one block of 32.
+constexpr int kDyMaxRows = 9;  // k slots + the shared expert
+
+__global__ void __launch_bounds__(256) dy_rows_kernel(SrcDy src, const int32_t* __restrict__ inv,
+                                                      int64_t T, int n_shared, int d,
+                                                      uint16_t* __restrict__ dyq) {
+    __shared__ int64_t dst[kDyMaxRows];
+    __shared__ float sc[kDyMaxRows];
+    const int k = src.k;
+    const int nd = k + (n_shared ? 1 : 0);
+    for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+        if (threadIdx.x < nd) {
+            const int j = threadIdx.x;
+            const bool ok = src.valid[t] != 0;
+            dst[j] = j < k ? static_cast<int64_t>(inv[t * k + j]) : src.Tk + t;
+            sc[j] = !ok ? 0.0f : (j < k ? src.gates[t * k + j] : 1.0f);
         }
-        const TqBlock cur = blk;
-        const bool cur_ok = ok;
-        const float cw = w;
-        it += gridDim.x;
-        const bool more = it < items && tq_tile<true>(a, it / cchunks, blk);
-        if (more) {
-            ok = r < blk.nvalid;
-            if (ok) src.row_of(blk.in_row0 + r, t, w);
-        }
-        float v[16];
-        {
-            float lo[8], hi[8];
-            unpack8(u0, lo);
-            unpack8(u1, hi);
+        __syncthreads();
+        // d is a multiple of 256: a warp's 32 threads are all inside the row or
+        // all past it
+        for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+            float x[8];
+            unpack8(src.load8(t, c), x);
+            for (int j = 0; j < nd; ++j) {
+                const float w = sc[j];
+                float v[8];
+                float m = 0.0f;
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                v[i] = cw * lo[i];
-                v[8 + i] = cw * hi[i];
+                for (int i = 0; i < 8; ++i) {
+                    v[i] = w * x[i];
+                    m = fmaxf(m, fabsf(v[i]));
+                }
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+                m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
+                *reinterpret_cast<uint4*>(dyq + dst[j] * d + c) = mx_qdq8(v, mx_block_exp(m));
             }
         }
-        row_q16(v, cur_ok, dyq + (cur.in_row0 + r) * d + cb + c16);
-        tf_put16(tf, r, c16, v);
-        __syncthreads();
-        {
-            const int c = tid >> 2, part = tid & 3;
-            col_q16(tf, c, part, a.out + static_cast<int64_t>(cb + c) * a.ld + cur.out_col + part * 16);
-        }
-        if (!more) break;
         __syncthreads();
     }
 }
@@ -619,13 +621,18 @@ cudaError_t launch_tq_segments(const uint16_t* src, int64_t src_ld, int C, const
 cudaError_t launch_dy_dual(const SegDyArgs& dy, int d, const int32_t* cnt, const int32_t* off,
                            const int32_t* poff, int E, int G, int shared_rows, int64_t kpad,
                            uint16_t* dyq, uint16_t* dyt, int sms, cudaStream_t s) {
-    if (kpad % kTqRows || d % 64) return cudaErrorInvalidValue;
-    const TqArgs a = seg_args(d, cnt, off, poff, E, G, dy.Tk, shared_rows, kpad, dyt);
-    const int64_t items = a.ntiles * (d / 64);
-    if (items == 0) return cudaSuccess;
+    if (kpad % kTqRows || d % 256 || dy.k + (dy.n_shared ? 1 : 0) > kDyMaxRows)
+        return cudaErrorInvalidValue;
     const SrcDy src{dy.dout, dy.gates, dy.perm, dy.valid, dy.k, dy.Tk, d};
-    dy_dual_kernel<<<grid_for(items, 1, sms, 8), 256, 0, s>>>(src, a, dyq, d);
-    return cudaGetLastError();
+    if (dy.T > 0) {
+        const int64_t cap = static_cast<int64_t>(sms) * 8;
+        dy_rows_kernel<<<static_cast<unsigned>(dy.T < cap ? dy.T : cap), 256, 0, s>>>(
+            src, dy.inv, dy.T, dy.n_shared, d, dyq);
+    }
+    // Q_tok(dY): the same values, quantised along each expert's tokens
+    return tq_launch<SrcDy, true>(src, seg_args(d, cnt, off, poff, E, G, dy.Tk, shared_rows, kpad,
+                                                dyt),
+                                  sms, s);
 }
 
 cudaError_t launch_swiglu_dual(const float* dh, const float* a_pre, const float* b_pre, int F,

@@ -185,6 +185,9 @@ struct SegDyArgs {
     const int32_t* valid;
     int k;
     int64_t Tk;
+    const int32_t* inv;  // dispatch position of each (token, slot) pair
+    int64_t T;
+    int n_shared;
 };
 // Segment mode: out[c][poff[g] + i] = Q(row i of group g)[c] for bf16 rows
 // (src, row stride src_ld), groups padded with zeros to their poff extent;
