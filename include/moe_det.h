@@ -387,12 +387,12 @@ typedef enum {
     MOE_BWD_STAGE_GATE_UP = 3,        /* forward recompute: gate/up (H, pre-activations)*/
     MOE_BWD_STAGE_DOWN = 4,           /* forward recompute: routed expert outputs Y     */
     MOE_BWD_STAGE_GATE = 5,           /* gate/logit gradients, router part of dx, dWr   */
-    MOE_BWD_STAGE_DY = 6,             /* dY rows quantised along d                      */
+    MOE_BWD_STAGE_DY = 6,             /* dY quantised along d and along tokens          */
     MOE_BWD_STAGE_DH = 7,             /* dH = Q(dY) Q(Wd)                               */
     MOE_BWD_STAGE_SWIGLU = 8,         /* SwiGLU backward, [dA | dB] quantised along F   */
     MOE_BWD_STAGE_DXP = 9,            /* dXp = Q(dA) Q(Wg) + Q(dB) Q(Wu)                */
     MOE_BWD_STAGE_DX = 10,            /* fixed-order sum into dx                        */
-    MOE_BWD_STAGE_TRANSPOSE = 11,     /* token-major operands quantised along tokens    */
+    MOE_BWD_STAGE_TRANSPOSE = 11,     /* token-major Xp and H quantised along tokens    */
     MOE_BWD_STAGE_WGRAD_DOWN = 12,    /* dWd                                            */
     MOE_BWD_STAGE_WGRAD_GATE_UP = 13, /* dWg, dWu                                       */
     MOE_BWD_NUM_STAGES = 14
