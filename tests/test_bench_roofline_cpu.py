@@ -1,0 +1,79 @@
+"""The roofline arithmetic bench.py reports, against closed forms written out
+independently here.
+
+Layer FLOPs are T (2 d E + 6 d F (k + S)): the router GEMM plus the three
+expert projections of k routed slots and S shared experts. The bytes are the
+touched experts' weights read once plus the router, x, out and the ids/gates
+traffic. Expert weight bytes are 3 d F per value: 2 B in bf16, 1 + 1/32 in
+MXFP8 (E4M3 plus an E8M0 scale per 32). The kernel launch counts per call are
+those of the launch lists under profiles/."""
+import os
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+from deterministic_rl_gb300.synthetic import CONFIGS  # noqa: E402
+
+D, F, E, K = 7168, 2048, 384, 8
+
+
+def test_expert_weight_bytes():
+    bf16 = bench.weight_bytes_per_value(CONFIGS["c4_train_32k"]) * 3 * D * F
+    mx = bench.weight_bytes_per_value(CONFIGS["c5_mxfp8"]) * 3 * D * F
+    assert bf16 == 88_080_384                  # 3 * 7168 * 2048 * 2
+    assert mx == pytest.approx(45_416_448)     # 3 * 7168 * 2048 * (1 + 1/32)
+
+
+@pytest.mark.parametrize("name,T,S,tflop", [
+    # each workload's FLOPs to three or four significant digits
+    ("c2_decode_replay", 64, 1, 0.0511),
+    ("c3_prefill_zipf", 4096, 1, 3.27),
+    ("c4_train_32k", 32768, 1, 26.16),
+    ("c5_mxfp8", 16384, 0, 11.64),
+])
+def test_layer_flops(name, T, S, tflop):
+    router = 2 * D * E          # per token
+    experts = 3 * 2 * D * F     # per token and expert: gate, up, down
+    flops, _ = bench.layer_work(CONFIGS[name], E)
+    assert flops == T * (router + experts * (K + S))
+    assert flops == pytest.approx(tflop * 1e12, rel=2e-3)
+
+
+def test_layer_bytes_32k_all_touched():
+    cfg = CONFIGS["c4_train_32k"]
+    T = cfg.T
+    expected = (E + 1) * 3 * D * F * 2 + E * D * 2 + 2 * T * D * 2 + T * K * 12
+    _, nbytes = bench.layer_work(cfg, E)
+    assert nbytes == expected == 34_859_122_688
+
+
+def test_roofline_bound_switches_with_the_batch():
+    """At the measured peaks the decode layer is HBM-bound and the 32k layer
+    tensor-bound (ridge point ~290 FLOP per byte)."""
+    tensor, hbm = 1958.8e12, 6761.6e9
+    for name, bound in (("c2_decode_replay", "hbm"), ("c4_train_32k", "tensor")):
+        flops, nbytes = bench.layer_work(CONFIGS[name], E)
+        assert ("tensor" if flops / tensor > nbytes / hbm else "hbm") == bound
+
+
+@pytest.mark.parametrize("name,launches", [
+    ("c1_tiny", 7),            # one-kernel dispatch (<= 4096 pairs), one-SM GEMMs
+    ("c2_decode_replay", 7),
+    ("c3_prefill_zipf", 10),   # histogram, scan, scatter; shared gate/up on its own stream
+    ("c4_train_32k", 10),
+    ("c5_mxfp8", 9),           # no shared expert
+    ("c5_mxfp8_act", 11),      # + two activation quantisers
+    ("c6_nvfp4", 11),
+])
+def test_forward_launches_per_call(name, launches):
+    assert bench.launches_per_step(CONFIGS[name]) == launches
+
+
+def test_backward_launches_per_call():
+    cfg = CONFIGS["c4_train_32k"]
+    assert bench.backward_launches(cfg) == 28
+    assert bench.backward_launches(cfg, train=True) == 29
