@@ -18,6 +18,7 @@
 
 #include "moe_det.h"
 #include "moe_internal.h"
+#include "route_launch.h"
 
 using namespace moe;
 
@@ -41,7 +42,6 @@ struct Layout {
     size_t total;
 };
 
-inline int router_split(const moe_dims* d) { return (d->d / BK) % kRouterSplit == 0 ? kRouterSplit : 1; }
 
 bool dims_ok(const moe_dims* d) {
     if (!d) return false;
@@ -68,7 +68,7 @@ Layout make_layout(const moe_dims* d) {
     auto take = [&](size_t bytes) { const size_t at = o; o = align256(o + bytes); return at; };
     L.status = take(32);  // int32 [0..3] status words, [4..5] SM-pair GEMM tile counters
     L.logits = take(T * E * 4);
-    L.rpart = take(router_split(d) > 1 ? T * E * 4 * router_split(d) : 0);
+    L.rpart = take(route_split(d) > 1 ? T * E * 4 * route_split(d) : 0);
     L.valid = take(T * 4);
     L.cnt = take(E * 4);
     L.off = take((E + 1) * 4);
@@ -195,22 +195,23 @@ inline moe_status mark_b(int stage, int edge, cudaStream_t s) {
 
 }  // namespace
 
-namespace {
+namespace moe {
+
+int route_split(const moe_dims* d) { return (d->d / BK) % kRouterSplit == 0 ? kRouterSplit : 1; }
 
 // Router logits (fp32, + bias) and the routing decision for every token.
-moe_status run_route(const moe_dims* d, const void* x, const moe_weights* w, const int32_t* ids_in,
-                     int32_t* ids_out, float* gates_out, uint8_t* ws, const Layout& L,
-                     cudaStream_t s, bool filter = false, float tau = 0.0f) {
+moe_status launch_route(const moe_dims* d, const void* x, const moe_weights* w,
+                        const int32_t* ids_in, int32_t* ids_out, float* gates_out,
+                        const RouteScratch& sc, cudaStream_t s, bool filter, float tau) {
     const int64_t T = d->T;
-    int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
-    MOE_TRY(cu(cudaMemsetAsync(status, 0, 32, s)));
+    MOE_TRY(cu(cudaMemsetAsync(sc.status, 0, 32, s)));
     GemmParams p;
     std::memset(&p, 0, sizeof p);
     if (!make_map(&p.a0, w->w_router, d->d, d->E, BM)) return MOE_ERR_CUDA;
     if (!make_map(&p.b, x, d->d, T, BN)) return MOE_ERR_CUDA;
     if (!make_map(&p.b32, x, d->d, T, 32)) return MOE_ERR_CUDA;
     p.partial_b = 1;
-    const int split = router_split(d);
+    const int split = route_split(d);
     p.ksplit = split;
     p.split_stride = T * d->E;
     p.G = 1;
@@ -218,10 +219,10 @@ moe_status run_route(const moe_dims* d, const void* x, const moe_weights* w, con
     p.M = d->E;
     p.MT = (d->E + BM - 1) / BM;
     p.KB = d->d / BK;
-    p.out = ws + (split > 1 ? L.rpart : L.logits);
+    p.out = split > 1 ? sc.parts : sc.logits;
     p.ldo = d->E;
     p.bias = split > 1 ? nullptr : w->router_bias;
-    p.status = status;
+    p.status = sc.status;
     p.timeout_ns = kWaitTimeoutNs;
     const int64_t tiles = int64_t(p.MT) * ((T + BN - 1) / BN) * split;
     const int sms = num_sms();
@@ -233,17 +234,28 @@ moe_status run_route(const moe_dims* d, const void* x, const moe_weights* w, con
     MOE_TRY(mark(MOE_STAGE_TOPK, 0, s));
     const float log_tau = tau > 0.0f ? std::log(tau) : -INFINITY;
     if (split > 1 || filter)
-        MOE_TRY(cu(launch_topk_gates_split(reinterpret_cast<const float*>(ws + L.rpart), split,
-                                           T * d->E, split > 1 ? w->router_bias : nullptr,
-                                           reinterpret_cast<float*>(ws + L.logits), T, d->E, d->k,
-                                           ids_in, ids_out, gates_out,
-                                           reinterpret_cast<int32_t*>(ws + L.valid), status, s,
-                                           filter ? 1 : 0, log_tau)));
+        MOE_TRY(cu(launch_topk_gates_split(sc.parts, split, T * d->E,
+                                           split > 1 ? w->router_bias : nullptr, sc.logits, T,
+                                           d->E, d->k, ids_in, ids_out, gates_out, sc.valid,
+                                           sc.status, s, filter ? 1 : 0, log_tau)));
     else
-        MOE_TRY(cu(launch_topk_gates(reinterpret_cast<const float*>(ws + L.logits), T, d->E, d->k,
-                                     ids_in, ids_out, gates_out,
-                                     reinterpret_cast<int32_t*>(ws + L.valid), status, s)));
+        MOE_TRY(cu(launch_topk_gates(sc.logits, T, d->E, d->k, ids_in, ids_out, gates_out,
+                                     sc.valid, sc.status, s)));
     return mark(MOE_STAGE_TOPK, 1, s);
+}
+
+}  // namespace moe
+
+namespace {
+
+moe_status run_route(const moe_dims* d, const void* x, const moe_weights* w, const int32_t* ids_in,
+                     int32_t* ids_out, float* gates_out, uint8_t* ws, const Layout& L,
+                     cudaStream_t s, bool filter = false, float tau = 0.0f) {
+    const RouteScratch sc{reinterpret_cast<int32_t*>(ws + L.status),
+                          reinterpret_cast<float*>(ws + L.logits),
+                          reinterpret_cast<float*>(ws + L.rpart),
+                          reinterpret_cast<int32_t*>(ws + L.valid)};
+    return launch_route(d, x, w, ids_in, ids_out, gates_out, sc, s, filter, tau);
 }
 
 // Kernel family of the expert GEMMs: the one-SM kernel for batches of at most

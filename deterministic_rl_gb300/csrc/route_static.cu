@@ -1,23 +1,26 @@
 // route_static.cu -- moe_route_static: the routing call (router GEMM, top-k,
 // gate weights) with its scratch memory in a static device array instead of a
 // caller-provided workspace, for callers that cannot allocate device memory.
+// It runs the very launch sequence moe_route runs (launch_route: the same
+// router GEMM with the same fixed K split, the same top-k and gate kernels),
+// so its ids and gate weights equal moe_route's bit for bit.
 //
-// The scratch (status word, per-token flags, fp32 logits) lives in
-// g_route_scratch below: kStaticScratchBytes bytes that every GPU which loads
-// this library keeps until the process exits.  In host code the array's name
+// The scratch (status word, per-token flags, fp32 logits and the router's
+// partial logits) lives in g_route_scratch below: kStaticScratchBytes bytes
+// that every GPU which loads this library keeps until the process exits.
+// In host code the array's name
 // is only a host-side stand-in, so its device address is looked up with
 // cudaGetSymbolAddress once per device (the first call on that device, with
 // that device current) and passed to the kernels.  All calls share the array:
 // calls that overlap on the GPU (different streams, or different host
 // threads on one device) race on it.
-#include <cudaTypedefs.h>
-
 #include <cstdint>
 #include <cstring>
 #include <mutex>
 
 #include "moe_det.h"
 #include "moe_internal.h"
+#include "route_launch.h"
 
 using namespace moe;
 
@@ -25,7 +28,6 @@ namespace {
 
 constexpr size_t kStaticScratchBytes = size_t(4) << 20;  // 4 MiB
 constexpr int kMaxDevices = 64;
-constexpr uint64_t kTimeoutNs = 1000000000ull;
 
 static __device__ __align__(256) unsigned char g_route_scratch[kStaticScratchBytes];
 
@@ -48,27 +50,6 @@ moe_status scratch_address(unsigned char** out) {
     return MOE_OK;
 }
 
-bool encode_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows) {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q{};
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {K, rows};
-    const cuuint64_t strides[1] = {K * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
 }  // namespace
@@ -85,41 +66,19 @@ extern "C" moe_status moe_route_static(const moe_dims* dims, const void* x, cons
         !aligned16(ids_out) || !aligned16(gates_out))
         return MOE_ERR_ALIGN;
     const size_t T = static_cast<size_t>(dims->T), E = static_cast<size_t>(dims->E);
+    const size_t nparts = route_split(dims) > 1 ? static_cast<size_t>(route_split(dims)) : 0;
     const size_t off_valid = 256, off_logits = off_valid + round256(T * 4);
-    if (T > (size_t(1) << 20) || off_logits + T * E * 4 > kStaticScratchBytes) return MOE_ERR_WORKSPACE;
+    const size_t off_parts = off_logits + round256(T * E * 4);
+    if (T > (size_t(1) << 20) || off_parts + nparts * T * E * 4 > kStaticScratchBytes)
+        return MOE_ERR_WORKSPACE;
 
     unsigned char* scratch = nullptr;
     const moe_status st = scratch_address(&scratch);
     if (st != MOE_OK) return st;
-    auto s = reinterpret_cast<cudaStream_t>(stream);
-    int32_t* status = reinterpret_cast<int32_t*>(scratch);
-    if (cudaMemsetAsync(status, 0, 16, s) != cudaSuccess) return MOE_ERR_CUDA;
-
-    GemmParams p;
-    std::memset(&p, 0, sizeof p);
-    if (!encode_map(&p.a0, w->w_router, dims->d, E, BM)) return MOE_ERR_CUDA;
-    if (!encode_map(&p.b, x, dims->d, T, BN)) return MOE_ERR_CUDA;
-    p.G = 1;
-    p.n_single = static_cast<int32_t>(T);
-    p.M = dims->E;
-    p.MT = (dims->E + BM - 1) / BM;
-    p.KB = dims->d / BK;
-    p.out = scratch + off_logits;
-    p.ldo = dims->E;
-    p.bias = w->router_bias;
-    p.status = status;
-    p.timeout_ns = kTimeoutNs;
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-        return MOE_ERR_CUDA;
-    const int64_t tiles = int64_t(p.MT) * ((dims->T + BN - 1) / BN);
-    if (launch_grouped_gemm(GEMM_ROUTER, p, static_cast<int>(tiles < sms ? tiles : sms), s) !=
-        cudaSuccess)
-        return MOE_ERR_CUDA;
-    if (launch_topk_gates(reinterpret_cast<const float*>(scratch + off_logits), dims->T, dims->E,
-                          dims->k, nullptr, ids_out, gates_out,
-                          reinterpret_cast<int32_t*>(scratch + off_valid), status, s) != cudaSuccess)
-        return MOE_ERR_CUDA;
-    return MOE_OK;
+    const RouteScratch sc{reinterpret_cast<int32_t*>(scratch),
+                          reinterpret_cast<float*>(scratch + off_logits),
+                          reinterpret_cast<float*>(scratch + off_parts),
+                          reinterpret_cast<int32_t*>(scratch + off_valid)};
+    return launch_route(dims, x, w, nullptr, ids_out, gates_out, sc,
+                        reinterpret_cast<cudaStream_t>(stream));
 }

@@ -209,10 +209,16 @@ moe_status moe_route(const moe_dims *dims, const void *x, const moe_weights *w,
                      int32_t *ids_out, float *gates_out, void *ws,
                      size_t ws_bytes, moe_stream_t stream);
 
-/* Full layer forward with the router's own selection:
+/* Full layer forward with the router's own selection -- the MoE layer of
+ * [TD] (section "浮点数不守规矩，MoE 火上浇油": the gate picks 8 of 384
+ * experts per token, and the experts' outputs are added in a fixed order so
+ * that results do not depend on the batch), with the grouped expert GEMMs and
+ * the dispatch/combine of [TR] §6.1 "Training infrastructure" (Fig. 10):
  *   out[t] = sum_{s<k} gates[t][s] * expert_{ids[t][s]}(x[t]) + shared(x[t]),
- * expert(x) = W_down . (silu(W_gate . x) * (W_up . x)).  Out: out [T][d]
- * (bf16 or fp32 per dims->out_fp32), ids_out, gates_out as in moe_route. */
+ * expert(x) = W_down . (silu(W_gate . x) * (W_up . x)), the k routed terms
+ * added in ascending slot order in fp32, then the shared expert's, rounded
+ * once.  Out: out [T][d] (bf16 or fp32 per dims->out_fp32), ids_out,
+ * gates_out as in moe_route. */
 moe_status moe_forward(const moe_dims *dims, const void *x, const moe_weights *w,
                        void *out, int32_t *ids_out, float *gates_out, void *ws,
                        size_t ws_bytes, moe_stream_t stream);
@@ -279,21 +285,25 @@ moe_status moe_set_stage_events(void *const *events);
 /* Routing that allocates nothing -- the pages have no counterpart of this
  * call; it is a convenience of this library.
  *
- * Same computation and outputs as moe_route (ids_out [T][k] int32 and
- * gates_out [T][k] fp32, device pointers the caller owns), but the scratch
- * memory moe_route takes from the caller's workspace (status word, per-token
- * flags, fp32 logits) lives in a static device array of 4 MiB inside this
- * library, which every GPU that loads the library holds until the process
- * exits.  It is meant for callers that cannot allocate device memory: an
- * inference engine recording routing decisions inside its decode loop, where
- * all device memory belongs to the engine's own pool and a cudaMalloc would
- * synchronise the device or fail, or a plugin whose host framework hands it
- * only input and output buffers.  The call itself makes no cudaMalloc,
- * cudaFree or other allocating call.
+ * Same computation and outputs as moe_route, bit for bit (ids_out [T][k]
+ * int32 and gates_out [T][k] fp32, device pointers the caller owns): it runs
+ * the same launch sequence, with the router GEMM's K split into the same
+ * fixed parts summed in the same order.  The scratch memory moe_route takes
+ * from the caller's workspace (status word, per-token flags, fp32 logits and
+ * the router's partial logits) lives in a static device array of 4 MiB inside
+ * this library, which every GPU that loads the library holds until the
+ * process exits.  It is meant for callers that cannot allocate device memory:
+ * an inference engine recording routing decisions inside its decode loop,
+ * where all device memory belongs to the engine's own pool and a cudaMalloc
+ * would synchronise the device or fail, or a plugin whose host framework
+ * hands it only input and output buffers.  The call itself makes no
+ * cudaMalloc, cudaFree or other allocating call.
  *
- * Limit: 256 + round_up(4*T, 256) + 4*T*E <= 4 MiB (T <= 2723 at E = 384);
- * larger requests return MOE_ERR_WORKSPACE before any launch.  Shape, null
- * and alignment errors are reported as for moe_route.
+ * Limit: with P = 4 partial-logit buffers when d/64 is a multiple of 4 (else
+ * P = 0), 256 + round_up(4*T, 256) + round_up(4*T*E, 256) + P*4*T*E <= 4 MiB
+ * (T <= 545 at E = 384, d = 7168); larger requests return MOE_ERR_WORKSPACE
+ * before any launch.  Shape, null and alignment errors are reported as for
+ * moe_route.
  * Set-up: the first call on a device looks up the array's device address
  * (cudaGetSymbolAddress) with that device current; make that first call before
  * any stream capture begins.
