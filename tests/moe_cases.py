@@ -238,3 +238,67 @@ def check_grad(name: str, gpu, ref: np.ndarray):
     mx = float(np.abs(g - ref).max())
     assert rel <= GRAD_REL_FRO, f"{name}: relative Frobenius error {rel:.3e}"
     assert mx <= GRAD_MAX_ABS_REL * scale, f"{name}: max-abs error {mx:.3e} (scale {scale:.3e})"
+
+
+# ---- whole-batch routing checks and sampled outputs at full size ----------------
+
+def boundary_tokens(cnt: np.ndarray, off: np.ndarray, perm: np.ndarray, k: int,
+                    tile: int = 256) -> list:
+    """Tokens at the edges the expert GEMMs' tiling creates: for one expert of
+    every class (no token tile larger than 64, 128, 192 or 256 rows; several
+    token tiles, with the last one full or ragged; the busiest and the least
+    busy expert), the tokens at rows 0, 31/32, 63/64, 127/128, 255/256,
+    511/512 and the last row of its segment in dispatch order."""
+    chosen = {}
+    nz = np.nonzero(cnt)[0]
+    for e in nz:
+        n = int(cnt[e])
+        cls = ("cold", (n + 63) // 64) if n <= tile else ("hot", min(n // tile, 3), n % tile == 0)
+        chosen.setdefault(cls, int(e))
+    if len(nz):
+        chosen["max"] = int(nz[np.argmax(cnt[nz])])
+        chosen["min"] = int(nz[np.argmin(cnt[nz])])
+    toks = set()
+    for e in chosen.values():
+        n = int(cnt[e])
+        for pos in (0, 31, 32, 63, 64, 127, 128, 255, 256, 511, 512, n - 1):
+            if 0 <= pos < n:
+                toks.add(int(perm[off[e] + pos]) // k)
+    return sorted(toks)
+
+
+def check_batch_routing(inp, x, layer, ids, gates, replay_ids=None):
+    """Whole-batch checks of one GPU call against the oracle: fp32 logits of
+    every token; ids by the id rules (own mode) or equal to the recorded ids
+    (replay); every token's gate weights against the oracle's gate weights over
+    the ids the GPU used (the oracle in replay mode with those ids); and the
+    counting sort (cnt, off, perm, inv) of those ids, bit for bit.  Returns
+    (oracle logits, GPU ids, mask of tokens whose GPU ids equal the oracle's
+    own selection, intermediates)."""
+    T, k, E = x.shape[0], inp.cfg.k, inp.cfg.E
+    wr, bias = router_host(inp)
+    ref_logits = oracle.router_logits(bf16_bits(x), wr, bias)
+    im = layer.intermediates(T)
+    check_logits(im["logits"].cpu().numpy(), ref_logits)
+    g_ids = ids.cpu().numpy()
+    if replay_ids is None:
+        same = check_ids(g_ids, ref_logits, k)
+    else:
+        assert np.array_equal(g_ids, replay_ids)
+        same = np.all(g_ids == oracle.select_topk(ref_logits, k), axis=1)
+    check_gates(gates.cpu().numpy(), oracle.gate_weights(ref_logits, g_ids))
+    cnt, off, perm, inv = oracle.counting_sort(g_ids, E)
+    assert np.array_equal(im["cnt"].cpu().numpy(), cnt)
+    assert np.array_equal(im["off"].cpu().numpy(), off)
+    assert np.array_equal(im["perm"].cpu().numpy(), perm)
+    assert np.array_equal(im["inv"].cpu().numpy(), inv)
+    return ref_logits, g_ids, same, (cnt, off, perm)
+
+
+def check_sampled_outputs(inp, x, out32, g_ids, tokens):
+    """Layer outputs of the sampled tokens against the oracle run in replay
+    mode with the ids the GPU used (for tokens whose ids equal the oracle's own
+    selection this is the own-mode oracle)."""
+    tk = np.asarray(sorted(set(int(t) for t in tokens)))
+    ref = oracle_layer(inp, tokens=tk, replay_ids=g_ids[tk], x=x)
+    return check_out(out32.cpu().numpy()[tk], ref.out)

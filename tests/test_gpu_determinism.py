@@ -111,8 +111,13 @@ def _sampled_parity(inp, layer, tokens, replay):
     else:
         assert np.array_equal(g_ids, rid)
         same = np.ones(len(tk), bool)
-    mc.check_gates(gates.cpu().numpy()[tk][same], ref.gates[same])
-    return mc.check_out(out.cpu().numpy()[tk][same], ref.out[same])
+    mc.check_gates(gates.cpu().numpy()[tk], oracle.gate_weights(ref.logits, g_ids))
+    rel_mx = mc.check_out(out.cpu().numpy()[tk][same], ref.out[same])
+    # tokens whose GPU ids differ from the oracle's own choice (near ties):
+    # the oracle replaying the GPU's ids
+    if not same.all():
+        mc.check_sampled_outputs(inp, inp.x, out, ids.cpu().numpy(), tk[~same])
+    return rel_mx
 
 
 @pytest.mark.slow

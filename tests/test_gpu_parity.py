@@ -51,8 +51,13 @@ def test_own_routing_matches_oracle(cfg):
     assert same.mean() > 0.95
     # logits themselves
     mc.check_logits(l32.intermediates(cfg.T)["logits"].cpu().numpy(), ref.logits)
-    mc.check_gates(gates.cpu().numpy()[same], ref.gates[same])
+    g_ids = ids.cpu().numpy()
+    # every token's gates over the ids the GPU chose (the oracle in replay mode)
+    mc.check_gates(gates.cpu().numpy(), oracle.gate_weights(ref.logits, g_ids))
     mc.check_out(out32.cpu().numpy()[same], ref.out[same])
+    # tokens whose GPU ids differ (near ties): the oracle replaying those ids
+    if not same.all():
+        mc.check_sampled_outputs(inp, inp.x, out32, g_ids, np.nonzero(~same)[0])
 
 
 @pytest.mark.parametrize("cfg", CASES, ids=lambda c: c.name)
