@@ -22,6 +22,12 @@ Under torchrun each rank runs its own batch on its own GPU (weak scaling, no
 collective on the data path; a barrier and a max over ranks for timing).
 --impl reference times the fp64 CPU oracle on a bounded sample of the same
 workload (rank 0 only).
+
+On one GPU the default (headline) run also times every other d=7168 workload
+of the layer -- prefill-like Zipf (replay and own), 32k tokens (uniform and
+Zipf s=1.2 routing, own), MXFP8 weights (own) -- one after another in the same
+process, and reports each under "workloads" in the same JSON line
+(--no-workloads skips them).
 """
 from __future__ import annotations
 
@@ -88,6 +94,9 @@ def parse():
                          "(default 64 forward, 2 backward)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="forward, 1 GPU: skip timing the other d=7168 workloads beside the "
+                         "headline one")
     args = ap.parse_args()
     if args.config is None:
         args.config = "c4_train_32k" if args.pass_ != "forward" else "c2_decode_replay"
@@ -356,28 +365,26 @@ def run_reference(args):
     return 0
 
 
-def run_ours(args):
+def time_forward(cfg, mode, K, warmup, world, local):
+    """Time K layer calls of workload cfg (own or replay mode) after `warmup`
+    untimed ones, on this rank's GPU: CUDA events on the launching stream,
+    barrier and synchronize on both sides, clocks sampled during the timed
+    region.  Returns the measurements and the layer (for the e2e leg)."""
     import torch
-    from deterministic_rl_gb300 import MoELayer, binding as B, build as lib_build
-    from deterministic_rl_gb300.synthetic import CONFIGS, make_layer
-    world, rank, local = dist_setup(args)
-    lib_build.build()
-    cfg = CONFIGS[args.config]
-    if args.experts:
-        cfg = cfg.with_(name=f"{cfg.name}_E{args.experts}", E=args.experts)
-    if args.tokens:
-        cfg = cfg.with_(name=f"{cfg.name}_T{args.tokens}", T=args.tokens)
+    from deterministic_rl_gb300 import MoELayer, binding as B
+    from deterministic_rl_gb300.synthetic import make_layer
+    rank = int(os.environ.get("RANK", "0"))
     # weak scaling: every rank runs its own batch (seed offset by rank)
     inp = make_layer(cfg.with_(seed=cfg.seed + 1000 * rank) if rank else cfg, "cuda")
     layer = MoELayer.from_inputs(inp)
-    T, K = cfg.T, args.steps
+    T = cfg.T
     # weight preparation at load time (untimed): the SM-pair forward reads the
     # gate/up weights from one packed tensor
     packed = cfg.wfmt == "bf16" and T > ONE_SM_MAX_TOKENS
     if packed:
         layer.pack_weights()
     replay = None
-    if args.mode == "replay":
+    if mode == "replay":
         rid, _ = layer.route(inp.x_replay_src)  # recorded at "inference": untimed
         replay = rid.clone()
     outs = layer.outputs(T)
@@ -385,7 +392,7 @@ def run_ours(args):
     def step(x=inp.x, ids=replay):
         layer.forward(x, replay_ids=ids, outputs=outs)
 
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     if layer.status() != 0:
@@ -468,6 +475,67 @@ def run_ours(args):
                   "roofline_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_per_step,
                   "frac_nominal_8tbs": 1e3 * max(flops / 2.25e15, nbytes / 8e12) / ms_per_step,
                   "peaks": f"{pk_kind}: {hbm} GB/s, {tensor} TFLOP/s bf16"}
+    return {"inp": inp, "layer": layer, "replay": replay, "outs": outs, "packed": packed,
+            "value": value, "ms_per_step": ms_per_step, "nbytes": nbytes, "need_flush": need_flush,
+            "roofline": roofline, "layer_roofline": layer_roof, "stages_ms": stage_ms,
+            "clocks": clk.summary()}
+
+
+# Every d = 7168 workload of the layer beside the headline one, timed in the
+# same run: (workload, mode, zipf override or None).
+EXTRA_WORKLOADS = [("c3_prefill_zipf", "replay", None), ("c3_prefill_zipf", "own", None),
+                   ("c4_train_32k", "own", None), ("c4_train_32k", "own", 1.2),
+                   ("c5_mxfp8", "own", None)]
+
+
+def run_workloads(args, world, local):
+    """The other d = 7168 workloads, each timed like the headline one (same
+    warm-up, at most 20 timed steps, clocks sampled), one after another with
+    the previous one's memory released."""
+    import torch
+    from deterministic_rl_gb300.synthetic import CONFIGS
+    res = []
+    for name, mode, zipf in EXTRA_WORKLOADS:
+        cfg = CONFIGS[name]
+        if zipf is not None:
+            cfg = cfg.with_(zipf=zipf, name=f"{name}_zipf{zipf}")
+        K = max(1, min(args.steps, 20))
+        r = time_forward(cfg, mode, K, args.warmup, world, local)
+        entry = {"workload": workload_desc(cfg, mode), "steps": K, "warmup": args.warmup,
+                 "ms_per_step": r["ms_per_step"], "tokens_per_s": r["value"],
+                 "layer_roofline_frac": r["layer_roofline"]["frac"],
+                 "layer_roofline": r["layer_roofline"],
+                 "dominant_kernel": {k: r["roofline"][k] for k in
+                                     ("kernel", "bound", "achieved", "peak", "unit", "frac",
+                                      "avg_launch_ms")},
+                 "stages_ms": r["stages_ms"], "clocks": r["clocks"],
+                 "gpu_launches": launches_per_step(cfg) * K,
+                 "weights": ("gate/up packed once at load (moe_pack_weights, untimed)"
+                             if r["packed"] else "as given")}
+        if cfg.near_tie_frac:
+            entry["note"] = ("near-tie tokens are not constructed here: they change no "
+                             "kernel's work (the parity tests construct them)")
+        res.append(entry)
+        del r
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+    return res
+
+
+def run_ours(args):
+    import torch
+    from deterministic_rl_gb300 import build as lib_build
+    from deterministic_rl_gb300.synthetic import CONFIGS
+    world, rank, local = dist_setup(args)
+    lib_build.build()
+    cfg = CONFIGS[args.config]
+    if args.experts:
+        cfg = cfg.with_(name=f"{cfg.name}_E{args.experts}", E=args.experts)
+    if args.tokens:
+        cfg = cfg.with_(name=f"{cfg.name}_T{args.tokens}", T=args.tokens)
+    T, K = cfg.T, args.steps
+    r = time_forward(cfg, args.mode, K, args.warmup, world, local)
+    inp, layer, replay, outs = r["inp"], r["layer"], r["replay"], r["outs"]
 
     e2e = None
     if not args.no_e2e:
@@ -507,19 +575,28 @@ def run_ours(args):
                "sample": f"first {len(tokens)} tokens of {cfg.name} ({args.mode}), {passes} fp64 "
                          f"oracle layer passes, {dt:.1f} s"}
 
+    workloads = None
+    if (world == 1 and args.config == "c2_decode_replay" and not args.no_workloads
+            and not args.experts and not args.tokens):
+        del inp, layer, replay, outs, r["inp"], r["layer"], r["outs"], r["replay"]
+        torch.cuda.empty_cache()
+        workloads = run_workloads(args, world, local)
+
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K,
-                "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        line = {"metric": METRIC, "value": r["value"], "unit": UNIT, "n_gpus": world, "steps": K,
+                "warmup": args.warmup, "ms_per_step": r["ms_per_step"], "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": workload_desc(cfg, args.mode), "tokens_per_step": T,
                            "weights": ("gate/up packed once at load (moe_pack_weights, untimed)"
-                                       if packed else "as given"),
+                                       if r["packed"] else "as given"),
                            "parallelism": f"replicas x{world} (own batch per GPU, no collective)",
-                           "l2": ("L2 flushed between steps" if need_flush else
-                                  f"inputs larger than L2: {nbytes / 1e9:.1f} GB read per step")},
-                "roofline": roofline, "layer_roofline": layer_roof, "stages_ms": stage_ms,
-                "clocks": clk.summary(), "e2e": e2e, "gpu_launches": launches_per_step(cfg) * K,
-                "cpu_baseline": cpu}
+                           "l2": ("L2 flushed between steps" if r["need_flush"] else
+                                  f"inputs larger than L2: {r['nbytes'] / 1e9:.1f} GB read per step")},
+                "roofline": r["roofline"], "layer_roofline": r["layer_roofline"],
+                "stages_ms": r["stages_ms"], "clocks": r["clocks"], "e2e": e2e,
+                "gpu_launches": launches_per_step(cfg) * K, "cpu_baseline": cpu}
+        if workloads is not None:
+            line["workloads"] = workloads
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
