@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
                     for (int j = 0; j < 32; ++j) {
                         if (row_ok && c0 + j < tl.n_valid) {
                             const float g = v[j];
-                            const float h = g / (1.0f + expf(-g)) * u[j];
+                            const float h = swiglu(g, u[j]);
                             H[static_cast<int64_t>(tl.brow + c0 + j) * p.ldo + row] = __float2bfloat16_rn(h);
                         }
                     }

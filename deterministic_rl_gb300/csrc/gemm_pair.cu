@@ -62,11 +62,20 @@ struct PCfg {
     static constexpr bool kConv = FMT != WFMT_BF16;   // weights converted in-kernel
     static constexpr bool kNv = FMT == WFMT_NVFP4;
     static constexpr bool kSmall = SMALL;
-    static constexpr int kTileN = SMALL ? kSmallTileN : BN_EXPERT;  // tokens per tile
+    static constexpr int kTileN = SMALL ? kSmallTileN : BN_EXPERT;  // tokens per MMA sub-tile
     static constexpr int kHalfN = kTileN / 2;                      // token rows per CTA
-    static constexpr uint32_t kBBytes = kHalfN * BK * 2;
+    // SUPER (the converting gate/up GEMMs on regular batches): a tile is one weight
+    // tile and up to kSuperN tokens of its group, in two MMA sub-tiles (the
+    // first of up to kTileN tokens, the second of up to kSuperN - kTileN), so
+    // that each weight k-block is converted once for all of them.  Its two
+    // accumulators take both TMEM slots; other tiles take one slot each and
+    // alternate between the two.
+    static constexpr bool kSuper = FMT != WFMT_BF16 && !SMALL && MODE == GEMM_SWIGLU;
+    static constexpr int kSuperN = kSuper ? 448 : kTileN;          // tokens per tile
+    static constexpr int kHalf1 = (kSuperN - kTileN) / 2;          // sub-tile 1 rows per CTA
+    static constexpr uint32_t kBBytes = (kHalfN + kHalf1) * BK * 2;
     static constexpr int kAccCols = kTileN;                        // TMEM columns per accumulator
-    static constexpr uint32_t kTmemCols = 2 * kAccCols;            // double-buffered
+    static constexpr uint32_t kTmemCols = 2 * kAccCols;            // two slots
     static constexpr int kChunks = SMALL ? 1 : 2;                  // 32-column TMEM loads per wait
     static constexpr bool kPair = MODE == GEMM_SWIGLU;      // 64 gate + 64 up rows per CTA
     static constexpr int kRowsCta = gemm_rows(MODE);        // output weight rows per CTA
@@ -81,10 +90,10 @@ struct PCfg {
     static constexpr bool kInterleave = kPair && kConv;
     static constexpr uint32_t kXBytes = kPair && !kConv ? 2 * 32 * kXPad * 4 : 0;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;  // operand ring entry
-    static constexpr int kStages = SMALL ? 4 : (kConv ? 5 : 6);
+    static constexpr int kStages = SMALL ? 4 : (kSuper ? 4 : (kConv ? 5 : 6));
     static constexpr uint32_t kF8RowBytes = kNv ? BK / 2 : BK;  // weight bytes per row and k-block
     static constexpr uint32_t kF8Bytes = BM * kF8RowBytes;      // fp8 / fp4 weight tile
-    static constexpr int kF8Stages = SMALL ? (kNv ? 24 : 12) : (kConv ? 5 : 0);
+    static constexpr int kF8Stages = SMALL ? (kNv ? 24 : 12) : (kSuper ? 4 : (kConv ? 5 : 0));
     static constexpr int kScPerKb = kNv ? BK / 16 : BK / 32;   // scale bytes per row and k-block
     static constexpr uint32_t kScBytes = BM * 8 * kScPerKb;     // 8 k-blocks of scales
     static constexpr int kScStages = kConv ? 2 : 0;
@@ -111,7 +120,9 @@ struct PCfg {
 
 struct Tile {
     int m, g, n_valid, brow, arow;
-    int half;     // MMA N / 2: token rows each CTA holds (a multiple of 32)
+    int half;     // sub-tile 0: MMA N / 2, token rows each CTA holds (a multiple of 16)
+    int n1;       // tokens of sub-tile 1 (the tile's tokens from kTileN on); 0: none
+    int half1;    // sub-tile 1: MMA N / 2 (0 when n1 == 0)
     bool shared;
     bool reused;  // the expert has several token tiles: its weight tiles are read again
 };
@@ -147,7 +158,12 @@ __device__ __forceinline__ int find_group(const int* start, int GG, int j) {
     return lo;
 }
 
-template <int MODE, int TN>
+// Token tiles of a group of c tokens: ceil(c / TS) of them, of equal size
+// (the last one taking the rest) when TS > TN (a tile then holds two MMA
+// sub-tiles: its first TN tokens and the rest), of TN and a tail otherwise.
+// A sub-tile's MMA width N is its token count rounded up to 32 (at least 64):
+// a valid N for the M = 256 pair MMA, which takes multiples of 16.
+template <int MODE, int TN, int TS>
 __device__ __forceinline__ Tile decode_tile(int t, uint32_t rank, const GemmParams& p,
                                             const Sched& sc) {
     Tile tl;
@@ -174,9 +190,18 @@ __device__ __forceinline__ Tile decode_tile(int t, uint32_t rank, const GemmPara
     const int lo = tl.g;
     const int* gcnt = sc.gcnt;
     const int* goff = sc.goff;
-    tl.n_valid = min(TN, gcnt[lo] - nt * TN);
-    tl.half = min(TN, max(64, (tl.n_valid + 63) & ~63)) >> 1;
-    tl.brow = goff[lo] + nt * TN;
+    const int c = gcnt[lo];
+    int sz = TS;
+    if (TS > TN) {
+        const int ntg = max(1, (c + TS - 1) / TS);
+        sz = (c + ntg - 1) / ntg;
+    }
+    tl.n_valid = min(sz, c - nt * sz);
+    const int n0 = min(TN, tl.n_valid);
+    tl.half = min(TN, max(64, (n0 + 31) & ~31)) >> 1;
+    tl.n1 = tl.n_valid - n0;
+    tl.half1 = tl.n1 > 0 ? max(64, (tl.n1 + 31) & ~31) >> 1 : 0;
+    tl.brow = goff[lo] + nt * sz;
     tl.shared = lo >= p.G;
     tl.arow = (tl.shared ? 0 : lo * p.M) + tl.m * 2 * gemm_rows(MODE) + rank * gemm_rows(MODE);
     return tl;
@@ -184,18 +209,23 @@ __device__ __forceinline__ Tile decode_tile(int t, uint32_t rank, const GemmPara
 
 // Token rows CTA `rank` holds of a tile: [rank * half, rank * half + half) of
 // the tile's tokens, of which this many exist; they are loaded in 32-row boxes
-// (a CTA with none leaves its rows stale: they only feed columns never stored).
+// (a CTA with none leaves its rows stale: they only feed columns never stored;
+// rows a last box loads past them, from the next group or zero-filled past
+// the tensor's end, likewise).
 __device__ __forceinline__ int b_rows(const Tile& tl, uint32_t rank) {
     return min(max(tl.n_valid - static_cast<int>(rank) * tl.half, 0), tl.half);
 }
 __device__ __forceinline__ uint32_t b_bytes(const Tile& tl, uint32_t rank) {
     return ((b_rows(tl, rank) + 31) >> 5) * kBox32Bytes;
 }
-
-// Instruction descriptor for this tile's MMA: M = 256, N = 2 * half.
-__device__ __forceinline__ uint32_t tile_idesc(const Tile& tl) {
-    return idesc_bf16_f32(2 * BM, 2 * tl.half);
+// The same for sub-tile 1 (tokens [TN, TN + n1) of the tile).
+__device__ __forceinline__ int b_rows1(const Tile& tl, uint32_t rank) {
+    return min(max(tl.n1 - static_cast<int>(rank) * tl.half1, 0), tl.half1);
 }
+__device__ __forceinline__ uint32_t b_bytes1(const Tile& tl, uint32_t rank) {
+    return ((b_rows1(tl, rank) + 31) >> 5) * kBox32Bytes;
+}
+
 
 __device__ __forceinline__ void raise_timeout(const GemmParams& p, volatile int* abort, int where) {
     atomicOr(p.status, STATUS_TIMEOUT);
@@ -230,23 +260,13 @@ __device__ __forceinline__ void e4m3x4_to_bf16x4(uint32_t w, uint32_t s, uint32_
     hi = e4m3x2_to_bf16x2(w >> 16, scale);
 }
 
-// Nonzero iff some byte of w is zero or subnormal (exponent field 0) or NaN
-// (low seven bits all ones): bit 7 of (b & 0x78) + 0x78 is set iff the
-// exponent is nonzero, bit 7 of (b & 0x7F) + 1 iff the low seven bits are ones;
-// neither sum carries out of its byte.
-__device__ __forceinline__ uint32_t e4m3x4_special(uint32_t w) {
-    const uint32_t e = (w & 0x78787878u) + 0x78787878u;
-    const uint32_t n = (w & 0x7F7F7F7Fu) + 0x01010101u;
-    return (~e | n) & 0x80808080u;
-}
-
 __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
     uint32_t d;
     asm("prmt.b32 %0, %1, 0, %2;" : "=r"(d) : "r"(a), "r"(sel));
     return d;
 }
 
-// Four normal E4M3 bytes (none flagged by e4m3x4_special) with 7 <= s <= 246
+// Four normal E4M3 bytes (none flagged by e4m3x16_special) with 7 <= s <= 246
 // -> four bf16, exactly.  The bf16 of e4m3 * 2^(s-127) is the E4M3 pattern
 // with its 7 exponent+mantissa bits moved to bf16 bits [10:4], the sign to bit
 // 15 and the exponent re-biased by s - 7 (E4M3 bias 7, bf16 bias 127); the
@@ -258,6 +278,95 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
 __device__ __forceinline__ void e4m3x4_rebias(uint32_t w, uint32_t k, uint32_t& lo, uint32_t& hi) {
     lo = (prmt(w, 0x9180u) & 0x087F087Fu) * 16u + k;  // bytes 0, 1
     hi = (prmt(w, 0xB3A2u) & 0x087F087Fu) * 16u + k;  // bytes 2, 3
+}
+
+// Nonzero (bit 7 of some byte) iff one of the sixteen E4M3 bytes of q is zero
+// or subnormal (low seven bits below 8) or NaN (low seven bits all ones): with
+// t the low seven bits of each byte, bit 7 of t + 0x78 is clear iff t < 8 and
+// bit 7 of t + 0x01 is set iff t == 0x7F; neither sum carries out of its byte.
+__device__ __forceinline__ uint32_t e4m3x16_special(const uint4& q) {
+    uint32_t acc = 0;
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t t = w[i] & 0x7F7F7F7Fu;
+        acc |= ~(t + 0x78787878u) | (t + 0x01010101u);
+    }
+    return acc & 0x80808080u;
+}
+
+// Operand row of converted weight row r (0..127) of a CTA's tile: with the
+// gate/up interleave, 16 gate rows then the same 16 up rows, four times (the
+// low 3 bits, which pick the 128-byte swizzle, stay r's).
+template <bool kInterleave>
+__device__ __forceinline__ int mx_operand_row(int r) {
+    return kInterleave ? ((r & 63) >> 4) * 2 * kSwigluBlock + (r >= 64 ? kSwigluBlock : 0) + (r & 15)
+                       : r;
+}
+
+// One converter warp's share of an MXFP8 k-block: rows [row0, row0 + kRows)
+// of the CTA's 128 (64 E4M3 bytes per row in f8, 16 scale bytes per row per 8
+// k-blocks in sc, this k-block's pair at 2 * kb8), written as bf16 into the
+// 128-byte-swizzled operand tile st.  Lane l takes the 16-value tasks
+// (c2 = 2 (l % 4), rows row0 + l / 4 + 8 i): its rows advance by 8, so the
+// swizzled 16-byte chunks it writes are the same in every row.  Four tasks'
+// loads are issued before their arithmetic and stores; the exceptional bytes
+// (zero, subnormal, NaN) and scales outside [7, 246] are only detected on the
+// way, and a lane redoes just the tasks that met one by the exact float route
+// after the fast pass (about one task in 800 for quantised N(0, 0.02) weights).
+template <int kRows, bool kInterleave>
+__device__ __forceinline__ void mx_convert_rows(const uint8_t* f8, const uint8_t* sc, int kb8,
+                                                uint8_t* st, int row0, int lane) {
+    constexpr int kIters = kRows * 4 / 32;
+    constexpr int kBatch = kIters < 4 ? kIters : 4;
+    static_assert(kIters % kBatch == 0, "whole batches");
+    const int rl = row0 + (lane >> 2);
+    const int c2 = (lane & 3) * 2;
+    const uint32_t sw0 = static_cast<uint32_t>((c2 ^ (rl & 7)) << 4);
+    const uint32_t sw1 = static_cast<uint32_t>(((c2 + 1) ^ (rl & 7)) << 4);
+    const uint8_t* fp = f8 + rl * 64 + c2 * 8;
+    const uint8_t* sp = sc + rl * 16 + kb8 * 2 + (c2 >> 2);
+    uint32_t bad = 0;
+#pragma unroll
+    for (int b0 = 0; b0 < kIters; b0 += kBatch) {
+        uint4 q[kBatch];
+        uint32_t sb[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            q[j] = *reinterpret_cast<const uint4*>(fp + (b0 + j) * 8 * 64);
+            sb[j] = sp[(b0 + j) * 8 * 16];
+        }
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+            // ((s - 7) << 7) in both 16-bit lanes
+            const uint32_t kk = sb[j] * 0x00800080u - 0x03800380u;
+            uint4 o0, o1;
+            e4m3x4_rebias(q[j].x, kk, o0.x, o0.y);
+            e4m3x4_rebias(q[j].y, kk, o0.z, o0.w);
+            e4m3x4_rebias(q[j].z, kk, o1.x, o1.y);
+            e4m3x4_rebias(q[j].w, kk, o1.z, o1.w);
+            if (e4m3x16_special(q[j]) | ((sb[j] - 7u) > 239u)) bad |= 1u << (b0 + j);
+            uint8_t* row = st + mx_operand_row<kInterleave>(rl + 8 * (b0 + j)) * 128;
+            *reinterpret_cast<uint4*>(row + sw0) = o0;
+            *reinterpret_cast<uint4*>(row + sw1) = o1;
+        }
+    }
+    while (bad) {
+        const int i = __ffs(bad) - 1;
+        bad &= bad - 1;
+        {
+            const uint4 q = *reinterpret_cast<const uint4*>(fp + i * 8 * 64);
+            const uint32_t sbyte = sp[i * 8 * 16];
+            uint4 o0, o1;
+            e4m3x4_to_bf16x4(q.x, sbyte, o0.x, o0.y);
+            e4m3x4_to_bf16x4(q.y, sbyte, o0.z, o0.w);
+            e4m3x4_to_bf16x4(q.z, sbyte, o1.x, o1.y);
+            e4m3x4_to_bf16x4(q.w, sbyte, o1.z, o1.w);
+            uint8_t* row = st + mx_operand_row<kInterleave>(rl + 8 * i) * 128;
+            *reinterpret_cast<uint4*>(row + sw0) = o0;
+            *reinterpret_cast<uint4*>(row + sw1) = o1;
+        }
+    }
 }
 
 // Sixteen E2M1 codes (two words, element 2j in the low nibble of byte j) of
@@ -354,7 +463,7 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
             }
             gcnt[g] = c;
             goff[g] = o;
-            const int ntg = (c + C::kTileN - 1) / C::kTileN;
+            const int ntg = (c + C::kSuperN - 1) / C::kSuperN;
             if (ntg > 1) local_h += ntg; else local_c += ntg;
         }
         int incl_h = local_h, incl_c = local_c;
@@ -371,7 +480,7 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
         for (int g = g0; g < min(g0 + per, GG); ++g) {
             hs[g] = run_h;
             cs[g] = run_c;
-            const int ntg = (gcnt[g] + C::kTileN - 1) / C::kTileN;
+            const int ntg = (gcnt[g] + C::kSuperN - 1) / C::kSuperN;
             if (ntg > 1) run_h += ntg; else run_c += ntg;
         }
         if (lane == 31) {
@@ -535,14 +644,19 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                     break;
                 }
                 if (t < 0) break;
-                const Tile tl = decode_tile<MODE, C::kTileN>(t, rank, p, sched);
+                const Tile tl = decode_tile<MODE, C::kTileN, C::kSuperN>(t, rank, p, sched);
                 const uint64_t pol_w = tl.reused ? pol_again : pol_once;
                 const CUtensorMap* ma0 = tl.shared ? &p.as0 : &p.a0;
                 const CUtensorMap* ma1 = tl.shared ? &p.as1 : &p.a1;
                 const int nbox = (b_rows(tl, rank) + 31) >> 5;
                 const bool whole = !C::kSmall && nbox == C::kHalfN / 32;
-                const uint32_t expect = (MX ? 0 : 2 * kABytes) + b_bytes(tl, 0) + b_bytes(tl, 1);
+                const uint32_t expect = (MX ? 0 : 2 * kABytes) + b_bytes(tl, 0) + b_bytes(tl, 1) +
+                                        b_bytes1(tl, 0) + b_bytes1(tl, 1);
                 const int brow = tl.brow + static_cast<int>(rank) * tl.half;
+                // sub-tile 1 (SUPER): its rows follow sub-tile 0's in the tile's
+                // tokens, and sub-tile 0's kHalfN rows in shared memory
+                const int nbox1 = (b_rows1(tl, rank) + 31) >> 5;
+                const int brow1 = tl.brow + C::kTileN + static_cast<int>(rank) * tl.half1;
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort, tmo)) {
                         if (!*abort) raise_timeout(p, abort, 11);
@@ -572,6 +686,11 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                             tma_load_2d_pair(sb + i * kBox32Bytes, &p.b32, bar, kb * BK, brow + 32 * i,
                                              pol_x);
                     }
+                    if constexpr (C::kSuper) {
+                        for (int i = 0; i < nbox1; ++i)
+                            tma_load_2d_pair(sb + (C::kHalfN / 32 + i) * kBox32Bytes, &p.b32, bar,
+                                             kb * BK, brow1 + 32 * i, pol_x);
+                    }
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == kStages) {
@@ -594,20 +713,28 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
             // ---------------- MMA issuer (leader only) ----------------
             int stage = 0;
             uint32_t phase = 0;
-            int acc = 0;
-            uint32_t acc_phase = 0;
+            // TMEM slot uses so far: use u takes slot u % 2 in phase (u / 2) % 2;
+            // a tile takes one slot, or two (sub-tiles 0 and 1) with SUPER
+            int su = 0;
             bool ok = true;
             for (int j = 0; ok; ++j) {
                 int t;
                 if (!next_tile(j, t, 27, false) || t < 0) break;
-                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort, tmo)) {
-                    if (!*abort) raise_timeout(p, abort, 13);
-                    break;
+                const Tile tl = decode_tile<MODE, C::kTileN, C::kSuperN>(t, rank, p, sched);
+                const int ns = tl.half1 ? 2 : 1;
+                for (int u = 0; u < ns && ok; ++u) {
+                    const int v = su + u;
+                    if (!mbar_wait(&tempty[v & 1], ((v >> 1) & 1) ^ 1u, abort, tmo)) {
+                        if (!*abort) raise_timeout(p, abort, 13);
+                        ok = false;
+                    }
                 }
+                if (!ok) break;
                 tc_fence_after();
-                const uint32_t d0 = tmem_base + acc * C::kAccCols;
-                const uint32_t idesc =
-                    tile_idesc(decode_tile<MODE, C::kTileN>(t, rank, p, sched));
+                const uint32_t d0 = tmem_base + (su & 1) * C::kAccCols;
+                const uint32_t d1 = tmem_base + ((su + 1) & 1) * C::kAccCols;
+                const uint32_t idesc = idesc_bf16_f32(2 * BM, 2 * tl.half);
+                const uint32_t idesc1 = idesc_bf16_f32(2 * BM, 2 * (ns == 2 ? tl.half1 : 32));
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort, tmo)) {
                         if (!*abort) raise_timeout(p, abort, 14);
@@ -617,10 +744,17 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                     tc_fence_after();
                     const uint32_t sa = smem_addr(smem + stage * kStageBytes);
                     const uint32_t sb = sa + kABytes;
+                    // the two sub-tiles' MMAs of each K step back to back: they
+                    // multiply the same A (weights) with different B (tokens)
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k)
+                    for (int k = 0; k < BK / 16; ++k) {
                         umma_bf16_pair(d0, sdesc_kmajor_sw128(sa + k * 32),
                                        sdesc_kmajor_sw128(sb + k * 32), idesc, (kb | k) != 0);
+                        if (C::kSuper && ns == 2)
+                            umma_bf16_pair(d1, sdesc_kmajor_sw128(sa + k * 32),
+                                           sdesc_kmajor_sw128(sb + C::kHalfN * 128 + k * 32),
+                                           idesc1, (kb | k) != 0);
+                    }
                     umma_commit_pair(&empty[stage], 0x3);
                     if (++stage == kStages) {
                         stage = 0;
@@ -628,11 +762,9 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                     }
                 }
                 if (!ok) break;
-                umma_commit_pair(&tfull[acc], 0x3);
-                if (++acc == 2) {
-                    acc = 0;
-                    acc_phase ^= 1u;
-                }
+                umma_commit_pair(&tfull[su & 1], 0x3);
+                if (ns == 2) umma_commit_pair(&tfull[(su + 1) & 1], 0x3);
+                su += ns;
             }
             umma_commit_pair(drain, 0x1);
             if (!mbar_wait(drain, 0, nullptr, tmo)) raise_timeout(p, abort, 15);
@@ -650,7 +782,7 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                 for (int j = 0; ok; ++j) {
                     int t;
                     if (!next_tile(j, t, 28, false) || t < 0) break;
-                    const Tile tl = decode_tile<MODE, C::kTileN>(t, rank, p, sched);
+                    const Tile tl = decode_tile<MODE, C::kTileN, C::kSuperN>(t, rank, p, sched);
                     const uint64_t pol_w = tl.reused ? pol_again : pol_once;
                     for (int kb = 0; kb < p.KB; ++kb) {
                         if ((kb & 7) == 0) {  // scales of the next 8 k-blocks
@@ -758,6 +890,10 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                 const uint8_t* f8 = f8ring + fs * C::kF8Bytes;
                 const uint8_t* sc = scring + ss * C::kScBytes;
                 const int kb8 = static_cast<int>(i & 7);
+                if constexpr (!C::kNv) {
+                    mx_convert_rows<kRowsPerWarp, C::kInterleave>(f8, sc, kb8, st,
+                                                                  sub * kRowsPerWarp, lane);
+                } else {
                 // 128 rows x 4 tasks of 16 values (one scale each); a task
                 // becomes two 16-byte chunks of the 128-byte-swizzled row.
 #pragma unroll 4
@@ -765,36 +901,14 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                     const int task = sub * kRowsPerWarp * 4 + it * 32 + lane;
                     const int r = task >> 2, c2 = (task & 3) * 2;
                     uint4 o0, o1;
-                    if constexpr (C::kNv) {
-                        // block c2 / 2 of the row: 8 code bytes, one scale byte
-                        const uint2 q = *reinterpret_cast<const uint2*>(f8 + r * 32 + c2 * 4);
-                        e2m1x16_to_bf16(q, sc[r * 32 + kb8 * 4 + (c2 >> 1)], o0, o1);
-                    } else {
-                        const uint4 q = *reinterpret_cast<const uint4*>(f8 + r * 64 + c2 * 8);
-                        const uint32_t sbyte = sc[r * 16 + kb8 * 2 + (c2 >> 2)];
-                        const uint32_t kk = ((sbyte - 7u) << 7) * 0x00010001u;
-                        e4m3x4_rebias(q.x, kk, o0.x, o0.y);
-                        e4m3x4_rebias(q.y, kk, o0.z, o0.w);
-                        e4m3x4_rebias(q.z, kk, o1.x, o1.y);
-                        e4m3x4_rebias(q.w, kk, o1.z, o1.w);
-                        const uint32_t special = e4m3x4_special(q.x) | e4m3x4_special(q.y) |
-                                                 e4m3x4_special(q.z) | e4m3x4_special(q.w) |
-                                                 ((sbyte - 7u) > 239u);  // s outside [7, 246]
-                        if (special) {  // rare: exact float route for all 16 values
-                            e4m3x4_to_bf16x4(q.x, sbyte, o0.x, o0.y);
-                            e4m3x4_to_bf16x4(q.y, sbyte, o0.z, o0.w);
-                            e4m3x4_to_bf16x4(q.z, sbyte, o1.x, o1.y);
-                            e4m3x4_to_bf16x4(q.w, sbyte, o1.z, o1.w);
-                        }
-                    }
+                    // block c2 / 2 of the row: 8 code bytes, one scale byte
+                    const uint2 q = *reinterpret_cast<const uint2*>(f8 + r * 32 + c2 * 4);
+                    e2m1x16_to_bf16(q, sc[r * 32 + kb8 * 4 + (c2 >> 1)], o0, o1);
                     // operand row: gate/up rows alternate in 16-row blocks
-                    // (the low 3 bits, which pick the swizzle, are r's)
-                    const int ar = C::kInterleave ? ((r & 63) >> 4) * 2 * kSwigluBlock +
-                                                  (r >= 64 ? kSwigluBlock : 0) + (r & 15)
-                                            : r;
-                    uint8_t* row = st + ar * 128;
+                    uint8_t* row = st + mx_operand_row<C::kInterleave>(r) * 128;
                     *reinterpret_cast<uint4*>(row + ((c2 ^ (r & 7)) << 4)) = o0;
                     *reinterpret_cast<uint4*>(row + (((c2 + 1) ^ (r & 7)) << 4)) = o1;
+                }
                 }
                 fence_proxy_async_smem();
                 __syncwarp();
@@ -820,17 +934,29 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
         const int pr = q & 1;
         const bool up_warp = q >= 2;
         const bool up_lane = lane >= kSwigluBlock;
-        int acc = 0;
-        uint32_t acc_phase = 0;
+        int su = 0;  // TMEM slot uses so far, as in the MMA issuer
         uint32_t xph = 0;
         bool ok = true;
         for (int j = 0; ok; ++j) {
             int t;
             if (!next_tile(j, t, 30, true) || t < 0) break;
-            const Tile tl = decode_tile<MODE, C::kTileN>(t, rank, p, sched);
+            const Tile tile = decode_tile<MODE, C::kTileN, C::kSuperN>(t, rank, p, sched);
+            const int ns = tile.half1 ? 2 : 1;
+          for (int sub = 0; sub < ns && ok; ++sub) {
+            // sub-tile `sub` of the tile: its tokens and its TMEM slot
+            Tile tl = tile;
+            if (sub == 1) {
+                tl.brow += C::kTileN;
+                tl.n_valid = tile.n1;
+            } else {
+                tl.n_valid = min(tile.n_valid, C::kTileN);
+            }
+            const int acc = (su + sub) & 1;
+            const uint32_t acc_phase = static_cast<uint32_t>((su + sub) >> 1) & 1u;
             const bool ready = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort, tmo));
             if (!ready) {
                 if (lane == 0 && !*abort) raise_timeout(p, abort, 16);
+                ok = false;
                 break;
             }
             tc_fence_after();
@@ -850,25 +976,31 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                 const float tok_scale = C::kNv && c0 + lane < tl.n_valid
                                             ? p.row_scale[tl.brow + c0 + lane] : 0.0f;
                 if constexpr (C::kInterleave) {
-                    __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out);
+                    // all exchanges first, then 16 independent SwiGLUs, then the
+                    // stores: no shuffle or store sits between two SwiGLUs, so
+                    // they overlap
                     const int cb = c0 + (up_lane ? 16 : 0);
+                    float other[16], h[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        other[j] = __shfl_xor_sync(0xffffffffu, up_lane ? v[j] : v[16 + j], 16);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float lo = v[j], hi = v[16 + j];
-                        const float other = __shfl_xor_sync(0xffffffffu, up_lane ? lo : hi, 16);
-                        float g = up_lane ? other : lo;
-                        float u = up_lane ? hi : other;
+                        float g = up_lane ? other[j] : v[j];
+                        float u = up_lane ? v[16 + j] : other[j];
                         if constexpr (C::kNv) {
                             const float st = __shfl_sync(0xffffffffu, tok_scale, cb - c0 + j);
                             g *= st * ws0;
                             u *= st * ws1;
                         }
-                        if (row_ok && cb + j < tl.n_valid) {
-                            const float h = g / (1.0f + expf(-g)) * u;
-                            H[static_cast<int64_t>(tl.brow + p.out_row_off + cb + j) * p.ldo + row] =
-                                __float2bfloat16_rn(h);
-                        }
+                        h[j] = swiglu(g, u);
                     }
+                    __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out) +
+                                       static_cast<int64_t>(tl.brow + p.out_row_off + cb) * p.ldo + row;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j)
+                        if (row_ok && cb + j < tl.n_valid)
+                            H[static_cast<int64_t>(j) * p.ldo] = __float2bfloat16_rn(h[j]);
                 } else if constexpr (C::kPair) {
                     float* xb = xbuf + pr * 32 * kXPad + lane * kXPad;
                     if (up_warp) {
@@ -895,7 +1027,7 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                         for (int j = 0; j < 32; ++j) {
                             if (row_ok && c0 + j < tl.n_valid) {
                                 const float g = v[j];
-                                const float h = g / (1.0f + expf(-g)) * u[j];
+                                const float h = swiglu(g, u[j]);
                                 const int64_t at =
                                     static_cast<int64_t>(tl.brow + p.out_row_off + c0 + j) * p.ldo + row;
                                 H[at] = __float2bfloat16_rn(h);
@@ -956,10 +1088,8 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(map_to_rank(&tempty[acc], 0));
-            if (++acc == 2) {
-                acc = 0;
-                acc_phase ^= 1u;
-            }
+          }
+            su += ns;
         }
     }
 

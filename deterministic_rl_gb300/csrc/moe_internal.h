@@ -23,6 +23,15 @@ constexpr int BK = 64;
 // up projection, four times, so that each epilogue warp's 32 accumulator lanes
 // hold both halves of 16 rows.
 constexpr int kSwigluBlock = 16;
+// SwiGLU of one gate/up pair of pre-activations: silu(g) * u = g / (1 + e^-g) * u,
+// in fp32 with the fast exponential and division.  Neither branches, so an
+// epilogue keeps many of them in flight; their errors (a few ulp) vanish in
+// the bf16 rounding of the result.  Every forward kernel computes SwiGLU with
+// this one routine, so the kernel families produce the same bits.
+__device__ __forceinline__ float swiglu(float g, float u) {
+    return __fdividef(g, 1.0f + __expf(-g)) * u;
+}
+
 // Expert weight storage formats (the values of the ABI's moe_wfmt).
 constexpr int WFMT_BF16 = 0;
 constexpr int WFMT_MXFP8 = 1;
