@@ -127,3 +127,55 @@ def test_filtered_replay_decode_layer_full_size():
     assert np.array_equal(ids.cpu().numpy()[ok], exp_ids[ok])
     ref = mc.oracle_layer(inp, replay_ids=exp_ids)
     mc.check_out(out.cpu().numpy()[ok], ref.out[ok])
+
+
+@pytest.mark.slow
+def test_replay_filter_p99_mismatch():
+    """The train/inference mismatch the replay filter is meant to lower
+    (Composer 2 Technical Report, §6.2, router-replay paragraph), measured on
+    synthetic inputs of the prefill-like layer's shape: "inference" is the
+    layer with its own routing on a perturbed copy of the hidden states
+    (x + N(0, sigma) rounded to bf16), the "trainer" runs the clean hidden
+    states with (a) its own routing, (b) plain replay of the inference ids, and
+    (c) filtered replay for tau in {0.1, 0.3, 0.5}.  Per token the mismatch is
+    ||out_trainer - out_inference|| / ||out_inference||; the test prints its
+    p99 (and mean) over the batch for several sigma.  Checked properties:
+    replay lowers the mismatch against own routing at every sigma, and a
+    filter that replaces nothing gives plain replay's bits."""
+    cfg = CONFIGS["c3_prefill_zipf"]
+    inp = make_layer(cfg, "cuda")
+    layer = MoELayer.from_inputs(inp, out_fp32=True)
+    x = inp.x
+    gen = torch.Generator(device="cuda").manual_seed(123)
+    noise = torch.randn(x.shape, generator=gen, device="cuda")
+    own_tr = layer.forward(x)[0].clone()
+
+    def mismatch(a, b):
+        r = (a - b).norm(dim=1) / b.norm(dim=1)
+        return float(torch.quantile(r, 0.99)), float(r.mean())
+
+    rows = []
+    for sigma in (1e-3, 3e-2, 1e-1, 3e-1):
+        x_inf = (x.float() + sigma * noise).to(torch.bfloat16)
+        out_inf, ids_inf, _ = [t.clone() for t in layer.forward(x_inf)]
+        flips = float((ids_inf != layer.forward(x)[1]).any(dim=1).float().mean())
+        row = {"sigma": sigma, "tokens_routed_differently": flips,
+               "own": mismatch(own_tr, out_inf)}
+        plain = layer.forward(x, replay_ids=ids_inf)[0].clone()
+        row["replay"] = mismatch(plain, out_inf)
+        for tau in (0.1, 0.3, 0.5):
+            out_f = layer.forward(x, replay_ids=ids_inf, filter_tau=tau)[0]
+            assert layer.status() == B.MOE_OK
+            replaced = int(layer.intermediates(cfg.T)["status"][3])
+            row[f"tau={tau}"] = mismatch(out_f, out_inf) + (replaced,)
+            if replaced == 0:
+                assert torch.equal(out_f, plain)
+        assert row["replay"][0] <= row["own"][0]
+        rows.append(row)
+    print("\nreplay filter, per-token relative output mismatch against the inference layer "
+          f"({cfg.name}, T={cfg.T}): p99 / mean [/ replaced slots]")
+    for row in rows:
+        print("  " + "  ".join(f"{k}: {v}" if not isinstance(v, tuple) else
+                                f"{k}: " + "/".join(f"{u:.3e}" if isinstance(u, float) else str(u)
+                                                    for u in v)
+                                for k, v in row.items()))
