@@ -41,7 +41,7 @@ constexpr int kXPad = 33;
 constexpr int kMaxGroups = 1024;
 
 // MX: expert weights stored as MXFP8 (E4M3 bytes + one E8M0 scale per 32
-// along K).  A dedicated producer warp (warp 14) streams the CTA's fp8 weight
+// along K).  A dedicated producer warp streams the CTA's fp8 weight
 // tiles into their own ring, far ahead, and a 16-byte scale box per row every
 // 8 k-blocks into a small scale ring; eight converter warps, in four groups
 // of two, convert whole k-blocks (group g takes k-blocks g, g+4, ...) into the
@@ -64,13 +64,13 @@ struct PCfg {
     static constexpr bool kSmall = SMALL;
     static constexpr int kTileN = SMALL ? kSmallTileN : BN_EXPERT;  // tokens per MMA sub-tile
     static constexpr int kHalfN = kTileN / 2;                      // token rows per CTA
-    // SUPER (the converting gate/up GEMMs on regular batches): a tile is one weight
+    // SUPER (the converting variants on regular batches): a tile is one weight
     // tile and up to kSuperN tokens of its group, in two MMA sub-tiles (the
     // first of up to kTileN tokens, the second of up to kSuperN - kTileN), so
     // that each weight k-block is converted once for all of them.  Its two
     // accumulators take both TMEM slots; other tiles take one slot each and
     // alternate between the two.
-    static constexpr bool kSuper = FMT != WFMT_BF16 && !SMALL && MODE == GEMM_SWIGLU;
+    static constexpr bool kSuper = FMT != WFMT_BF16 && !SMALL;
     static constexpr int kSuperN = kSuper ? 448 : kTileN;          // tokens per tile
     static constexpr int kHalf1 = (kSuperN - kTileN) / 2;          // sub-tile 1 rows per CTA
     static constexpr uint32_t kBBytes = (kHalfN + kHalf1) * BK * 2;
@@ -114,8 +114,16 @@ struct PCfg {
     static constexpr int kConvWarps = SMALL ? 16 : 8;
     static constexpr int kConvPerKb = SMALL ? 4 : 2;            // warps per k-block
     static constexpr int kConvGroups = kConvWarps / kConvPerKb;  // k-blocks in flight
-    static constexpr int kThreads = kConv ? 192 + 32 * kConvWarps + 32 : 192;
-    static constexpr int kFp8Warp = 6 + kConvWarps;
+    // Warps: 0 TMA producer, 1 MMA issuer, 2..5 epilogue, then the converters
+    // and the fp8 producer.  A warp issues on scheduler warp % 4; with SUPER
+    // the block has 16 warps and no converter shares scheduler 1 with the MMA
+    // issuer (converters 6, 7, 8, 10, 11, 12, 14, 15; fp8 producer 9; 13 idle):
+    // the converters' dense arithmetic otherwise takes the issue slots the MMA
+    // thread needs to keep the tensor pipe fed (measured: gate/up 14 % faster).
+    static constexpr bool kRemap = kSuper;
+    static constexpr int kThreads = kRemap ? 512 : (kConv ? 192 + 32 * kConvWarps + 32 : 192);
+    static constexpr int kFp8Warp = kRemap ? 9 : 6 + kConvWarps;
+    static constexpr int kIdleWarp = kRemap ? 13 : -1;
 };
 
 struct Tile {
@@ -742,18 +750,19 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                         break;
                     }
                     tc_fence_after();
+                    // descriptors of the stage's tiles (1024-byte aligned); a
+                    // K step of 16 advances the start address by 32 bytes
                     const uint32_t sa = smem_addr(smem + stage * kStageBytes);
-                    const uint32_t sb = sa + kABytes;
+                    const uint64_t da = sdesc_kmajor_sw128(sa);
+                    const uint64_t db = sdesc_kmajor_sw128(sa + kABytes);
+                    const uint64_t db1 = sdesc_kmajor_sw128(sa + kABytes + C::kHalfN * 128);
                     // the two sub-tiles' MMAs of each K step back to back: they
                     // multiply the same A (weights) with different B (tokens)
 #pragma unroll
                     for (int k = 0; k < BK / 16; ++k) {
-                        umma_bf16_pair(d0, sdesc_kmajor_sw128(sa + k * 32),
-                                       sdesc_kmajor_sw128(sb + k * 32), idesc, (kb | k) != 0);
+                        umma_bf16_pair(d0, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
                         if (C::kSuper && ns == 2)
-                            umma_bf16_pair(d1, sdesc_kmajor_sw128(sa + k * 32),
-                                           sdesc_kmajor_sw128(sb + C::kHalfN * 128 + k * 32),
-                                           idesc1, (kb | k) != 0);
+                            umma_bf16_pair(d1, da + 2 * k, db1 + 2 * k, idesc1, (kb | k) != 0);
                     }
                     umma_commit_pair(&empty[stage], 0x3);
                     if (++stage == kStages) {
@@ -839,9 +848,11 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                             raise_timeout(p, abort, 23);
             }
         }
+    } else if (warp == C::kIdleWarp) {
+        // no role: keeps converter warps off the MMA issuer's scheduler
     } else if (warp >= 6) {
         if constexpr (MX) {
-            // ---------------- converters (warps 6..13, both CTAs) ----------------
+            // ---------------- converters (warps >= 6, both CTAs) ----------------
             // kConvGroups groups of kConvPerKb warps; group g converts this CTA's
             // k-blocks i = g, g + kConvGroups, ... of the tile sequence, warp j
             // of the group rows [j * 128 / kConvPerKb, ...).  A tile has KB
@@ -854,7 +865,9 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
             static_assert(C::kConvGroups <= C::kStages && C::kConvGroups <= C::kF8Stages &&
                               C::kConvGroups <= 8,
                           "converter groups must not outrun the rings");
-            const int cw = warp - 6;  // 0 .. kConvWarps - 1
+            // 0 .. kConvWarps - 1, skipping the fp8 producer and idle warps
+            const int cw = C::kRemap ? warp - 6 - (warp > C::kFp8Warp) - (warp > C::kIdleWarp)
+                                     : warp - 6;
             const int grp_w = cw / C::kConvPerKb;
             const int sub = cw % C::kConvPerKb;
             constexpr int kRowsPerWarp = BM / C::kConvPerKb;
@@ -1054,15 +1067,40 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                             if (row_ok && c0 + j < tl.n_valid)
                                 Yf[static_cast<int64_t>(tl.brow + c0 + j) * p.ldo + row] = v[j];
                     } else {
-                        __nv_bfloat16* Y = static_cast<__nv_bfloat16*>(p.out);
+                        // Lanes 2i and 2i + 1 (rows r, r + 1 of the output)
+                        // swap values so that each stores both rows of one
+                        // token as a bf16 pair: lane 2i the chunk's even
+                        // tokens, lane 2i + 1 the odd ones.  The exchanges
+                        // come first, then the conversions, then the stores.
+                        const int odd = lane & 1;
+                        float mine[16], other[16];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            float y = v[j];
-                            if constexpr (C::kNv) y *= __shfl_sync(0xffffffffu, tok_scale, j) * ws0;
-                            if (row_ok && c0 + j < tl.n_valid)
-                                Y[static_cast<int64_t>(tl.brow + c0 + j) * p.ldo + row] =
-                                    __float2bfloat16_rn(y);
+                        for (int jj = 0; jj < 16; ++jj) {
+                            other[jj] = __shfl_xor_sync(0xffffffffu, odd ? v[2 * jj] : v[2 * jj + 1], 1);
+                            mine[jj] = odd ? v[2 * jj + 1] : v[2 * jj];
                         }
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj) {
+                            float lo = odd ? other[jj] : mine[jj];  // row r of token 2 jj + odd
+                            float hi = odd ? mine[jj] : other[jj];  // row r + 1
+                            if constexpr (C::kNv) {
+                                const float sc = __shfl_sync(0xffffffffu, tok_scale, 2 * jj + odd) * ws0;
+                                lo *= sc;
+                                hi *= sc;
+                            }
+                            const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+                            pk[jj] = *reinterpret_cast<const uint32_t*>(&b);
+                        }
+                        // rows come in pairs within M (a multiple of 64), so
+                        // both lanes of a pair agree on row_ok
+                        uint32_t* Y = reinterpret_cast<uint32_t*>(
+                            static_cast<__nv_bfloat16*>(p.out) +
+                            static_cast<int64_t>(tl.brow + c0 + odd) * p.ldo + (row & ~1));
+#pragma unroll
+                        for (int jj = 0; jj < 16; ++jj)
+                            if (row_ok && c0 + 2 * jj + odd < tl.n_valid)
+                                Y[static_cast<int64_t>(2 * jj) * (p.ldo >> 1)] = pk[jj];
                     }
                 }
                 return true;
