@@ -413,6 +413,32 @@ __device__ __forceinline__ void e2m1x16_to_bf16(uint2 q, uint32_t s, uint4& o0, 
     o1 = make_uint4(out[4], out[5], out[6], out[7]);
 }
 
+// Epilogue store of bf16 outputs: lanes 2i and 2i + 1 hold the values of two
+// adjacent output rows (r, r + 1; rows are the contiguous axis of the output)
+// for the same N tokens; they swap half of them so that lane 2i stores the
+// even tokens' and lane 2i + 1 the odd tokens' row pair as one bf16x2 word:
+// one conversion and one store per two outputs, the exchanges first.  `at`
+// is the output element (first token, row r & ~1), `ld` the row stride of a
+// token in elements, n_left the valid tokens from the first on.
+template <int N>
+__device__ __forceinline__ void store_bf16_row_pairs(const float (&h)[N], int lane,
+                                                     __nv_bfloat16* at, int64_t ld, int n_left,
+                                                     bool row_ok) {
+    const int odd = lane & 1;
+    uint32_t pk[N / 2];
+#pragma unroll
+    for (int jj = 0; jj < N / 2; ++jj) {
+        const float other = __shfl_xor_sync(0xffffffffu, odd ? h[2 * jj] : h[2 * jj + 1], 1);
+        const float mine = odd ? h[2 * jj + 1] : h[2 * jj];
+        const __nv_bfloat162 b = __floats2bfloat162_rn(odd ? other : mine, odd ? mine : other);
+        pk[jj] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    uint32_t* y = reinterpret_cast<uint32_t*>(at + odd * ld);
+#pragma unroll
+    for (int jj = 0; jj < N / 2; ++jj)
+        if (row_ok && 2 * jj + odd < n_left) y[jj * ld] = pk[jj];  // token 2 jj + odd
+}
+
 template <int MODE, int FMT, bool SMALL>
 __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
     pair_gemm_kernel(const __grid_constant__ GemmParams p) {
@@ -1008,12 +1034,13 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                         }
                         h[j] = swiglu(g, u);
                     }
-                    __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out) +
-                                       static_cast<int64_t>(tl.brow + p.out_row_off + cb) * p.ldo + row;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j)
-                        if (row_ok && cb + j < tl.n_valid)
-                            H[static_cast<int64_t>(j) * p.ldo] = __float2bfloat16_rn(h[j]);
+                    // rows pair up within M (a multiple of 64): both lanes of
+                    // a pair agree on row_ok
+                    store_bf16_row_pairs<16>(
+                        h, lane,
+                        static_cast<__nv_bfloat16*>(p.out) +
+                            static_cast<int64_t>(tl.brow + p.out_row_off + cb) * p.ldo + (row & ~1),
+                        p.ldo, tl.n_valid - cb, row_ok);
                 } else if constexpr (C::kPair) {
                     float* xb = xbuf + pr * 32 * kXPad + lane * kXPad;
                     if (up_warp) {
@@ -1035,17 +1062,21 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                         for (int j = 0; j < 32; ++j) u[j] = xb[j];
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&xempty[pr]);
-                        __nv_bfloat16* H = static_cast<__nv_bfloat16*>(p.out);
+                        float h[32];
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            if (row_ok && c0 + j < tl.n_valid) {
-                                const float g = v[j];
-                                const float h = swiglu(g, u[j]);
-                                const int64_t at =
-                                    static_cast<int64_t>(tl.brow + p.out_row_off + c0 + j) * p.ldo + row;
-                                H[at] = __float2bfloat16_rn(h);
-                                if (p.save_a) {  // the backward keeps the pre-activations
-                                    p.save_a[at] = g;
+                        for (int j = 0; j < 32; ++j) h[j] = swiglu(v[j], u[j]);
+                        store_bf16_row_pairs<32>(
+                            h, lane,
+                            static_cast<__nv_bfloat16*>(p.out) +
+                                static_cast<int64_t>(tl.brow + p.out_row_off + c0) * p.ldo + (row & ~1),
+                            p.ldo, tl.n_valid - c0, row_ok);
+                        if (p.save_a) {  // the backward keeps the pre-activations
+#pragma unroll
+                            for (int j = 0; j < 32; ++j) {
+                                if (row_ok && c0 + j < tl.n_valid) {
+                                    const int64_t at =
+                                        static_cast<int64_t>(tl.brow + p.out_row_off + c0 + j) * p.ldo + row;
+                                    p.save_a[at] = v[j];
                                     p.save_b[at] = u[j];
                                 }
                             }
@@ -1067,40 +1098,17 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                             if (row_ok && c0 + j < tl.n_valid)
                                 Yf[static_cast<int64_t>(tl.brow + c0 + j) * p.ldo + row] = v[j];
                     } else {
-                        // Lanes 2i and 2i + 1 (rows r, r + 1 of the output)
-                        // swap values so that each stores both rows of one
-                        // token as a bf16 pair: lane 2i the chunk's even
-                        // tokens, lane 2i + 1 the odd ones.  The exchanges
-                        // come first, then the conversions, then the stores.
-                        const int odd = lane & 1;
-                        float mine[16], other[16];
+                        float h[32];
 #pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            other[jj] = __shfl_xor_sync(0xffffffffu, odd ? v[2 * jj] : v[2 * jj + 1], 1);
-                            mine[jj] = odd ? v[2 * jj + 1] : v[2 * jj];
+                        for (int j = 0; j < 32; ++j) {
+                            h[j] = v[j];
+                            if constexpr (C::kNv) h[j] *= __shfl_sync(0xffffffffu, tok_scale, j) * ws0;
                         }
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj) {
-                            float lo = odd ? other[jj] : mine[jj];  // row r of token 2 jj + odd
-                            float hi = odd ? mine[jj] : other[jj];  // row r + 1
-                            if constexpr (C::kNv) {
-                                const float sc = __shfl_sync(0xffffffffu, tok_scale, 2 * jj + odd) * ws0;
-                                lo *= sc;
-                                hi *= sc;
-                            }
-                            const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
-                            pk[jj] = *reinterpret_cast<const uint32_t*>(&b);
-                        }
-                        // rows come in pairs within M (a multiple of 64), so
-                        // both lanes of a pair agree on row_ok
-                        uint32_t* Y = reinterpret_cast<uint32_t*>(
+                        store_bf16_row_pairs<32>(
+                            h, lane,
                             static_cast<__nv_bfloat16*>(p.out) +
-                            static_cast<int64_t>(tl.brow + c0 + odd) * p.ldo + (row & ~1));
-#pragma unroll
-                        for (int jj = 0; jj < 16; ++jj)
-                            if (row_ok && c0 + 2 * jj + odd < tl.n_valid)
-                                Y[static_cast<int64_t>(2 * jj) * (p.ldo >> 1)] = pk[jj];
+                                static_cast<int64_t>(tl.brow + c0) * p.ldo + (row & ~1),
+                            p.ldo, tl.n_valid - c0, row_ok);
                     }
                 }
                 return true;
