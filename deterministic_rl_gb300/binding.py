@@ -62,7 +62,7 @@ class moe_weights(ctypes.Structure):
 class moe_ws_layout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("status", "logits", "valid", "cnt", "off", "perm", "inv", "xp", "h", "y",
-                 "ysh", "xq", "sx", "sxp", "sh", "total")]
+                 "ysh", "xq", "sx", "sxp", "sh", "hq", "total")]
 
 
 class moe_grads(ctypes.Structure):

@@ -38,7 +38,8 @@ inline size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255);
 
 struct Layout {
     size_t status, logits, rpart, valid, cnt, off, perm, inv, scratch, xp, h, y, ysh;
-    size_t xq, sx, sxp, sh;  // NVFP4 only
+    size_t xq, sx, sxp, sh;  // NVFP4; xq also MXFP8 activations (codes, scales)
+    size_t hq;               // MXFP8 activations: codes and scales of h
     size_t total;
 };
 
@@ -81,10 +82,13 @@ Layout make_layout(const moe_dims* d) {
     L.ysh = take(S ? T * d->d * 4 : 0);
     const bool nv = d->wfmt == MOE_W_NVFP4;
     const bool mxa = d->wfmt == MOE_W_MXFP8_ACT;
-    L.xq = take(nv || mxa ? T * d->d * 2 : 0);
+    // MXFP8 activations: E4M3 codes [T][d] then E8M0 scales [T][d/32] of x (and
+    // the gathered rows' codes and scales in xp, those of h in hq)
+    L.xq = take(nv ? T * d->d * 2 : (mxa ? T * d->d + T * d->d / 32 : 0));
     L.sx = take(nv ? T * 4 : 0);
     L.sxp = take(nv ? T * k * 4 : 0);
     L.sh = take(nv ? T * k * 4 : 0);
+    L.hq = take(mxa ? T * k * d->F + T * k * d->F / 32 : 0);
     L.total = o;
     return L;
 }
@@ -117,9 +121,10 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint3
 }
 
 // 2-D byte map over [rows][K] (K bytes contiguous), box box_k x box_rows, no
-// swizzle: MXFP8 weight tiles (64-byte boxes) and their E8M0 scales (16-byte).
+// swizzle (or the 128-byte swizzle, for 128-byte boxes that feed the MMA
+// directly): MXFP8 weight tiles and their E8M0 scales (16-byte boxes).
 bool make_map_u8(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, uint32_t box_k,
-                 uint32_t box_rows) {
+                 uint32_t box_rows, bool swizzle128 = false) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {K, rows};
@@ -127,7 +132,8 @@ bool make_map_u8(CUtensorMap* m, const void* base, uint64_t K, uint64_t rows, ui
     const cuuint32_t box[2] = {box_k, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -334,10 +340,111 @@ moe_status side_stream(SideStream** out) {
     return MOE_OK;
 }
 
+// MXFP8 weights and MXFP8 activations: every token row of x, and every row of
+// the SwiGLU output h, is quantised to E4M3 codes and E8M0 scales along K,
+// gathered as codes and scales, and both expert GEMMs run on the block-scaled
+// tensor-core MMA (gemm_mx8.cu).  Any batch size takes this one path, so the
+// result of a token never depends on its batch.
+moe_status run_experts_mx8(const moe_dims* d, const void* x, const moe_weights* w, void* out,
+                           const int32_t* ids, const float* gates, uint8_t* ws, const Layout& L,
+                           cudaStream_t s) {
+    const int64_t T = d->T;
+    const int k = d->k, E = d->E;
+    const int64_t rows = T * k;
+    const int D = d->d, F = d->F;
+    int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
+    int32_t* cnt = reinterpret_cast<int32_t*>(ws + L.cnt);
+    int32_t* off = reinterpret_cast<int32_t*>(ws + L.off);
+    int32_t* perm = reinterpret_cast<int32_t*>(ws + L.perm);
+    int32_t* inv = reinterpret_cast<int32_t*>(ws + L.inv);
+    const int sms = num_sms();
+    if (sms <= 0) return MOE_ERR_CUDA;
+    if (d->n_shared) return MOE_ERR_UNSUPPORTED;
+    uint8_t* x8 = ws + L.xq;                     // [T][D] codes, then [T][D/32] scales
+    uint8_t* xs = x8 + T * D;
+    uint8_t* xp8 = ws + L.xp;                    // gathered: [rows][D], then [rows][D/32]
+    uint8_t* xps = xp8 + rows * D;
+    uint8_t* h8 = ws + L.hq;                     // [rows][F] codes, then [rows][F/32] scales
+    uint8_t* hs = h8 + rows * F;
+    const uint64_t EF = uint64_t(E) * F, ED = uint64_t(E) * D;
+    const int units = sms / 2;
+
+    MOE_TRY(mark(MOE_STAGE_DISPATCH, 0, s));
+    MOE_TRY(cu(launch_dispatch(ids, T, k, E, cnt, off, perm, inv,
+                               reinterpret_cast<int32_t*>(ws + L.scratch), s)));
+    MOE_TRY(mark(MOE_STAGE_DISPATCH, 1, s));
+    MOE_TRY(mark(MOE_STAGE_GATHER, 0, s));
+    MOE_TRY(cu(launch_mx_rows_fp8(static_cast<const uint16_t*>(x), x8, xs, T, D, sms, s)));
+    // rows of codes and of scales moved as 2-byte units (D and D / 32 bytes)
+    MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(x8), inv, T, k, D / 2, 0,
+                             reinterpret_cast<uint16_t*>(xp8), s)));
+    MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(xs), inv, T, k, D / 64, 0,
+                             reinterpret_cast<uint16_t*>(xps), s)));
+    MOE_TRY(mark(MOE_STAGE_GATHER, 1, s));
+
+    const int tn = mx8_tile_tokens(), kk = mx8_k_block();
+    const int64_t ntiles = (rows + tn - 1) / tn + E;
+    auto common = [&](GemmParams& p) {
+        p.cnt = cnt;
+        p.off = off;
+        p.G = E;
+        p.status = status;
+        p.timeout_ns = kWaitTimeoutNs;
+    };
+    const uint32_t rg = gemm_rows(GEMM_SWIGLU);
+    GemmParams p1;
+    std::memset(&p1, 0, sizeof p1);
+    common(p1);
+    if (!make_map_u8(&p1.a0, w->w_gate, D, EF, kk, rg, true)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p1.a1, w->w_up, D, EF, kk, rg, true)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p1.sa0, w->s_gate, D / 32, EF, 16, rg)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p1.sa1, w->s_up, D / 32, EF, 16, rg)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p1.b, xp8, D, rows, kk, 128, true)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p1.b32, xp8, D, rows, kk, 32, true)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p1.sb_scale, xps, D / 32, rows, 16, 128)) return MOE_ERR_CUDA;
+    p1.M = F;
+    p1.MT = F / (2 * static_cast<int>(rg));
+    p1.KB = D / kk;
+    p1.out = ws + L.h;
+    p1.ldo = F;
+    p1.stall_test = take_stall_test() ? 1 : 0;
+    int64_t tb = ntiles * p1.MT;
+    MOE_TRY(mark(MOE_STAGE_GATE_UP, 0, s));
+    MOE_TRY(cu(launch_mx8_gemm(GEMM_SWIGLU, p1, static_cast<int>(tb < units ? tb : units), s)));
+    MOE_TRY(mark(MOE_STAGE_GATE_UP, 1, s));
+
+    GemmParams p2;
+    std::memset(&p2, 0, sizeof p2);
+    common(p2);
+    if (!make_map_u8(&p2.a0, w->w_down, F, ED, kk, BM, true)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p2.sa0, w->s_down, F / 32, ED, 16, BM)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p2.b, h8, F, rows, kk, 128, true)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p2.b32, h8, F, rows, kk, 32, true)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p2.sb_scale, hs, F / 32, rows, 16, 128)) return MOE_ERR_CUDA;
+    p2.M = D;
+    p2.MT = D / (2 * BM);
+    p2.KB = F / kk;
+    p2.out = ws + L.y;
+    p2.ldo = D;
+    tb = ntiles * p2.MT;
+    MOE_TRY(mark(MOE_STAGE_DOWN, 0, s));
+    MOE_TRY(cu(launch_mx_rows_fp8(reinterpret_cast<const uint16_t*>(ws + L.h), h8, hs, rows, F, sms,
+                                  s)));
+    MOE_TRY(cu(launch_mx8_gemm(GEMM_DOWN, p2, static_cast<int>(tb < units ? tb : units), s)));
+    MOE_TRY(mark(MOE_STAGE_DOWN, 1, s));
+
+    MOE_TRY(mark(MOE_STAGE_COMBINE, 0, s));
+    MOE_TRY(cu(launch_combine(reinterpret_cast<const uint16_t*>(ws + L.y), nullptr, inv, gates,
+                              reinterpret_cast<const int32_t*>(ws + L.valid), T, k, D,
+                              d->out_fp32, out, s)));
+    return mark(MOE_STAGE_COMBINE, 1, s);
+}
+
 // Dispatch, expert FFNs and combine, given ids/gates of every token.
 moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, void* out,
                        const int32_t* ids, const float* gates, uint8_t* ws, const Layout& L,
                        cudaStream_t s) {
+    if (d->wfmt == MOE_W_MXFP8_ACT) return run_experts_mx8(d, x, w, out, ids, gates, ws, L, s);
     const int64_t T = d->T;
     const int k = d->k, E = d->E, S = d->n_shared;
     const int64_t rows = T * k + T * S;
@@ -348,10 +455,7 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     int32_t* inv = reinterpret_cast<int32_t*>(ws + L.inv);
     const int sms = num_sms();
     if (sms <= 0) return MOE_ERR_CUDA;
-    // MXFP8 activations: MXFP8 weights (the same kernels) and activations
-    // quantised along K before each expert GEMM
-    const bool mxa = d->wfmt == MOE_W_MXFP8_ACT;
-    const bool mx = d->wfmt == MOE_W_MXFP8 || mxa;
+    const bool mx = d->wfmt == MOE_W_MXFP8;
     const bool nv = d->wfmt == MOE_W_NVFP4;
     const int kfmt = mx ? WFMT_MXFP8 : d->wfmt;  // the GEMM kernels' weight format
     const bool one = one_sm_experts(d);
@@ -429,12 +533,6 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
         MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(ws + L.xq), inv, T, k, d->d, S,
                                  reinterpret_cast<uint16_t*>(ws + L.xp), s,
                                  reinterpret_cast<const float*>(ws + L.sx), sxp)));
-    } else if (mxa) {
-        // MXFP8 activations: each token row quantised once along d, then gathered
-        MOE_TRY(cu(launch_mx_rows(static_cast<const uint16_t*>(x),
-                                  reinterpret_cast<uint16_t*>(ws + L.xq), T, d->d, sms, s)));
-        MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(ws + L.xq), inv, T, k, d->d,
-                                 Sg, reinterpret_cast<uint16_t*>(ws + L.xp), s)));
     } else {
         MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), inv, T, k, d->d, Sg,
                                  reinterpret_cast<uint16_t*>(ws + L.xp), s)));
@@ -536,9 +634,6 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     const int g2 = static_cast<int>(tb < units ? tb : units);
     if (overlap) MOE_TRY(cu(cudaStreamWaitEvent(s, side->join, 0)));
     MOE_TRY(mark(MOE_STAGE_DOWN, 0, s));
-    if (mxa)  // MXFP8 activations: each row of h quantised in place along F
-        MOE_TRY(cu(launch_mx_rows(reinterpret_cast<const uint16_t*>(ws + L.h),
-                                  reinterpret_cast<uint16_t*>(ws + L.h), T * k, d->F, sms, s)));
     if (nv)  // NVFP4: each row of h quantised in place (per-token scale)
         MOE_TRY(cu(launch_nvfp4_qdq(reinterpret_cast<const uint16_t*>(ws + L.h),
                                     reinterpret_cast<uint16_t*>(ws + L.h), nullptr, sh, T * k,
@@ -962,6 +1057,7 @@ moe_status moe_workspace_layout(const moe_dims* dims, moe_ws_layout* out) {
     out->sx = L.sx;
     out->sxp = L.sxp;
     out->sh = L.sh;
+    out->hq = L.hq;
     out->total = L.total;
     return MOE_OK;
 }

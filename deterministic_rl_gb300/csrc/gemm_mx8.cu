@@ -1,0 +1,610 @@
+// gemm_mx8.cu -- the expert GEMMs with MXFP8 on both operands (E4M3 weights and
+// E4M3 token rows, each with one E8M0 scale per 32 along K): the block-scaled
+// tensor-core MMA tcgen05.mma.kind::mxf8f6f4.block_scale multiplies the E4M3
+// values and applies the scales itself, so nothing is converted and the tensor
+// pipe runs at its 8-bit rate.  This is the MXFP8 expert compute of the
+// Composer 2 Technical Report, §6.1 "Training infrastructure", Kernels
+// paragraph (block-scaled tensor-core matmul; MXFP8 = E4M3 values, E8M0 scale
+// per 32 elements).
+//
+// Shape: SM pairs (tcgen05 cta_group::2), M = 256 weight rows (128 per CTA),
+// N = up to 224 tokens (each CTA loads half), K in blocks of 128 (128 bytes per
+// row: one 128-byte-swizzled row of the operand tile, four MMAs of K = 32).
+// Each output element is one pair's fixed-order K loop into one TMEM
+// accumulator; no split-K, no atomics; the MMA width N only selects how many
+// independent token columns one instruction produces.
+//
+// Roles in each CTA (352 threads): warp 0 TMA producer of the weight tiles (and
+// every 4 K blocks the scale tiles); warp 10 TMA producer of the token tiles;
+// warp 1 TMEM owner and, in the pair's leader, the MMA issuer; warps 2..5
+// epilogue; warps 6..9 write each K block's scales into TMEM (one warp per
+// TMEM lane quadrant), where the MMA reads them.
+#include <cuda_bf16.h>
+
+#include "moe_internal.h"
+#include "ptx.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kK8 = 128;                   // K elements (bytes) per stage and row
+constexpr int kTile8 = 224;                // tokens per tile (MMA N <= 224)
+constexpr int kHalf8 = 128;                // token rows per CTA in shared memory
+constexpr int kStages8 = 5;
+constexpr uint32_t kA8 = 128 * kK8;        // weight tile of a CTA: 16 KB
+constexpr uint32_t kB8 = kHalf8 * kK8;     // token tile of a CTA: 16 KB
+constexpr uint32_t kStage8 = kA8 + kB8;
+constexpr uint32_t kBox8 = 32 * kK8;       // one 32-row token box
+// Scale ring: a slot holds the scales of 4 consecutive K blocks of one tile
+// (16 bytes per row): the CTA's 128 weight rows, then the tile's tokens of
+// both CTAs (CTA 0's half at rows 0..127, CTA 1's at 128..255).
+constexpr int kScKb = 4;
+constexpr int kScSlots8 = 4;  // the scales run up to 16 K blocks ahead of their MMAs
+constexpr uint32_t kScA8 = 128 * 16;
+constexpr uint32_t kScB8 = 256 * 16;
+constexpr uint32_t kScSlot8 = kScA8 + kScB8;
+// TMEM: two accumulator slots of kTile8 columns, then per stage 4 columns of
+// weight-row scales and 8 of token scales.
+constexpr uint32_t kAcc8 = kTile8;
+constexpr uint32_t kSfCol8 = 2 * kAcc8;
+constexpr uint32_t kSfStage8 = 12;
+static_assert(kSfCol8 + kStages8 * kSfStage8 <= 512, "TMEM columns");
+constexpr uint32_t kTmemCols8 = 512;
+constexpr int kThreads8 = 352;
+constexpr int kXPad8 = 33;
+constexpr uint32_t kXBytes8 = 2 * 32 * kXPad8 * 4;   // gate/up: up values handed to the gate warps
+constexpr int kBarriers8 = 2 * kStages8 + 2 * kScSlots8 + 2 + 2 + 4 + 1;
+constexpr int kMaxGroups8 = 1024;
+
+struct Tile8 {
+    int m, g, n_valid, brow, arow;
+    int half;  // MMA N / 2
+};
+
+struct Sched8 {
+    const int* hs;
+    const int* cs;
+    const int* gcnt;
+    const int* goff;
+    int GG;
+    int64_t H, N;
+};
+
+__device__ __forceinline__ int find_group8(const int* start, int GG, int j) {
+    int lo = 0, hi = GG;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (start[mid] <= j) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+// Tile t of the order: experts with several token tiles ("hot") and with one
+// ("cold") are interleaved in proportion, so that every wave mixes
+// tensor-bound and weight-streaming tiles; the token tiles of a hot expert's
+// weight tile are consecutive.  Which pair computes a tile never changes how.
+template <int MODE>
+__device__ __forceinline__ Tile8 decode_tile8(int t, uint32_t rank, const GemmParams& p,
+                                              const Sched8& sc) {
+    Tile8 tl;
+    const int64_t h0 = static_cast<int64_t>(t) * sc.H / sc.N;
+    const int64_t h1 = static_cast<int64_t>(t + 1) * sc.H / sc.N;
+    int nt;
+    if (h1 > h0) {
+        const int j = static_cast<int>(h0);
+        const int g = find_group8(sc.hs, sc.GG, j / p.MT);
+        const int ntg = sc.hs[g + 1] - sc.hs[g];
+        const int l = j - sc.hs[g] * p.MT;
+        tl.g = g;
+        tl.m = l / ntg;
+        nt = l - tl.m * ntg;
+    } else {
+        const int j = t - static_cast<int>(h0);
+        const int g = find_group8(sc.cs, sc.GG, j / p.MT);
+        tl.g = g;
+        tl.m = j - sc.cs[g] * p.MT;
+        nt = 0;
+    }
+    tl.n_valid = min(kTile8, sc.gcnt[tl.g] - nt * kTile8);
+    tl.half = min(kTile8, max(64, (tl.n_valid + 31) & ~31)) >> 1;
+    tl.brow = sc.goff[tl.g] + nt * kTile8;
+    tl.arow = tl.g * p.M + tl.m * 2 * gemm_rows(MODE) + static_cast<int>(rank) * gemm_rows(MODE);
+    return tl;
+}
+
+__device__ __forceinline__ int b_rows8(const Tile8& tl, uint32_t rank) {
+    return min(max(tl.n_valid - static_cast<int>(rank) * tl.half, 0), tl.half);
+}
+
+__device__ __forceinline__ void raise_timeout8(const GemmParams& p, volatile int* abort, int where) {
+    atomicOr(p.status, STATUS_TIMEOUT);
+    atomicMax(p.status + 1, where);
+    *abort = 1;
+}
+
+// bf16 row pairs of one token per 4-byte store (as in the other SM-pair
+// epilogues): lanes 2i, 2i + 1 hold rows r, r + 1 for the same tokens.
+template <int N>
+__device__ __forceinline__ void store_pairs8(const float (&h)[N], int lane, __nv_bfloat16* at,
+                                             int64_t ld, int n_left, bool row_ok) {
+    const int odd = lane & 1;
+    uint32_t pk[N / 2];
+#pragma unroll
+    for (int jj = 0; jj < N / 2; ++jj) {
+        const float other = __shfl_xor_sync(0xffffffffu, odd ? h[2 * jj] : h[2 * jj + 1], 1);
+        const float mine = odd ? h[2 * jj + 1] : h[2 * jj];
+        const __nv_bfloat162 b = __floats2bfloat162_rn(odd ? other : mine, odd ? mine : other);
+        pk[jj] = *reinterpret_cast<const uint32_t*>(&b);
+    }
+    uint32_t* y = reinterpret_cast<uint32_t*>(at + odd * ld);
+#pragma unroll
+    for (int jj = 0; jj < N / 2; ++jj)
+        if (row_ok && 2 * jj + odd < n_left) y[jj * ld] = pk[jj];
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_constant__ GemmParams p) {
+    constexpr bool kPair = MODE == GEMM_SWIGLU;  // 64 gate + 64 up weight rows per CTA
+    constexpr int kRowsCta = gemm_rows(MODE);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+    uint8_t* scring = smem + kStages8 * kStage8;
+    float* xbuf = reinterpret_cast<float*>(scring + kScSlots8 * kScSlot8);
+    uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xbuf) + kXBytes8);
+    uint64_t* empty = full + kStages8;
+    uint64_t* scfull = empty + kStages8;
+    uint64_t* scempty = scfull + kScSlots8;
+    uint64_t* tfull = scempty + kScSlots8;
+    uint64_t* tempty = tfull + 2;
+    uint64_t* xfull = tempty + 2;
+    uint64_t* xempty = xfull + 2;
+    uint64_t* drain = xempty + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + kBarriers8);
+    volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    const int GG = p.G;
+    int* hs = reinterpret_cast<int*>(tmem_slot + 4);
+    int* cs = hs + GG + 1;
+    int* gcnt = cs + GG + 1;
+    int* goff = gcnt + GG;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+
+    if (warp == 0) {
+        // per group: token tiles if hot (several), 1 in the cold count if cold
+        const int per = (GG + 31) / 32;
+        const int g0 = lane * per;
+        int local_h = 0, local_c = 0;
+        for (int g = g0; g < min(g0 + per, GG); ++g) {
+            const int c = p.cnt[g];
+            gcnt[g] = c;
+            goff[g] = p.off[g];
+            const int ntg = (c + kTile8 - 1) / kTile8;
+            if (ntg > 1) local_h += ntg; else local_c += ntg;
+        }
+        int incl_h = local_h, incl_c = local_c;
+#pragma unroll
+        for (int s = 1; s < 32; s <<= 1) {
+            const int vh = __shfl_up_sync(0xffffffffu, incl_h, s);
+            const int vc = __shfl_up_sync(0xffffffffu, incl_c, s);
+            if (lane >= s) {
+                incl_h += vh;
+                incl_c += vc;
+            }
+        }
+        int run_h = incl_h - local_h, run_c = incl_c - local_c;
+        for (int g = g0; g < min(g0 + per, GG); ++g) {
+            hs[g] = run_h;
+            cs[g] = run_c;
+            const int ntg = (gcnt[g] + kTile8 - 1) / kTile8;
+            if (ntg > 1) run_h += ntg; else run_c += ntg;
+        }
+        if (lane == 31) {
+            hs[GG] = incl_h;
+            cs[GG] = incl_c;
+        }
+    } else if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, kTmemCols8);
+        tmem_relinquish_pair();
+    } else if (threadIdx.x == 64) {
+        for (int s = 0; s < kStages8; ++s) {
+            mbar_init(&full[s], 1 + 2 * 4);  // producer + the scale writers of both CTAs
+            mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < kScSlots8; ++s) {
+            mbar_init(&scfull[s], 1);
+            mbar_init(&scempty[s], 4);  // the 4 scale writers, after the slot's last K block
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&tfull[a], 1);
+            mbar_init(&tempty[a], 8);  // 4 epilogue warps in each CTA
+            mbar_init(&xfull[a], 1);
+            mbar_init(&xempty[a], 1);
+        }
+        mbar_init(drain, 1);
+        *abort = 0;
+        fence_mbar_init();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const Sched8 sched{hs, cs, gcnt, goff, GG, static_cast<int64_t>(hs[GG]) * p.MT,
+                       static_cast<int64_t>(hs[GG] + cs[GG]) * p.MT};
+    const int total = static_cast<int>(sched.N);
+    const uint64_t tmo = p.timeout_ns;
+    const int cid = static_cast<int>(cluster_id_x());
+    const int ncl = static_cast<int>(nclusters_x());
+    auto tile_at = [&](int j) -> int {
+        const int64_t t = cid + static_cast<int64_t>(j) * ncl;
+        return t < total ? static_cast<int>(t) : -1;
+    };
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------- TMA producer (both CTAs) ----------------
+            tma_prefetch_desc(&p.a0);
+            tma_prefetch_desc(&p.b32);
+            const uint64_t pol_w = l2_policy_evict_first();
+            const uint64_t pol_x = l2_policy_evict_last();
+            int stage = 0, ss = 0;
+            uint32_t phase = 0, sph = 0;
+            uint32_t issued = 0, last_par = 0, s_issued = 0, s_par = 0;
+            bool ok = p.stall_test == 0;
+            for (int j = 0; ok; ++j) {
+                const int t = tile_at(j);
+                if (t < 0) break;
+                const Tile8 tl = decode_tile8<MODE>(t, rank, p, sched);
+                // a CTA's token rows (loaded by warp 10): one 128-row box when they
+                // need three or four 32-row boxes (fewer copies), else 32-row boxes
+                auto boxes = [&](uint32_t r) {
+                    const int n = (b_rows8(tl, r) + 31) >> 5;
+                    return n >= 3 ? 4 : n;
+                };
+                const uint32_t expect = 2 * kA8 + (boxes(0) + boxes(1)) * kBox8;
+                for (int kb = 0; kb < p.KB; ++kb) {
+                    if (kb % kScKb == 0) {
+                        // the scales of K blocks kb .. kb + 3: weight rows, then both
+                        // halves of the tile's tokens
+                        if (!mbar_wait(&scempty[ss], sph ^ 1u, abort, tmo)) {
+                            if (!*abort) raise_timeout8(p, abort, 40);
+                            ok = false;
+                            break;
+                        }
+                        uint8_t* sc = scring + ss * kScSlot8;
+                        mbar_arrive_expect_tx(&scfull[ss], kScA8 + 2 * 128 * 16);
+                        const int x = kb * (kK8 / 32);
+                        if constexpr (kPair) {
+                            tma_load_2d(sc, &p.sa0, &scfull[ss], x, tl.arow, pol_w);
+                            tma_load_2d(sc + kScA8 / 2, &p.sa1, &scfull[ss], x, tl.arow, pol_w);
+                        } else {
+                            tma_load_2d(sc, &p.sa0, &scfull[ss], x, tl.arow, pol_w);
+                        }
+                        tma_load_2d(sc + kScA8, &p.sb_scale, &scfull[ss], x, tl.brow, pol_x);
+                        tma_load_2d(sc + kScA8 + 128 * 16, &p.sb_scale, &scfull[ss], x,
+                                    tl.brow + tl.half, pol_x);
+                        s_issued |= 1u << ss;
+                        s_par = (s_par & ~(1u << ss)) | (sph << ss);
+                        if (++ss == kScSlots8) {
+                            ss = 0;
+                            sph ^= 1u;
+                        }
+                    }
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort, tmo)) {
+                        if (!*abort) raise_timeout8(p, abort, 41);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + stage * kStage8;
+                    if (leader) mbar_arrive_expect_tx(&full[stage], expect);
+                    const uint32_t bar = map_to_rank(&full[stage], 0);
+                    if constexpr (kPair) {
+                        tma_load_2d_pair(st, &p.a0, bar, kb * kK8, tl.arow, pol_w);
+                        tma_load_2d_pair(st + kA8 / 2, &p.a1, bar, kb * kK8, tl.arow, pol_w);
+                    } else {
+                        tma_load_2d_pair(st, &p.a0, bar, kb * kK8, tl.arow, pol_w);
+                    }
+                    issued |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == kStages8) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (leader)
+                for (int s = 0; s < kStages8; ++s)
+                    if (issued & (1u << s))
+                        if (!mbar_wait(&full[s], (last_par >> s) & 1u, nullptr, tmo))
+                            raise_timeout8(p, abort, 42);
+            for (int s = 0; s < kScSlots8; ++s)
+                if (s_issued & (1u << s))
+                    if (!mbar_wait(&scfull[s], (s_par >> s) & 1u, nullptr, tmo))
+                        raise_timeout8(p, abort, 43);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ---------------- MMA issuer (leader only) ----------------
+            int stage = 0, acc = 0;
+            uint32_t phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int j = 0; ok; ++j) {
+                const int t = tile_at(j);
+                if (t < 0) break;
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort, tmo)) {
+                    if (!*abort) raise_timeout8(p, abort, 44);
+                    break;
+                }
+                tc_fence_after();
+                const Tile8 tl = decode_tile8<MODE>(t, rank, p, sched);
+                const uint32_t d0 = tmem_base + acc * kAcc8;
+                const uint32_t idesc = idesc_mx8(2 * BM, 2 * tl.half);
+                for (int kb = 0; kb < p.KB; ++kb) {
+                    if (!mbar_wait(&full[stage], phase, abort, tmo)) {
+                        if (!*abort) raise_timeout8(p, abort, 45);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_addr(smem + stage * kStage8);
+                    const uint64_t da = sdesc_kmajor_sw128(sa);
+                    const uint64_t db = sdesc_kmajor_sw128(sa + kA8);
+                    const uint32_t sfa = tmem_base + kSfCol8 + stage * kSfStage8;
+#pragma unroll
+                    for (int k = 0; k < kK8 / 32; ++k)
+                        umma_mx8_pair(d0, da + 2 * k, db + 2 * k, idesc_mx8_step(idesc, k), sfa,
+                                      sfa + 4, (kb | k) != 0);
+                    umma_commit_pair(&empty[stage], 0x3);
+                    if (++stage == kStages8) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                umma_commit_pair(&tfull[acc], 0x3);
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
+                }
+            }
+            umma_commit_pair(drain, 0x1);
+            if (!mbar_wait(drain, 0, nullptr, tmo)) raise_timeout8(p, abort, 46);
+        }
+    } else if (warp == 10) {
+        if (lane == 0) {
+            // ---------------- token TMA producer (both CTAs) ----------------
+            // The token tiles come from a thread of their own: one thread
+            // issuing every copy of a K block was the pipeline's limit.
+            const uint64_t pol_x = l2_policy_evict_last();
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = p.stall_test == 0;
+            for (int j = 0; ok; ++j) {
+                const int t = tile_at(j);
+                if (t < 0) break;
+                const Tile8 tl = decode_tile8<MODE>(t, rank, p, sched);
+                const int nb = (b_rows8(tl, rank) + 31) >> 5;
+                const int nbox = nb >= 3 ? 4 : nb;
+                const int brow = tl.brow + static_cast<int>(rank) * tl.half;
+                for (int kb = 0; kb < p.KB; ++kb) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, abort, tmo)) {
+                        if (!*abort) raise_timeout8(p, abort, 52);
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + stage * kStage8;
+                    const uint32_t bar = map_to_rank(&full[stage], 0);
+                    if (nbox == 4) {
+                        tma_load_2d_pair(st + kA8, &p.b, bar, kb * kK8, brow, pol_x);
+                    } else {
+                        for (int i = 0; i < nbox; ++i)
+                            tma_load_2d_pair(st + kA8 + i * kBox8, &p.b32, bar, kb * kK8, brow + 32 * i,
+                                             pol_x);
+                    }
+                    if (++stage == kStages8) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // its copies complete on the leader's full barriers, which the
+            // weight producer waits out before the block exits
+        }
+    } else if (warp >= 6) {
+        // ---------------- scale writers (warps 6..9, both CTAs) ----------------
+        // Warp of lane quadrant q writes, for each K block, the weight-row scales
+        // of rows 32q .. 32q + 31 (lane r, column r / 32) and the scales of all
+        // N token columns (lane 32q + n % 32, column 4 + n / 32) into the stage's
+        // TMEM scale columns, after the stage's previous MMAs completed.
+        const int q = warp & 3;
+        const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
+        auto wait_all = [&](uint64_t* bar, uint32_t par, int where) {
+            if (__all_sync(0xffffffffu, mbar_wait(bar, par, abort, tmo))) return true;
+            if (lane == 0 && !*abort) raise_timeout8(p, abort, where);
+            return false;
+        };
+        int stage = 0;
+        uint32_t phase = 0;
+        int64_t i = 0;  // K blocks done, over the pair's tile sequence
+        bool ok = true;
+        for (int j = 0; ok; ++j) {
+            const int t = tile_at(j);
+            if (t < 0) break;
+            const Tile8 tl = decode_tile8<MODE>(t, rank, p, sched);
+            const int n_cols = 2 * tl.half;
+            for (int kb = 0; kb < p.KB; ++kb, ++i) {
+                const int ss = static_cast<int>((i / kScKb) % kScSlots8);
+                const uint32_t sph = static_cast<uint32_t>((i / kScKb / kScSlots8) & 1);
+                if (!wait_all(&scfull[ss], sph, 47) || !wait_all(&empty[stage], phase ^ 1u, 48)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* sc = scring + ss * kScSlot8;
+                const int kq = kb % kScKb;
+                const uint32_t sf = tmem_base + lane_base + kSfCol8 + stage * kSfStage8;
+                tmem_st1(sf + q, *reinterpret_cast<const uint32_t*>(sc + (32 * q + lane) * 16 + kq * 4));
+                uint32_t bw[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const int n = 32 * c + lane;  // token column of the MMA
+                    const int r = n < tl.half ? n : 128 + n - tl.half;
+                    bw[c] = n < n_cols ? *reinterpret_cast<const uint32_t*>(sc + kScA8 + r * 16 + kq * 4)
+                                       : 0x7F7F7F7Fu;
+                }
+                tmem_st8(sf + 4, bw);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    // CTA-scope release: the scales are read by the pair's MMA from
+                    // this CTA's own TMEM, after the fence above
+                    if (leader)
+                        mbar_arrive(&full[stage]);
+                    else
+                        mbar_arrive_operand_ready(map_to_rank(&full[stage], 0));
+                    if (kq == kScKb - 1) mbar_arrive(&scempty[ss]);
+                }
+                if (++stage == kStages8) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else {
+        // ---------------- epilogue (warps 2..5, both CTAs) ----------------
+        // Warp q reads accumulator lanes [32q, 32q + 32).  gate/up: warps 0, 1
+        // hold gate rows and warps 2, 3 the matching up rows, which they pass
+        // on through xbuf.
+        const int q = warp & 3;
+        const int pr = q & 1;
+        const bool up_warp = q >= 2;
+        int acc = 0;
+        uint32_t acc_phase = 0, xph = 0;
+        bool ok = true;
+        for (int j = 0; ok; ++j) {
+            const int t = tile_at(j);
+            if (t < 0) break;
+            const Tile8 tl = decode_tile8<MODE>(t, rank, p, sched);
+            if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort, tmo))) {
+                if (lane == 0 && !*abort) raise_timeout8(p, abort, 49);
+                break;
+            }
+            tc_fence_after();
+            const int row = tl.m * 2 * kRowsCta + static_cast<int>(rank) * kRowsCta +
+                            (kPair ? pr : q) * 32 + lane;
+            const bool row_ok = row < p.M;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAcc8;
+            for (int c0 = 0; c0 < tl.n_valid && ok; c0 += 32) {
+                float v[32];
+                tmem_ld32(taddr + c0, v);
+                tmem_ld_wait();
+                tmem_regs_ready(v);
+                if constexpr (kPair) {
+                    float* xb = xbuf + pr * 32 * kXPad8 + lane * kXPad8;
+                    if (up_warp) {
+                        if (!__all_sync(0xffffffffu, mbar_wait(&xempty[pr], xph ^ 1u, abort, tmo))) {
+                            if (lane == 0 && !*abort) raise_timeout8(p, abort, 50);
+                            ok = false;
+                            break;
+                        }
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) xb[jj] = v[jj];
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&xfull[pr]);
+                    } else {
+                        if (!__all_sync(0xffffffffu, mbar_wait(&xfull[pr], xph, abort, tmo))) {
+                            if (lane == 0 && !*abort) raise_timeout8(p, abort, 51);
+                            ok = false;
+                            break;
+                        }
+                        float h[32];
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj) h[jj] = swiglu(v[jj], xb[jj]);
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&xempty[pr]);
+                        store_pairs8<32>(h, lane,
+                                         static_cast<__nv_bfloat16*>(p.out) +
+                                             static_cast<int64_t>(tl.brow + c0) * p.ldo + (row & ~1),
+                                         p.ldo, tl.n_valid - c0, row_ok);
+                    }
+                    xph ^= 1u;
+                } else {
+                    store_pairs8<32>(v, lane,
+                                     static_cast<__nv_bfloat16*>(p.out) +
+                                         static_cast<int64_t>(tl.brow + c0) * p.ldo + (row & ~1),
+                                     p.ldo, tl.n_valid - c0, row_ok);
+                }
+            }
+            if (!ok) break;
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(map_to_rank(&tempty[acc], 0));
+            if (++acc == 2) {
+                acc = 0;
+                acc_phase ^= 1u;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols8);
+    }
+}
+
+size_t mx8_smem_bytes(int GG) {
+    return 1024 + kStages8 * kStage8 + kScSlots8 * kScSlot8 + kXBytes8 + kBarriers8 * 8 + 16 +
+           static_cast<size_t>(4 * GG + 2) * 4;
+}
+
+template <int MODE>
+cudaError_t launch_mx8_mode(const GemmParams& p, int clusters, cudaStream_t s) {
+    const size_t smem = mx8_smem_bytes(p.G);
+    cudaError_t e = cudaFuncSetAttribute(mx8_pair_kernel<MODE>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * clusters, 1, 1);
+    cfg.blockDim = dim3(kThreads8, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int resident = 0;
+    e = cudaOccupancyMaxActiveClusters(&resident, mx8_pair_kernel<MODE>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (resident <= 0) return cudaErrorInvalidConfiguration;
+    if (clusters > resident) {
+        clusters = resident;
+        cfg.gridDim = dim3(2 * clusters, 1, 1);
+    }
+    return cudaLaunchKernelEx(&cfg, mx8_pair_kernel<MODE>, p);
+}
+
+}  // namespace
+
+int mx8_tile_tokens() { return kTile8; }
+int mx8_k_block() { return kK8; }
+
+cudaError_t launch_mx8_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s) {
+    if (p.G > kMaxGroups8 || p.has_shared || clusters <= 0 || !p.cnt || !p.off)
+        return cudaErrorInvalidValue;
+    if (p.KB % kScKb) return cudaErrorInvalidValue;  // scale slots never straddle tiles
+    if (mode == GEMM_SWIGLU) return launch_mx8_mode<GEMM_SWIGLU>(p, clusters, s);
+    if (mode == GEMM_DOWN) return launch_mx8_mode<GEMM_DOWN>(p, clusters, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

@@ -101,6 +101,9 @@ struct GemmParams {
     // (64 gate rows then the same 64 up rows per block; 128-row boxes); the
     // CTA's 128 operand rows are one box at packed row 2 * arow.
     int32_t a_packed;
+    // MXFP8 x MXFP8 GEMMs (gemm_mx8.cu): the token rows' E8M0 scales, one per
+    // 32 along K ([rows][K/32] bytes, 16-byte x 128-row boxes).
+    CUtensorMap sb_scale;
 };
 
 size_t gemm_smem_bytes(int mode, int n_groups_total);
@@ -117,6 +120,23 @@ cudaError_t launch_grouped_gemm(int mode, const GemmParams& p, int grid, cudaStr
 // weight-streaming variant with 64-token tiles and a deeper weight ring.
 cudaError_t launch_pair_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s,
                              int wfmt = 0, int small = 0);
+
+// The expert GEMMs with MXFP8 weights and MXFP8 token rows (gemm_mx8.cu), on the
+// block-scaled tensor-core MMA: a0/a1 (gate, up) or a0 (down) map the E4M3
+// weights with 128-byte boxes and the 128-byte swizzle (64 or 128 rows), sa0/sa1
+// their E8M0 scales (16-byte boxes); b32 the gathered E4M3 token rows (128-byte
+// boxes of 32 rows, swizzled) and sb_scale their scales (16-byte x 128-row
+// boxes); K is in blocks of mx8_k_block() (KB a multiple of 4); tiles of at most
+// mx8_tile_tokens() tokens; no shared expert.
+cudaError_t launch_mx8_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s);
+int mx8_tile_tokens();
+int mx8_k_block();
+// MXFP8 quantisation of R rows of K bf16 values (K % 256 == 0) in blocks of 32
+// along the row: E4M3 codes to codes [R][K] and E8M0 scale bytes to scales
+// [R][K/32] (OCP MX v1.0: X = floor(log2 max|v|) - 8, codes E4M3(v / 2^X)
+// nearest even, saturating; scale byte X + 127).
+cudaError_t launch_mx_rows_fp8(const uint16_t* src, uint8_t* codes, uint8_t* scales, int64_t R,
+                               int K, int sms, cudaStream_t s);
 
 // Routing: top-k selection (own mode) or replay validation, then gate weights.
 cudaError_t launch_topk_gates(const float* logits, int64_t T, int E, int k,
@@ -235,10 +255,6 @@ cudaError_t launch_router_wgrad(const uint16_t* xp, const int32_t* perm, const i
 cudaError_t launch_dx_assemble(const float* dxp, const int32_t* inv, float* dx, int64_t T, int k,
                                int d, int n_shared, int sms, cudaStream_t s);
 
-// MXFP8 activations: R rows of K bf16 values (K % 256 == 0) quantised along
-// the row in blocks of 32, written as the exact bf16 values to dst (may be src).
-cudaError_t launch_mx_rows(const uint16_t* src, uint16_t* dst, int64_t R, int K, int sms,
-                           cudaStream_t s);
 
 // Packed gate/up weights: G matrices pairs [F][d] (gate, up) -> [G][F/64][128][d]
 // (64 gate rows, then the same 64 up rows).  gate[g], up[g] are the g-th

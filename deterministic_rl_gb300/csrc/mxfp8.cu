@@ -4,8 +4,9 @@
 // tokens are quantised to MXFP8 before dispatch, and the expert compute runs
 // in MXFP8.  With MXFP8 weights, each token row of x is quantised along d and
 // each row of the SwiGLU output h (stored in bf16) along F, in blocks of 32
-// (mx.cuh); the expert GEMMs then multiply the exact MXFP8 values of both
-// operands.
+// (mx.cuh), into E4M3 codes and E8M0 scale bytes; the expert GEMMs then
+// multiply the MXFP8 values of both operands on the block-scaled tensor-core
+// MMA (gemm_mx8.cu).
 #include <cuda_bf16.h>
 
 #include <cstdint>
@@ -26,17 +27,18 @@ __device__ __forceinline__ void unpack8_bf16(const uint4& u, float (&v)[8]) {
 }
 
 // One warp per (row, 256-column chunk): lane l holds columns 8l .. 8l + 7, so
-// a block of 32 is held by lanes 4i .. 4i + 3.  src and dst may be the same
-// rows (each lane reads its 8 values before it writes them).
-__global__ void __launch_bounds__(256) mx_rows_kernel(const uint4* src, uint4* dst, int64_t R,
-                                                      int K) {
+// a block of 32 is held by lanes 4i .. 4i + 3.  Each lane writes its 8 E4M3
+// codes, and the first lane of each block the block's E8M0 scale byte X + 127.
+__global__ void __launch_bounds__(256) mx_rows_fp8_kernel(const uint4* src, uint2* codes,
+                                                          uint8_t* scales, int64_t R, int K) {
     const int lane = threadIdx.x & 31;
     const int chunks = K / 256;
     const int64_t items = R * chunks;
     for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i < items;
          i += (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5) {
         const int64_t r = i / chunks;
-        const int64_t at = (r * K + static_cast<int64_t>(i % chunks) * 256 + lane * 8) / 8;
+        const int c = static_cast<int>(i % chunks);
+        const int64_t at = (r * K + static_cast<int64_t>(c) * 256 + lane * 8) / 8;
         float v[8];
         unpack8_bf16(src[at], v);
         float m = 0.0f;
@@ -44,21 +46,29 @@ __global__ void __launch_bounds__(256) mx_rows_kernel(const uint4* src, uint4* d
         for (int j = 0; j < 8; ++j) m = fmaxf(m, fabsf(v[j]));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
         m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-        dst[at] = mx_qdq8(v, mx_block_exp(m));
+        const int X = mx_block_exp(m);
+        const float inv = exp2i(-X);
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            w[j] = __nv_cvt_float2_to_fp8x2(make_float2(v[2 * j] * inv, v[2 * j + 1] * inv),
+                                            __NV_SATFINITE, __NV_E4M3);
+        codes[at] = make_uint2(w[0] | (w[1] << 16), w[2] | (w[3] << 16));
+        if ((lane & 3) == 0) scales[r * (K / 32) + c * 8 + (lane >> 2)] = static_cast<uint8_t>(X + 127);
     }
 }
 
 }  // namespace
 
-cudaError_t launch_mx_rows(const uint16_t* src, uint16_t* dst, int64_t R, int K, int sms,
-                           cudaStream_t s) {
+cudaError_t launch_mx_rows_fp8(const uint16_t* src, uint8_t* codes, uint8_t* scales, int64_t R,
+                               int K, int sms, cudaStream_t s) {
     if (K % 256) return cudaErrorInvalidValue;
     if (R == 0) return cudaSuccess;
     int64_t blocks = (R * (K / 256) + 7) / 8;  // 8 warps per block
     const int64_t cap = static_cast<int64_t>(sms) * 8;
     if (blocks > cap) blocks = cap;
-    mx_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-        reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), R, K);
+    mx_rows_fp8_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
+        reinterpret_cast<const uint4*>(src), reinterpret_cast<uint2*>(codes), scales, R, K);
     return cudaGetLastError();
 }
 

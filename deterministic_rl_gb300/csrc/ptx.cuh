@@ -336,6 +336,59 @@ __device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t a_desc,
         : "memory");
 }
 
+// ---- block-scaled MMA (MXFP8 x MXFP8) ---------------------------------------------
+
+// Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale with A and B
+// E4M3, K-major, E8M0 scales: N / 8 at bits 17-22, scale type E8M0 at bit 23,
+// M / 16 at bits 24-28; the scale bytes of a K step (scale_vec::1X: one per
+// row per 32 along K) are picked by the ids at bits 29-30 (A) and 4-5 (B), see
+// idesc_mx8_step.  Checked on the GPU against exact sums of E4M3 products.
+__host__ __device__ constexpr uint32_t idesc_mx8(int M, int N) {
+    return (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// The descriptor of K step k (0..3) of a 128-wide K block: byte k of each
+// 32-bit scale word in TMEM holds that step's scale.
+__host__ __device__ constexpr uint32_t idesc_mx8_step(uint32_t idesc, int k) {
+    return idesc | (static_cast<uint32_t>(k) << 29) | (static_cast<uint32_t>(k) << 4);
+}
+
+// Leader CTA, single thread: D (+)= (A x 2^sa) . (B x 2^sb)^T over the CTA pair,
+// A and B E4M3 in shared memory (K = 32 per instruction), their per-32 E8M0
+// scales in TMEM.  Scale layout (measured on the GPU with marker scales): the
+// scale of A row r (0..127 in each CTA) is read from lane r, column sfa + r/32
+// of that CTA's TMEM; that of B column n (0..N-1) by the rows of TMEM lane
+// quadrant q from lane 32q + n % 32, column sfb + n / 32 of each CTA's TMEM,
+// so B's scales are written to all four quadrants of both CTAs.
+__device__ __forceinline__ void umma_mx8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+        "r"(accumulate)
+        : "memory");
+}
+
+// Whole warp: lane i writes 1 (or 8) consecutive 32-bit columns of TMEM lane
+// (taddr's lane + i); the warp's lane quadrant must be taddr's.
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&v)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+                     taddr),
+                 "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Leader CTA, single thread: when its prior MMAs complete, arrive once on the
 // mbarrier at this shared offset in every CTA of `cta_mask`.
 __device__ __forceinline__ void umma_commit_pair(uint64_t* bar, uint16_t cta_mask) {

@@ -139,7 +139,12 @@ class MoELayer:
         if self.n_shared:
             r["ysh"] = view(L.ysh, T * d, torch.float32).view(T, d)
         if self.wfmt == B.MOE_W_MXFP8_ACT:
-            r["xq"] = view(L.xq, T * d, torch.bfloat16).view(T, d)
+            # E4M3 codes and E8M0 scales of the quantised token rows and of h
+            r["x8"] = view(L.xq, T * d, torch.uint8).view(T, d)
+            r["xs"] = ws[L.xq + T * d:L.xq + T * d + T * d // 32].view(T, d // 32)
+            r["xp8"] = view(L.xp, T * k * d, torch.uint8).view(T * k, d)
+            r["h8"] = view(L.hq, T * k * F, torch.uint8).view(T * k, F)
+            r["hs"] = ws[L.hq + T * k * F:L.hq + T * k * F + T * k * F // 32].view(T * k, F // 32)
         if self.wfmt == B.MOE_W_NVFP4:
             r["xq"] = view(L.xq, T * d, torch.bfloat16).view(T, d)
             r["sx"] = view(L.sx, T, torch.float32)

@@ -173,10 +173,15 @@ typedef struct {
  *   sxp      fp32 [T*k]    the scale of each gathered row of xp
  *   sh       fp32 [T*k]    the scale of each row of h (h itself then holds
  *                          e2m1 * e4m3 of the quantised activations)
+ *   MOE_W_MXFP8_ACT: the MXFP8 activations as E4M3 codes and E8M0 scales:
+ *   xq       u8 [T][d] codes, then u8 [T][d/32] scales of each token row of x
+ *   xp       u8 [T*k][d] codes, then u8 [T*k][d/32] scales: the gathered rows
+ *   hq       u8 [T*k][F] codes, then u8 [T*k][F/32] scales of each row of h
  * Offsets are 256-byte aligned; `total` equals moe_workspace_size(dims). */
 typedef struct {
     size_t status, logits, valid, cnt, off, perm, inv, xp, h, y, ysh;
     size_t xq, sx, sxp, sh;
+    size_t hq;
     size_t total;
 } moe_ws_layout;
 

@@ -1,11 +1,12 @@
 """MXFP8 expert compute (MXFP8 weights and MXFP8 activations: each token row
 quantised along d before the gate/up GEMM, each bf16 row of the SwiGLU output
-along F before the down GEMM; the pages' MXFP8 format) on the GPU path.
+along F before the down GEMM; the pages' MXFP8 format) on the GPU path, where
+both expert GEMMs run on the block-scaled tensor-core MMA.
 
-The quantised activations are bitwise the oracle's quantisation of the same
-rows; the layer matches the oracle within the usual tolerance, equals the
-MXFP8-weight layer fed with the quantised rows where that is exact, and keeps
-batch invariance and run-to-run determinism."""
+The quantised activations (E4M3 codes and E8M0 scales) decode bitwise to the
+oracle's quantisation of the same rows; the layer matches the oracle within
+the usual tolerance and keeps batch invariance (across every tile width) and
+run-to-run determinism."""
 import numpy as np
 import pytest
 import torch
@@ -23,6 +24,13 @@ pytestmark = pytest.mark.gpu
 def _built():
     build.build()
     oracle.build()
+
+
+def _decoded(codes, scales):
+    """E4M3 codes times 2^(E8M0 scale - 127), one scale per 32 codes (fp64)."""
+    v = codes.contiguous().view(torch.float8_e4m3fn).to(torch.float64).cpu().numpy()
+    e = (scales.to(torch.int64) - 127).repeat_interleave(32, dim=-1).cpu().numpy()
+    return np.ldexp(v, e)  # exact (a power-of-two multiply on the host)
 
 
 def small_mxa(T=300, E=32, seed=43):
@@ -45,8 +53,12 @@ def test_mxfp8_activations_match_oracle(T):
     mc.check_gates(gates_r.cpu().numpy(), ref_r.gates)
     mc.check_out(out_r.cpu().numpy(), ref_r.out)
     # the token rows entering the experts: the oracle's quantisation, bitwise
-    xq = layer.intermediates(T)["xq"].to(torch.float64).cpu().numpy()
-    np.testing.assert_array_equal(xq, oracle.mx_qdq_rows(inp.x.to(torch.float64).cpu().numpy()))
+    im = layer.intermediates(T)
+    np.testing.assert_array_equal(_decoded(im["x8"], im["xs"]),
+                                  oracle.mx_qdq_rows(inp.x.to(torch.float64).cpu().numpy()))
+    # and the rows of h entering the down GEMM: h8 / hs are h's quantisation
+    h = im["h"][: T * 8].to(torch.float64).cpu().numpy()
+    np.testing.assert_array_equal(_decoded(im["h8"], im["hs"]), oracle.mx_qdq_rows(h))
 
 
 def test_quantised_rows_feed_the_mxfp8_weight_layer():
@@ -91,7 +103,8 @@ def test_mxfp8_activations_full_size_sampled():
     ref = mc.oracle_layer(inp, tokens=tokens)
     same = mc.check_ids(ids.cpu().numpy()[tokens], ref.logits, 8)
     mc.check_out(out.cpu().numpy()[tokens][same], ref.out[same])
-    xq = layer.intermediates(cfg.T)["xq"][torch.as_tensor(tokens, device="cuda")]
+    im = layer.intermediates(cfg.T)
+    tk = torch.as_tensor(tokens, device="cuda")
     np.testing.assert_array_equal(
-        xq.to(torch.float64).cpu().numpy(),
-        oracle.mx_qdq_rows(inp.x[torch.as_tensor(tokens, device="cuda")].to(torch.float64).cpu().numpy()))
+        _decoded(im["x8"][tk], im["xs"][tk]),
+        oracle.mx_qdq_rows(inp.x[tk].to(torch.float64).cpu().numpy()))
