@@ -60,9 +60,9 @@ def kernels_per_step(T, k, wfmt="bf16", act_mx=False):
     """Launches of one layer call: router GEMM, top-k, dispatch (one kernel for
     at most one segment of pairs, else histogram, scan and scatter), gather,
     gate/up, down, combine; NVFP4 and MXFP8 activations add the two activation
-    quantisers."""
+    quantisers and a second gather (codes, then block scales)."""
     n = 7 if T * k <= DISPATCH_SEGMENT_PAIRS else 9
-    return n + (2 if wfmt == "nvfp4" or act_mx else 0)
+    return n + (3 if wfmt == "nvfp4" or act_mx else 0)
 
 
 def launches_per_step(cfg):
@@ -127,6 +127,26 @@ def weight_bytes_per_value(cfg):
     return {"bf16": 2.0, "mxfp8": 1 + 1 / 32, "nvfp4": 0.5 + 1 / 16}[cfg.wfmt]
 
 
+def act_bytes_per_value(cfg):
+    """Bytes per value of the token rows the expert GEMMs read: bf16 2; MXFP8
+    activations 1 + an E8M0 scale per 32; NVFP4 1/2 + an E4M3 scale per 16."""
+    if cfg.wfmt == "nvfp4":
+        return 0.5 + 1 / 16
+    return 1 + 1 / 32 if cfg.act_mx else 2.0
+
+
+def mma_peak(cfg, bf16_tflops):
+    """The expert GEMMs' tensor peak for their operand type: the measured bf16
+    peak times the nominal dense ratio (fp8 4.5 / 2.25 = 2, fp4 13.5 / 2.25 =
+    6) for the block-scaled kinds; bf16 for the rest (MXFP8 weights with bf16
+    activations are dequantised to bf16)."""
+    if cfg.wfmt == "nvfp4":
+        return 6.0 * bf16_tflops, "fp4 (e2m1, block-scaled) = 6 x bf16"
+    if cfg.act_mx:
+        return 2.0 * bf16_tflops, "fp8 (e4m3, block-scaled) = 2 x bf16"
+    return bf16_tflops, "bf16"
+
+
 def layer_work(cfg, touched):
     """Algorithmic FLOPs and bytes of one layer call (touched = routed experts
     with at least one token)."""
@@ -147,14 +167,15 @@ def gate_up_bytes(cfg, touched, with_shared=True):
     S = cfg.n_shared if with_shared else 0
     rows = T * k + T * S
     wb = weight_bytes_per_value(cfg)
-    return (touched + S) * 2 * F * d * wb + rows * d * 2 + rows * F * 2
+    return (touched + S) * 2 * F * d * wb + rows * d * act_bytes_per_value(cfg) + rows * F * 2
 
 
 def down_bytes(cfg, touched):
     T, d, k, F, S = cfg.T, cfg.d, cfg.k, cfg.F, cfg.n_shared
     rows = T * k + T * S
     wb = weight_bytes_per_value(cfg)
-    return (touched + S) * d * F * wb + rows * F * 2 + T * k * d * 2 + S * T * d * 4
+    return ((touched + S) * d * F * wb + rows * F * act_bytes_per_value(cfg) + T * k * d * 2
+            + S * T * d * 4)
 
 
 class ClockSampler:
@@ -442,23 +463,31 @@ def time_forward(cfg, mode, K, warmup, world, local):
     pk, pk_kind = peaks()
     hbm = float(pk["hbm_gbs"])
     tensor = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    t_mma, mma_kind = mma_peak(cfg, tensor)
     # the dominant kernel: the grouped gate/up GEMM (+ SwiGLU)
     one_sm = cfg.wfmt == "bf16" and T <= ONE_SM_MAX_TOKENS
+    block_scaled = cfg.wfmt == "nvfp4" or cfg.act_mx
     # on SM pairs with bf16 weights the shared expert's gate/up runs on a second
     # stream beside the routing, outside the timed gate/up stage
     shared_in = not (cfg.n_shared and not one_sm and cfg.wfmt == "bf16")
     gu_bytes = gate_up_bytes(cfg, touched, shared_in)
     gu_flops = 4.0 * cfg.d * cfg.F * (T * cfg.k + (T * cfg.n_shared if shared_in else 0))
     gu_ms = stage_ms["gate_up"]
-    kname = ("grouped_gemm_kernel<GEMM_SWIGLU> (one-SM grouped gate/up GEMM + SwiGLU)" if one_sm
-             else f"pair_gemm_kernel<GEMM_SWIGLU, {cfg.wfmt}> (SM-pair grouped gate/up GEMM + SwiGLU)")
-    if gu_flops / (tensor * 1e12) > gu_bytes / (hbm * 1e9):
+    if one_sm:
+        kname = "grouped_gemm_kernel<GEMM_SWIGLU> (one-SM grouped gate/up GEMM + SwiGLU)"
+    elif block_scaled:
+        kname = (f"bs_pair_kernel<GEMM_SWIGLU, {'nvfp4' if cfg.wfmt == 'nvfp4' else 'mxfp8'}> "
+                 "(SM-pair block-scaled gate/up GEMM + SwiGLU)")
+    else:
+        kname = f"pair_gemm_kernel<GEMM_SWIGLU, {cfg.wfmt}> (SM-pair grouped gate/up GEMM + SwiGLU)"
+    if gu_flops / (t_mma * 1e12) > gu_bytes / (hbm * 1e9):
         achieved = gu_flops / (gu_ms / 1e3) / 1e12
-        roofline = {"bound": "tensor", "achieved": achieved, "peak": tensor, "unit": "TFLOP/s",
-                    "frac": achieved / tensor, "traffic": None,
-                    "algorithmic_flops_per_launch": gu_flops,
-                    "peak_source": f"{pk_kind} (MEASURED_PEAKS.json bf16_tflops, burst)"
-                    if pk_kind == "measured" else "fallback 1.9 PFLOP/s"}
+        roofline = {"bound": "tensor", "achieved": achieved, "peak": t_mma, "unit": "TFLOP/s",
+                    "frac": achieved / t_mma, "traffic": None,
+                    "algorithmic_flops_per_launch": gu_flops, "mma": mma_kind,
+                    "peak_source": (f"{pk_kind} (MEASURED_PEAKS.json bf16_tflops, burst)"
+                                    if pk_kind == "measured" else "fallback 1.9 PFLOP/s")
+                    + ("" if t_mma == tensor else f", scaled: {mma_kind}")}
     else:
         achieved = gu_bytes / (gu_ms / 1e3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
@@ -469,11 +498,16 @@ def time_forward(cfg, mode, K, warmup, world, local):
                     if pk_kind == "measured" else "fallback 6.8 TB/s"}
     roofline.update({"kernel": kname, "algorithmic_bytes_per_launch": gu_bytes,
                      "avg_launch_ms": gu_ms})
-    t_roof = max(flops / (tensor * 1e12), nbytes / (hbm * 1e9))
+    # the router GEMM runs in bf16, the expert GEMMs at their operand type's rate
+    r_flops = 2.0 * T * cfg.d * cfg.E
+    t_tensor = r_flops / (tensor * 1e12) + (flops - r_flops) / (t_mma * 1e12)
+    t_nom = r_flops / 2.25e15 + (flops - r_flops) / (2.25e15 * t_mma / tensor)
+    t_roof = max(t_tensor, nbytes / (hbm * 1e9))
     layer_roof = {"flops": flops, "bytes": nbytes, "touched_experts": touched,
-                  "bound": "tensor" if flops / (tensor * 1e12) > nbytes / (hbm * 1e9) else "hbm",
+                  "bound": "tensor" if t_tensor > nbytes / (hbm * 1e9) else "hbm",
                   "roofline_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_per_step,
-                  "frac_nominal_8tbs": 1e3 * max(flops / 2.25e15, nbytes / 8e12) / ms_per_step,
+                  "frac_nominal_8tbs": 1e3 * max(t_nom, nbytes / 8e12) / ms_per_step,
+                  "expert_mma": mma_kind,
                   "peaks": f"{pk_kind}: {hbm} GB/s, {tensor} TFLOP/s bf16"}
     return {"inp": inp, "layer": layer, "replay": replay, "outs": outs, "packed": packed,
             "value": value, "ms_per_step": ms_per_step, "nbytes": nbytes, "need_flush": need_flush,
@@ -485,7 +519,8 @@ def time_forward(cfg, mode, K, warmup, world, local):
 # same run: (workload, mode, zipf override or None).
 EXTRA_WORKLOADS = [("c3_prefill_zipf", "replay", None), ("c3_prefill_zipf", "own", None),
                    ("c4_train_32k", "own", None), ("c4_train_32k", "own", 1.2),
-                   ("c5_mxfp8", "own", None)]
+                   ("c5_mxfp8", "own", None), ("c5_mxfp8_act", "own", None),
+                   ("c6_nvfp4", "own", None)]
 
 
 def run_workloads(args, world, local):

@@ -82,13 +82,15 @@ Layout make_layout(const moe_dims* d) {
     L.ysh = take(S ? T * d->d * 4 : 0);
     const bool nv = d->wfmt == MOE_W_NVFP4;
     const bool mxa = d->wfmt == MOE_W_MXFP8_ACT;
-    // MXFP8 activations: E4M3 codes [T][d] then E8M0 scales [T][d/32] of x (and
-    // the gathered rows' codes and scales in xp, those of h in hq)
-    L.xq = take(nv ? T * d->d * 2 : (mxa ? T * d->d + T * d->d / 32 : 0));
+    // Narrow activations, codes then block scales: MXFP8 E4M3 codes [T][d] and
+    // E8M0 scales [T][d/32] of x; NVFP4 E2M1 codes [T][d/2] and E4M3 scales
+    // [T][d/16] (the gathered rows' codes and scales in xp, those of h in hq)
+    L.xq = take(nv ? T * d->d / 2 + T * d->d / 16 : (mxa ? T * d->d + T * d->d / 32 : 0));
     L.sx = take(nv ? T * 4 : 0);
     L.sxp = take(nv ? T * k * 4 : 0);
     L.sh = take(nv ? T * k * 4 : 0);
-    L.hq = take(mxa ? T * k * d->F + T * k * d->F / 32 : 0);
+    L.hq = take(mxa ? T * k * d->F + T * k * d->F / 32
+                    : (nv ? T * k * d->F / 2 + T * k * d->F / 16 : 0));
     L.total = o;
     return L;
 }
@@ -340,18 +342,21 @@ moe_status side_stream(SideStream** out) {
     return MOE_OK;
 }
 
-// MXFP8 weights and MXFP8 activations: every token row of x, and every row of
-// the SwiGLU output h, is quantised to E4M3 codes and E8M0 scales along K,
-// gathered as codes and scales, and both expert GEMMs run on the block-scaled
-// tensor-core MMA (gemm_mx8.cu).  Any batch size takes this one path, so the
-// result of a token never depends on its batch.
-moe_status run_experts_mx8(const moe_dims* d, const void* x, const moe_weights* w, void* out,
-                           const int32_t* ids, const float* gates, uint8_t* ws, const Layout& L,
-                           cudaStream_t s) {
+// Both expert GEMMs on the block-scaled tensor-core MMA (gemm_bs.cu): every
+// token row of x, and every row of the SwiGLU output h, is quantised along K
+// (MXFP8 weights and activations: E4M3 codes with E8M0 scales per 32; NVFP4:
+// E2M1 codes with E4M3 scales per 16 and an fp32 scale per row), gathered as
+// codes and scales, and multiplied by the narrow weights.  Any batch size
+// takes this one path, so the result of a token never depends on its batch.
+moe_status run_experts_bs(const moe_dims* d, const void* x, const moe_weights* w, void* out,
+                          const int32_t* ids, const float* gates, uint8_t* ws, const Layout& L,
+                          cudaStream_t s) {
     const int64_t T = d->T;
     const int k = d->k, E = d->E;
     const int64_t rows = T * k;
     const int D = d->d, F = d->F;
+    const bool nv = d->wfmt == MOE_W_NVFP4;
+    const int fmt = nv ? BS_NVFP4 : BS_MXFP8;
     int32_t* status = reinterpret_cast<int32_t*>(ws + L.status);
     int32_t* cnt = reinterpret_cast<int32_t*>(ws + L.cnt);
     int32_t* off = reinterpret_cast<int32_t*>(ws + L.off);
@@ -360,12 +365,18 @@ moe_status run_experts_mx8(const moe_dims* d, const void* x, const moe_weights* 
     const int sms = num_sms();
     if (sms <= 0) return MOE_ERR_CUDA;
     if (d->n_shared) return MOE_ERR_UNSUPPORTED;
-    uint8_t* x8 = ws + L.xq;                     // [T][D] codes, then [T][D/32] scales
-    uint8_t* xs = x8 + T * D;
-    uint8_t* xp8 = ws + L.xp;                    // gathered: [rows][D], then [rows][D/32]
-    uint8_t* xps = xp8 + rows * D;
-    uint8_t* h8 = ws + L.hq;                     // [rows][F] codes, then [rows][F/32] scales
-    uint8_t* hs = h8 + rows * F;
+    // bytes per row of codes and of scales, along d and along F
+    const int cd = nv ? D / 2 : D, sd = nv ? D / 16 : D / 32;
+    const int cf = nv ? F / 2 : F, sf = nv ? F / 16 : F / 32;
+    uint8_t* xc = ws + L.xq;                     // [T][cd] codes, then [T][sd] scales
+    uint8_t* xs = xc + T * cd;
+    uint8_t* xpc = ws + L.xp;                    // gathered: [rows][cd], then [rows][sd]
+    uint8_t* xps = xpc + rows * cd;
+    uint8_t* hc = ws + L.hq;                     // [rows][cf] codes, then [rows][sf] scales
+    uint8_t* hsc = hc + rows * cf;
+    float* sx = reinterpret_cast<float*>(ws + L.sx);    // NVFP4 row scales
+    float* sxp = reinterpret_cast<float*>(ws + L.sxp);
+    float* sh = reinterpret_cast<float*>(ws + L.sh);
     const uint64_t EF = uint64_t(E) * F, ED = uint64_t(E) * D;
     const int units = sms / 2;
 
@@ -374,15 +385,20 @@ moe_status run_experts_mx8(const moe_dims* d, const void* x, const moe_weights* 
                                reinterpret_cast<int32_t*>(ws + L.scratch), s)));
     MOE_TRY(mark(MOE_STAGE_DISPATCH, 1, s));
     MOE_TRY(mark(MOE_STAGE_GATHER, 0, s));
-    MOE_TRY(cu(launch_mx_rows_fp8(static_cast<const uint16_t*>(x), x8, xs, T, D, sms, s)));
-    // rows of codes and of scales moved as 2-byte units (D and D / 32 bytes)
-    MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(x8), inv, T, k, D / 2, 0,
-                             reinterpret_cast<uint16_t*>(xp8), s)));
-    MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(xs), inv, T, k, D / 64, 0,
+    if (nv)
+        MOE_TRY(cu(launch_nvfp4_codes(static_cast<const uint16_t*>(x), xc, xs, sx, T, D, sms, s)));
+    else
+        MOE_TRY(cu(launch_mx_rows_fp8(static_cast<const uint16_t*>(x), xc, xs, T, D, sms, s)));
+    // rows of codes and of scales moved as 2-byte units; NVFP4 rows take their
+    // token's fp32 scale along
+    MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(xc), inv, T, k, cd / 2, 0,
+                             reinterpret_cast<uint16_t*>(xpc), s, nv ? sx : nullptr,
+                             nv ? sxp : nullptr)));
+    MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(xs), inv, T, k, sd / 2, 0,
                              reinterpret_cast<uint16_t*>(xps), s)));
     MOE_TRY(mark(MOE_STAGE_GATHER, 1, s));
 
-    const int tn = mx8_tile_tokens(), kk = mx8_k_block();
+    const int tn = bs_tile_tokens(fmt), kk = 128, big = bs_big_box(fmt), sbox = bs_scale_box(fmt);
     const int64_t ntiles = (rows + tn - 1) / tn + E;
     auto common = [&](GemmParams& p) {
         p.cnt = cnt;
@@ -395,42 +411,54 @@ moe_status run_experts_mx8(const moe_dims* d, const void* x, const moe_weights* 
     GemmParams p1;
     std::memset(&p1, 0, sizeof p1);
     common(p1);
-    if (!make_map_u8(&p1.a0, w->w_gate, D, EF, kk, rg, true)) return MOE_ERR_CUDA;
-    if (!make_map_u8(&p1.a1, w->w_up, D, EF, kk, rg, true)) return MOE_ERR_CUDA;
-    if (!make_map_u8(&p1.sa0, w->s_gate, D / 32, EF, 16, rg)) return MOE_ERR_CUDA;
-    if (!make_map_u8(&p1.sa1, w->s_up, D / 32, EF, 16, rg)) return MOE_ERR_CUDA;
-    if (!make_map_u8(&p1.b, xp8, D, rows, kk, 128, true)) return MOE_ERR_CUDA;
-    if (!make_map_u8(&p1.b32, xp8, D, rows, kk, 32, true)) return MOE_ERR_CUDA;
-    if (!make_map_u8(&p1.sb_scale, xps, D / 32, rows, 16, 128)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p1.a0, w->w_gate, cd, EF, kk, rg, true)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p1.a1, w->w_up, cd, EF, kk, rg, true)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p1.sa0, w->s_gate, sd, EF, sbox, rg)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p1.sa1, w->s_up, sd, EF, sbox, rg)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p1.b, xpc, cd, rows, kk, big, true)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p1.b32, xpc, cd, rows, kk, 32, true)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p1.sb_scale, xps, sd, rows, sbox, 128)) return MOE_ERR_CUDA;
+    if (nv) {
+        p1.row_scale = sxp;
+        p1.wscale0 = w->gs_gate;
+        p1.wscale1 = w->gs_up;
+    }
     p1.M = F;
     p1.MT = F / (2 * static_cast<int>(rg));
-    p1.KB = D / kk;
+    p1.KB = cd / kk;
     p1.out = ws + L.h;
     p1.ldo = F;
     p1.stall_test = take_stall_test() ? 1 : 0;
     int64_t tb = ntiles * p1.MT;
     MOE_TRY(mark(MOE_STAGE_GATE_UP, 0, s));
-    MOE_TRY(cu(launch_mx8_gemm(GEMM_SWIGLU, p1, static_cast<int>(tb < units ? tb : units), s)));
+    MOE_TRY(cu(launch_bs_gemm(fmt, GEMM_SWIGLU, p1, static_cast<int>(tb < units ? tb : units), s)));
     MOE_TRY(mark(MOE_STAGE_GATE_UP, 1, s));
 
     GemmParams p2;
     std::memset(&p2, 0, sizeof p2);
     common(p2);
-    if (!make_map_u8(&p2.a0, w->w_down, F, ED, kk, BM, true)) return MOE_ERR_CUDA;
-    if (!make_map_u8(&p2.sa0, w->s_down, F / 32, ED, 16, BM)) return MOE_ERR_CUDA;
-    if (!make_map_u8(&p2.b, h8, F, rows, kk, 128, true)) return MOE_ERR_CUDA;
-    if (!make_map_u8(&p2.b32, h8, F, rows, kk, 32, true)) return MOE_ERR_CUDA;
-    if (!make_map_u8(&p2.sb_scale, hs, F / 32, rows, 16, 128)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p2.a0, w->w_down, cf, ED, kk, BM, true)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p2.sa0, w->s_down, sf, ED, sbox, BM)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p2.b, hc, cf, rows, kk, big, true)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p2.b32, hc, cf, rows, kk, 32, true)) return MOE_ERR_CUDA;
+    if (!make_map_u8(&p2.sb_scale, hsc, sf, rows, sbox, 128)) return MOE_ERR_CUDA;
+    if (nv) {
+        p2.row_scale = sh;
+        p2.wscale0 = w->gs_down;
+    }
     p2.M = D;
     p2.MT = D / (2 * BM);
-    p2.KB = F / kk;
+    p2.KB = cf / kk;
     p2.out = ws + L.y;
     p2.ldo = D;
     tb = ntiles * p2.MT;
     MOE_TRY(mark(MOE_STAGE_DOWN, 0, s));
-    MOE_TRY(cu(launch_mx_rows_fp8(reinterpret_cast<const uint16_t*>(ws + L.h), h8, hs, rows, F, sms,
-                                  s)));
-    MOE_TRY(cu(launch_mx8_gemm(GEMM_DOWN, p2, static_cast<int>(tb < units ? tb : units), s)));
+    const uint16_t* h = reinterpret_cast<const uint16_t*>(ws + L.h);
+    if (nv)
+        MOE_TRY(cu(launch_nvfp4_codes(h, hc, hsc, sh, rows, F, sms, s)));
+    else
+        MOE_TRY(cu(launch_mx_rows_fp8(h, hc, hsc, rows, F, sms, s)));
+    MOE_TRY(cu(launch_bs_gemm(fmt, GEMM_DOWN, p2, static_cast<int>(tb < units ? tb : units), s)));
     MOE_TRY(mark(MOE_STAGE_DOWN, 1, s));
 
     MOE_TRY(mark(MOE_STAGE_COMBINE, 0, s));
@@ -444,7 +472,8 @@ moe_status run_experts_mx8(const moe_dims* d, const void* x, const moe_weights* 
 moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, void* out,
                        const int32_t* ids, const float* gates, uint8_t* ws, const Layout& L,
                        cudaStream_t s) {
-    if (d->wfmt == MOE_W_MXFP8_ACT) return run_experts_mx8(d, x, w, out, ids, gates, ws, L, s);
+    if (d->wfmt == MOE_W_MXFP8_ACT || d->wfmt == MOE_W_NVFP4)
+        return run_experts_bs(d, x, w, out, ids, gates, ws, L, s);
     const int64_t T = d->T;
     const int k = d->k, E = d->E, S = d->n_shared;
     const int64_t rows = T * k + T * S;
@@ -456,11 +485,10 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     const int sms = num_sms();
     if (sms <= 0) return MOE_ERR_CUDA;
     const bool mx = d->wfmt == MOE_W_MXFP8;
-    const bool nv = d->wfmt == MOE_W_NVFP4;
-    const int kfmt = mx ? WFMT_MXFP8 : d->wfmt;  // the GEMM kernels' weight format
+    const int kfmt = mx ? WFMT_MXFP8 : WFMT_BF16;  // the GEMM kernels' weight format
     const bool one = one_sm_experts(d);
-    // MXFP8 / NVFP4 weights with few tokens: the SM-pair weight-streaming variant
-    const int small = !one && d->wfmt != MOE_W_BF16 && T <= kOneSmMaxTokens;
+    // MXFP8 weights with few tokens: the SM-pair weight-streaming variant
+    const int small = !one && mx && T <= kOneSmMaxTokens;
     const int bn = one ? BN : (small ? 64 : BN_EXPERT);           // tokens per tile
     const uint32_t box_b = one ? BN : BN_EXPERT / 2;              // token rows per CTA
     const uint32_t rg = one ? BM : gemm_rows(GEMM_SWIGLU);        // gate (= up) rows per CTA
@@ -522,21 +550,9 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     MOE_TRY(cu(launch_dispatch(ids, T, k, E, cnt, off, perm, inv,
                                reinterpret_cast<int32_t*>(ws + L.scratch), s)));
     MOE_TRY(mark(MOE_STAGE_DISPATCH, 1, s));
-    float* sxp = reinterpret_cast<float*>(ws + L.sxp);
-    float* sh = reinterpret_cast<float*>(ws + L.sh);
     MOE_TRY(mark(MOE_STAGE_GATHER, 0, s));
-    if (nv) {
-        // NVFP4: each token row quantised once (per-token scale), then gathered
-        MOE_TRY(cu(launch_nvfp4_qdq(static_cast<const uint16_t*>(x),
-                                    reinterpret_cast<uint16_t*>(ws + L.xq), nullptr,
-                                    reinterpret_cast<float*>(ws + L.sx), T, d->d, sms, s)));
-        MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(ws + L.xq), inv, T, k, d->d, S,
-                                 reinterpret_cast<uint16_t*>(ws + L.xp), s,
-                                 reinterpret_cast<const float*>(ws + L.sx), sxp)));
-    } else {
-        MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), inv, T, k, d->d, Sg,
-                                 reinterpret_cast<uint16_t*>(ws + L.xp), s)));
-    }
+    MOE_TRY(cu(launch_gather(static_cast<const uint16_t*>(x), inv, T, k, d->d, Sg,
+                             reinterpret_cast<uint16_t*>(ws + L.xp), s)));
     MOE_TRY(mark(MOE_STAGE_GATHER, 1, s));
 
     const int64_t ntiles = (T * k + bn - 1) / bn + E + (S ? (T + bn - 1) / bn : 0);
@@ -563,15 +579,6 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
         if (!make_map_u8(&p1.a1, w->w_up, d->d, EF, BK, rg)) return MOE_ERR_CUDA;
         if (!make_map_u8(&p1.sa0, w->s_gate, d->d / 32, EF, 16, rg)) return MOE_ERR_CUDA;
         if (!make_map_u8(&p1.sa1, w->s_up, d->d / 32, EF, 16, rg)) return MOE_ERR_CUDA;
-    } else if (nv) {
-        // 32 code bytes (64 values) per row and k-block; 32 scale bytes per 8 k-blocks
-        if (!make_map_u8(&p1.a0, w->w_gate, d->d / 2, EF, BK / 2, rg)) return MOE_ERR_CUDA;
-        if (!make_map_u8(&p1.a1, w->w_up, d->d / 2, EF, BK / 2, rg)) return MOE_ERR_CUDA;
-        if (!make_map_u8(&p1.sa0, w->s_gate, d->d / 16, EF, 32, rg)) return MOE_ERR_CUDA;
-        if (!make_map_u8(&p1.sa1, w->s_up, d->d / 16, EF, 32, rg)) return MOE_ERR_CUDA;
-        p1.row_scale = sxp;
-        p1.wscale0 = w->gs_gate;
-        p1.wscale1 = w->gs_up;
     } else if (packed) {
         if (!make_map(&p1.a0, pk, d->d, 2 * EF, 2 * rg)) return MOE_ERR_CUDA;
         p1.a1 = p1.a0;
@@ -612,11 +619,6 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     if (mx) {
         if (!make_map_u8(&p2.a0, w->w_down, d->F, ED, BK, BM)) return MOE_ERR_CUDA;
         if (!make_map_u8(&p2.sa0, w->s_down, d->F / 32, ED, 16, BM)) return MOE_ERR_CUDA;
-    } else if (nv) {
-        if (!make_map_u8(&p2.a0, w->w_down, d->F / 2, ED, BK / 2, BM)) return MOE_ERR_CUDA;
-        if (!make_map_u8(&p2.sa0, w->s_down, d->F / 16, ED, 32, BM)) return MOE_ERR_CUDA;
-        p2.row_scale = sh;
-        p2.wscale0 = w->gs_down;
     } else if (!make_map(&p2.a0, w->w_down, d->F, ED, BM)) {
         return MOE_ERR_CUDA;
     }
@@ -634,10 +636,6 @@ moe_status run_experts(const moe_dims* d, const void* x, const moe_weights* w, v
     const int g2 = static_cast<int>(tb < units ? tb : units);
     if (overlap) MOE_TRY(cu(cudaStreamWaitEvent(s, side->join, 0)));
     MOE_TRY(mark(MOE_STAGE_DOWN, 0, s));
-    if (nv)  // NVFP4: each row of h quantised in place (per-token scale)
-        MOE_TRY(cu(launch_nvfp4_qdq(reinterpret_cast<const uint16_t*>(ws + L.h),
-                                    reinterpret_cast<uint16_t*>(ws + L.h), nullptr, sh, T * k,
-                                    d->F, sms, s)));
     MOE_TRY(cu(one ? launch_grouped_gemm(GEMM_DOWN, p2, g2, s)
                    : launch_pair_gemm(GEMM_DOWN, p2, g2, s, kfmt, small)));
     MOE_TRY(mark(MOE_STAGE_DOWN, 1, s));

@@ -1,24 +1,27 @@
-// gemm_mx8.cu -- the expert GEMMs with MXFP8 on both operands (E4M3 weights and
-// E4M3 token rows, each with one E8M0 scale per 32 along K): the block-scaled
-// tensor-core MMA tcgen05.mma.kind::mxf8f6f4.block_scale multiplies the E4M3
-// values and applies the scales itself, so nothing is converted and the tensor
-// pipe runs at its 8-bit rate.  This is the MXFP8 expert compute of the
-// Composer 2 Technical Report, §6.1 "Training infrastructure", Kernels
-// paragraph (block-scaled tensor-core matmul; MXFP8 = E4M3 values, E8M0 scale
-// per 32 elements).
+// gemm_bs.cu -- the expert GEMMs with both operands narrow, on the block-scaled
+// tensor-core MMA, which multiplies the narrow values and applies their block
+// scales itself: nothing is converted and the tensor pipe runs at its 8-bit or
+// 4-bit rate.  Two formats, both from the Composer 2 Technical Report, §6.1
+// "Training infrastructure", Kernels paragraph (block-scaled tensor-core matmul):
+//   * MXFP8 (E4M3 weights and token rows, one E8M0 scale per 32 along K):
+//     tcgen05.mma.kind::mxf8f6f4.block_scale.scale_vec::1X, K = 32 per MMA;
+//   * NVFP4 (E2M1 weights and token rows, two per byte, one E4M3 scale per 16
+//     along K, plus an fp32 scale per token and per weight matrix that the
+//     epilogue applies): tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X,
+//     K = 64 per MMA.
 //
 // Shape: SM pairs (tcgen05 cta_group::2), M = 256 weight rows (128 per CTA),
-// N = up to 224 tokens (each CTA loads half), K in blocks of 128 (128 bytes per
-// row: one 128-byte-swizzled row of the operand tile, four MMAs of K = 32).
-// Each output element is one pair's fixed-order K loop into one TMEM
-// accumulator; no split-K, no atomics; the MMA width N only selects how many
-// independent token columns one instruction produces.
+// N = up to 224 (MXFP8) or 192 (NVFP4) tokens (each CTA loads half), K in
+// blocks of 128 bytes per row (one 128-byte-swizzled row of the operand tile,
+// four MMAs).  Each output element is one pair's fixed-order K loop into one
+// TMEM accumulator; no split-K, no atomics; the MMA width N only selects how
+// many independent token columns one instruction produces.
 //
 // Roles in each CTA (352 threads): warp 0 TMA producer of the weight tiles (and
-// every 4 K blocks the scale tiles); warp 10 TMA producer of the token tiles;
-// warp 1 TMEM owner and, in the pair's leader, the MMA issuer; warps 2..5
-// epilogue; warps 6..9 write each K block's scales into TMEM (one warp per
-// TMEM lane quadrant), where the MMA reads them.
+// of the scale tiles); warp 10 TMA producer of the token tiles; warp 1 TMEM
+// owner and, in the pair's leader, the MMA issuer; warps 2..5 epilogue; warps
+// 6..9 write each K block's scales into TMEM (one warp per TMEM lane
+// quadrant), where the MMA reads them.
 #include <cuda_bf16.h>
 
 #include "moe_internal.h"
@@ -27,34 +30,62 @@
 namespace moe {
 namespace {
 
-constexpr int kK8 = 128;                   // K elements (bytes) per stage and row
-constexpr int kTile8 = 224;                // tokens per tile (MMA N <= 224)
-constexpr int kHalf8 = 128;                // token rows per CTA in shared memory
+constexpr int kK8 = 128;                   // bytes per stage and row (K block)
+constexpr int kHalf8 = 128;                // token rows per CTA in shared memory (at most)
 constexpr int kStages8 = 5;
 constexpr uint32_t kA8 = 128 * kK8;        // weight tile of a CTA: 16 KB
-constexpr uint32_t kB8 = kHalf8 * kK8;     // token tile of a CTA: 16 KB
-constexpr uint32_t kStage8 = kA8 + kB8;
 constexpr uint32_t kBox8 = 32 * kK8;       // one 32-row token box
-// Scale ring: a slot holds the scales of 4 consecutive K blocks of one tile
-// (16 bytes per row): the CTA's 128 weight rows, then the tile's tokens of
-// both CTAs (CTA 0's half at rows 0..127, CTA 1's at 128..255).
-constexpr int kScKb = 4;
-constexpr int kScSlots8 = 4;  // the scales run up to 16 K blocks ahead of their MMAs
-constexpr uint32_t kScA8 = 128 * 16;
-constexpr uint32_t kScB8 = 256 * 16;
-constexpr uint32_t kScSlot8 = kScA8 + kScB8;
-// TMEM: two accumulator slots of kTile8 columns, then per stage 4 columns of
-// weight-row scales and 8 of token scales.
-constexpr uint32_t kAcc8 = kTile8;
-constexpr uint32_t kSfCol8 = 2 * kAcc8;
-constexpr uint32_t kSfStage8 = 12;
-static_assert(kSfCol8 + kStages8 * kSfStage8 <= 512, "TMEM columns");
-constexpr uint32_t kTmemCols8 = 512;
 constexpr int kThreads8 = 352;
 constexpr int kXPad8 = 33;
 constexpr uint32_t kXBytes8 = 2 * 32 * kXPad8 * 4;   // gate/up: up values handed to the gate warps
-constexpr int kBarriers8 = 2 * kStages8 + 2 * kScSlots8 + 2 + 2 + 4 + 1;
 constexpr int kMaxGroups8 = 1024;
+constexpr uint32_t kTmemCols8 = 512;
+
+// Per format:
+//   kTile     tokens per tile (MMA N at most);
+//   kBigBox   token rows of the one-copy box of a CTA's rows (3 or 4 32-row boxes);
+//   kScRow    scale bytes per row and K block; kScKb K blocks per scale slot;
+//   kSfKb     TMEM columns of one K block's scales: per K step 4 columns of
+//             weight-row scales and 8 of token scales (MXFP8: one word per row
+//             serves the block's four K steps, a byte each; NVFP4: a word per
+//             K step);
+//   kSfSets   sets of those columns in flight.  MXFP8: one per stage, reused
+//             once the stage's MMAs complete; NVFP4: two, each freed by its
+//             own commit (the accumulators leave room for no more).
+template <int FMT>
+struct BsCfg;
+template <>
+struct BsCfg<BS_MXFP8> {
+    static constexpr int kTile = 224, kBigBox = 128, kScRow = 4, kScKb = 4, kScSlots = 4;
+    static constexpr uint32_t kSfKb = 12;
+    static constexpr int kSfSets = kStages8;
+};
+template <>
+struct BsCfg<BS_NVFP4> {
+    static constexpr int kTile = 192, kBigBox = 96, kScRow = 16, kScKb = 2, kScSlots = 3;
+    static constexpr uint32_t kSfKb = 48;
+    static constexpr int kSfSets = 2;
+};
+
+template <int FMT>
+struct BsLayout {
+    using C = BsCfg<FMT>;
+    // token tile of a CTA: its rows at most, 1024-aligned for the swizzle
+    static constexpr uint32_t kB = static_cast<uint32_t>(C::kTile / 2 + 31) / 32 * kBox8;
+    static constexpr uint32_t kStage = kA8 + kB;
+    // Scale ring: a slot holds the scales of kScKb consecutive K blocks of one
+    // tile: the CTA's 128 weight rows, then the tile's tokens of both CTAs
+    // (CTA 0's half at rows 0..127, CTA 1's at 128..255).
+    static constexpr uint32_t kScRowBytes = C::kScRow * C::kScKb;  // one TMA box wide
+    static constexpr uint32_t kScA = 128 * kScRowBytes;
+    static constexpr uint32_t kScSlot = kScA + 256 * kScRowBytes;
+    // TMEM: two accumulator slots of kTile columns, then the scale column sets
+    static constexpr uint32_t kAcc = C::kTile;
+    static constexpr uint32_t kSfCol = 2 * kAcc;
+    static constexpr int kBarriers = 2 * kStages8 + 2 * C::kScSlots + C::kSfSets + 2 + 2 + 4 + 1;
+    static_assert(kSfCol + C::kSfSets * C::kSfKb <= kTmemCols8, "TMEM columns");
+    static_assert(kStage % 1024 == 0, "stages keep the 128-byte swizzle's alignment");
+};
 
 struct Tile8 {
     int m, g, n_valid, brow, arow;
@@ -83,9 +114,10 @@ __device__ __forceinline__ int find_group8(const int* start, int GG, int j) {
 // ("cold") are interleaved in proportion, so that every wave mixes
 // tensor-bound and weight-streaming tiles; the token tiles of a hot expert's
 // weight tile are consecutive.  Which pair computes a tile never changes how.
-template <int MODE>
+template <int MODE, int FMT>
 __device__ __forceinline__ Tile8 decode_tile8(int t, uint32_t rank, const GemmParams& p,
                                               const Sched8& sc) {
+    constexpr int kTile8 = BsCfg<FMT>::kTile;
     Tile8 tl;
     const int64_t h0 = static_cast<int64_t>(t) * sc.H / sc.N;
     const int64_t h1 = static_cast<int64_t>(t + 1) * sc.H / sc.N;
@@ -142,24 +174,31 @@ __device__ __forceinline__ void store_pairs8(const float (&h)[N], int lane, __nv
         if (row_ok && 2 * jj + odd < n_left) y[jj * ld] = pk[jj];
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_constant__ GemmParams p) {
+template <int MODE, int FMT>
+__global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_constant__ GemmParams p) {
+    using C = BsCfg<FMT>;
+    using L = BsLayout<FMT>;
+    constexpr bool kNv = FMT == BS_NVFP4;
     constexpr bool kPair = MODE == GEMM_SWIGLU;  // 64 gate + 64 up weight rows per CTA
     constexpr int kRowsCta = gemm_rows(MODE);
+    constexpr int kTile = C::kTile;
+    constexpr int kScKb = C::kScKb;
+    constexpr int kScSlots = C::kScSlots;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint8_t* scring = smem + kStages8 * kStage8;
-    float* xbuf = reinterpret_cast<float*>(scring + kScSlots8 * kScSlot8);
+    uint8_t* scring = smem + kStages8 * L::kStage;
+    float* xbuf = reinterpret_cast<float*>(scring + kScSlots * L::kScSlot);
     uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xbuf) + kXBytes8);
     uint64_t* empty = full + kStages8;
     uint64_t* scfull = empty + kStages8;
-    uint64_t* scempty = scfull + kScSlots8;
-    uint64_t* tfull = scempty + kScSlots8;
+    uint64_t* scempty = scfull + kScSlots;
+    uint64_t* sffree = scempty + kScSlots;  // NVFP4: a TMEM scale set's MMAs completed
+    uint64_t* tfull = sffree + C::kSfSets;
     uint64_t* tempty = tfull + 2;
     uint64_t* xfull = tempty + 2;
     uint64_t* xempty = xfull + 2;
     uint64_t* drain = xempty + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + kBarriers8);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + L::kBarriers);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
     const int GG = p.G;
     int* hs = reinterpret_cast<int*>(tmem_slot + 4);
@@ -181,7 +220,7 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
             const int c = p.cnt[g];
             gcnt[g] = c;
             goff[g] = p.off[g];
-            const int ntg = (c + kTile8 - 1) / kTile8;
+            const int ntg = (c + kTile - 1) / kTile;
             if (ntg > 1) local_h += ntg; else local_c += ntg;
         }
         int incl_h = local_h, incl_c = local_c;
@@ -198,7 +237,7 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
         for (int g = g0; g < min(g0 + per, GG); ++g) {
             hs[g] = run_h;
             cs[g] = run_c;
-            const int ntg = (gcnt[g] + kTile8 - 1) / kTile8;
+            const int ntg = (gcnt[g] + kTile - 1) / kTile;
             if (ntg > 1) run_h += ntg; else run_c += ntg;
         }
         if (lane == 31) {
@@ -213,10 +252,11 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
             mbar_init(&full[s], 1 + 2 * 4);  // producer + the scale writers of both CTAs
             mbar_init(&empty[s], 1);
         }
-        for (int s = 0; s < kScSlots8; ++s) {
+        for (int s = 0; s < kScSlots; ++s) {
             mbar_init(&scfull[s], 1);
             mbar_init(&scempty[s], 4);  // the 4 scale writers, after the slot's last K block
         }
+        for (int s = 0; s < C::kSfSets; ++s) mbar_init(&sffree[s], 1);
         for (int a = 0; a < 2; ++a) {
             mbar_init(&tfull[a], 1);
             mbar_init(&tempty[a], 8);  // 4 epilogue warps in each CTA
@@ -242,6 +282,12 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
         const int64_t t = cid + static_cast<int64_t>(j) * ncl;
         return t < total ? static_cast<int>(t) : -1;
     };
+    // a CTA's token rows: one kBigBox-row box when they need three or more
+    // 32-row boxes (fewer copies), else 32-row boxes
+    auto token_boxes = [](int rows) {
+        const int n = (rows + 31) >> 5;
+        return n >= 3 ? C::kBigBox / 32 : n;
+    };
 
     if (warp == 0) {
         if (lane == 0) {
@@ -257,38 +303,33 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
             for (int j = 0; ok; ++j) {
                 const int t = tile_at(j);
                 if (t < 0) break;
-                const Tile8 tl = decode_tile8<MODE>(t, rank, p, sched);
-                // a CTA's token rows (loaded by warp 10): one 128-row box when they
-                // need three or four 32-row boxes (fewer copies), else 32-row boxes
-                auto boxes = [&](uint32_t r) {
-                    const int n = (b_rows8(tl, r) + 31) >> 5;
-                    return n >= 3 ? 4 : n;
-                };
-                const uint32_t expect = 2 * kA8 + (boxes(0) + boxes(1)) * kBox8;
+                const Tile8 tl = decode_tile8<MODE, FMT>(t, rank, p, sched);
+                const uint32_t expect =
+                    2 * kA8 + (token_boxes(b_rows8(tl, 0)) + token_boxes(b_rows8(tl, 1))) * kBox8;
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (kb % kScKb == 0) {
-                        // the scales of K blocks kb .. kb + 3: weight rows, then both
-                        // halves of the tile's tokens
+                        // the scales of K blocks kb .. kb + kScKb - 1: weight rows,
+                        // then both halves of the tile's tokens
                         if (!mbar_wait(&scempty[ss], sph ^ 1u, abort, tmo)) {
                             if (!*abort) raise_timeout8(p, abort, 40);
                             ok = false;
                             break;
                         }
-                        uint8_t* sc = scring + ss * kScSlot8;
-                        mbar_arrive_expect_tx(&scfull[ss], kScA8 + 2 * 128 * 16);
-                        const int x = kb * (kK8 / 32);
+                        uint8_t* sc = scring + ss * L::kScSlot;
+                        mbar_arrive_expect_tx(&scfull[ss], L::kScA + 2 * 128 * L::kScRowBytes);
+                        const int x = kb * C::kScRow;
                         if constexpr (kPair) {
                             tma_load_2d(sc, &p.sa0, &scfull[ss], x, tl.arow, pol_w);
-                            tma_load_2d(sc + kScA8 / 2, &p.sa1, &scfull[ss], x, tl.arow, pol_w);
+                            tma_load_2d(sc + L::kScA / 2, &p.sa1, &scfull[ss], x, tl.arow, pol_w);
                         } else {
                             tma_load_2d(sc, &p.sa0, &scfull[ss], x, tl.arow, pol_w);
                         }
-                        tma_load_2d(sc + kScA8, &p.sb_scale, &scfull[ss], x, tl.brow, pol_x);
-                        tma_load_2d(sc + kScA8 + 128 * 16, &p.sb_scale, &scfull[ss], x,
+                        tma_load_2d(sc + L::kScA, &p.sb_scale, &scfull[ss], x, tl.brow, pol_x);
+                        tma_load_2d(sc + L::kScA + 128 * L::kScRowBytes, &p.sb_scale, &scfull[ss], x,
                                     tl.brow + tl.half, pol_x);
                         s_issued |= 1u << ss;
                         s_par = (s_par & ~(1u << ss)) | (sph << ss);
-                        if (++ss == kScSlots8) {
+                        if (++ss == kScSlots) {
                             ss = 0;
                             sph ^= 1u;
                         }
@@ -298,7 +339,7 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
                         ok = false;
                         break;
                     }
-                    uint8_t* st = smem + stage * kStage8;
+                    uint8_t* st = smem + stage * L::kStage;
                     if (leader) mbar_arrive_expect_tx(&full[stage], expect);
                     const uint32_t bar = map_to_rank(&full[stage], 0);
                     if constexpr (kPair) {
@@ -320,7 +361,7 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
                     if (issued & (1u << s))
                         if (!mbar_wait(&full[s], (last_par >> s) & 1u, nullptr, tmo))
                             raise_timeout8(p, abort, 42);
-            for (int s = 0; s < kScSlots8; ++s)
+            for (int s = 0; s < kScSlots; ++s)
                 if (s_issued & (1u << s))
                     if (!mbar_wait(&scfull[s], (s_par >> s) & 1u, nullptr, tmo))
                         raise_timeout8(p, abort, 43);
@@ -328,7 +369,7 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ---------------- MMA issuer (leader only) ----------------
-            int stage = 0, acc = 0;
+            int stage = 0, acc = 0, sfs = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             for (int j = 0; ok; ++j) {
@@ -339,9 +380,9 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
                     break;
                 }
                 tc_fence_after();
-                const Tile8 tl = decode_tile8<MODE>(t, rank, p, sched);
-                const uint32_t d0 = tmem_base + acc * kAcc8;
-                const uint32_t idesc = idesc_mx8(2 * BM, 2 * tl.half);
+                const Tile8 tl = decode_tile8<MODE, FMT>(t, rank, p, sched);
+                const uint32_t d0 = tmem_base + acc * L::kAcc;
+                const uint32_t idesc = kNv ? idesc_nv4(2 * BM, 2 * tl.half) : idesc_mx8(2 * BM, 2 * tl.half);
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(&full[stage], phase, abort, tmo)) {
                         if (!*abort) raise_timeout8(p, abort, 45);
@@ -349,14 +390,24 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_addr(smem + stage * kStage8);
+                    const uint32_t sa = smem_addr(smem + stage * L::kStage);
                     const uint64_t da = sdesc_kmajor_sw128(sa);
                     const uint64_t db = sdesc_kmajor_sw128(sa + kA8);
-                    const uint32_t sfa = tmem_base + kSfCol8 + stage * kSfStage8;
+                    if constexpr (kNv) {
+                        const uint32_t sfa = tmem_base + L::kSfCol + sfs * C::kSfKb;
 #pragma unroll
-                    for (int k = 0; k < kK8 / 32; ++k)
-                        umma_mx8_pair(d0, da + 2 * k, db + 2 * k, idesc_mx8_step(idesc, k), sfa,
-                                      sfa + 4, (kb | k) != 0);
+                        for (int k = 0; k < 4; ++k)
+                            umma_nv4_pair(d0, da + 2 * k, db + 2 * k, idesc, sfa + 12 * k,
+                                          sfa + 12 * k + 4, (kb | k) != 0);
+                        umma_commit_pair(&sffree[sfs], 0x3);
+                        if (++sfs == C::kSfSets) sfs = 0;
+                    } else {
+                        const uint32_t sfa = tmem_base + L::kSfCol + stage * C::kSfKb;
+#pragma unroll
+                        for (int k = 0; k < 4; ++k)
+                            umma_mx8_pair(d0, da + 2 * k, db + 2 * k, idesc_mx8_step(idesc, k), sfa,
+                                          sfa + 4, (kb | k) != 0);
+                    }
                     umma_commit_pair(&empty[stage], 0x3);
                     if (++stage == kStages8) {
                         stage = 0;
@@ -385,9 +436,8 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
             for (int j = 0; ok; ++j) {
                 const int t = tile_at(j);
                 if (t < 0) break;
-                const Tile8 tl = decode_tile8<MODE>(t, rank, p, sched);
-                const int nb = (b_rows8(tl, rank) + 31) >> 5;
-                const int nbox = nb >= 3 ? 4 : nb;
+                const Tile8 tl = decode_tile8<MODE, FMT>(t, rank, p, sched);
+                const int nb = token_boxes(b_rows8(tl, rank));
                 const int brow = tl.brow + static_cast<int>(rank) * tl.half;
                 for (int kb = 0; kb < p.KB; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, abort, tmo)) {
@@ -395,12 +445,12 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
                         ok = false;
                         break;
                     }
-                    uint8_t* st = smem + stage * kStage8;
+                    uint8_t* st = smem + stage * L::kStage;
                     const uint32_t bar = map_to_rank(&full[stage], 0);
-                    if (nbox == 4) {
+                    if (nb == C::kBigBox / 32) {
                         tma_load_2d_pair(st + kA8, &p.b, bar, kb * kK8, brow, pol_x);
                     } else {
-                        for (int i = 0; i < nbox; ++i)
+                        for (int i = 0; i < nb; ++i)
                             tma_load_2d_pair(st + kA8 + i * kBox8, &p.b32, bar, kb * kK8, brow + 32 * i,
                                              pol_x);
                     }
@@ -417,8 +467,8 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
         // ---------------- scale writers (warps 6..9, both CTAs) ----------------
         // Warp of lane quadrant q writes, for each K block, the weight-row scales
         // of rows 32q .. 32q + 31 (lane r, column r / 32) and the scales of all
-        // N token columns (lane 32q + n % 32, column 4 + n / 32) into the stage's
-        // TMEM scale columns, after the stage's previous MMAs completed.
+        // N token columns (lane 32q + n % 32, column 4 + n / 32) into a set of
+        // TMEM scale columns, once the MMAs that last read that set completed.
         const int q = warp & 3;
         const uint32_t lane_base = static_cast<uint32_t>(32 * q) << 16;
         auto wait_all = [&](uint64_t* bar, uint32_t par, int where) {
@@ -433,28 +483,41 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
         for (int j = 0; ok; ++j) {
             const int t = tile_at(j);
             if (t < 0) break;
-            const Tile8 tl = decode_tile8<MODE>(t, rank, p, sched);
+            const Tile8 tl = decode_tile8<MODE, FMT>(t, rank, p, sched);
             const int n_cols = 2 * tl.half;
             for (int kb = 0; kb < p.KB; ++kb, ++i) {
-                const int ss = static_cast<int>((i / kScKb) % kScSlots8);
-                const uint32_t sph = static_cast<uint32_t>((i / kScKb / kScSlots8) & 1);
-                if (!wait_all(&scfull[ss], sph, 47) || !wait_all(&empty[stage], phase ^ 1u, 48)) {
+                const int ss = static_cast<int>((i / kScKb) % kScSlots);
+                const uint32_t sph = static_cast<uint32_t>((i / kScKb / kScSlots) & 1);
+                const int set = kNv ? static_cast<int>(i % C::kSfSets) : stage;
+                const bool freed =
+                    kNv ? wait_all(&sffree[set], static_cast<uint32_t>((i / C::kSfSets) & 1) ^ 1u, 53)
+                        : wait_all(&empty[stage], phase ^ 1u, 48);
+                if (!wait_all(&scfull[ss], sph, 47) || !freed) {
                     ok = false;
                     break;
                 }
-                const uint8_t* sc = scring + ss * kScSlot8;
+                const uint8_t* sc = scring + ss * L::kScSlot;
                 const int kq = kb % kScKb;
-                const uint32_t sf = tmem_base + lane_base + kSfCol8 + stage * kSfStage8;
-                tmem_st1(sf + q, *reinterpret_cast<const uint32_t*>(sc + (32 * q + lane) * 16 + kq * 4));
-                uint32_t bw[8];
+                const uint32_t sf = tmem_base + lane_base + L::kSfCol + set * C::kSfKb;
+                // MXFP8: one word per row (its 4 bytes the block's 4 K steps);
+                // NVFP4: one word per row and K step (its bytes the 4 16-blocks)
+                constexpr int kWords = kNv ? 4 : 1;
 #pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const int n = 32 * c + lane;  // token column of the MMA
-                    const int r = n < tl.half ? n : 128 + n - tl.half;
-                    bw[c] = n < n_cols ? *reinterpret_cast<const uint32_t*>(sc + kScA8 + r * 16 + kq * 4)
-                                       : 0x7F7F7F7Fu;
+                for (int w = 0; w < kWords; ++w) {
+                    const int off = kq * C::kScRow + w * 4;
+                    tmem_st1(sf + 12 * w + q,
+                             *reinterpret_cast<const uint32_t*>(sc + (32 * q + lane) * L::kScRowBytes + off));
+                    uint32_t bw[8];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int n = 32 * c + lane;  // token column of the MMA
+                        const int r = n < tl.half ? n : 128 + n - tl.half;
+                        bw[c] = n < n_cols ? *reinterpret_cast<const uint32_t*>(
+                                                 sc + L::kScA + r * L::kScRowBytes + off)
+                                           : (kNv ? 0x38383838u : 0x7F7F7F7Fu);  // 1.0
+                    }
+                    tmem_st8(sf + 12 * w + 4, bw);
                 }
-                tmem_st8(sf + 4, bw);
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -477,7 +540,8 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
         // ---------------- epilogue (warps 2..5, both CTAs) ----------------
         // Warp q reads accumulator lanes [32q, 32q + 32).  gate/up: warps 0, 1
         // hold gate rows and warps 2, 3 the matching up rows, which they pass
-        // on through xbuf.
+        // on through xbuf.  NVFP4: each output is first multiplied by its
+        // token's scale times the matrix's scale.
         const int q = warp & 3;
         const int pr = q & 1;
         const bool up_warp = q >= 2;
@@ -487,7 +551,7 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
         for (int j = 0; ok; ++j) {
             const int t = tile_at(j);
             if (t < 0) break;
-            const Tile8 tl = decode_tile8<MODE>(t, rank, p, sched);
+            const Tile8 tl = decode_tile8<MODE, FMT>(t, rank, p, sched);
             if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort, tmo))) {
                 if (lane == 0 && !*abort) raise_timeout8(p, abort, 49);
                 break;
@@ -496,12 +560,17 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
             const int row = tl.m * 2 * kRowsCta + static_cast<int>(rank) * kRowsCta +
                             (kPair ? pr : q) * 32 + lane;
             const bool row_ok = row < p.M;
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * kAcc8;
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * L::kAcc;
+            const float ws0 = kNv ? p.wscale0[tl.g] : 1.0f;
+            const float ws1 = kNv && kPair ? p.wscale1[tl.g] : 1.0f;
             for (int c0 = 0; c0 < tl.n_valid && ok; c0 += 32) {
                 float v[32];
                 tmem_ld32(taddr + c0, v);
                 tmem_ld_wait();
                 tmem_regs_ready(v);
+                // NVFP4: lane j holds the scale of the chunk's token j
+                const float tok_scale =
+                    kNv && c0 + lane < tl.n_valid ? p.row_scale[tl.brow + c0 + lane] : 0.0f;
                 if constexpr (kPair) {
                     float* xb = xbuf + pr * 32 * kXPad8 + lane * kXPad8;
                     if (up_warp) {
@@ -522,7 +591,15 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
                         }
                         float h[32];
 #pragma unroll
-                        for (int jj = 0; jj < 32; ++jj) h[jj] = swiglu(v[jj], xb[jj]);
+                        for (int jj = 0; jj < 32; ++jj) {
+                            float g = v[jj], u = xb[jj];
+                            if constexpr (kNv) {
+                                const float st = __shfl_sync(0xffffffffu, tok_scale, jj);
+                                g *= st * ws0;
+                                u *= st * ws1;
+                            }
+                            h[jj] = swiglu(g, u);
+                        }
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&xempty[pr]);
                         store_pairs8<32>(h, lane,
@@ -532,6 +609,11 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
                     }
                     xph ^= 1u;
                 } else {
+                    if constexpr (kNv) {
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj)
+                            v[jj] *= __shfl_sync(0xffffffffu, tok_scale, jj) * ws0;
+                    }
                     store_pairs8<32>(v, lane,
                                      static_cast<__nv_bfloat16*>(p.out) +
                                          static_cast<int64_t>(tl.brow + c0) * p.ldo + (row & ~1),
@@ -558,15 +640,17 @@ __global__ void __launch_bounds__(kThreads8, 1) mx8_pair_kernel(const __grid_con
     }
 }
 
-size_t mx8_smem_bytes(int GG) {
-    return 1024 + kStages8 * kStage8 + kScSlots8 * kScSlot8 + kXBytes8 + kBarriers8 * 8 + 16 +
-           static_cast<size_t>(4 * GG + 2) * 4;
+template <int FMT>
+size_t bs_smem_bytes(int GG) {
+    using L = BsLayout<FMT>;
+    return 1024 + kStages8 * L::kStage + BsCfg<FMT>::kScSlots * L::kScSlot + kXBytes8 +
+           L::kBarriers * 8 + 16 + static_cast<size_t>(4 * GG + 2) * 4;
 }
 
-template <int MODE>
-cudaError_t launch_mx8_mode(const GemmParams& p, int clusters, cudaStream_t s) {
-    const size_t smem = mx8_smem_bytes(p.G);
-    cudaError_t e = cudaFuncSetAttribute(mx8_pair_kernel<MODE>,
+template <int MODE, int FMT>
+cudaError_t launch_bs_mode(const GemmParams& p, int clusters, cudaStream_t s) {
+    const size_t smem = bs_smem_bytes<FMT>(p.G);
+    cudaError_t e = cudaFuncSetAttribute(bs_pair_kernel<MODE, FMT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
@@ -583,27 +667,43 @@ cudaError_t launch_mx8_mode(const GemmParams& p, int clusters, cudaStream_t s) {
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     int resident = 0;
-    e = cudaOccupancyMaxActiveClusters(&resident, mx8_pair_kernel<MODE>, &cfg);
+    e = cudaOccupancyMaxActiveClusters(&resident, bs_pair_kernel<MODE, FMT>, &cfg);
     if (e != cudaSuccess) return e;
     if (resident <= 0) return cudaErrorInvalidConfiguration;
     if (clusters > resident) {
         clusters = resident;
         cfg.gridDim = dim3(2 * clusters, 1, 1);
     }
-    return cudaLaunchKernelEx(&cfg, mx8_pair_kernel<MODE>, p);
+    return cudaLaunchKernelEx(&cfg, bs_pair_kernel<MODE, FMT>, p);
+}
+
+template <int FMT>
+cudaError_t launch_bs_fmt(int mode, const GemmParams& p, int clusters, cudaStream_t s) {
+    if (p.KB % BsCfg<FMT>::kScKb) return cudaErrorInvalidValue;  // scale slots never straddle tiles
+    if (mode == GEMM_SWIGLU) return launch_bs_mode<GEMM_SWIGLU, FMT>(p, clusters, s);
+    if (mode == GEMM_DOWN) return launch_bs_mode<GEMM_DOWN, FMT>(p, clusters, s);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace
 
-int mx8_tile_tokens() { return kTile8; }
-int mx8_k_block() { return kK8; }
+int bs_tile_tokens(int fmt) { return fmt == BS_NVFP4 ? BsCfg<BS_NVFP4>::kTile : BsCfg<BS_MXFP8>::kTile; }
+int bs_big_box(int fmt) { return fmt == BS_NVFP4 ? BsCfg<BS_NVFP4>::kBigBox : BsCfg<BS_MXFP8>::kBigBox; }
+int bs_scale_box(int fmt) {
+    return fmt == BS_NVFP4 ? static_cast<int>(BsLayout<BS_NVFP4>::kScRowBytes)
+                           : static_cast<int>(BsLayout<BS_MXFP8>::kScRowBytes);
+}
+int bs_scale_kb(int fmt) { return fmt == BS_NVFP4 ? BsCfg<BS_NVFP4>::kScKb : BsCfg<BS_MXFP8>::kScKb; }
 
-cudaError_t launch_mx8_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s) {
+cudaError_t launch_bs_gemm(int fmt, int mode, const GemmParams& p, int clusters, cudaStream_t s) {
     if (p.G > kMaxGroups8 || p.has_shared || clusters <= 0 || !p.cnt || !p.off)
         return cudaErrorInvalidValue;
-    if (p.KB % kScKb) return cudaErrorInvalidValue;  // scale slots never straddle tiles
-    if (mode == GEMM_SWIGLU) return launch_mx8_mode<GEMM_SWIGLU>(p, clusters, s);
-    if (mode == GEMM_DOWN) return launch_mx8_mode<GEMM_DOWN>(p, clusters, s);
+    if (fmt == BS_MXFP8) return launch_bs_fmt<BS_MXFP8>(mode, p, clusters, s);
+    if (fmt == BS_NVFP4) {
+        if (!p.row_scale || !p.wscale0 || (mode == GEMM_SWIGLU && !p.wscale1))
+            return cudaErrorInvalidValue;
+        return launch_bs_fmt<BS_NVFP4>(mode, p, clusters, s);
+    }
     return cudaErrorInvalidValue;
 }
 

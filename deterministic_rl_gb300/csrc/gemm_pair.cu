@@ -47,12 +47,7 @@ constexpr int kMaxGroups = 1024;
 // of two, convert whole k-blocks (group g takes k-blocks g, g+4, ...) into the
 // operand ring's A buffer, so several k-blocks are converted at once and HBM
 // latency never sits between a conversion and its MMA.
-// NV: expert weights stored as NVFP4 (E2M1 codes two per byte + one E4M3 scale
-// per 16 along K + one fp32 scale per matrix), converted the same way (a
-// 32-byte code row and four scale bytes per row and k-block); the token
-// operand arrives as bf16 e2m1 * e4m3 values (quantised per token) and the
-// epilogue scales each output by its token's and its matrix's fp32 scales.
-// SMALL (converting formats, batches of at most 128 tokens): weight streaming
+// SMALL (MXFP8 weights, batches of at most 128 tokens): weight streaming
 // with few tokens per expert.  Tiles of 64 tokens leave a 4 KB token slot per
 // stage, so four operand stages take 80 KB and the weight ring gets 96 KB (the
 // bytes in flight that streaming at an SM's share of HBM bandwidth needs), and
@@ -60,7 +55,6 @@ constexpr int kMaxGroups = 1024;
 template <int MODE, int FMT, bool SMALL>
 struct PCfg {
     static constexpr bool kConv = FMT != WFMT_BF16;   // weights converted in-kernel
-    static constexpr bool kNv = FMT == WFMT_NVFP4;
     static constexpr bool kSmall = SMALL;
     static constexpr int kTileN = SMALL ? kSmallTileN : BN_EXPERT;  // tokens per MMA sub-tile
     static constexpr int kHalfN = kTileN / 2;                      // token rows per CTA
@@ -91,10 +85,10 @@ struct PCfg {
     static constexpr uint32_t kXBytes = kPair && !kConv ? 2 * 32 * kXPad * 4 : 0;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;  // operand ring entry
     static constexpr int kStages = SMALL ? 4 : (kSuper ? 4 : (kConv ? 5 : 6));
-    static constexpr uint32_t kF8RowBytes = kNv ? BK / 2 : BK;  // weight bytes per row and k-block
-    static constexpr uint32_t kF8Bytes = BM * kF8RowBytes;      // fp8 / fp4 weight tile
-    static constexpr int kF8Stages = SMALL ? (kNv ? 24 : 12) : (kSuper ? 4 : (kConv ? 5 : 0));
-    static constexpr int kScPerKb = kNv ? BK / 16 : BK / 32;   // scale bytes per row and k-block
+    static constexpr uint32_t kF8RowBytes = BK;                 // weight bytes per row and k-block
+    static constexpr uint32_t kF8Bytes = BM * kF8RowBytes;      // fp8 weight tile
+    static constexpr int kF8Stages = SMALL ? 12 : (kSuper ? 4 : (kConv ? 5 : 0));
+    static constexpr int kScPerKb = BK / 32;                    // scale bytes per row and k-block
     static constexpr uint32_t kScBytes = BM * 8 * kScPerKb;     // 8 k-blocks of scales
     static constexpr int kScStages = kConv ? 2 : 0;
     static constexpr uint32_t kRingBytes =
@@ -375,42 +369,6 @@ __device__ __forceinline__ void mx_convert_rows(const uint8_t* f8, const uint8_t
             *reinterpret_cast<uint4*>(row + sw1) = o1;
         }
     }
-}
-
-// Sixteen E2M1 codes (two words, element 2j in the low nibble of byte j) of
-// one block with E4M3 scale byte s -> sixteen bf16 values e2m1 * e4m3, exactly
-// (a product of at most 2 and 4 significant bits).  The eight magnitudes
-// times the scale form a table whose low and high bytes the codes select
-// with byte permutes (a code's three magnitude bits are a permute selector);
-// each code's sign bit is moved to its bf16 sign bit.  A NaN scale gives NaN.
-__device__ __forceinline__ uint32_t prmt2(uint32_t a, uint32_t b, uint32_t sel) {
-    uint32_t d;
-    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
-    return d;
-}
-
-__device__ __forceinline__ void e2m1x16_to_bf16(uint2 q, uint32_t s, uint4& o0, uint4& o1) {
-    const float Sf = __half2float(__half(__nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(s), __NV_E4M3)));
-    // magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6 times the scale, as bf16 pairs
-    const uint32_t w01 = prmt2(0u, __float_as_uint(0.5f * Sf), 0x7632);
-    const uint32_t w23 = prmt2(__float_as_uint(Sf), __float_as_uint(1.5f * Sf), 0x7632);
-    const uint32_t w45 = prmt2(__float_as_uint(2.0f * Sf), __float_as_uint(3.0f * Sf), 0x7632);
-    const uint32_t w67 = prmt2(__float_as_uint(4.0f * Sf), __float_as_uint(6.0f * Sf), 0x7632);
-    const uint32_t lo0 = prmt2(w01, w23, 0x6420), hi0 = prmt2(w01, w23, 0x7531);  // entries 0..3
-    const uint32_t lo1 = prmt2(w45, w67, 0x6420), hi1 = prmt2(w45, w67, 0x7531);  // entries 4..7
-    uint32_t out[8];
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {  // four codes per step: word h/2, half h%2
-        const uint32_t w = h < 2 ? q.x : q.y;
-        const uint32_t codes = (h & 1) ? (w >> 16) : w;
-        const uint32_t sel = codes & 0x7777u;
-        const uint32_t L = prmt2(lo0, lo1, sel), H = prmt2(hi0, hi1, sel);
-        // signs of codes 0..3 sit at bits 3, 7, 11, 15 of `codes`
-        out[2 * h] = prmt2(L, H, 0x5140) | ((codes << 12) & 0x8000u) | ((codes << 24) & 0x80000000u);
-        out[2 * h + 1] = prmt2(L, H, 0x7362) | ((codes << 4) & 0x8000u) | ((codes << 16) & 0x80000000u);
-    }
-    o0 = make_uint4(out[0], out[1], out[2], out[3]);
-    o1 = make_uint4(out[4], out[5], out[6], out[7]);
 }
 
 // Epilogue store of bf16 outputs: lanes 2i and 2i + 1 hold the values of two
@@ -929,26 +887,8 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                 const uint8_t* f8 = f8ring + fs * C::kF8Bytes;
                 const uint8_t* sc = scring + ss * C::kScBytes;
                 const int kb8 = static_cast<int>(i & 7);
-                if constexpr (!C::kNv) {
-                    mx_convert_rows<kRowsPerWarp, C::kInterleave>(f8, sc, kb8, st,
-                                                                  sub * kRowsPerWarp, lane);
-                } else {
-                // 128 rows x 4 tasks of 16 values (one scale each); a task
-                // becomes two 16-byte chunks of the 128-byte-swizzled row.
-#pragma unroll 4
-                for (int it = 0; it < (kRowsPerWarp * 4) / 32; ++it) {
-                    const int task = sub * kRowsPerWarp * 4 + it * 32 + lane;
-                    const int r = task >> 2, c2 = (task & 3) * 2;
-                    uint4 o0, o1;
-                    // block c2 / 2 of the row: 8 code bytes, one scale byte
-                    const uint2 q = *reinterpret_cast<const uint2*>(f8 + r * 32 + c2 * 4);
-                    e2m1x16_to_bf16(q, sc[r * 32 + kb8 * 4 + (c2 >> 1)], o0, o1);
-                    // operand row: gate/up rows alternate in 16-row blocks
-                    uint8_t* row = st + mx_operand_row<C::kInterleave>(r) * 128;
-                    *reinterpret_cast<uint4*>(row + ((c2 ^ (r & 7)) << 4)) = o0;
-                    *reinterpret_cast<uint4*>(row + (((c2 + 1) ^ (r & 7)) << 4)) = o1;
-                }
-                }
+                mx_convert_rows<kRowsPerWarp, C::kInterleave>(f8, sc, kb8, st, sub * kRowsPerWarp,
+                                                              lane);
                 fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
@@ -1005,15 +945,9 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
             const bool row_ok = row < p.M;
             const uint32_t taddr =
                 tmem_base + (static_cast<uint32_t>(q * 32) << 16) + acc * C::kAccCols;
-            // NVFP4: the matrices' fp32 scales for this group
-            const float ws0 = C::kNv ? p.wscale0[tl.g] : 1.0f;
-            const float ws1 = C::kNv && C::kPair ? p.wscale1[tl.g] : 1.0f;
             // One chunk of 32 accumulator columns (tokens c0 .. c0 + 31);
             // false when a wait of the bf16 gate/up handoff ran out.
             auto chunk = [&](const float (&v)[32], int c0) -> bool {
-                // NVFP4: lane j holds the fp32 scale of the chunk's token j
-                const float tok_scale = C::kNv && c0 + lane < tl.n_valid
-                                            ? p.row_scale[tl.brow + c0 + lane] : 0.0f;
                 if constexpr (C::kInterleave) {
                     // all exchanges first, then 16 independent SwiGLUs, then the
                     // stores: no shuffle or store sits between two SwiGLUs, so
@@ -1025,13 +959,8 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                         other[j] = __shfl_xor_sync(0xffffffffu, up_lane ? v[j] : v[16 + j], 16);
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        float g = up_lane ? other[j] : v[j];
-                        float u = up_lane ? v[16 + j] : other[j];
-                        if constexpr (C::kNv) {
-                            const float st = __shfl_sync(0xffffffffu, tok_scale, cb - c0 + j);
-                            g *= st * ws0;
-                            u *= st * ws1;
-                        }
+                        const float g = up_lane ? other[j] : v[j];
+                        const float u = up_lane ? v[16 + j] : other[j];
                         h[j] = swiglu(g, u);
                     }
                     // rows pair up within M (a multiple of 64): both lanes of
@@ -1098,14 +1027,8 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                             if (row_ok && c0 + j < tl.n_valid)
                                 Yf[static_cast<int64_t>(tl.brow + c0 + j) * p.ldo + row] = v[j];
                     } else {
-                        float h[32];
-#pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            h[j] = v[j];
-                            if constexpr (C::kNv) h[j] *= __shfl_sync(0xffffffffu, tok_scale, j) * ws0;
-                        }
                         store_bf16_row_pairs<32>(
-                            h, lane,
+                            v, lane,
                             static_cast<__nv_bfloat16*>(p.out) +
                                 static_cast<int64_t>(tl.brow + c0) * p.ldo + (row & ~1),
                             p.ldo, tl.n_valid - c0, row_ok);
@@ -1195,25 +1118,18 @@ cudaError_t launch_pair_gemm(int mode, const GemmParams& p, int clusters, cudaSt
     if (p.G + p.has_shared > kMaxGroups || clusters <= 0 || !p.cnt || !p.off || !p.tile_counter)
         return cudaErrorInvalidValue;
     if (wfmt != WFMT_BF16 && p.has_shared) return cudaErrorInvalidValue;  // shared expert is bf16
-    if (wfmt == WFMT_NVFP4 && (!p.row_scale || !p.wscale0 || (mode == GEMM_SWIGLU && !p.wscale1)))
-        return cudaErrorInvalidValue;
+    if (wfmt != WFMT_BF16 && wfmt != WFMT_MXFP8) return cudaErrorInvalidValue;
     if (small && wfmt == WFMT_BF16) return cudaErrorInvalidValue;  // bf16 small batches: one-SM kernel
     if (mode == GEMM_SWIGLU) {
         if (wfmt == WFMT_MXFP8)
             return small ? launch_pair_mode<GEMM_SWIGLU, WFMT_MXFP8, true>(p, clusters, s)
                          : launch_pair_mode<GEMM_SWIGLU, WFMT_MXFP8, false>(p, clusters, s);
-        if (wfmt == WFMT_NVFP4)
-            return small ? launch_pair_mode<GEMM_SWIGLU, WFMT_NVFP4, true>(p, clusters, s)
-                         : launch_pair_mode<GEMM_SWIGLU, WFMT_NVFP4, false>(p, clusters, s);
         return launch_pair_mode<GEMM_SWIGLU, WFMT_BF16, false>(p, clusters, s);
     }
     if (mode == GEMM_DOWN) {
         if (wfmt == WFMT_MXFP8)
             return small ? launch_pair_mode<GEMM_DOWN, WFMT_MXFP8, true>(p, clusters, s)
                          : launch_pair_mode<GEMM_DOWN, WFMT_MXFP8, false>(p, clusters, s);
-        if (wfmt == WFMT_NVFP4)
-            return small ? launch_pair_mode<GEMM_DOWN, WFMT_NVFP4, true>(p, clusters, s)
-                         : launch_pair_mode<GEMM_DOWN, WFMT_NVFP4, false>(p, clusters, s);
         return launch_pair_mode<GEMM_DOWN, WFMT_BF16, false>(p, clusters, s);
     }
     return cudaErrorInvalidValue;

@@ -101,8 +101,8 @@ struct GemmParams {
     // (64 gate rows then the same 64 up rows per block; 128-row boxes); the
     // CTA's 128 operand rows are one box at packed row 2 * arow.
     int32_t a_packed;
-    // MXFP8 x MXFP8 GEMMs (gemm_mx8.cu): the token rows' E8M0 scales, one per
-    // 32 along K ([rows][K/32] bytes, 16-byte x 128-row boxes).
+    // Block-scaled GEMMs (gemm_bs.cu): the token rows' block scales (E8M0 per
+    // 32 for MXFP8, E4M3 per 16 for NVFP4), [rows][K/32 or K/16] bytes.
     CUtensorMap sb_scale;
 };
 
@@ -112,25 +112,29 @@ cudaError_t launch_grouped_gemm(int mode, const GemmParams& p, int grid, cudaStr
 // `clusters` pairs of SMs; M is split in tiles of 2 * gemm_rows(mode) rows.
 // wfmt WFMT_MXFP8: a0/a1 are E4M3 weight maps (64-byte boxes) with scale maps
 // sa0/sa1; the kernel dequantises them exactly to bf16 in shared memory.
-// wfmt WFMT_NVFP4: a0/a1 are packed E2M1 maps (32-byte boxes) with E4M3
-// scale maps sa0/sa1 (32-byte boxes, one per 16 values); the kernel
-// dequantises them exactly to bf16 and scales each output by row_scale of its
-// token times the group's weight scale.
-// small != 0 (MXFP8 / NVFP4 weights, batches of at most kOneSmMaxTokens): the
+// small != 0 (MXFP8 weights, batches of at most kOneSmMaxTokens): the
 // weight-streaming variant with 64-token tiles and a deeper weight ring.
 cudaError_t launch_pair_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s,
                              int wfmt = 0, int small = 0);
 
-// The expert GEMMs with MXFP8 weights and MXFP8 token rows (gemm_mx8.cu), on the
-// block-scaled tensor-core MMA: a0/a1 (gate, up) or a0 (down) map the E4M3
-// weights with 128-byte boxes and the 128-byte swizzle (64 or 128 rows), sa0/sa1
-// their E8M0 scales (16-byte boxes); b32 the gathered E4M3 token rows (128-byte
-// boxes of 32 rows, swizzled) and sb_scale their scales (16-byte x 128-row
-// boxes); K is in blocks of mx8_k_block() (KB a multiple of 4); tiles of at most
-// mx8_tile_tokens() tokens; no shared expert.
-cudaError_t launch_mx8_gemm(int mode, const GemmParams& p, int clusters, cudaStream_t s);
-int mx8_tile_tokens();
-int mx8_k_block();
+// The expert GEMMs on the block-scaled tensor-core MMA (gemm_bs.cu), both
+// operands narrow.  fmt BS_MXFP8: E4M3 weights and token rows with E8M0 scales
+// per 32; fmt BS_NVFP4: packed E2M1 weights and token rows (two per byte) with
+// E4M3 scales per 16, each output then scaled by row_scale of its token times
+// the group's wscale0 (gate, down) or wscale1 (up).  a0/a1 (gate, up) or a0
+// (down) map the weights with 128-byte boxes and the 128-byte swizzle (64 or
+// 128 rows), sa0/sa1 their scales; b and b32 the gathered token rows (128-byte
+// boxes of bs_big_box(fmt) and of 32 rows, swizzled) and sb_scale their scales
+// (128-row boxes).  Scale boxes are bs_scale_box(fmt) bytes wide.  K runs in
+// blocks of 128 bytes (KB a multiple of bs_scale_kb(fmt)); tiles of at most
+// bs_tile_tokens(fmt) tokens; no shared expert.
+constexpr int BS_MXFP8 = 0;
+constexpr int BS_NVFP4 = 1;
+cudaError_t launch_bs_gemm(int fmt, int mode, const GemmParams& p, int clusters, cudaStream_t s);
+int bs_tile_tokens(int fmt);
+int bs_big_box(int fmt);
+int bs_scale_box(int fmt);
+int bs_scale_kb(int fmt);
 // MXFP8 quantisation of R rows of K bf16 values (K % 256 == 0) in blocks of 32
 // along the row: E4M3 codes to codes [R][K] and E8M0 scale bytes to scales
 // [R][K/32] (OCP MX v1.0: X = floor(log2 max|v|) - 8, codes E4M3(v / 2^X)
@@ -166,12 +170,11 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* inv, int64_t T, int 
                           int n_shared, uint16_t* xp, cudaStream_t s,
                           const float* scale_in = nullptr, float* scale_out = nullptr);
 
-// NVFP4 activations (per-token scales): quantise R rows of K bf16 values and
-// write the bf16 values e2m1 * e4m3 block scale (exact) to dst (may be src),
-// the fp32 row scales to rscale and, if not null, the E4M3 block scales.
-cudaError_t launch_nvfp4_qdq(const uint16_t* src, uint16_t* dst, uint8_t* bscale, float* rscale,
-                             int64_t R, int K, int sms, cudaStream_t s);
-
+// NVFP4 quantisation of R rows of K bf16 values (K % 16 == 0), per row: codes
+// [R][K/2] bytes (two E2M1 codes, element 2j in the low nibble), bscale
+// [R][K/16] E4M3 block scales, rscale [R] the fp32 row scale (nvfp4.cu).
+cudaError_t launch_nvfp4_codes(const uint16_t* src, uint8_t* codes, uint8_t* bscale, float* rscale,
+                               int64_t R, int K, int sms, cudaStream_t s);
 // ---- backward (backward.cu, wgrad.cu) ----
 
 // Grouped weight-gradient GEMM: for group g, out[g][n][m] = sum over the

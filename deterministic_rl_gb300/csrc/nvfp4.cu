@@ -9,9 +9,9 @@
 //   S_b = E4M3(amax(block) / 6 / s)   nearest even, saturating at 448
 //   q_i = E2M1(x_i / (S_b * s))       nearest, ties to the even code, +-6 at most
 // (s = 0 for an all-zero row; a block whose S_b is 0 has all codes 0; zero is
-// always +0).  The kernel writes, per row, s and the bf16 values e2m1(q_i) *
-// e4m3(S_b) -- exact in bf16 (at most 6 significant bits) -- which the expert
-// GEMMs take as their token operand; s is applied in the GEMM epilogue.
+// always +0).  The kernel writes the E2M1 codes (two per byte, element 2j in
+// the low nibble), the E4M3 bytes S_b and s: the operands of the block-scaled
+// FP4 expert GEMMs, which apply s in their epilogue.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -42,33 +42,43 @@ __device__ __forceinline__ int e2m1_index(float a) {
            (a > 5.0f);
 }
 
-__device__ __forceinline__ float e2m1_magnitude(int m) {
-    // 0, 0.5, 1, 1.5, 2, 3, 4, 6
-    return m < 4 ? 0.5f * m : (m == 7 ? 6.0f : static_cast<float>(m - 2));
-}
-
-// Quantise one value and return the bf16 bits of e2m1(q) * S (exact).
-__device__ __forceinline__ uint32_t qdq_one(float v, float denom, float Sf) {
+// The E2M1 code (sign bit 8, magnitude index 0..7) of one value; zero is +0.
+__device__ __forceinline__ uint32_t code_one(float v, float denom) {
     if (!(denom > 0.0f)) return 0u;
     const float t = __fdiv_rn(v, denom);
     const int m = e2m1_index(fabsf(t));
-    float val = e2m1_magnitude(m) * Sf;  // exact: <= 6 significant bits
-    if (t < 0.0f && m != 0) val = -val;
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(val)));
+    return static_cast<uint32_t>(m) | (t < 0.0f && m != 0 ? 8u : 0u);
 }
 
-__device__ __forceinline__ uint32_t qdq_pair(uint32_t w, float denom, float Sf) {
-    return qdq_one(bf16_lo(w), denom, Sf) | (qdq_one(bf16_hi(w), denom, Sf) << 16);
+// Four bf16 pairs (8 values) -> 8 codes, element 0 in the lowest nibble.
+__device__ __forceinline__ uint32_t codes8(const uint4& a, float denom) {
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+    uint32_t r = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        r |= (code_one(bf16_lo(w[i]), denom) | (code_one(bf16_hi(w[i]), denom) << 4)) << (8 * i);
+    return r;
 }
 
-// src and dst may be the same rows (in place): a lane reads its blocks in full
-// before it writes them, and no lane touches another lane's blocks.
-__global__ void __launch_bounds__(32 * kWarps) nvfp4_qdq_kernel(
-    const uint4* src, uint4* dst, uint8_t* __restrict__ bscale,
+// The block scale S_b of a 16-value block with largest magnitude bmax, as its
+// E4M3 byte (0 when the row scale is 0).
+__device__ __forceinline__ __nv_fp8_storage_t block_scale(float bmax, float s) {
+    if (!(s > 0.0f)) return 0;
+    return __nv_cvt_float_to_fp8(__fdiv_rn(__fdiv_rn(bmax, 6.0f), s), __NV_SATFINITE, __NV_E4M3);
+}
+
+__device__ __forceinline__ float e4m3_value(__nv_fp8_storage_t S) {
+    return __half2float(__half(__nv_cvt_fp8_to_halfraw(S, __NV_E4M3)));
+}
+
+// One warp per row (a lane per 16-value block): codes [R][K/2] bytes,
+// bscale [R][K/16] E4M3 bytes, rscale [R] fp32.
+__global__ void __launch_bounds__(32 * kWarps) nvfp4_codes_kernel(
+    const uint4* __restrict__ src, uint2* __restrict__ codes, uint8_t* __restrict__ bscale,
     float* __restrict__ rscale, int64_t R, int K) {
     const int lane = threadIdx.x & 31;
-    const int nb = K / 16;        // 16-value blocks per row, 2 uint4 each
-    const int vpr = K / 8;        // uint4 per row
+    const int nb = K / 16;
+    const int vpr = K / 8;
     for (int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); r < R;
          r += static_cast<int64_t>(gridDim.x) * kWarps) {
         const uint4* row = src + r * vpr;
@@ -78,43 +88,27 @@ __global__ void __launch_bounds__(32 * kWarps) nvfp4_qdq_kernel(
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         const float s = __fdiv_rn(amax, 2688.0f);  // 6 * 448
         if (lane == 0) rscale[r] = s;
-        uint4* out = dst + r * vpr;
         for (int b = lane; b < nb; b += 32) {
             const uint4 a0 = row[2 * b], a1 = row[2 * b + 1];
-            const float bmax = absmax8(a1, absmax8(a0, 0.0f));
-            __nv_fp8_storage_t S = 0;
-            if (s > 0.0f)
-                S = __nv_cvt_float_to_fp8(__fdiv_rn(__fdiv_rn(bmax, 6.0f), s), __NV_SATFINITE,
-                                          __NV_E4M3);
-            const float Sf = __half2float(__half(__nv_cvt_fp8_to_halfraw(S, __NV_E4M3)));
-            const float denom = __fmul_rn(Sf, s);
-            uint4 o0, o1;
-            o0.x = qdq_pair(a0.x, denom, Sf);
-            o0.y = qdq_pair(a0.y, denom, Sf);
-            o0.z = qdq_pair(a0.z, denom, Sf);
-            o0.w = qdq_pair(a0.w, denom, Sf);
-            o1.x = qdq_pair(a1.x, denom, Sf);
-            o1.y = qdq_pair(a1.y, denom, Sf);
-            o1.z = qdq_pair(a1.z, denom, Sf);
-            o1.w = qdq_pair(a1.w, denom, Sf);
-            out[2 * b] = o0;
-            out[2 * b + 1] = o1;
-            if (bscale) bscale[r * nb + b] = S;
+            const __nv_fp8_storage_t S = block_scale(absmax8(a1, absmax8(a0, 0.0f)), s);
+            const float denom = __fmul_rn(e4m3_value(S), s);
+            codes[r * nb + b] = make_uint2(codes8(a0, denom), codes8(a1, denom));
+            bscale[r * nb + b] = S;
         }
     }
 }
 
 }  // namespace
 
-cudaError_t launch_nvfp4_qdq(const uint16_t* src, uint16_t* dst, uint8_t* bscale, float* rscale,
-                             int64_t R, int K, int sms, cudaStream_t s) {
+cudaError_t launch_nvfp4_codes(const uint16_t* src, uint8_t* codes, uint8_t* bscale, float* rscale,
+                               int64_t R, int K, int sms, cudaStream_t s) {
     if (R == 0) return cudaSuccess;
     if (K % 16) return cudaErrorInvalidValue;
     int64_t blocks = (R + kWarps - 1) / kWarps;
     const int64_t cap = static_cast<int64_t>(sms) * 8;
     if (blocks > cap) blocks = cap;
-    nvfp4_qdq_kernel<<<static_cast<unsigned>(blocks), 32 * kWarps, 0, s>>>(
-        reinterpret_cast<const uint4*>(src), reinterpret_cast<uint4*>(dst), bscale, rscale, R, K);
+    nvfp4_codes_kernel<<<static_cast<unsigned>(blocks), 32 * kWarps, 0, s>>>(
+        reinterpret_cast<const uint4*>(src), reinterpret_cast<uint2*>(codes), bscale, rscale, R, K);
     return cudaGetLastError();
 }
 

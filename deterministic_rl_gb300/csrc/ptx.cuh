@@ -372,6 +372,34 @@ __device__ __forceinline__ void umma_mx8_pair(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
+// ---- block-scaled MMA (NVFP4 x NVFP4) ---------------------------------------------
+
+// Instruction descriptor of tcgen05.mma.kind::mxf4nvf4.block_scale with A and B
+// E2M1 (format 1 at bits 7-9 and 10-12), K-major, E4M3 scales (scale type bit
+// 23 clear): N / 8 at bits 17-22, M / 16 at bits 24-28.  With scale_vec::4X a
+// K step (64 values) takes one 32-bit scale word per row, its bytes the four
+// 16-value blocks in order, so the scale ids stay 0.  Checked on the GPU
+// against exact sums of E2M1 products.
+__host__ __device__ constexpr uint32_t idesc_nv4(int M, int N) {
+    return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) |
+           (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Leader CTA, single thread: one K step of 64 E2M1 values (32 bytes) per row,
+// D (+)= sum over its four 16-blocks of (A . B^T) x sa x sb.  Scale layout as
+// for umma_mx8_pair, one word per row and K step.
+__device__ __forceinline__ void umma_nv4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                              uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+        "r"(accumulate)
+        : "memory");
+}
+
 // Whole warp: lane i writes 1 (or 8) consecutive 32-bit columns of TMEM lane
 // (taddr's lane + i); the warp's lane quadrant must be taddr's.
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {

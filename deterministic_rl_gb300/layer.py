@@ -146,7 +146,16 @@ class MoELayer:
             r["h8"] = view(L.hq, T * k * F, torch.uint8).view(T * k, F)
             r["hs"] = ws[L.hq + T * k * F:L.hq + T * k * F + T * k * F // 32].view(T * k, F // 32)
         if self.wfmt == B.MOE_W_NVFP4:
-            r["xq"] = view(L.xq, T * d, torch.bfloat16).view(T, d)
+            # packed E2M1 codes (element 2j in the low nibble of byte j), E4M3
+            # block scales per 16 and fp32 row scales of x, the gathered rows
+            # and h
+            tk = T * k
+            r["x4"] = view(L.xq, T * d // 2, torch.uint8).view(T, d // 2)
+            r["xb"] = ws[L.xq + T * d // 2:L.xq + T * d // 2 + T * d // 16].view(T, d // 16)
+            r["xp4"] = view(L.xp, tk * d // 2, torch.uint8).view(tk, d // 2)
+            r["xpb"] = ws[L.xp + tk * d // 2:L.xp + tk * d // 2 + tk * d // 16].view(tk, d // 16)
+            r["h4"] = view(L.hq, tk * F // 2, torch.uint8).view(tk, F // 2)
+            r["hb"] = ws[L.hq + tk * F // 2:L.hq + tk * F // 2 + tk * F // 16].view(tk, F // 16)
             r["sx"] = view(L.sx, T, torch.float32)
             r["sxp"] = view(L.sxp, T * k, torch.float32)
             r["sh"] = view(L.sh, T * k, torch.float32)

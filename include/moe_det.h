@@ -167,12 +167,15 @@ typedef struct {
  *   h        bf16 [T*k + T*n_shared][F]  SwiGLU activations
  *   y        bf16 [T*k][d]               routed expert outputs (dst order)
  *   ysh      fp32 [T][d]                 shared expert output
- *   MOE_W_NVFP4 only (else empty):
- *   xq       bf16 [T][d]   each token row quantised: e2m1 * e4m3 block scale
+ *   MOE_W_NVFP4 only (else empty): the NVFP4 activations as packed E2M1
+ *   codes (element 2j in the low nibble of byte j) and E4M3 block scales:
+ *   xq       u8 [T][d/2] codes, then u8 [T][d/16] scales of each token row of x
  *   sx       fp32 [T]      each token row's fp32 scale
+ *   xp       u8 [T*k][d/2] codes, then u8 [T*k][d/16] scales: the gathered rows
  *   sxp      fp32 [T*k]    the scale of each gathered row of xp
- *   sh       fp32 [T*k]    the scale of each row of h (h itself then holds
- *                          e2m1 * e4m3 of the quantised activations)
+ *   hq       u8 [T*k][F/2] codes, then u8 [T*k][F/16] scales of each row of h
+ *            (h keeps the bf16 SwiGLU output)
+ *   sh       fp32 [T*k]    the scale of each row of h
  *   MOE_W_MXFP8_ACT: the MXFP8 activations as E4M3 codes and E8M0 scales:
  *   xq       u8 [T][d] codes, then u8 [T][d/32] scales of each token row of x
  *   xp       u8 [T*k][d] codes, then u8 [T*k][d/32] scales: the gathered rows

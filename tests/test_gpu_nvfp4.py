@@ -1,8 +1,10 @@
 """The NVFP4 forward with per-token scales (Composer 2 Technical Report, §6.1,
 Kernels: BF16 values quantised to FP4 E2M1 with an FP8 E4M3 scale per 16 and
-an FP32 scale per token, IEEE division in the quantiser) on the GPU:
+an FP32 scale per token, IEEE division in the quantiser; block-scaled
+tensor-core matmul) on the GPU:
   * the token-row quantiser, bitwise against the oracle's (both take their
-    rounding decisions on the same fp32 quotients);
+    rounding decisions on the same fp32 quotients): codes, block scales and
+    row scales, of x and of h;
   * the layer against the oracle (which quantises its own h, rounded to bf16,
     the same way);
   * batch invariance, bitwise: a token's scales depend on that token only."""
@@ -30,13 +32,19 @@ def small_nv(T=300, E=32, seed=51):
 
 
 def _expect_quantised(x_bf16: torch.Tensor):
-    """The oracle's quantisation of bf16 rows: (values e2m1 * e4m3 as fp64,
-    row scales fp32, block scales)."""
+    """The oracle's quantisation of bf16 rows: (codes [R][K] 0..15, E4M3 block
+    scales [R][K/16], fp32 row scales [R])."""
     xf = torch.from_numpy(bf16_bits(x_bf16).view(np.int16)).view(torch.bfloat16).float().numpy()
-    codes, bs, rs = oracle.nvfp4_quantize_rows(xf)
-    tab = np.array([oracle.e2m1_to_f64(c) for c in range(16)])
-    sc = np.array([oracle.e4m3_to_f64(b) for b in range(256)])
-    return tab[codes] * np.repeat(sc[bs], 16, axis=1), rs, bs
+    return oracle.nvfp4_quantize_rows(xf)
+
+
+def _unpack(packed: torch.Tensor) -> np.ndarray:
+    """Packed bytes [R][K/2] -> codes [R][K] (element 2j in the low nibble)."""
+    b = packed.cpu().numpy()
+    out = np.empty((b.shape[0], 2 * b.shape[1]), np.uint8)
+    out[:, 0::2] = b & 15
+    out[:, 1::2] = b >> 4
+    return out
 
 
 @pytest.mark.parametrize("T", [1, 37, 300])
@@ -53,9 +61,9 @@ def test_token_quantiser_bitwise_against_oracle(T):
     layer.forward(x)
     assert layer.status() == B.MOE_OK
     im = layer.intermediates(T)
-    vals, rs, _ = _expect_quantised(x)
-    got = im["xq"].double().cpu().numpy()
-    assert np.array_equal(got, vals)
+    codes, bs, rs = _expect_quantised(x)
+    assert np.array_equal(_unpack(im["x4"]), codes)
+    assert np.array_equal(im["xb"].cpu().numpy(), bs)
     assert np.array_equal(im["sx"].cpu().numpy(), rs)
 
 
@@ -67,31 +75,22 @@ def test_gathered_rows_carry_their_token_scale():
     perm = im["perm"].long()
     tok = perm // 8
     assert torch.equal(im["sxp"], im["sx"][tok])
-    assert torch.equal(im["xp"][: 200 * 8], im["xq"][tok])
+    assert torch.equal(im["xp4"], im["x4"][tok])
+    assert torch.equal(im["xpb"], im["xb"][tok])
 
 
-def test_activation_rows_are_quantised_values():
-    """h after the call holds e2m1 * e4m3 of each row's quantisation: every
-    16-value block is a set of E2M1 magnitudes times one E4M3 scale, and the
-    row scales are the rows' amax / 2688 up to that quantisation."""
+def test_activation_rows_quantised_like_the_oracle():
+    """Each row of h (the bf16 SwiGLU output) is quantised like the oracle
+    quantises it: codes, block scales and row scales bitwise."""
     inp = make_layer(small_nv(64), "cuda")
     layer = MoELayer.from_inputs(inp, out_fp32=True)
     layer.forward(inp.x)
     im = layer.intermediates(64)
-    h = im["h"].float().cpu().numpy().reshape(-1, 16)
-    sh = im["sh"].cpu().numpy()
-    mags = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
-    e4m3 = np.array([oracle.e4m3_to_f64(b) for b in range(0x7F)])
-    bmax = np.abs(h).max(axis=1)
-    nz = bmax > 0
-    # the largest value of a nonzero block is 6 x its E4M3 scale (see the
-    # oracle's pins: a block's largest magnitude becomes 6)
-    S = bmax[nz] / 6.0
-    exact = np.isin(S, e4m3)
-    assert exact.mean() > 0.99
-    ratio = np.abs(h[nz][exact]) / S[exact][:, None]
-    assert np.isin(ratio, mags).all()
-    assert (sh >= 0).all() and (sh > 0).mean() > 0.99
+    codes, bs, rs = _expect_quantised(im["h"])
+    assert np.array_equal(_unpack(im["h4"]), codes)
+    assert np.array_equal(im["hb"].cpu().numpy(), bs)
+    assert np.array_equal(im["sh"].cpu().numpy(), rs)
+    assert (rs > 0).mean() > 0.99
 
 
 @pytest.mark.parametrize("T,E", [(1, 16), (130, 32), (300, 32)])
@@ -149,8 +148,10 @@ def test_nvfp4_full_size_sampled_parity_and_invariance():
     assert layer.status() == B.MOE_OK
     im = layer.intermediates(cfg.T)
     tk = np.array([0, 1, 777, 8191, 16383])
-    vals, rs, _ = _expect_quantised(inp.x[torch.as_tensor(tk, device="cuda")])
-    assert np.array_equal(im["xq"][torch.as_tensor(tk, device="cuda")].double().cpu().numpy(), vals)
+    sel = torch.as_tensor(tk, device="cuda")
+    codes, bs, rs = _expect_quantised(inp.x[sel])
+    assert np.array_equal(_unpack(im["x4"][sel]), codes)
+    assert np.array_equal(im["xb"][sel].cpu().numpy(), bs)
     assert np.array_equal(im["sx"].cpu().numpy()[tk], rs)
     part = MoELayer.from_inputs(inp, out_fp32=True).forward(inp.x[:512].contiguous())
     for a, b in zip((out, ids, gates), part):
