@@ -31,7 +31,6 @@ namespace moe {
 namespace {
 
 constexpr int kK8 = 128;                   // bytes per stage and row (K block)
-constexpr int kHalf8 = 128;                // token rows per CTA in shared memory (at most)
 constexpr int kStages8 = 5;
 constexpr uint32_t kA8 = 128 * kK8;        // weight tile of a CTA: 16 KB
 constexpr uint32_t kBox8 = 32 * kK8;       // one 32-row token box
@@ -45,10 +44,11 @@ constexpr uint32_t kTmemCols8 = 512;
 //   kTile     tokens per tile (MMA N at most);
 //   kBigBox   token rows of the one-copy box of a CTA's rows (3 or 4 32-row boxes);
 //   kScRow    scale bytes per row and K block; kScKb K blocks per scale slot;
-//   kSfKb     TMEM columns of one K block's scales: per K step 4 columns of
-//             weight-row scales and 8 of token scales (MXFP8: one word per row
-//             serves the block's four K steps, a byte each; NVFP4: a word per
-//             K step);
+//   kSfKb     TMEM columns of one K block's scales.  MXFP8: one word per row
+//             serves the block's four K steps (a byte each): 4 columns of
+//             weight-row scales, then 8 of token scales.  NVFP4: a word per row
+//             and K step: K step w's weight-row scales at columns 4w .. 4w + 3,
+//             its token scales at 16 + 8w .. 16 + 8w + 7;
 //   kSfSets   sets of those columns in flight.  MXFP8: one per stage, reused
 //             once the stage's MMAs complete; NVFP4: two, each freed by its
 //             own commit (the accumulators leave room for no more).
@@ -294,7 +294,10 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
             // ---------------- TMA producer (both CTAs) ----------------
             tma_prefetch_desc(&p.a0);
             tma_prefetch_desc(&p.b32);
-            const uint64_t pol_w = l2_policy_evict_first();
+            // weights: normal eviction, so that the next token tile of the
+            // same weight tile, usually running at the same time on another
+            // pair, still finds them in L2
+            const uint64_t pol_w = l2_policy_evict_normal();
             const uint64_t pol_x = l2_policy_evict_last();
             int stage = 0, ss = 0;
             uint32_t phase = 0, sph = 0;
@@ -397,8 +400,8 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
                         const uint32_t sfa = tmem_base + L::kSfCol + sfs * C::kSfKb;
 #pragma unroll
                         for (int k = 0; k < 4; ++k)
-                            umma_nv4_pair(d0, da + 2 * k, db + 2 * k, idesc, sfa + 12 * k,
-                                          sfa + 12 * k + 4, (kb | k) != 0);
+                            umma_nv4_pair(d0, da + 2 * k, db + 2 * k, idesc, sfa + 4 * k,
+                                          sfa + 16 + 8 * k, (kb | k) != 0);
                         umma_commit_pair(&sffree[sfs], 0x3);
                         if (++sfs == C::kSfSets) sfs = 0;
                     } else {
@@ -499,24 +502,45 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
                 const uint8_t* sc = scring + ss * L::kScSlot;
                 const int kq = kb % kScKb;
                 const uint32_t sf = tmem_base + lane_base + L::kSfCol + set * C::kSfKb;
-                // MXFP8: one word per row (its 4 bytes the block's 4 K steps);
-                // NVFP4: one word per row and K step (its bytes the 4 16-blocks)
-                constexpr int kWords = kNv ? 4 : 1;
+                if constexpr (kNv) {
+                    // a row's four K-step words are one 16-byte load; this
+                    // quadrant's lanes of columns 4w .. 4w + 3 all get K step w's
+                    // word (the MMA reads column 4w + q)
+                    const uint4 a = *reinterpret_cast<const uint4*>(
+                        sc + (32 * q + lane) * L::kScRowBytes + kq * 16);
+                    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+                    uint32_t av[16];
 #pragma unroll
-                for (int w = 0; w < kWords; ++w) {
-                    const int off = kq * C::kScRow + w * 4;
-                    tmem_st1(sf + 12 * w + q,
-                             *reinterpret_cast<const uint32_t*>(sc + (32 * q + lane) * L::kScRowBytes + off));
+                    for (int c = 0; c < 16; ++c) av[c] = aw[c >> 2];
+                    uint32_t bv[32];
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int n = 32 * c + lane;  // token column of the MMA
+                        const int r = n < tl.half ? n : 128 + n - tl.half;
+                        uint4 b = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+                        if (n < n_cols)
+                            b = *reinterpret_cast<const uint4*>(sc + L::kScA + r * L::kScRowBytes + kq * 16);
+                        bv[c] = b.x;
+                        bv[8 + c] = b.y;
+                        bv[16 + c] = b.z;
+                        bv[24 + c] = b.w;
+                    }
+                    tmem_st16(sf, av);
+                    tmem_st32(sf + 16, bv);
+                } else {
+                    // one word per row: its 4 bytes are the block's 4 K steps
+                    tmem_st1(sf + q, *reinterpret_cast<const uint32_t*>(
+                                         sc + (32 * q + lane) * L::kScRowBytes + kq * C::kScRow));
                     uint32_t bw[8];
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         const int n = 32 * c + lane;  // token column of the MMA
                         const int r = n < tl.half ? n : 128 + n - tl.half;
                         bw[c] = n < n_cols ? *reinterpret_cast<const uint32_t*>(
-                                                 sc + L::kScA + r * L::kScRowBytes + off)
-                                           : (kNv ? 0x38383838u : 0x7F7F7F7Fu);  // 1.0
+                                                 sc + L::kScA + r * L::kScRowBytes + kq * C::kScRow)
+                                           : 0x7F7F7F7Fu;  // 1.0
                     }
-                    tmem_st8(sf + 12 * w + 4, bw);
+                    tmem_st8(sf + 4, bw);
                 }
                 tmem_st_wait();
                 tc_fence_before();
