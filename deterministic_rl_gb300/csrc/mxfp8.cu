@@ -6,7 +6,7 @@
 // each row of the SwiGLU output h (stored in bf16) along F, in blocks of 32
 // (mx.cuh), into E4M3 codes and E8M0 scale bytes; the expert GEMMs then
 // multiply the MXFP8 values of both operands on the block-scaled tensor-core
-// MMA (gemm_mx8.cu).
+// MMA (gemm_bs.cu).
 #include <cuda_bf16.h>
 
 #include <cstdint>
