@@ -31,7 +31,6 @@ namespace moe {
 namespace {
 
 constexpr int kK8 = 128;                   // bytes per stage and row (K block)
-constexpr int kStages8 = 5;
 constexpr uint32_t kA8 = 128 * kK8;        // weight tile of a CTA: 16 KB
 constexpr uint32_t kBox8 = 32 * kK8;       // one 32-row token box
 constexpr int kThreads8 = 352;
@@ -41,7 +40,7 @@ constexpr int kMaxGroups8 = 1024;
 constexpr uint32_t kTmemCols8 = 512;
 
 // Per format:
-//   kTile     tokens per tile (MMA N at most);
+//   kTile     tokens per tile (MMA N at most); kStages operand stages;
 //   kBigBox   token rows of the one-copy box of a CTA's rows (3 or 4 32-row boxes);
 //   kScRow    scale bytes per row and K block; kScKb K blocks per scale slot;
 //   kSfKb     TMEM columns of one K block's scales.  MXFP8: one word per row
@@ -57,12 +56,14 @@ struct BsCfg;
 template <>
 struct BsCfg<BS_MXFP8> {
     static constexpr int kTile = 224, kBigBox = 128, kScRow = 4, kScKb = 4, kScSlots = 4;
+    static constexpr int kStages = 5;
     static constexpr uint32_t kSfKb = 12;
-    static constexpr int kSfSets = kStages8;
+    static constexpr int kSfSets = kStages;
 };
 template <>
 struct BsCfg<BS_NVFP4> {
     static constexpr int kTile = 192, kBigBox = 96, kScRow = 16, kScKb = 2, kScSlots = 3;
+    static constexpr int kStages = 5;
     static constexpr uint32_t kSfKb = 48;
     static constexpr int kSfSets = 2;
 };
@@ -82,7 +83,7 @@ struct BsLayout {
     // TMEM: two accumulator slots of kTile columns, then the scale column sets
     static constexpr uint32_t kAcc = C::kTile;
     static constexpr uint32_t kSfCol = 2 * kAcc;
-    static constexpr int kBarriers = 2 * kStages8 + 2 * C::kScSlots + C::kSfSets + 2 + 2 + 4 + 1;
+    static constexpr int kBarriers = 2 * C::kStages + 2 * C::kScSlots + C::kSfSets + 2 + 2 + 4 + 1;
     static_assert(kSfCol + C::kSfSets * C::kSfKb <= kTmemCols8, "TMEM columns");
     static_assert(kStage % 1024 == 0, "stages keep the 128-byte swizzle's alignment");
 };
@@ -184,13 +185,14 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
     constexpr int kTile = C::kTile;
     constexpr int kScKb = C::kScKb;
     constexpr int kScSlots = C::kScSlots;
+    constexpr int kStages = C::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
-    uint8_t* scring = smem + kStages8 * L::kStage;
+    uint8_t* scring = smem + kStages * L::kStage;
     float* xbuf = reinterpret_cast<float*>(scring + kScSlots * L::kScSlot);
     uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(xbuf) + kXBytes8);
-    uint64_t* empty = full + kStages8;
-    uint64_t* scfull = empty + kStages8;
+    uint64_t* empty = full + kStages;
+    uint64_t* scfull = empty + kStages;
     uint64_t* scempty = scfull + kScSlots;
     uint64_t* sffree = scempty + kScSlots;  // NVFP4: a TMEM scale set's MMAs completed
     uint64_t* tfull = sffree + C::kSfSets;
@@ -248,7 +250,7 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
         tmem_alloc_pair(tmem_slot, kTmemCols8);
         tmem_relinquish_pair();
     } else if (threadIdx.x == 64) {
-        for (int s = 0; s < kStages8; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1 + 2 * 4);  // producer + the scale writers of both CTAs
             mbar_init(&empty[s], 1);
         }
@@ -353,14 +355,14 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
                     }
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
-                    if (++stage == kStages8) {
+                    if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
             if (leader)
-                for (int s = 0; s < kStages8; ++s)
+                for (int s = 0; s < kStages; ++s)
                     if (issued & (1u << s))
                         if (!mbar_wait(&full[s], (last_par >> s) & 1u, nullptr, tmo))
                             raise_timeout8(p, abort, 42);
@@ -412,7 +414,7 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
                                           sfa + 4, (kb | k) != 0);
                     }
                     umma_commit_pair(&empty[stage], 0x3);
-                    if (++stage == kStages8) {
+                    if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -457,7 +459,7 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
                             tma_load_2d_pair(st + kA8 + i * kBox8, &p.b32, bar, kb * kK8, brow + 32 * i,
                                              pol_x);
                     }
-                    if (++stage == kStages8) {
+                    if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
@@ -554,7 +556,7 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
                         mbar_arrive_operand_ready(map_to_rank(&full[stage], 0));
                     if (kq == kScKb - 1) mbar_arrive(&scempty[ss]);
                 }
-                if (++stage == kStages8) {
+                if (++stage == kStages) {
                     stage = 0;
                     phase ^= 1u;
                 }
@@ -667,7 +669,7 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
 template <int FMT>
 size_t bs_smem_bytes(int GG) {
     using L = BsLayout<FMT>;
-    return 1024 + kStages8 * L::kStage + BsCfg<FMT>::kScSlots * L::kScSlot + kXBytes8 +
+    return 1024 + BsCfg<FMT>::kStages * L::kStage + BsCfg<FMT>::kScSlots * L::kScSlot + kXBytes8 +
            L::kBarriers * 8 + 16 + static_cast<size_t>(4 * GG + 2) * 4;
 }
 
