@@ -26,6 +26,7 @@
 
 #include "moe_internal.h"
 #include "ptx.cuh"
+#include "tile_walk.cuh"
 
 namespace moe {
 namespace {
@@ -93,54 +94,17 @@ struct Tile8 {
     int half;  // MMA N / 2
 };
 
-struct Sched8 {
-    const int* hs;
-    const int* cs;
-    const int* gcnt;
-    const int* goff;
-    int GG;
-    int64_t H, N;
-};
-
-__device__ __forceinline__ int find_group8(const int* start, int GG, int j) {
-    int lo = 0, hi = GG;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (start[mid] <= j) lo = mid; else hi = mid;
-    }
-    return lo;
-}
-
-// Tile t of the order: experts with several token tiles ("hot") and with one
-// ("cold") are interleaved in proportion, so that every wave mixes
-// tensor-bound and weight-streaming tiles; the token tiles of a hot expert's
-// weight tile are consecutive.  Which pair computes a tile never changes how.
+// The tile at list position (g, m, nt): its token rows and the CTA's weight rows.
 template <int MODE, int FMT>
-__device__ __forceinline__ Tile8 decode_tile8(int t, uint32_t rank, const GemmParams& p,
-                                              const Sched8& sc) {
+__device__ __forceinline__ Tile8 make_tile8(const TilePos& pos, uint32_t rank, const GemmParams& p,
+                                            const int* gcnt, const int* goff) {
     constexpr int kTile8 = BsCfg<FMT>::kTile;
     Tile8 tl;
-    const int64_t h0 = static_cast<int64_t>(t) * sc.H / sc.N;
-    const int64_t h1 = static_cast<int64_t>(t + 1) * sc.H / sc.N;
-    int nt;
-    if (h1 > h0) {
-        const int j = static_cast<int>(h0);
-        const int g = find_group8(sc.hs, sc.GG, j / p.MT);
-        const int ntg = sc.hs[g + 1] - sc.hs[g];
-        const int l = j - sc.hs[g] * p.MT;
-        tl.g = g;
-        tl.m = l / ntg;
-        nt = l - tl.m * ntg;
-    } else {
-        const int j = t - static_cast<int>(h0);
-        const int g = find_group8(sc.cs, sc.GG, j / p.MT);
-        tl.g = g;
-        tl.m = j - sc.cs[g] * p.MT;
-        nt = 0;
-    }
-    tl.n_valid = min(kTile8, sc.gcnt[tl.g] - nt * kTile8);
+    tl.g = pos.g;
+    tl.m = pos.m;
+    tl.n_valid = min(kTile8, gcnt[tl.g] - pos.nt * kTile8);
     tl.half = min(kTile8, max(64, (tl.n_valid + 31) & ~31)) >> 1;
-    tl.brow = sc.goff[tl.g] + nt * kTile8;
+    tl.brow = goff[tl.g] + pos.nt * kTile8;
     tl.arow = tl.g * p.M + tl.m * 2 * gemm_rows(MODE) + static_cast<int>(rank) * gemm_rows(MODE);
     return tl;
 }
@@ -274,16 +238,13 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
     cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
-    const Sched8 sched{hs, cs, gcnt, goff, GG, static_cast<int64_t>(hs[GG]) * p.MT,
-                       static_cast<int64_t>(hs[GG] + cs[GG]) * p.MT};
-    const int total = static_cast<int>(sched.N);
+    // the static tile order (tile_walk.cuh); this pair takes positions cid,
+    // cid + ncl, ...
+    const TileOrder order{hs, cs, GG, p.MT, static_cast<uint32_t>(hs[GG] * p.MT),
+                          static_cast<uint32_t>((hs[GG] + cs[GG]) * p.MT)};
     const uint64_t tmo = p.timeout_ns;
     const int cid = static_cast<int>(cluster_id_x());
     const int ncl = static_cast<int>(nclusters_x());
-    auto tile_at = [&](int j) -> int {
-        const int64_t t = cid + static_cast<int64_t>(j) * ncl;
-        return t < total ? static_cast<int>(t) : -1;
-    };
     // a CTA's token rows: one kBigBox-row box when they need three or more
     // 32-row boxes (fewer copies), else 32-row boxes
     auto token_boxes = [](int rows) {
@@ -305,10 +266,8 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
             uint32_t phase = 0, sph = 0;
             uint32_t issued = 0, last_par = 0, s_issued = 0, s_par = 0;
             bool ok = p.stall_test == 0;
-            for (int j = 0; ok; ++j) {
-                const int t = tile_at(j);
-                if (t < 0) break;
-                const Tile8 tl = decode_tile8<MODE, FMT>(t, rank, p, sched);
+            for (TileWalk w = tile_walk_begin(cid, order); ok && w.t >= 0; tile_walk_next(w, ncl, order)) {
+                const Tile8 tl = make_tile8<MODE, FMT>(tile_walk_pos(w, order), rank, p, gcnt, goff);
                 const uint32_t expect =
                     2 * kA8 + (token_boxes(b_rows8(tl, 0)) + token_boxes(b_rows8(tl, 1))) * kBox8;
                 for (int kb = 0; kb < p.KB; ++kb) {
@@ -377,15 +336,13 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
             int stage = 0, acc = 0, sfs = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int j = 0; ok; ++j) {
-                const int t = tile_at(j);
-                if (t < 0) break;
+            for (TileWalk w = tile_walk_begin(cid, order); ok && w.t >= 0; tile_walk_next(w, ncl, order)) {
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort, tmo)) {
                     if (!*abort) raise_timeout8(p, abort, 44);
                     break;
                 }
                 tc_fence_after();
-                const Tile8 tl = decode_tile8<MODE, FMT>(t, rank, p, sched);
+                const Tile8 tl = make_tile8<MODE, FMT>(tile_walk_pos(w, order), rank, p, gcnt, goff);
                 const uint32_t d0 = tmem_base + acc * L::kAcc;
                 const uint32_t idesc = kNv ? idesc_nv4(2 * BM, 2 * tl.half) : idesc_mx8(2 * BM, 2 * tl.half);
                 for (int kb = 0; kb < p.KB; ++kb) {
@@ -438,10 +395,8 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
             int stage = 0;
             uint32_t phase = 0;
             bool ok = p.stall_test == 0;
-            for (int j = 0; ok; ++j) {
-                const int t = tile_at(j);
-                if (t < 0) break;
-                const Tile8 tl = decode_tile8<MODE, FMT>(t, rank, p, sched);
+            for (TileWalk w = tile_walk_begin(cid, order); ok && w.t >= 0; tile_walk_next(w, ncl, order)) {
+                const Tile8 tl = make_tile8<MODE, FMT>(tile_walk_pos(w, order), rank, p, gcnt, goff);
                 const int nb = token_boxes(b_rows8(tl, rank));
                 const int brow = tl.brow + static_cast<int>(rank) * tl.half;
                 for (int kb = 0; kb < p.KB; ++kb) {
@@ -485,10 +440,8 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
         uint32_t phase = 0;
         int64_t i = 0;  // K blocks done, over the pair's tile sequence
         bool ok = true;
-        for (int j = 0; ok; ++j) {
-            const int t = tile_at(j);
-            if (t < 0) break;
-            const Tile8 tl = decode_tile8<MODE, FMT>(t, rank, p, sched);
+        for (TileWalk w = tile_walk_begin(cid, order); ok && w.t >= 0; tile_walk_next(w, ncl, order)) {
+            const Tile8 tl = make_tile8<MODE, FMT>(tile_walk_pos(w, order), rank, p, gcnt, goff);
             const int n_cols = 2 * tl.half;
             for (int kb = 0; kb < p.KB; ++kb, ++i) {
                 const int ss = static_cast<int>((i / kScKb) % kScSlots);
@@ -574,10 +527,8 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
         int acc = 0;
         uint32_t acc_phase = 0, xph = 0;
         bool ok = true;
-        for (int j = 0; ok; ++j) {
-            const int t = tile_at(j);
-            if (t < 0) break;
-            const Tile8 tl = decode_tile8<MODE, FMT>(t, rank, p, sched);
+        for (TileWalk w = tile_walk_begin(cid, order); ok && w.t >= 0; tile_walk_next(w, ncl, order)) {
+            const Tile8 tl = make_tile8<MODE, FMT>(tile_walk_pos(w, order), rank, p, gcnt, goff);
             if (!__all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, abort, tmo))) {
                 if (lane == 0 && !*abort) raise_timeout8(p, abort, 49);
                 break;
