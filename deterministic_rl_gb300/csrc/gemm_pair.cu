@@ -30,6 +30,7 @@
 
 #include "moe_internal.h"
 #include "ptx.cuh"
+#include "tile_walk.cuh"
 
 namespace moe {
 namespace {
@@ -149,46 +150,19 @@ struct Sched {
     int64_t H, N;     // hot tiles, all tiles
 };
 
-__device__ __forceinline__ int find_group(const int* start, int GG, int j) {
-    // the last group whose start is <= j (groups of width 0 share a start
-    // with the next group and are never chosen)
-    int lo = 0, hi = GG;
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (start[mid] <= j) lo = mid; else hi = mid;
-    }
-    return lo;
-}
-
 // Token tiles of a group of c tokens: ceil(c / TS) of them, of equal size
 // (the last one taking the rest) when TS > TN (a tile then holds two MMA
 // sub-tiles: its first TN tokens and the rest), of TN and a tail otherwise.
 // A sub-tile's MMA width N is its token count rounded up to 32 (at least 64):
 // a valid N for the M = 256 pair MMA, which takes multiples of 16.
 template <int MODE, int TN, int TS>
-__device__ __forceinline__ Tile decode_tile(int t, uint32_t rank, const GemmParams& p,
-                                            const Sched& sc) {
+__device__ __forceinline__ Tile make_tile(const TilePos& pos, uint32_t rank, const GemmParams& p,
+                                          const Sched& sc) {
     Tile tl;
-    const int64_t h0 = static_cast<int64_t>(t) * sc.H / sc.N;
-    const int64_t h1 = static_cast<int64_t>(t + 1) * sc.H / sc.N;
-    int nt;
-    if (h1 > h0) {
-        const int j = static_cast<int>(h0);
-        const int g = find_group(sc.hs, sc.GG, j / p.MT);
-        const int ntg = sc.hs[g + 1] - sc.hs[g];
-        const int l = j - sc.hs[g] * p.MT;
-        tl.g = g;
-        tl.m = l / ntg;
-        nt = l - tl.m * ntg;
-        tl.reused = true;
-    } else {
-        const int j = t - static_cast<int>(h0);
-        const int g = find_group(sc.cs, sc.GG, j / p.MT);
-        tl.g = g;
-        tl.m = j - sc.cs[g] * p.MT;
-        nt = 0;
-        tl.reused = false;
-    }
+    tl.g = pos.g;
+    tl.m = pos.m;
+    tl.reused = pos.hot;
+    const int nt = pos.nt;
     const int lo = tl.g;
     const int* gcnt = sc.gcnt;
     const int* goff = sc.goff;
@@ -521,6 +495,11 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                    static_cast<int64_t>(hs[GG] + cs[GG]) * p.MT};
     const int total = static_cast<int>(sched.N);
     const uint64_t tmo = p.timeout_ns;
+    // the tile order (tile_walk.cuh), walked forward by each role as it reads
+    // the tiles (static: every ncl-th; dynamic: the queue's increasing entries)
+    const TileOrder order{hs, cs, GG, p.MT, static_cast<uint32_t>(sched.H),
+                          static_cast<uint32_t>(sched.N)};
+    TileWalk walk = tile_walk_begin(0, order);
 
     // ---- tile queue ----
     // The pair takes tiles in order from the global counter: the leader's
@@ -636,7 +615,9 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                     break;
                 }
                 if (t < 0) break;
-                const Tile tl = decode_tile<MODE, C::kTileN, C::kSuperN>(t, rank, p, sched);
+                tile_walk_to(walk, t, order);
+                const Tile tl =
+                    make_tile<MODE, C::kTileN, C::kSuperN>(tile_walk_pos(walk, order), rank, p, sched);
                 const uint64_t pol_w = tl.reused ? pol_again : pol_once;
                 const CUtensorMap* ma0 = tl.shared ? &p.as0 : &p.a0;
                 const CUtensorMap* ma1 = tl.shared ? &p.as1 : &p.a1;
@@ -712,7 +693,9 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
             for (int j = 0; ok; ++j) {
                 int t;
                 if (!next_tile(j, t, 27, false) || t < 0) break;
-                const Tile tl = decode_tile<MODE, C::kTileN, C::kSuperN>(t, rank, p, sched);
+                tile_walk_to(walk, t, order);
+                const Tile tl =
+                    make_tile<MODE, C::kTileN, C::kSuperN>(tile_walk_pos(walk, order), rank, p, sched);
                 const int ns = tl.half1 ? 2 : 1;
                 for (int u = 0; u < ns && ok; ++u) {
                     const int v = su + u;
@@ -775,7 +758,9 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                 for (int j = 0; ok; ++j) {
                     int t;
                     if (!next_tile(j, t, 28, false) || t < 0) break;
-                    const Tile tl = decode_tile<MODE, C::kTileN, C::kSuperN>(t, rank, p, sched);
+                    tile_walk_to(walk, t, order);
+                    const Tile tl =
+                        make_tile<MODE, C::kTileN, C::kSuperN>(tile_walk_pos(walk, order), rank, p, sched);
                     const uint64_t pol_w = tl.reused ? pol_again : pol_once;
                     for (int kb = 0; kb < p.KB; ++kb) {
                         if ((kb & 7) == 0) {  // scales of the next 8 k-blocks
@@ -919,7 +904,9 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
         for (int j = 0; ok; ++j) {
             int t;
             if (!next_tile(j, t, 30, true) || t < 0) break;
-            const Tile tile = decode_tile<MODE, C::kTileN, C::kSuperN>(t, rank, p, sched);
+            tile_walk_to(walk, t, order);
+            const Tile tile =
+                make_tile<MODE, C::kTileN, C::kSuperN>(tile_walk_pos(walk, order), rank, p, sched);
             const int ns = tile.half1 ? 2 : 1;
           for (int sub = 0; sub < ns && ok; ++sub) {
             // sub-tile `sub` of the tile: its tokens and its TMEM slot

@@ -43,6 +43,7 @@ struct TileOrder {
 
 struct TilePos {
     int g, m, nt;
+    bool hot;  // from the hot list (the group has several token tiles)
 };
 
 __host__ __device__ __forceinline__ TileWalk tile_walk_begin(int first, const TileOrder& o) {
@@ -75,6 +76,32 @@ __host__ __device__ __forceinline__ void tile_walk_next(TileWalk& w, int step, c
     w.t = static_cast<int>(nt);
 }
 
+// Moves the walker forward to position t (t >= its position; -1 or t >= N end
+// it), for tiles handed out in increasing order with arbitrary gaps.
+__host__ __device__ __forceinline__ void tile_walk_to(TileWalk& w, int t, const TileOrder& o) {
+    if (t < 0 || static_cast<uint32_t>(t) >= o.N) {
+        w.t = -1;
+        return;
+    }
+    if (w.t < 0) {
+        const int gh = w.gh, gc = w.gc;
+        w = tile_walk_begin(t, o);
+        w.gh = gh;
+        w.gc = gc;
+        return;
+    }
+    const uint64_t rr = w.r + static_cast<uint64_t>(t - w.t) * o.H;
+    if (rr < (static_cast<uint64_t>(1) << 32)) {
+        const uint32_t r32 = static_cast<uint32_t>(rr);
+        w.q += r32 / o.N;
+        w.r = r32 % o.N;
+    } else {
+        w.q += static_cast<uint32_t>(rr / o.N);
+        w.r = static_cast<uint32_t>(rr % o.N);
+    }
+    w.t = t;
+}
+
 // The (group, weight tile, token tile) of the walker's position; moves the
 // list cursors forward (positions must be visited in increasing order).
 __host__ __device__ __forceinline__ TilePos tile_walk_pos(TileWalk& w, const TileOrder& o) {
@@ -88,6 +115,7 @@ __host__ __device__ __forceinline__ TilePos tile_walk_pos(TileWalk& w, const Til
         p.g = w.gh;
         p.m = l / ntg;
         p.nt = l - p.m * ntg;
+        p.hot = true;
     } else {  // cold: cold tile t - q
         const int j = w.t - static_cast<int>(w.q);
         const int x = j / o.MT;
@@ -95,6 +123,7 @@ __host__ __device__ __forceinline__ TilePos tile_walk_pos(TileWalk& w, const Til
         p.g = w.gc;
         p.m = j - o.cs[w.gc] * o.MT;
         p.nt = 0;
+        p.hot = false;
     }
     return p;
 }

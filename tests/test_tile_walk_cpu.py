@@ -24,9 +24,19 @@ int main() {
     for (auto& v : cs) if (scanf("%d", &v) != 1) return 1;
     moe::TileOrder o{hs.data(), cs.data(), GG, MT, (uint32_t)(hs[GG] * MT),
                      (uint32_t)((hs[GG] + cs[GG]) * MT)};
-    for (moe::TileWalk w = moe::tile_walk_begin(first, o); w.t >= 0; moe::tile_walk_next(w, step, o)) {
-        const moe::TilePos p = moe::tile_walk_pos(w, o);
-        printf("%d %d %d %d\n", w.t, p.g, p.m, p.nt);
+    if (step > 0) {
+        for (moe::TileWalk w = moe::tile_walk_begin(first, o); w.t >= 0; moe::tile_walk_next(w, step, o)) {
+            const moe::TilePos p = moe::tile_walk_pos(w, o);
+            printf("%d %d %d %d %d\n", w.t, p.g, p.m, p.nt, (int)p.hot);
+        }
+    } else {  // positions from stdin, increasing, -1 ends
+        moe::TileWalk w = moe::tile_walk_begin(0, o);
+        int t;
+        while (scanf("%d", &t) == 1 && t >= 0) {
+            moe::tile_walk_to(w, t, o);
+            const moe::TilePos p = moe::tile_walk_pos(w, o);
+            printf("%d %d %d %d %d\n", w.t, p.g, p.m, p.nt, (int)p.hot);
+        }
     }
     return 0;
 }
@@ -43,7 +53,7 @@ def walker(tmp_path_factory):
     return str(exe)
 
 
-def expected(hs, cs, MT, first, step):
+def expected(hs, cs, MT, first, step, positions=None):
     GG = len(hs) - 1
     H, N = hs[GG] * MT, (hs[GG] + cs[GG]) * MT
 
@@ -51,18 +61,18 @@ def expected(hs, cs, MT, first, step):
         return int(np.searchsorted(np.asarray(start[:GG]), x, side="right")) - 1
 
     out = []
-    for t in range(first, N, step):
+    for t in (range(first, N, step) if positions is None else positions):
         h0, h1 = t * H // N, (t + 1) * H // N
         if h1 > h0:
             j = h0
             g = group(hs, j // MT)
             ntg = hs[g + 1] - hs[g]
             l = j - hs[g] * MT
-            out.append((t, g, l // ntg, l % ntg))
+            out.append((t, g, l // ntg, l % ntg, 1))
         else:
             j = t - h0
             g = group(cs, j // MT)
-            out.append((t, g, j - cs[g] * MT, 0))
+            out.append((t, g, j - cs[g] * MT, 0, 0))
     return out
 
 
@@ -100,3 +110,22 @@ def test_walk_all_hot_all_cold_and_empty(walker):
             got = subprocess.run([walker], input=inp, capture_output=True, text=True, check=True).stdout
             got = [tuple(map(int, line.split())) for line in got.splitlines()]
             assert got == expected(hs, cs, 4, 0, step)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_walk_to_increasing_positions(walker, seed):
+    """Tiles handed out by a counter: each reader sees increasing positions
+    with arbitrary gaps (tile_walk_to)."""
+    rng = np.random.default_rng(100 + seed)
+    GG = int(rng.choice([5, 384]))
+    MT = int(rng.choice([8, 28]))
+    ntiles = rng.choice([0, 1, 1, 2, 4], size=GG)
+    ntiles[0] = max(ntiles[0], 1)
+    hs, cs = order_from_counts(ntiles)
+    N = (hs[-1] + cs[-1]) * MT
+    pos = np.sort(rng.choice(N, size=min(N, 200), replace=False)).tolist()
+    inp = (f"{GG} {MT} 0 0\n" + " ".join(map(str, hs)) + "\n" + " ".join(map(str, cs)) + "\n"
+           + " ".join(map(str, pos)) + " -1\n")
+    got = subprocess.run([walker], input=inp, capture_output=True, text=True, check=True).stdout
+    got = [tuple(map(int, line.split())) for line in got.splitlines()]
+    assert got == expected(hs, cs, MT, 0, 1, positions=pos)
