@@ -682,37 +682,35 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                     }
         }
     } else if (warp == 1) {
-        if (lane == 0 && leader) {
-            // ---------------- MMA issuer (leader only) ----------------
+        // bf16 and small-batch variants: the whole warp runs the issue loop and
+        // one elected lane issues each MMA and commit, a shorter issue path than
+        // a lone thread's (an N = 64 pair MMA every 67 cycles instead of 119;
+        // decode-sized MXFP8 layer 3.95 -> 3.67 ms).  The super-tile variant
+        // keeps one thread (its 16-warp block ran ~1.5 % slower the other way).
+        if constexpr (!C::kSuper) {
+          if (leader) {
+            // ---------------- MMA issuer (leader only, whole warp) ----------------
+            auto wait_w = [&](uint64_t* bar, uint32_t par, int where) {
+                if (__all_sync(0xffffffffu, mbar_wait(bar, par, abort, tmo))) return true;
+                if (lane == 0 && !*abort) raise_timeout(p, abort, where);
+                return false;
+            };
             int stage = 0;
             uint32_t phase = 0;
-            // TMEM slot uses so far: use u takes slot u % 2 in phase (u / 2) % 2;
-            // a tile takes one slot, or two (sub-tiles 0 and 1) with SUPER
-            int su = 0;
+            int su = 0;  // TMEM slot uses so far (one per tile)
             bool ok = true;
             for (int j = 0; ok; ++j) {
                 int t;
-                if (!next_tile(j, t, 27, false) || t < 0) break;
+                if (!next_tile(j, t, 27, true) || t < 0) break;
                 tile_walk_to(walk, t, order);
                 const Tile tl =
                     make_tile<MODE, C::kTileN, C::kSuperN>(tile_walk_pos(walk, order), rank, p, sched);
-                const int ns = tl.half1 ? 2 : 1;
-                for (int u = 0; u < ns && ok; ++u) {
-                    const int v = su + u;
-                    if (!mbar_wait(&tempty[v & 1], ((v >> 1) & 1) ^ 1u, abort, tmo)) {
-                        if (!*abort) raise_timeout(p, abort, 13);
-                        ok = false;
-                    }
-                }
-                if (!ok) break;
+                if (!wait_w(&tempty[su & 1], ((su >> 1) & 1) ^ 1u, 13)) break;
                 tc_fence_after();
                 const uint32_t d0 = tmem_base + (su & 1) * C::kAccCols;
-                const uint32_t d1 = tmem_base + ((su + 1) & 1) * C::kAccCols;
                 const uint32_t idesc = idesc_bf16_f32(2 * BM, 2 * tl.half);
-                const uint32_t idesc1 = idesc_bf16_f32(2 * BM, 2 * (ns == 2 ? tl.half1 : 32));
                 for (int kb = 0; kb < p.KB; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, abort, tmo)) {
-                        if (!*abort) raise_timeout(p, abort, 14);
+                    if (!wait_w(&full[stage], phase, 14)) {
                         ok = false;
                         break;
                     }
@@ -722,28 +720,88 @@ __global__ void __launch_bounds__(PCfg<MODE, FMT, SMALL>::kThreads, 1)
                     const uint32_t sa = smem_addr(smem + stage * kStageBytes);
                     const uint64_t da = sdesc_kmajor_sw128(sa);
                     const uint64_t db = sdesc_kmajor_sw128(sa + kABytes);
-                    const uint64_t db1 = sdesc_kmajor_sw128(sa + kABytes + C::kHalfN * 128);
-                    // the two sub-tiles' MMAs of each K step back to back: they
-                    // multiply the same A (weights) with different B (tokens)
 #pragma unroll
-                    for (int k = 0; k < BK / 16; ++k) {
-                        umma_bf16_pair(d0, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
-                        if (C::kSuper && ns == 2)
-                            umma_bf16_pair(d1, da + 2 * k, db1 + 2 * k, idesc1, (kb | k) != 0);
-                    }
-                    umma_commit_pair(&empty[stage], 0x3);
+                    for (int k = 0; k < BK / 16; ++k)
+                        umma_bf16_pair_w(d0, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+                    umma_commit_pair_w(&empty[stage], 0x3);
                     if (++stage == kStages) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                umma_commit_pair(&tfull[su & 1], 0x3);
-                if (ns == 2) umma_commit_pair(&tfull[(su + 1) & 1], 0x3);
-                su += ns;
+                umma_commit_pair_w(&tfull[su & 1], 0x3);
+                ++su;
             }
-            umma_commit_pair(drain, 0x1);
-            if (!mbar_wait(drain, 0, nullptr, tmo)) raise_timeout(p, abort, 15);
+            __syncwarp();
+            umma_commit_pair_w(drain, 0x1);
+            if (!__all_sync(0xffffffffu, mbar_wait(drain, 0, nullptr, tmo)) && lane == 0)
+                raise_timeout(p, abort, 15);
+          }
+        } else {
+          if (lane == 0 && leader) {
+              // ---------------- MMA issuer (leader only) ----------------
+              int stage = 0;
+              uint32_t phase = 0;
+              // TMEM slot uses so far: use u takes slot u % 2 in phase (u / 2) % 2;
+              // a tile takes one slot, or two (sub-tiles 0 and 1) with SUPER
+              int su = 0;
+              bool ok = true;
+              for (int j = 0; ok; ++j) {
+                  int t;
+                  if (!next_tile(j, t, 27, false) || t < 0) break;
+                  tile_walk_to(walk, t, order);
+                  const Tile tl =
+                      make_tile<MODE, C::kTileN, C::kSuperN>(tile_walk_pos(walk, order), rank, p, sched);
+                  const int ns = tl.half1 ? 2 : 1;
+                  for (int u = 0; u < ns && ok; ++u) {
+                      const int v = su + u;
+                      if (!mbar_wait(&tempty[v & 1], ((v >> 1) & 1) ^ 1u, abort, tmo)) {
+                          if (!*abort) raise_timeout(p, abort, 13);
+                          ok = false;
+                      }
+                  }
+                  if (!ok) break;
+                  tc_fence_after();
+                  const uint32_t d0 = tmem_base + (su & 1) * C::kAccCols;
+                  const uint32_t d1 = tmem_base + ((su + 1) & 1) * C::kAccCols;
+                  const uint32_t idesc = idesc_bf16_f32(2 * BM, 2 * tl.half);
+                  const uint32_t idesc1 = idesc_bf16_f32(2 * BM, 2 * (ns == 2 ? tl.half1 : 32));
+                  for (int kb = 0; kb < p.KB; ++kb) {
+                      if (!mbar_wait(&full[stage], phase, abort, tmo)) {
+                          if (!*abort) raise_timeout(p, abort, 14);
+                          ok = false;
+                          break;
+                      }
+                      tc_fence_after();
+                      // descriptors of the stage's tiles (1024-byte aligned); a
+                      // K step of 16 advances the start address by 32 bytes
+                      const uint32_t sa = smem_addr(smem + stage * kStageBytes);
+                      const uint64_t da = sdesc_kmajor_sw128(sa);
+                      const uint64_t db = sdesc_kmajor_sw128(sa + kABytes);
+                      const uint64_t db1 = sdesc_kmajor_sw128(sa + kABytes + C::kHalfN * 128);
+                      // the two sub-tiles' MMAs of each K step back to back: they
+                      // multiply the same A (weights) with different B (tokens)
+  #pragma unroll
+                      for (int k = 0; k < BK / 16; ++k) {
+                          umma_bf16_pair(d0, da + 2 * k, db + 2 * k, idesc, (kb | k) != 0);
+                          if (C::kSuper && ns == 2)
+                              umma_bf16_pair(d1, da + 2 * k, db1 + 2 * k, idesc1, (kb | k) != 0);
+                      }
+                      umma_commit_pair(&empty[stage], 0x3);
+                      if (++stage == kStages) {
+                          stage = 0;
+                          phase ^= 1u;
+                      }
+                  }
+                  if (!ok) break;
+                  umma_commit_pair(&tfull[su & 1], 0x3);
+                  if (ns == 2) umma_commit_pair(&tfull[(su + 1) & 1], 0x3);
+                  su += ns;
+              }
+              umma_commit_pair(drain, 0x1);
+              if (!mbar_wait(drain, 0, nullptr, tmo)) raise_timeout(p, abort, 15);
+          }
         }
     } else if (warp == C::kFp8Warp) {
         if constexpr (MX) {

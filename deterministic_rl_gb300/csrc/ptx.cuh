@@ -400,6 +400,49 @@ __device__ __forceinline__ void umma_nv4_pair(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
+// ---- warp-wide issue --------------------------------------------------------------
+// The same MMAs and commit, called by a whole converged warp: elect.sync picks
+// one lane, which issues the instruction.  The warp's other lanes keep the
+// descriptor arithmetic warp-uniform, which shortens the issue path (measured:
+// a pair MMA of N = 192 FP4 every 96 cycles instead of 117 from one thread).
+
+__device__ __forceinline__ void umma_bf16_pair_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_mx8_pair_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+        "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_nv4_pair_w(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred e, p;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "@e tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem),
+        "r"(accumulate)
+        : "memory");
+}
+
 // Whole warp: lane i writes 1 (8, 16, 32) consecutive 32-bit columns of TMEM
 // lane (taddr's lane + i); the warp's lane quadrant must be taddr's.
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
@@ -439,6 +482,17 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&v)[32
 
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Whole converged warp: umma_commit_pair issued by one elected lane.
+__device__ __forceinline__ void umma_commit_pair_w(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;\n\t}" ::"r"(smem_addr(bar)),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // Leader CTA, single thread: when its prior MMAs complete, arrive once on the
