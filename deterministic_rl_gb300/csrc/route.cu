@@ -20,6 +20,7 @@ namespace {
 
 constexpr int kMaxK = 8;
 constexpr int kWarpsPerBlock = 8;
+constexpr int kMaxSplit = 4;  // partial-logit buffers of the router's K split
 
 // a ranks before b: larger value, or equal value and lower expert id.
 __device__ __forceinline__ bool before(float va, int ea, float vb, int eb) {
@@ -74,16 +75,28 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) topk_gates_kernel(
     const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * kWarpsPerBlock + (threadIdx.x >> 5);
     if (t >= T) return;
+    float v[J];
     if (parts) {
+        // all partial sums are loaded first (independent loads), then added
+        // in the fixed order; the token's logits stay in registers
+        float pv[kMaxSplit][J];
+#pragma unroll
+        for (int s = 0; s < kMaxSplit; ++s)
+#pragma unroll
+            for (int j = 0; j < J; ++j) {
+                const int e = lane + 32 * j;
+                pv[s][j] = s < nsplit && e < E ? parts[s * stride + t * E + e] : 0.0f;
+            }
 #pragma unroll
         for (int j = 0; j < J; ++j) {
             const int e = lane + 32 * j;
-            if (e < E) {
-                float acc = parts[t * E + e];
-                for (int s = 1; s < nsplit; ++s) acc += parts[s * stride + t * E + e];
-                if (bias) acc += bias[e];
-                logits_out[t * E + e] = acc;
-            }
+            float acc = pv[0][j];
+#pragma unroll
+            for (int s = 1; s < kMaxSplit; ++s)
+                if (s < nsplit) acc += pv[s][j];
+            if (bias && e < E) acc += bias[e];
+            if (e < E) logits_out[t * E + e] = acc;
+            v[j] = e < E ? acc : -FLT_MAX;
         }
         __syncwarp();
         logits = logits_out;
@@ -93,8 +106,7 @@ __global__ void __launch_bounds__(32 * kWarpsPerBlock) topk_gates_kernel(
     int sel[kMaxK];
     float sl[kMaxK];
     bool ok = true;
-    float v[J];
-    if (ids_in == nullptr || filter) {
+    if (!parts && (ids_in == nullptr || filter)) {
 #pragma unroll
         for (int j = 0; j < J; ++j) {
             const int e = lane + 32 * j;
@@ -234,7 +246,8 @@ cudaError_t launch_topk_gates_split(const float* parts, int nsplit, int64_t stri
                                     int k, const int32_t* ids_in, int32_t* ids_out,
                                     float* gates_out, int32_t* valid, int32_t* status,
                                     cudaStream_t s, int filter, float log_tau) {
-    if (!logits_out || nsplit < 1 || (nsplit > 1 && !parts)) return cudaErrorInvalidValue;
+    if (!logits_out || nsplit < 1 || nsplit > kMaxSplit || (nsplit > 1 && !parts))
+        return cudaErrorInvalidValue;
     if (filter && !ids_in) return cudaErrorInvalidValue;
     const TopkArgs a{logits_out, nsplit > 1 ? parts : nullptr, nsplit, stride, bias, logits_out,
                      T, E, k, ids_in, ids_out, gates_out, valid, status, filter, log_tau};
