@@ -59,10 +59,11 @@ ONE_SM_MAX_TOKENS = 128        # bf16 batches up to this size run the one-SM exp
 def kernels_per_step(T, k, wfmt="bf16", act_mx=False):
     """Launches of one layer call: router GEMM, top-k, dispatch (one kernel for
     at most one segment of pairs, else histogram, scan and scatter), gather,
-    gate/up, down, combine; NVFP4 and MXFP8 activations add the two activation
-    quantisers and a second gather (codes, then block scales)."""
+    gate/up, down, combine; with NVFP4 or MXFP8 activations the gather is the
+    token rows' quantiser (which writes the gathered rows too) and the rows of h
+    have a quantiser of their own."""
     n = 7 if T * k <= DISPATCH_SEGMENT_PAIRS else 9
-    return n + (3 if wfmt == "nvfp4" or act_mx else 0)
+    return n + (1 if wfmt == "nvfp4" or act_mx else 0)
 
 
 def launches_per_step(cfg):

@@ -385,17 +385,14 @@ moe_status run_experts_bs(const moe_dims* d, const void* x, const moe_weights* w
                                reinterpret_cast<int32_t*>(ws + L.scratch), s)));
     MOE_TRY(mark(MOE_STAGE_DISPATCH, 1, s));
     MOE_TRY(mark(MOE_STAGE_GATHER, 0, s));
+    // each token row quantised once and written to its own row and to its k
+    // gathered rows (codes, block scales; NVFP4 also the row scale)
     if (nv)
-        MOE_TRY(cu(launch_nvfp4_codes(static_cast<const uint16_t*>(x), xc, xs, sx, T, D, sms, s)));
+        MOE_TRY(cu(launch_nvfp4_codes(static_cast<const uint16_t*>(x), xc, xs, sx, T, D, sms, s, inv,
+                                      k, xpc, xps, sxp)));
     else
-        MOE_TRY(cu(launch_mx_rows_fp8(static_cast<const uint16_t*>(x), xc, xs, T, D, sms, s)));
-    // rows of codes and of scales moved as 2-byte units; NVFP4 rows take their
-    // token's fp32 scale along
-    MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(xc), inv, T, k, cd / 2, 0,
-                             reinterpret_cast<uint16_t*>(xpc), s, nv ? sx : nullptr,
-                             nv ? sxp : nullptr)));
-    MOE_TRY(cu(launch_gather(reinterpret_cast<const uint16_t*>(xs), inv, T, k, sd / 2, 0,
-                             reinterpret_cast<uint16_t*>(xps), s)));
+        MOE_TRY(cu(launch_mx_rows_fp8(static_cast<const uint16_t*>(x), xc, xs, T, D, sms, s, inv, k,
+                                      xpc, xps)));
     MOE_TRY(mark(MOE_STAGE_GATHER, 1, s));
 
     const int tn = bs_tile_tokens(fmt), kk = 128, big = bs_big_box(fmt), sbox = bs_scale_box(fmt);

@@ -138,9 +138,12 @@ int bs_scale_kb(int fmt);
 // MXFP8 quantisation of R rows of K bf16 values (K % 256 == 0) in blocks of 32
 // along the row: E4M3 codes to codes [R][K] and E8M0 scale bytes to scales
 // [R][K/32] (OCP MX v1.0: X = floor(log2 max|v|) - 8, codes E4M3(v / 2^X)
-// nearest even, saturating; scale byte X + 127).
+// nearest even, saturating; scale byte X + 127).  With inv (R token rows,
+// k <= 8): each row's codes and scales also go to its k gathered rows
+// inv[r * k + j] of codes_p, scales_p (the gather, fused).
 cudaError_t launch_mx_rows_fp8(const uint16_t* src, uint8_t* codes, uint8_t* scales, int64_t R,
-                               int K, int sms, cudaStream_t s);
+                               int K, int sms, cudaStream_t s, const int32_t* inv = nullptr,
+                               int k = 0, uint8_t* codes_p = nullptr, uint8_t* scales_p = nullptr);
 
 // Routing: top-k selection (own mode) or replay validation, then gate weights.
 cudaError_t launch_topk_gates(const float* logits, int64_t T, int E, int k,
@@ -173,8 +176,13 @@ cudaError_t launch_gather(const uint16_t* x, const int32_t* inv, int64_t T, int 
 // NVFP4 quantisation of R rows of K bf16 values (K % 16 == 0), per row: codes
 // [R][K/2] bytes (two E2M1 codes, element 2j in the low nibble), bscale
 // [R][K/16] E4M3 block scales, rscale [R] the fp32 row scale (nvfp4.cu).
+// With inv (R token rows, k <= 8): each row's codes, block scales and row
+// scale also go to its k gathered rows inv[r * k + j] of codes_p, bscale_p,
+// rscale_p (the gather of the quantised rows, fused).
 cudaError_t launch_nvfp4_codes(const uint16_t* src, uint8_t* codes, uint8_t* bscale, float* rscale,
-                               int64_t R, int K, int sms, cudaStream_t s);
+                               int64_t R, int K, int sms, cudaStream_t s,
+                               const int32_t* inv = nullptr, int k = 0, uint8_t* codes_p = nullptr,
+                               uint8_t* bscale_p = nullptr, float* rscale_p = nullptr);
 // ---- backward (backward.cu, wgrad.cu) ----
 
 // Grouped weight-gradient GEMM: for group g, out[g][n][m] = sum over the

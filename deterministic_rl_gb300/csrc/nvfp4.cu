@@ -72,10 +72,13 @@ __device__ __forceinline__ float e4m3_value(__nv_fp8_storage_t S) {
 }
 
 // One warp per row (a lane per 16-value block): codes [R][K/2] bytes,
-// bscale [R][K/16] E4M3 bytes, rscale [R] fp32.
+// bscale [R][K/16] E4M3 bytes, rscale [R] fp32.  With inv (token rows of x):
+// the same codes and scales also go to the k gathered rows inv[r * k + j] of
+// codes_p, bscale_p, rscale_p (the gather, fused).
 __global__ void __launch_bounds__(32 * kWarps) nvfp4_codes_kernel(
     const uint4* __restrict__ src, uint2* __restrict__ codes, uint8_t* __restrict__ bscale,
-    float* __restrict__ rscale, int64_t R, int K) {
+    float* __restrict__ rscale, int64_t R, int K, const int32_t* __restrict__ inv, int k,
+    uint2* __restrict__ codes_p, uint8_t* __restrict__ bscale_p, float* __restrict__ rscale_p) {
     const int lane = threadIdx.x & 31;
     const int nb = K / 16;
     const int vpr = K / 8;
@@ -88,12 +91,29 @@ __global__ void __launch_bounds__(32 * kWarps) nvfp4_codes_kernel(
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         const float s = __fdiv_rn(amax, 2688.0f);  // 6 * 448
         if (lane == 0) rscale[r] = s;
+        // the row's gathered destinations, in every lane (k <= 8)
+        int64_t dst[8];
+        {
+            const int dl = inv && lane < k ? inv[r * k + lane] : 0;
+            if (inv && lane < k) rscale_p[dl] = s;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) dst[j] = __shfl_sync(0xffffffffu, dl, j);
+        }
         for (int b = lane; b < nb; b += 32) {
             const uint4 a0 = row[2 * b], a1 = row[2 * b + 1];
             const __nv_fp8_storage_t S = block_scale(absmax8(a1, absmax8(a0, 0.0f)), s);
             const float denom = __fmul_rn(e4m3_value(S), s);
-            codes[r * nb + b] = make_uint2(codes8(a0, denom), codes8(a1, denom));
+            const uint2 cw = make_uint2(codes8(a0, denom), codes8(a1, denom));
+            codes[r * nb + b] = cw;
             bscale[r * nb + b] = S;
+            if (inv) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    if (j < k) {
+                        codes_p[dst[j] * nb + b] = cw;
+                        bscale_p[dst[j] * nb + b] = S;
+                    }
+            }
         }
     }
 }
@@ -101,14 +121,17 @@ __global__ void __launch_bounds__(32 * kWarps) nvfp4_codes_kernel(
 }  // namespace
 
 cudaError_t launch_nvfp4_codes(const uint16_t* src, uint8_t* codes, uint8_t* bscale, float* rscale,
-                               int64_t R, int K, int sms, cudaStream_t s) {
+                               int64_t R, int K, int sms, cudaStream_t s, const int32_t* inv, int k,
+                               uint8_t* codes_p, uint8_t* bscale_p, float* rscale_p) {
     if (R == 0) return cudaSuccess;
     if (K % 16) return cudaErrorInvalidValue;
+    if (inv && (k < 1 || k > 8 || !codes_p || !bscale_p || !rscale_p)) return cudaErrorInvalidValue;
     int64_t blocks = (R + kWarps - 1) / kWarps;
     const int64_t cap = static_cast<int64_t>(sms) * 8;
     if (blocks > cap) blocks = cap;
     nvfp4_codes_kernel<<<static_cast<unsigned>(blocks), 32 * kWarps, 0, s>>>(
-        reinterpret_cast<const uint4*>(src), reinterpret_cast<uint2*>(codes), bscale, rscale, R, K);
+        reinterpret_cast<const uint4*>(src), reinterpret_cast<uint2*>(codes), bscale, rscale, R, K,
+        inv, k, reinterpret_cast<uint2*>(codes_p), bscale_p, rscale_p);
     return cudaGetLastError();
 }
 
