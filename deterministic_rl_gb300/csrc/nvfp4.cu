@@ -71,35 +71,54 @@ __device__ __forceinline__ float e4m3_value(__nv_fp8_storage_t S) {
     return __half2float(__half(__nv_cvt_fp8_to_halfraw(S, __NV_E4M3)));
 }
 
-// One warp per row (a lane per 16-value block): codes [R][K/2] bytes,
-// bscale [R][K/16] E4M3 bytes, rscale [R] fp32.  With inv (token rows of x):
-// the same codes and scales also go to the k gathered rows inv[r * k + j] of
-// codes_p, bscale_p, rscale_p (the gather, fused).
+// Four warps per row, a lane per 16-value block: codes [R][K/2] bytes,
+// bscale [R][K/16] E4M3 bytes, rscale [R] fp32.  The row's maximum is the
+// maximum over its warps (exact, whatever the order).  With inv (token rows
+// of x): the same codes and scales also go to the k gathered rows
+// inv[r * k + j] of codes_p, bscale_p, rscale_p (the gather, fused).
+constexpr int kWarpsPerRow = 4;
+constexpr int kRowsPerBlock = kWarps / kWarpsPerRow;
+
 __global__ void __launch_bounds__(32 * kWarps) nvfp4_codes_kernel(
     const uint4* __restrict__ src, uint2* __restrict__ codes, uint8_t* __restrict__ bscale,
     float* __restrict__ rscale, int64_t R, int K, const int32_t* __restrict__ inv, int k,
     uint2* __restrict__ codes_p, uint8_t* __restrict__ bscale_p, float* __restrict__ rscale_p) {
+    __shared__ float red[kWarps];
     const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int wr = warp % kWarpsPerRow;  // this warp's share of its row
+    const int slot = warp / kWarpsPerRow;
     const int nb = K / 16;
     const int vpr = K / 8;
-    for (int64_t r = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5); r < R;
-         r += static_cast<int64_t>(gridDim.x) * kWarps) {
-        const uint4* row = src + r * vpr;
+    // the loop bound is the same for the whole block (it meets __syncthreads)
+    for (int64_t r0 = static_cast<int64_t>(blockIdx.x) * kRowsPerBlock; r0 < R;
+         r0 += static_cast<int64_t>(gridDim.x) * kRowsPerBlock) {
+        const int64_t r = r0 + slot;
+        const bool have = r < R;
+        const uint4* row = src + (have ? r : 0) * vpr;
         float amax = 0.0f;
-        for (int b = lane; b < nb; b += 32) amax = absmax8(row[2 * b + 1], absmax8(row[2 * b], amax));
+        if (have)
+            for (int b = wr * 32 + lane; b < nb; b += 32 * kWarpsPerRow)
+                amax = absmax8(row[2 * b + 1], absmax8(row[2 * b], amax));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        if (lane == 0) red[warp] = amax;
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < kWarpsPerRow; ++w) amax = fmaxf(amax, red[slot * kWarpsPerRow + w]);
+        __syncthreads();
+        if (!have) continue;
         const float s = __fdiv_rn(amax, 2688.0f);  // 6 * 448
-        if (lane == 0) rscale[r] = s;
+        if (wr == 0 && lane == 0) rscale[r] = s;
         // the row's gathered destinations, in every lane (k <= 8)
         int64_t dst[8];
         {
             const int dl = inv && lane < k ? inv[r * k + lane] : 0;
-            if (inv && lane < k) rscale_p[dl] = s;
+            if (inv && wr == 0 && lane < k) rscale_p[dl] = s;
 #pragma unroll
             for (int j = 0; j < 8; ++j) dst[j] = __shfl_sync(0xffffffffu, dl, j);
         }
-        for (int b = lane; b < nb; b += 32) {
+        for (int b = wr * 32 + lane; b < nb; b += 32 * kWarpsPerRow) {
             const uint4 a0 = row[2 * b], a1 = row[2 * b + 1];
             const __nv_fp8_storage_t S = block_scale(absmax8(a1, absmax8(a0, 0.0f)), s);
             const float denom = __fmul_rn(e4m3_value(S), s);
@@ -126,7 +145,7 @@ cudaError_t launch_nvfp4_codes(const uint16_t* src, uint8_t* codes, uint8_t* bsc
     if (R == 0) return cudaSuccess;
     if (K % 16) return cudaErrorInvalidValue;
     if (inv && (k < 1 || k > 8 || !codes_p || !bscale_p || !rscale_p)) return cudaErrorInvalidValue;
-    int64_t blocks = (R + kWarps - 1) / kWarps;
+    int64_t blocks = (R + kRowsPerBlock - 1) / kRowsPerBlock;
     const int64_t cap = static_cast<int64_t>(sms) * 8;
     if (blocks > cap) blocks = cap;
     nvfp4_codes_kernel<<<static_cast<unsigned>(blocks), 32 * kWarps, 0, s>>>(
