@@ -134,8 +134,12 @@ __global__ void __launch_bounds__(32 * kSegWarps) dispatch_small_kernel(
     const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < kSegWarps * kMaxE; i += blockDim.x) (&h[0][0])[i] = 0;
     __syncthreads();
-    const int64_t base = static_cast<int64_t>(w) * kWarpPairs;
-    for (int r = 0; r < kWarpPairs; r += 32) {  // per-warp histograms
+    // each warp takes an equal run of consecutive pairs (a multiple of 32):
+    // both passes below use the same runs, in warp order, so ranks stay in
+    // pair order
+    const int per = static_cast<int>((n + 32 * kSegWarps - 1) / (32 * kSegWarps)) * 32;
+    const int64_t base = static_cast<int64_t>(w) * per;
+    for (int r = 0; r < per; r += 32) {  // per-warp histograms
         const int64_t i = base + r + lane;
         const bool in = i < n;
         const int key = in ? ids[i] : -1;
@@ -182,7 +186,7 @@ __global__ void __launch_bounds__(32 * kSegWarps) dispatch_small_kernel(
         }
     }
     __syncthreads();
-    for (int r = 0; r < kWarpPairs; r += 32) {  // in-order ranks
+    for (int r = 0; r < per; r += 32) {  // in-order ranks
         const int64_t i = base + r + lane;
         const bool in = i < n;
         const int key = in ? ids[i] : -1;
