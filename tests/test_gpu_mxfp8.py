@@ -40,7 +40,7 @@ def dequantised(inp):
     return deq(inp.w_gate, inp.s_gate), deq(inp.w_up, inp.s_up), deq(inp.w_down, inp.s_down)
 
 
-@pytest.mark.parametrize("T", [1, 300])
+@pytest.mark.parametrize("T", [1, 64, 128, 300])  # small-batch variant up to 128 tokens
 def test_mxfp8_equals_bf16_on_dequantised_weights_bitwise(T):
     inp = make_layer(small_mx(T), "cuda")
     mx = MoELayer.from_inputs(inp, out_fp32=True)
