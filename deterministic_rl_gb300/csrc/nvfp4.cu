@@ -71,18 +71,18 @@ __device__ __forceinline__ float e4m3_value(__nv_fp8_storage_t S) {
     return __half2float(__half(__nv_cvt_fp8_to_halfraw(S, __NV_E4M3)));
 }
 
-// Four warps per row, a lane per 16-value block: codes [R][K/2] bytes,
-// bscale [R][K/16] E4M3 bytes, rscale [R] fp32.  The row's maximum is the
-// maximum over its warps (exact, whatever the order).  With inv (token rows
-// of x): the same codes and scales also go to the k gathered rows
-// inv[r * k + j] of codes_p, bscale_p, rscale_p (the gather, fused).
-constexpr int kWarpsPerRow = 4;
-constexpr int kRowsPerBlock = kWarps / kWarpsPerRow;
-
+// W warps per row (1 for many rows, 4 for few), a lane per 16-value block:
+// codes [R][K/2] bytes, bscale [R][K/16] E4M3 bytes, rscale [R] fp32.  The
+// row's maximum is the maximum over its warps (exact, whatever the order).
+// With inv (token rows of x): the same codes and scales also go to the k
+// gathered rows inv[r * k + j] of codes_p, bscale_p, rscale_p (the gather,
+// fused).
+template <int kWarpsPerRow>
 __global__ void __launch_bounds__(32 * kWarps) nvfp4_codes_kernel(
     const uint4* __restrict__ src, uint2* __restrict__ codes, uint8_t* __restrict__ bscale,
     float* __restrict__ rscale, int64_t R, int K, const int32_t* __restrict__ inv, int k,
     uint2* __restrict__ codes_p, uint8_t* __restrict__ bscale_p, float* __restrict__ rscale_p) {
+    constexpr int kRowsPerBlock = kWarps / kWarpsPerRow;
     __shared__ float red[kWarps];
     const int lane = threadIdx.x & 31;
     const int warp = threadIdx.x >> 5;
@@ -102,11 +102,13 @@ __global__ void __launch_bounds__(32 * kWarps) nvfp4_codes_kernel(
                 amax = absmax8(row[2 * b + 1], absmax8(row[2 * b], amax));
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        if (lane == 0) red[warp] = amax;
-        __syncthreads();
+        if constexpr (kWarpsPerRow > 1) {
+            if (lane == 0) red[warp] = amax;
+            __syncthreads();
 #pragma unroll
-        for (int w = 0; w < kWarpsPerRow; ++w) amax = fmaxf(amax, red[slot * kWarpsPerRow + w]);
-        __syncthreads();
+            for (int w = 0; w < kWarpsPerRow; ++w) amax = fmaxf(amax, red[slot * kWarpsPerRow + w]);
+            __syncthreads();
+        }
         if (!have) continue;
         const float s = __fdiv_rn(amax, 2688.0f);  // 6 * 448
         if (wr == 0 && lane == 0) rscale[r] = s;
@@ -145,12 +147,22 @@ cudaError_t launch_nvfp4_codes(const uint16_t* src, uint8_t* codes, uint8_t* bsc
     if (R == 0) return cudaSuccess;
     if (K % 16) return cudaErrorInvalidValue;
     if (inv && (k < 1 || k > 8 || !codes_p || !bscale_p || !rscale_p)) return cudaErrorInvalidValue;
-    int64_t blocks = (R + kRowsPerBlock - 1) / kRowsPerBlock;
     const int64_t cap = static_cast<int64_t>(sms) * 8;
-    if (blocks > cap) blocks = cap;
-    nvfp4_codes_kernel<<<static_cast<unsigned>(blocks), 32 * kWarps, 0, s>>>(
-        reinterpret_cast<const uint4*>(src), reinterpret_cast<uint2*>(codes), bscale, rscale, R, K,
-        inv, k, reinterpret_cast<uint2*>(codes_p), bscale_p, rscale_p);
+    // few rows (a decode batch): four warps per row, else one
+    if (R < cap * kWarps) {
+        constexpr int kW = 4;
+        int64_t blocks = (R + kWarps / kW - 1) / (kWarps / kW);
+        if (blocks > cap) blocks = cap;
+        nvfp4_codes_kernel<kW><<<static_cast<unsigned>(blocks), 32 * kWarps, 0, s>>>(
+            reinterpret_cast<const uint4*>(src), reinterpret_cast<uint2*>(codes), bscale, rscale, R,
+            K, inv, k, reinterpret_cast<uint2*>(codes_p), bscale_p, rscale_p);
+    } else {
+        int64_t blocks = (R + kWarps - 1) / kWarps;
+        if (blocks > cap) blocks = cap;
+        nvfp4_codes_kernel<1><<<static_cast<unsigned>(blocks), 32 * kWarps, 0, s>>>(
+            reinterpret_cast<const uint4*>(src), reinterpret_cast<uint2*>(codes), bscale, rscale, R,
+            K, inv, k, reinterpret_cast<uint2*>(codes_p), bscale_p, rscale_p);
+    }
     return cudaGetLastError();
 }
 
