@@ -403,6 +403,8 @@ moe_status run_experts_bs(const moe_dims* d, const void* x, const moe_weights* w
         p.G = E;
         p.status = status;
         p.timeout_ns = kWaitTimeoutNs;
+        // scales ahead of the weights once the experts average a full tile
+        p.sc_ahead = rows >= static_cast<int64_t>(E) * tn ? 1 : 0;
     };
     const uint32_t rg = gemm_rows(GEMM_SWIGLU);
     GemmParams p1;

@@ -104,6 +104,9 @@ struct GemmParams {
     // Block-scaled GEMMs (gemm_bs.cu): the token rows' block scales (E8M0 per
     // 32 for MXFP8, E4M3 per 16 for NVFP4), [rows][K/32 or K/16] bytes.
     CUtensorMap sb_scale;
+    // Block-scaled GEMMs: 1 = load scale groups ahead of the weights (large
+    // batches; 0 keeps them with their K block, better for weight streaming).
+    int32_t sc_ahead;
 };
 
 size_t gemm_smem_bytes(int mode, int n_groups_total);
