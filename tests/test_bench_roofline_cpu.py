@@ -77,3 +77,24 @@ def test_backward_launches_per_call():
     cfg = CONFIGS["c4_train_32k"]
     assert bench.backward_launches(cfg) == 28
     assert bench.backward_launches(cfg, train=True) == 29
+
+
+def test_block_scaled_peaks_and_row_bytes():
+    """The expert GEMMs' tensor peak follows their operand type (the measured
+    bf16 peak times the nominal dense ratio: fp8 2x, fp4 6x; MXFP8 weights with
+    bf16 activations are dequantised and run at the bf16 rate), and the token
+    rows they read are counted at their stored size."""
+    bf = 1958.8
+    assert bench.mma_peak(CONFIGS["c4_train_32k"], bf)[0] == bf
+    assert bench.mma_peak(CONFIGS["c5_mxfp8"], bf)[0] == bf
+    assert bench.mma_peak(CONFIGS["c5_mxfp8_act"], bf)[0] == 2 * bf
+    assert bench.mma_peak(CONFIGS["c6_nvfp4"], bf)[0] == 6 * bf
+    assert bench.act_bytes_per_value(CONFIGS["c5_mxfp8"]) == 2.0
+    assert bench.act_bytes_per_value(CONFIGS["c5_mxfp8_act"]) == 1 + 1 / 32
+    assert bench.act_bytes_per_value(CONFIGS["c6_nvfp4"]) == 0.5 + 1 / 16
+    # gate/up bytes of the NVFP4 layer: 384 experts' E2M1 + E4M3 weights, the
+    # gathered narrow rows, the bf16 h written
+    cfg = CONFIGS["c6_nvfp4"]
+    T, d, F, k = cfg.T, cfg.d, cfg.F, cfg.k
+    want = 384 * 2 * F * d * (0.5 + 1 / 16) + T * k * d * (0.5 + 1 / 16) + T * k * F * 2
+    assert abs(bench.gate_up_bytes(cfg, 384) - want) < 1.0
