@@ -257,3 +257,23 @@ def test_pack_weights_validation(lib):
     rc = _call(lib, "moe_forward", good_dims(wfmt=1, n_shared=0), x, w, out, ids, g)
     assert rc in (B.MOE_ERR_ARG, B.MOE_ERR_UNSUPPORTED)
     assert _call(lib, "moe_forward", d, x, _weights(w_gate_up=_Fake(0x90004)), out, ids, g) == B.MOE_ERR_ALIGN
+
+
+@pytest.mark.parametrize("wfmt", [2, 3])  # NVFP4, MXFP8 weights and activations
+def test_narrow_activation_regions_fit(lib, wfmt):
+    """The regions the block-scaled layers write hold what they must: the codes
+    and block scales of x ([T][d/2] + [T][d/16] for NVFP4, [T][d] + [T][d/32]
+    for MXFP8), of the gathered rows (in the xp region) and of h (hq); NVFP4's
+    fp32 row scales of x, of the gathered rows and of h."""
+    T, d, F, k = 300, 7168, 2048, 8
+    dims = good_dims(T=T, n_shared=0, wfmt=wfmt)
+    L = B.moe_workspace_layout(dims)
+    nv = wfmt == 2
+    per = (lambda K: K // 2 + K // 16) if nv else (lambda K: K + K // 32)
+    regions = sorted([(L.xp, L.h), (L.xq, L.sx), (L.hq, L.total)])
+    assert L.h - L.xp >= T * k * per(d)
+    assert L.sx - L.xq >= T * per(d)
+    assert L.total - L.hq >= T * k * per(F)
+    if nv:
+        assert L.sxp - L.sx >= T * 4 and L.sh - L.sxp >= T * k * 4 and L.hq - L.sh >= T * k * 4
+    assert all(a % 256 == 0 for a, _ in regions)
