@@ -518,7 +518,8 @@ def time_forward(cfg, mode, K, warmup, world, local):
 
 # Every d = 7168 workload of the layer beside the headline one, timed in the
 # same run: (workload, mode, zipf override or None).
-EXTRA_WORKLOADS = [("c3_prefill_zipf", "replay", None), ("c3_prefill_zipf", "own", None),
+EXTRA_WORKLOADS = [("c2_decode_replay", "own", None),
+                   ("c3_prefill_zipf", "replay", None), ("c3_prefill_zipf", "own", None),
                    ("c4_train_32k", "own", None), ("c4_train_32k", "own", 1.2),
                    ("c5_mxfp8", "own", None), ("c5_mxfp8_act", "own", None),
                    ("c6_nvfp4", "own", None)]
