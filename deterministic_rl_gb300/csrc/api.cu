@@ -676,19 +676,19 @@ struct BwdLayout {
     size_t total;
 };
 
+// The weight copies of the dH and dXp GEMMs: E4M3 codes, then E8M0 scale
+// bytes, of the routed experts followed by the shared expert (group E).
 struct BwdWeights {
-    size_t wdt, w2t, swdt, sw2t, total;
+    size_t wd, wds, w2, w2s, total;
 };
 
-bool bwd_dims_ok(const moe_dims* d) {
-    return dims_ok(d) && d->wfmt == MOE_W_BF16 && d->d % 256 == 0 && d->F % 256 == 0;
-}
-
+// d and 2F are multiples of 512: the block-scaled GEMMs load scales for four
+// 128-wide K blocks at a time
 moe_status bwd_dims_status(const moe_dims* d) {
     if (!d) return MOE_ERR_ARG;
     if (!dims_ok(d)) return MOE_ERR_SHAPE;
     if (d->wfmt != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
-    if (d->d % 256 || d->F % 256) return MOE_ERR_SHAPE;
+    if (d->d % 512 || d->F % 256) return MOE_ERR_SHAPE;
     return MOE_OK;
 }
 
@@ -711,9 +711,9 @@ BwdLayout make_bwd_layout(const moe_dims* d) {
     L.b = take(rows * F * 4);
     L.dg = take(T * k * 4);
     L.dl = take(T * k * 4);
-    L.dyq = take(rows * D * 2);
+    L.dyq = take(rows * D + rows * D / 32);          // codes, then scale bytes
     L.dh = take(rows * F * 4);
-    L.dabq = take(rows * 2 * F * 2);
+    L.dabq = take(rows * 2 * F + rows * 2 * F / 32);  // codes, then scale bytes
     L.dxp = take(rows * D * 4);
     L.xpt = take(D * kp * 2);
     L.dyt = take(D * kp * 2);
@@ -725,13 +725,13 @@ BwdLayout make_bwd_layout(const moe_dims* d) {
 
 BwdWeights make_bwd_weights(const moe_dims* d) {
     BwdWeights W{};
-    const size_t E = d->E, S = d->n_shared, FD = size_t(d->F) * d->d;
+    const size_t G = size_t(d->E) + d->n_shared, FD = size_t(d->F) * d->d;
     size_t o = 0;
     auto take = [&](size_t bytes) { const size_t at = o; o = align256(o + bytes); return at; };
-    W.wdt = take(E * FD * 2);
-    W.w2t = take(E * FD * 2 * 2);
-    W.swdt = take(S * FD * 2);
-    W.sw2t = take(S * FD * 2 * 2);
+    W.wd = take(G * FD);
+    W.wds = take(G * FD / 32);
+    W.w2 = take(G * FD * 2);
+    W.w2s = take(G * FD * 2 / 32);
     W.total = o;
     return W;
 }
@@ -901,8 +901,9 @@ moe_status train_impl(TrainMode mode, const moe_dims* d, const void* x, const mo
                                    sms, s)));
     MOE_TRY(mark_b(MOE_BWD_STAGE_GATE, 1, s));
 
-    // 4. dH = Q_d(dY) Q_d(Wd)  (SM-pair grouped GEMM, fp32 rows)
-    uint16_t* dyq = reinterpret_cast<uint16_t*>(wsb + L.dyq);
+    // 4. dH = Q_d(dY) Q_d(Wd)  (block-scaled MXFP8 SM-pair GEMM, fp32 rows)
+    uint8_t* dyc = wsb + L.dyq;
+    uint8_t* dys = dyc + rows * D;
     uint16_t* xpt = reinterpret_cast<uint16_t*>(wsb + L.xpt);
     uint16_t* dyt = reinterpret_cast<uint16_t*>(wsb + L.dyt);
     uint16_t* ht = reinterpret_cast<uint16_t*>(wsb + L.ht);
@@ -910,51 +911,63 @@ moe_status train_impl(TrainMode mode, const moe_dims* d, const void* x, const mo
     const int srows = S ? static_cast<int>(T) : 0;
     MOE_TRY(mark_b(MOE_BWD_STAGE_DY, 0, s));
     const SegDyArgs dya{static_cast<const uint16_t*>(dout), gates, perm, valid, k, Tk, inv, T, S};
-    MOE_TRY(cu(launch_dy_dual(dya, D, cnt, off, poff, E, G, srows, L.kpad, dyq, dyt, sms, s)));
+    MOE_TRY(cu(launch_dy_dual(dya, D, cnt, off, poff, E, G, srows, L.kpad, dyc, dys, dyt, sms, s)));
     MOE_TRY(mark_b(MOE_BWD_STAGE_DY, 1, s));
+    // The dH and dXp GEMMs on the block-scaled MMA: E4M3 codes of the weight
+    // copies (groups 0..E-1, the shared expert as group E) and of the token
+    // rows, 128-byte K blocks, scale bytes per 32 along K; fp32 rows out.
+    const int tn8 = bs_tile_tokens(BS_MXFP8), big8 = bs_big_box(BS_MXFP8);
+    const int sbox8 = bs_scale_box(BS_MXFP8), kk8 = 128;
+    const uint64_t GF = uint64_t(G) * F, GD = uint64_t(G) * D;
+    auto bs_down = [&](GemmParams& p, const uint8_t* wc, const uint8_t* wsc, const uint8_t* bc,
+                       const uint8_t* bsc, int K, uint64_t wrows, int M, void* out) -> moe_status {
+        std::memset(&p, 0, sizeof p);
+        p.cnt = cnt;
+        p.off = off;
+        p.G = E;
+        p.has_shared = S;
+        p.shared_rows = static_cast<int32_t>(T);
+        p.shared_b_off = static_cast<int32_t>(Tk);
+        p.status = status;
+        p.timeout_ns = kWaitTimeoutNs;
+        if (!make_map_u8(&p.a0, wc, K, wrows, kk8, BM, true) ||
+            !make_map_u8(&p.sa0, wsc, K / 32, wrows, sbox8, BM) ||
+            !make_map_u8(&p.b, bc, K, rows, kk8, big8, true) ||
+            !make_map_u8(&p.b32, bc, K, rows, kk8, 32, true) ||
+            !make_map_u8(&p.sb_scale, bsc, K / 32, rows, sbox8, 128))
+            return MOE_ERR_CUDA;
+        p.M = M;
+        p.MT = M / (2 * BM);
+        p.KB = K / kk8;
+        p.out = out;
+        p.out_f32 = 1;
+        p.ldo = M;
+        p.sc_ahead = rows >= static_cast<int64_t>(G) * tn8 ? 1 : 0;
+        const int64_t tb = ((rows + tn8 - 1) / tn8 + G) * p.MT;
+        return cu(launch_bs_gemm(BS_MXFP8, GEMM_DOWN, p, static_cast<int>(tb < units ? tb : units), s));
+    };
     {
         GemmParams p;
-        common(p, S, status + 6);
-        if (!make_map(&p.a0, wtb + WW.wdt, D, EF, BM)) return MOE_ERR_CUDA;
-        if (S && !make_map(&p.as0, wtb + WW.swdt, D, F, BM)) return MOE_ERR_CUDA;
-        if (!make_map(&p.b, dyq, D, rows, box_b) || !make_map(&p.b32, dyq, D, rows, 32))
-            return MOE_ERR_CUDA;
-        p.M = F;
-        p.MT = (F + 2 * BM - 1) / (2 * BM);
-        p.KB = D / BK;
-        p.out = wsb + L.dh;
-        p.out_f32 = 1;
-        p.ldo = F;
         MOE_TRY(mark_b(MOE_BWD_STAGE_DH, 0, s));
-        MOE_TRY(launch(GEMM_DOWN, p, tok_tiles + sh_tiles));
+        MOE_TRY(bs_down(p, wtb + WW.wd, wtb + WW.wds, dyc, dys, D, GF, F, wsb + L.dh));
         MOE_TRY(mark_b(MOE_BWD_STAGE_DH, 1, s));
     }
 
     // 5. SwiGLU backward -> [dA | dB], quantised along F and along tokens
-    uint16_t* dabq = reinterpret_cast<uint16_t*>(wsb + L.dabq);
+    uint8_t* dabc = wsb + L.dabq;
+    uint8_t* dabs = dabc + rows * 2 * F;
     MOE_TRY(mark_b(MOE_BWD_STAGE_SWIGLU, 0, s));
     MOE_TRY(cu(launch_swiglu_dual(reinterpret_cast<const float*>(wsb + L.dh),
                                   reinterpret_cast<const float*>(wsb + L.a),
                                   reinterpret_cast<const float*>(wsb + L.b), F, cnt, off, poff, E, G,
-                                  Tk, srows, L.kpad, dabq, dabt, sms, s)));
+                                  Tk, srows, L.kpad, dabc, dabs, dabt, sms, s)));
     MOE_TRY(mark_b(MOE_BWD_STAGE_SWIGLU, 1, s));
 
     // 6. dXp = Q_F(dA) Q_F(Wg) + Q_F(dB) Q_F(Wu)  (one K = 2F GEMM), then dx
     {
         GemmParams p;
-        common(p, S, status + 7);
-        if (!make_map(&p.a0, wtb + WW.w2t, 2 * F, ED, BM)) return MOE_ERR_CUDA;
-        if (S && !make_map(&p.as0, wtb + WW.sw2t, 2 * F, D, BM)) return MOE_ERR_CUDA;
-        if (!make_map(&p.b, dabq, 2 * F, rows, box_b) || !make_map(&p.b32, dabq, 2 * F, rows, 32))
-            return MOE_ERR_CUDA;
-        p.M = D;
-        p.MT = (D + 2 * BM - 1) / (2 * BM);
-        p.KB = 2 * F / BK;
-        p.out = wsb + L.dxp;
-        p.out_f32 = 1;
-        p.ldo = D;
         MOE_TRY(mark_b(MOE_BWD_STAGE_DXP, 0, s));
-        MOE_TRY(launch(GEMM_DOWN, p, tok_tiles + sh_tiles));
+        MOE_TRY(bs_down(p, wtb + WW.w2, wtb + WW.w2s, dabc, dabs, 2 * F, GD, D, wsb + L.dxp));
         MOE_TRY(mark_b(MOE_BWD_STAGE_DXP, 1, s));
     }
     MOE_TRY(mark_b(MOE_BWD_STAGE_DX, 0, s));
@@ -1174,24 +1187,26 @@ moe_status moe_backward_prepare_weights(const moe_dims* d, const moe_weights* w,
     auto* o = static_cast<uint8_t*>(wt);
     const int E = d->E, D = d->d, F = d->F;
     const int64_t FD = int64_t(F) * D;
-    auto* wdt = reinterpret_cast<uint16_t*>(o + W.wdt);
-    auto* w2t = reinterpret_cast<uint16_t*>(o + W.w2t);
-    // Wd [d][F] -> [F][d] quantised along d; Wg, Wu [F][d] -> [d][2F] quantised along F
+    uint8_t* wd = o + W.wd;
+    uint8_t* wds = o + W.wds;
+    uint8_t* w2 = o + W.w2;
+    uint8_t* w2s = o + W.w2s;
+    // Wd [d][F] -> [F][d] quantised along d; Wg, Wu [F][d] -> [d][2F] quantised
+    // along F; codes, and scale bytes at the code offset / 32; the shared
+    // expert is group E
+    auto q = [&](const void* src, int nb, int R, int C, int64_t g0, int64_t per, int64_t ld,
+                 int64_t col0, uint8_t* codes, uint8_t* scales) {
+        return cu(launch_tq_batch(static_cast<const uint16_t*>(src), nb, R, C, codes + g0 * per,
+                                  scales + g0 * per / 32, per, ld, col0, sms, s));
+    };
     MOE_TRY(mark_b(MOE_BWD_STAGE_PREPARE, 0, s));
-    MOE_TRY(cu(launch_tq_batch(static_cast<const uint16_t*>(w->w_down), E, D, F, wdt, FD, D, 0, sms, s)));
-    MOE_TRY(cu(launch_tq_batch(static_cast<const uint16_t*>(w->w_gate), E, F, D, w2t, 2 * FD, 2 * F, 0,
-                               sms, s)));
-    MOE_TRY(cu(launch_tq_batch(static_cast<const uint16_t*>(w->w_up), E, F, D, w2t, 2 * FD, 2 * F, F,
-                               sms, s)));
+    MOE_TRY(q(w->w_down, E, D, F, 0, FD, D, 0, wd, wds));
+    MOE_TRY(q(w->w_gate, E, F, D, 0, 2 * FD, 2 * F, 0, w2, w2s));
+    MOE_TRY(q(w->w_up, E, F, D, 0, 2 * FD, 2 * F, F, w2, w2s));
     if (d->n_shared) {
-        auto* swdt = reinterpret_cast<uint16_t*>(o + W.swdt);
-        auto* sw2t = reinterpret_cast<uint16_t*>(o + W.sw2t);
-        MOE_TRY(cu(launch_tq_batch(static_cast<const uint16_t*>(w->ws_down), 1, D, F, swdt, FD, D, 0,
-                                   sms, s)));
-        MOE_TRY(cu(launch_tq_batch(static_cast<const uint16_t*>(w->ws_gate), 1, F, D, sw2t, 2 * FD,
-                                   2 * F, 0, sms, s)));
-        MOE_TRY(cu(launch_tq_batch(static_cast<const uint16_t*>(w->ws_up), 1, F, D, sw2t, 2 * FD,
-                                   2 * F, F, sms, s)));
+        MOE_TRY(q(w->ws_down, 1, D, F, E, FD, D, 0, wd, wds));
+        MOE_TRY(q(w->ws_gate, 1, F, D, E, 2 * FD, 2 * F, 0, w2, w2s));
+        MOE_TRY(q(w->ws_up, 1, F, D, E, 2 * FD, 2 * F, F, w2, w2s));
     }
     return mark_b(MOE_BWD_STAGE_PREPARE, 1, s);
 }

@@ -7,10 +7,13 @@
 // Microscaling Formats (MX) v1.0 specification defines it: per block,
 // X = floor(log2(max |v|)) - 8 (8 = the exponent of E4M3's largest normal),
 // element = E4M3(v * 2^-X), nearest even, clamped to +-448.  Every operand of
-// a grouped GEMM is quantised along that GEMM's contraction axis; the kernels
-// here write the dequantised values e4m3 * 2^X as bf16, which holds them
-// exactly (at most 4 significant bits, and the exponents the layer produces),
-// so the bf16 tcgen05 MMAs that follow multiply exactly the MXFP8 values.
+// a grouped GEMM is quantised along that GEMM's contraction axis.  The operands
+// of the dH and dXp GEMMs (the weight copies, dY and [dA | dB] along their
+// rows) are written as E4M3 codes and E8M0 scale bytes (X + 127) for the
+// block-scaled tensor-core MMA (gemm_bs.cu); the token-major operands of the
+// weight-gradient GEMMs as the dequantised values e4m3 * 2^X in bf16, which
+// holds them exactly (at most 4 significant bits, and the exponents the layer
+// produces), so the bf16 tcgen05 MMAs there multiply exactly the MXFP8 values.
 // The pages prefer a fast approximate division in the MXFP8 quantiser; the
 // scaling by 2^-X here is a multiplication by a power of two, which is exact.
 #include <cuda_bf16.h>
@@ -88,7 +91,14 @@ struct TqBlock {
 struct TqArgs {
     int C;        // input columns = output rows
     int64_t ld;   // output row stride (elements)
-    uint16_t* out;
+    uint16_t* out;  // bf16 values (segment mode)
+    // batch mode: E4M3 codes at the element offsets of `out`, and the E8M0
+    // scale byte of each block of 32 at that offset / 32; sc_vec: every
+    // group of kTqGroup tiles starts a 32-byte run of the scales (ld,
+    // out_bstride and out_off multiples of 1024, scales 16-byte aligned)
+    uint8_t* codes;
+    uint8_t* scales;
+    int sc_vec;
     // segment mode: groups of rows, each padded to a multiple of 64 output
     // columns starting at poff[g]; group g < E reads rows off[g] .. + cnt[g],
     // group E (the shared expert) rows shared_row0 .. + shared_rows
@@ -150,11 +160,85 @@ __device__ __forceinline__ void tq_store16(uint16_t* out, int64_t at, const floa
     o[1] = mx_qdq8(v1, X);
 }
 
+// 16 values of one block half as E4M3 codes of v * 2^-X (one 16-byte store),
+// and the block's scale byte X + 127 from the thread holding its first half.
+__device__ __forceinline__ uint4 mx_codes16(const float (&v)[16], int X) {
+    const float inv = exp2i(-X);
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        w[i] = __nv_cvt_float2_to_fp8x2(make_float2(v[2 * i] * inv, v[2 * i + 1] * inv),
+                                        __NV_SATFINITE, __NV_E4M3);
+    return make_uint4(w[0] | (w[1] << 16), w[2] | (w[3] << 16), w[4] | (w[5] << 16),
+                      w[6] | (w[7] << 16));
+}
+
+__device__ __forceinline__ void mx_store_codes16(uint8_t* codes, uint8_t* scales, int64_t at,
+                                                 const float (&v)[16], int X, bool first_half) {
+    *reinterpret_cast<uint4*>(codes + at) = mx_codes16(v, X);
+    if (first_half) scales[at / 32] = static_cast<uint8_t>(X + 127);
+}
+
 // bf16 rows as stored, times the row's factor where the source has one (the
 // product is taken in fp32 before quantising): the tile holds the bf16 of
 // rows 2R and 2R + 1 of a column in one 32-bit word, tp[R][column ^ sw(R)],
 // sw(R) = 8 * ((R / 8) % 4).  Loading: thread t reads rows 2 (t / 8) and
 // 2 (t / 8) + 1, columns 8 (t % 8) .. + 7 (two 16-byte loads).
+// Rows 2R and 2R + 1 (R = t / 8), columns 8 (t % 8) .. + 7 into the tile.
+__device__ __forceinline__ void tq_put_pair(uint32_t (*tp)[64], int tid, const uint4& lo,
+                                            const uint4& hi) {
+    const int R = tid >> 3, c8 = (tid & 7) * 8;
+    const uint32_t l[4] = {lo.x, lo.y, lo.z, lo.w}, h[4] = {hi.x, hi.y, hi.z, hi.w};
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        w[2 * i] = __byte_perm(l[i], h[i], 0x5410);      // column 2i of both rows
+        w[2 * i + 1] = __byte_perm(l[i], h[i], 0x7632);  // column 2i + 1
+    }
+    uint4* dst = reinterpret_cast<uint4*>(&tp[R][c8 ^ (((R >> 3) & 3) << 3)]);
+    dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+template <class Src>
+__device__ __forceinline__ void tq_load_tile(const Src& src, const TqBlock& blk, int cb, int tid,
+                                             uint32_t (*tp)[64], float* rs) {
+    const int R = tid >> 3, c8 = (tid & 7) * 8;
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+    float s0 = 0.0f, s1 = 0.0f;
+    if (2 * R < blk.nvalid) lo = src.raw8(blk.in_row0 + 2 * R, cb + c8, s0);
+    if (2 * R + 1 < blk.nvalid) hi = src.raw8(blk.in_row0 + 2 * R + 1, cb + c8, s1);
+    if constexpr (!Src::kUnitScale) {
+        if ((tid & 7) == 0) {
+            rs[2 * R] = s0;
+            rs[2 * R + 1] = s1;
+        }
+    }
+    tq_put_pair(tp, tid, lo, hi);
+}
+
+// Column pass: thread t takes column c = t / 4, rows 16 (t % 4) .. + 15, times
+// their factors; returns the block maximum shared with thread t ^ 1.
+template <bool kUnitScale>
+__device__ __forceinline__ float tq_column16(const uint32_t (*tp)[64], const float* rs, int tid,
+                                             float (&v)[16]) {
+    const int c = tid >> 2, part = tid & 3;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const uint32_t w = tp[part * 8 + j][c ^ (part << 3)];
+        v[2 * j] = __uint_as_float(w << 16);
+        v[2 * j + 1] = __uint_as_float(w & 0xFFFF0000u);
+        if constexpr (!kUnitScale) {
+            v[2 * j] *= rs[part * 16 + 2 * j];
+            v[2 * j + 1] *= rs[part * 16 + 2 * j + 1];
+        }
+    }
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
+    return fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+}
+
 template <class Src, bool SEG>
 __global__ void __launch_bounds__(256, 8) tq16_kernel(Src src, TqArgs a) {
     __shared__ __align__(16) uint32_t tp[kTqRows / 2][64];
@@ -167,51 +251,75 @@ __global__ void __launch_bounds__(256, 8) tq16_kernel(Src src, TqArgs a) {
         const int cb = static_cast<int>(it % cchunks) * 64;
         TqBlock blk;
         if (!tq_tile<SEG>(a, rt, blk)) continue;  // uniform across the CTA
-        {
-            const int R = tid >> 3, c8 = (tid & 7) * 8;
-            uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
-            float s0 = 0.0f, s1 = 0.0f;
-            if (2 * R < blk.nvalid) lo = src.raw8(blk.in_row0 + 2 * R, cb + c8, s0);
-            if (2 * R + 1 < blk.nvalid) hi = src.raw8(blk.in_row0 + 2 * R + 1, cb + c8, s1);
-            if constexpr (!Src::kUnitScale) {
-                if ((tid & 7) == 0) {
-                    rs[2 * R] = s0;
-                    rs[2 * R + 1] = s1;
-                }
-            }
-            const uint32_t l[4] = {lo.x, lo.y, lo.z, lo.w}, h[4] = {hi.x, hi.y, hi.z, hi.w};
-            uint32_t w[8];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                w[2 * i] = __byte_perm(l[i], h[i], 0x5410);      // column 2i of both rows
-                w[2 * i + 1] = __byte_perm(l[i], h[i], 0x7632);  // column 2i + 1
-            }
-            uint4* dst = reinterpret_cast<uint4*>(&tp[R][c8 ^ (((R >> 3) & 3) << 3)]);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
-        }
+        tq_load_tile(src, blk, cb, tid, tp, rs);
         __syncthreads();
         {
             const int c = tid >> 2, part = tid & 3;
             float v[16];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t w = tp[part * 8 + j][c ^ (part << 3)];
-                v[2 * j] = __uint_as_float(w << 16);
-                v[2 * j + 1] = __uint_as_float(w & 0xFFFF0000u);
-                if constexpr (!Src::kUnitScale) {
-                    v[2 * j] *= rs[part * 16 + 2 * j];
-                    v[2 * j + 1] *= rs[part * 16 + 2 * j + 1];
-                }
-            }
-            float m = 0.0f;
-#pragma unroll
-            for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
-            m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+            const float m = tq_column16<Src::kUnitScale>(tp, rs, tid, v);
             tq_store16(a.out, static_cast<int64_t>(cb + c) * a.ld + blk.out_col + part * 16, v,
                        mx_block_exp(m));
         }
         __syncthreads();
+    }
+}
+
+// The weight copies (batch mode) as E4M3 codes and scale bytes.  A tile gives
+// each output row 2 scale bytes; a CTA item therefore takes one 64-column chunk
+// of up to kTqGroup consecutive tiles of a matrix, collects their scale bytes
+// in shared memory and stores each output row's 2 * kTqGroup = 32 bytes as one
+// whole 32-byte sector (two 16-byte stores of neighbouring lanes) when the
+// layout aligns them (a.sc_vec), bytewise otherwise.
+constexpr int kTqGroup = 16;
+
+__global__ void __launch_bounds__(256, 8) tq_codes_kernel(SrcBf16 src, TqArgs a) {
+    __shared__ __align__(16) uint32_t tp[kTqRows / 2][64];
+    __shared__ __align__(16) uint8_t sc[64][2 * kTqGroup];
+    const int tid = threadIdx.x;
+    const int cchunks = a.C / 64;
+    const int per = a.R / kTqRows;                     // tiles per matrix
+    const int gper = (per + kTqGroup - 1) / kTqGroup;  // tile groups per matrix
+    const int64_t items = a.ntiles / per * gper * cchunks;
+    const int c = tid >> 2, part = tid & 3;
+    for (int64_t it = blockIdx.x; it < items; it += gridDim.x) {
+        const int64_t grp = it / cchunks;
+        const int cb = static_cast<int>(it % cchunks) * 64;
+        const int64_t b = grp / gper;
+        const int t0 = static_cast<int>(grp % gper) * kTqGroup;
+        const int n = min(kTqGroup, per - t0);
+        const int64_t col0 = b * a.out_bstride + a.out_off + static_cast<int64_t>(t0) * kTqRows;
+        // this thread's input rows 2 (t / 8) and + 1 of the group's first tile,
+        // and its 16 codes in output row cb + c; both advance by one tile
+        const uint16_t* in =
+            src.p + (b * a.R + t0 * kTqRows + 2 * (tid >> 3)) * src.ld + cb + (tid & 7) * 8;
+        uint8_t* out = a.codes + static_cast<int64_t>(cb + c) * a.ld + col0 + part * 16;
+        for (int j = 0; j < n; ++j) {
+            tq_put_pair(tp, tid, *reinterpret_cast<const uint4*>(in),
+                        *reinterpret_cast<const uint4*>(in + src.ld));
+            in += kTqRows * src.ld;
+            __syncthreads();
+            float v[16];
+            const int X = mx_block_exp(tq_column16<true>(tp, nullptr, tid, v));
+            *reinterpret_cast<uint4*>(out) = mx_codes16(v, X);
+            out += kTqRows;
+            if ((part & 1) == 0) sc[c][2 * j + (part >> 1)] = static_cast<uint8_t>(X + 127);
+            __syncthreads();
+        }
+        // row cb + r gets bytes [s0, s0 + 2n) of the scales; the next item's
+        // first barrier orders these reads before sc is written again
+        if (a.sc_vec && n == kTqGroup) {
+            if (tid < 128) {
+                const int r = tid >> 1, h = tid & 1;
+                const int64_t s0 = (static_cast<int64_t>(cb + r) * a.ld + col0) / 32;
+                *reinterpret_cast<uint4*>(a.scales + s0 + 16 * h) =
+                    *reinterpret_cast<const uint4*>(&sc[r][16 * h]);
+            }
+        } else {
+            for (int i = tid; i < 64 * 2 * n; i += blockDim.x) {
+                const int r = i / (2 * n), q = i % (2 * n);
+                a.scales[(static_cast<int64_t>(cb + r) * a.ld + col0) / 32 + q] = sc[r][q];
+            }
+        }
     }
 }
 
@@ -235,13 +343,15 @@ __device__ __forceinline__ void tf_put16(float (*tf)[64], int r, int c16, const 
 }
 
 // Row pass: the block maximum of threads t and t ^ 1 (every lane takes part in
-// the shuffle); the quantised values are written only for rows that exist.
-__device__ __forceinline__ void row_q16(const float (&v)[16], bool store, uint16_t* dst) {
+// the shuffle); codes and scale byte (element offset `at` of a row-major
+// operand) are written only for rows that exist.
+__device__ __forceinline__ void row_q16(const float (&v)[16], bool store, uint8_t* codes,
+                                        uint8_t* scales, int64_t at, bool first_half) {
     float m = 0.0f;
 #pragma unroll
     for (int i = 0; i < 16; ++i) m = fmaxf(m, fabsf(v[i]));
     m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
-    if (store) tq_store16(dst, 0, v, mx_block_exp(m));
+    if (store) mx_store_codes16(codes, scales, at, v, mx_block_exp(m), first_half);
 }
 
 // Column pass: thread (column c, part) takes rows 16 part .. + 15 of column c.
@@ -259,13 +369,15 @@ __device__ __forceinline__ void col_q16(const float (*tf)[64], int c, int part, 
 // Q_d(dY), dY = gate * dout, in token order: each token's dout row is read
 // once and its k routed rows (gate(t, s) * dout[t], at dispatch position
 // inv[t k + s]) and its shared-expert row (dout[t], at Tk + t) are quantised
-// along d and stored; zero rows for a token whose replayed ids were rejected.
-// Thread i takes 8 columns; four neighbouring threads hold one block of 32.
+// along d and stored as codes dyc [rows][d] and scale bytes dys [rows][d / 32];
+// zero rows for a token whose replayed ids were rejected.  Thread i takes 8
+// columns; four neighbouring threads hold one block of 32.
 constexpr int kDyMaxRows = 9;  // k slots + the shared expert
 
 __global__ void __launch_bounds__(256) dy_rows_kernel(SrcDy src, const int32_t* __restrict__ inv,
                                                       int64_t T, int n_shared, int d,
-                                                      uint16_t* __restrict__ dyq) {
+                                                      uint8_t* __restrict__ dyc,
+                                                      uint8_t* __restrict__ dys) {
     __shared__ int64_t dst[kDyMaxRows];
     __shared__ float sc[kDyMaxRows];
     const int k = src.k;
@@ -294,7 +406,16 @@ __global__ void __launch_bounds__(256) dy_rows_kernel(SrcDy src, const int32_t* 
                 }
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
-                *reinterpret_cast<uint4*>(dyq + dst[j] * d + c) = mx_qdq8(v, mx_block_exp(m));
+                const int X = mx_block_exp(m);
+                const float inv = exp2i(-X);
+                uint32_t cw[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    cw[i] = __nv_cvt_float2_to_fp8x2(make_float2(v[2 * i] * inv, v[2 * i + 1] * inv),
+                                                     __NV_SATFINITE, __NV_E4M3);
+                *reinterpret_cast<uint2*>(dyc + dst[j] * d + c) =
+                    make_uint2(cw[0] | (cw[1] << 16), cw[2] | (cw[3] << 16));
+                if ((threadIdx.x & 3) == 0) dys[dst[j] * (d / 32) + c / 32] = static_cast<uint8_t>(X + 127);
             }
         }
         __syncthreads();
@@ -303,11 +424,12 @@ __global__ void __launch_bounds__(256) dy_rows_kernel(SrcDy src, const int32_t* 
 
 // SwiGLU backward (h = silu(a) * b, silu(a) = a * sigmoid(a)):
 //   dA = dH * b * sigmoid(a) * (1 + a * (1 - sigmoid(a))),   dB = dH * silu(a),
-// quantised into [Q_F(dA) | Q_F(dB)] rows [rows][2F] for the dXp GEMM and the
-// token-major [Q_tok(dA) ; Q_tok(dB)] [2F][kpad] for the dWg / dWu GEMM.
+// quantised into [Q_F(dA) | Q_F(dB)] rows [rows][2F] for the dXp GEMM (codes
+// dabc, scale bytes dabs [rows][2F / 32]) and the token-major
+// [Q_tok(dA) ; Q_tok(dB)] [2F][kpad] (bf16) for the dWg / dWu GEMM.
 __global__ void __launch_bounds__(256, 4) swiglu_dual_kernel(
     const float* __restrict__ dh, const float* __restrict__ A, const float* __restrict__ Bv,
-    TqArgs a, uint16_t* __restrict__ dabq, int F) {
+    TqArgs a, uint8_t* __restrict__ dabc, uint8_t* __restrict__ dabs, int F) {
     __shared__ __align__(16) float ta[kTqRows][64];
     __shared__ __align__(16) float tb[kTqRows][64];
     const int tid = threadIdx.x;
@@ -340,9 +462,10 @@ __global__ void __launch_bounds__(256, 4) swiglu_dual_kernel(
                     db[4 * q + j] = gg[j] * (xa[j] * sg);
                 }
             }
-            uint16_t* qrow = dabq + row * 2 * F + cb + c16;
-            row_q16(da, ok, qrow);
-            row_q16(db, ok, qrow + F);
+            const int64_t at = row * 2 * F + cb + c16;
+            const bool first = (tid & 1) == 0;
+            row_q16(da, ok, dabc, dabs, at, first);
+            row_q16(db, ok, dabc, dabs, at + F, first);
             tf_put16(ta, r, c16, da);
             tf_put16(tb, r, c16, db);
         }
@@ -620,14 +743,14 @@ cudaError_t launch_tq_segments(const uint16_t* src, int64_t src_ld, int C, const
 
 cudaError_t launch_dy_dual(const SegDyArgs& dy, int d, const int32_t* cnt, const int32_t* off,
                            const int32_t* poff, int E, int G, int shared_rows, int64_t kpad,
-                           uint16_t* dyq, uint16_t* dyt, int sms, cudaStream_t s) {
+                           uint8_t* dyc, uint8_t* dys, uint16_t* dyt, int sms, cudaStream_t s) {
     if (kpad % kTqRows || d % 256 || dy.k + (dy.n_shared ? 1 : 0) > kDyMaxRows)
         return cudaErrorInvalidValue;
     const SrcDy src{dy.dout, dy.gates, dy.perm, dy.valid, dy.k, dy.Tk, d};
     if (dy.T > 0) {
         const int64_t cap = static_cast<int64_t>(sms) * 8;
         dy_rows_kernel<<<static_cast<unsigned>(dy.T < cap ? dy.T : cap), 256, 0, s>>>(
-            src, dy.inv, dy.T, dy.n_shared, d, dyq);
+            src, dy.inv, dy.T, dy.n_shared, d, dyc, dys);
     }
     // Q_tok(dY): the same values, quantised along each expert's tokens
     return tq_launch<SrcDy, true>(src, seg_args(d, cnt, off, poff, E, G, dy.Tk, shared_rows, kpad,
@@ -638,29 +761,39 @@ cudaError_t launch_dy_dual(const SegDyArgs& dy, int d, const int32_t* cnt, const
 cudaError_t launch_swiglu_dual(const float* dh, const float* a_pre, const float* b_pre, int F,
                                const int32_t* cnt, const int32_t* off, const int32_t* poff, int E,
                                int G, int64_t shared_row0, int shared_rows, int64_t kpad,
-                               uint16_t* dabq, uint16_t* dabt, int sms, cudaStream_t s) {
+                               uint8_t* dabc, uint8_t* dabs, uint16_t* dabt, int sms,
+                               cudaStream_t s) {
     if (kpad % kTqRows || F % 64) return cudaErrorInvalidValue;
     const TqArgs a = seg_args(F, cnt, off, poff, E, G, shared_row0, shared_rows, kpad, dabt);
     const int64_t items = a.ntiles * (F / 64);
     if (items == 0) return cudaSuccess;
-    swiglu_dual_kernel<<<grid_for(items, 1, sms, 4), 256, 0, s>>>(dh, a_pre, b_pre, a, dabq, F);
+    swiglu_dual_kernel<<<grid_for(items, 1, sms, 4), 256, 0, s>>>(dh, a_pre, b_pre, a, dabc, dabs,
+                                                                   F);
     return cudaGetLastError();
 }
 
-cudaError_t launch_tq_batch(const uint16_t* src, int nb, int R, int C, uint16_t* out,
-                            int64_t out_bstride, int64_t out_ld, int64_t out_off, int sms,
-                            cudaStream_t s) {
+cudaError_t launch_tq_batch(const uint16_t* src, int nb, int R, int C, uint8_t* codes,
+                            uint8_t* scales, int64_t out_bstride, int64_t out_ld, int64_t out_off,
+                            int sms, cudaStream_t s) {
     if (R % kTqRows) return cudaErrorInvalidValue;
     TqArgs a{};
     a.C = C;
     a.ld = out_ld;
-    a.out = out;
+    a.codes = codes;
+    a.scales = scales;
     a.R = R;
     a.out_bstride = out_bstride;
     a.out_off = out_off;
     a.ntiles = static_cast<int64_t>(nb) * (R / kTqRows);
-    if (out_off % 8 || out_bstride % 8) return cudaErrorInvalidValue;
-    return tq_launch<SrcBf16, false>(SrcBf16{src, C}, a, sms, s);
+    // every block of 32 starts on a multiple of 32 (one scale byte each)
+    if (C % 64 || out_ld % 32 || out_off % 32 || out_bstride % 32) return cudaErrorInvalidValue;
+    a.sc_vec = out_ld % 1024 == 0 && out_bstride % 1024 == 0 && out_off % 1024 == 0 &&
+               (reinterpret_cast<uintptr_t>(scales) & 15) == 0;
+    const int per = R / kTqRows, gper = (per + kTqGroup - 1) / kTqGroup;
+    const int64_t items = static_cast<int64_t>(nb) * gper * (C / 64);
+    if (items == 0) return cudaSuccess;
+    tq_codes_kernel<<<grid_for(items, 1, sms, 8), 256, 0, s>>>(SrcBf16{src, C}, a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_gate_bwd(const uint16_t* dout, const uint16_t* y, const int32_t* inv,

@@ -15,7 +15,10 @@
 // blocks of 128 bytes per row (one 128-byte-swizzled row of the operand tile,
 // four MMAs).  Each output element is one pair's fixed-order K loop into one
 // TMEM accumulator; no split-K, no atomics; the MMA width N only selects how
-// many independent token columns one instruction produces.
+// many independent token columns one instruction produces.  The MoE backward
+// runs its dH and dXp GEMMs here too (MXFP8 down mode): fp32 output rows
+// (out_f32) and the shared expert as one more group (has_shared) whose weights
+// follow the routed experts' in the same tensors.
 //
 // Roles in each CTA (352 threads): warp 0 TMA producer of the weight tiles (and
 // of the scale tiles); warp 10 TMA producer of the token tiles; warp 1 TMEM
@@ -172,7 +175,9 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
     uint64_t* drain = xempty + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(full + L::kBarriers);
     volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    const int GG = p.G;
+    // the shared expert (has_shared) is group G: its weights are group G of
+    // the same tensors, its token rows shared_rows rows from shared_b_off
+    const int GG = p.G + (p.has_shared ? 1 : 0);
     int* hs = reinterpret_cast<int*>(tmem_slot + 4);
     int* cs = hs + GG + 1;
     int* gcnt = cs + GG + 1;
@@ -189,9 +194,9 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
         const int g0 = lane * per;
         int local_h = 0, local_c = 0;
         for (int g = g0; g < min(g0 + per, GG); ++g) {
-            const int c = p.cnt[g];
+            const int c = g < p.G ? p.cnt[g] : p.shared_rows;
             gcnt[g] = c;
-            goff[g] = p.off[g];
+            goff[g] = g < p.G ? p.off[g] : p.shared_b_off;
             const int ntg = (c + kTile - 1) / kTile;
             if (ntg > 1) local_h += ntg; else local_c += ntg;
         }
@@ -624,10 +629,18 @@ __global__ void __launch_bounds__(kThreads8, 1) bs_pair_kernel(const __grid_cons
                         for (int jj = 0; jj < 32; ++jj)
                             v[jj] *= __shfl_sync(0xffffffffu, tok_scale, jj) * ws0;
                     }
-                    store_pairs8<32>(v, lane,
-                                     static_cast<__nv_bfloat16*>(p.out) +
-                                         static_cast<int64_t>(tl.brow + c0) * p.ldo + (row & ~1),
-                                     p.ldo, tl.n_valid - c0, row_ok);
+                    if (!kNv && p.out_f32) {
+                        // fp32 rows: for each token the 32 lanes store 128 bytes
+                        float* yf = static_cast<float*>(p.out) + static_cast<int64_t>(tl.brow + c0) * p.ldo + row;
+#pragma unroll
+                        for (int jj = 0; jj < 32; ++jj)
+                            if (row_ok && c0 + jj < tl.n_valid) yf[static_cast<int64_t>(jj) * p.ldo] = v[jj];
+                    } else {
+                        store_pairs8<32>(v, lane,
+                                         static_cast<__nv_bfloat16*>(p.out) +
+                                             static_cast<int64_t>(tl.brow + c0) * p.ldo + (row & ~1),
+                                         p.ldo, tl.n_valid - c0, row_ok);
+                    }
                 }
             }
             if (!ok) break;
@@ -659,7 +672,7 @@ size_t bs_smem_bytes(int GG) {
 
 template <int MODE, int FMT>
 cudaError_t launch_bs_mode(const GemmParams& p, int clusters, cudaStream_t s) {
-    const size_t smem = bs_smem_bytes<FMT>(p.G);
+    const size_t smem = bs_smem_bytes<FMT>(p.G + (p.has_shared ? 1 : 0));
     cudaError_t e = cudaFuncSetAttribute(bs_pair_kernel<MODE, FMT>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
@@ -706,7 +719,10 @@ int bs_scale_box(int fmt) {
 int bs_scale_kb(int fmt) { return fmt == BS_NVFP4 ? BsCfg<BS_NVFP4>::kScKb : BsCfg<BS_MXFP8>::kScKb; }
 
 cudaError_t launch_bs_gemm(int fmt, int mode, const GemmParams& p, int clusters, cudaStream_t s) {
-    if (p.G > kMaxGroups8 || p.has_shared || clusters <= 0 || !p.cnt || !p.off)
+    if (p.G + (p.has_shared ? 1 : 0) > kMaxGroups8 || clusters <= 0 || !p.cnt || !p.off)
+        return cudaErrorInvalidValue;
+    // fp32 rows: MXFP8 down projections only; the shared group: MXFP8 only
+    if ((p.out_f32 && (fmt != BS_MXFP8 || mode != GEMM_DOWN)) || (p.has_shared && fmt != BS_MXFP8))
         return cudaErrorInvalidValue;
     if (fmt == BS_MXFP8) return launch_bs_fmt<BS_MXFP8>(mode, p, clusters, s);
     if (fmt == BS_NVFP4) {

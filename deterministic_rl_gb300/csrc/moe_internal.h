@@ -95,7 +95,9 @@ struct GemmParams {
     float* save_a;
     float* save_b;
     // SM-pair down (MODE 2): 1 = fp32 output rows; with out_shared null the
-    // shared group's rows are stored like routed rows (at its B rows).
+    // shared group's rows are stored like routed rows (at its B rows).  The
+    // block-scaled MXFP8 down GEMM takes it too (its shared group, has_shared,
+    // always stores like routed rows).
     int32_t out_f32;
     // SM-pair bf16 gate/up: a0 (and as0) map the packed gate/up weights
     // (64 gate rows then the same 64 up rows per block; 128-row boxes); the
@@ -240,23 +242,26 @@ cudaError_t launch_tq_segments(const uint16_t* src, int64_t src_ld, int C, const
                                int64_t shared_row0, int shared_rows, int64_t kpad, uint16_t* out,
                                int sms, cudaStream_t s);
 // dY (gate(t,s) * dout[t] for the routed row of pair t*k + s, dout[t] for shared
-// row Tk + t; zero for rejected tokens), quantised along d into dyq [rows][d]
-// and along each expert's tokens into dyt [d][kpad].
+// row Tk + t; zero for rejected tokens), quantised along d into E4M3 codes dyc
+// [rows][d] with E8M0 scale bytes dys [rows][d / 32], and along each expert's
+// tokens into dyt [d][kpad] (bf16 values).
 cudaError_t launch_dy_dual(const SegDyArgs& dy, int d, const int32_t* cnt, const int32_t* off,
                            const int32_t* poff, int E, int G, int shared_rows, int64_t kpad,
-                           uint16_t* dyq, uint16_t* dyt, int sms, cudaStream_t s);
+                           uint8_t* dyc, uint8_t* dys, uint16_t* dyt, int sms, cudaStream_t s);
 // SwiGLU backward from dH and the fp32 pre-activations, quantised along F into
-// dabq [rows][2F] = [dA | dB] and along each expert's tokens into dabt
-// [2F][kpad] = [dA ; dB].
+// codes dabc [rows][2F] = [dA | dB] with scale bytes dabs [rows][2F / 32], and
+// along each expert's tokens into dabt [2F][kpad] = [dA ; dB] (bf16 values).
 cudaError_t launch_swiglu_dual(const float* dh, const float* a_pre, const float* b_pre, int F,
                                const int32_t* cnt, const int32_t* off, const int32_t* poff, int E,
                                int G, int64_t shared_row0, int shared_rows, int64_t kpad,
-                               uint16_t* dabq, uint16_t* dabt, int sms, cudaStream_t s);
-// Batch mode: nb matrices [R][C] bf16 -> out[b * out_bstride + c * out_ld +
-// out_off + r] quantised along r.
-cudaError_t launch_tq_batch(const uint16_t* src, int nb, int R, int C, uint16_t* out,
-                            int64_t out_bstride, int64_t out_ld, int64_t out_off, int sms,
-                            cudaStream_t s);
+                               uint8_t* dabc, uint8_t* dabs, uint16_t* dabt, int sms,
+                               cudaStream_t s);
+// Batch mode: nb matrices [R][C] bf16 -> E4M3 codes at codes[b * out_bstride +
+// c * out_ld + out_off + r], quantised along r, and the E8M0 scale byte of each
+// block of 32 at scales[that offset / 32].
+cudaError_t launch_tq_batch(const uint16_t* src, int nb, int R, int C, uint8_t* codes,
+                            uint8_t* scales, int64_t out_bstride, int64_t out_ld, int64_t out_off,
+                            int sms, cudaStream_t s);
 // Gate gradients, softmax backward and the router's part of dx (written to dx).
 cudaError_t launch_gate_bwd(const uint16_t* dout, const uint16_t* y, const int32_t* inv,
                             const int32_t* ids, const float* gates, const int32_t* valid,

@@ -269,9 +269,13 @@ class MoELayer:
             "y": view(L.y, T * k * d, torch.bfloat16).view(T * k, d),
             "dg": view(L.dg, T * k, torch.float32).view(T, k),
             "dl": view(L.dl, T * k, torch.float32).view(T, k),
-            "dyq": view(L.dyq, rows * d, torch.bfloat16).view(rows, d),
+            # E4M3 codes and E8M0 scale bytes of the dH and dXp GEMMs' token rows
+            "dyq": view(L.dyq, rows * d, torch.uint8).view(rows, d),
+            "dyq_scales": view(L.dyq + rows * d, rows * d // 32, torch.uint8).view(rows, d // 32),
             "dh": view(L.dh, rows * F, torch.float32).view(rows, F),
-            "dabq": view(L.dabq, rows * 2 * F, torch.bfloat16).view(rows, 2 * F),
+            "dabq": view(L.dabq, rows * 2 * F, torch.uint8).view(rows, 2 * F),
+            "dabq_scales": view(L.dabq + rows * 2 * F, rows * 2 * F // 32,
+                                torch.uint8).view(rows, 2 * F // 32),
             "dxp": view(L.dxp, rows * d, torch.float32).view(rows, d),
             "xpt": view(L.xpt, d * kp, torch.bfloat16).view(d, kp),
             "dyt": view(L.dyt, d * kp, torch.bfloat16).view(d, kp),

@@ -339,7 +339,9 @@ moe_status moe_route_static(const moe_dims *dims, const void *x, const moe_weigh
  *     dWg = Q_tok(dA)^T . Q_tok(Xp),  dWu = Q_tok(dB)^T . Q_tok(Xp)
  * where along tokens an expert's blocks start at its first row in dispatch
  * order (pairs t*k + s ascending), the last block zero-padded.  The products
- * are exact and accumulate in fp32 (tcgen05, TMEM).  The gate and router
+ * are exact and accumulate in fp32 (tcgen05, TMEM): dH and dXp on the
+ * block-scaled MXFP8 MMA (E4M3 codes and E8M0 scales of both operands), the
+ * weight gradients on bf16 MMAs of the exact MXFP8 values.  The gate and router
  * gradients are not grouped GEMMs and are taken in fp32 from the forward's
  * values: dg_s = dout . Y_s (Y the forward's bf16 expert output),
  * dl_s = w_s (dg_s - sum_s' w_s' dg_s'), d_router[e] = sum over e's rows of
@@ -352,8 +354,9 @@ moe_status moe_route_static(const moe_dims *dims, const void *x, const moe_weigh
  * invariant).  Weight gradients are fp32 and are written, not accumulated
  * into; each element is one CTA's fixed-order K loop (bitwise repeatable).
  *
- * Limits: bf16 expert weights (MOE_ERR_UNSUPPORTED otherwise); d and F
- * multiples of 256 (MOE_ERR_SHAPE otherwise); the other limits of the forward.
+ * Limits: bf16 expert weights (MOE_ERR_UNSUPPORTED otherwise); d a multiple of
+ * 512 and F of 256 (MOE_ERR_SHAPE otherwise: the block-scaled GEMMs take K in
+ * steps of 512); the other limits of the forward.
  */
 typedef struct {
     float *d_router;                  /* [E][d]                                  */
@@ -369,10 +372,12 @@ size_t moe_backward_weights_size(const moe_dims *dims);
 
 /* The expert weights quantised along the backward's contraction axes and
  * transposed, into wt (device, caller-owned, moe_backward_weights_size bytes,
- * 16-byte aligned): per expert Q_d(Wd)^T [F][d], then [Q_F(Wg)^T | Q_F(Wu)^T]
- * [d][2F], then the same for the shared expert, as bf16 holding the exact
- * MXFP8 values.  Depends on the weights only: call it once per weight update
- * and pass wt to every moe_backward with those weights. */
+ * 16-byte aligned), G = E + n_shared groups (the shared expert is group E),
+ * each region starting on a 256-byte boundary: E4M3 codes of Q_d(Wd)^T
+ * [G][F][d]; their E8M0 scale bytes [G][F][d/32]; codes of
+ * [Q_F(Wg)^T | Q_F(Wu)^T] [G][d][2F]; their scale bytes [G][d][2F/32].
+ * Depends on the weights only: call it once per weight update and pass wt to
+ * every moe_backward with those weights. */
 moe_status moe_backward_prepare_weights(const moe_dims *dims, const moe_weights *w, void *wt,
                                         size_t wt_bytes, moe_stream_t stream);
 
@@ -385,7 +390,9 @@ size_t moe_backward_workspace_size(const moe_dims *dims);
  * used, poff [E+S+1] int32 padded token offsets per expert (followed by
  * [kpad/64] int32: the group of each 64-row tile, -1 past the last), a/b [rows][F]
  * fp32 gate/up pre-activations, dg/dl [T][k] fp32 gate and logit gradients,
- * dyq [rows][d], dh [rows][F] fp32, dabq [rows][2F] (quantised dA | dB),
+ * dyq: Q_d(dY) as E4M3 codes [rows][d] then E8M0 scale bytes [rows][d/32],
+ * dh [rows][F] fp32, dabq: [Q_F(dA) | Q_F(dB)] as codes [rows][2F] then scale
+ * bytes [rows][2F/32],
  * dxp [rows][d] fp32, and the token-major operands xpt, dyt [d][kpad],
  * ht [F][kpad], dabt [2F][kpad] (bf16), rows = T*k + T*n_shared. */
 typedef struct {

@@ -161,12 +161,18 @@ def test_backward_sizes_and_layout(lib):
     assert n - L.dabt >= 2 * 2048 * L.kpad * 2
     # the forward's status word sits at the same place
     assert L.status == B.moe_workspace_layout(d).status
-    assert B.moe_backward_weights_size(d) >= (3 * 384 + 3) * 2048 * 7168 * 2
+    # E4M3 codes and one E8M0 byte per 32 of three matrices per expert, shared one included
+    G, FD = 385, 2048 * 7168
+    assert B.moe_backward_weights_size(d) >= 3 * G * FD * 33 // 32
+    assert B.moe_backward_weights_size(d) < 3 * G * FD * 33 // 32 + 4 * 256
     assert B.moe_backward_weights_size(good_dims(n_shared=0)) < B.moe_backward_weights_size(d)
+    # Q(dY) and [Q(dA) | Q(dB)]: codes then scale bytes
+    assert L.dh - L.dyq >= rows * 7168 * 33 // 32
+    assert L.dxp - L.dabq >= rows * 2 * 2048 * 33 // 32
 
 
-@pytest.mark.parametrize("bad", [dict(d=7168 - 64), dict(F=2048 + 64), dict(k=4), dict(wfmt=1),
-                                 dict(wfmt=2)])
+@pytest.mark.parametrize("bad", [dict(d=7168 - 64), dict(d=7168 - 256), dict(F=2048 + 64),
+                                 dict(k=4), dict(wfmt=1), dict(wfmt=2)])
 def test_backward_unserved_dims(lib, bad):
     d = good_dims(**bad)
     assert B.moe_backward_workspace_size(d) == 0

@@ -23,7 +23,7 @@ def _built():
     oracle.build()
 
 
-def small_cfg(T, d=256, E=16, F=256, shared=1, seed=21, zipf=0.0):
+def small_cfg(T, d=512, E=16, F=256, shared=1, seed=21, zipf=0.0):
     return CONFIGS["c1_tiny"].with_(name=f"bwd_T{T}_E{E}_S{shared}", seed=seed, T=T, d=d, E=E,
                                     F=F, n_shared=shared, zipf=zipf)
 
@@ -108,31 +108,60 @@ def test_rejected_replay_ids_contribute_nothing():
     compare_all(inp, used, dout, dx, g, valid=valid)
 
 
+def mx_values(codes, scales):
+    """fp64 values of E4M3 codes [..., n] with E8M0 scale bytes [..., n / 32]."""
+    v = codes.cpu().view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    x = np.exp2(scales.cpu().numpy().astype(np.float64) - 127.0)
+    return v * np.repeat(x, 32, axis=-1)
+
+
 def test_weight_copies_are_the_oracle_quantisation_bit_for_bit():
+    """The block-scaled operands of dH and dXp: codes and scale bytes of the
+    transposed weights, routed experts then the shared one (group E)."""
     cfg = small_cfg(16, d=512, E=8, F=256)
     inp = make_layer(cfg, "cuda")
     layer = MoELayer.from_inputs(inp)
     wt = layer.prepare_backward()
     torch.cuda.synchronize()
     E, d, F = cfg.E, cfg.d, cfg.F
-    bf = wt.view(torch.bfloat16)
-    n = E * F * d
+    G = E + 1
+    n = G * F * d
     align = lambda b: (b + 255) // 256 * 256  # noqa: E731
-    wdt = bf[:n].view(E, F, d)
-    o2 = align(n * 2) // 2
-    w2t = bf[o2:o2 + 2 * n].view(E, d, 2 * F)
-    o3 = o2 + align(2 * n * 2) // 2
-    swdt = bf[o3:o3 + F * d].view(F, d)
-    o4 = o3 + align(F * d * 2) // 2
-    sw2t = bf[o4:o4 + 2 * F * d].view(d, 2 * F)
+    o_wds = align(n)
+    o_w2 = o_wds + align(n // 32)
+    o_w2s = o_w2 + align(2 * n)
+    assert wt.numel() >= o_w2s + 2 * n // 32
+    wd = mx_values(wt[:n].view(G, F, d), wt[o_wds:o_wds + n // 32].view(G, F, d // 32))
+    w2 = mx_values(wt[o_w2:o_w2 + 2 * n].view(G, d, 2 * F),
+                   wt[o_w2s:o_w2s + 2 * n // 32].view(G, d, 2 * F // 32))
     f64 = lambda t: t.to(torch.float64).cpu().numpy()  # noqa: E731
-    for e in range(E):
-        np.testing.assert_array_equal(f64(wdt[e]), OB.mx_quantize(f64(inp.w_down[e]), 0).T)
-        np.testing.assert_array_equal(f64(w2t[e][:, :F]), OB.mx_quantize(f64(inp.w_gate[e]), 0).T)
-        np.testing.assert_array_equal(f64(w2t[e][:, F:]), OB.mx_quantize(f64(inp.w_up[e]), 0).T)
-    np.testing.assert_array_equal(f64(swdt), OB.mx_quantize(f64(inp.ws_down), 0).T)
-    np.testing.assert_array_equal(f64(sw2t[:, :F]), OB.mx_quantize(f64(inp.ws_gate), 0).T)
-    np.testing.assert_array_equal(f64(sw2t[:, F:]), OB.mx_quantize(f64(inp.ws_up), 0).T)
+    mats = [(inp.w_gate[e], inp.w_up[e], inp.w_down[e]) for e in range(E)]
+    mats.append((inp.ws_gate, inp.ws_up, inp.ws_down))
+    for g, (wg, wu, wdn) in enumerate(mats):
+        np.testing.assert_array_equal(wd[g], OB.mx_quantize(f64(wdn), 0).T)
+        np.testing.assert_array_equal(w2[g][:, :F], OB.mx_quantize(f64(wg), 0).T)
+        np.testing.assert_array_equal(w2[g][:, F:], OB.mx_quantize(f64(wu), 0).T)
+
+
+def test_row_operands_are_the_oracle_quantisation_bit_for_bit():
+    """Q_d(dY) rows (codes and scale bytes) of the dH GEMM: gate(t, s) * dout[t]
+    at the pair's dispatch row, dout[t] at shared row T k + t."""
+    cfg = small_cfg(150, E=16, zipf=1.0)
+    inp = make_layer(cfg, "cuda")
+    layer, ids, dout, dx, g = run_backward(inp)
+    inter = layer.backward_intermediates(cfg.T)
+    T, k, d = cfg.T, cfg.k, cfg.d
+    dyq = mx_values(inter["dyq"], inter["dyq_scales"])
+    gates = inter["gates"].cpu().numpy().astype(np.float64)
+    do = dout.to(torch.float64).cpu().numpy()
+    perm = inter["perm"].cpu().numpy()
+    rows = np.empty((T * k + T, d))
+    for r in range(T * k):
+        pair = perm[r]
+        # the product in fp32, as the kernel forms it before quantising
+        rows[r] = gates.reshape(-1)[pair].astype(np.float32) * do[pair // k].astype(np.float32)
+    rows[T * k:] = do
+    np.testing.assert_array_equal(dyq, OB.mx_quantize(rows, 1))
 
 
 def test_token_major_inputs_are_the_oracle_quantisation_bit_for_bit():
