@@ -371,8 +371,11 @@ __device__ __forceinline__ void col_q16(const float (*tf)[64], int c, int part, 
 // inv[t k + s]) and its shared-expert row (dout[t], at Tk + t) are quantised
 // along d and stored as codes dyc [rows][d] and scale bytes dys [rows][d / 32];
 // zero rows for a token whose replayed ids were rejected.  Thread i takes 8
-// columns; four neighbouring threads hold one block of 32.
+// columns; four neighbouring threads hold one block of 32.  A token's scale
+// bytes are gathered in shared memory and stored as whole 16-byte runs once its
+// rows are done (byte stores from different warps would leave partial sectors).
 constexpr int kDyMaxRows = 9;  // k slots + the shared expert
+constexpr int kDyMaxD = 16384;
 
 __global__ void __launch_bounds__(256) dy_rows_kernel(SrcDy src, const int32_t* __restrict__ inv,
                                                       int64_t T, int n_shared, int d,
@@ -380,6 +383,7 @@ __global__ void __launch_bounds__(256) dy_rows_kernel(SrcDy src, const int32_t* 
                                                       uint8_t* __restrict__ dys) {
     __shared__ int64_t dst[kDyMaxRows];
     __shared__ float sc[kDyMaxRows];
+    __shared__ __align__(16) uint8_t sb[kDyMaxRows][kDyMaxD / 32];
     const int k = src.k;
     const int nd = k + (n_shared ? 1 : 0);
     for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
@@ -415,8 +419,16 @@ __global__ void __launch_bounds__(256) dy_rows_kernel(SrcDy src, const int32_t* 
                                                      __NV_SATFINITE, __NV_E4M3);
                 *reinterpret_cast<uint2*>(dyc + dst[j] * d + c) =
                     make_uint2(cw[0] | (cw[1] << 16), cw[2] | (cw[3] << 16));
-                if ((threadIdx.x & 3) == 0) dys[dst[j] * (d / 32) + c / 32] = static_cast<uint8_t>(X + 127);
+                if ((threadIdx.x & 3) == 0) sb[j][c / 32] = static_cast<uint8_t>(X + 127);
             }
+        }
+        __syncthreads();
+        // d / 32 scale bytes per row, a multiple of 16 (d % 512 == 0)
+        const int runs = d / 512;
+        for (int i = threadIdx.x; i < nd * runs; i += blockDim.x) {
+            const int j = i / runs, q = i % runs;
+            *reinterpret_cast<uint4*>(dys + dst[j] * (d / 32) + 16 * q) =
+                *reinterpret_cast<const uint4*>(&sb[j][16 * q]);
         }
         __syncthreads();
     }
@@ -744,7 +756,8 @@ cudaError_t launch_tq_segments(const uint16_t* src, int64_t src_ld, int C, const
 cudaError_t launch_dy_dual(const SegDyArgs& dy, int d, const int32_t* cnt, const int32_t* off,
                            const int32_t* poff, int E, int G, int shared_rows, int64_t kpad,
                            uint8_t* dyc, uint8_t* dys, uint16_t* dyt, int sms, cudaStream_t s) {
-    if (kpad % kTqRows || d % 256 || dy.k + (dy.n_shared ? 1 : 0) > kDyMaxRows)
+    if (kpad % kTqRows || d % 512 || d > kDyMaxD || dy.k + (dy.n_shared ? 1 : 0) > kDyMaxRows ||
+        (reinterpret_cast<uintptr_t>(dys) & 15))
         return cudaErrorInvalidValue;
     const SrcDy src{dy.dout, dy.gates, dy.perm, dy.valid, dy.k, dy.Tk, d};
     if (dy.T > 0) {
