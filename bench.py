@@ -684,6 +684,54 @@ def backward_launches(cfg, train=False):
     return prep + 2 + disp + 2 + 1 + 2 + 2 + 2 + 1 + 1 + 1 + 1 + 2 + 2 + (1 if train else 0)
 
 
+def backward_roofline(cfg, stage_ms, ms_per_step, pk, pk_kind, train=False):
+    """Per-kernel fractions, the dominant kernel's roofline and the layer roofline
+    of one backward (or training) step from its per-stage times (ms): each grouped
+    GEMM against the peak of the MMA it runs on -- dH and dXp on the block-scaled
+    MXFP8 MMA at the fp8 peak (the measured bf16 figure times the nominal 2x), the
+    others at the bf16 peak -- and the layer's tensor time as the sum of those."""
+    flops, nbytes = backward_work(cfg, train)
+    hbm = float(pk["hbm_gbs"])
+    tensor = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    tensor_s = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    kf = backward_kernel_flops(cfg, train)
+    # dH and dXp run on the block-scaled MXFP8 MMA: the fp8 peak, the measured
+    # bf16 figure times the nominal 2x ratio; the rest on bf16 MMAs
+    kpeak = {n: tensor * (FP8_OVER_BF16 if n in BS_BWD_KERNELS else 1.0) for n in kf}
+    kernels = {n: {"ms": stage_ms[n], "tflops": kf[n] / (stage_ms[n] / 1e3) / 1e12,
+                   "peak_tflops": kpeak[n],
+                   "frac": kf[n] / (stage_ms[n] / 1e3) / 1e12 / kpeak[n]} for n in kf}
+    dom = max(kf, key=lambda n: stage_ms[n])
+    knames = {"gate_up": "pair_gemm_kernel<GEMM_SWIGLU, bf16> (gate/up, keeps pre-activations)",
+              "down": "pair_gemm_kernel<GEMM_DOWN, bf16> (expert outputs)",
+              "dh": "bs_pair_kernel<GEMM_DOWN, MXFP8> (dH = Q(dY) Q(Wd), block-scaled, fp32 rows)",
+              "dxp": "bs_pair_kernel<GEMM_DOWN, MXFP8> (dXp, K = 2F, block-scaled, fp32 rows)",
+              "wgrad_down": "wgrad_kernel (dWd, ragged K)",
+              "wgrad_gate_up": "wgrad_kernel (dWg and dWu, ragged K)"}
+    achieved = kernels[dom]["tflops"]
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": kpeak[dom], "unit": "TFLOP/s",
+                "frac": achieved / kpeak[dom], "traffic": None, "kernel": knames[dom],
+                "algorithmic_flops_per_launch": kf[dom], "avg_launch_ms": stage_ms[dom],
+                "frac_of_sustained": achieved / (tensor_s * kpeak[dom] / tensor),
+                "peak_source": (f"{pk_kind} (MEASURED_PEAKS.json bf16_tflops, burst)"
+                                if pk_kind == "measured" else "fallback 1.9 PFLOP/s")
+                + (" x 2 (fp8 over bf16, nominal)" if dom in BS_BWD_KERNELS else "")}
+    # tensor time: each grouped GEMM at its own peak, the router and gate work at bf16
+    t_tensor = (sum(kf[n] / kpeak[n] for n in kf) + (flops - sum(kf.values())) / tensor) / 1e12
+    t_tensor_s = t_tensor * tensor / tensor_s
+    t_roof = max(t_tensor, nbytes / (hbm * 1e9))
+    layer_roof = {"flops": flops, "bytes": nbytes,
+                  "bound": "tensor" if t_tensor > nbytes / (hbm * 1e9) else "hbm",
+                  "roofline_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_per_step,
+                  "frac_of_sustained": 1e3 * max(t_tensor_s, nbytes / (hbm * 1e9)) / ms_per_step,
+                  "peaks": f"{pk_kind}: {hbm} GB/s, {tensor} TFLOP/s bf16 burst, "
+                           f"{tensor_s} sustained; fp8 = 2 x bf16",
+                  "note": "dH and dXp at the fp8 peak (block-scaled MXFP8 MMA); the weight "
+                          "gradients and the forward recompute at the bf16 peak (bf16 MMAs of "
+                          "the exact MXFP8 values, and the bf16 forward)"}
+    return kernels, roofline, layer_roof
+
+
 def _bwd_cfg(args):
     from deterministic_rl_gb300.synthetic import CONFIGS
     cfg = CONFIGS[args.config]
@@ -810,7 +858,7 @@ def run_backward_ours(args):
     torch.cuda.synchronize()
     if layer.backward_status() != 0:
         raise RuntimeError(f"device status after warm-up: {B.status_str(layer.backward_status())}")
-    flops, nbytes = backward_work(cfg, train)
+    _, nbytes = backward_work(cfg, train)
     ns = len(B.BWD_STAGES)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * ns)] for _ in range(K)]
     for row in evs:
@@ -839,44 +887,8 @@ def run_backward_ours(args):
                 for j, name in enumerate(B.BWD_STAGES)}
 
     pk, pk_kind = peaks()
-    hbm = float(pk["hbm_gbs"])
-    tensor = float(pk.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    tensor_s = float(pk.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
-    kf = backward_kernel_flops(cfg, train)
-    # dH and dXp run on the block-scaled MXFP8 MMA: the fp8 peak, the measured
-    # bf16 figure times the nominal 2x ratio; the rest on bf16 MMAs
-    kpeak = {n: tensor * (FP8_OVER_BF16 if n in BS_BWD_KERNELS else 1.0) for n in kf}
-    kernels = {n: {"ms": stage_ms[n], "tflops": kf[n] / (stage_ms[n] / 1e3) / 1e12,
-                   "peak_tflops": kpeak[n],
-                   "frac": kf[n] / (stage_ms[n] / 1e3) / 1e12 / kpeak[n]} for n in kf}
-    dom = max(kf, key=lambda n: stage_ms[n])
-    knames = {"gate_up": "pair_gemm_kernel<GEMM_SWIGLU, bf16> (gate/up, keeps pre-activations)",
-              "down": "pair_gemm_kernel<GEMM_DOWN, bf16> (expert outputs)",
-              "dh": "bs_pair_kernel<GEMM_DOWN, MXFP8> (dH = Q(dY) Q(Wd), block-scaled, fp32 rows)",
-              "dxp": "bs_pair_kernel<GEMM_DOWN, MXFP8> (dXp, K = 2F, block-scaled, fp32 rows)",
-              "wgrad_down": "wgrad_kernel (dWd, ragged K)",
-              "wgrad_gate_up": "wgrad_kernel (dWg and dWu, ragged K)"}
-    achieved = kernels[dom]["tflops"]
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": kpeak[dom], "unit": "TFLOP/s",
-                "frac": achieved / kpeak[dom], "traffic": None, "kernel": knames[dom],
-                "algorithmic_flops_per_launch": kf[dom], "avg_launch_ms": stage_ms[dom],
-                "frac_of_sustained": achieved / (tensor_s * kpeak[dom] / tensor),
-                "peak_source": (f"{pk_kind} (MEASURED_PEAKS.json bf16_tflops, burst)"
-                                if pk_kind == "measured" else "fallback 1.9 PFLOP/s")
-                + (" x 2 (fp8 over bf16, nominal)" if dom in BS_BWD_KERNELS else "")}
-    # tensor time: each grouped GEMM at its own peak, the router and gate work at bf16
-    t_tensor = (sum(kf[n] / kpeak[n] for n in kf) + (flops - sum(kf.values())) / tensor) / 1e12
-    t_tensor_s = t_tensor * tensor / tensor_s
-    t_roof = max(t_tensor, nbytes / (hbm * 1e9))
-    layer_roof = {"flops": flops, "bytes": nbytes,
-                  "bound": "tensor" if t_tensor > nbytes / (hbm * 1e9) else "hbm",
-                  "roofline_ms": 1e3 * t_roof, "frac": 1e3 * t_roof / ms_per_step,
-                  "frac_of_sustained": 1e3 * max(t_tensor_s, nbytes / (hbm * 1e9)) / ms_per_step,
-                  "peaks": f"{pk_kind}: {hbm} GB/s, {tensor} TFLOP/s bf16 burst, "
-                           f"{tensor_s} sustained; fp8 = 2 x bf16",
-                  "note": "dH and dXp at the fp8 peak (block-scaled MXFP8 MMA); the weight "
-                          "gradients and the forward recompute at the bf16 peak (bf16 MMAs of "
-                          "the exact MXFP8 values, and the bf16 forward)"}
+    kernels, roofline, layer_roof = backward_roofline(cfg, stage_ms, ms_per_step, pk, pk_kind,
+                                                      train)
 
     e2e = None
     if not args.no_e2e:

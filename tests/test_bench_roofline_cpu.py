@@ -98,3 +98,36 @@ def test_block_scaled_peaks_and_row_bytes():
     T, d, F, k = cfg.T, cfg.d, cfg.F, cfg.k
     want = 384 * 2 * F * d * (0.5 + 1 / 16) + T * k * d * (0.5 + 1 / 16) + T * k * F * 2
     assert abs(bench.gate_up_bytes(cfg, 384) - want) < 1.0
+
+
+def test_backward_roofline_takes_each_gemm_at_its_own_peak():
+    """dH and dXp run on the block-scaled MXFP8 MMA and are measured against the
+    fp8 peak (2x the measured bf16 figure); the weight-gradient GEMMs and the
+    forward recompute against bf16; the layer's tensor time sums the grouped
+    GEMMs at their peaks plus the router and gate work at bf16."""
+    cfg = CONFIGS["c4_train_32k"]
+    T, d, k, F, S = cfg.T, cfg.d, cfg.k, cfg.F, cfg.n_shared
+    rows = T * k + T * S
+    pk = {"hbm_gbs": 6761.6, "bf16_tflops": 1958.8, "bf16_tflops_sustained": 1730.0}
+    ms = {"gate_up": 11.97, "down": 5.13, "dh": 3.82, "dxp": 7.98, "wgrad_down": 7.21,
+          "wgrad_gate_up": 13.73}
+    kernels, roof, layer = bench.backward_roofline(cfg, ms, 70.3, pk, "measured")
+    bf, f8 = 1958.8, 2 * 1958.8
+    assert kernels["dh"]["peak_tflops"] == f8 and kernels["dxp"]["peak_tflops"] == f8
+    for n in ("gate_up", "down", "wgrad_down", "wgrad_gate_up"):
+        assert kernels[n]["peak_tflops"] == bf
+    assert kernels["dh"]["frac"] == pytest.approx(2 * d * F * rows / 3.82e-3 / 1e12 / f8)
+    assert kernels["dxp"]["frac"] == pytest.approx(4 * d * F * rows / 7.98e-3 / 1e12 / f8)
+    # the dominant kernel is the longest stage: dWg/dWu, at the bf16 peak
+    assert roof["kernel"].startswith("wgrad_kernel (dWg") and roof["peak"] == bf
+    assert roof["frac"] == pytest.approx(4 * d * F * rows / 13.73e-3 / 1e12 / bf)
+    flops, _ = bench.backward_work(cfg)
+    kf = bench.backward_kernel_flops(cfg)
+    t = (sum(kf.values()) - kf["dh"] - kf["dxp"]) / bf + (kf["dh"] + kf["dxp"]) / f8
+    t += (flops - sum(kf.values())) / bf
+    assert layer["bound"] == "tensor"
+    assert layer["roofline_ms"] == pytest.approx(t / 1e9)
+    assert layer["frac"] == pytest.approx(t / 1e9 / 70.3)
+    # a block-scaled stage that dominates is quoted against the fp8 peak
+    _, roof2, _ = bench.backward_roofline(cfg, dict(ms, dxp=20.0), 80.0, pk, "measured")
+    assert roof2["peak"] == f8 and "x 2" in roof2["peak_source"]
