@@ -411,11 +411,11 @@ __global__ void __launch_bounds__(256) dy_rows_kernel(SrcDy src, const int32_t* 
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
                 m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 2));
                 const int X = mx_block_exp(m);
-                const float inv = exp2i(-X);
+                const float rs = exp2i(-X);  // 2^-X
                 uint32_t cw[4];
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    cw[i] = __nv_cvt_float2_to_fp8x2(make_float2(v[2 * i] * inv, v[2 * i + 1] * inv),
+                    cw[i] = __nv_cvt_float2_to_fp8x2(make_float2(v[2 * i] * rs, v[2 * i + 1] * rs),
                                                      __NV_SATFINITE, __NV_E4M3);
                 *reinterpret_cast<uint2*>(dyc + dst[j] * d + c) =
                     make_uint2(cw[0] | (cw[1] << 16), cw[2] | (cw[3] << 16));
