@@ -11,10 +11,11 @@ perturbed copy of the hidden states.  Prints one JSON line (rank 0).
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--config NAME] [--mode replay|own] [--pass forward|backward]
 
---pass backward times the layer backward instead (MXFP8 expert GEMMs; one
-step = the weight copies quantised along the backward's contraction axes,
-then the whole backward of one batch with recorded ids, forward recomputed),
-by default on the 32k-token training layer.  --pass train times a training
+--pass backward times the layer backward instead (MXFP8 expert GEMMs: dH and
+dXp on the block-scaled FP8 MMA, quoted against the fp8 peak, the weight
+gradients on bf16 MMAs; one step = the weight copies quantised along the
+backward's contraction axes, then the whole backward of one batch with
+recorded ids, forward recomputed), by default on the 32k-token training layer.  --pass train times a training
 step of the layer: weight copies, the forward keeping its activations, and
 the backward from them.
 
@@ -25,9 +26,10 @@ workload (rank 0 only).
 
 On one GPU the default (headline) run also times every other d=7168 workload
 of the layer -- prefill-like Zipf (replay and own), 32k tokens (uniform and
-Zipf s=1.2 routing, own), MXFP8 weights (own) -- one after another in the same
-process, and reports each under "workloads" in the same JSON line
-(--no-workloads skips them).
+Zipf s=1.2 routing, own), decode with own routing, MXFP8 weights, MXFP8
+weights and activations, NVFP4 (own) -- one after another in the same process,
+and reports each under "workloads" in the same JSON line (--no-workloads skips
+them).
 """
 from __future__ import annotations
 
